@@ -1,0 +1,697 @@
+/*
+ * moe_oracle.c -- CPU oracle for the fused MoE hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or helper with the
+ * CUDA library; the two meet only through the seeded input generators.
+ *
+ * It is written to be checked by eye against the definition of a top-k
+ * mixture-of-experts layer, not to be fast:
+ *   - one token at a time, one routed slot at a time, plain loops;
+ *   - every floating-point sum of the experts' arithmetic in double (fp64);
+ *   - the decisions that pick an integer (which experts a token goes to, which
+ *     e4m3 code a value gets) are taken in fp32, the precision the CUDA
+ *     kernels take them in, so that ids and codes can be compared bit for bit.
+ *
+ * Passages followed (web pages on the subject, cited by title and section):
+ *   [MK]  "vllm/model_executor/layers/fused_moe/modular_kernel.py"
+ *         (vllm-cpu 0.11.0.post2 diff view):
+ *         - module comment: [Router] -> [Quantize-Dispatch] ->
+ *           [Permute-Experts-Unpermute] -> [Combine];
+ *         - _moe_problem_size: E, M, N, K, topk; w1 is (E, 2N, K) with the
+ *           gated pair stacked along its rows, w2 is (E, K, N); Standard
+ *           format a1 (M, K), BatchedExperts format a1 (E, max_tokens, K);
+ *         - ExpertTokensMetadata: per-expert token counts;
+ *         - FusedMoEPrepareAndFinalize.prepare: quantisation happens before
+ *           the experts run;
+ *         - FusedMoEPermuteExpertsUnpermute.activation: a gated activation
+ *           whose output is half as wide as its input (silu_and_mul);
+ *         - FusedMoEPrepareAndFinalize.finalize: fused_expert_output has
+ *           shape (M, topk, K); weights are applied and the topk slots are
+ *           reduced into output (M, K).
+ *   [WT]  "EP: CUDA-graph-safe HT internode dispatch+combine (worst-tokens
+ *         mode)" (uccl pull request 7): a device int32[num_local_experts]
+ *         count per expert, read by a masked grouped GEMM that only touches
+ *         the first count rows of each expert's padded block.
+ *
+ * The pages do not spell out the router, the FP8 formula or which half of w1
+ * is the gate; the readings taken here (named R1..R6, Q1..Q5, G1, G2, F1, B1,
+ * B2 in the design notes) are:
+ *   R1 softmax router: top-k on the raw logits (softmax is monotone), weight
+ *      p_j = softmax(l)_j, renormalised over the chosen k when asked.
+ *   R2 sigmoid grouped router: s_e = sigmoid(l_e + b_e); E experts in
+ *      n_groups contiguous groups; group key = sum of the group's two largest
+ *      s; keep the topk_groups best groups, then the topk best experts by s
+ *      among them; weight s_j, renormalised when asked.
+ *   R4 equal keys: the lower index wins (expert id, group id).
+ *   R5 s_e is the fp32 rounding of the fp64 value 1/(1+exp(-(double)v)),
+ *      v = l_e + b_e added in fp32; the group key is an fp32 add.
+ *   R6 ids in a row are in descending score order.
+ *   P1 within one expert, pairs keep ascending pair order p = t*topk + j.
+ *   Q1 FP8 group quant: s = max(amax, 1e-12) / 448 in fp32,
+ *      q = e4m3(x / s) with round-to-nearest-even, saturating at +-448.
+ *   G1 rows [0, N) of w1[e] are the gate (SiLU applied), rows [N, 2N) the up
+ *      projection; G2 silu(z) = z / (1 + exp(-z)).
+ *   Q5 optional requantisation of the hidden row h in 128-wide groups.
+ *   F1 the topk slots are summed in slot order j = 0..topk-1.
+ *   B1 batched rows r >= count[e] are neither read nor written.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORC_BF16 = 0, ORC_FP8 = 1 };
+enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16 is the top half of an IEEE binary32: widening is exact. */
+static double bf16_value(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* e4m3 ("fn" variant): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits, subnormals when the exponent field is 0, no infinities, and the
+ * single NaN pattern S.1111.111.  Largest finite magnitude 1.75 * 2^8 = 448. */
+double orc_e4m3_value(uint8_t code)
+{
+    int sign = code >> 7;
+    int ex = (code >> 3) & 15;
+    int man = code & 7;
+    double v;
+    if (ex == 15 && man == 7)
+        return NAN;
+    if (ex == 0)
+        v = ldexp((double)man / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)man / 8.0, ex - 7);
+    return sign ? -v : v;
+}
+
+/* orc_e4m3_value of every code, filled once before any parallel loop */
+static double e4m3_table[256];
+static void fill_e4m3_table(void)
+{
+    int c;
+    for (c = 0; c < 256; ++c)
+        e4m3_table[c] = orc_e4m3_value((uint8_t)c);
+}
+
+/* Round-to-nearest-even onto the e4m3 grid, saturating to +-448.  The
+ * non-negative finite codes 0x00..0x7e are in increasing order of value, so
+ * the nearest code is found by bisection for the last code whose value does
+ * not exceed |x|, then a comparison with the next one; a tie (|x| exactly half
+ * way) goes to the even code, the one whose mantissa ends in 0.  The sign is
+ * carried separately, so negative values that round to zero give 0x80. */
+uint8_t orc_e4m3_encode(float x)
+{
+    uint8_t sign;
+    double a, dlo, dhi;
+    int lo, hi, c;
+    if (isnan(x))
+        return 0x7f;
+    sign = signbit(x) ? 0x80 : 0x00;
+    a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7e);
+    lo = 0;    /* value(lo) <= a */
+    hi = 0x7e; /* value(hi) >  a */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (orc_e4m3_value((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    dlo = a - orc_e4m3_value((uint8_t)lo);
+    dhi = orc_e4m3_value((uint8_t)hi) - a;
+    if (dlo < dhi)
+        c = lo;
+    else if (dhi < dlo)
+        c = hi;
+    else
+        c = (lo & 1) == 0 ? lo : hi;
+    return (uint8_t)(sign | c);
+}
+
+/* Q1: scale of one group from its largest magnitude (fp32 arithmetic). */
+static float group_scale(float amax)
+{
+    float m = amax > 1e-12f ? amax : 1e-12f;
+    return m / 448.0f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [Router] -- R1, R2, R4, R5, R6                                            */
+/* ------------------------------------------------------------------------ */
+
+/* R1 for one token.  ids[j], w[j] for j < topk. */
+static void route_softmax_row(const float *l, int E, int topk, int renorm,
+                              int32_t *ids, double *w)
+{
+    int j, e;
+    float lmax = l[0];
+    double denom = 0.0, sel = 0.0;
+    char *taken = (char *)calloc((size_t)E, 1);
+    for (e = 1; e < E; ++e)
+        if (l[e] > lmax)
+            lmax = l[e];
+    for (e = 0; e < E; ++e)
+        denom += exp((double)l[e] - (double)lmax);
+    for (j = 0; j < topk; ++j) {
+        int best = -1;
+        for (e = 0; e < E; ++e) {
+            if (taken[e])
+                continue;
+            if (best < 0 || l[e] > l[best]) /* strict: lower id wins ties */
+                best = e;
+        }
+        taken[best] = 1;
+        ids[j] = best;
+        w[j] = exp((double)l[best] - (double)lmax) / denom;
+        sel += w[j];
+    }
+    if (renorm)
+        for (j = 0; j < topk; ++j)
+            w[j] /= sel;
+    free(taken);
+}
+
+/* R5: the fp32 score. */
+static float sigmoid_score(float logit, float bias)
+{
+    float v = logit + bias;
+    return (float)(1.0 / (1.0 + exp(-(double)v)));
+}
+
+static double sigmoid_exact(float logit, float bias)
+{
+    float v = logit + bias;
+    return 1.0 / (1.0 + exp(-(double)v));
+}
+
+/* R2 for one token.  margin (optional) receives the smallest fp64 gap at a
+ * selection boundary: between the last kept and the best dropped group key,
+ * and between the last chosen and the best unchosen eligible expert.  A tiny
+ * or negative margin marks a token whose choice an fp32 rounding could flip. */
+static void route_sigmoid_row(const float *l, const float *bias, int E,
+                              int topk, int n_groups, int topk_groups,
+                              int renorm, int32_t *ids, double *w,
+                              double *margin)
+{
+    int gsz, g, e, j, i;
+    float *s = (float *)malloc(sizeof(float) * (size_t)E);
+    double *s64 = (double *)malloc(sizeof(double) * (size_t)E);
+    float *key;
+    double *key64;
+    char *gsel, *taken;
+    double sel = 0.0, mg = INFINITY;
+
+    if (n_groups < 1)
+        n_groups = 1;
+    if (topk_groups < 1 || topk_groups > n_groups)
+        topk_groups = n_groups;
+    gsz = E / n_groups;
+    key = (float *)malloc(sizeof(float) * (size_t)n_groups);
+    key64 = (double *)malloc(sizeof(double) * (size_t)n_groups);
+    gsel = (char *)calloc((size_t)n_groups, 1);
+    taken = (char *)calloc((size_t)E, 1);
+
+    for (e = 0; e < E; ++e) {
+        float b = bias ? bias[e] : 0.0f;
+        s[e] = sigmoid_score(l[e], b);
+        s64[e] = sigmoid_exact(l[e], b);
+    }
+
+    /* group key: sum of the two largest scores of the group (one when the
+     * group has a single expert); the fp32 add is exact-order independent */
+    for (g = 0; g < n_groups; ++g) {
+        int a = -1, c = -1;
+        for (i = 0; i < gsz; ++i) {
+            e = g * gsz + i;
+            if (a < 0 || s[e] > s[a]) {
+                c = a;
+                a = e;
+            } else if (c < 0 || s[e] > s[c]) {
+                c = e;
+            }
+        }
+        key[g] = c >= 0 ? s[a] + s[c] : s[a];
+        key64[g] = c >= 0 ? s64[a] + s64[c] : s64[a];
+    }
+
+    if (topk_groups < n_groups) {
+        int last = -1;
+        for (i = 0; i < topk_groups; ++i) {
+            int best = -1;
+            for (g = 0; g < n_groups; ++g) {
+                if (gsel[g])
+                    continue;
+                if (best < 0 || key[g] > key[best])
+                    best = g;
+            }
+            gsel[best] = 1;
+            last = best;
+        }
+        for (g = 0; g < n_groups; ++g)
+            if (!gsel[g] && key64[last] - key64[g] < mg)
+                mg = key64[last] - key64[g];
+    } else {
+        for (g = 0; g < n_groups; ++g)
+            gsel[g] = 1;
+    }
+
+    for (j = 0; j < topk; ++j) {
+        int best = -1;
+        for (e = 0; e < E; ++e) {
+            if (taken[e] || !gsel[e / gsz])
+                continue;
+            if (best < 0 || s[e] > s[best])
+                best = e;
+        }
+        taken[best] = 1;
+        ids[j] = best;
+        w[j] = (double)s[best];
+        sel += w[j];
+    }
+    for (e = 0; e < E; ++e)
+        if (!taken[e] && gsel[e / gsz] &&
+            s64[ids[topk - 1]] - s64[e] < mg)
+            mg = s64[ids[topk - 1]] - s64[e];
+    if (renorm)
+        for (j = 0; j < topk; ++j)
+            w[j] /= sel;
+    if (margin)
+        *margin = mg;
+
+    free(s);
+    free(s64);
+    free(key);
+    free(key64);
+    free(gsel);
+    free(taken);
+}
+
+/* [Router] over M tokens: logits (M, E) fp32, optional bias (E) fp32;
+ * ids (M, topk) int32, w (M, topk) fp64, margin (M) fp64 or NULL. */
+void orc_route(const float *logits, const float *bias, int M, int E, int topk,
+               int score_fn, int n_groups, int topk_groups, int renorm,
+               int32_t *ids, double *w, double *margin)
+{
+    int t;
+    for (t = 0; t < M; ++t) {
+        const float *l = logits + (size_t)t * E;
+        if (score_fn == ORC_SOFTMAX) {
+            route_softmax_row(l, E, topk, renorm, ids + (size_t)t * topk,
+                              w + (size_t)t * topk);
+            if (margin)
+                margin[t] = INFINITY;
+        } else {
+            route_sigmoid_row(l, bias, E, topk, n_groups, topk_groups, renorm,
+                              ids + (size_t)t * topk, w + (size_t)t * topk,
+                              margin ? margin + t : NULL);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Counts and permutation -- ExpertTokensMetadata, "Permute" of             */
+/* [Permute-Experts-Unpermute]; P1                                           */
+/* ------------------------------------------------------------------------ */
+
+/* counts[e] = number of pairs p < P with ids[p] == e.  Returns how many ids
+ * were outside [0, E) (those pairs are left out). */
+int orc_count(const int32_t *ids, int P, int E, int32_t *counts)
+{
+    int p, bad = 0;
+    memset(counts, 0, sizeof(int32_t) * (size_t)E);
+    for (p = 0; p < P; ++p) {
+        if (ids[p] < 0 || ids[p] >= E) {
+            ++bad;
+            continue;
+        }
+        counts[ids[p]] += 1;
+    }
+    return bad;
+}
+
+/* Stable counting sort of pair ids by expert: offsets (E+1) exclusive
+ * prefix sums of the counts; sorted[offsets[e] + r] = the r-th pair (in
+ * ascending pair order) routed to e; inv[p] = its position, -1 for a pair
+ * whose id is out of range. */
+void orc_align(const int32_t *ids, int P, int E, int32_t *offsets,
+               int32_t *sorted, int32_t *inv)
+{
+    int p, e;
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    orc_count(ids, P, E, cursor);
+    offsets[0] = 0;
+    for (e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + cursor[e];
+    for (e = 0; e < E; ++e)
+        cursor[e] = offsets[e];
+    for (p = 0; p < P; ++p) {
+        if (ids[p] < 0 || ids[p] >= E) {
+            inv[p] = -1;
+            continue;
+        }
+        sorted[cursor[ids[p]]] = p;
+        inv[p] = cursor[ids[p]];
+        cursor[ids[p]] += 1;
+    }
+    free(cursor);
+}
+
+/* Gather: xperm[i] = x[sorted[i] / topk] for i < n_rows (rows of K doubles). */
+void orc_permute_rows(const double *x, const int32_t *sorted, int n_rows,
+                      int topk, int K, double *xperm)
+{
+    int i, k;
+    for (i = 0; i < n_rows; ++i)
+        for (k = 0; k < K; ++k)
+            xperm[(size_t)i * K + k] = x[(size_t)(sorted[i] / topk) * K + k];
+}
+
+/* Unpermute + TopKWeightAndReduce: out[t] = sum_{j=0..topk-1}
+ * w[t,j] * yperm[inv[t*topk+j]] in slot order (F1).  Pairs with inv < 0
+ * contribute nothing. */
+void orc_unpermute_reduce(const double *yperm, const int32_t *inv,
+                          const double *w, int M, int topk, int K, double *out)
+{
+    int t, j, k;
+    for (t = 0; t < M; ++t) {
+        for (k = 0; k < K; ++k)
+            out[(size_t)t * K + k] = 0.0;
+        for (j = 0; j < topk; ++j) {
+            int p = t * topk + j;
+            if (inv[p] < 0)
+                continue;
+            for (k = 0; k < K; ++k)
+                out[(size_t)t * K + k] +=
+                    w[p] * yperm[(size_t)inv[p] * K + k];
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* [Quantize-Prepare] -- Q1 and its 2-D block form for weights               */
+/* ------------------------------------------------------------------------ */
+
+/* x (M, K) bf16 -> q (M, K) e4m3 codes, scales (M, K / group) fp32. */
+void orc_quant_fp8_group(const uint16_t *x, int M, int K, int group,
+                         uint8_t *q, float *scales)
+{
+    int t, g, k, G = K / group;
+    for (t = 0; t < M; ++t) {
+        for (g = 0; g < G; ++g) {
+            const uint16_t *xg = x + (size_t)t * K + (size_t)g * group;
+            float amax = 0.0f, s;
+            for (k = 0; k < group; ++k) {
+                float v = (float)fabs(bf16_value(xg[k]));
+                if (v > amax)
+                    amax = v;
+            }
+            s = group_scale(amax);
+            scales[(size_t)t * G + g] = s;
+            for (k = 0; k < group; ++k)
+                q[(size_t)t * K + (size_t)g * group + k] =
+                    orc_e4m3_encode((float)bf16_value(xg[k]) / s);
+        }
+    }
+}
+
+/* w (R, C) bf16 -> q (R, C) e4m3, scales (R / block, C / block) fp32; one
+ * scale per block x block tile from the tile's largest magnitude. */
+void orc_quant_fp8_block(const uint16_t *w, int R, int C, int block,
+                         uint8_t *q, float *scales)
+{
+    int br, BR = R / block, BC = C / block;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (br = 0; br < BR; ++br) {
+        int bc, r, c;
+        for (bc = 0; bc < BC; ++bc) {
+            float amax = 0.0f, s;
+            for (r = br * block; r < (br + 1) * block; ++r)
+                for (c = bc * block; c < (bc + 1) * block; ++c) {
+                    float v = (float)fabs(bf16_value(w[(size_t)r * C + c]));
+                    if (v > amax)
+                        amax = v;
+                }
+            s = group_scale(amax);
+            scales[(size_t)br * BC + bc] = s;
+            for (r = br * block; r < (br + 1) * block; ++r)
+                for (c = bc * block; c < (bc + 1) * block; ++c)
+                    q[(size_t)r * C + c] = orc_e4m3_encode(
+                        (float)bf16_value(w[(size_t)r * C + c]) / s);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* One expert on one row -- [Permute-Experts-Unpermute] apply: matmul,       */
+/* act_mul, optional quant, matmul; G1, G2, Q5                               */
+/* ------------------------------------------------------------------------ */
+
+/* The weights of one run, one pointer per expert (NULL for an expert the
+ * caller did not supply; using one is an error the caller must avoid).
+ * dtype ORC_BF16: w1[e] (2N, K) and w2[e] (K, N) hold bf16 bits.  ORC_FP8:
+ * they hold e4m3 codes, and w1s[e] (2N/128, K/128), w2s[e] (K/128, N/128)
+ * hold the 128 x 128 block scales. */
+typedef struct {
+    int dtype, E, N, K;
+    const void *const *w1, *const *w2;
+    const float *const *w1s, *const *w2s;
+} orc_weights;
+
+/* element (e, row, col) of a weight tensor (E, R, C), dequantised */
+static double weight_at(const orc_weights *W, int which, int e, int row,
+                        int col)
+{
+    int C = which == 1 ? W->K : W->N;
+    size_t idx = (size_t)row * C + col;
+    if (W->dtype == ORC_BF16) {
+        const uint16_t *b = (const uint16_t *)(which == 1 ? W->w1[e] : W->w2[e]);
+        return bf16_value(b[idx]);
+    } else {
+        const uint8_t *q = (const uint8_t *)(which == 1 ? W->w1[e] : W->w2[e]);
+        const float *sc = which == 1 ? W->w1s[e] : W->w2s[e];
+        size_t sidx = (size_t)(row / 128) * (C / 128) + col / 128;
+        return e4m3_table[q[idx]] * (double)sc[sidx];
+    }
+}
+
+/* h (N) = silu(x W1[e][0:N]^T) * (x W1[e][N:2N]^T); optional Q5 requant of
+ * h; y (K) = h W2[e]^T.  x is the (dequantised) input row of K values. */
+static void expert_row(const orc_weights *W, int e, const double *x,
+                       int requant_h, double *h, double *y)
+{
+    int n, k, N = W->N, K = W->K;
+    for (n = 0; n < N; ++n) {
+        double g = 0.0, u = 0.0;
+        for (k = 0; k < K; ++k) {
+            g += x[k] * weight_at(W, 1, e, n, k);
+            u += x[k] * weight_at(W, 1, e, N + n, k);
+        }
+        h[n] = g / (1.0 + exp(-g)) * u;
+    }
+    if (requant_h) {
+        int gi;
+        for (gi = 0; gi < N / 128; ++gi) {
+            float amax = 0.0f, s;
+            for (n = gi * 128; n < (gi + 1) * 128; ++n) {
+                float v = (float)fabs((float)h[n]);
+                if (v > amax)
+                    amax = v;
+            }
+            s = group_scale(amax);
+            for (n = gi * 128; n < (gi + 1) * 128; ++n)
+                h[n] = orc_e4m3_value(orc_e4m3_encode((float)h[n] / s)) *
+                       (double)s;
+        }
+    }
+    for (k = 0; k < K; ++k) {
+        double acc = 0.0;
+        for (n = 0; n < N; ++n)
+            acc += h[n] * weight_at(W, 2, e, k, n);
+        y[k] = acc;
+    }
+}
+
+/* Input row t of x (M, K) bf16, dequantised as the experts see it: as is for
+ * bf16, or through Q1 (groups of 128) for FP8. */
+static void input_row(int dtype, const uint16_t *x, int t, int K, double *xr)
+{
+    int k;
+    const uint16_t *row = x + (size_t)t * K;
+    if (dtype == ORC_BF16) {
+        for (k = 0; k < K; ++k)
+            xr[k] = bf16_value(row[k]);
+    } else {
+        uint8_t *q = (uint8_t *)malloc((size_t)K);
+        float *s = (float *)malloc(sizeof(float) * (size_t)(K / 128));
+        orc_quant_fp8_group(row, 1, K, 128, q, s);
+        for (k = 0; k < K; ++k)
+            xr[k] = orc_e4m3_value(q[k]) * (double)s[k / 128];
+        free(q);
+        free(s);
+    }
+}
+
+/* h and y of one expert on one row of x (bf16 bits); for checking the two
+ * grouped GEMMs separately.  h (N), y (K) fp64. */
+void orc_expert_row(int dtype, const uint16_t *x, int t, int e, int E, int N,
+                    int K, const void *const *w1, const float *const *w1s,
+                    const void *const *w2, const float *const *w2s,
+                    int requant_h, double *h, double *y)
+{
+    orc_weights W;
+    double *xr = (double *)malloc(sizeof(double) * (size_t)K);
+    fill_e4m3_table();
+    W.dtype = dtype; W.E = E; W.N = N; W.K = K;
+    W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
+    input_row(dtype, x, t, K, xr);
+    expert_row(&W, e, xr, requant_h, h, y);
+    free(xr);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The layer, Standard format (M, K): for each listed token t,               */
+/*   out[t] = sum_{j=0..topk-1} w[t,j] * expert_{ids[t,j]}(x[t])             */
+/* -- FusedMoEModularKernel.forward with finalize's weight-and-reduce; F1    */
+/* ------------------------------------------------------------------------ */
+
+/* tokens (n_tok) lists which tokens to compute (NULL: all M, n_tok = M);
+ * out (n_tok, K), ids_out (n_tok, topk), w_out (n_tok, topk) fp64.
+ * Tokens are independent, so a listed subset is computed exactly as it
+ * would be in a full run.  nthreads <= 0: the OpenMP default. */
+void orc_moe_forward(const uint16_t *x, const float *logits, const float *bias,
+                     int M, int K, int N, int E, int topk, int score_fn,
+                     int n_groups, int topk_groups, int renorm, int dtype,
+                     int requant_h, const void *const *w1,
+                     const float *const *w1s, const void *const *w2,
+                     const float *const *w2s, const int32_t *tokens,
+                     int n_tok, int32_t *ids_out, double *w_out, double *out,
+                     int nthreads)
+{
+    int i;
+    orc_weights W;
+    fill_e4m3_table();
+    W.dtype = dtype; W.E = E; W.N = N; W.K = K;
+    W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
+    if (!tokens)
+        n_tok = M;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (i = 0; i < n_tok; ++i) {
+        int t = tokens ? tokens[i] : i;
+        int j, k;
+        int32_t *ids = ids_out + (size_t)i * topk;
+        double *w = w_out + (size_t)i * topk;
+        double *xr = (double *)malloc(sizeof(double) * (size_t)K);
+        double *h = (double *)malloc(sizeof(double) * (size_t)N);
+        double *y = (double *)malloc(sizeof(double) * (size_t)K);
+        double *o = out + (size_t)i * K;
+        orc_route(logits + (size_t)t * E, bias, 1, E, topk, score_fn, n_groups,
+                  topk_groups, renorm, ids, w, NULL);
+        input_row(dtype, x, t, K, xr);
+        for (k = 0; k < K; ++k)
+            o[k] = 0.0;
+        for (j = 0; j < topk; ++j) {
+            expert_row(&W, ids[j], xr, requant_h, h, y);
+            for (k = 0; k < K; ++k)
+                o[k] += w[j] * y[k];
+        }
+        free(xr);
+        free(h);
+        free(y);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* BatchedExperts format (E, T, K) masked by per-expert counts -- [WT];      */
+/* B1: y_b[e, r] = expert_e(x_b[e, r]) for r < min(count[e], T) only.        */
+/* ------------------------------------------------------------------------ */
+
+/* rows (n_rows, 2) lists (e, r) pairs to compute (NULL: every valid row of
+ * every expert, in (e, r) order, n_rows ignored).  yb (E*T, K) fp64 is
+ * written only at the computed rows.  Returns the number of rows computed. */
+int orc_batched_experts(const uint16_t *xb, const int32_t *counts, int E,
+                        int T, int N, int K, int dtype, int requant_h,
+                        const void *const *w1, const float *const *w1s,
+                        const void *const *w2, const float *const *w2s,
+                        const int32_t *rows, int n_rows,
+                        double *yb, int nthreads)
+{
+    int e, i, n = 0;
+    int32_t *list;
+    orc_weights W;
+    fill_e4m3_table();
+    W.dtype = dtype; W.E = E; W.N = N; W.K = K;
+    W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
+    if (rows) {
+        list = (int32_t *)rows;
+        n = n_rows;
+    } else {
+        int total = 0, r;
+        for (e = 0; e < E; ++e) {
+            int c = counts[e] < 0 ? 0 : (counts[e] > T ? T : counts[e]);
+            total += c;
+        }
+        list = (int32_t *)malloc(sizeof(int32_t) * 2 * (size_t)(total > 0 ? total : 1));
+        for (e = 0; e < E; ++e) {
+            int c = counts[e] < 0 ? 0 : (counts[e] > T ? T : counts[e]);
+            for (r = 0; r < c; ++r) {
+                list[2 * n] = e;
+                list[2 * n + 1] = r;
+                ++n;
+            }
+        }
+    }
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (i = 0; i < n; ++i) {
+        int ee = list[2 * i], r = list[2 * i + 1];
+        int c = counts[ee] < 0 ? 0 : (counts[ee] > T ? T : counts[ee]);
+        double *xr, *h;
+        if (r >= c)
+            continue; /* B1: a padded row is never touched */
+        xr = (double *)malloc(sizeof(double) * (size_t)K);
+        h = (double *)malloc(sizeof(double) * (size_t)N);
+        input_row(dtype, xb, ee * T + r, K, xr);
+        expert_row(&W, ee, xr, requant_h, h, yb + ((size_t)ee * T + r) * K);
+        free(xr);
+        free(h);
+    }
+    if (!rows)
+        free(list);
+    return n;
+}
+
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

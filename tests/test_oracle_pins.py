@@ -1,0 +1,342 @@
+"""Pins of the CPU oracle against things other than itself: worked examples,
+library routines, closed forms, invariants and brute force (no GPU)."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as WL
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for ln in f:
+            ln = ln.strip()
+            if ln and not ln.startswith("#"):
+                yield [c.strip() for c in ln.split("|")]
+
+
+# ---------------------------------------------------------------- e4m3 ----
+
+def test_e4m3_decode_all_codes_match_torch(orc):
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = np.array([orc.e4m3_value(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(mine))
+    assert np.array_equal(ref[~nan], mine[~nan])
+
+
+def test_e4m3_golden_examples(orc):
+    for val, code in _lines("e4m3_examples.txt"):
+        got = int(orc.e4m3_encode([float(val)])[0])
+        assert got == int(code, 16), (val, hex(got), code)
+
+
+def test_e4m3_encode_matches_torch_cast_in_range(orc):
+    rng = np.random.default_rng(0)
+    # every code value, every midpoint between neighbours, and random values
+    vals = np.array([orc.e4m3_value(c) for c in range(0x7f)])
+    mids = (vals[:-1] + vals[1:]) / 2
+    rand = np.concatenate([rng.normal(0, s, 4000) for s in (1e-3, 0.1, 1, 30, 150)])
+    x = np.concatenate([vals, mids, -vals, -mids, rand]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = orc.e4m3_encode(x)
+    # +0 / -0 both encode zero; torch keeps the sign like the oracle does
+    assert np.array_equal(ref, got), np.flatnonzero(ref != got)[:10]
+
+
+def test_e4m3_saturates(orc):
+    got = orc.e4m3_encode([449.0, 463.9, 464.0, 1e6, -1e30])
+    assert list(got) == [0x7e, 0x7e, 0x7e, 0x7e, 0xfe]
+
+
+# -------------------------------------------------------------- router ----
+
+def test_route_golden_examples(orc):
+    for kind, E, topk, ng, tg, rn, logits, bias, ids, w in _lines("route_examples.txt"):
+        E, topk, ng, tg, rn = int(E), int(topk), int(ng), int(tg), int(rn)
+        lg = np.array([float(v) for v in logits.split()], np.float32).reshape(1, E)
+        b = None if bias == "-" else np.array([float(v) for v in bias.split()], np.float32)
+        fn = orc.SOFTMAX if kind == "softmax" else orc.SIGMOID
+        gi, gw, _ = orc.route(lg, b, topk, fn, ng, tg, bool(rn))
+        assert list(gi[0]) == [int(v) for v in ids.split()], (kind, logits, gi)
+        np.testing.assert_allclose(gw[0], [float(v) for v in w.split()], atol=2e-7)
+
+
+def test_route_softmax_topk_is_stable_argsort(orc):
+    rng = np.random.default_rng(1)
+    for E, topk in ((8, 2), (64, 6), (256, 8)):
+        lg = rng.standard_normal((300, E)).astype(np.float32)
+        lg[:20, :] = np.round(lg[:20, :])  # many exact ties
+        ids, w, _ = orc.route(lg, None, topk, orc.SOFTMAX)
+        ref = np.argsort(-lg, axis=1, kind="stable")[:, :topk]
+        assert np.array_equal(ids, ref)
+        np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-12)
+        if topk == 2:  # closed form of a renormalised top-2 softmax
+            l0 = np.take_along_axis(lg, ids[:, :1], 1)[:, 0].astype(np.float64)
+            l1 = np.take_along_axis(lg, ids[:, 1:2], 1)[:, 0].astype(np.float64)
+            np.testing.assert_allclose(w[:, 0], 1 / (1 + np.exp(l1 - l0)), rtol=1e-12)
+        # unrenormalised weights are the softmax probabilities themselves
+        _, wp, _ = orc.route(lg, None, topk, orc.SOFTMAX, renorm=False)
+        p = torch.softmax(torch.from_numpy(lg).double(), 1).numpy()
+        np.testing.assert_allclose(wp, np.take_along_axis(p, ids, 1), rtol=1e-12)
+
+
+def test_route_sigmoid_one_group_is_argsort_of_logit_plus_bias(orc):
+    rng = np.random.default_rng(2)
+    E, topk = 256, 8
+    lg = rng.standard_normal((200, E)).astype(np.float32)
+    b = rng.uniform(-3, 0, E).astype(np.float32)
+    ids, w, _ = orc.route(lg, b, topk, orc.SIGMOID, 1, 1)
+    v = (lg + b).astype(np.float32)
+    # sigmoid is monotone: away from fp32 ties the top-k by score is the top-k by v
+    ref = np.argsort(-v, axis=1, kind="stable")[:, :topk]
+    s = 1 / (1 + np.exp(-v.astype(np.float64)))
+    same = (ids == ref).all(1)
+    for t in np.flatnonzero(~same):  # only fp32 score ties may differ
+        sv = np.sort(s[t])[::-1]
+        assert abs(sv[topk - 1] - sv[topk]) < 1e-7
+    assert same.mean() > 0.95
+    sel = np.take_along_axis(s, ids, 1)
+    np.testing.assert_allclose(w, sel / sel.sum(1, keepdims=True), rtol=1e-6)
+
+
+def test_route_sigmoid_grouped_invariants(orc):
+    """Every choice of the group-limited router is valid: kept groups have
+    keys no smaller than dropped ones, all ids lie in kept groups, and no
+    eligible unchosen expert scores above a chosen one."""
+    cfg = WL.SMALL_SIGMOID
+    d = WL.make_inputs(cfg)
+    lg, b = d["logits"].numpy(), d["bias"].numpy()
+    ids, w, margin = orc.route(lg, b, cfg.topk, orc.SIGMOID, cfg.n_groups, cfg.topk_groups)
+    E, G, tg, k = cfg.E, cfg.n_groups, cfg.topk_groups, cfg.topk
+    gs = E // G
+    s = (1 / (1 + np.exp(-(lg + b).astype(np.float32).astype(np.float64))))
+    for t in range(cfg.M):
+        key = np.sort(s[t].reshape(G, gs), 1)[:, -2:].sum(1)
+        kept = set(np.argsort(-key, kind="stable")[:tg].tolist())
+        chosen_groups = set(int(e) // gs for e in ids[t])
+        assert len(set(ids[t].tolist())) == k
+        # every chosen expert sits in one of the best topk_groups groups
+        # (a group tied with the weakest kept one may stand in for it)
+        kth = np.sort(key)[::-1][tg - 1]
+        assert all(key[g] >= kth - 1e-6 for g in chosen_groups)
+        chosen_min = s[t, ids[t]].min()
+        for e in range(E):
+            if e // gs in kept and e not in ids[t]:
+                assert s[t, e] <= chosen_min + 1e-6
+        assert np.all(np.diff(s[t, ids[t]]) <= 1e-7)  # descending order
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-12)
+    assert np.all(margin >= -1e-6)
+
+
+# ------------------------------------------------------ count / permute ----
+
+def test_count_matches_bincount_and_sums_to_P(orc):
+    rng = np.random.default_rng(3)
+    for E, P in ((8, 128), (256, 65536), (32, 7)):
+        ids = rng.integers(0, E, P).astype(np.int32)
+        c, bad = orc.count(ids, E)
+        assert bad == 0
+        assert np.array_equal(c, np.bincount(ids, minlength=E))
+        assert c.sum() == P
+    ids = np.array([0, 5, -1, 3, 9, 3], np.int32)
+    c, bad = orc.count(ids, 4)
+    assert bad == 3 and list(c) == [1, 0, 0, 2]
+
+
+def test_align_is_stable_argsort_and_inverse(orc):
+    rng = np.random.default_rng(4)
+    for E, M, k in ((8, 64, 2), (256, 1000, 8), (4, 3, 1)):
+        ids = rng.integers(0, E, (M, k)).astype(np.int32)
+        off, srt, inv = orc.align(ids, E)
+        flat = ids.ravel()
+        assert np.array_equal(srt, np.argsort(flat, kind="stable"))
+        assert off[0] == 0 and off[E] == M * k
+        assert np.array_equal(np.diff(off), np.bincount(flat, minlength=E))
+        assert np.array_equal(inv[srt], np.arange(M * k))
+        assert np.array_equal(srt[inv], np.arange(M * k))
+        for e in range(E):
+            assert np.all(flat[srt[off[e]:off[e + 1]]] == e)
+
+
+def test_permute_then_unpermute_is_identity(orc):
+    """Identity experts with weights summing to 1 give back the input."""
+    rng = np.random.default_rng(5)
+    M, K, E, k = 50, 24, 8, 3
+    x = rng.standard_normal((M, K))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+    w = rng.uniform(0.1, 1, (M, k))
+    w /= w.sum(1, keepdims=True)
+    off, srt, inv = orc.align(ids, E)
+    xp = orc.permute_rows(x, srt, k)
+    out = orc.unpermute_reduce(xp, inv, w)
+    np.testing.assert_allclose(out, x, rtol=1e-12, atol=1e-12)
+    # a non-identity expert: scaling every permuted row by 2 doubles the output
+    out2 = orc.unpermute_reduce(2 * xp, inv, w)
+    np.testing.assert_allclose(out2, 2 * x, rtol=1e-12, atol=1e-12)
+
+
+# -------------------------------------------------------------- quant ----
+
+def _bits(t):
+    return WL.bf16_bits(t)
+
+
+def test_quant_group_codes_are_torch_cast_and_max_maps_to_448(orc):
+    g = torch.Generator().manual_seed(6)
+    x = (torch.randn(37, 512, generator=g) * torch.logspace(-3, 2, 512)).to(torch.bfloat16)
+    x[3, :128] = 0  # an all-zero group
+    q, s = orc.quant_fp8_group(_bits(x), 128)
+    xf = x.float().view(37, 4, 128)
+    amax = xf.abs().amax(-1)
+    # the group's largest magnitude lands on the top code
+    top = torch.from_numpy(q).view(37, 4, 128)[torch.arange(37)[:, None], torch.arange(4)[None], xf.abs().argmax(-1)]
+    nz = amax > 0
+    assert torch.all((top[nz] & 0x7f) == 0x7e)
+    # codes are the library cast of x / s
+    sf = torch.from_numpy(s).view(37, 4, 1)
+    ref = (xf / sf).to(torch.float8_e4m3fn).view(torch.uint8).view(37, 512).numpy()
+    assert np.array_equal(q, ref)
+    # dequantisation error bound of a 3-bit mantissa (2^-4 relative; 2^-10 s
+    # absolute in the subnormal range)
+    deq = torch.from_numpy(q).view(torch.float8_e4m3fn).double().view(37, 4, 128) * sf.double()
+    err = (deq - xf.double()).abs()
+    bound = torch.maximum(xf.double().abs() * 2.0 ** -4, sf.double() * 2.0 ** -10)
+    assert torch.all(err <= bound * (1 + 1e-9))
+    assert q[3, :128].max() == 0 and s[3, 0] == np.float32(1e-12) / np.float32(448)
+
+
+def test_quant_block_is_per_tile_group_quant(orc):
+    g = torch.Generator().manual_seed(7)
+    w = (torch.randn(256, 384, generator=g) * 0.05).to(torch.bfloat16)
+    q, s = orc.quant_fp8_block(_bits(w), 128)
+    assert s.shape == (2, 3)
+    wf = w.float()
+    for br in range(2):
+        for bc in range(3):
+            tile = wf[br * 128:(br + 1) * 128, bc * 128:(bc + 1) * 128]
+            assert s[br, bc] == np.float32(tile.abs().max().item()) / np.float32(448)
+            ref = (tile / float(s[br, bc])).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(q[br * 128:(br + 1) * 128, bc * 128:(bc + 1) * 128], ref)
+
+
+# ------------------------------------------------------------- experts ----
+
+def _silu(z):
+    return z / (1 + np.exp(-z))
+
+
+def test_single_expert_is_dense_swiglu_mlp(orc):
+    """E = 1, topk = 1: the layer is a dense SwiGLU MLP, checked against
+    fp64 numpy matmuls (rows [0, N) of w1 are the gate, [N, 2N) the up)."""
+    cfg = WL.MoEConfig("e1", M=9, K=64, N=32, E=1, topk=1, seed=21)
+    d = WL.make_inputs(cfg)
+    W = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"]))
+    out, ids, w = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1,
+                                  orc.SOFTMAX, W)
+    x = d["x"].double().numpy()
+    w1 = d["w1"][0].double().numpy()
+    w2 = d["w2"][0].double().numpy()
+    h = _silu(x @ w1[:32].T) * (x @ w1[32:].T)
+    ref = h @ w2.T
+    assert np.all(ids == 0) and np.all(w == 1.0)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    hh, yy = orc.expert_row(_bits(d["x"]), 4, 0, W)
+    np.testing.assert_allclose(hh, h[4], rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(yy, ref[4], rtol=1e-10, atol=1e-13)
+
+
+def test_layer_equals_per_expert_batched_loop(orc):
+    """Two routes to one answer: the oracle's per-token loop against a
+    per-expert loop of numpy matmuls over gathered tokens."""
+    cfg = WL.SMALL_BF16
+    cfg = WL.MoEConfig("pe", M=40, K=128, N=64, E=8, topk=3, seed=22)
+    d = WL.make_inputs(cfg)
+    W = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"]))
+    out, ids, w = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None,
+                                  cfg.topk, orc.SOFTMAX, W)
+    x = d["x"].double().numpy()
+    ref = np.zeros_like(out)
+    for e in range(cfg.E):
+        t, j = np.nonzero(ids == e)
+        if t.size == 0:
+            continue
+        w1 = d["w1"][e].double().numpy()
+        w2 = d["w2"][e].double().numpy()
+        y = (_silu(x[t] @ w1[:cfg.N].T) * (x[t] @ w1[cfg.N:].T)) @ w2.T
+        np.add.at(ref, t, w[t, j][:, None] * y)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    # linearity in w2: doubling w2 doubles the output exactly
+    W2 = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"] * 2))
+    out2, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None,
+                                 cfg.topk, orc.SOFTMAX, W2)
+    np.testing.assert_array_equal(out2, 2 * out)
+    # a listed subset of tokens gives exactly the rows of the full run
+    sub, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None,
+                                cfg.topk, orc.SOFTMAX, W, tokens=[7, 0, 39])
+    np.testing.assert_array_equal(sub, out[[7, 0, 39]])
+
+
+def test_fp8_single_expert_is_dequantised_swiglu(orc):
+    """FP8: with E = 1 the layer is the dense SwiGLU MLP of the dequantised
+    operands (library cast of the codes times the block scales)."""
+    cfg = WL.MoEConfig("f8", M=6, K=256, N=128, E=1, topk=1, dtype=WL.FP8, seed=23)
+    d = WL.make_inputs(cfg)
+    q1, s1 = orc.quant_fp8_block(_bits(d["w1"][0]))
+    q2, s2 = orc.quant_fp8_block(_bits(d["w2"][0]))
+    W = orc.Weights(orc.FP8, q1[None], q2[None], s1[None], s2[None])
+    out, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1,
+                                orc.SOFTMAX, W, requant_h=False)
+
+    def deq(q, s, rows, cols):
+        v = torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy()
+        return v * np.kron(s.astype(np.float64), np.ones((rows, cols)))
+
+    qx, sx = orc.quant_fp8_group(_bits(d["x"]))
+    x = deq(qx, sx, 1, 128)
+    w1 = deq(q1, s1, 128, 128)
+    w2 = deq(q2, s2, 128, 128)
+    h = _silu(x @ w1[:128].T) * (x @ w1[128:].T)
+    np.testing.assert_allclose(out, h @ w2.T, rtol=1e-10, atol=1e-12)
+    # with requantisation of h, each 128-group of h goes through the same
+    # quantiser; check h of one row against the library cast
+    hq, _ = orc.expert_row(_bits(d["x"]), 2, 0, W, requant_h=True)
+    h32 = h[2].astype(np.float32)
+    s = np.float32(np.abs(h32).max()) / np.float32(448)
+    ref = torch.from_numpy(h32 / s).to(torch.float8_e4m3fn).double().numpy() * float(s)
+    np.testing.assert_allclose(hq, ref, rtol=0, atol=float(s) * 2 ** -3 + 1e-12)
+    assert np.mean(np.abs(hq - ref) < 1e-12) > 0.99
+
+
+def test_batched_equals_standard_on_the_same_routing(orc):
+    """BatchedExperts rows computed by the oracle equal the Standard layer's
+    unweighted expert outputs when x_b is built from the Standard permutation;
+    padded rows are never written."""
+    cfg = WL.MoEConfig("bs", M=30, K=128, N=128, E=4, topk=1, seed=24)
+    d = WL.make_inputs(cfg)
+    W = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"]))
+    out, ids, w = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1,
+                                  orc.SOFTMAX, W)
+    assert np.all(w == 1.0)
+    off, srt, inv = orc.align(ids, cfg.E)
+    T = 16
+    counts = np.minimum(np.diff(off), T).astype(np.int32)
+    xb = torch.full((cfg.E, T, cfg.K), 77.0, dtype=torch.bfloat16)
+    for e in range(cfg.E):
+        for r in range(counts[e]):
+            xb[e, r] = d["x"][srt[off[e] + r]]
+    yb, n = orc.batched_experts(_bits(xb), counts, W)
+    assert n == counts.sum()
+    for e in range(cfg.E):
+        for r in range(T):
+            if r < counts[e]:
+                np.testing.assert_allclose(yb[e, r], out[srt[off[e] + r]], rtol=1e-12, atol=1e-14)
+            else:
+                assert np.all(np.isnan(yb[e, r]))

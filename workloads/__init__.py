@@ -1,0 +1,189 @@
+"""Seeded synthetic inputs for the fused MoE layer.
+
+Shared by the tests, the smoke check and the benchmark for both the CUDA
+path and the oracle.  This module holds only random draws and their recipe:
+none of the layer's arithmetic (no routing, no quantisation, no GEMM).
+
+Recipe (the pages measure serving on real models; these synthetic tensors
+stand in for them -- no dataset or trained weight is used):
+  * one ``torch.Generator`` seeded per workload, on the device the tensors are
+    made on; draw order logits, x, w1, w2, then the router bias or the
+    batched counts;
+  * hidden states x ~ N(0, 1) rounded to bf16; router logits ~ N(0, 1) fp32;
+  * w1 (E, 2N, K) ~ N(0, 1/K), w2 (E, K, N) ~ N(0, 1/N), drawn in bf16;
+  * skewed routing (DeepSeek-V3-shaped prefill): a per-expert bias
+    b_e = -s * ln(rank_e), rank a seeded permutation of 1..E and s = 1.1 --
+    the log of a Zipf(s) probability up to a constant, added to the logits;
+  * batched masked format: counts[e] ~ U{0..T} with two experts forced to 0
+    and one to T (positions drawn), valid rows N(0, 1), padded rows
+    N(0, 10^2) garbage that must not reach the output.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+SOFTMAX, SIGMOID = 0, 1
+BF16, FP8 = 0, 1
+
+
+@dataclasses.dataclass(frozen=True)
+class MoEConfig:
+    name: str
+    M: int                 # tokens (Standard) -- or T, max tokens per expert (Batched)
+    K: int                 # hidden size
+    N: int                 # intermediate size (w1 has 2N rows per expert)
+    E: int                 # experts
+    topk: int
+    dtype: int = BF16      # BF16 or FP8 (e4m3, 1x128 activation / 128x128 weight scales)
+    score_fn: int = SOFTMAX
+    n_groups: int = 1
+    topk_groups: int = 1
+    zipf_bias: bool = False
+    renorm: bool = True
+    batched: bool = False  # BatchedExperts (E, T, K) masked by counts
+    seed: int = 0
+
+    @property
+    def P(self) -> int:
+        return self.M * self.topk
+
+    @property
+    def requant_h(self) -> bool:
+        return self.dtype == FP8
+
+
+# The workloads the layer is specified on.
+TINY = MoEConfig("tiny_bf16_M64_K256_N128_E8_top2", M=64, K=256, N=128, E=8,
+                 topk=2, seed=0)
+MIXTRAL_PREFILL = MoEConfig("mixtral8x7b_prefill_bf16_M4096_K4096_N14336_E8_top2",
+                            M=4096, K=4096, N=14336, E=8, topk=2, seed=2)
+DSV3_PREFILL_FP8 = MoEConfig("dsv3_prefill_fp8_M8192_K7168_N2048_E256_top8",
+                             M=8192, K=7168, N=2048, E=256, topk=8, dtype=FP8,
+                             score_fn=SIGMOID, n_groups=8, topk_groups=4,
+                             zipf_bias=True, seed=3)
+DSV3_DECODE = MoEConfig("dsv3_decode_bf16_M64_K7168_N2048_E256_top8",
+                        M=64, K=7168, N=2048, E=256, topk=8, score_fn=SIGMOID,
+                        n_groups=8, topk_groups=4, seed=4)
+BATCHED_MASKED = MoEConfig("batched_masked_bf16_E32_T1024_K7168_N2048",
+                           M=1024, K=7168, N=2048, E=32, topk=1, batched=True,
+                           seed=5000)
+
+# Smaller cases of the same kinds, for parity tests that the oracle finishes in
+# seconds while still spanning several tiles and a ragged tail.
+SMALL_BF16 = MoEConfig("small_bf16_M300_K512_N384_E8_top2", M=300, K=512, N=384,
+                       E=8, topk=2, seed=11)
+SMALL_SIGMOID = MoEConfig("small_sigmoid_bf16_M200_K384_N256_E64_top6",
+                          M=200, K=384, N=256, E=64, topk=6, score_fn=SIGMOID,
+                          n_groups=8, topk_groups=4, zipf_bias=True, seed=12)
+SMALL_FP8 = MoEConfig("small_fp8_M256_K512_N256_E16_top4", M=256, K=512, N=256,
+                      E=16, topk=4, dtype=FP8, score_fn=SIGMOID, n_groups=4,
+                      topk_groups=2, zipf_bias=True, seed=13)
+SMALL_BATCHED = MoEConfig("small_batched_bf16_E6_T200_K256_N256", M=200, K=256,
+                          N=256, E=6, topk=1, batched=True, seed=14)
+
+ALL = [TINY, MIXTRAL_PREFILL, DSV3_PREFILL_FP8, DSV3_DECODE, BATCHED_MASKED]
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _randn(shape, g, device, std=1.0, dtype=torch.float32):
+    t = torch.randn(shape, generator=g, device=device, dtype=dtype)
+    if std != 1.0:
+        t.mul_(std)
+    return t
+
+
+def make_standard(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
+                  with_weights: bool = True) -> dict:
+    """Inputs of the Standard format: logits (M, E) fp32, x (M, K) bf16,
+    w1 (E, 2N, K) bf16, w2 (E, K, N) bf16, bias (E) fp32 or None."""
+    seed = cfg.seed if seed is None else seed
+    g = _gen(seed, device)
+    out = {}
+    out["logits"] = _randn((cfg.M, cfg.E), g, device)
+    out["x"] = _randn((cfg.M, cfg.K), g, device).to(torch.bfloat16)
+    if with_weights:
+        out["w1"] = _randn((cfg.E, 2 * cfg.N, cfg.K), g, device,
+                           std=1.0 / math.sqrt(cfg.K), dtype=torch.bfloat16)
+        out["w2"] = _randn((cfg.E, cfg.K, cfg.N), g, device,
+                           std=1.0 / math.sqrt(cfg.N), dtype=torch.bfloat16)
+    out["bias"] = None
+    if cfg.zipf_bias:
+        rank = torch.randperm(cfg.E, generator=g, device=device).to(torch.float32) + 1.0
+        out["bias"] = (-1.1 * torch.log(rank)).to(torch.float32)
+    return out
+
+
+def make_weights(cfg: MoEConfig, device="cpu", seed: Optional[int] = None) -> dict:
+    """Only the expert weights (the same draws as make_standard/make_batched
+    would give for this seed, skipping the activations)."""
+    seed = cfg.seed if seed is None else seed
+    g = _gen(seed, device)
+    if cfg.batched:
+        _ = _randn((cfg.E, cfg.M, cfg.K), g, device)  # keep the draw order
+    else:
+        _ = _randn((cfg.M, cfg.E), g, device)
+        _ = _randn((cfg.M, cfg.K), g, device)
+    w1 = _randn((cfg.E, 2 * cfg.N, cfg.K), g, device, std=1.0 / math.sqrt(cfg.K),
+                dtype=torch.bfloat16)
+    w2 = _randn((cfg.E, cfg.K, cfg.N), g, device, std=1.0 / math.sqrt(cfg.N),
+                dtype=torch.bfloat16)
+    return {"w1": w1, "w2": w2}
+
+
+def make_batched(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
+                 with_weights: bool = True) -> dict:
+    """Inputs of the BatchedExperts format: x_b (E, T, K) bf16 whose rows
+    r >= counts[e] are N(0, 10^2) garbage, counts (E) int32, w1, w2."""
+    assert cfg.batched
+    seed = cfg.seed if seed is None else seed
+    E, T = cfg.E, cfg.M
+    g = _gen(seed, device)
+    out = {}
+    xb = _randn((E, T, cfg.K), g, device)
+    if with_weights:
+        out["w1"] = _randn((E, 2 * cfg.N, cfg.K), g, device,
+                           std=1.0 / math.sqrt(cfg.K), dtype=torch.bfloat16)
+        out["w2"] = _randn((E, cfg.K, cfg.N), g, device,
+                           std=1.0 / math.sqrt(cfg.N), dtype=torch.bfloat16)
+    counts = torch.randint(0, T + 1, (E,), generator=g, device=device,
+                           dtype=torch.int64)
+    pos = torch.randperm(E, generator=g, device=device)
+    if E >= 3:
+        counts[pos[0]] = 0
+        counts[pos[1]] = 0
+        counts[pos[2]] = T
+    counts = counts.to(torch.int32)
+    rows = torch.arange(T, device=device).view(1, T, 1)
+    pad = rows >= counts.view(E, 1, 1).to(rows.dtype)
+    garbage = _randn((E, T, cfg.K), g, device, std=10.0)
+    xb = torch.where(pad, garbage, xb)
+    out["x_b"] = xb.to(torch.bfloat16)
+    out["counts"] = counts
+    return out
+
+
+def make_inputs(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
+                with_weights: bool = True) -> dict:
+    if cfg.batched:
+        return make_batched(cfg, device, seed, with_weights)
+    return make_standard(cfg, device, seed, with_weights)
+
+
+def bf16_bits(t: torch.Tensor):
+    """numpy uint16 view of a bf16 tensor's bits (on the host)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
+
+
+def flops(cfg: MoEConfig, rows: int) -> float:
+    """Algorithmic FLOPs of the two expert GEMMs for `rows` routed rows:
+    4*K*N for the gate/up GEMM plus 2*K*N for the down GEMM per row."""
+    return 6.0 * cfg.K * cfg.N * rows
