@@ -43,10 +43,11 @@
  *   R2 sigmoid grouped router: s_e = sigmoid(l_e + b_e); E experts in
  *      n_groups contiguous groups; group key = sum of the group's two largest
  *      s; keep the topk_groups best groups, then the topk best experts by s
- *      among them; weight s_j, renormalised when asked.
+ *      among them; weight s_j, renormalised when asked.  Experts are ranked
+ *      by v_e = l_e + b_e (fp32), the order of the real-valued scores.
  *   R4 equal keys: the lower index wins (expert id, group id).
- *   R5 s_e is the fp32 rounding of the fp64 value 1/(1+exp(-(double)v)),
- *      v = l_e + b_e added in fp32; the group key is an fp32 add.
+ *   R5 in a group key each s is the fp32 rounding of the fp64 value
+ *      1/(1+exp(-(double)v)); the key is the fp32 add of the two.
  *   R6 ids in a row are in descending score order.
  *   P1 within one expert, pairs keep ascending pair order p = t*topk + j.
  *   Q1 FP8 group quant: s = max(amax, 1e-12) / 448 in fp32,
@@ -189,31 +190,28 @@ static void route_softmax_row(const float *l, int E, int topk, int renorm,
     free(taken);
 }
 
-/* R5: the fp32 score. */
-static float sigmoid_score(float logit, float bias)
+/* R5: the score a group key is built from -- the fp32 rounding of the fp64
+ * value 1 / (1 + exp(-v)). */
+static float sigmoid_score(float v)
 {
-    float v = logit + bias;
     return (float)(1.0 / (1.0 + exp(-(double)v)));
 }
 
-static double sigmoid_exact(float logit, float bias)
-{
-    float v = logit + bias;
-    return 1.0 / (1.0 + exp(-(double)v));
-}
-
-/* R2 for one token.  margin (optional) receives the smallest fp64 gap at a
- * selection boundary: between the last kept and the best dropped group key,
- * and between the last chosen and the best unchosen eligible expert.  A tiny
- * or negative margin marks a token whose choice an fp32 rounding could flip. */
+/* R2 for one token.  The sigmoid is strictly increasing, so ranking experts
+ * by their score is ranking them by v_e = l_e + b_e (an exact fp32 add);
+ * experts are chosen on v, which keeps the order of the real-valued scores
+ * (no ties made by rounding s to fp32).  A group's key is the fp32 sum of the
+ * fp32 scores of its two largest v.
+ * margin (optional) receives the fp64 gap between the last kept and the best
+ * dropped group key (+inf without group limit): a tiny gap marks a token
+ * whose group choice a last-bit difference in exp could flip. */
 static void route_sigmoid_row(const float *l, const float *bias, int E,
                               int topk, int n_groups, int topk_groups,
                               int renorm, int32_t *ids, double *w,
                               double *margin)
 {
     int gsz, g, e, j, i;
-    float *s = (float *)malloc(sizeof(float) * (size_t)E);
-    double *s64 = (double *)malloc(sizeof(double) * (size_t)E);
+    float *v = (float *)malloc(sizeof(float) * (size_t)E);
     float *key;
     double *key64;
     char *gsel, *taken;
@@ -229,27 +227,30 @@ static void route_sigmoid_row(const float *l, const float *bias, int E,
     gsel = (char *)calloc((size_t)n_groups, 1);
     taken = (char *)calloc((size_t)E, 1);
 
-    for (e = 0; e < E; ++e) {
-        float b = bias ? bias[e] : 0.0f;
-        s[e] = sigmoid_score(l[e], b);
-        s64[e] = sigmoid_exact(l[e], b);
-    }
+    for (e = 0; e < E; ++e)
+        v[e] = l[e] + (bias ? bias[e] : 0.0f);
 
-    /* group key: sum of the two largest scores of the group (one when the
-     * group has a single expert); the fp32 add is exact-order independent */
+    /* group key from the group's two largest v (one when the group has a
+     * single expert); which of two equal v is "first" does not matter */
     for (g = 0; g < n_groups; ++g) {
         int a = -1, c = -1;
         for (i = 0; i < gsz; ++i) {
             e = g * gsz + i;
-            if (a < 0 || s[e] > s[a]) {
+            if (a < 0 || v[e] > v[a]) {
                 c = a;
                 a = e;
-            } else if (c < 0 || s[e] > s[c]) {
+            } else if (c < 0 || v[e] > v[c]) {
                 c = e;
             }
         }
-        key[g] = c >= 0 ? s[a] + s[c] : s[a];
-        key64[g] = c >= 0 ? s64[a] + s64[c] : s64[a];
+        if (c >= 0) {
+            key[g] = sigmoid_score(v[a]) + sigmoid_score(v[c]);
+            key64[g] = 1.0 / (1.0 + exp(-(double)v[a])) +
+                       1.0 / (1.0 + exp(-(double)v[c]));
+        } else {
+            key[g] = sigmoid_score(v[a]);
+            key64[g] = 1.0 / (1.0 + exp(-(double)v[a]));
+        }
     }
 
     if (topk_groups < n_groups) {
@@ -278,26 +279,21 @@ static void route_sigmoid_row(const float *l, const float *bias, int E,
         for (e = 0; e < E; ++e) {
             if (taken[e] || !gsel[e / gsz])
                 continue;
-            if (best < 0 || s[e] > s[best])
+            if (best < 0 || v[e] > v[best])
                 best = e;
         }
         taken[best] = 1;
         ids[j] = best;
-        w[j] = (double)s[best];
+        w[j] = 1.0 / (1.0 + exp(-(double)v[best]));
         sel += w[j];
     }
-    for (e = 0; e < E; ++e)
-        if (!taken[e] && gsel[e / gsz] &&
-            s64[ids[topk - 1]] - s64[e] < mg)
-            mg = s64[ids[topk - 1]] - s64[e];
     if (renorm)
         for (j = 0; j < topk; ++j)
             w[j] /= sel;
     if (margin)
         *margin = mg;
 
-    free(s);
-    free(s64);
+    free(v);
     free(key);
     free(key64);
     free(gsel);
