@@ -1,0 +1,455 @@
+"""Benchmark of the fused MoE layer on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic tokens:
+route -> align/permute -> [FP8 quantise] -> gather -> gate/up GEMM + SiLU*mul
+-> down GEMM + router weight -> ordered top-k reduce, each a CUDA kernel of
+libgbmoe.so launched through its C ABI.
+
+Default workload: the Mixtral-8x7B-shaped prefill layer in bf16 (M=4096 tokens,
+K=4096, N=14336, E=8, top-2), synthetic seeded inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on host cores
+
+Multi-GPU: the layer is data parallel over tokens and needs no exchange, so
+N ranks run N independent replicas (weak scaling); ranks only meet at the
+timing barriers.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+WORKLOADS = {c.name: c for c in WL.ALL}
+DEFAULT = WL.MIXTRAL_PREFILL.name
+METRIC = "MoE-layer tokens/s and % of roofline (TFLOP/s or HBM GB/s) on 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 2 ** 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _kernel_traffic(kernel_key: str):
+    """DRAM bytes per launch of a kernel from a committed ncu summary in
+    profiles/ (a line 'traffic_bytes_per_launch: <n>' and 'source_sha256:
+    <hash of csrc/gemm.cu>'); None when absent or the kernel source changed."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_key}.traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for ln in f:
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                vals[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "mixture_experts_layer_count_gb300", "csrc", "gemm.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if vals.get("source_sha256") != h:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+class Layer:
+    """Device buffers of one Standard-format layer plus the staged launch
+    sequence (the same kernels moe_forward launches, called one by one so
+    the dominant GEMM can be timed with events on the launching stream)."""
+
+    def __init__(self, cfg, device):
+        import torch
+        import mixture_experts_layer_count_gb300 as g
+        self.g, self.torch, self.cfg = g, torch, cfg
+        g.load()
+        d = WL.make_inputs(cfg, device)
+        self.x, self.logits, self.bias = d["x"], d["logits"], d["bias"]
+        M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
+        P = M * k
+        self.fp8 = cfg.dtype == WL.FP8
+        if self.fp8:
+            self.w1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=device)
+            self.w2 = torch.empty((E, K, N), dtype=torch.uint8, device=device)
+            self.w1s = torch.empty((E, 2 * N // 128, K // 128), dtype=torch.float32, device=device)
+            self.w2s = torch.empty((E, K // 128, N // 128), dtype=torch.float32, device=device)
+            g.moe_quant_fp8_block(d["w1"], self.w1, self.w1s)
+            g.moe_quant_fp8_block(d["w2"], self.w2, self.w2s)
+            del d
+            torch.cuda.empty_cache()
+        else:
+            self.w1, self.w2, self.w1s, self.w2s = d["w1"], d["w2"], None, None
+        i32, f32 = torch.int32, torch.float32
+        self.ids = torch.empty((M, k), dtype=i32, device=device)
+        self.wts = torch.empty((M, k), dtype=f32, device=device)
+        self.counts = torch.empty(E, dtype=i32, device=device)
+        self.offsets = torch.empty(E + 1, dtype=i32, device=device)
+        self.sorted = torch.empty(P, dtype=i32, device=device)
+        self.inv = torch.empty(P, dtype=i32, device=device)
+        self.align_ws = g.workspace(g.WS_ALIGN, M, E, 0, 0, k, 0, device=device)
+        adt = torch.uint8 if self.fp8 else torch.bfloat16
+        self.xq = torch.empty((M, K), dtype=torch.uint8, device=device) if self.fp8 else None
+        self.xs = torch.empty((M, K // 128), dtype=f32, device=device) if self.fp8 else None
+        self.A = torch.empty((P, K), dtype=adt, device=device)
+        self.As = torch.empty((P, K // 128), dtype=f32, device=device) if self.fp8 else None
+        self.H = torch.empty((P, N), dtype=adt, device=device)
+        self.Hs = torch.empty((P, N // 128), dtype=f32, device=device) if self.fp8 else None
+        self.y = torch.empty((M, k, K), dtype=torch.bfloat16, device=device)
+        self.out = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+        self.err = torch.zeros(1, dtype=i32, device=device)
+        self.fwd_ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype, device=device)
+        self.launches_per_step = 8 + (1 if self.fp8 else 0)  # route, 3 align, [quant], gather, 2 GEMMs, reduce
+
+    def step(self, ev_gemm=None):
+        g, c = self.g, self.cfg
+        M, E, N, K, k = c.M, c.E, c.N, c.K, c.topk
+        g.moe_topk_route(self.logits, self.bias, k, c.score_fn, c.n_groups, c.topk_groups,
+                         c.renorm, self.ids, self.wts)
+        g.moe_align_permute(self.ids, E, self.counts, self.offsets, self.sorted, self.inv,
+                            self.align_ws, self.err)
+        src, src_s = self.x, None
+        if self.fp8:
+            g.moe_quant_fp8_group(self.x, self.xq, self.xs)
+            src, src_s = self.xq, self.xs
+        g.moe_permute_rows(src, src_s, self.sorted, self.offsets, k, E, c.dtype, self.A, self.As)
+        if ev_gemm is not None:
+            ev_gemm[0].record()
+        g.moe_grouped_gemm_gate_up_silu(self.A, self.As, self.offsets, M, k, E, N, K, self.w1,
+                                        self.w1s, c.dtype, self.H, self.Hs, self.err)
+        if ev_gemm is not None:
+            ev_gemm[1].record()
+        g.moe_grouped_gemm_down(self.H, self.Hs, self.sorted, self.offsets, self.wts, M, k, E,
+                                N, K, self.w2, self.w2s, c.dtype, self.y, self.err)
+        g.moe_unpermute_weighted_reduce(self.y, self.inv, M, k, K, self.out)
+
+    def forward_public(self, x, logits, out):
+        """The public one-call API on device tensors."""
+        c = self.cfg
+        self.g.moe_forward(x, logits, self.bias, c.N, c.E, c.topk, c.score_fn, c.n_groups,
+                           c.topk_groups, c.renorm, c.dtype, self.w1, self.w1s, self.w2,
+                           self.w2s, out, self.fwd_ws, err_word=self.err)
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_gpu(args, cfg):
+    import torch
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    layer = Layer(cfg, dev)
+    # warm-up (untimed)
+    for _ in range(args.warmup):
+        layer.step()
+    torch.cuda.synchronize()
+    assert layer.err.item() == 0, f"device error word {layer.err.item()}"
+
+    steps = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t0.record()
+        for i in range(steps):
+            layer.step(ev[i])
+        t1.record()
+        barrier()
+    ms = t0.elapsed_time(t1)
+    gemm_ms = [a.elapsed_time(b) for a, b in ev]
+    assert layer.err.item() == 0, f"device error word {layer.err.item()}"
+
+    # end to end through the public one-call API: pinned host inputs copied in,
+    # the output copied back, every step inside the timed region
+    x_h = layer.x.cpu().pin_memory()
+    lg_h = layer.logits.cpu().pin_memory()
+    out_h = torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory()
+    x_d = torch.empty_like(layer.x)
+    lg_d = torch.empty_like(layer.logits)
+    out_d = torch.empty_like(layer.out)
+    for _ in range(max(1, args.warmup)):
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        layer.forward_public(x_d, lg_d, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        layer.forward_public(x_d, lg_d, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    assert layer.err.item() == 0
+
+    # max over ranks
+    if pg is not None:
+        t = torch.tensor([ms, e2e_ms, float(np.mean(gemm_ms))], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms, e2e_ms, gemm_avg = t.tolist()
+    else:
+        gemm_avg = float(np.mean(gemm_ms))
+
+    tokens = cfg.M * steps * world
+    value = tokens / (ms / 1e3)
+    e2e_value = tokens / (e2e_ms / 1e3)
+    peaks, src = _peaks()
+    P = cfg.M * cfg.topk
+    gemm_flop = 4.0 * cfg.K * cfg.N * P  # gate/up GEMM, algorithmic
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    if cfg.dtype == WL.FP8:
+        peak = peak * 2.0  # nominal fp8 : bf16 dense ratio
+    achieved = gemm_flop / (gemm_avg / 1e3) / 1e12
+    traffic = _kernel_traffic(f"grouped_gemm_gate_up_{'fp8' if cfg.dtype == WL.FP8 else 'bf16'}")
+    layer_flop = 6.0 * cfg.K * cfg.N * P
+    clocks = clk.summary()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3" if cfg.dtype == WL.FP8 else "bf16",
+        "data": "synthetic (seeded N(0,1) activations/logits, N(0,1/K), N(0,1/N) weights)",
+        "config": {"workload": cfg.name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "E": cfg.E,
+                   "topk": cfg.topk, "format": "standard",
+                   "l2": "working set > L2 (weights %.2f GB stream every step)" %
+                         ((cfg.E * 3 * cfg.N * cfg.K * (1 if cfg.dtype == WL.FP8 else 2)) / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "layer_tflops": layer_flop / (ms / steps / 1e3) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (gate/up + SiLU*mul)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{src} bf16 sustained" + (" x2 (fp8 nominal ratio)" if cfg.dtype == WL.FP8 else ""),
+                     "gemm_ms": gemm_avg, "flop_per_launch": gemm_flop},
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(layer.x.numel() * 2 + layer.logits.numel() * 4),
+                "d2h_bytes_per_step": int(layer.out.numel() * 2)},
+        "gpu_launches": layer.launches_per_step * steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(cfg, layer, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def _oracle_inputs(cfg, d, tokens):
+    import oracle as orc
+    rid, _, _ = orc.route(d["logits"].cpu().numpy(),
+                          None if d["bias"] is None else d["bias"].cpu().numpy(),
+                          cfg.topk, cfg.score_fn, cfg.n_groups, cfg.topk_groups, cfg.renorm)
+    experts = np.unique(rid[tokens])
+    blocks = {}
+    for e in experts:
+        b1 = WL.bf16_bits(d["w1"][e])
+        b2 = WL.bf16_bits(d["w2"][e])
+        if cfg.dtype == WL.BF16:
+            blocks[int(e)] = (b1, b2)
+        else:
+            q1, s1 = orc.quant_fp8_block(b1)
+            q2, s2 = orc.quant_fp8_block(b2)
+            blocks[int(e)] = (q1, q2, s1, s2)
+    return orc.Weights(cfg.dtype, experts=blocks, E=cfg.E, N=cfg.N, K=cfg.K)
+
+
+def _time_oracle(cfg, d, W, tokens, threads):
+    import oracle as orc
+    t = time.perf_counter()
+    orc.moe_forward(WL.bf16_bits(d["x"]), d["logits"].cpu().numpy(),
+                    None if d["bias"] is None else d["bias"].cpu().numpy(), cfg.topk,
+                    cfg.score_fn, W, cfg.n_groups, cfg.topk_groups, cfg.renorm,
+                    cfg.requant_h, tokens=tokens, nthreads=threads)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(cfg, layer, budget_s):
+    """The oracle as it stands on the host cores, on a bounded token sample."""
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    d = {"x": layer.x, "logits": layer.logits, "bias": layer.bias}
+    wd = WL.make_weights(cfg, layer.x.device)
+    d.update(wd)
+    rng = np.random.default_rng(0)
+    probe = rng.choice(cfg.M, cores, replace=False)
+    n_target = cores
+    W = _oracle_inputs(cfg, d, np.arange(cfg.M))
+    dt = _time_oracle(cfg, d, W, probe, cores)
+    n_target = int(max(cores, min(cfg.M, cores * max(1, math.floor(budget_s / max(dt, 1e-3))))))
+    tokens = rng.choice(cfg.M, n_target, replace=False)
+    dt = _time_oracle(cfg, d, W, tokens, cores)
+    return {"value": len(tokens) / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(tokens)} of {cfg.M} tokens of {cfg.name}, fp64 per-token loops, "
+                      f"{cores} OpenMP threads, {dt:.1f} s"}
+
+
+def run_reference(args, cfg):
+    """--impl reference: the CPU oracle (this build's reference arm), timed
+    per step on a bounded token sample of the same workload."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import torch
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = WL.make_inputs(cfg, dev)
+    tokens_per_step = cores
+    rng = np.random.default_rng(0)
+    W = _oracle_inputs(cfg, d, np.arange(cfg.M))
+    for _ in range(args.warmup):
+        _time_oracle(cfg, d, W, rng.choice(cfg.M, 1, replace=False), cores)
+    total = 0.0
+    for _ in range(args.steps):
+        total += _time_oracle(cfg, d, W, rng.choice(cfg.M, tokens_per_step, replace=False), cores)
+    value = tokens_per_step * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3" if cfg.dtype == WL.FP8 else "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "E": cfg.E,
+                       "topk": cfg.topk, "format": "standard",
+                       "sample_tokens_per_step": tokens_per_step},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{tokens_per_step} tokens per step of {cfg.name}"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gbmoe", choices=["gbmoe", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    cfg = WORKLOADS[args.workload]
+    if cfg.batched:
+        raise SystemExit("the batched workload is measured by its own test, not a bench line")
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_gpu(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,275 @@
+/*
+ * gbmoe.h -- C ABI of the GB300 (sm_103a) fused mixture-of-experts layer.
+ *
+ * The layer follows the modular decomposition of
+ * "vllm/model_executor/layers/fused_moe/modular_kernel.py" (vllm-cpu
+ * 0.11.0.post2 diff view), module comment:
+ *     [Router] -> [Quantize-Prepare] -> [Permute-Experts-Unpermute] -> [Finalize]
+ * with its problem statement from _moe_problem_size: E experts, M tokens,
+ * hidden size K, intermediate size N, topk experts per token,
+ * w1 (E, 2N, K) and w2 (E, K, N); and its two activation formats from
+ * FusedMoEActivationFormat: Standard (M, K) and BatchedExperts
+ * (E, max_tokens, K).  The batched format is masked by a device-resident
+ * per-expert token count, as in "EP: CUDA-graph-safe HT internode
+ * dispatch+combine (worst-tokens mode)" (uccl pull request 7), so that the
+ * whole layer can be captured in a CUDA graph without reading counts on the
+ * host.
+ *
+ * Conventions for every call below:
+ *   - Pointers are DEVICE pointers to caller-owned memory unless stated
+ *     otherwise; every tensor is row-major with its last index contiguous.
+ *     bf16 is IEEE bfloat16 bits (uint16), e4m3 is the OCP "E4M3FN" byte.
+ *   - The library allocates no device memory and never synchronises the
+ *     host: each call validates its arguments, enqueues kernels on `stream`
+ *     and returns.  Scratch memory comes from a caller buffer `ws` of at least
+ *     moe_workspace_size(...) bytes, 256-byte aligned.
+ *   - Tensors read by the tensor-core GEMMs (x / A rows, w1, w2, H) must start
+ *     on a 16-byte boundary.
+ *   - Return value: GBMOE_OK, or GBMOE_INVALID_ARG (null pointer, bad size,
+ *     K or N not a multiple of 128, topk > E, workspace too small,
+ *     misaligned pointer), GBMOE_UNSUPPORTED (dtype, or a device that is not
+ *     sm_103), GBMOE_CUDA_ERROR (a launch failed; see gbmoe_last_cuda_error).
+ *     Nothing is enqueued when a call returns an error.
+ *   - Errors in the DATA (an expert id outside [0, E), a batched count
+ *     outside [0, T], a device wait that ran out of time) cannot be seen on
+ *     the host without a sync.  Kernels skip the offending element and OR a
+ *     GBMOE_ERR_* bit into the caller's device word `err_word` (may be NULL
+ *     where noted); read it after synchronising.  No kernel traps.
+ *   - M == 0 (or E * T == 0) is a valid no-op and returns GBMOE_OK.
+ */
+#ifndef GBMOE_H
+#define GBMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gbmoe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    GBMOE_OK = 0,
+    GBMOE_INVALID_ARG = 1,
+    GBMOE_UNSUPPORTED = 2,
+    GBMOE_CUDA_ERROR = 3
+} gbmoe_status_t;
+
+/* element type of activations / weights fed to the expert GEMMs */
+enum { GBMOE_BF16 = 0, GBMOE_FP8_E4M3 = 1 };
+/* router score function */
+enum { GBMOE_SOFTMAX = 0, GBMOE_SIGMOID = 1 };
+/* which call a workspace is sized for (moe_workspace_size) */
+enum {
+    GBMOE_WS_ALIGN = 0,    /* moe_align_permute                       */
+    GBMOE_WS_BATCHED = 2,  /* moe_batched_masked_experts              */
+    GBMOE_WS_FORWARD = 3   /* moe_forward (the whole Standard layer)  */
+};
+
+/* bits OR-ed into *err_word by the kernels */
+#define GBMOE_ERR_BAD_EXPERT_ID 0x1  /* an id outside [0, E): the pair is skipped  */
+#define GBMOE_ERR_COUNT_RANGE 0x2    /* a batched count outside [0, T]: clamped    */
+#define GBMOE_ERR_TIMEOUT 0x4        /* a pipeline wait ran out of time: tile left  */
+
+/* Status code as a short English string (static storage). */
+const char *gbmoe_status_string(gbmoe_status_t status);
+
+/* The cudaError_t (as int) of the last failed launch in this process, 0 if none. */
+int gbmoe_last_cuda_error(void);
+
+/* Bytes of workspace a call needs.  `which` is a GBMOE_WS_* value; M_or_T is
+ * M for the Standard calls and T (max tokens per expert) for the batched one.
+ * Returns 0 for invalid arguments. */
+size_t moe_workspace_size(int which, int M_or_T, int E, int N, int K, int topk,
+                          int dtype);
+
+/* [Router] -- the first stage of the module comment of modular_kernel.py;
+ * FusedMoEModularKernel.forward receives its topk_weights / topk_ids.
+ * Per token t:
+ *   score_fn GBMOE_SOFTMAX: the topk largest logits (softmax is monotone);
+ *     weight = softmax(logits[t])[e], divided by its sum over the chosen
+ *     experts when renormalize != 0.
+ *   score_fn GBMOE_SIGMOID: s_e = sigmoid(v_e), v_e = logits[t,e] + bias[e]
+ *     (fp32 add).  The E experts form n_groups contiguous groups; a group's
+ *     key is the fp32 sum of the scores of its two largest v, each score the
+ *     fp32 rounding of an fp64 sigmoid; the topk_groups groups with the
+ *     largest keys are kept, and the topk experts with the largest v (the
+ *     sigmoid's order) among them are chosen; weight = s_e, renormalised as
+ *     above.  n_groups <= 1 means no group limit.
+ *   Ties go to the lower expert (group) index; a row lists its experts in
+ *   descending score order.
+ * logits (M, E) fp32; bias (E) fp32 or NULL (sigmoid only);
+ * topk_ids (M, topk) int32 out; topk_weights (M, topk) fp32 out.
+ * 1 <= topk <= E <= 512; for sigmoid, E % n_groups == 0 and
+ * topk <= topk_groups * (E / n_groups).  err_word unused (may be NULL). */
+gbmoe_status_t moe_topk_route(const float *logits, const float *bias, int M,
+                              int E, int topk, int score_fn, int n_groups,
+                              int topk_groups, int renormalize,
+                              int32_t *topk_ids, float *topk_weights,
+                              int32_t *err_word, gbmoe_stream_t stream);
+
+/* count_expert_num_tokens as named in modular_kernel.py
+ * (FusedMoEModularKernel._maybe_chunk_fused_experts) and the
+ * ExpertTokensMetadata.expert_num_tokens it fills:
+ * counts[e] = #{p < M*topk : topk_ids[p] == e}, computed on the device.
+ * Ids outside [0, E) are skipped and set GBMOE_ERR_BAD_EXPERT_ID.
+ * topk_ids (M, topk) int32; counts (E) int32 out (overwritten). */
+gbmoe_status_t moe_count_expert_tokens(const int32_t *topk_ids, int M,
+                                       int topk, int E, int32_t *counts,
+                                       int32_t *err_word,
+                                       gbmoe_stream_t stream);
+
+/* The "Permute" of [Permute-Experts-Unpermute]: a stable counting sort of the
+ * P = M*topk (token, slot) pairs by expert.  Pair p = t*topk + j.
+ *   counts (E) int32 out, or NULL: counts[e] = #{p : topk_ids[p] == e}, the
+ *     ExpertTokensMetadata.expert_num_tokens of the pages;
+ *   offsets (E+1) int32 out: offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e];
+ *   sorted_pair_ids (M*topk) int32 out: sorted_pair_ids[offsets[e] + r] is the
+ *     r-th pair, in ascending p, routed to expert e (entries at and beyond
+ *     offsets[E] are left unwritten);
+ *   inv (M*topk) int32 out: inv[p] = the position of p in sorted_pair_ids,
+ *     -1 for a pair whose id is outside [0, E) (which also sets
+ *     GBMOE_ERR_BAD_EXPERT_ID).
+ * ws: moe_workspace_size(GBMOE_WS_ALIGN, M, E, 0, 0, topk, 0) bytes (one
+ * histogram per chunk of 2048 pairs).  err_word may be NULL. */
+gbmoe_status_t moe_align_permute(const int32_t *topk_ids, int M, int topk,
+                                 int E, int32_t *counts, int32_t *offsets,
+                                 int32_t *sorted_pair_ids, int32_t *inv,
+                                 void *ws, size_t ws_bytes, int32_t *err_word,
+                                 gbmoe_stream_t stream);
+
+/* [Quantize-Prepare] (FusedMoEPrepareAndFinalize.prepare quantises the
+ * activations before the experts run), per-token-group FP8:
+ * for each token t and each group g of `group` consecutive columns,
+ *   s = max(max_k |x[t,k]|, 1e-12) / 448   (fp32, IEEE division)
+ *   q[t,k] = e4m3(x[t,k] / s)               (round to nearest even, saturating at 448)
+ * x (M, K) bf16; q (M, K) e4m3 out; scales (M, K/group) fp32 out.
+ * group must be 128 and K % 128 == 0. */
+gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, int M, int K, int group,
+                                   uint8_t *q, float *scales,
+                                   gbmoe_stream_t stream);
+
+/* The same quantiser over block x block tiles of a weight matrix, for
+ * preparing FP8 expert weights (not part of the timed layer):
+ * w (R, C) bf16 -> q (R, C) e4m3 and scales (R/block, C/block) fp32, one
+ * scale per tile from the tile's largest magnitude.  block must be 128,
+ * R % 128 == 0 and C % 128 == 0.  w1 (E, 2N, K) is passed as R = E*2N,
+ * C = K; w2 (E, K, N) as R = E*K, C = N. */
+gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
+                                   int block, uint8_t *q, float *scales,
+                                   gbmoe_stream_t stream);
+
+/* The data movement of the "Permute": the rows of the first GEMM in sorted
+ * order, A[i] = x[sorted_pair_ids[i] / topk] for i < offsets[E] (rows at and
+ * beyond offsets[E] are left unwritten).
+ * dtype GBMOE_BF16: x (M, K) bf16 -> A (M*topk, K) bf16; scales unused.
+ * dtype GBMOE_FP8_E4M3: x (M, K) e4m3 with x_scales (M, K/128) fp32 ->
+ *   A (M*topk, K) e4m3 with A_scales (M*topk, K/128).
+ * K % 128 == 0; x and A 16-byte aligned. */
+gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
+                                const int32_t *sorted_pair_ids,
+                                const int32_t *offsets, int M, int topk, int E,
+                                int K, int dtype, void *A, float *A_scales,
+                                gbmoe_stream_t stream);
+
+/* First expert GEMM with the gated activation fused into its epilogue:
+ * FusedMoEPermuteExpertsUnpermute.apply ("matmul + act_mul + optionally
+ * quant") with activation "silu" (silu_and_mul: the output is half as wide as
+ * the GEMM).  For every sorted position i in [offsets[e], offsets[e+1]):
+ *   g[n] = A[i] . w1[e, n, :],   u[n] = A[i] . w1[e, N + n, :]   (n < N)
+ *   H[i, n] = silu(g[n]) * u[n],  silu(z) = z / (1 + exp(-z))
+ * Rows [0, N) of w1[e] are the gate, rows [N, 2N) the up projection.
+ * A (M*topk, K) is in sorted order (moe_permute_rows); rows of H at and beyond
+ * offsets[E] are left unwritten.
+ * dtype GBMOE_BF16: A bf16, w1 (E, 2N, K) bf16, H (M*topk, N) bf16;
+ *   A_scales / w1_scales / H_scales unused (NULL).
+ * dtype GBMOE_FP8_E4M3: A e4m3 with A_scales (M*topk, K/128) fp32; w1 e4m3
+ *   with w1_scales (E, 2N/128, K/128) fp32 (128 x 128 blocks); each 128-wide
+ *   K block is accumulated in fp32 and scaled by A_scale * w1_scale before it
+ *   is added.  H is written as e4m3 with H_scales (M*topk, N/128) fp32,
+ *   requantised per 128-group of a row with the moe_quant_fp8_group rule.
+ * Accumulation is fp32.  N % 128 == 0, K % 128 == 0.  err_word may be NULL. */
+gbmoe_status_t moe_grouped_gemm_gate_up_silu(
+    const void *A, const float *A_scales, const int32_t *offsets, int M,
+    int topk, int E, int N, int K, const void *w1, const float *w1_scales,
+    int dtype, void *H, float *H_scales, int32_t *err_word,
+    gbmoe_stream_t stream);
+
+/* Second expert GEMM with the router weight fused into its epilogue
+ * (the experts own the weight application, which
+ * FusedMoEPermuteExpertsUnpermute.finalize_weight_and_reduce_impl hands to
+ * [Finalize]).  For every sorted position i of expert e, with
+ * p = sorted_pair_ids[i]:
+ *   y_slot[p, k] = topk_weights[p] * (H[i, :] . w2[e, k, :])      (k < K)
+ * y_slot (M, topk, K) bf16 is the fused_expert_output of
+ * FusedMoEPrepareAndFinalize.finalize, already weighted; its rows of pairs
+ * whose id is invalid are not written.
+ * dtype GBMOE_BF16: H (M*topk, N) bf16, w2 (E, K, N) bf16.
+ * dtype GBMOE_FP8_E4M3: H e4m3 + H_scales (M*topk, N/128); w2 e4m3 +
+ *   w2_scales (E, K/128, N/128).  Accumulation fp32.  err_word may be NULL. */
+gbmoe_status_t moe_grouped_gemm_down(
+    const void *H, const float *H_scales, const int32_t *sorted_pair_ids,
+    const int32_t *offsets, const float *topk_weights, int M, int topk, int E,
+    int N, int K, const void *w2, const float *w2_scales, int dtype,
+    uint16_t *y_slot, int32_t *err_word, gbmoe_stream_t stream);
+
+/* [Finalize]: TopKWeightAndReduce.apply and FusedMoEPrepareAndFinalize.finalize
+ * (output (M, K) from fused_expert_output (M, topk, K)).  The weights are
+ * already applied, so
+ *   out[t, k] = bf16( sum_{j = 0 .. topk-1} y_slot[t, j, k] )
+ * summed in fp32 in slot order j = 0, 1, ... (deterministic), skipping the
+ * pairs with inv[t*topk + j] < 0 when inv is not NULL.
+ * y_slot (M, topk, K) bf16; out (M, K) bf16. */
+gbmoe_status_t moe_unpermute_weighted_reduce(const uint16_t *y_slot,
+                                             const int32_t *inv, int M,
+                                             int topk, int K, uint16_t *out,
+                                             gbmoe_stream_t stream);
+
+/* Both expert GEMMs in the BatchedExperts format (E, T, K), masked by the
+ * device-resident expert_num_tokens as the masked grouped GEMM of the
+ * worst-tokens mode reads it: for every expert e and row r < c_e,
+ * c_e = min(max(expert_num_tokens[e], 0), T),
+ *   h = silu(x_b[e,r] . w1[e, 0:N]^T) * (x_b[e,r] . w1[e, N:2N]^T)
+ *   y_b[e, r, :] = h . w2[e]^T           (unweighted; no reduction)
+ * Rows r >= c_e of x_b are never read and rows r >= c_e of y_b are never
+ * written.  A count outside [0, T] is clamped and sets GBMOE_ERR_COUNT_RANGE.
+ * No count is read on the host, so the call can be captured in a CUDA graph
+ * and replayed with new counts.
+ * dtype GBMOE_BF16 only: x_b (E, T, K) bf16, w1 (E, 2N, K), w2 (E, K, N)
+ * bf16, y_b (E, T, K) bf16; x_b_scales, w1_scales, w2_scales NULL.
+ * ws: moe_workspace_size(GBMOE_WS_BATCHED, T, E, N, K, 1, dtype) bytes. */
+gbmoe_status_t moe_batched_masked_experts(
+    const void *x_b, const float *x_b_scales,
+    const int32_t *expert_num_tokens, int E, int T, int N, int K,
+    const void *w1, const float *w1_scales, const void *w2,
+    const float *w2_scales, int dtype, uint16_t *y_b, void *ws,
+    size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream);
+
+/* The whole layer in the Standard format, FusedMoEModularKernel.forward
+ * without expert_map / apply_router_weight_on_input / shared experts:
+ * route -> count -> align/permute -> [quantise] -> gate/up GEMM + SiLU*mul
+ * -> down GEMM + weight -> ordered reduce, all on `stream`.
+ * x (M, K) bf16; logits (M, E) fp32; bias (E) fp32 or NULL;
+ * dtype GBMOE_BF16: w1/w2 bf16, scales NULL;
+ * dtype GBMOE_FP8_E4M3: w1/w2 e4m3 with their block scales; the activations
+ *   are quantised per token in groups of 128 and H is requantised.
+ * out (M, K) bf16.  topk_ids / topk_weights (M, topk) may be NULL; when given
+ * they receive the router's output.
+ * ws: moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype) bytes.
+ * err_word may be NULL. */
+gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
+                           const float *bias, int M, int K, int N, int E,
+                           int topk, int score_fn, int n_groups,
+                           int topk_groups, int renormalize, int dtype,
+                           const void *w1, const float *w1_scales,
+                           const void *w2, const float *w2_scales,
+                           uint16_t *out, int32_t *topk_ids,
+                           float *topk_weights, void *ws, size_t ws_bytes,
+                           int32_t *err_word, gbmoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBMOE_H */

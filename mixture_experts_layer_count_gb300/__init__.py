@@ -1,0 +1,208 @@
+"""Python binding of libgbmoe.so, the GB300 (sm_103a) fused MoE layer.
+
+Argument marshalling only: every function here has the name of a C entry
+point of ``include/gbmoe.h``, takes torch tensors (device memory) and plain
+ints, passes their pointers and the current CUDA stream through ctypes, and
+raises ``GbmoeError`` when the call returns a non-OK status.  All arithmetic
+runs in the library's CUDA kernels; there is no fallback path: if the
+library cannot be built or loaded, importing this package fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+BF16, FP8_E4M3 = 0, 1
+SOFTMAX, SIGMOID = 0, 1
+WS_ALIGN, WS_BATCHED, WS_FORWARD = 0, 2, 3
+ERR_BAD_EXPERT_ID, ERR_COUNT_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype or device",
+           3: "CUDA launch error"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GbmoeError(RuntimeError):
+    def __init__(self, name, status, cuda_error=0):
+        msg = f"{name}: {_STATUS.get(status, status)}"
+        if status == 3:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+        self.status = status
+
+
+# C signatures: (name, restype, argtypes)
+_P, _I, _Z, _L = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int64
+_SIGS = {
+    "gbmoe_status_string": (ctypes.c_char_p, [_I]),
+    "gbmoe_last_cuda_error": (_I, []),
+    "moe_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_count_expert_tokens": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_align_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
+    "moe_quant_fp8_group": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
+    "moe_permute_rows": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_grouped_gemm_gate_up_silu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
+                                           _I, _P, _P, _P, _P]),
+    "moe_grouped_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
+                                   _I, _P, _P, _P]),
+    "moe_unpermute_weighted_reduce": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "moe_batched_masked_experts": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                        _I, _P, _P, _Z, _P, _P]),
+    "moe_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
+                         _P, _P, _P, _P, _P, _P, _Z, _P, _P]),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libgbmoe.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not _build.up_to_date():
+                _build.build()
+            lib = ctypes.CDLL(_build.LIB)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(name, st):
+    if st != 0:
+        raise GbmoeError(name, st, load().gbmoe_last_cuda_error())
+
+
+def moe_workspace_size(which, M_or_T, E, N, K, topk, dtype) -> int:
+    return int(load().moe_workspace_size(which, M_or_T, E, N, K, topk, dtype))
+
+
+def moe_topk_route(logits, bias, topk, score_fn, n_groups, topk_groups,
+                   renormalize, topk_ids, topk_weights, err_word=None,
+                   stream=None):
+    M, E = logits.shape
+    _check("moe_topk_route", load().moe_topk_route(
+        _ptr(logits), _ptr(bias), M, E, topk, score_fn, n_groups, topk_groups,
+        int(renormalize), _ptr(topk_ids), _ptr(topk_weights), _ptr(err_word),
+        _stream(stream)))
+
+
+def moe_count_expert_tokens(topk_ids, E, counts, err_word=None, stream=None):
+    M, topk = topk_ids.shape
+    _check("moe_count_expert_tokens", load().moe_count_expert_tokens(
+        _ptr(topk_ids), M, topk, E, _ptr(counts), _ptr(err_word), _stream(stream)))
+
+
+def moe_align_permute(topk_ids, E, counts, offsets, sorted_pair_ids, inv, ws,
+                      err_word=None, stream=None):
+    M, topk = topk_ids.shape
+    _check("moe_align_permute", load().moe_align_permute(
+        _ptr(topk_ids), M, topk, E, _ptr(counts), _ptr(offsets),
+        _ptr(sorted_pair_ids), _ptr(inv), _ptr(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _ptr(err_word),
+        _stream(stream)))
+
+
+def moe_quant_fp8_group(x, q, scales, group=128, stream=None):
+    M, K = x.shape
+    _check("moe_quant_fp8_group", load().moe_quant_fp8_group(
+        _ptr(x), M, K, group, _ptr(q), _ptr(scales), _stream(stream)))
+
+
+def moe_quant_fp8_block(w, q, scales, block=128, stream=None):
+    R = w.numel() // w.shape[-1]
+    C = w.shape[-1]
+    _check("moe_quant_fp8_block", load().moe_quant_fp8_block(
+        _ptr(w), R, C, block, _ptr(q), _ptr(scales), _stream(stream)))
+
+
+def moe_permute_rows(x, x_scales, sorted_pair_ids, offsets, topk, E, dtype, A,
+                     A_scales=None, stream=None):
+    M, K = x.shape
+    _check("moe_permute_rows", load().moe_permute_rows(
+        _ptr(x), _ptr(x_scales), _ptr(sorted_pair_ids), _ptr(offsets), M, topk, E,
+        K, dtype, _ptr(A), _ptr(A_scales), _stream(stream)))
+
+
+def moe_grouped_gemm_gate_up_silu(A, A_scales, offsets, M, topk, E, N, K, w1,
+                                  w1_scales, dtype, H, H_scales, err_word=None,
+                                  stream=None):
+    _check("moe_grouped_gemm_gate_up_silu", load().moe_grouped_gemm_gate_up_silu(
+        _ptr(A), _ptr(A_scales), _ptr(offsets), M, topk, E, N, K, _ptr(w1),
+        _ptr(w1_scales), dtype, _ptr(H), _ptr(H_scales), _ptr(err_word),
+        _stream(stream)))
+
+
+def moe_grouped_gemm_down(H, H_scales, sorted_pair_ids, offsets, topk_weights,
+                          M, topk, E, N, K, w2, w2_scales, dtype, y_slot,
+                          err_word=None, stream=None):
+    _check("moe_grouped_gemm_down", load().moe_grouped_gemm_down(
+        _ptr(H), _ptr(H_scales), _ptr(sorted_pair_ids), _ptr(offsets),
+        _ptr(topk_weights), M, topk, E, N, K, _ptr(w2), _ptr(w2_scales), dtype,
+        _ptr(y_slot), _ptr(err_word), _stream(stream)))
+
+
+def moe_unpermute_weighted_reduce(y_slot, inv, M, topk, K, out, stream=None):
+    _check("moe_unpermute_weighted_reduce", load().moe_unpermute_weighted_reduce(
+        _ptr(y_slot), _ptr(inv), M, topk, K, _ptr(out), _stream(stream)))
+
+
+def moe_batched_masked_experts(x_b, expert_num_tokens, N, w1, w2, y_b, ws,
+                               dtype=BF16, x_b_scales=None, w1_scales=None,
+                               w2_scales=None, err_word=None, stream=None):
+    E, T, K = x_b.shape
+    _check("moe_batched_masked_experts", load().moe_batched_masked_experts(
+        _ptr(x_b), _ptr(x_b_scales), _ptr(expert_num_tokens), E, T, N, K,
+        _ptr(w1), _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), dtype, _ptr(y_b),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
+        _stream(stream)))
+
+
+def moe_forward(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
+                renormalize, dtype, w1, w1_scales, w2, w2_scales, out, ws,
+                topk_ids=None, topk_weights=None, err_word=None, stream=None):
+    M, K = x.shape
+    _check("moe_forward", load().moe_forward(
+        _ptr(x), _ptr(logits), _ptr(bias), M, K, N, E, topk, score_fn, n_groups,
+        topk_groups, int(renormalize), dtype, _ptr(w1), _ptr(w1_scales),
+        _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(err_word), _stream(stream)))
+
+
+def workspace(which, M_or_T, E, N, K, topk, dtype, device="cuda"):
+    """A device byte buffer of the size moe_workspace_size asks for."""
+    n = moe_workspace_size(which, M_or_T, E, N, K, topk, dtype)
+    if n == 0:
+        raise GbmoeError("moe_workspace_size", 1)
+    return torch.empty(n, dtype=torch.uint8, device=device)

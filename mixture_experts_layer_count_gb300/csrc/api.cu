@@ -1,0 +1,486 @@
+// api.cu -- the extern "C" entry points declared in gbmoe.h: argument
+// validation, workspace carving and kernel launches.  No device memory is
+// allocated here and the host is never synchronised.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gbmoe.h"
+#include "kernels.h"
+
+namespace gbmoe {
+namespace {
+
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopk = 32;
+constexpr size_t kWsAlign = 256;
+
+thread_local int g_last_cuda_error = 0;
+
+struct DeviceInfo {
+  int checked = 0;  // 0: not yet, 1: supported, -1: not supported
+  int num_sms = 0;
+};
+DeviceInfo g_dev[64];
+std::mutex g_dev_mu;
+
+// The kernels are compiled for sm_103a only.
+gbmoe_status_t device_info(int *num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBMOE_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (d.checked == 0) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    d.checked = (major == 10 && minor == 3 && sms > 0) ? 1 : -1;
+    d.num_sms = sms;
+  }
+  if (d.checked < 0) return GBMOE_UNSUPPORTED;
+  *num_sms = d.num_sms;
+  return GBMOE_OK;
+}
+
+gbmoe_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return GBMOE_OK;
+  g_last_cuda_error = (int)e;
+  return GBMOE_CUDA_ERROR;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v) { return (v + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+// carve consecutive 256-byte aligned pieces out of a workspace
+struct Carver {
+  uint8_t *base;
+  size_t off = 0;
+  explicit Carver(void *b) : base(static_cast<uint8_t *>(b)) {}
+  void *take(size_t bytes) {
+    void *p = base ? base + off : nullptr;
+    off += round_up(bytes);
+    return p;
+  }
+};
+
+size_t elem_bytes(int dtype) { return dtype == GBMOE_FP8_E4M3 ? 1 : 2; }
+
+bool valid_dtype(int dtype) { return dtype == GBMOE_BF16 || dtype == GBMOE_FP8_E4M3; }
+
+struct ForwardWs {
+  int32_t *ids, *counts, *offsets, *sorted, *inv, *chunk_hist;
+  float *weights;
+  uint8_t *xq;
+  float *xs;
+  void *A;
+  float *As;
+  void *H;
+  float *Hs;
+  uint16_t *y_slot;
+};
+ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dtype) {
+  const size_t P = (size_t)M * topk;
+  ForwardWs w;
+  w.ids = static_cast<int32_t *>(c.take(P * 4));
+  w.weights = static_cast<float *>(c.take(P * 4));
+  w.counts = static_cast<int32_t *>(c.take((size_t)E * 4));
+  w.offsets = static_cast<int32_t *>(c.take((size_t)(E + 1) * 4));
+  w.sorted = static_cast<int32_t *>(c.take(P * 4));
+  w.inv = static_cast<int32_t *>(c.take(P * 4));
+  w.chunk_hist = static_cast<int32_t *>(c.take((size_t)align_num_chunks((int)P) * E * 4));
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  w.xq = fp8 ? static_cast<uint8_t *>(c.take((size_t)M * K)) : nullptr;
+  w.xs = fp8 ? static_cast<float *>(c.take((size_t)M * (K / 128) * 4)) : nullptr;
+  w.A = c.take(P * (size_t)K * elem_bytes(dtype));
+  w.As = fp8 ? static_cast<float *>(c.take(P * (size_t)(K / 128) * 4)) : nullptr;
+  w.H = c.take(P * (size_t)N * elem_bytes(dtype));
+  w.Hs = fp8 ? static_cast<float *>(c.take(P * (size_t)(N / 128) * 4)) : nullptr;
+  w.y_slot = static_cast<uint16_t *>(c.take(P * (size_t)K * 2));
+  return w;
+}
+
+bool route_args_ok(int M, int E, int topk, int score_fn, const float *bias,
+                   int n_groups, int topk_groups) {
+  if (M < 0 || E < 1 || E > kMaxExperts || topk < 1 || topk > kMaxTopk || topk > E)
+    return false;
+  if (score_fn == GBMOE_SOFTMAX) return bias == nullptr;
+  if (score_fn != GBMOE_SIGMOID) return false;
+  if (n_groups > 1) {
+    if (n_groups > 32 || E % n_groups != 0) return false;
+    if (topk_groups < 1 || topk_groups > n_groups) return false;
+    if (topk > topk_groups * (E / n_groups)) return false;
+  }
+  return true;
+}
+
+gbmoe_status_t gate_up_impl(const void *A, const float *A_scales,
+                            const int32_t *offsets, int M, int topk, int E,
+                            int N, int K, const void *w1, const float *w1_scales,
+                            int dtype, void *H, float *H_scales, int32_t *err,
+                            int num_sms, cudaStream_t s) {
+  GroupedGemmArgs a{};
+  a.mode = kGateUp;
+  a.fp8 = dtype == GBMOE_FP8_E4M3;
+  a.offsets = offsets;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.A = A;
+  a.a_rows = (int64_t)M * topk;
+  a.A_scales = A_scales;
+  a.B = w1;
+  a.B_scales = w1_scales;
+  a.out = H;
+  a.out_scales = H_scales;
+  a.err = err;
+  return from_cuda(launch_grouped_gemm(a, num_sms, s));
+}
+
+gbmoe_status_t permute_impl(const void *x, const float *x_scales,
+                            const int32_t *sorted, const int32_t *offsets, int M,
+                            int topk, int E, int K, int dtype, void *A,
+                            float *A_scales, int num_sms, cudaStream_t s) {
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  return from_cuda(launch_gather_rows(x, fp8 ? x_scales : nullptr,
+                                      (int)(K * elem_bytes(dtype)), K / 128, sorted,
+                                      offsets + E, M * topk, topk, A,
+                                      fp8 ? A_scales : nullptr, num_sms, s));
+}
+
+gbmoe_status_t down_impl(const void *H, const float *H_scales,
+                         const int32_t *sorted, const int32_t *offsets,
+                         const float *topk_weights, int M, int topk, int E,
+                         int N, int K, const void *w2, const float *w2_scales,
+                         int dtype, uint16_t *y_slot, int32_t *err, int num_sms,
+                         cudaStream_t s) {
+  GroupedGemmArgs a{};
+  a.mode = kDown;
+  a.fp8 = dtype == GBMOE_FP8_E4M3;
+  a.offsets = offsets;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.A = H;
+  a.a_rows = (int64_t)M * topk;
+  a.A_scales = H_scales;
+  a.B = w2;
+  a.B_scales = w2_scales;
+  a.out = y_slot;
+  a.sorted_pair_ids = sorted;
+  a.topk_weights = topk_weights;
+  a.err = err;
+  return from_cuda(launch_grouped_gemm(a, num_sms, s));
+}
+
+bool gemm_shape_ok(int M, int topk, int E, int N, int K, int dtype) {
+  return M >= 0 && topk >= 1 && topk <= kMaxTopk && E >= 1 && E <= kMaxExperts &&
+         N >= 128 && K >= 128 && N % 128 == 0 && K % 128 == 0 && valid_dtype(dtype) &&
+         (size_t)M * topk <= (size_t)INT32_MAX && (size_t)E * 2 * N <= (size_t)INT32_MAX &&
+         (size_t)E * K <= (size_t)INT32_MAX;
+}
+
+}  // namespace
+}  // namespace gbmoe
+
+using namespace gbmoe;
+
+extern "C" {
+
+const char *gbmoe_status_string(gbmoe_status_t status) {
+  switch (status) {
+    case GBMOE_OK: return "ok";
+    case GBMOE_INVALID_ARG: return "invalid argument";
+    case GBMOE_UNSUPPORTED: return "unsupported dtype or device";
+    case GBMOE_CUDA_ERROR: return "CUDA launch error";
+  }
+  return "unknown status";
+}
+
+int gbmoe_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t moe_workspace_size(int which, int M_or_T, int E, int N, int K, int topk,
+                          int dtype) {
+  if (M_or_T < 0 || E < 1 || E > kMaxExperts) return 0;
+  Carver c(nullptr);
+  switch (which) {
+    case GBMOE_WS_ALIGN: {
+      if (topk < 1) return 0;
+      const size_t P = (size_t)M_or_T * topk;
+      c.take((size_t)align_num_chunks((int)P) * E * 4);
+      return c.off > 0 ? c.off : kWsAlign;
+    }
+    case GBMOE_WS_BATCHED:
+      if (!gemm_shape_ok(M_or_T, 1, E, N, K, dtype) || dtype != GBMOE_BF16) return 0;
+      c.take((size_t)E * M_or_T * N * 2);
+      return c.off > 0 ? c.off : kWsAlign;
+    case GBMOE_WS_FORWARD:
+      if (!gemm_shape_ok(M_or_T, topk, E, N, K, dtype)) return 0;
+      carve_forward(c, M_or_T, E, N, K, topk, dtype);
+      return c.off;
+  }
+  return 0;
+}
+
+gbmoe_status_t moe_topk_route(const float *logits, const float *bias, int M,
+                              int E, int topk, int score_fn, int n_groups,
+                              int topk_groups, int renormalize,
+                              int32_t *topk_ids, float *topk_weights,
+                              int32_t *err_word, gbmoe_stream_t stream) {
+  (void)err_word;
+  if (!route_args_ok(M, E, topk, score_fn, bias, n_groups, topk_groups))
+    return GBMOE_INVALID_ARG;
+  if (M > 0 && (!logits || !topk_ids || !topk_weights)) return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  if (M == 0) return GBMOE_OK;
+  return from_cuda(launch_route(logits, bias, M, E, topk, score_fn,
+                                n_groups < 1 ? 1 : n_groups, topk_groups,
+                                renormalize, topk_ids, topk_weights,
+                                (cudaStream_t)stream));
+}
+
+gbmoe_status_t moe_count_expert_tokens(const int32_t *topk_ids, int M,
+                                       int topk, int E, int32_t *counts,
+                                       int32_t *err_word,
+                                       gbmoe_stream_t stream) {
+  if (M < 0 || topk < 1 || E < 1 || E > kMaxExperts || !counts) return GBMOE_INVALID_ARG;
+  if (M > 0 && !topk_ids) return GBMOE_INVALID_ARG;
+  if ((size_t)M * topk > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  if (M == 0)
+    return from_cuda(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, (cudaStream_t)stream));
+  return from_cuda(launch_count(topk_ids, M * topk, E, counts, err_word, sms,
+                                (cudaStream_t)stream));
+}
+
+gbmoe_status_t moe_align_permute(const int32_t *topk_ids, int M, int topk,
+                                 int E, int32_t *counts, int32_t *offsets,
+                                 int32_t *sorted_pair_ids, int32_t *inv,
+                                 void *ws, size_t ws_bytes, int32_t *err_word,
+                                 gbmoe_stream_t stream) {
+  if (M < 0 || topk < 1 || E < 1 || E > kMaxExperts || !offsets) return GBMOE_INVALID_ARG;
+  if ((size_t)M * topk > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
+  if (M > 0 && (!topk_ids || !sorted_pair_ids || !inv || !ws)) return GBMOE_INVALID_ARG;
+  if (ws_bytes < moe_workspace_size(GBMOE_WS_ALIGN, M, E, 0, 0, topk, 0)) return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  return from_cuda(launch_align(topk_ids, M * topk, E, counts, offsets,
+                                sorted_pair_ids, inv, static_cast<int32_t *>(ws),
+                                err_word, (cudaStream_t)stream));
+}
+
+gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, int M, int K, int group,
+                                   uint8_t *q, float *scales,
+                                   gbmoe_stream_t stream) {
+  if (M < 0 || K < 128 || K % 128 != 0 || group != 128) return GBMOE_INVALID_ARG;
+  if (M > 0 && (!x || !q || !scales || !aligned16(x) || !aligned16(q)))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  if (M == 0) return GBMOE_OK;
+  return from_cuda(launch_quant_group(x, M, K, q, scales, (cudaStream_t)stream));
+}
+
+gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
+                                   int block, uint8_t *q, float *scales,
+                                   gbmoe_stream_t stream) {
+  if (R < 0 || C < 128 || R % 128 != 0 || C % 128 != 0 || block != 128)
+    return GBMOE_INVALID_ARG;
+  if ((R / 128) * (C / 128) > (int64_t)INT32_MAX) return GBMOE_INVALID_ARG;
+  if (R > 0 && (!w || !q || !scales || !aligned16(w) || !aligned16(q)))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  if (R == 0) return GBMOE_OK;
+  return from_cuda(launch_quant_block(w, R, C, q, scales, (cudaStream_t)stream));
+}
+
+gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
+                                const int32_t *sorted_pair_ids,
+                                const int32_t *offsets, int M, int topk, int E,
+                                int K, int dtype, void *A, float *A_scales,
+                                gbmoe_stream_t stream) {
+  if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
+  if (M < 0 || topk < 1 || topk > kMaxTopk || E < 1 || E > kMaxExperts || K < 128 ||
+      K % 128 != 0 || (size_t)M * topk > (size_t)INT32_MAX)
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK || M == 0) return st;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  if (!x || !sorted_pair_ids || !offsets || !A || !aligned16(x) || !aligned16(A))
+    return GBMOE_INVALID_ARG;
+  if (fp8 && (!x_scales || !A_scales)) return GBMOE_INVALID_ARG;
+  return permute_impl(x, x_scales, sorted_pair_ids, offsets, M, topk, E, K, dtype, A,
+                      A_scales, sms, (cudaStream_t)stream);
+}
+
+gbmoe_status_t moe_grouped_gemm_gate_up_silu(
+    const void *A, const float *A_scales, const int32_t *offsets, int M,
+    int topk, int E, int N, int K, const void *w1, const float *w1_scales,
+    int dtype, void *H, float *H_scales, int32_t *err_word,
+    gbmoe_stream_t stream) {
+  if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
+  if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK || M == 0) return st;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  if (!A || !offsets || !w1 || !H) return GBMOE_INVALID_ARG;
+  if (fp8 && (!A_scales || !w1_scales || !H_scales)) return GBMOE_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(w1) || !aligned16(H)) return GBMOE_INVALID_ARG;
+  return gate_up_impl(A, A_scales, offsets, M, topk, E, N, K, w1, w1_scales, dtype, H,
+                      H_scales, err_word, sms, (cudaStream_t)stream);
+}
+
+gbmoe_status_t moe_grouped_gemm_down(
+    const void *H, const float *H_scales, const int32_t *sorted_pair_ids,
+    const int32_t *offsets, const float *topk_weights, int M, int topk, int E,
+    int N, int K, const void *w2, const float *w2_scales, int dtype,
+    uint16_t *y_slot, int32_t *err_word, gbmoe_stream_t stream) {
+  if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
+  if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
+  if (M == 0) {
+    int sms;
+    return device_info(&sms);
+  }
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  if (!H || !sorted_pair_ids || !offsets || !topk_weights || !w2 || !y_slot)
+    return GBMOE_INVALID_ARG;
+  if (fp8 && (!H_scales || !w2_scales)) return GBMOE_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(w2) || !aligned16(y_slot)) return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  return down_impl(H, H_scales, sorted_pair_ids, offsets, topk_weights, M, topk, E, N,
+                   K, w2, w2_scales, dtype, y_slot, err_word, sms,
+                   (cudaStream_t)stream);
+}
+
+gbmoe_status_t moe_unpermute_weighted_reduce(const uint16_t *y_slot,
+                                             const int32_t *inv, int M,
+                                             int topk, int K, uint16_t *out,
+                                             gbmoe_stream_t stream) {
+  if (M < 0 || topk < 1 || topk > kMaxTopk || K < 8 || K % 8 != 0) return GBMOE_INVALID_ARG;
+  if (M > 0 && (!y_slot || !out || !aligned16(y_slot) || !aligned16(out)))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  if (M == 0) return GBMOE_OK;
+  return from_cuda(launch_reduce(y_slot, inv, M, topk, K, out, sms, (cudaStream_t)stream));
+}
+
+gbmoe_status_t moe_batched_masked_experts(
+    const void *x_b, const float *x_b_scales,
+    const int32_t *expert_num_tokens, int E, int T, int N, int K,
+    const void *w1, const float *w1_scales, const void *w2,
+    const float *w2_scales, int dtype, uint16_t *y_b, void *ws,
+    size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream) {
+  (void)x_b_scales;
+  (void)w1_scales;
+  (void)w2_scales;
+  if (dtype != GBMOE_BF16) return GBMOE_UNSUPPORTED;
+  if (!gemm_shape_ok(T, 1, E, N, K, dtype)) return GBMOE_INVALID_ARG;
+  if ((size_t)E * T > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
+  if (T == 0) {
+    int sms;
+    return device_info(&sms);
+  }
+  if (!x_b || !expert_num_tokens || !w1 || !w2 || !y_b || !ws) return GBMOE_INVALID_ARG;
+  if (!aligned16(x_b) || !aligned16(w1) || !aligned16(w2) || !aligned16(y_b) || !aligned16(ws))
+    return GBMOE_INVALID_ARG;
+  if (ws_bytes < moe_workspace_size(GBMOE_WS_BATCHED, T, E, N, K, 1, dtype))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  void *Hb = ws;
+  GroupedGemmArgs a{};
+  a.mode = kGateUp;
+  a.counts = expert_num_tokens;
+  a.E = E;
+  a.T = T;
+  a.N = N;
+  a.K = K;
+  a.A = x_b;
+  a.a_rows = (int64_t)E * T;
+  a.B = w1;
+  a.out = Hb;
+  a.err = err_word;
+  cudaError_t ce = launch_grouped_gemm(a, sms, s);
+  if (ce != cudaSuccess) return from_cuda(ce);
+  a.mode = kDown;
+  a.A = Hb;
+  a.B = w2;
+  a.out = y_b;
+  return from_cuda(launch_grouped_gemm(a, sms, s));
+}
+
+gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
+                           const float *bias, int M, int K, int N, int E,
+                           int topk, int score_fn, int n_groups,
+                           int topk_groups, int renormalize, int dtype,
+                           const void *w1, const float *w1_scales,
+                           const void *w2, const float *w2_scales,
+                           uint16_t *out, int32_t *topk_ids,
+                           float *topk_weights, void *ws, size_t ws_bytes,
+                           int32_t *err_word, gbmoe_stream_t stream) {
+  if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
+  if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
+  if (!route_args_ok(M, E, topk, score_fn, bias, n_groups, topk_groups))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  if (M == 0) return GBMOE_OK;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  if (!x || !logits || !w1 || !w2 || !out || !ws) return GBMOE_INVALID_ARG;
+  if (fp8 && (!w1_scales || !w2_scales)) return GBMOE_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(ws))
+    return GBMOE_INVALID_ARG;
+  if (ws_bytes < moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype))
+    return GBMOE_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  Carver c(ws);
+  ForwardWs w = carve_forward(c, M, E, N, K, topk, dtype);
+  int32_t *ids = topk_ids ? topk_ids : w.ids;
+  float *wts = topk_weights ? topk_weights : w.weights;
+  const int P = M * topk;
+  cudaError_t ce = launch_route(logits, bias, M, E, topk, score_fn,
+                                n_groups < 1 ? 1 : n_groups, topk_groups, renormalize,
+                                ids, wts, s);
+  if (ce != cudaSuccess) return from_cuda(ce);
+  ce = launch_align(ids, P, E, w.counts, w.offsets, w.sorted, w.inv, w.chunk_hist,
+                    err_word, s);
+  if (ce != cudaSuccess) return from_cuda(ce);
+  const void *a_src = x;
+  const float *a_src_s = nullptr;
+  if (fp8) {
+    ce = launch_quant_group(x, M, K, w.xq, w.xs, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+    a_src = w.xq;
+    a_src_s = w.xs;
+  }
+  st = permute_impl(a_src, a_src_s, w.sorted, w.offsets, M, topk, E, K, dtype, w.A, w.As,
+                    sms, s);
+  if (st != GBMOE_OK) return st;
+  st = gate_up_impl(w.A, w.As, w.offsets, M, topk, E, N, K, w1, w1_scales, dtype, w.H,
+                    w.Hs, err_word, sms, s);
+  if (st != GBMOE_OK) return st;
+  st = down_impl(w.H, w.Hs, w.sorted, w.offsets, wts, M, topk, E, N, K, w2, w2_scales,
+                 dtype, w.y_slot, err_word, sms, s);
+  if (st != GBMOE_OK) return st;
+  return from_cuda(launch_reduce(w.y_slot, w.inv, M, topk, K, out, sms, s));
+}
+
+}  // extern "C"

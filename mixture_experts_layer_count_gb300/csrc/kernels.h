@@ -1,0 +1,73 @@
+// kernels.h -- host-side launchers of the library's kernels (internal).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gbmoe {
+
+// route.cu
+cudaError_t launch_route(const float *logits, const float *bias, int M, int E,
+                         int topk, int score_fn, int n_groups, int topk_groups,
+                         int renorm, int32_t *ids, float *weights,
+                         cudaStream_t s);
+
+// permute.cu
+cudaError_t launch_count(const int32_t *ids, int P, int E, int32_t *counts,
+                         int32_t *err, int num_sms, cudaStream_t s);
+int align_num_chunks(int P);
+cudaError_t launch_align(const int32_t *ids, int P, int E, int32_t *counts,
+                         int32_t *offsets, int32_t *sorted, int32_t *inv,
+                         int32_t *chunk_hist, int32_t *err, cudaStream_t s);
+cudaError_t launch_gather_rows(const void *x, const float *xs, int row_bytes,
+                               int n_scales, const int32_t *sorted,
+                               const int32_t *total, int P, int topk,
+                               void *out, float *out_s, int num_sms,
+                               cudaStream_t s);
+cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
+                          int topk, int K, uint16_t *out, int num_sms,
+                          cudaStream_t s);
+
+// quant.cu
+cudaError_t launch_quant_group(const uint16_t *x, int M, int K, uint8_t *q,
+                               float *scales, cudaStream_t s);
+cudaError_t launch_quant_block(const uint16_t *w, int64_t R, int C, uint8_t *q,
+                               float *scales, cudaStream_t s);
+
+// gemm.cu -- grouped GEMMs on tcgen05 / TMEM fed by TMA
+enum GemmMode { kGateUp = 0, kDown = 1 };
+
+struct GroupedGemmArgs {
+  int mode;                  // kGateUp or kDown
+  int fp8;                   // 0: bf16 operands, 1: e4m3 with fp32 block scales
+  // row groups: Standard (offsets != nullptr): expert e owns rows
+  // [offsets[e], offsets[e+1]) of A.  Batched: rows [e*T, e*T + min(counts[e], T)).
+  const int32_t *offsets;
+  const int32_t *counts;
+  int E, T;
+  int N, K;                  // problem sizes (w1 (E, 2N, K), w2 (E, K, N))
+  // operands
+  const void *A;             // (rows, Kd) bf16 or e4m3, Kd = K (gate-up) or N (down)
+  int64_t a_rows;            // rows of A's allocation
+  const float *A_scales;     // fp8: (a_rows, Kd/128)
+  const void *B;             // w1 or w2
+  const float *B_scales;     // fp8: w1 (E, 2N/128, K/128) / w2 (E, K/128, N/128)
+  // outputs
+  void *out;                 // gate-up: H (a_rows, N); down: y rows of K bf16
+  float *out_scales;         // fp8 gate-up: H scales (a_rows, N/128)
+  const int32_t *sorted_pair_ids;  // down, Standard: output row = pair id
+  const float *topk_weights;       // down, Standard: row scale
+  int32_t *err;
+};
+
+cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,
+                                cudaStream_t s);
+
+// driver entry point for tensor-map encoding (resolved once)
+bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes,
+                    uint64_t cols, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows);
+
+}  // namespace gbmoe

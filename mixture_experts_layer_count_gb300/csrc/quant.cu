@@ -1,0 +1,131 @@
+// quant.cu -- [Quantize-Prepare] FP8 e4m3 quantisation.
+//
+// FusedMoEPrepareAndFinalize.prepare in
+// "vllm/model_executor/layers/fused_moe/modular_kernel.py" quantises the
+// activations before the experts run (per_act_token_quant / block_shape of the
+// quant config).  Rule for one group (128 consecutive values of a token, or a
+// 128 x 128 tile of a weight matrix):
+//     s = max(amax, 1e-12) / 448       (fp32, IEEE division)
+//     q = e4m3(x / s)                  (IEEE division, round to nearest even,
+//                                       saturating at +-448)
+// HBM-bound: each kernel reads its input once and writes q and s once.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbmoe {
+
+namespace {
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ uint32_t e4m3_of(float v) {
+  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float group_scale(float amax) {
+  return __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
+}
+
+// one warp per (token, 128-group): 4 values per lane
+__global__ void __launch_bounds__(256)
+    quant_group_kernel(const uint2 *__restrict__ x, int M, int K,
+                       uint32_t *__restrict__ q, float *__restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int G = K / 128;
+  const size_t n = (size_t)M * G;
+  for (size_t w = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; w < n;
+       w += ((size_t)gridDim.x * blockDim.x) >> 5) {
+    const size_t t = w / G, g = w % G;
+    const size_t base = t * K + g * 128 + lane * 4;  // element index
+    uint2 raw = x[base / 4];
+    float f[4] = {bf16_bits_to_float(raw.x & 0xffffu), bf16_bits_to_float(raw.x >> 16),
+                  bf16_bits_to_float(raw.y & 0xffffu), bf16_bits_to_float(raw.y >> 16)};
+    float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = group_scale(amax);
+    uint32_t packed = e4m3_of(__fdiv_rn(f[0], s)) | (e4m3_of(__fdiv_rn(f[1], s)) << 8) |
+                      (e4m3_of(__fdiv_rn(f[2], s)) << 16) |
+                      (e4m3_of(__fdiv_rn(f[3], s)) << 24);
+    q[base / 4] = packed;
+    if (lane == 0) scales[t * G + g] = s;
+  }
+}
+
+// one block of 256 threads per 128 x 128 tile; thread i reads rows
+// (i / 16) + 16 r, r < 8, columns (i % 16) * 8 .. + 8
+__global__ void __launch_bounds__(256)
+    quant_block_kernel(const uint4 *__restrict__ w, int64_t R, int C,
+                       uint2 *__restrict__ q, float *__restrict__ scales) {
+  __shared__ float red[8];
+  const int BC = C / 128;
+  const int64_t tile = blockIdx.x;
+  const int64_t br = tile / BC;
+  const int bc = (int)(tile % BC);
+  const int tid = threadIdx.x;
+  const int cvec = C / 8;  // 16-byte vectors per row
+  float f[8][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int64_t row = br * 128 + tid / 16 + 16 * r;
+    uint4 v = w[row * cvec + bc * 16 + (tid % 16)];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[r][2 * i] = bf16_bits_to_float(u[i] & 0xffffu);
+      f[r][2 * i + 1] = bf16_bits_to_float(u[i] >> 16);
+      amax = fmaxf(amax, fmaxf(fabsf(f[r][2 * i]), fabsf(f[r][2 * i + 1])));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const float s = group_scale(amax);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int64_t row = br * 128 + tid / 16 + 16 * r;
+    uint2 o;
+    o.x = e4m3_of(__fdiv_rn(f[r][0], s)) | (e4m3_of(__fdiv_rn(f[r][1], s)) << 8) |
+          (e4m3_of(__fdiv_rn(f[r][2], s)) << 16) | (e4m3_of(__fdiv_rn(f[r][3], s)) << 24);
+    o.y = e4m3_of(__fdiv_rn(f[r][4], s)) | (e4m3_of(__fdiv_rn(f[r][5], s)) << 8) |
+          (e4m3_of(__fdiv_rn(f[r][6], s)) << 16) | (e4m3_of(__fdiv_rn(f[r][7], s)) << 24);
+    q[row * cvec + bc * 16 + (tid % 16)] = o;
+  }
+  if (tid == 0) scales[br * BC + bc] = s;
+}
+
+}  // namespace
+
+cudaError_t launch_quant_group(const uint16_t *x, int M, int K, uint8_t *q,
+                               float *scales, cudaStream_t s) {
+  const size_t warps = (size_t)M * (K / 128);
+  size_t blocks = (warps + 7) / 8;
+  if (blocks > 65535u * 16u) blocks = 65535u * 16u;
+  quant_group_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+      reinterpret_cast<const uint2 *>(x), M, K, reinterpret_cast<uint32_t *>(q),
+      scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_block(const uint16_t *w, int64_t R, int C, uint8_t *q,
+                               float *scales, cudaStream_t s) {
+  const int64_t tiles = (R / 128) * (C / 128);
+  quant_block_kernel<<<(unsigned)tiles, 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(w), R, C, reinterpret_cast<uint2 *>(q),
+      scales);
+  return cudaGetLastError();
+}
+
+}  // namespace gbmoe

@@ -1,0 +1,145 @@
+"""BatchedExperts (E, T, K) masked by device-resident counts: parity with the
+oracle, padded rows never read or written, capture in a CUDA graph and
+replay with fresh inputs and counts (no host count read)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads as WL
+from gpu_common import TOL, assert_close_rel, gbmoe, oracle_weights
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+SENTINEL = 0x7E7E  # a bf16 bit pattern no expert output takes by accident
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gbmoe()
+
+
+def _run(cfg, xb, counts, w1, w2, yb, ws, err, stream=None):
+    gbmoe().moe_batched_masked_experts(xb, counts, cfg.N, w1, w2, yb, ws,
+                                       err_word=err, stream=stream)
+
+
+def _fresh(cfg):
+    E, T, K = cfg.E, cfg.M, cfg.K
+    yb = torch.empty((E, T, K), dtype=torch.bfloat16, device=DEV)
+    yb.view(torch.int16).fill_(SENTINEL)
+    return yb
+
+
+def _check_rows(cfg, d, yb, W, rows=None):
+    counts = d["counts"].cpu().numpy()
+    ref, n = orc.batched_experts(WL.bf16_bits(d["x_b"]), counts, W, rows=rows)
+    got = yb.float().cpu().numpy()
+    mask = ~np.isnan(ref[..., 0])
+    assert mask.sum() == n
+    assert_close_rel(got[mask], ref[mask], TOL[WL.BF16], cfg.name)
+    bits = yb.view(torch.int16).cpu().numpy()
+    for e in range(cfg.E):
+        c = min(max(int(counts[e]), 0), cfg.M)
+        assert np.all(bits[e, c:] == np.int16(SENTINEL)), f"padded rows of expert {e} written"
+
+
+def test_batched_small_all_rows():
+    cfg = WL.SMALL_BATCHED
+    d = WL.make_inputs(cfg, DEV)
+    g = gbmoe()
+    yb = _fresh(cfg)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = g.workspace(g.WS_BATCHED, cfg.M, cfg.E, cfg.N, cfg.K, 1, WL.BF16)
+    _run(cfg, d["x_b"], d["counts"], d["w1"], d["w2"], yb, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    _check_rows(cfg, d, yb, oracle_weights(cfg, d["w1"], d["w2"]))
+
+
+def test_batched_padding_garbage_does_not_matter():
+    cfg = WL.SMALL_BATCHED
+    d = WL.make_inputs(cfg, DEV)
+    g = gbmoe()
+    ws = g.workspace(g.WS_BATCHED, cfg.M, cfg.E, cfg.N, cfg.K, 1, WL.BF16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    a = _fresh(cfg)
+    _run(cfg, d["x_b"], d["counts"], d["w1"], d["w2"], a, ws, err)
+    xb2 = d["x_b"].clone()
+    gen = torch.Generator(device=DEV).manual_seed(99)
+    for e in range(cfg.E):
+        c = int(d["counts"][e])
+        xb2[e, c:] = (torch.randn((cfg.M - c, cfg.K), generator=gen, device=DEV) * 1e4).to(torch.bfloat16)
+    b = _fresh(cfg)
+    _run(cfg, xb2, d["counts"], d["w1"], d["w2"], b, ws, err)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_batched_count_out_of_range_is_clamped_and_flagged():
+    cfg = WL.SMALL_BATCHED
+    d = WL.make_inputs(cfg, DEV)
+    g = gbmoe()
+    counts = d["counts"].clone()
+    counts[0] = cfg.M + 50
+    counts[1] = -3
+    ws = g.workspace(g.WS_BATCHED, cfg.M, cfg.E, cfg.N, cfg.K, 1, WL.BF16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    yb = _fresh(cfg)
+    _run(cfg, d["x_b"], counts, d["w1"], d["w2"], yb, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() & g.ERR_COUNT_RANGE
+    d2 = dict(d)
+    d2["counts"] = counts
+    _check_rows(cfg, d2, yb, oracle_weights(cfg, d["w1"], d["w2"]))
+
+
+def test_batched_full_size_graph_replays():
+    """E=32, T=1024, K=7168, N=2048: captured once, replayed with fresh seeds
+    copied into the static buffers; each replay equals the eager call bit for
+    bit and matches the oracle on sampled rows; padded rows stay untouched."""
+    cfg = WL.BATCHED_MASKED
+    g = gbmoe()
+    d0 = WL.make_inputs(cfg, DEV, seed=cfg.seed)
+    w1, w2 = d0["w1"], d0["w2"]
+    xb = d0["x_b"].clone()
+    counts = d0["counts"].clone()
+    yb = _fresh(cfg)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = g.workspace(g.WS_BATCHED, cfg.M, cfg.E, cfg.N, cfg.K, 1, WL.BF16)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _run(cfg, xb, counts, w1, w2, yb, ws, err, stream=s)  # warm up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        _run(cfg, xb, counts, w1, w2, yb, ws, err)
+    W = None
+    rng = np.random.default_rng(7)
+    for r in range(4):
+        dr = WL.make_inputs(cfg, DEV, seed=cfg.seed + r + 1, with_weights=False)
+        xb.copy_(dr["x_b"])
+        counts.copy_(dr["counts"])
+        yb.view(torch.int16).fill_(SENTINEL)
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = _fresh(cfg)
+        _run(cfg, dr["x_b"], dr["counts"], w1, w2, eager, ws, err)
+        torch.cuda.synchronize()
+        assert torch.equal(eager.view(torch.int16), yb.view(torch.int16)), f"replay {r}"
+        assert err.item() == 0
+        if r < 2:
+            c = dr["counts"].cpu().numpy()
+            rows = [(e, int(rr)) for e in range(cfg.E) if c[e] > 0
+                    for rr in rng.choice(c[e], min(2, c[e]), replace=False)]
+            rows = np.array(rows, np.int32)[rng.choice(len(rows), min(24, len(rows)), replace=False)]
+            if W is None:
+                W = oracle_weights(cfg, w1, w2, np.unique(rows[:, 0]))
+            else:
+                W = oracle_weights(cfg, w1, w2, np.unique(rows[:, 0]))
+            dd = {"x_b": dr["x_b"], "counts": dr["counts"]}
+            _check_rows(cfg, dd, yb, W, rows=rows)

@@ -1,0 +1,323 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on the same
+seeded inputs: indices bit-exact, values within the tolerance of the layer's
+precision (max|d| <= 2e-2 max|ref| for bf16, 5e-2 for FP8)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads as WL
+from gpu_common import (TOL, GpuWeights, assert_close_rel, check_ids, gbmoe,
+                        oracle_forward, oracle_weights, run_forward)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gbmoe()
+
+
+# ------------------------------------------------------------------ router --
+
+ROUTE_CFGS = [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.MIXTRAL_PREFILL,
+              WL.DSV3_PREFILL_FP8, WL.DSV3_DECODE]
+
+
+@pytest.mark.parametrize("cfg", ROUTE_CFGS, ids=lambda c: c.name)
+def test_route_parity(cfg):
+    g = gbmoe()
+    d = WL.make_inputs(cfg, DEV, with_weights=False)
+    ids = torch.empty((cfg.M, cfg.topk), dtype=torch.int32, device=DEV)
+    w = torch.empty((cfg.M, cfg.topk), dtype=torch.float32, device=DEV)
+    g.moe_topk_route(d["logits"], d["bias"], cfg.topk, cfg.score_fn, cfg.n_groups,
+                     cfg.topk_groups, cfg.renorm, ids, w)
+    torch.cuda.synchronize()
+    rid, rw, margin = orc.route(d["logits"].cpu().numpy(),
+                                None if d["bias"] is None else d["bias"].cpu().numpy(),
+                                cfg.topk, cfg.score_fn, cfg.n_groups, cfg.topk_groups,
+                                cfg.renorm)
+    gid = ids.cpu().numpy()
+    diff = check_ids(gid, rid, margin, cfg.name)
+    same = np.setdiff1d(np.arange(cfg.M), diff)
+    np.testing.assert_allclose(w.cpu().numpy()[same], rw[same], atol=2e-6, rtol=0)
+
+
+def test_route_unrenormalised_and_ungrouped():
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(31)
+    for E, k, fn in ((8, 2, orc.SOFTMAX), (256, 8, orc.SIGMOID), (512, 32, orc.SOFTMAX),
+                     (40, 3, orc.SIGMOID)):
+        lg = torch.randn((257, E), generator=gen, device=DEV)
+        lg[:16] = lg[:16].round()  # exact ties
+        ids = torch.empty((257, k), dtype=torch.int32, device=DEV)
+        w = torch.empty((257, k), dtype=torch.float32, device=DEV)
+        g.moe_topk_route(lg, None, k, fn, 1, 1, False, ids, w)
+        rid, rw, _ = orc.route(lg.cpu().numpy(), None, k, fn, 1, 1, False)
+        assert np.array_equal(ids.cpu().numpy(), rid)
+        np.testing.assert_allclose(w.cpu().numpy(), rw, atol=2e-6, rtol=0)
+
+
+# -------------------------------------------------------- count / permute --
+
+@pytest.mark.parametrize("E,M,k,skew", [(8, 64, 2, 0.0), (256, 8192, 8, 1.1),
+                                        (32, 1, 1, 0.0), (512, 3001, 5, 2.0)])
+def test_count_and_align_bit_exact(E, M, k, skew):
+    g = gbmoe()
+    rng = np.random.default_rng(E * 7 + M)
+    p = np.arange(1, E + 1, dtype=np.float64) ** -skew
+    ids_np = rng.choice(E, size=(M, k), p=p / p.sum()).astype(np.int32)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    counts = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    counts2 = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    srt = torch.full((M * k,), -5, dtype=torch.int32, device=DEV)
+    inv = torch.empty(M * k, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = g.workspace(g.WS_ALIGN, M, E, 0, 0, k, 0)
+    g.moe_count_expert_tokens(ids, E, counts, err)
+    g.moe_align_permute(ids, E, counts2, offsets, srt, inv, ws, err)
+    rc, bad = orc.count(ids_np, E)
+    ro, rs, ri = orc.align(ids_np, E)
+    assert bad == 0 and err.item() == 0
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(counts2.cpu().numpy(), rc)
+    assert counts.sum().item() == M * k  # every pair lands in one expert
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(srt.cpu().numpy(), rs)
+    assert np.array_equal(inv.cpu().numpy(), ri)
+
+
+def test_align_skips_bad_ids_and_flags_them():
+    g = gbmoe()
+    E = 6
+    ids_np = np.array([[0, 5], [6, 1], [-1, 2], [5, 5]], np.int32)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    srt = torch.full((8,), -5, dtype=torch.int32, device=DEV)
+    inv = torch.empty(8, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    g.moe_align_permute(ids, E, counts, offsets, srt, inv, g.workspace(g.WS_ALIGN, 4, E, 0, 0, 2, 0), err)
+    ro, rs, ri = orc.align(ids_np, E)
+    assert err.item() & g.ERR_BAD_EXPERT_ID
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(srt.cpu().numpy()[: ro[E]], rs)
+    assert np.array_equal(inv.cpu().numpy(), ri)
+    assert list(srt.cpu().numpy()[ro[E]:]) == [-5] * (8 - ro[E])
+
+
+# ------------------------------------------------------------------ quant --
+
+def test_quant_fp8_group_bit_exact():
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(41)
+    M, K = 333, 1024
+    x = (torch.randn((M, K), generator=gen, device=DEV) *
+         torch.logspace(-4, 3, K, device=DEV)).to(torch.bfloat16)
+    x[5, :128] = 0
+    x[6, 128:256] = -0.0
+    x[7, :] = x[7, :].abs() * -1
+    q = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    s = torch.empty((M, K // 128), dtype=torch.float32, device=DEV)
+    g.moe_quant_fp8_group(x, q, s)
+    rq, rs = orc.quant_fp8_group(WL.bf16_bits(x))
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_quant_fp8_block_bit_exact():
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(42)
+    w = (torch.randn((3, 256, 384), generator=gen, device=DEV) * 0.03).to(torch.bfloat16)
+    q = torch.empty(w.shape, dtype=torch.uint8, device=DEV)
+    s = torch.empty((3, 2, 3), dtype=torch.float32, device=DEV)
+    g.moe_quant_fp8_block(w, q, s)
+    for e in range(3):
+        rq, rs = orc.quant_fp8_block(WL.bf16_bits(w[e]))
+        assert np.array_equal(s[e].cpu().numpy(), rs)
+        assert np.array_equal(q[e].cpu().numpy(), rq)
+
+
+# ------------------------------------------------------- expert GEMMs ------
+
+def _stage_inputs(cfg):
+    """Route with the oracle (inputs for the GEMM stages never come from the
+    CUDA path), then permute on the GPU."""
+    g = gbmoe()
+    d = WL.make_inputs(cfg, DEV)
+    rid, rw, _ = orc.route(d["logits"].cpu().numpy(),
+                           None if d["bias"] is None else d["bias"].cpu().numpy(),
+                           cfg.topk, cfg.score_fn, cfg.n_groups, cfg.topk_groups,
+                           cfg.renorm)
+    ids = torch.from_numpy(rid).to(DEV)
+    wts = torch.from_numpy(rw.astype(np.float32)).to(DEV)
+    P = cfg.P
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=DEV)
+    srt = torch.empty(P, dtype=torch.int32, device=DEV)
+    inv = torch.empty(P, dtype=torch.int32, device=DEV)
+    g.moe_align_permute(ids, cfg.E, None, offsets, srt, inv,
+                        g.workspace(g.WS_ALIGN, cfg.M, cfg.E, 0, 0, cfg.topk, 0))
+    return d, rid, rw, ids, wts, offsets, srt, inv
+
+
+@pytest.mark.parametrize("cfg", [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.SMALL_FP8],
+                         ids=lambda c: c.name)
+def test_gate_up_then_down_stages(cfg):
+    """Each grouped GEMM against the oracle's expert rows."""
+    g = gbmoe()
+    d, rid, rw, ids, wts, offsets, srt, inv = _stage_inputs(cfg)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    W = oracle_weights(cfg, d["w1"], d["w2"])
+    M, E, N, K, k, P = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk, cfg.P
+    fp8 = cfg.dtype == WL.FP8
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    if fp8:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+        xs = torch.empty((M, K // 128), dtype=torch.float32, device=DEV)
+        g.moe_quant_fp8_group(d["x"], xq, xs)
+        xin, xin_s = xq, xs
+        H = torch.empty((P, N), dtype=torch.uint8, device=DEV)
+        Hs = torch.empty((P, N // 128), dtype=torch.float32, device=DEV)
+    else:
+        xin, xin_s = d["x"], None
+        H = torch.empty((P, N), dtype=torch.bfloat16, device=DEV)
+        Hs = None
+    A = torch.empty((P, K), dtype=xin.dtype, device=DEV)
+    As = torch.empty((P, K // 128), dtype=torch.float32, device=DEV) if fp8 else None
+    g.moe_permute_rows(xin, xin_s, srt, offsets, k, E, cfg.dtype, A, As)
+    g.moe_grouped_gemm_gate_up_silu(A, As, offsets, M, k, E, N, K, gw.w1, gw.w1s,
+                                    cfg.dtype, H, Hs, err)
+    y = torch.empty((M, k, K), dtype=torch.bfloat16, device=DEV)
+    g.moe_grouped_gemm_down(H, Hs, srt, offsets, wts, M, k, E, N, K, gw.w2, gw.w2s,
+                            cfg.dtype, y, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    if fp8:
+        Hf = (H.view(torch.float8_e4m3fn).float().view(P, N // 128, 128) *
+              Hs.view(P, N // 128, 1)).view(P, N).cpu().numpy()
+    else:
+        Hf = H.float().cpu().numpy()
+    yf = y.float().cpu().numpy()
+    srt_np = srt.cpu().numpy()
+    xbits = WL.bf16_bits(d["x"])
+    rows = range(P) if P <= 600 else np.random.default_rng(0).choice(P, 600, replace=False)
+    href = np.zeros((len(rows), N))
+    yref = np.zeros((len(rows), K))
+    hgot = np.zeros_like(href)
+    ygot = np.zeros_like(yref)
+    for n, i in enumerate(rows):
+        pair = srt_np[i]
+        t, j = divmod(int(pair), k)
+        h, yy = orc.expert_row(xbits, t, rid[t, j], W, requant_h=cfg.requant_h)
+        href[n] = h
+        yref[n] = rw[t, j] * yy
+        hgot[n] = Hf[i]
+        ygot[n] = yf[t, j]
+    assert_close_rel(hgot, href, TOL[cfg.dtype], "H")
+    assert_close_rel(ygot, yref, TOL[cfg.dtype], "weighted y")
+
+
+@pytest.mark.parametrize("cfg", [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.SMALL_FP8],
+                         ids=lambda c: c.name)
+def test_forward_parity_small(cfg):
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    out, ids, wts, err = run_forward(cfg, d, gw)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    W = oracle_weights(cfg, d["w1"], d["w2"])
+    ref, rid, rw = oracle_forward(cfg, d, W)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, atol=2e-6, rtol=0)
+    assert_close_rel(out.float().cpu().numpy(), ref, TOL[cfg.dtype], cfg.name)
+
+
+def test_forward_is_deterministic():
+    cfg = WL.SMALL_SIGMOID
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    a, _, _, _ = run_forward(cfg, d, gw)
+    b, _, _, _ = run_forward(cfg, d, gw)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [0, 1, 129])
+def test_forward_edge_sizes(M):
+    """Empty input is a no-op; one token and a 129-token ragged tail."""
+    base = WL.SMALL_BF16
+    cfg = WL.MoEConfig("edge", M=M, K=base.K, N=base.N, E=base.E, topk=base.topk, seed=5)
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    if M == 0:
+        g = gbmoe()
+        out = torch.full((1, cfg.K), 3.0, dtype=torch.bfloat16, device=DEV)
+        ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+        g.moe_forward(d["x"], d["logits"], None, cfg.N, cfg.E, cfg.topk, cfg.score_fn,
+                      1, 1, True, cfg.dtype, gw.w1, None, gw.w2, None, out, ws)
+        torch.cuda.synchronize()
+        assert torch.all(out == 3.0)
+        return
+    out, _, _, err = run_forward(cfg, d, gw)
+    torch.cuda.synchronize()
+    W = oracle_weights(cfg, d["w1"], d["w2"])
+    ref, _, _ = oracle_forward(cfg, d, W)
+    assert_close_rel(out.float().cpu().numpy(), ref, TOL[cfg.dtype], f"M={M}")
+
+
+def test_one_expert_takes_every_token_matches_torch_matmul():
+    """All tokens on one expert: the grouped GEMMs reduce to dense matmuls,
+    checked against torch's own bf16 matmul on the GPU (a second reference)."""
+    g = gbmoe()
+    cfg = WL.MoEConfig("one", M=300, K=512, N=256, E=4, topk=1, seed=6)
+    d = WL.make_inputs(cfg, DEV)
+    d["logits"][:, 2] += 100.0  # every token picks expert 2
+    out, ids, wts, err = run_forward(cfg, d, GpuWeights(cfg, d["w1"], d["w2"]))
+    torch.cuda.synchronize()
+    assert torch.all(ids == 2)
+    x = d["x"].float()
+    w1 = d["w1"][2].float()
+    h = torch.nn.functional.silu(x @ w1[:256].T) * (x @ w1[256:].T)
+    ref = (h.to(torch.bfloat16).float() @ d["w2"][2].float().T)
+    assert_close_rel(out.float().cpu().numpy(), ref.cpu().numpy(), 2e-2, "dense")
+
+
+# ------------------------------------------------- full-size, sampled ------
+
+FULL_CFGS = [WL.MIXTRAL_PREFILL, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8]
+
+
+@pytest.mark.parametrize("cfg", FULL_CFGS, ids=lambda c: c.name)
+def test_forward_parity_full_size_sampled(cfg):
+    """The bench's workloads at full size: routing, counts and permutation of
+    every token against the oracle; output values on a seeded sample of
+    tokens, plus tokens of the most loaded expert (tokens are independent, so
+    a sample is computed exactly as in the full run)."""
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    out, ids, wts, err = run_forward(cfg, d, gw)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rid, rw, margin = orc.route(d["logits"].cpu().numpy(),
+                                None if d["bias"] is None else d["bias"].cpu().numpy(),
+                                cfg.topk, cfg.score_fn, cfg.n_groups, cfg.topk_groups,
+                                cfg.renorm)
+    diff = check_ids(ids.cpu().numpy(), rid, margin, cfg.name)
+    rng = np.random.default_rng(1)
+    n_sample = 24 if cfg.M > 64 else 16
+    counts = np.bincount(rid.ravel(), minlength=cfg.E)
+    top = int(np.argmax(counts))
+    on_top = np.flatnonzero((rid == top).any(1))
+    tokens = np.unique(np.concatenate([rng.choice(cfg.M, n_sample, replace=False),
+                                       on_top[:4]]))
+    tokens = np.setdiff1d(tokens, diff)
+    experts = np.unique(rid[tokens])
+    W = oracle_weights(cfg, d["w1"], d["w2"], experts)
+    ref, rid_s, _ = oracle_forward(cfg, d, W, tokens=tokens)
+    assert np.array_equal(rid_s, rid[tokens])
+    assert_close_rel(out[torch.from_numpy(tokens).to(DEV)].float().cpu().numpy(), ref,
+                     TOL[cfg.dtype], cfg.name)
