@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 import workloads as WL  # noqa: E402
 
-WORKLOADS = {c.name: c for c in WL.ALL}
+WORKLOADS = {n: c for n, c in WL.BY_NAME.items() if not c.batched}
 DEFAULT = WL.MIXTRAL_PREFILL.name
 METRIC = "MoE-layer tokens/s and % of roofline (TFLOP/s or HBM GB/s) on 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -50,11 +50,13 @@ def _peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def _kernel_traffic(kernel_key: str):
-    """DRAM bytes per launch of a kernel from a committed ncu summary in
-    profiles/ (a line 'traffic_bytes_per_launch: <n>' and 'source_sha256:
-    <hash of csrc/gemm.cu>'); None when absent or the kernel source changed."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_key}.traffic.txt")
+def _kernel_traffic(cfg, which: str):
+    """DRAM bytes per launch of the dominant kernel on this workload, from a
+    committed ncu summary profiles/<workload>.<which>.traffic.txt (lines
+    'traffic_bytes_per_launch: <n>' and 'source_sha256: <sha256 of
+    csrc/gemm.cu>').  None when there is none, or when the kernel source has
+    changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", f"{cfg.name}.{which}.traffic.txt")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -64,7 +66,8 @@ def _kernel_traffic(kernel_key: str):
                 k, v = ln.split(":", 1)
                 vals[k.strip()] = v.strip()
     src = os.path.join(ROOT, "mixture_experts_layer_count_gb300", "csrc", "gemm.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
     if vals.get("source_sha256") != h:
         return None
     try:
@@ -100,7 +103,7 @@ class ClockSampler:
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.time(), ln.strip()))
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -111,10 +114,14 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in samples taken
+        between wall times t0 and t1 (all samples when not given)."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if t0 is not None and not (t0 - 0.1 <= ts <= t1 + 0.1):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -248,11 +255,13 @@ def run_gpu(args, cfg):
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
+        wall0 = time.time()
         t0.record()
         for i in range(steps):
             layer.step(ev[i])
         t1.record()
         barrier()
+        wall1 = time.time()
     ms = t0.elapsed_time(t1)
     gemm_ms = [a.elapsed_time(b) for a, b in ev]
     assert layer.err.item() == 0, f"device error word {layer.err.item()}"
@@ -295,21 +304,56 @@ def run_gpu(args, cfg):
     tokens = cfg.M * steps * world
     value = tokens / (ms / 1e3)
     e2e_value = tokens / (e2e_ms / 1e3)
-    peaks, src = _peaks()
-    P = cfg.M * cfg.topk
-    gemm_flop = 4.0 * cfg.K * cfg.N * P  # gate/up GEMM, algorithmic
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    if cfg.dtype == WL.FP8:
-        peak = peak * 2.0  # nominal fp8 : bf16 dense ratio
-    achieved = gemm_flop / (gemm_avg / 1e3) / 1e12
-    traffic = _kernel_traffic(f"grouped_gemm_gate_up_{'fp8' if cfg.dtype == WL.FP8 else 'bf16'}")
-    layer_flop = 6.0 * cfg.K * cfg.N * P
-    clocks = clk.summary()
+    line = _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms,
+                 clk.summary(wall0, wall1))
+    line["value"] = value
+    line["e2e"]["value"] = e2e_value
     if rank != 0:
         return
-    line = {
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(cfg, layer, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
+    """The JSON result line (value fields filled in by the caller)."""
+    peaks, src = _peaks()
+    P = cfg.M * cfg.topk
+    fp8 = cfg.dtype == WL.FP8
+    eb = 1 if fp8 else 2
+    # the dominant kernel: the gate/up grouped GEMM (2/3 of the layer's FLOPs)
+    gemm_flop = 4.0 * cfg.K * cfg.N * P
+    counts = layer.counts.cpu().numpy()
+    touched = int((counts > 0).sum())
+    gemm_bytes = (touched * 2 * cfg.N * cfg.K * eb            # w1 of the experts with rows
+                  + (touched * (2 * cfg.N // 128) * (cfg.K // 128) * 4 if fp8 else 0)
+                  + P * cfg.K * eb + P * cfg.N * eb)          # A rows read, H written
+    tc_time = gemm_flop / (peaks.get("bf16_tflops", 1900.0) * (2 if fp8 else 1) * 1e12)
+    hbm_time = gemm_bytes / (peaks.get("hbm_gbs", 6800.0) * 1e9)
+    timed_s = ms / 1e3
+    if tc_time >= hbm_time:
+        key = "bf16_tflops" if timed_s < 2.0 else "bf16_tflops_sustained"
+        peak = peaks.get(key, FALLBACK_PEAKS[key]) * (2.0 if fp8 else 1.0)
+        achieved = gemm_flop / (gemm_avg / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"{src} {key}" + (" x2 (nominal fp8:bf16 dense ratio)" if fp8 else "")
+                               + f" (timed region {timed_s:.2f} s)"}
+    else:
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        achieved = gemm_bytes / (gemm_avg / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{src} hbm_gbs (copy)"}
+    roof.update({"traffic": _kernel_traffic(cfg, "gate_up"),
+                 "kernel": "grouped_gemm_kernel, gate/up + SiLU*mul",
+                 "kernel_ms": gemm_avg, "flop_per_launch": gemm_flop,
+                 "alg_bytes_per_launch": gemm_bytes, "experts_with_rows": touched})
+    layer_flop = 6.0 * cfg.K * cfg.N * P
+    return {
         "metric": METRIC,
-        "value": value,
+        "value": None,
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": steps,
@@ -318,30 +362,21 @@ def run_gpu(args, cfg):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3" if cfg.dtype == WL.FP8 else "bf16",
-        "data": "synthetic (seeded N(0,1) activations/logits, N(0,1/K), N(0,1/N) weights)",
+        "dtype": "fp8_e4m3" if fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1) activations and logits; N(0,1/K), N(0,1/N) weights)",
         "config": {"workload": cfg.name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "E": cfg.E,
                    "topk": cfg.topk, "format": "standard",
-                   "l2": "working set > L2 (weights %.2f GB stream every step)" %
-                         ((cfg.E * 3 * cfg.N * cfg.K * (1 if cfg.dtype == WL.FP8 else 2)) / 1e9),
-                   "parallelism": f"replicas x{world}"},
+                   "l2": "no flush; working set > L2 (%.2f GB of expert weights read per step)" %
+                         (touched * 3 * cfg.N * cfg.K * eb / 1e9),
+                   "parallelism": f"{world} independent replica(s)"},
         "layer_tflops": layer_flop / (ms / steps / 1e3) / 1e12,
-        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (gate/up + SiLU*mul)",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{src} bf16 sustained" + (" x2 (fp8 nominal ratio)" if cfg.dtype == WL.FP8 else ""),
-                     "gemm_ms": gemm_avg, "flop_per_launch": gemm_flop},
-        "e2e": {"value": e2e_value, "unit": "tokens/s",
+        "roofline": roof,
+        "e2e": {"value": None, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(layer.x.numel() * 2 + layer.logits.numel() * 4),
                 "d2h_bytes_per_step": int(layer.out.numel() * 2)},
         "gpu_launches": layer.launches_per_step * steps,
         "clocks": clocks,
     }
-    if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(cfg, layer, args.cpu_seconds)
-    print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -435,16 +470,14 @@ def run_reference(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gbmoe", choices=["gbmoe", "reference"])
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     cfg = WORKLOADS[args.workload]
-    if cfg.batched:
-        raise SystemExit("the batched workload is measured by its own test, not a bench line")
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

@@ -7,8 +7,9 @@ none of the layer's arithmetic (no routing, no quantisation, no GEMM).
 Recipe (the pages measure serving on real models; these synthetic tensors
 stand in for them -- no dataset or trained weight is used):
   * one ``torch.Generator`` seeded per workload, on the device the tensors are
-    made on; draw order logits, x, w1, w2, then the router bias or the
-    batched counts;
+    made on; draw order: logits, x, router bias (Standard) or x_b, counts,
+    padding garbage (Batched); then w1, w2 -- so the activations of a seed do
+    not depend on whether its weights are drawn;
   * hidden states x ~ N(0, 1) rounded to bf16; router logits ~ N(0, 1) fp32;
   * w1 (E, 2N, K) ~ N(0, 1/K), w2 (E, K, N) ~ N(0, 1/N), drawn in bf16;
   * skewed routing (DeepSeek-V3-shaped prefill): a per-expert bias
@@ -87,6 +88,20 @@ SMALL_BATCHED = MoEConfig("small_batched_bf16_E6_T200_K256_N256", M=200, K=256,
 
 ALL = [TINY, MIXTRAL_PREFILL, DSV3_PREFILL_FP8, DSV3_DECODE, BATCHED_MASKED]
 
+# Small cases of the same kernels for profiler captures: operands larger than
+# the 129 MB L2, a few hundred MB to ~1 GB on the device.
+PROFILE_BF16 = MoEConfig("profile_bf16_M2048_K4096_N14336_E2_top1", M=2048, K=4096,
+                         N=14336, E=2, topk=1, seed=21)
+PROFILE_FP8 = MoEConfig("profile_fp8_M2048_K7168_N2048_E16_top2", M=2048, K=7168,
+                        N=2048, E=16, topk=2, dtype=FP8, score_fn=SIGMOID,
+                        n_groups=4, topk_groups=2, seed=22)
+PROFILE_DECODE = MoEConfig("profile_decode_bf16_M16_K7168_N2048_E32_top4", M=16,
+                           K=7168, N=2048, E=32, topk=4, score_fn=SIGMOID,
+                           n_groups=4, topk_groups=2, seed=23)
+
+BY_NAME = {c.name: c for c in ALL + [SMALL_BF16, SMALL_SIGMOID, SMALL_FP8,
+                                     PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE]}
+
 
 def _gen(seed: int, device) -> torch.Generator:
     g = torch.Generator(device=device)
@@ -101,20 +116,16 @@ def _randn(shape, g, device, std=1.0, dtype=torch.float32):
     return t
 
 
-def make_standard(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
-                  with_weights: bool = True) -> dict:
-    """Inputs of the Standard format: logits (M, E) fp32, x (M, K) bf16,
-    w1 (E, 2N, K) bf16, w2 (E, K, N) bf16, bias (E) fp32 or None."""
-    seed = cfg.seed if seed is None else seed
-    g = _gen(seed, device)
-    out = {}
-    out["logits"] = _randn((cfg.M, cfg.E), g, device)
+def _weights(cfg: MoEConfig, g, device) -> dict:
+    return {"w1": _randn((cfg.E, 2 * cfg.N, cfg.K), g, device,
+                         std=1.0 / math.sqrt(cfg.K), dtype=torch.bfloat16),
+            "w2": _randn((cfg.E, cfg.K, cfg.N), g, device,
+                         std=1.0 / math.sqrt(cfg.N), dtype=torch.bfloat16)}
+
+
+def _standard_acts(cfg: MoEConfig, g, device) -> dict:
+    out = {"logits": _randn((cfg.M, cfg.E), g, device)}
     out["x"] = _randn((cfg.M, cfg.K), g, device).to(torch.bfloat16)
-    if with_weights:
-        out["w1"] = _randn((cfg.E, 2 * cfg.N, cfg.K), g, device,
-                           std=1.0 / math.sqrt(cfg.K), dtype=torch.bfloat16)
-        out["w2"] = _randn((cfg.E, cfg.K, cfg.N), g, device,
-                           std=1.0 / math.sqrt(cfg.N), dtype=torch.bfloat16)
     out["bias"] = None
     if cfg.zipf_bias:
         rank = torch.randperm(cfg.E, generator=g, device=device).to(torch.float32) + 1.0
@@ -122,38 +133,9 @@ def make_standard(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
     return out
 
 
-def make_weights(cfg: MoEConfig, device="cpu", seed: Optional[int] = None) -> dict:
-    """Only the expert weights (the same draws as make_standard/make_batched
-    would give for this seed, skipping the activations)."""
-    seed = cfg.seed if seed is None else seed
-    g = _gen(seed, device)
-    if cfg.batched:
-        _ = _randn((cfg.E, cfg.M, cfg.K), g, device)  # keep the draw order
-    else:
-        _ = _randn((cfg.M, cfg.E), g, device)
-        _ = _randn((cfg.M, cfg.K), g, device)
-    w1 = _randn((cfg.E, 2 * cfg.N, cfg.K), g, device, std=1.0 / math.sqrt(cfg.K),
-                dtype=torch.bfloat16)
-    w2 = _randn((cfg.E, cfg.K, cfg.N), g, device, std=1.0 / math.sqrt(cfg.N),
-                dtype=torch.bfloat16)
-    return {"w1": w1, "w2": w2}
-
-
-def make_batched(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
-                 with_weights: bool = True) -> dict:
-    """Inputs of the BatchedExperts format: x_b (E, T, K) bf16 whose rows
-    r >= counts[e] are N(0, 10^2) garbage, counts (E) int32, w1, w2."""
-    assert cfg.batched
-    seed = cfg.seed if seed is None else seed
+def _batched_acts(cfg: MoEConfig, g, device) -> dict:
     E, T = cfg.E, cfg.M
-    g = _gen(seed, device)
-    out = {}
     xb = _randn((E, T, cfg.K), g, device)
-    if with_weights:
-        out["w1"] = _randn((E, 2 * cfg.N, cfg.K), g, device,
-                           std=1.0 / math.sqrt(cfg.K), dtype=torch.bfloat16)
-        out["w2"] = _randn((E, cfg.K, cfg.N), g, device,
-                           std=1.0 / math.sqrt(cfg.N), dtype=torch.bfloat16)
     counts = torch.randint(0, T + 1, (E,), generator=g, device=device,
                            dtype=torch.int64)
     pos = torch.randperm(E, generator=g, device=device)
@@ -165,10 +147,41 @@ def make_batched(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
     rows = torch.arange(T, device=device).view(1, T, 1)
     pad = rows >= counts.view(E, 1, 1).to(rows.dtype)
     garbage = _randn((E, T, cfg.K), g, device, std=10.0)
-    xb = torch.where(pad, garbage, xb)
-    out["x_b"] = xb.to(torch.bfloat16)
-    out["counts"] = counts
+    return {"x_b": torch.where(pad, garbage, xb).to(torch.bfloat16), "counts": counts}
+
+
+def make_standard(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
+                  with_weights: bool = True) -> dict:
+    """Inputs of the Standard format: logits (M, E) fp32, x (M, K) bf16,
+    bias (E) fp32 or None, w1 (E, 2N, K) bf16, w2 (E, K, N) bf16."""
+    g = _gen(cfg.seed if seed is None else seed, device)
+    out = _standard_acts(cfg, g, device)
+    if with_weights:
+        out.update(_weights(cfg, g, device))
     return out
+
+
+def make_batched(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
+                 with_weights: bool = True) -> dict:
+    """Inputs of the BatchedExperts format: x_b (E, T, K) bf16 whose rows
+    r >= counts[e] are N(0, 10^2) garbage, counts (E) int32, w1, w2."""
+    assert cfg.batched
+    g = _gen(cfg.seed if seed is None else seed, device)
+    out = _batched_acts(cfg, g, device)
+    if with_weights:
+        out.update(_weights(cfg, g, device))
+    return out
+
+
+def make_weights(cfg: MoEConfig, device="cpu", seed: Optional[int] = None) -> dict:
+    """Only the expert weights: the same draws make_inputs gives for this
+    seed (the activations are drawn first and dropped)."""
+    g = _gen(cfg.seed if seed is None else seed, device)
+    if cfg.batched:
+        _batched_acts(cfg, g, device)
+    else:
+        _standard_acts(cfg, g, device)
+    return _weights(cfg, g, device)
 
 
 def make_inputs(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
