@@ -268,6 +268,33 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                            float *topk_weights, void *ws, size_t ws_bytes,
                            int32_t *err_word, gbmoe_stream_t stream);
 
+/* moe_align_permute without a workspace argument.  The pages have no
+ * counterpart of this call: it exists for callers that cannot give the
+ * library scratch memory -- for instance a plugin interface that hands an
+ * operator only its input and output buffers, or a serving engine that has
+ * carved up all device memory in advance and has no spare buffer to lend
+ * per call.  It computes exactly what moe_align_permute computes (same
+ * arguments and results, minus ws / ws_bytes) and allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ * Its scratch (one int32 histogram of E entries per chunk of 2048 pairs) is a
+ * fixed 256 KiB array in device memory that belongs to the library: every
+ * GPU that loads the library keeps it until the process exits.  Limit:
+ * ceil(M*topk / 2048) * E <= 65536 (for example M*topk <= 524288 pairs with
+ * E = 256); larger problems return GBMOE_INVALID_ARG and enqueue nothing.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * All calls share the one array and it keeps the last call's contents; every
+ * entry a call reads is first written by the same call, so nothing needs
+ * clearing.  Two calls that overlap on the GPU (different streams without
+ * ordering between them) race on the array and give wrong results. */
+gbmoe_status_t moe_align_permute_no_ws(const int32_t *topk_ids, int M,
+                                       int topk, int E, int32_t *counts,
+                                       int32_t *offsets,
+                                       int32_t *sorted_pair_ids, int32_t *inv,
+                                       int32_t *err_word,
+                                       gbmoe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

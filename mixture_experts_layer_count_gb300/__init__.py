@@ -47,6 +47,7 @@ _SIGS = {
     "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_count_expert_tokens": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_align_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
+    "moe_align_permute_no_ws": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_group": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
     "moe_permute_rows": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
@@ -131,6 +132,18 @@ def moe_align_permute(topk_ids, E, counts, offsets, sorted_pair_ids, inv, ws,
         _ptr(sorted_pair_ids), _ptr(inv), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _ptr(err_word),
         _stream(stream)))
+
+
+def moe_align_permute_no_ws(topk_ids, E, counts, offsets, sorted_pair_ids, inv,
+                            err_word=None, stream=None):
+    """moe_align_permute for callers that have no scratch buffer to give:
+    the histograms live in a fixed 256 KiB array owned by the library (see
+    include/gbmoe.h for the size limit and the rule against overlapping
+    calls)."""
+    M, topk = topk_ids.shape
+    _check("moe_align_permute_no_ws", load().moe_align_permute_no_ws(
+        _ptr(topk_ids), M, topk, E, _ptr(counts), _ptr(offsets),
+        _ptr(sorted_pair_ids), _ptr(inv), _ptr(err_word), _stream(stream)))
 
 
 def moe_quant_fp8_group(x, q, scales, group=128, stream=None):

@@ -182,6 +182,9 @@ bool gemm_shape_ok(int M, int topk, int E, int N, int K, int dtype) {
 }
 
 }  // namespace
+
+gbmoe_status_t status_from_cuda(cudaError_t e) { return from_cuda(e); }
+
 }  // namespace gbmoe
 
 using namespace gbmoe;

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "gbmoe.h"
+
 namespace gbmoe {
 
 // route.cu
@@ -64,6 +66,10 @@ struct GroupedGemmArgs {
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,
                                 cudaStream_t s);
+
+// api.cu: map a cudaError_t to a status, remembering it for
+// gbmoe_last_cuda_error
+gbmoe_status_t status_from_cuda(cudaError_t e);
 
 // driver entry point for tensor-map encoding (resolved once)
 bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes,
