@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 import workloads as WL  # noqa: E402
 
-WORKLOADS = {n: c for n, c in WL.BY_NAME.items() if not c.batched}
+WORKLOADS = dict(WL.BY_NAME)
 DEFAULT = WL.MIXTRAL_PREFILL.name
 METRIC = "MoE-layer tokens/s and % of roofline (TFLOP/s or HBM GB/s) on 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -179,9 +179,10 @@ class Layer:
         self.xq = torch.empty((M, K), dtype=torch.uint8, device=device) if self.fp8 else None
         self.xs = torch.empty((M, K // 128), dtype=f32, device=device) if self.fp8 else None
         self.A = torch.empty((P, K), dtype=adt, device=device)
-        self.As = torch.empty((P, K // 128), dtype=f32, device=device) if self.fp8 else None
+        ld = (P + 3) // 4 * 4  # group-major FP8 row scales
+        self.As = torch.empty((K // 128, ld), dtype=f32, device=device) if self.fp8 else None
         self.H = torch.empty((P, N), dtype=adt, device=device)
-        self.Hs = torch.empty((P, N // 128), dtype=f32, device=device) if self.fp8 else None
+        self.Hs = torch.empty((N // 128, ld), dtype=f32, device=device) if self.fp8 else None
         self.y = torch.empty((M, k, K), dtype=torch.bfloat16, device=device)
         self.out = torch.empty((M, K), dtype=torch.bfloat16, device=device)
         self.err = torch.zeros(1, dtype=i32, device=device)
@@ -216,6 +217,23 @@ class Layer:
         self.g.moe_forward(x, logits, self.bias, c.N, c.E, c.topk, c.score_fn, c.n_groups,
                            c.topk_groups, c.renorm, c.dtype, self.w1, self.w1s, self.w2,
                            self.w2s, out, self.fwd_ws, err_word=self.err)
+
+
+def reduce_max(values, dist=None, device="cpu"):
+    """Element-wise max of a list of floats over all ranks (identity with one
+    process).  The only cross-rank operation of the benchmark."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_throughput(tokens_per_step, steps, world, max_ms):
+    """Whole-job tokens/s of `world` independent replicas: every rank's
+    tokens over the slowest rank's time."""
+    return tokens_per_step * steps * world / (max_ms / 1e3)
 
 
 def _dist():
@@ -294,16 +312,9 @@ def run_gpu(args, cfg):
     assert layer.err.item() == 0
 
     # max over ranks
-    if pg is not None:
-        t = torch.tensor([ms, e2e_ms, float(np.mean(gemm_ms))], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms, e2e_ms, gemm_avg = t.tolist()
-    else:
-        gemm_avg = float(np.mean(gemm_ms))
-
-    tokens = cfg.M * steps * world
-    value = tokens / (ms / 1e3)
-    e2e_value = tokens / (e2e_ms / 1e3)
+    ms, e2e_ms, gemm_avg = reduce_max([ms, e2e_ms, float(np.mean(gemm_ms))], pg, device=dev)
+    value = replica_throughput(cfg.M, steps, world, ms)
+    e2e_value = replica_throughput(cfg.M, steps, world, e2e_ms)
     line = _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms,
                  clk.summary(wall0, wall1))
     line["value"] = value
@@ -377,6 +388,119 @@ def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
         "gpu_launches": layer.launches_per_step * steps,
         "clocks": clocks,
     }
+
+
+def run_gpu_batched(args, cfg):
+    """BatchedExperts (E, T, K) masked by device counts, as it is used: one
+    CUDA graph of moe_batched_masked_experts captured once and replayed
+    (step = one replay over resident inputs).  Throughput counts the valid
+    rows (a token routed to an expert); the roofline covers both grouped
+    GEMM launches of the call (6*K*N FLOP per valid row)."""
+    import torch
+    import mixture_experts_layer_count_gb300 as g
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    g.load()
+    d = WL.make_inputs(cfg, dev)
+    E, T, N, K = cfg.E, cfg.M, cfg.N, cfg.K
+    xb, counts, w1, w2 = d["x_b"], d["counts"], d["w1"], d["w2"]
+    yb = torch.empty_like(xb)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = g.workspace(g.WS_BATCHED, T, E, N, K, 1, WL.BF16, device=dev)
+    rows = int(counts.clamp(0, T).sum().item())
+
+    def call(x, c, y):
+        g.moe_batched_masked_experts(x, c, N, w1, w2, y, ws, err_word=err)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(max(1, args.warmup)):
+            call(xb, counts, yb)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(xb, counts, yb)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    steps = args.steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        t0.record()
+        for _ in range(steps):
+            graph.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+        wall1 = time.time()
+    ms = t0.elapsed_time(t1)
+    assert err.item() == 0, f"device error word {err.item()}"
+    # end to end: pinned host inputs in, the result out, every step
+    xh = xb.cpu().pin_memory()
+    ch = counts.cpu().pin_memory()
+    yh = torch.empty(yb.shape, dtype=yb.dtype).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(steps, 20))
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(e2e_steps):
+        xb.copy_(xh, non_blocking=True)
+        counts.copy_(ch, non_blocking=True)
+        graph.replay()
+        yh.copy_(yb, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    ms, e2e_ms = reduce_max([ms, e2e_ms], pg, device=dev)
+    if rank != 0:
+        return
+    peaks, src = _peaks()
+    timed_s = ms / 1e3
+    key = "bf16_tflops" if timed_s < 2.0 else "bf16_tflops_sustained"
+    peak = peaks.get(key, FALLBACK_PEAKS[key])
+    flop = 6.0 * K * N * rows
+    achieved = flop / (ms / steps / 1e3) / 1e12
+    touched = int((counts > 0).sum().item())
+    line = {
+        "metric": METRIC, "value": replica_throughput(rows, steps, world, ms),
+        "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; padded rows N(0,10^2) garbage)",
+        "config": {"workload": cfg.name, "E": E, "T": T, "K": K, "N": N,
+                   "format": "batched_experts, CUDA graph replay",
+                   "valid_rows": rows, "experts_with_rows": touched,
+                   "l2": "no flush; working set > L2 (%.2f GB of expert weights per step)" %
+                         (touched * 3 * N * K * 2 / 1e9),
+                   "parallelism": f"{world} independent replica(s)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "grouped_gemm_kernel, gate/up + down (one graph replay)",
+                     "peak_source": f"{src} {key} (timed region {timed_s:.2f} s)",
+                     "flop_per_launch": flop},
+        "e2e": {"value": rows * e2e_steps * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(xb.numel() * 2 + counts.numel() * 4),
+                "d2h_bytes_per_step": int(yb.numel() * 2)},
+        "gpu_launches": 2 * steps,
+        "clocks": clk.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -479,7 +603,11 @@ def main():
     args = ap.parse_args()
     cfg = WORKLOADS[args.workload]
     if args.impl == "reference":
+        if cfg.batched:
+            raise SystemExit("the reference arm times the Standard workloads")
         run_reference(args, cfg)
+    elif cfg.batched:
+        run_gpu_batched(args, cfg)
     else:
         run_gpu(args, cfg)
 

@@ -165,7 +165,10 @@ gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
  * beyond offsets[E] are left unwritten).
  * dtype GBMOE_BF16: x (M, K) bf16 -> A (M*topk, K) bf16; scales unused.
  * dtype GBMOE_FP8_E4M3: x (M, K) e4m3 with x_scales (M, K/128) fp32 ->
- *   A (M*topk, K) e4m3 with A_scales (M*topk, K/128).
+ *   A (M*topk, K) e4m3 with A_scales stored GROUP-MAJOR: A_scales[g * ld + i]
+ *   is the scale of row i, K block g, with ld = M*topk rounded up to a
+ *   multiple of 4 (a (K/128, ld) array), so that the scales of one K block
+ *   of consecutive rows are contiguous for the GEMM's TMA loads.
  * K % 128 == 0; x and A 16-byte aligned. */
 gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
                                 const int32_t *sorted_pair_ids,
@@ -184,11 +187,13 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
  * offsets[E] are left unwritten.
  * dtype GBMOE_BF16: A bf16, w1 (E, 2N, K) bf16, H (M*topk, N) bf16;
  *   A_scales / w1_scales / H_scales unused (NULL).
- * dtype GBMOE_FP8_E4M3: A e4m3 with A_scales (M*topk, K/128) fp32; w1 e4m3
- *   with w1_scales (E, 2N/128, K/128) fp32 (128 x 128 blocks); each 128-wide
- *   K block is accumulated in fp32 and scaled by A_scale * w1_scale before it
- *   is added.  H is written as e4m3 with H_scales (M*topk, N/128) fp32,
- *   requantised per 128-group of a row with the moe_quant_fp8_group rule.
+ * dtype GBMOE_FP8_E4M3: A e4m3 with group-major A_scales (K/128, ld) fp32
+ *   (moe_permute_rows; ld = M*topk rounded up to 4, 16-byte aligned); w1
+ *   e4m3 with w1_scales (E, 2N/128, K/128) fp32 (128 x 128 blocks); each
+ *   128-wide K block is accumulated in fp32 and scaled by A_scale * w1_scale
+ *   before it is added.  H is written as e4m3 with group-major H_scales
+ *   (N/128, ld) fp32, requantised per 128-group of a row with the
+ *   moe_quant_fp8_group rule.
  * Accumulation is fp32.  N % 128 == 0, K % 128 == 0.  err_word may be NULL. */
 gbmoe_status_t moe_grouped_gemm_gate_up_silu(
     const void *A, const float *A_scales, const int32_t *offsets, int M,
@@ -206,7 +211,8 @@ gbmoe_status_t moe_grouped_gemm_gate_up_silu(
  * FusedMoEPrepareAndFinalize.finalize, already weighted; its rows of pairs
  * whose id is invalid are not written.
  * dtype GBMOE_BF16: H (M*topk, N) bf16, w2 (E, K, N) bf16.
- * dtype GBMOE_FP8_E4M3: H e4m3 + H_scales (M*topk, N/128); w2 e4m3 +
+ * dtype GBMOE_FP8_E4M3: H e4m3 + group-major H_scales (N/128, ld), ld =
+ *   M*topk rounded up to 4 (as written by the gate/up call); w2 e4m3 +
  *   w2_scales (E, K/128, N/128).  Accumulation fp32.  err_word may be NULL. */
 gbmoe_status_t moe_grouped_gemm_down(
     const void *H, const float *H_scales, const int32_t *sorted_pair_ids,

@@ -67,6 +67,9 @@ struct Carver {
 
 size_t elem_bytes(int dtype) { return dtype == GBMOE_FP8_E4M3 ? 1 : 2; }
 
+// leading dimension of the group-major FP8 row scales of M*topk rows
+int64_t scale_ld(size_t P) { return (int64_t)((P + 3) / 4 * 4); }
+
 bool valid_dtype(int dtype) { return dtype == GBMOE_BF16 || dtype == GBMOE_FP8_E4M3; }
 
 struct ForwardWs {
@@ -94,9 +97,9 @@ ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dty
   w.xq = fp8 ? static_cast<uint8_t *>(c.take((size_t)M * K)) : nullptr;
   w.xs = fp8 ? static_cast<float *>(c.take((size_t)M * (K / 128) * 4)) : nullptr;
   w.A = c.take(P * (size_t)K * elem_bytes(dtype));
-  w.As = fp8 ? static_cast<float *>(c.take(P * (size_t)(K / 128) * 4)) : nullptr;
+  w.As = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * (K / 128) * 4)) : nullptr;
   w.H = c.take(P * (size_t)N * elem_bytes(dtype));
-  w.Hs = fp8 ? static_cast<float *>(c.take(P * (size_t)(N / 128) * 4)) : nullptr;
+  w.Hs = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * (N / 128) * 4)) : nullptr;
   w.y_slot = static_cast<uint16_t *>(c.take(P * (size_t)K * 2));
   return w;
 }
@@ -130,6 +133,7 @@ gbmoe_status_t gate_up_impl(const void *A, const float *A_scales,
   a.A = A;
   a.a_rows = (int64_t)M * topk;
   a.A_scales = A_scales;
+  a.scale_ld = scale_ld((size_t)M * topk);
   a.B = w1;
   a.B_scales = w1_scales;
   a.out = H;
@@ -146,7 +150,8 @@ gbmoe_status_t permute_impl(const void *x, const float *x_scales,
   return from_cuda(launch_gather_rows(x, fp8 ? x_scales : nullptr,
                                       (int)(K * elem_bytes(dtype)), K / 128, sorted,
                                       offsets + E, M * topk, topk, A,
-                                      fp8 ? A_scales : nullptr, num_sms, s));
+                                      fp8 ? A_scales : nullptr,
+                                      scale_ld((size_t)M * topk), num_sms, s));
 }
 
 gbmoe_status_t down_impl(const void *H, const float *H_scales,
@@ -165,6 +170,7 @@ gbmoe_status_t down_impl(const void *H, const float *H_scales,
   a.A = H;
   a.a_rows = (int64_t)M * topk;
   a.A_scales = H_scales;
+  a.scale_ld = scale_ld((size_t)M * topk);
   a.B = w2;
   a.B_scales = w2_scales;
   a.out = y_slot;
@@ -315,13 +321,15 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
   if (M < 0 || topk < 1 || topk > kMaxTopk || E < 1 || E > kMaxExperts || K < 128 ||
       K % 128 != 0 || (size_t)M * topk > (size_t)INT32_MAX)
     return GBMOE_INVALID_ARG;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  if (M > 0) {
+    if (!x || !sorted_pair_ids || !offsets || !A || !aligned16(x) || !aligned16(A))
+      return GBMOE_INVALID_ARG;
+    if (fp8 && (!x_scales || !A_scales)) return GBMOE_INVALID_ARG;
+  }
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK || M == 0) return st;
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
-  if (!x || !sorted_pair_ids || !offsets || !A || !aligned16(x) || !aligned16(A))
-    return GBMOE_INVALID_ARG;
-  if (fp8 && (!x_scales || !A_scales)) return GBMOE_INVALID_ARG;
   return permute_impl(x, x_scales, sorted_pair_ids, offsets, M, topk, E, K, dtype, A,
                       A_scales, sms, (cudaStream_t)stream);
 }
@@ -333,13 +341,15 @@ gbmoe_status_t moe_grouped_gemm_gate_up_silu(
     gbmoe_stream_t stream) {
   if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
   if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  if (M > 0) {
+    if (!A || !offsets || !w1 || !H) return GBMOE_INVALID_ARG;
+    if (fp8 && (!A_scales || !w1_scales || !H_scales)) return GBMOE_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(w1) || !aligned16(H)) return GBMOE_INVALID_ARG;
+  }
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK || M == 0) return st;
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
-  if (!A || !offsets || !w1 || !H) return GBMOE_INVALID_ARG;
-  if (fp8 && (!A_scales || !w1_scales || !H_scales)) return GBMOE_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(w1) || !aligned16(H)) return GBMOE_INVALID_ARG;
   return gate_up_impl(A, A_scales, offsets, M, topk, E, N, K, w1, w1_scales, dtype, H,
                       H_scales, err_word, sms, (cudaStream_t)stream);
 }
@@ -442,17 +452,19 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
   if (!route_args_ok(M, E, topk, score_fn, bias, n_groups, topk_groups))
     return GBMOE_INVALID_ARG;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  if (M > 0) {
+    if (!x || !logits || !w1 || !w2 || !out || !ws) return GBMOE_INVALID_ARG;
+    if (fp8 && (!w1_scales || !w2_scales)) return GBMOE_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(ws))
+      return GBMOE_INVALID_ARG;
+    if (ws_bytes < moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype))
+      return GBMOE_INVALID_ARG;
+  }
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK) return st;
   if (M == 0) return GBMOE_OK;
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
-  if (!x || !logits || !w1 || !w2 || !out || !ws) return GBMOE_INVALID_ARG;
-  if (fp8 && (!w1_scales || !w2_scales)) return GBMOE_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(ws))
-    return GBMOE_INVALID_ARG;
-  if (ws_bytes < moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype))
-    return GBMOE_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   Carver c(ws);
   ForwardWs w = carve_forward(c, M, E, N, K, topk, dtype);

@@ -1,0 +1,457 @@
+// gemm_fp8.cu -- the two expert GEMMs with e4m3 operands and fp32 block
+// scales (1 x 128 along K for the rows of A, 128 x 128 for the weights), on
+// tcgen05.mma kind::f8f6f4 with the fp32 scale promotion done by the
+// epilogue warps.
+//
+// Both scales change every 128 elements of K, so a K block's products cannot
+// be accumulated across blocks inside the tensor core.  Each K block (4 MMAs
+// of K 32) is accumulated alone into one of two 256-column TMEM buffers; 16
+// epilogue warps then add it into fp32 registers,
+//     acc += (s_a[row, kb] * s_w[blk, kb]) * partial,
+// while the tensor core fills the other buffer.  Each epilogue thread owns one
+// row and 64 columns (4 lane quarters x 4 column quarters cover the 128 x 256
+// tile), so the promotion is 32 packed FFMA2 per thread per K block.  The
+// per-row scales of a K block travel with the operand tiles: the producer
+// loads them by TMA from the group-major scale array (one contiguous run of
+// rows per K block) into the stage's shared memory; the weight-block scales
+// of a tile (two rows of K blocks) are staged in shared memory once per tile.
+//
+// gate/up ends with h = silu(gate) * up and the e4m3 requantisation of h in
+// 128-wide groups (one scale per row and n-tile; the row maximum is
+// exchanged between the four warps holding that row); down ends with the
+// router weight and bf16 stores into the (token, slot) rows.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "gemm_common.cuh"
+#include "kernels.h"
+
+namespace gbmoe {
+
+namespace {
+
+using namespace gemm;
+
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;      // 576
+constexpr int kBK = kBKB;                       // e4m3 elements per stage row
+constexpr int kMmaPerStage = kBK / 32;          // kind::f8f6f4 has K = 32
+constexpr uint32_t kIdesc = umma_idesc(kBM, kBN, kFmtE4M3);
+constexpr int kMaxKB = 128;                     // K up to 16384
+constexpr int kASBox = kBM + 4;                 // row scales per K block (rows from a 4-aligned start)
+constexpr int kASStage = 640;                   // bytes per ring slot (528 used)
+constexpr int kASStages = 8;                    // row-scale ring, deeper than the operand ring
+
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kAStage;
+constexpr int kOffAS = kOffB + kStages * kBStage;            // 196608
+constexpr int kOffBar = kOffAS + kASStages * kASStage;
+// full[4], empty[4], tfull[2], tempty[2], done, bsc[2], xchg[2], as_full[8], as_empty[8]
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 2 + 2 + 2 * kASStages;
+constexpr int kOffTmem = kOffBar + 8 * kNumBars;
+constexpr int kOffBsc = kOffTmem + 16;                       // [2 bufs][2][kMaxKB] f32
+constexpr int kOffAmax = kOffBsc + 2 * 2 * kMaxKB * 4;       // [2 bufs][4][128] f32
+constexpr int kOffPrefix = kOffAmax + 2 * 4 * 128 * 4;
+constexpr int kOffRBase = kOffPrefix + (kMaxE + 1) * 4;
+constexpr int kOffRCnt = kOffRBase + kMaxE * 4;
+constexpr int kSmemUsed = kOffRCnt + kMaxE * 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;
+
+struct KParams {
+  const int32_t *offsets;
+  int E, N, K;
+  int n_tiles;
+  int num_kb;
+  int b_rows;               // rows of B per expert (2N or K)
+  void *out;
+  float *out_scales;        // gate/up: H scales (N/128, scale_ld)
+  int64_t scale_ld;
+  const float *b_scales;    // (E, b_rows/128, num_kb)
+  const int32_t *sorted;
+  const float *topk_w;
+  int32_t *err;
+};
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// acc[0..16) += f * v[0..16) with packed fp32x2 FMAs
+__device__ __forceinline__ void promote16(float *acc, const uint32_t (&v)[16], float f) {
+  const float2 f2 = make_float2(f, f);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float2 a = make_float2(acc[2 * j], acc[2 * j + 1]);
+    const float2 x = make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+    a = __ffma2_rn(x, f2, a);
+    acc[2 * j] = a.x;
+    acc[2 * j + 1] = a.y;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmAS,
+                            const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t *sbase = smem_raw + (base - raw_u32);
+
+  const uint32_t sA = base + kOffA;
+  const uint32_t sB = base + kOffB;
+  const uint32_t sAS = base + kOffAS;
+  const uint32_t bar0 = base + kOffBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
+  auto bsc_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 5 + b); };
+  auto xchg_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 7 + b); };
+  auto as_full_bar = [&](int s) { return bar0 + 8u * (2 * kStages + 9 + s); };
+  auto as_empty_bar = [&](int s) { return bar0 + 8u * (2 * kStages + 9 + kASStages + s); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + kOffTmem);
+  const float *as_smem = reinterpret_cast<const float *>(sbase + kOffAS);
+  float *bsc_smem = reinterpret_cast<float *>(sbase + kOffBsc);
+  float *amax_x = reinterpret_cast<float *>(sbase + kOffAmax);
+  int *prefix = reinterpret_cast<int *>(sbase + kOffPrefix);
+  int *rbase = reinterpret_cast<int *>(sbase + kOffRBase);
+  int *rcnt = reinterpret_cast<int *>(sbase + kOffRCnt);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  tile_table_fill(p.offsets, nullptr, E, 0, p.n_tiles, prefix, rbase, rcnt, p.err);
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < kASStages; ++s) {
+      mbar_init(as_full_bar(s), 1);
+      mbar_init(as_empty_bar(s), kEpiWarps);  // every epilogue warp has read its scale
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kEpiWarps);
+      mbar_init(bsc_bar(b), kEpiThreads);
+      mbar_init(xchg_bar(b), kEpiThreads);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmAS);
+  }
+  if (warp == 1) tmem_alloc<512>(smem_u32(tmem_slot));
+  __syncthreads();
+  if (warp == 0) tile_table_scan(prefix, E, lane);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = prefix[E];
+  const int num_kb = p.num_kb;
+
+  if (warp == 0) {
+    // =========================== TMA producer ===========================
+    if (lane == 0) {
+      int it = 0;
+      int last_round[kStages], last_as_round[kASStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
+#pragma unroll
+      for (int s = 0; s < kASStages; ++s) last_as_round[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int e, mt, nt;
+        decode_tile(prefix, E, p.n_tiles, tile, e, mt, nt);
+        const int a_row = rbase[e] + mt * kBM;
+        int b_row0, b_row1;
+        if (MODE == kGateUpMode) {
+          b_row0 = e * p.b_rows + nt * 128;
+          b_row1 = e * p.b_rows + p.N + nt * 128;
+        } else {
+          b_row0 = e * p.b_rows + nt * kBN;
+          b_row1 = b_row0 + 128;
+        }
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kStages, round = it / kStages;
+          const int s8 = it % kASStages, round8 = it / kASStages;
+          if (!mbar_wait(empty_bar(s), (round & 1) ^ 1) ||
+              !mbar_wait(as_empty_bar(s8), (round8 & 1) ^ 1)) {
+            set_err(p.err, GBMOE_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(s), kAStage + kBStage);
+          const int x = kb * kBK;
+          tma_load_2d(sA + s * kAStage, &tmA, full_bar(s), x, a_row);
+          tma_load_2d(sB + s * kBStage, &tmB, full_bar(s), x, b_row0);
+          tma_load_2d(sB + s * kBStage + kBStage / 2, &tmB, full_bar(s), x, b_row1);
+          last_round[s] = round;
+          // row scales of K block kb for rows [a_row & ~3, +132): the start
+          // is rounded down to 4 floats (16 bytes) as TMA requires
+          mbar_arrive_expect_tx(as_full_bar(s8), kASBox * 4);
+          tma_load_2d(sAS + s8 * kASStage, &tmAS, as_full_bar(s8), a_row & ~3, kb);
+          last_as_round[s8] = round8;
+        }
+      }
+      // copies still in flight land before the CTA can leave
+#pragma unroll
+      for (int s = 0; s < kStages; ++s)
+        if (last_round[s] >= 0) mbar_wait(full_bar(s), last_round[s] & 1, 100000000ull);
+#pragma unroll
+      for (int s = 0; s < kASStages; ++s)
+        if (last_as_round[s] >= 0) mbar_wait(as_full_bar(s), last_as_round[s] & 1, 100000000ull);
+    }
+  } else if (warp == 1) {
+    // =========================== MMA issuer =============================
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int buf = it & 1, use = it >> 1;
+          const int s = it % kStages, round = it / kStages;
+          if (!mbar_wait(tempty_bar(buf), (use & 1) ^ 1) ||
+              !mbar_wait(full_bar(s), round & 1)) {
+            set_err(p.err, GBMOE_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + buf * kBN;
+          const uint64_t da = umma_desc_sw128(sA + s * kAStage);
+          const uint64_t db = umma_desc_sw128(sB + s * kBStage);
+#pragma unroll
+          for (int k = 0; k < kMmaPerStage; ++k)
+            umma_f8(d, da + 2 * k, db + 2 * k, kIdesc, k != 0);
+          umma_commit(empty_bar(s));
+          umma_commit(tfull_bar(buf));
+        }
+      }
+      umma_commit(done_bar);
+      mbar_wait(done_bar, 0, 100000000ull);
+    }
+  } else {
+    // ============================= epilogue =============================
+    const int ew = warp - 2;           // 0..15
+    const int q = warp & 3;            // TMEM lane quarter of this warp
+    const int cq = ew >> 2;            // column quarter of this warp
+    const int etid = ew * 32 + lane;   // 0..511
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(q * 32) << 16;
+    const int b_blk_rows = p.b_rows / 128;
+    int it = 0, tile_no = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tile_no) {
+      int e, mt, nt;
+      decode_tile(prefix, E, p.n_tiles, tile, e, mt, nt);
+      const int a_row = rbase[e] + mt * kBM;
+      const int r = mt * kBM + row_in_tile;
+      const bool valid = r < rcnt[e];
+      const int arow = a_row + row_in_tile;
+      const int as_idx = (a_row & 3) + row_in_tile;
+
+      // weight-block scales of this tile: [0] gate (or the first 128
+      // columns), [1] up (or the second 128 columns), for every K block
+      const int tb = tile_no & 1;
+      float *bsc = bsc_smem + tb * 2 * kMaxKB;
+      for (int i = etid; i < 2 * num_kb; i += kEpiThreads) {
+        const int h = i / num_kb, kb = i - h * num_kb;
+        int blk = MODE == kGateUpMode ? (h == 0 ? nt : p.N / 128 + nt) : nt * 2 + h;
+        if (blk >= b_blk_rows) blk = b_blk_rows - 1;  // columns past K: masked
+        bsc[h * kMaxKB + kb] = p.b_scales[((size_t)e * b_blk_rows + blk) * num_kb + kb];
+      }
+      mbar_arrive(bsc_bar(tb));
+      if (!mbar_wait(bsc_bar(tb), (tile_no >> 1) & 1)) {
+        set_err(p.err, GBMOE_ERR_TIMEOUT);
+        break;
+      }
+      const float *bs_g = bsc;                     // gate / this quarter's block (down)
+      const float *bs_u = bsc + kMaxKB;            // up
+      const float *bs_d = bsc + (cq >> 1) * kMaxKB;
+
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int buf = it & 1, use = it >> 1;
+        const int s8 = it % kASStages, round8 = it / kASStages;
+        if (!mbar_wait(as_full_bar(s8), round8 & 1)) {
+          set_err(p.err, GBMOE_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        const float sa = as_smem[s8 * (kASStage / 4) + as_idx];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(as_empty_bar(s8));
+        if (!mbar_wait(tfull_bar(buf), use & 1)) {
+          set_err(p.err, GBMOE_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbuf = tmem_base + t_lane + buf * kBN;
+        uint32_t v0[16], v1[16];
+        if (MODE == kGateUpMode) {
+          const float fg = sa * bs_g[kb], fu = sa * bs_u[kb];
+          const uint32_t cg = tbuf + cq * 32, cu = tbuf + 128 + cq * 32;
+          tmem_ld16(cg, v0);
+          tmem_ld16(cg + 16, v1);
+          tmem_ld_wait();
+          promote16(acc, v0, fg);
+          promote16(acc + 16, v1, fg);
+          tmem_ld16(cu, v0);
+          tmem_ld16(cu + 16, v1);
+          tmem_ld_wait();
+          promote16(acc + 32, v0, fu);
+          promote16(acc + 48, v1, fu);
+        } else {
+          const float f = sa * bs_d[kb];
+          const uint32_t c0 = tbuf + cq * 64;
+          tmem_ld16(c0, v0);
+          tmem_ld16(c0 + 16, v1);
+          tmem_ld_wait();
+          promote16(acc, v0, f);
+          promote16(acc + 16, v1, f);
+          tmem_ld16(c0 + 32, v0);
+          tmem_ld16(c0 + 48, v1);
+          tmem_ld_wait();
+          promote16(acc + 32, v0, f);
+          promote16(acc + 48, v1, f);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+      }
+      if (!ok) break;
+
+      if (MODE == kGateUpMode) {
+        // h on this thread's 32 columns, then one e4m3 scale per 128-wide
+        // group: the row maximum over the four column quarters
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          acc[i] = silu_f(acc[i]) * acc[32 + i];
+          amax = fmaxf(amax, fabsf(acc[i]));
+        }
+        const int xb = tile_no & 1;
+        amax_x[(xb * 4 + cq) * 128 + row_in_tile] = amax;
+        mbar_arrive(xchg_bar(xb));
+        if (!mbar_wait(xchg_bar(xb), (tile_no >> 1) & 1)) {
+          set_err(p.err, GBMOE_ERR_TIMEOUT);
+          break;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) amax = fmaxf(amax, amax_x[(xb * 4 + c) * 128 + row_in_tile]);
+        const float sc = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
+        if (valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
+                                                 (size_t)arow * p.N + nt * 128 + cq * 32);
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int i0 = v * 16 + j * 4;
+              w4[j] = e4m3x4(__fdiv_rn(acc[i0], sc), __fdiv_rn(acc[i0 + 1], sc),
+                             __fdiv_rn(acc[i0 + 2], sc), __fdiv_rn(acc[i0 + 3], sc));
+            }
+            dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          if (cq == 0) p.out_scales[(size_t)nt * p.scale_ld + arow] = sc;
+        }
+      } else {
+        const int col0 = nt * kBN + cq * 64;
+        if (valid && col0 < p.K) {
+          const int pair = p.sorted[arow];
+          const float w = p.topk_w[pair];
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                 (size_t)pair * p.K + col0);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_uint4(pack_bf16x2(w * acc[8 * v], w * acc[8 * v + 1]),
+                                pack_bf16x2(w * acc[8 * v + 2], w * acc[8 * v + 3]),
+                                pack_bf16x2(w * acc[8 * v + 4], w * acc[8 * v + 5]),
+                                pack_bf16x2(w * acc[8 * v + 6], w * acc[8 * v + 7]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc<512>(tmem_base);
+}
+
+template <int MODE>
+cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_fp8_kernel<MODE>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          kSmemBytes);
+    if (st != cudaSuccess) return st;
+    attr_set = true;
+  }
+  const bool gate_up = MODE == kGateUpMode;
+  const int Kd = gate_up ? a.K : a.N;
+  const int b_rows = gate_up ? 2 * a.N : a.K;
+  const int num_kb = Kd / kBK;
+  if (num_kb > kMaxKB || !a.offsets || a.scale_ld % 4 != 0 || a.scale_ld < a.a_rows)
+    return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB, tmAS;
+  if (!encode_tmap_2d(&tmA, a.A, kTmapU8, (uint64_t)Kd, (uint64_t)a.a_rows, (uint64_t)Kd,
+                      kBK, kBM, true) ||
+      !encode_tmap_2d(&tmB, a.B, kTmapU8, (uint64_t)Kd, (uint64_t)a.E * b_rows, (uint64_t)Kd,
+                      kBK, 128, true) ||
+      !encode_tmap_2d(&tmAS, a.A_scales, kTmapF32, (uint64_t)a.scale_ld, (uint64_t)num_kb,
+                      (uint64_t)a.scale_ld * 4, kASBox, 1, false))
+    return cudaErrorInvalidValue;
+  KParams p;
+  p.offsets = a.offsets;
+  p.E = a.E;
+  p.N = a.N;
+  p.K = a.K;
+  p.n_tiles = gate_up ? a.N / 128 : (a.K + kBN - 1) / kBN;
+  p.num_kb = num_kb;
+  p.b_rows = b_rows;
+  p.out = a.out;
+  p.out_scales = a.out_scales;
+  p.scale_ld = a.scale_ld;
+  p.b_scales = a.B_scales;
+  p.sorted = a.sorted_pair_ids;
+  p.topk_w = a.topk_weights;
+  p.err = a.err;
+  long long tiles = ((a.a_rows + kBM - 1) / kBM + a.E) * (long long)p.n_tiles;
+  int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  if (grid < 1) grid = 1;
+  grouped_gemm_fp8_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmAS, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_fp8(const GroupedGemmArgs &a, int num_sms,
+                                    cudaStream_t s) {
+  return a.mode == kGateUp ? launch_fp8<kGateUpMode>(a, num_sms, s)
+                           : launch_fp8<kDownMode>(a, num_sms, s);
+}
+
+}  // namespace gbmoe

@@ -23,11 +23,12 @@ int align_num_chunks(int P);
 cudaError_t launch_align(const int32_t *ids, int P, int E, int32_t *counts,
                          int32_t *offsets, int32_t *sorted, int32_t *inv,
                          int32_t *chunk_hist, int32_t *err, cudaStream_t s);
+// out_s is group-major: (n_scales, out_s_ld)
 cudaError_t launch_gather_rows(const void *x, const float *xs, int row_bytes,
                                int n_scales, const int32_t *sorted,
                                const int32_t *total, int P, int topk,
-                               void *out, float *out_s, int num_sms,
-                               cudaStream_t s);
+                               void *out, float *out_s, int64_t out_s_ld,
+                               int num_sms, cudaStream_t s);
 cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
                           int topk, int K, uint16_t *out, int num_sms,
                           cudaStream_t s);
@@ -53,12 +54,13 @@ struct GroupedGemmArgs {
   // operands
   const void *A;             // (rows, Kd) bf16 or e4m3, Kd = K (gate-up) or N (down)
   int64_t a_rows;            // rows of A's allocation
-  const float *A_scales;     // fp8: (a_rows, Kd/128)
+  const float *A_scales;     // fp8: (Kd/128, scale_ld), group-major
+  int64_t scale_ld;          // fp8: leading dimension of A_scales / out_scales (a_rows rounded up to 4)
   const void *B;             // w1 or w2
   const float *B_scales;     // fp8: w1 (E, 2N/128, K/128) / w2 (E, K/128, N/128)
   // outputs
   void *out;                 // gate-up: H (a_rows, N); down: y rows of K bf16
-  float *out_scales;         // fp8 gate-up: H scales (a_rows, N/128)
+  float *out_scales;         // fp8 gate-up: H scales (N/128, scale_ld), group-major
   const int32_t *sorted_pair_ids;  // down, Standard: output row = pair id
   const float *topk_weights;       // down, Standard: row scale
   int32_t *err;
@@ -66,14 +68,20 @@ struct GroupedGemmArgs {
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,
                                 cudaStream_t s);
+// gemm_fp8.cu
+cudaError_t launch_grouped_gemm_fp8(const GroupedGemmArgs &a, int num_sms,
+                                    cudaStream_t s);
 
 // api.cu: map a cudaError_t to a status, remembering it for
 // gbmoe_last_cuda_error
 gbmoe_status_t status_from_cuda(cudaError_t e);
 
-// driver entry point for tensor-map encoding (resolved once)
-bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes,
-                    uint64_t cols, uint64_t rows, uint32_t box_cols,
-                    uint32_t box_rows);
+// 2-D TMA tensor map (cuTensorMapEncodeTiled, resolved once through the
+// runtime): `cols` x `rows` elements, rows `row_stride_bytes` apart, boxes of
+// box_cols x box_rows, 128-byte swizzle or none.
+enum { kTmapU8 = 0, kTmapBF16 = 1, kTmapF32 = 2 };
+bool encode_tmap_2d(CUtensorMap *map, const void *base, int kind, uint64_t cols,
+                    uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols,
+                    uint32_t box_rows, bool swizzle128);
 
 }  // namespace gbmoe

@@ -173,13 +173,16 @@ __global__ void __launch_bounds__(kAlignThreads)
 // ------------------------------------------------------------------ gather --
 
 // out[i] = x[sorted[i] / topk] for i < *total (one warp per row, 16-byte
-// vectors); FP8 also carries the row's group scales.
+// vectors); FP8 also carries the row's group scales, written group-major
+// (out_s[g * out_s_ld + i]) so that a GEMM tile's scales of one K block are
+// contiguous.
 __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint4 *__restrict__ x, const float *__restrict__ xs,
                        int row_vecs, int n_scales,
                        const int32_t *__restrict__ sorted,
                        const int32_t *__restrict__ total, int P, int topk,
-                       uint4 *__restrict__ out, float *__restrict__ out_s) {
+                       uint4 *__restrict__ out, float *__restrict__ out_s,
+                       int64_t out_s_ld) {
   const int lane = threadIdx.x & 31;
   const int n = min(*total, P);
   for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n;
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(256)
     for (int v = lane; v < row_vecs; v += 32) dst[v] = src[v];
     if (xs)
       for (int g = lane; g < n_scales; g += 32)
-        out_s[(size_t)i * n_scales + g] = xs[(size_t)t * n_scales + g];
+        out_s[(size_t)g * out_s_ld + i] = xs[(size_t)t * n_scales + g];
   }
 }
 
@@ -265,15 +268,15 @@ cudaError_t launch_align(const int32_t *ids, int P, int E, int32_t *counts,
 cudaError_t launch_gather_rows(const void *x, const float *xs, int row_bytes,
                                int n_scales, const int32_t *sorted,
                                const int32_t *total, int P, int topk,
-                               void *out, float *out_s, int num_sms,
-                               cudaStream_t s) {
+                               void *out, float *out_s, int64_t out_s_ld,
+                               int num_sms, cudaStream_t s) {
   const int warps_per_block = 8;
   int blocks = (P + warps_per_block - 1) / warps_per_block;
   if (blocks > 8 * num_sms) blocks = 8 * num_sms;
   if (blocks < 1) blocks = 1;
   gather_rows_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(
       static_cast<const uint4 *>(x), xs, row_bytes / 16, n_scales, sorted,
-      total, P, topk, static_cast<uint4 *>(out), out_s);
+      total, P, topk, static_cast<uint4 *>(out), out_s, out_s_ld);
   return cudaGetLastError();
 }
 

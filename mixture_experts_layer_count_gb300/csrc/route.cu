@@ -67,11 +67,15 @@ __global__ void __launch_bounds__(256)
     if (e < E) v[i] = row[e] + ((sigmoid && bias) ? bias[e] : 0.0f);
   }
 
-  // ---- group limit (sigmoid only): lane g ends up holding group g's key
+  // ---- group limit (sigmoid only): lane g ends up holding the two largest
+  // v of group g and computes the group's key itself, so the warp issues the
+  // fp64 sigmoid sequence twice in all rather than twice per group (the fp64
+  // pipe is narrow: a warp-wide fp64 instruction costs the same with one
+  // lane active as with 32)
   const int gs = E / (n_groups > 0 ? n_groups : 1);
   uint32_t gmask = kFull;
   if (sigmoid && n_groups > 1 && topk_groups < n_groups) {
-    float my_key = -INFINITY;
+    float my_t1 = -INFINITY, my_t2 = -INFINITY;
     for (int g = 0; g < n_groups; ++g) {
       float t1 = -INFINITY, t2 = -INFINITY;  // two largest v of group g
 #pragma unroll
@@ -96,9 +100,14 @@ __global__ void __launch_bounds__(256)
         t1 = hi;
         t2 = lo;
       }
-      if (lane == g)
-        my_key = gs >= 2 ? key_sigmoid(t1) + key_sigmoid(t2) : key_sigmoid(t1);
+      if (lane == g) {
+        my_t1 = t1;
+        my_t2 = t2;
+      }
     }
+    float my_key = -INFINITY;
+    if (lane < n_groups)
+      my_key = gs >= 2 ? key_sigmoid(my_t1) + key_sigmoid(my_t2) : key_sigmoid(my_t1);
     gmask = 0;
     for (int r = 0; r < topk_groups; ++r) {
       bool cand = lane < n_groups && !((gmask >> lane) & 1u);

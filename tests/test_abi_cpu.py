@@ -55,3 +55,98 @@ def test_status_strings():
     lib = g.load()
     assert lib.gbmoe_status_string(0) == b"ok"
     assert lib.gbmoe_status_string(1) == b"invalid argument"
+
+
+# ---------------------------------------------------------------------------
+# Argument checks: every call below is invalid and must be refused on the
+# host, before any device query or launch.  The pointers are stand-ins that
+# are never dereferenced.  Skipped where a CUDA device is visible, so that a
+# mistake in the checks could never turn into a launch on garbage pointers.
+
+P16 = 1 << 20          # a 16-byte aligned stand-in pointer
+P_ODD = (1 << 20) + 4  # misaligned for TMA / vector access
+
+
+@pytest.fixture
+def lib():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-side argument checks run where no device is visible")
+    import mixture_experts_layer_count_gb300 as g
+    return g.load()
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+def test_route_rejects_bad_arguments(lib):
+    f = lib.moe_topk_route
+    #        logits bias  M   E  topk fn ng tg rn ids  w   err stream
+    assert f(P16, None, 8, 8, 9, 0, 1, 1, 1, P16, P16, None, None) == INVALID   # topk > E
+    assert f(P16, None, 8, 64, 33, 0, 1, 1, 1, P16, P16, None, None) == INVALID  # topk > 32
+    assert f(P16, None, 8, 513, 2, 0, 1, 1, 1, P16, P16, None, None) == INVALID  # E > 512
+    assert f(P16, P16, 8, 8, 2, 0, 1, 1, 1, P16, P16, None, None) == INVALID     # bias with softmax
+    assert f(P16, None, 8, 10, 2, 1, 4, 2, 1, P16, P16, None, None) == INVALID   # E % groups
+    assert f(P16, None, 8, 16, 5, 1, 4, 1, 1, P16, P16, None, None) == INVALID   # topk > kept experts
+    assert f(P16, None, 8, 8, 2, 7, 1, 1, 1, P16, P16, None, None) == INVALID    # score function
+    assert f(None, None, 8, 8, 2, 0, 1, 1, 1, P16, P16, None, None) == INVALID   # null logits
+
+
+def test_count_align_reject_bad_arguments(lib):
+    assert lib.moe_count_expert_tokens(P16, 8, 2, 8, None, None, None) == INVALID
+    assert lib.moe_count_expert_tokens(P16, -1, 2, 8, P16, None, None) == INVALID
+    assert lib.moe_count_expert_tokens(None, 8, 2, 8, P16, None, None) == INVALID
+    # workspace too small
+    assert lib.moe_align_permute(P16, 8, 2, 8, None, P16, P16, P16, P16, 0, None, None) == INVALID
+    assert lib.moe_align_permute(P16, 8, 2, 600, None, P16, P16, P16, P16, 1 << 20, None, None) == INVALID
+    # the no-workspace variant refuses sizes beyond its fixed array
+    assert lib.moe_align_permute_no_ws(P16, 65536, 8, 512, None, P16, P16, P16, None, None) == INVALID
+
+
+def test_quant_rejects_bad_arguments(lib):
+    assert lib.moe_quant_fp8_group(P16, 4, 256, 64, P16, P16, None) == INVALID     # group
+    assert lib.moe_quant_fp8_group(P16, 4, 200, 128, P16, P16, None) == INVALID    # K % 128
+    assert lib.moe_quant_fp8_group(P_ODD, 4, 256, 128, P16, P16, None) == INVALID  # alignment
+    assert lib.moe_quant_fp8_block(P16, 100, 256, 128, P16, P16, None) == INVALID  # R % 128
+    assert lib.moe_quant_fp8_block(P16, 128, 256, 128, None, P16, None) == INVALID
+
+
+def test_gemm_calls_reject_bad_arguments(lib):
+    g = lib.moe_grouped_gemm_gate_up_silu
+    #        A   As    off  M  k  E  N    K    w1   w1s  dt H    Hs   err  s
+    assert g(P16, None, P16, 8, 2, 8, 100, 256, P16, None, 0, P16, None, None, None) == INVALID
+    assert g(P16, None, P16, 8, 2, 8, 128, 256, P16, None, 5, P16, None, None, None) == UNSUPPORTED
+    assert g(P_ODD, None, P16, 8, 2, 8, 128, 256, P16, None, 0, P16, None, None, None) == INVALID
+    assert g(P16, None, P16, 8, 2, 8, 128, 256, P16, None, 1, P16, None, None, None) == INVALID  # fp8 w/o scales
+    assert g(P16, None, P16, 8, 2, 8, 128, 256, None, None, 0, P16, None, None, None) == INVALID
+    d = lib.moe_grouped_gemm_down
+    assert d(P16, None, P16, P16, P16, 8, 2, 8, 128, 256, P16, None, 1, P16, None, None) == INVALID
+    assert d(P16, None, P16, P16, None, 8, 2, 8, 128, 256, P16, None, 0, P16, None, None) == INVALID
+    assert lib.moe_permute_rows(P16, None, P16, P16, 8, 2, 8, 256, 9, P16, None, None) == UNSUPPORTED
+    assert lib.moe_permute_rows(P16, None, P16, P16, 8, 2, 8, 200, 0, P16, None, None) == INVALID
+    assert lib.moe_permute_rows(None, None, P16, P16, 8, 2, 8, 256, 0, P16, None, None) == INVALID
+    assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 2, 12, P16, None) == INVALID
+    assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 33, 256, P16, None) == INVALID
+    b = lib.moe_batched_masked_experts
+    #        xb  xbs   cnt E  T   N    K    w1   w1s  w2   w2s  dt yb   ws   wsb  err  s
+    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 1, P16, P16, 1 << 30, None, None) == UNSUPPORTED
+    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 0, P16, P16, 16, None, None) == INVALID
+    assert b(P16, None, None, 4, 16, 128, 256, P16, None, P16, None, 0, P16, P16, 1 << 30, None, None) == INVALID
+
+
+def test_forward_rejects_bad_arguments(lib):
+    f = lib.moe_forward
+    args = [P16, P16, None, 64, 256, 128, 8, 2, 0, 1, 1, 1, 0, P16, None, P16, None,
+            P16, None, None, P16, 1 << 30, None, None]
+    small = list(args)
+    small[21] = 1024  # workspace too small
+    assert f(*small) == INVALID
+    with_bias = list(args)
+    with_bias[2] = P16  # bias with a softmax router
+    assert f(*with_bias) == INVALID
+    odd = list(args)
+    odd[17] = P_ODD  # misaligned output
+    assert f(*odd) == INVALID
+    fp8 = list(args)
+    fp8[12] = 1  # FP8 weights without their scales
+    assert f(*fp8) == INVALID

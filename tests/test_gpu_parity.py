@@ -182,13 +182,14 @@ def test_gate_up_then_down_stages(cfg):
         g.moe_quant_fp8_group(d["x"], xq, xs)
         xin, xin_s = xq, xs
         H = torch.empty((P, N), dtype=torch.uint8, device=DEV)
-        Hs = torch.empty((P, N // 128), dtype=torch.float32, device=DEV)
+        ld = (P + 3) // 4 * 4  # group-major scales, leading dimension rounded to 4
+        Hs = torch.empty((N // 128, ld), dtype=torch.float32, device=DEV)
     else:
         xin, xin_s = d["x"], None
         H = torch.empty((P, N), dtype=torch.bfloat16, device=DEV)
         Hs = None
     A = torch.empty((P, K), dtype=xin.dtype, device=DEV)
-    As = torch.empty((P, K // 128), dtype=torch.float32, device=DEV) if fp8 else None
+    As = torch.empty((K // 128, (P + 3) // 4 * 4), dtype=torch.float32, device=DEV) if fp8 else None
     g.moe_permute_rows(xin, xin_s, srt, offsets, k, E, cfg.dtype, A, As)
     g.moe_grouped_gemm_gate_up_silu(A, As, offsets, M, k, E, N, K, gw.w1, gw.w1s,
                                     cfg.dtype, H, Hs, err)
@@ -199,7 +200,7 @@ def test_gate_up_then_down_stages(cfg):
     assert err.item() == 0
     if fp8:
         Hf = (H.view(torch.float8_e4m3fn).float().view(P, N // 128, 128) *
-              Hs.view(P, N // 128, 1)).view(P, N).cpu().numpy()
+              Hs[:, :P].t().reshape(P, N // 128, 1)).view(P, N).cpu().numpy()
     else:
         Hf = H.float().cpu().numpy()
     yf = y.float().cpu().numpy()
