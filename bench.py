@@ -53,19 +53,21 @@ def _peaks():
 def _kernel_traffic(cfg, which: str):
     """DRAM bytes per launch of the dominant kernel on this workload, from a
     committed ncu summary profiles/<workload>.<which>.traffic.txt (lines
-    'traffic_bytes_per_launch: <n>' and 'source_sha256: <sha256 of
-    csrc/gemm.cu>').  None when there is none, or when the kernel source has
-    changed since the counters were taken."""
+    'traffic_bytes_per_launch: <n>', 'source_file: <kernel source>' and
+    'source_sha256: <its sha256>').  None when there is none, or when the
+    kernel source has changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", f"{cfg.name}.{which}.traffic.txt")
     if not os.path.exists(path):
         return None
     vals = {}
     with open(path) as f:
         for ln in f:
-            if ":" in ln:
+            if ":" in ln and not ln.startswith("#"):
                 k, v = ln.split(":", 1)
                 vals[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "mixture_experts_layer_count_gb300", "csrc", "gemm.cu")
+    src = os.path.join(ROOT, vals.get("source_file", ""))
+    if not os.path.isfile(src):
+        return None
     with open(src, "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()
     if vals.get("source_sha256") != h:
