@@ -61,8 +61,18 @@ def _load():
             lib.orc_route.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P]
             lib.orc_count.restype = I
             lib.orc_count.argtypes = [P, I, I, P]
+            lib.orc_count_mapped.restype = I
+            lib.orc_count_mapped.argtypes = [P, I, I, P, I, P]
             lib.orc_align.restype = None
             lib.orc_align.argtypes = [P, I, I, P, P, P]
+            lib.orc_align_mapped.restype = None
+            lib.orc_align_mapped.argtypes = [P, I, I, P, I, P, P, P]
+            lib.orc_quant_fp8_group_w.restype = None
+            lib.orc_quant_fp8_group_w.argtypes = [P, P, I, I, I, P, P]
+            lib.orc_moe_forward_ep.restype = None
+            lib.orc_moe_forward_ep.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I,
+                                               I, I, P, I, I, P, P, P, P, P, I,
+                                               P, P, P, I]
             lib.orc_permute_rows.restype = None
             lib.orc_permute_rows.argtypes = [P, P, I, I, I, P]
             lib.orc_unpermute_reduce.restype = None
@@ -137,24 +147,31 @@ def route(logits, bias, topk, score_fn, n_groups=1, topk_groups=1,
     return ids, w, margin
 
 
-def count(ids, E):
+def count(ids, E, expert_map=None, E_local=None):
+    """Per-(local-)expert counts; returns (counts, number of invalid ids).
+    With expert_map (E global ids -> local id or -1), counts has E_local
+    entries and pairs of experts that are not local are left out."""
     lib = _load()
     ids = _c(ids, np.int32).ravel()
-    counts = np.empty((E,), np.int32)
-    bad = lib.orc_count(_p(ids), ids.size, E, _p(counts))
+    El = E if E_local is None else E_local
+    counts = np.empty((El,), np.int32)
+    m = _c(expert_map, np.int32)
+    bad = lib.orc_count_mapped(_p(ids), ids.size, E, _p(m), El, _p(counts))
     return counts, int(bad)
 
 
-def align(ids, E):
-    """Returns offsets (E+1), sorted pair ids (offsets[E]), inv (P)."""
+def align(ids, E, expert_map=None, E_local=None):
+    """Returns offsets (E_local+1), sorted pair ids (offsets[-1]), inv (P)."""
     lib = _load()
     ids = _c(ids, np.int32).ravel()
     P = ids.size
-    offsets = np.empty((E + 1,), np.int32)
+    El = E if E_local is None else E_local
+    offsets = np.empty((El + 1,), np.int32)
     sorted_ids = np.full((P,), -1, np.int32)
     inv = np.empty((P,), np.int32)
-    lib.orc_align(_p(ids), P, E, _p(offsets), _p(sorted_ids), _p(inv))
-    return offsets, sorted_ids[: offsets[E]].copy(), inv
+    m = _c(expert_map, np.int32)
+    lib.orc_align_mapped(_p(ids), P, E, _p(m), El, _p(offsets), _p(sorted_ids), _p(inv))
+    return offsets, sorted_ids[: offsets[El]].copy(), inv
 
 
 def permute_rows(x, sorted_ids, topk):
@@ -179,14 +196,16 @@ def unpermute_reduce(yperm, inv, w):
     return out
 
 
-def quant_fp8_group(x_bf16_bits, group=128):
-    """x (M, K) as uint16 bf16 bits -> q (M, K) uint8 codes, scales (M, K/group)."""
+def quant_fp8_group(x_bf16_bits, group=128, row_weights=None):
+    """x (M, K) as uint16 bf16 bits -> q (M, K) uint8 codes, scales (M, K/group).
+    row_weights (M) fp32 or None: rows multiplied (in fp32) before quantising."""
     lib = _load()
     x = _c(x_bf16_bits, np.uint16)
     M, K = x.shape
     q = np.empty((M, K), np.uint8)
     s = np.empty((M, K // group), np.float32)
-    lib.orc_quant_fp8_group(_p(x), M, K, group, _p(q), _p(s))
+    rw = _c(row_weights, np.float32)
+    lib.orc_quant_fp8_group_w(_p(x), _p(rw), M, K, group, _p(q), _p(s))
     return q, s
 
 
@@ -262,26 +281,33 @@ def expert_row(x_bf16_bits, t, e, W: Weights, requant_h=False):
 
 def moe_forward(x_bf16_bits, logits, bias, topk, score_fn, W: Weights,
                 n_groups=1, topk_groups=1, renorm=True, requant_h=False,
-                tokens=None, nthreads=0):
+                tokens=None, nthreads=0, expert_map=None,
+                weight_on_input=False):
     """The layer in the Standard format for the listed tokens (all when None).
-    Returns out (n, K) fp64, ids (n, topk) int32, weights (n, topk) fp64."""
+    logits (M, E) cover the E routed (global) experts; W holds W.E local
+    experts, reached through expert_map (E) when given (-1: not local, the
+    pair adds nothing).  weight_on_input: the router weight scales the
+    expert's input instead of its output.
+    Returns out (n, K) fp64, ids (n, topk) int32 (global), weights (n, topk)."""
     lib = _load()
     x = _c(x_bf16_bits, np.uint16)
     logits = _c(logits, np.float32)
     bias = _c(bias, np.float32)
     M, K = x.shape
     E = logits.shape[1]
-    assert E == W.E and K == W.K
+    assert K == W.K
+    assert (expert_map is None and E == W.E) or expert_map is not None
+    emap = _c(expert_map, np.int32)
     tok = None if tokens is None else _c(np.asarray(tokens), np.int32)
     n = M if tok is None else tok.size
     out = np.empty((n, K), np.float64)
     ids = np.empty((n, topk), np.int32)
     w = np.empty((n, topk), np.float64)
-    lib.orc_moe_forward(_p(x), _p(logits), _p(bias), M, K, W.N, E, topk,
-                        score_fn, n_groups, topk_groups, int(renorm), W.dtype,
-                        int(requant_h), _p(W.w1), _p(W.w1s), _p(W.w2),
-                        _p(W.w2s), _p(tok), n, _p(ids), _p(w), _p(out),
-                        int(nthreads))
+    lib.orc_moe_forward_ep(_p(x), _p(logits), _p(bias), M, K, W.N, E, topk,
+                           score_fn, n_groups, topk_groups, int(renorm), W.dtype,
+                           int(requant_h), _p(emap), W.E, int(weight_on_input),
+                           _p(W.w1), _p(W.w1s), _p(W.w2), _p(W.w2s), _p(tok), n,
+                           _p(ids), _p(w), _p(out), int(nthreads))
     return out, ids, w
 
 

@@ -57,6 +57,10 @@
  *   Q5 optional requantisation of the hidden row h in 128-wide groups.
  *   F1 the topk slots are summed in slot order j = 0..topk-1.
  *   B1 batched rows r >= count[e] are neither read nor written.
+ *   B3 expert_map (FusedMoEModularKernel.forward): global -> local expert
+ *      ids of this shard, -1 = not here (the pair adds nothing);
+ *      apply_router_weight_on_input (prepare, forward; topk 1): the router
+ *      weight multiplies the expert's input, not its output.
  */
 #include <math.h>
 #include <stdint.h>
@@ -327,47 +331,84 @@ void orc_route(const float *logits, const float *bias, int M, int E, int topk,
 /* [Permute-Experts-Unpermute]; P1                                           */
 /* ------------------------------------------------------------------------ */
 
-/* counts[e] = number of pairs p < P with ids[p] == e.  Returns how many ids
- * were outside [0, E) (those pairs are left out). */
-int orc_count(const int32_t *ids, int P, int E, int32_t *counts)
+/* The local expert of a routed (global) id -- the expert_map argument of
+ * FusedMoEModularKernel.forward / FusedMoEPermuteExpertsUnpermute.apply maps
+ * global expert ids to this expert-parallel shard's local ids.  map NULL:
+ * the identity (E_global == E_local).  Returns the local id, -1 for an
+ * expert that is not on this shard (map value -1: the pair is not computed
+ * here), -2 for an id that is invalid (outside [0, E_global), or mapped
+ * outside [0, E_local)). */
+static int local_expert(int g, int E_global, const int32_t *map, int E_local)
+{
+    int l;
+    if (g < 0 || g >= E_global)
+        return -2;
+    l = map ? map[g] : g;
+    if (l == -1)
+        return -1;
+    if (l < 0 || l >= E_local)
+        return -2;
+    return l;
+}
+
+/* counts[l] = number of pairs p < P whose id maps to local expert l.
+ * Returns how many ids were invalid (those pairs are left out, as are the
+ * pairs of experts that are not local). */
+int orc_count_mapped(const int32_t *ids, int P, int E_global,
+                     const int32_t *map, int E_local, int32_t *counts)
 {
     int p, bad = 0;
-    memset(counts, 0, sizeof(int32_t) * (size_t)E);
+    memset(counts, 0, sizeof(int32_t) * (size_t)E_local);
     for (p = 0; p < P; ++p) {
-        if (ids[p] < 0 || ids[p] >= E) {
+        int l = local_expert(ids[p], E_global, map, E_local);
+        if (l == -2)
             ++bad;
+        if (l < 0)
             continue;
-        }
-        counts[ids[p]] += 1;
+        counts[l] += 1;
     }
     return bad;
 }
 
-/* Stable counting sort of pair ids by expert: offsets (E+1) exclusive
- * prefix sums of the counts; sorted[offsets[e] + r] = the r-th pair (in
- * ascending pair order) routed to e; inv[p] = its position, -1 for a pair
- * whose id is out of range. */
-void orc_align(const int32_t *ids, int P, int E, int32_t *offsets,
-               int32_t *sorted, int32_t *inv)
+int orc_count(const int32_t *ids, int P, int E, int32_t *counts)
+{
+    return orc_count_mapped(ids, P, E, NULL, E, counts);
+}
+
+/* Stable counting sort of pair ids by (local) expert: offsets (E_local+1)
+ * exclusive prefix sums of the counts; sorted[offsets[l] + r] = the r-th
+ * pair (in ascending pair order) routed to l; inv[p] = its position, -1 for
+ * a pair that is not computed here (invalid id, or an expert that is not
+ * local). */
+void orc_align_mapped(const int32_t *ids, int P, int E_global,
+                      const int32_t *map, int E_local, int32_t *offsets,
+                      int32_t *sorted, int32_t *inv)
 {
     int p, e;
-    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
-    orc_count(ids, P, E, cursor);
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E_local > 0 ? E_local : 1));
+    orc_count_mapped(ids, P, E_global, map, E_local, cursor);
     offsets[0] = 0;
-    for (e = 0; e < E; ++e)
+    for (e = 0; e < E_local; ++e)
         offsets[e + 1] = offsets[e] + cursor[e];
-    for (e = 0; e < E; ++e)
+    for (e = 0; e < E_local; ++e)
         cursor[e] = offsets[e];
     for (p = 0; p < P; ++p) {
-        if (ids[p] < 0 || ids[p] >= E) {
+        int l = local_expert(ids[p], E_global, map, E_local);
+        if (l < 0) {
             inv[p] = -1;
             continue;
         }
-        sorted[cursor[ids[p]]] = p;
-        inv[p] = cursor[ids[p]];
-        cursor[ids[p]] += 1;
+        sorted[cursor[l]] = p;
+        inv[p] = cursor[l];
+        cursor[l] += 1;
     }
     free(cursor);
+}
+
+void orc_align(const int32_t *ids, int P, int E, int32_t *offsets,
+               int32_t *sorted, int32_t *inv)
+{
+    orc_align_mapped(ids, P, E, NULL, E, offsets, sorted, inv);
 }
 
 /* Gather: xperm[i] = x[sorted[i] / topk] for i < n_rows (rows of K doubles). */
@@ -405,17 +446,22 @@ void orc_unpermute_reduce(const double *yperm, const int32_t *inv,
 /* [Quantize-Prepare] -- Q1 and its 2-D block form for weights               */
 /* ------------------------------------------------------------------------ */
 
-/* x (M, K) bf16 -> q (M, K) e4m3 codes, scales (M, K / group) fp32. */
-void orc_quant_fp8_group(const uint16_t *x, int M, int K, int group,
-                         uint8_t *q, float *scales)
+/* x (M, K) bf16 -> q (M, K) e4m3 codes, scales (M, K / group) fp32.
+ * row_w (M) or NULL: with apply_router_weight_on_input (prepare applies the
+ * router weight to the activations before quantising), row t is first
+ * multiplied by row_w[t] -- an fp32 product, the precision the codes are
+ * decided in. */
+void orc_quant_fp8_group_w(const uint16_t *x, const float *row_w, int M,
+                           int K, int group, uint8_t *q, float *scales)
 {
     int t, g, k, G = K / group;
     for (t = 0; t < M; ++t) {
+        const float rw = row_w ? row_w[t] : 1.0f;
         for (g = 0; g < G; ++g) {
             const uint16_t *xg = x + (size_t)t * K + (size_t)g * group;
             float amax = 0.0f, s;
             for (k = 0; k < group; ++k) {
-                float v = (float)fabs(bf16_value(xg[k]));
+                float v = (float)fabs((float)bf16_value(xg[k]) * rw);
                 if (v > amax)
                     amax = v;
             }
@@ -423,9 +469,15 @@ void orc_quant_fp8_group(const uint16_t *x, int M, int K, int group,
             scales[(size_t)t * G + g] = s;
             for (k = 0; k < group; ++k)
                 q[(size_t)t * K + (size_t)g * group + k] =
-                    orc_e4m3_encode((float)bf16_value(xg[k]) / s);
+                    orc_e4m3_encode(((float)bf16_value(xg[k]) * rw) / s);
         }
     }
+}
+
+void orc_quant_fp8_group(const uint16_t *x, int M, int K, int group,
+                         uint8_t *q, float *scales)
+{
+    orc_quant_fp8_group_w(x, NULL, M, K, group, q, scales);
 }
 
 /* w (R, C) bf16 -> q (R, C) e4m3, scales (R / block, C / block) fp32; one
@@ -527,24 +579,33 @@ static void expert_row(const orc_weights *W, int e, const double *x,
     }
 }
 
-/* Input row t of x (M, K) bf16, dequantised as the experts see it: as is for
- * bf16, or through Q1 (groups of 128) for FP8. */
-static void input_row(int dtype, const uint16_t *x, int t, int K, double *xr)
+/* Input row t of x (M, K) bf16 times `scale`, as the experts see it: the
+ * product as is for bf16, or through Q1 (groups of 128, with the product
+ * formed in fp32) for FP8.  scale is 1 except with
+ * apply_router_weight_on_input. */
+static void input_row_scaled(int dtype, const uint16_t *x, int t, int K,
+                             double scale, double *xr)
 {
     int k;
     const uint16_t *row = x + (size_t)t * K;
     if (dtype == ORC_BF16) {
         for (k = 0; k < K; ++k)
-            xr[k] = bf16_value(row[k]);
+            xr[k] = bf16_value(row[k]) * scale;
     } else {
+        float fs = (float)scale;
         uint8_t *q = (uint8_t *)malloc((size_t)K);
         float *s = (float *)malloc(sizeof(float) * (size_t)(K / 128));
-        orc_quant_fp8_group(row, 1, K, 128, q, s);
+        orc_quant_fp8_group_w(row, &fs, 1, K, 128, q, s);
         for (k = 0; k < K; ++k)
             xr[k] = orc_e4m3_value(q[k]) * (double)s[k / 128];
         free(q);
         free(s);
     }
+}
+
+static void input_row(int dtype, const uint16_t *x, int t, int K, double *xr)
+{
+    input_row_scaled(dtype, x, t, K, 1.0, xr);
 }
 
 /* h and y of one expert on one row of x (bf16 bits); for checking the two
@@ -573,20 +634,29 @@ void orc_expert_row(int dtype, const uint16_t *x, int t, int e, int E, int N,
 /* tokens (n_tok) lists which tokens to compute (NULL: all M, n_tok = M);
  * out (n_tok, K), ids_out (n_tok, topk), w_out (n_tok, topk) fp64.
  * Tokens are independent, so a listed subset is computed exactly as it
- * would be in a full run.  nthreads <= 0: the OpenMP default. */
-void orc_moe_forward(const uint16_t *x, const float *logits, const float *bias,
-                     int M, int K, int N, int E, int topk, int score_fn,
-                     int n_groups, int topk_groups, int renorm, int dtype,
-                     int requant_h, const void *const *w1,
-                     const float *const *w1s, const void *const *w2,
-                     const float *const *w2s, const int32_t *tokens,
-                     int n_tok, int32_t *ids_out, double *w_out, double *out,
-                     int nthreads)
+ * would be in a full run.  nthreads <= 0: the OpenMP default.
+ * E is the number of routed (global) experts, the width of the logits.
+ * expert_map (E) or NULL, E_local: the weights hold E_local experts; a pair
+ * whose expert maps to -1 is not computed on this shard and adds nothing
+ * (FusedMoEModularKernel.forward's expert_map).  weight_on_input
+ * (apply_router_weight_on_input, meant for topk == 1): the router weight
+ * multiplies the expert's input instead of its output,
+ *   out[t] = sum_j expert(w[t,j] * x[t]). */
+void orc_moe_forward_ep(const uint16_t *x, const float *logits,
+                        const float *bias, int M, int K, int N, int E,
+                        int topk, int score_fn, int n_groups, int topk_groups,
+                        int renorm, int dtype, int requant_h,
+                        const int32_t *expert_map, int E_local,
+                        int weight_on_input, const void *const *w1,
+                        const float *const *w1s, const void *const *w2,
+                        const float *const *w2s, const int32_t *tokens,
+                        int n_tok, int32_t *ids_out, double *w_out,
+                        double *out, int nthreads)
 {
     int i;
     orc_weights W;
     fill_e4m3_table();
-    W.dtype = dtype; W.E = E; W.N = N; W.K = K;
+    W.dtype = dtype; W.E = E_local; W.N = N; W.K = K;
     W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
     if (!tokens)
         n_tok = M;
@@ -606,18 +676,45 @@ void orc_moe_forward(const uint16_t *x, const float *logits, const float *bias,
         double *o = out + (size_t)i * K;
         orc_route(logits + (size_t)t * E, bias, 1, E, topk, score_fn, n_groups,
                   topk_groups, renorm, ids, w, NULL);
-        input_row(dtype, x, t, K, xr);
+        if (!weight_on_input)
+            input_row(dtype, x, t, K, xr);
         for (k = 0; k < K; ++k)
             o[k] = 0.0;
         for (j = 0; j < topk; ++j) {
-            expert_row(&W, ids[j], xr, requant_h, h, y);
-            for (k = 0; k < K; ++k)
-                o[k] += w[j] * y[k];
+            int l = local_expert(ids[j], E, expert_map, E_local);
+            if (l < 0)
+                continue;
+            if (weight_on_input) {
+                /* the weight as the kernels hold it: fp32 */
+                input_row_scaled(dtype, x, t, K, (double)(float)w[j], xr);
+                expert_row(&W, l, xr, requant_h, h, y);
+                for (k = 0; k < K; ++k)
+                    o[k] += y[k];
+            } else {
+                expert_row(&W, l, xr, requant_h, h, y);
+                for (k = 0; k < K; ++k)
+                    o[k] += w[j] * y[k];
+            }
         }
         free(xr);
         free(h);
         free(y);
     }
+}
+
+void orc_moe_forward(const uint16_t *x, const float *logits, const float *bias,
+                     int M, int K, int N, int E, int topk, int score_fn,
+                     int n_groups, int topk_groups, int renorm, int dtype,
+                     int requant_h, const void *const *w1,
+                     const float *const *w1s, const void *const *w2,
+                     const float *const *w2s, const int32_t *tokens,
+                     int n_tok, int32_t *ids_out, double *w_out, double *out,
+                     int nthreads)
+{
+    orc_moe_forward_ep(x, logits, bias, M, K, N, E, topk, score_fn, n_groups,
+                       topk_groups, renorm, dtype, requant_h, NULL, E, 0, w1,
+                       w1s, w2, w2s, tokens, n_tok, ids_out, w_out, out,
+                       nthreads);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -336,3 +336,90 @@ def test_batched_equals_standard_on_the_same_routing(orc):
                 np.testing.assert_allclose(yb[e, r], out[srt[off[e] + r]], rtol=1e-12, atol=1e-14)
             else:
                 assert np.all(np.isnan(yb[e, r]))
+
+
+# ------------------------------------------- expert_map / weight on input ----
+
+def _swiglu_np(x, w1, w2, N):
+    return (_silu(x @ w1[:N].T) * (x @ w1[N:].T)) @ w2.T
+
+
+def test_count_align_with_expert_map_match_numpy(orc):
+    rng = np.random.default_rng(30)
+    Eg, El, P = 16, 5, 3000
+    emap = np.full(Eg, -1, np.int32)
+    local_globals = np.array([2, 3, 7, 11, 15])
+    emap[local_globals] = np.arange(El)
+    ids = rng.integers(0, Eg, P).astype(np.int32)
+    ids[:3] = [-1, 16, 99]  # invalid ids
+    c, bad = orc.count(ids, Eg, emap, El)
+    off, srt, inv = orc.align(ids, Eg, emap, El)
+    ok = (ids >= 0) & (ids < Eg)
+    lid = np.where(ok, emap[np.clip(ids, 0, Eg - 1)], -1)
+    assert bad == 3
+    assert np.array_equal(c, np.bincount(lid[lid >= 0], minlength=El))
+    keep = np.flatnonzero(lid >= 0)
+    assert np.array_equal(srt, keep[np.argsort(lid[keep], kind="stable")])
+    assert np.all(inv[lid < 0] == -1)
+    assert np.array_equal(srt[inv[keep]], keep)
+    # the identity map is the same as no map
+    ident = np.arange(Eg, dtype=np.int32)
+    assert np.array_equal(orc.align(ids, Eg, ident, Eg)[1], orc.align(ids, Eg)[1])
+
+
+def test_forward_with_expert_map_is_the_local_part_of_the_layer(orc):
+    """A shard holding experts {1, 4, 6} of 8: its output is the weighted sum
+    over the routed slots whose expert is local (numpy per-expert loop)."""
+    cfg = WL.MoEConfig("ep", M=37, K=128, N=64, E=8, topk=3, seed=31)
+    d = WL.make_inputs(cfg)
+    local = [1, 4, 6]
+    emap = np.full(8, -1, np.int32)
+    emap[local] = np.arange(3)
+    Wl = orc.Weights(orc.BF16, _bits(d["w1"][local]), _bits(d["w2"][local]))
+    out, ids, w = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 3,
+                                  orc.SOFTMAX, Wl, expert_map=emap)
+    x = d["x"].double().numpy()
+    ref = np.zeros_like(out)
+    for g in local:
+        t, j = np.nonzero(ids == g)
+        y = _swiglu_np(x[t], d["w1"][g].double().numpy(), d["w2"][g].double().numpy(), cfg.N)
+        np.add.at(ref, t, w[t, j][:, None] * y)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    # every expert local through the identity map: the plain layer
+    Wg = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"]))
+    full, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 3, orc.SOFTMAX, Wg)
+    same, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 3, orc.SOFTMAX, Wg,
+                                 expert_map=np.arange(8, dtype=np.int32))
+    np.testing.assert_array_equal(full, same)
+
+
+def test_weight_on_input_scales_the_expert_input(orc):
+    """apply_router_weight_on_input, top-1, unrenormalised softmax weight p:
+    out[t] = expert(p * x[t]) (numpy), which differs from p * expert(x[t])."""
+    cfg = WL.MoEConfig("woi", M=29, K=128, N=64, E=4, topk=1, renorm=False, seed=32)
+    d = WL.make_inputs(cfg)
+    W = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"]))
+    out, ids, w = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1,
+                                  orc.SOFTMAX, W, renorm=False, weight_on_input=True)
+    assert np.all(w < 1.0)
+    x = d["x"].double().numpy()
+    ref = np.zeros_like(out)
+    for e in range(4):
+        t = np.flatnonzero(ids[:, 0] == e)
+        xin = x[t] * w[t, 0].astype(np.float32).astype(np.float64)[:, None]
+        ref[t] = _swiglu_np(xin, d["w1"][e].double().numpy(), d["w2"][e].double().numpy(), cfg.N)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    plain, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1,
+                                  orc.SOFTMAX, W, renorm=False)
+    assert np.abs(plain - out).max() > 1e-3 * np.abs(out).max()
+
+
+def test_quant_with_row_weights_is_cast_of_the_fp32_product(orc):
+    g = torch.Generator().manual_seed(33)
+    x = torch.randn(17, 256, generator=g).to(torch.bfloat16)
+    rw = torch.rand(17, generator=g).to(torch.float32)
+    q, s = orc.quant_fp8_group(_bits(x), row_weights=rw.numpy())
+    v = (x.float() * rw[:, None]).view(17, 2, 128)
+    assert np.array_equal(s, (v.abs().amax(-1) / 448.0).numpy())
+    ref = (v / torch.from_numpy(s).view(17, 2, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(q, ref.view(17, 256).numpy())
