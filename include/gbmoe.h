@@ -80,6 +80,7 @@ int gbmoe_last_cuda_error(void);
 
 /* Bytes of workspace a call needs.  `which` is a GBMOE_WS_* value; M_or_T is
  * M for the Standard calls and T (max tokens per expert) for the batched one.
+ * E is the number of local experts (the first dimension of w1 / w2).
  * Returns 0 for invalid arguments. */
 size_t moe_workspace_size(int which, int M_or_T, int E, int N, int K, int topk,
                           int dtype);
@@ -109,46 +110,60 @@ gbmoe_status_t moe_topk_route(const float *logits, const float *bias, int M,
                               int32_t *topk_ids, float *topk_weights,
                               int32_t *err_word, gbmoe_stream_t stream);
 
+/* Expert ids and the expert-parallel map.  The router picks among E_global
+ * (routed, global) experts; this shard holds the E local experts of w1 / w2.
+ * expert_map (E_global) int32, as the expert_map argument of
+ * FusedMoEModularKernel.forward: expert_map[g] is the local id of global
+ * expert g, or -1 when g is not on this shard -- its (token, slot) pairs are
+ * not computed here and add nothing to the output.  expert_map NULL: ids are
+ * local already and E_global must equal E.  A routed id outside
+ * [0, E_global), or mapped outside [-1, E), is invalid: it is skipped and
+ * sets GBMOE_ERR_BAD_EXPERT_ID. */
+
 /* count_expert_num_tokens as named in modular_kernel.py
  * (FusedMoEModularKernel._maybe_chunk_fused_experts) and the
  * ExpertTokensMetadata.expert_num_tokens it fills:
- * counts[e] = #{p < M*topk : topk_ids[p] == e}, computed on the device.
- * Ids outside [0, E) are skipped and set GBMOE_ERR_BAD_EXPERT_ID.
- * topk_ids (M, topk) int32; counts (E) int32 out (overwritten). */
+ * counts[l] = #{p < M*topk : topk_ids[p] maps to local expert l}, computed on
+ * the device.  topk_ids (M, topk) int32; counts (E) int32 out (overwritten). */
 gbmoe_status_t moe_count_expert_tokens(const int32_t *topk_ids, int M,
-                                       int topk, int E, int32_t *counts,
-                                       int32_t *err_word,
+                                       int topk, int E_global,
+                                       const int32_t *expert_map, int E,
+                                       int32_t *counts, int32_t *err_word,
                                        gbmoe_stream_t stream);
 
 /* The "Permute" of [Permute-Experts-Unpermute]: a stable counting sort of the
- * P = M*topk (token, slot) pairs by expert.  Pair p = t*topk + j.
- *   counts (E) int32 out, or NULL: counts[e] = #{p : topk_ids[p] == e}, the
- *     ExpertTokensMetadata.expert_num_tokens of the pages;
- *   offsets (E+1) int32 out: offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e];
- *   sorted_pair_ids (M*topk) int32 out: sorted_pair_ids[offsets[e] + r] is the
- *     r-th pair, in ascending p, routed to expert e (entries at and beyond
- *     offsets[E] are left unwritten);
+ * P = M*topk (token, slot) pairs by local expert.  Pair p = t*topk + j.
+ *   counts (E) int32 out, or NULL: counts[l] as in moe_count_expert_tokens,
+ *     the ExpertTokensMetadata.expert_num_tokens of the pages;
+ *   offsets (E+1) int32 out: offsets[0] = 0, offsets[l+1] = offsets[l] + counts[l];
+ *   sorted_pair_ids (M*topk) int32 out: sorted_pair_ids[offsets[l] + r] is the
+ *     r-th pair, in ascending p, routed to local expert l (entries at and
+ *     beyond offsets[E] are left unwritten);
  *   inv (M*topk) int32 out: inv[p] = the position of p in sorted_pair_ids,
- *     -1 for a pair whose id is outside [0, E) (which also sets
- *     GBMOE_ERR_BAD_EXPERT_ID).
+ *     -1 for a pair that is not computed here (invalid id, or an expert that
+ *     is not local).
  * ws: moe_workspace_size(GBMOE_WS_ALIGN, M, E, 0, 0, topk, 0) bytes (one
  * histogram per chunk of 2048 pairs).  err_word may be NULL. */
 gbmoe_status_t moe_align_permute(const int32_t *topk_ids, int M, int topk,
-                                 int E, int32_t *counts, int32_t *offsets,
+                                 int E_global, const int32_t *expert_map, int E,
+                                 int32_t *counts, int32_t *offsets,
                                  int32_t *sorted_pair_ids, int32_t *inv,
                                  void *ws, size_t ws_bytes, int32_t *err_word,
                                  gbmoe_stream_t stream);
 
 /* [Quantize-Prepare] (FusedMoEPrepareAndFinalize.prepare quantises the
  * activations before the experts run), per-token-group FP8:
- * for each token t and each group g of `group` consecutive columns,
- *   s = max(max_k |x[t,k]|, 1e-12) / 448   (fp32, IEEE division)
- *   q[t,k] = e4m3(x[t,k] / s)               (round to nearest even, saturating at 448)
- * x (M, K) bf16; q (M, K) e4m3 out; scales (M, K/group) fp32 out.
- * group must be 128 and K % 128 == 0. */
-gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, int M, int K, int group,
-                                   uint8_t *q, float *scales,
-                                   gbmoe_stream_t stream);
+ * for each token t and each group g of `group` consecutive columns, with
+ * v[t,k] = x[t,k] * row_weights[t] (an fp32 product; v = x when row_weights
+ * is NULL -- the weights are given with apply_router_weight_on_input, when
+ * prepare applies the router weight to the activations):
+ *   s = max(max_k |v[t,k]|, 1e-12) / 448   (fp32, IEEE division)
+ *   q[t,k] = e4m3(v[t,k] / s)               (round to nearest even, saturating at 448)
+ * x (M, K) bf16; row_weights (M) fp32 or NULL; q (M, K) e4m3 out;
+ * scales (M, K/group) fp32 out.  group must be 128 and K % 128 == 0. */
+gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, const float *row_weights,
+                                   int M, int K, int group, uint8_t *q,
+                                   float *scales, gbmoe_stream_t stream);
 
 /* The same quantiser over block x block tiles of a weight matrix, for
  * preparing FP8 expert weights (not part of the timed layer):
@@ -163,14 +178,19 @@ gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
 /* The data movement of the "Permute": the rows of the first GEMM in sorted
  * order, A[i] = x[sorted_pair_ids[i] / topk] for i < offsets[E] (rows at and
  * beyond offsets[E] are left unwritten).
- * dtype GBMOE_BF16: x (M, K) bf16 -> A (M*topk, K) bf16; scales unused.
+ * dtype GBMOE_BF16: x (M, K) bf16 -> A (M*topk, K) bf16; scales unused;
+ *   row_weights (M*topk) fp32 or NULL: with apply_router_weight_on_input,
+ *   A[i] = bf16(x[t] * row_weights[p]) with p = sorted_pair_ids[i].
  * dtype GBMOE_FP8_E4M3: x (M, K) e4m3 with x_scales (M, K/128) fp32 ->
  *   A (M*topk, K) e4m3 with A_scales stored GROUP-MAJOR: A_scales[g * ld + i]
  *   is the scale of row i, K block g, with ld = M*topk rounded up to a
  *   multiple of 4 (a (K/128, ld) array), so that the scales of one K block
  *   of consecutive rows are contiguous for the GEMM's TMA loads.
+ *   row_weights must be NULL (the FP8 rows take the weight in
+ *   moe_quant_fp8_group, before the codes are chosen).
  * K % 128 == 0; x and A 16-byte aligned. */
 gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
+                                const float *row_weights,
                                 const int32_t *sorted_pair_ids,
                                 const int32_t *offsets, int M, int topk, int E,
                                 int K, int dtype, void *A, float *A_scales,
@@ -209,7 +229,8 @@ gbmoe_status_t moe_grouped_gemm_gate_up_silu(
  *   y_slot[p, k] = topk_weights[p] * (H[i, :] . w2[e, k, :])      (k < K)
  * y_slot (M, topk, K) bf16 is the fused_expert_output of
  * FusedMoEPrepareAndFinalize.finalize, already weighted; its rows of pairs
- * whose id is invalid are not written.
+ * that are not computed here are not written.  topk_weights NULL: no weight
+ * (apply_router_weight_on_input applied it to the input instead).
  * dtype GBMOE_BF16: H (M*topk, N) bf16, w2 (E, K, N) bf16.
  * dtype GBMOE_FP8_E4M3: H e4m3 + group-major H_scales (N/128, ld), ld =
  *   M*topk rounded up to 4 (as written by the gate/up call); w2 e4m3 +
@@ -253,22 +274,28 @@ gbmoe_status_t moe_batched_masked_experts(
     size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream);
 
 /* The whole layer in the Standard format, FusedMoEModularKernel.forward
- * without expert_map / apply_router_weight_on_input / shared experts:
- * route -> count -> align/permute -> [quantise] -> gate/up GEMM + SiLU*mul
- * -> down GEMM + weight -> ordered reduce, all on `stream`.
- * x (M, K) bf16; logits (M, E) fp32; bias (E) fp32 or NULL;
- * dtype GBMOE_BF16: w1/w2 bf16, scales NULL;
+ * without shared experts: route -> count -> align/permute -> [quantise] ->
+ * gate/up GEMM + SiLU*mul -> down GEMM + weight -> ordered reduce, all on
+ * `stream`.
+ * x (M, K) bf16; logits (M, E_global) fp32; bias (E_global) fp32 or NULL;
+ * expert_map (E_global) or NULL and E local experts, as described above
+ * moe_count_expert_tokens (the output then holds the local experts' part);
+ * apply_router_weight_on_input != 0 (topk must be 1): the router weight
+ * multiplies the activations (before FP8 quantisation) instead of the expert
+ * output, out[t] = expert(w[t] * x[t]);
+ * dtype GBMOE_BF16: w1 (E, 2N, K) / w2 (E, K, N) bf16, scales NULL;
  * dtype GBMOE_FP8_E4M3: w1/w2 e4m3 with their block scales; the activations
  *   are quantised per token in groups of 128 and H is requantised.
  * out (M, K) bf16.  topk_ids / topk_weights (M, topk) may be NULL; when given
- * they receive the router's output.
+ * they receive the router's output (global ids).
  * ws: moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype) bytes.
  * err_word may be NULL. */
 gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
-                           const float *bias, int M, int K, int N, int E,
-                           int topk, int score_fn, int n_groups,
-                           int topk_groups, int renormalize, int dtype,
-                           const void *w1, const float *w1_scales,
+                           const float *bias, int M, int K, int N, int E_global,
+                           const int32_t *expert_map, int E, int topk,
+                           int score_fn, int n_groups, int topk_groups,
+                           int renormalize, int apply_router_weight_on_input,
+                           int dtype, const void *w1, const float *w1_scales,
                            const void *w2, const float *w2_scales,
                            uint16_t *out, int32_t *topk_ids,
                            float *topk_weights, void *ws, size_t ws_bytes,

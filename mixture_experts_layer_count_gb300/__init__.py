@@ -45,12 +45,12 @@ _SIGS = {
     "gbmoe_last_cuda_error": (_I, []),
     "moe_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
-    "moe_count_expert_tokens": (_I, [_P, _I, _I, _I, _P, _P, _P]),
-    "moe_align_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
+    "moe_count_expert_tokens": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_align_permute": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
     "moe_align_permute_no_ws": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
-    "moe_quant_fp8_group": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_quant_fp8_group": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
-    "moe_permute_rows": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_permute_rows": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm_gate_up_silu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                                            _I, _P, _P, _P, _P]),
     "moe_grouped_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
@@ -58,8 +58,8 @@ _SIGS = {
     "moe_unpermute_weighted_reduce": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_batched_masked_experts": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                         _I, _P, _P, _Z, _P, _P]),
-    "moe_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
-                         _P, _P, _P, _P, _P, _P, _Z, _P, _P]),
+    "moe_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
+                         _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P]),
 }
 
 
@@ -118,18 +118,24 @@ def moe_topk_route(logits, bias, topk, score_fn, n_groups, topk_groups,
         _stream(stream)))
 
 
-def moe_count_expert_tokens(topk_ids, E, counts, err_word=None, stream=None):
+def moe_count_expert_tokens(topk_ids, E, counts, err_word=None, stream=None,
+                            expert_map=None, E_global=None):
+    """counts (E) of the local experts; with expert_map (E_global) the ids are
+    global and mapped (-1: not local)."""
     M, topk = topk_ids.shape
+    Eg = E if E_global is None else E_global
     _check("moe_count_expert_tokens", load().moe_count_expert_tokens(
-        _ptr(topk_ids), M, topk, E, _ptr(counts), _ptr(err_word), _stream(stream)))
+        _ptr(topk_ids), M, topk, Eg, _ptr(expert_map), E, _ptr(counts),
+        _ptr(err_word), _stream(stream)))
 
 
 def moe_align_permute(topk_ids, E, counts, offsets, sorted_pair_ids, inv, ws,
-                      err_word=None, stream=None):
+                      err_word=None, stream=None, expert_map=None, E_global=None):
     M, topk = topk_ids.shape
+    Eg = E if E_global is None else E_global
     _check("moe_align_permute", load().moe_align_permute(
-        _ptr(topk_ids), M, topk, E, _ptr(counts), _ptr(offsets),
-        _ptr(sorted_pair_ids), _ptr(inv), _ptr(ws),
+        _ptr(topk_ids), M, topk, Eg, _ptr(expert_map), E, _ptr(counts),
+        _ptr(offsets), _ptr(sorted_pair_ids), _ptr(inv), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _ptr(err_word),
         _stream(stream)))
 
@@ -146,10 +152,11 @@ def moe_align_permute_no_ws(topk_ids, E, counts, offsets, sorted_pair_ids, inv,
         _ptr(sorted_pair_ids), _ptr(inv), _ptr(err_word), _stream(stream)))
 
 
-def moe_quant_fp8_group(x, q, scales, group=128, stream=None):
+def moe_quant_fp8_group(x, q, scales, group=128, stream=None, row_weights=None):
     M, K = x.shape
     _check("moe_quant_fp8_group", load().moe_quant_fp8_group(
-        _ptr(x), M, K, group, _ptr(q), _ptr(scales), _stream(stream)))
+        _ptr(x), _ptr(row_weights), M, K, group, _ptr(q), _ptr(scales),
+        _stream(stream)))
 
 
 def moe_quant_fp8_block(w, q, scales, block=128, stream=None):
@@ -160,11 +167,12 @@ def moe_quant_fp8_block(w, q, scales, block=128, stream=None):
 
 
 def moe_permute_rows(x, x_scales, sorted_pair_ids, offsets, topk, E, dtype, A,
-                     A_scales=None, stream=None):
+                     A_scales=None, stream=None, row_weights=None):
     M, K = x.shape
     _check("moe_permute_rows", load().moe_permute_rows(
-        _ptr(x), _ptr(x_scales), _ptr(sorted_pair_ids), _ptr(offsets), M, topk, E,
-        K, dtype, _ptr(A), _ptr(A_scales), _stream(stream)))
+        _ptr(x), _ptr(x_scales), _ptr(row_weights), _ptr(sorted_pair_ids),
+        _ptr(offsets), M, topk, E, K, dtype, _ptr(A), _ptr(A_scales),
+        _stream(stream)))
 
 
 def moe_grouped_gemm_gate_up_silu(A, A_scales, offsets, M, topk, E, N, K, w1,
@@ -203,14 +211,20 @@ def moe_batched_masked_experts(x_b, expert_num_tokens, N, w1, w2, y_b, ws,
 
 def moe_forward(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
                 renormalize, dtype, w1, w1_scales, w2, w2_scales, out, ws,
-                topk_ids=None, topk_weights=None, err_word=None, stream=None):
+                topk_ids=None, topk_weights=None, err_word=None, stream=None,
+                expert_map=None, apply_router_weight_on_input=False):
+    """The whole Standard layer.  E is the number of local experts (w1.shape[0]);
+    the router picks among logits.shape[1] experts, mapped to local ones by
+    expert_map when given."""
     M, K = x.shape
+    E_global = logits.shape[1]
     _check("moe_forward", load().moe_forward(
-        _ptr(x), _ptr(logits), _ptr(bias), M, K, N, E, topk, score_fn, n_groups,
-        topk_groups, int(renormalize), dtype, _ptr(w1), _ptr(w1_scales),
-        _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids),
-        _ptr(topk_weights), _ptr(ws), ws.numel() * ws.element_size(),
-        _ptr(err_word), _stream(stream)))
+        _ptr(x), _ptr(logits), _ptr(bias), M, K, N, E_global, _ptr(expert_map), E,
+        topk, score_fn, n_groups, topk_groups, int(renormalize),
+        int(apply_router_weight_on_input), dtype, _ptr(w1), _ptr(w1_scales),
+        _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
+        _stream(stream)))
 
 
 def workspace(which, M_or_T, E, N, K, topk, dtype, device="cuda"):

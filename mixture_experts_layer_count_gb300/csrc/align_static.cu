@@ -64,6 +64,7 @@ extern "C" gbmoe_status_t moe_align_permute_no_ws(const int32_t *topk_ids, int M
   int32_t *hist = nullptr;
   gbmoe_status_t st = hist_address(&hist);
   if (st != GBMOE_OK) return st;
-  return status_from_cuda(launch_align(topk_ids, P, E, counts, offsets, sorted_pair_ids, inv,
-                                       hist, err_word, (cudaStream_t)stream));
+  return status_from_cuda(launch_align(topk_ids, P, E, nullptr, E, counts, offsets,
+                                       sorted_pair_ids, inv, hist, err_word,
+                                       (cudaStream_t)stream));
 }

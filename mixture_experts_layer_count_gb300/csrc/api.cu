@@ -104,6 +104,13 @@ ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dty
   return w;
 }
 
+// expert_map NULL: the routed ids are local ids (E_global == E); otherwise
+// E_global routed experts map to E local ones
+bool map_args_ok(int E_global, const int32_t *expert_map, int E) {
+  if (E_global < 1) return false;
+  return expert_map ? E_global <= (1 << 24) : E_global == E;
+}
+
 bool route_args_ok(int M, int E, int topk, int score_fn, const float *bias,
                    int n_groups, int topk_groups) {
   if (M < 0 || E < 1 || E > kMaxExperts || topk < 1 || topk > kMaxTopk || topk > E)
@@ -143,11 +150,13 @@ gbmoe_status_t gate_up_impl(const void *A, const float *A_scales,
 }
 
 gbmoe_status_t permute_impl(const void *x, const float *x_scales,
-                            const int32_t *sorted, const int32_t *offsets, int M,
-                            int topk, int E, int K, int dtype, void *A,
-                            float *A_scales, int num_sms, cudaStream_t s) {
+                            const float *row_weights, const int32_t *sorted,
+                            const int32_t *offsets, int M, int topk, int E, int K,
+                            int dtype, void *A, float *A_scales, int num_sms,
+                            cudaStream_t s) {
   const bool fp8 = dtype == GBMOE_FP8_E4M3;
   return from_cuda(launch_gather_rows(x, fp8 ? x_scales : nullptr,
+                                      fp8 ? nullptr : row_weights,
                                       (int)(K * elem_bytes(dtype)), K / 128, sorted,
                                       offsets + E, M * topk, topk, A,
                                       fp8 ? A_scales : nullptr,
@@ -252,10 +261,12 @@ gbmoe_status_t moe_topk_route(const float *logits, const float *bias, int M,
 }
 
 gbmoe_status_t moe_count_expert_tokens(const int32_t *topk_ids, int M,
-                                       int topk, int E, int32_t *counts,
-                                       int32_t *err_word,
+                                       int topk, int E_global,
+                                       const int32_t *expert_map, int E,
+                                       int32_t *counts, int32_t *err_word,
                                        gbmoe_stream_t stream) {
   if (M < 0 || topk < 1 || E < 1 || E > kMaxExperts || !counts) return GBMOE_INVALID_ARG;
+  if (!map_args_ok(E_global, expert_map, E)) return GBMOE_INVALID_ARG;
   if (M > 0 && !topk_ids) return GBMOE_INVALID_ARG;
   if ((size_t)M * topk > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
   int sms;
@@ -263,30 +274,32 @@ gbmoe_status_t moe_count_expert_tokens(const int32_t *topk_ids, int M,
   if (st != GBMOE_OK) return st;
   if (M == 0)
     return from_cuda(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, (cudaStream_t)stream));
-  return from_cuda(launch_count(topk_ids, M * topk, E, counts, err_word, sms,
-                                (cudaStream_t)stream));
+  return from_cuda(launch_count(topk_ids, M * topk, E_global, expert_map, E, counts,
+                                err_word, sms, (cudaStream_t)stream));
 }
 
 gbmoe_status_t moe_align_permute(const int32_t *topk_ids, int M, int topk,
-                                 int E, int32_t *counts, int32_t *offsets,
+                                 int E_global, const int32_t *expert_map, int E,
+                                 int32_t *counts, int32_t *offsets,
                                  int32_t *sorted_pair_ids, int32_t *inv,
                                  void *ws, size_t ws_bytes, int32_t *err_word,
                                  gbmoe_stream_t stream) {
   if (M < 0 || topk < 1 || E < 1 || E > kMaxExperts || !offsets) return GBMOE_INVALID_ARG;
+  if (!map_args_ok(E_global, expert_map, E)) return GBMOE_INVALID_ARG;
   if ((size_t)M * topk > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
   if (M > 0 && (!topk_ids || !sorted_pair_ids || !inv || !ws)) return GBMOE_INVALID_ARG;
   if (ws_bytes < moe_workspace_size(GBMOE_WS_ALIGN, M, E, 0, 0, topk, 0)) return GBMOE_INVALID_ARG;
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK) return st;
-  return from_cuda(launch_align(topk_ids, M * topk, E, counts, offsets,
+  return from_cuda(launch_align(topk_ids, M * topk, E_global, expert_map, E, counts, offsets,
                                 sorted_pair_ids, inv, static_cast<int32_t *>(ws),
                                 err_word, (cudaStream_t)stream));
 }
 
-gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, int M, int K, int group,
-                                   uint8_t *q, float *scales,
-                                   gbmoe_stream_t stream) {
+gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, const float *row_weights,
+                                   int M, int K, int group, uint8_t *q,
+                                   float *scales, gbmoe_stream_t stream) {
   if (M < 0 || K < 128 || K % 128 != 0 || group != 128) return GBMOE_INVALID_ARG;
   if (M > 0 && (!x || !q || !scales || !aligned16(x) || !aligned16(q)))
     return GBMOE_INVALID_ARG;
@@ -294,7 +307,7 @@ gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, int M, int K, int group,
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK) return st;
   if (M == 0) return GBMOE_OK;
-  return from_cuda(launch_quant_group(x, M, K, q, scales, (cudaStream_t)stream));
+  return from_cuda(launch_quant_group(x, row_weights, M, K, q, scales, (cudaStream_t)stream));
 }
 
 gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
@@ -313,6 +326,7 @@ gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
 }
 
 gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
+                                const float *row_weights,
                                 const int32_t *sorted_pair_ids,
                                 const int32_t *offsets, int M, int topk, int E,
                                 int K, int dtype, void *A, float *A_scales,
@@ -327,11 +341,13 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
       return GBMOE_INVALID_ARG;
     if (fp8 && (!x_scales || !A_scales)) return GBMOE_INVALID_ARG;
   }
+  // FP8 rows take their router weight in moe_quant_fp8_group, before the codes
+  if (fp8 && row_weights) return GBMOE_INVALID_ARG;
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK || M == 0) return st;
-  return permute_impl(x, x_scales, sorted_pair_ids, offsets, M, topk, E, K, dtype, A,
-                      A_scales, sms, (cudaStream_t)stream);
+  return permute_impl(x, x_scales, row_weights, sorted_pair_ids, offsets, M, topk, E, K,
+                      dtype, A, A_scales, sms, (cudaStream_t)stream);
 }
 
 gbmoe_status_t moe_grouped_gemm_gate_up_silu(
@@ -366,8 +382,7 @@ gbmoe_status_t moe_grouped_gemm_down(
     return device_info(&sms);
   }
   const bool fp8 = dtype == GBMOE_FP8_E4M3;
-  if (!H || !sorted_pair_ids || !offsets || !topk_weights || !w2 || !y_slot)
-    return GBMOE_INVALID_ARG;
+  if (!H || !sorted_pair_ids || !offsets || !w2 || !y_slot) return GBMOE_INVALID_ARG;
   if (fp8 && (!H_scales || !w2_scales)) return GBMOE_INVALID_ARG;
   if (!aligned16(H) || !aligned16(w2) || !aligned16(y_slot)) return GBMOE_INVALID_ARG;
   int sms;
@@ -440,18 +455,21 @@ gbmoe_status_t moe_batched_masked_experts(
 }
 
 gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
-                           const float *bias, int M, int K, int N, int E,
-                           int topk, int score_fn, int n_groups,
-                           int topk_groups, int renormalize, int dtype,
-                           const void *w1, const float *w1_scales,
+                           const float *bias, int M, int K, int N, int E_global,
+                           const int32_t *expert_map, int E, int topk,
+                           int score_fn, int n_groups, int topk_groups,
+                           int renormalize, int apply_router_weight_on_input,
+                           int dtype, const void *w1, const float *w1_scales,
                            const void *w2, const float *w2_scales,
                            uint16_t *out, int32_t *topk_ids,
                            float *topk_weights, void *ws, size_t ws_bytes,
                            int32_t *err_word, gbmoe_stream_t stream) {
   if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
   if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
-  if (!route_args_ok(M, E, topk, score_fn, bias, n_groups, topk_groups))
+  if (!map_args_ok(E_global, expert_map, E)) return GBMOE_INVALID_ARG;
+  if (!route_args_ok(M, E_global, topk, score_fn, bias, n_groups, topk_groups))
     return GBMOE_INVALID_ARG;
+  if (apply_router_weight_on_input && topk != 1) return GBMOE_INVALID_ARG;
   const bool fp8 = dtype == GBMOE_FP8_E4M3;
   if (M > 0) {
     if (!x || !logits || !w1 || !w2 || !out || !ws) return GBMOE_INVALID_ARG;
@@ -471,29 +489,32 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   int32_t *ids = topk_ids ? topk_ids : w.ids;
   float *wts = topk_weights ? topk_weights : w.weights;
   const int P = M * topk;
-  cudaError_t ce = launch_route(logits, bias, M, E, topk, score_fn,
+  cudaError_t ce = launch_route(logits, bias, M, E_global, topk, score_fn,
                                 n_groups < 1 ? 1 : n_groups, topk_groups, renormalize,
                                 ids, wts, s);
   if (ce != cudaSuccess) return from_cuda(ce);
-  ce = launch_align(ids, P, E, w.counts, w.offsets, w.sorted, w.inv, w.chunk_hist,
-                    err_word, s);
+  ce = launch_align(ids, P, E_global, expert_map, E, w.counts, w.offsets, w.sorted, w.inv,
+                    w.chunk_hist, err_word, s);
   if (ce != cudaSuccess) return from_cuda(ce);
+  // apply_router_weight_on_input (top-1): the weight scales the activations
+  // (before the FP8 codes are chosen) and not the expert output
+  const float *in_w = apply_router_weight_on_input ? wts : nullptr;
   const void *a_src = x;
   const float *a_src_s = nullptr;
   if (fp8) {
-    ce = launch_quant_group(x, M, K, w.xq, w.xs, s);
+    ce = launch_quant_group(x, in_w, M, K, w.xq, w.xs, s);
     if (ce != cudaSuccess) return from_cuda(ce);
     a_src = w.xq;
     a_src_s = w.xs;
   }
-  st = permute_impl(a_src, a_src_s, w.sorted, w.offsets, M, topk, E, K, dtype, w.A, w.As,
-                    sms, s);
+  st = permute_impl(a_src, a_src_s, fp8 ? nullptr : in_w, w.sorted, w.offsets, M, topk, E, K,
+                    dtype, w.A, w.As, sms, s);
   if (st != GBMOE_OK) return st;
   st = gate_up_impl(w.A, w.As, w.offsets, M, topk, E, N, K, w1, w1_scales, dtype, w.H,
                     w.Hs, err_word, sms, s);
   if (st != GBMOE_OK) return st;
-  st = down_impl(w.H, w.Hs, w.sorted, w.offsets, wts, M, topk, E, N, K, w2, w2_scales,
-                 dtype, w.y_slot, err_word, sms, s);
+  st = down_impl(w.H, w.Hs, w.sorted, w.offsets, in_w ? nullptr : wts, M, topk, E, N, K, w2,
+                 w2_scales, dtype, w.y_slot, err_word, sms, s);
   if (st != GBMOE_OK) return st;
   return from_cuda(launch_reduce(w.y_slot, w.inv, M, topk, K, out, sms, s));
 }

@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.sorted) {
             const int pair = p.sorted[arow];
             orow = (size_t)pair;
-            w = p.topk_w[pair];
+            w = p.topk_w ? p.topk_w[pair] : 1.0f;
           } else {
             orow = (size_t)arow;
           }

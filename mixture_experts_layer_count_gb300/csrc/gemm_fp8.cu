@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = nt * kBN + cq * 64;
         if (valid && col0 < p.K) {
           const int pair = p.sorted[arow];
-          const float w = p.topk_w[pair];
+          const float w = p.topk_w ? p.topk_w[pair] : 1.0f;
           uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
                                                  (size_t)pair * p.K + col0);
 #pragma unroll

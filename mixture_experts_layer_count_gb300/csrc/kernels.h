@@ -17,15 +17,20 @@ cudaError_t launch_route(const float *logits, const float *bias, int M, int E,
                          cudaStream_t s);
 
 // permute.cu
-cudaError_t launch_count(const int32_t *ids, int P, int E, int32_t *counts,
-                         int32_t *err, int num_sms, cudaStream_t s);
+// Eg: routed (global) experts; map (Eg) global -> local id or -1 (NULL:
+// identity, Eg == E); E: local experts
+cudaError_t launch_count(const int32_t *ids, int P, int Eg, const int32_t *map,
+                         int E, int32_t *counts, int32_t *err, int num_sms,
+                         cudaStream_t s);
 int align_num_chunks(int P);
-cudaError_t launch_align(const int32_t *ids, int P, int E, int32_t *counts,
-                         int32_t *offsets, int32_t *sorted, int32_t *inv,
-                         int32_t *chunk_hist, int32_t *err, cudaStream_t s);
-// out_s is group-major: (n_scales, out_s_ld)
-cudaError_t launch_gather_rows(const void *x, const float *xs, int row_bytes,
-                               int n_scales, const int32_t *sorted,
+cudaError_t launch_align(const int32_t *ids, int P, int Eg, const int32_t *map,
+                         int E, int32_t *counts, int32_t *offsets, int32_t *sorted,
+                         int32_t *inv, int32_t *chunk_hist, int32_t *err,
+                         cudaStream_t s);
+// out_s is group-major: (n_scales, out_s_ld); row_w (per pair, bf16 rows
+// only) or NULL
+cudaError_t launch_gather_rows(const void *x, const float *xs, const float *row_w,
+                               int row_bytes, int n_scales, const int32_t *sorted,
                                const int32_t *total, int P, int topk,
                                void *out, float *out_s, int64_t out_s_ld,
                                int num_sms, cudaStream_t s);
@@ -34,8 +39,9 @@ cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
                           cudaStream_t s);
 
 // quant.cu
-cudaError_t launch_quant_group(const uint16_t *x, int M, int K, uint8_t *q,
-                               float *scales, cudaStream_t s);
+// row_w (M) or NULL: rows multiplied by their weight (fp32) before quantising
+cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int K,
+                               uint8_t *q, float *scales, cudaStream_t s);
 cudaError_t launch_quant_block(const uint16_t *w, int64_t R, int C, uint8_t *q,
                                float *scales, cudaStream_t s);
 

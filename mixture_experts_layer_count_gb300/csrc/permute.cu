@@ -22,12 +22,22 @@ constexpr int kAlignChunk = 2048;   // pairs per block in the sort
 constexpr int kAlignThreads = 256;  // 8 warps
 constexpr int kAlignWarps = kAlignThreads / 32;
 
-__device__ __forceinline__ bool valid_id(int e, int E) { return e >= 0 && e < E; }
+// The local expert of a routed (global) id through expert_map (NULL: the
+// identity): the local id, -1 for an expert that is not on this shard (the
+// pair is skipped silently), -2 for an invalid id (skipped and flagged).
+__device__ __forceinline__ int local_expert(int g, int Eg, const int32_t *__restrict__ map,
+                                            int El) {
+  if (g < 0 || g >= Eg) return -2;
+  const int l = map ? map[g] : g;
+  if (l == -1) return -1;
+  return (l >= 0 && l < El) ? l : -2;
+}
 
 // ---------------------------------------------------------------- counts --
 
 __global__ void __launch_bounds__(1024)
-    count_kernel(const int32_t *__restrict__ ids, int P, int E,
+    count_kernel(const int32_t *__restrict__ ids, int P, int Eg,
+                 const int32_t *__restrict__ map, int E,
                  int32_t *__restrict__ counts, int32_t *err) {
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -35,10 +45,10 @@ __global__ void __launch_bounds__(1024)
   bool bad = false;
   for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P;
        p += gridDim.x * blockDim.x) {
-    int e = ids[p];
-    if (valid_id(e, E))
+    const int e = local_expert(ids[p], Eg, map, E);
+    if (e >= 0)
       atomicAdd(&hist[e], 1);
-    else
+    else if (e == -2)
       bad = true;
   }
   if (bad) set_err(err, GBMOE_ERR_BAD_EXPERT_ID);
@@ -51,7 +61,8 @@ __global__ void __launch_bounds__(1024)
 
 // pass 1: histogram of each chunk of kAlignChunk pairs -> chunk_hist[b][e]
 __global__ void __launch_bounds__(kAlignThreads)
-    align_hist_kernel(const int32_t *__restrict__ ids, int P, int E,
+    align_hist_kernel(const int32_t *__restrict__ ids, int P, int Eg,
+                      const int32_t *__restrict__ map, int E,
                       int32_t *__restrict__ chunk_hist, int32_t *err) {
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -60,10 +71,10 @@ __global__ void __launch_bounds__(kAlignThreads)
   const int p1 = min(P, p0 + kAlignChunk);
   bool bad = false;
   for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-    int e = ids[p];
-    if (valid_id(e, E))
+    const int e = local_expert(ids[p], Eg, map, E);
+    if (e >= 0)
       atomicAdd(&hist[e], 1);
-    else
+    else if (e == -2)
       bad = true;
   }
   if (bad) set_err(err, GBMOE_ERR_BAD_EXPERT_ID);
@@ -123,7 +134,8 @@ __global__ void __launch_bounds__(1024)
 // position = chunk base of its expert + pairs of that expert in earlier rounds
 // + in earlier warps of this round + in lower lanes of its warp.
 __global__ void __launch_bounds__(kAlignThreads)
-    align_scatter_kernel(const int32_t *__restrict__ ids, int P, int E,
+    align_scatter_kernel(const int32_t *__restrict__ ids, int P, int Eg,
+                         const int32_t *__restrict__ map, int E,
                          const int32_t *__restrict__ chunk_base,
                          int32_t *__restrict__ sorted,
                          int32_t *__restrict__ inv) {
@@ -142,8 +154,8 @@ __global__ void __launch_bounds__(kAlignThreads)
   for (int r0 = p0; r0 < p1; r0 += kAlignThreads) {
     const int p = r0 + tid;
     const bool in = p < p1;
-    const int e = in ? ids[p] : -1;
-    const bool ok = in && valid_id(e, E);
+    const int e = in ? local_expert(ids[p], Eg, map, E) : -1;
+    const bool ok = e >= 0;
     const int key = ok ? e : -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
     const int rank = __popc(peers & lt_mask);
@@ -175,10 +187,12 @@ __global__ void __launch_bounds__(kAlignThreads)
 // out[i] = x[sorted[i] / topk] for i < *total (one warp per row, 16-byte
 // vectors); FP8 also carries the row's group scales, written group-major
 // (out_s[g * out_s_ld + i]) so that a GEMM tile's scales of one K block are
-// contiguous.
+// contiguous.  row_w (bf16 rows only, per pair or NULL): the row is scaled by
+// the pair's router weight in fp32 and rounded back to bf16
+// (apply_router_weight_on_input).
 __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint4 *__restrict__ x, const float *__restrict__ xs,
-                       int row_vecs, int n_scales,
+                       const float *__restrict__ row_w, int row_vecs, int n_scales,
                        const int32_t *__restrict__ sorted,
                        const int32_t *__restrict__ total, int P, int topk,
                        uint4 *__restrict__ out, float *__restrict__ out_s,
@@ -187,10 +201,26 @@ __global__ void __launch_bounds__(256)
   const int n = min(*total, P);
   for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n;
        i += (gridDim.x * blockDim.x) >> 5) {
-    const int t = sorted[i] / topk;
+    const int pair = sorted[i];
+    const int t = pair / topk;
     const uint4 *src = x + (size_t)t * row_vecs;
     uint4 *dst = out + (size_t)i * row_vecs;
-    for (int v = lane; v < row_vecs; v += 32) dst[v] = src[v];
+    if (row_w) {
+      const float w = row_w[pair];
+      for (int v = lane; v < row_vecs; v += 32) {
+        uint4 u = src[v];
+        uint32_t *h = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(h[j] << 16) * w;
+          const float hi = __uint_as_float(h[j] & 0xffff0000u) * w;
+          h[j] = pack_bf16x2(lo, hi);
+        }
+        dst[v] = u;
+      }
+    } else {
+      for (int v = lane; v < row_vecs; v += 32) dst[v] = src[v];
+    }
     if (xs)
       for (int g = lane; g < n_scales; g += 32)
         out_s[(size_t)g * out_s_ld + i] = xs[(size_t)t * n_scales + g];
@@ -235,38 +265,40 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_count(const int32_t *ids, int P, int E, int32_t *counts,
-                         int32_t *err, int num_sms, cudaStream_t s) {
+cudaError_t launch_count(const int32_t *ids, int P, int Eg, const int32_t *map,
+                         int E, int32_t *counts, int32_t *err, int num_sms,
+                         cudaStream_t s) {
   cudaError_t st = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
   if (st != cudaSuccess) return st;
   int blocks = (P + 1023) / 1024;
   if (blocks > 2 * num_sms) blocks = 2 * num_sms;
   if (blocks < 1) blocks = 1;
-  count_kernel<<<blocks, 1024, sizeof(int32_t) * E, s>>>(ids, P, E, counts, err);
+  count_kernel<<<blocks, 1024, sizeof(int32_t) * E, s>>>(ids, P, Eg, map, E, counts, err);
   return cudaGetLastError();
 }
 
 int align_num_chunks(int P) { return (P + kAlignChunk - 1) / kAlignChunk; }
 
-cudaError_t launch_align(const int32_t *ids, int P, int E, int32_t *counts,
-                         int32_t *offsets, int32_t *sorted, int32_t *inv,
-                         int32_t *chunk_hist, int32_t *err, cudaStream_t s) {
+cudaError_t launch_align(const int32_t *ids, int P, int Eg, const int32_t *map,
+                         int E, int32_t *counts, int32_t *offsets, int32_t *sorted,
+                         int32_t *inv, int32_t *chunk_hist, int32_t *err,
+                         cudaStream_t s) {
   const int nb = align_num_chunks(P);
   if (nb > 0) {
-    align_hist_kernel<<<nb, kAlignThreads, sizeof(int32_t) * E, s>>>(ids, P, E,
+    align_hist_kernel<<<nb, kAlignThreads, sizeof(int32_t) * E, s>>>(ids, P, Eg, map, E,
                                                                     chunk_hist, err);
   }
   align_scan_kernel<<<1, 1024, 0, s>>>(E, nb, chunk_hist, counts, offsets);
   if (nb > 0) {
     const size_t smem = sizeof(int32_t) * (size_t)E * (1 + kAlignWarps);
-    align_scatter_kernel<<<nb, kAlignThreads, smem, s>>>(ids, P, E, chunk_hist,
+    align_scatter_kernel<<<nb, kAlignThreads, smem, s>>>(ids, P, Eg, map, E, chunk_hist,
                                                          sorted, inv);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows(const void *x, const float *xs, int row_bytes,
-                               int n_scales, const int32_t *sorted,
+cudaError_t launch_gather_rows(const void *x, const float *xs, const float *row_w,
+                               int row_bytes, int n_scales, const int32_t *sorted,
                                const int32_t *total, int P, int topk,
                                void *out, float *out_s, int64_t out_s_ld,
                                int num_sms, cudaStream_t s) {
@@ -275,7 +307,7 @@ cudaError_t launch_gather_rows(const void *x, const float *xs, int row_bytes,
   if (blocks > 8 * num_sms) blocks = 8 * num_sms;
   if (blocks < 1) blocks = 1;
   gather_rows_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(
-      static_cast<const uint4 *>(x), xs, row_bytes / 16, n_scales, sorted,
+      static_cast<const uint4 *>(x), xs, row_w, row_bytes / 16, n_scales, sorted,
       total, P, topk, static_cast<uint4 *>(out), out_s, out_s_ld);
   return cudaGetLastError();
 }

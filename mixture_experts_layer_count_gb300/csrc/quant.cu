@@ -33,8 +33,9 @@ __device__ __forceinline__ float group_scale(float amax) {
 
 // one warp per (token, 128-group): 4 values per lane
 __global__ void __launch_bounds__(256)
-    quant_group_kernel(const uint2 *__restrict__ x, int M, int K,
-                       uint32_t *__restrict__ q, float *__restrict__ scales) {
+    quant_group_kernel(const uint2 *__restrict__ x, const float *__restrict__ row_w,
+                       int M, int K, uint32_t *__restrict__ q,
+                       float *__restrict__ scales) {
   const int lane = threadIdx.x & 31;
   const int G = K / 128;
   const size_t n = (size_t)M * G;
@@ -45,6 +46,11 @@ __global__ void __launch_bounds__(256)
     uint2 raw = x[base / 4];
     float f[4] = {bf16_bits_to_float(raw.x & 0xffffu), bf16_bits_to_float(raw.x >> 16),
                   bf16_bits_to_float(raw.y & 0xffffu), bf16_bits_to_float(raw.y >> 16)};
+    if (row_w) {  // apply_router_weight_on_input: the fp32 product is quantised
+      const float w = row_w[t];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) f[i] = __fmul_rn(f[i], w);
+    }
     float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
@@ -108,13 +114,13 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_quant_group(const uint16_t *x, int M, int K, uint8_t *q,
-                               float *scales, cudaStream_t s) {
+cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int K,
+                               uint8_t *q, float *scales, cudaStream_t s) {
   const size_t warps = (size_t)M * (K / 128);
   size_t blocks = (warps + 7) / 8;
   if (blocks > 65535u * 16u) blocks = 65535u * 16u;
   quant_group_kernel<<<(unsigned)blocks, 256, 0, s>>>(
-      reinterpret_cast<const uint2 *>(x), M, K, reinterpret_cast<uint32_t *>(q),
+      reinterpret_cast<const uint2 *>(x), row_w, M, K, reinterpret_cast<uint32_t *>(q),
       scales);
   return cudaGetLastError();
 }

@@ -93,20 +93,27 @@ def test_route_rejects_bad_arguments(lib):
 
 
 def test_count_align_reject_bad_arguments(lib):
-    assert lib.moe_count_expert_tokens(P16, 8, 2, 8, None, None, None) == INVALID
-    assert lib.moe_count_expert_tokens(P16, -1, 2, 8, P16, None, None) == INVALID
-    assert lib.moe_count_expert_tokens(None, 8, 2, 8, P16, None, None) == INVALID
-    # workspace too small
-    assert lib.moe_align_permute(P16, 8, 2, 8, None, P16, P16, P16, P16, 0, None, None) == INVALID
-    assert lib.moe_align_permute(P16, 8, 2, 600, None, P16, P16, P16, P16, 1 << 20, None, None) == INVALID
+    c = lib.moe_count_expert_tokens
+    #        ids  M  k  Eg map  E  counts err  s
+    assert c(P16, 8, 2, 8, None, 8, None, None, None) == INVALID
+    assert c(P16, -1, 2, 8, None, 8, P16, None, None) == INVALID
+    assert c(None, 8, 2, 8, None, 8, P16, None, None) == INVALID
+    assert c(P16, 8, 2, 16, None, 8, P16, None, None) == INVALID  # no map: Eg must equal E
+    assert c(P16, 8, 2, 0, P16, 8, P16, None, None) == INVALID    # no routed experts
+    a = lib.moe_align_permute
+    #        ids  M  k  Eg map   E  cnt  off  srt  inv  ws   wsb  err  s
+    assert a(P16, 8, 2, 8, None, 8, None, P16, P16, P16, P16, 0, None, None) == INVALID  # ws too small
+    assert a(P16, 8, 2, 600, None, 600, None, P16, P16, P16, P16, 1 << 20, None, None) == INVALID
+    assert a(P16, 8, 2, 12, None, 8, None, P16, P16, P16, P16, 1 << 20, None, None) == INVALID
     # the no-workspace variant refuses sizes beyond its fixed array
     assert lib.moe_align_permute_no_ws(P16, 65536, 8, 512, None, P16, P16, P16, None, None) == INVALID
 
 
 def test_quant_rejects_bad_arguments(lib):
-    assert lib.moe_quant_fp8_group(P16, 4, 256, 64, P16, P16, None) == INVALID     # group
-    assert lib.moe_quant_fp8_group(P16, 4, 200, 128, P16, P16, None) == INVALID    # K % 128
-    assert lib.moe_quant_fp8_group(P_ODD, 4, 256, 128, P16, P16, None) == INVALID  # alignment
+    q = lib.moe_quant_fp8_group
+    assert q(P16, None, 4, 256, 64, P16, P16, None) == INVALID     # group
+    assert q(P16, None, 4, 200, 128, P16, P16, None) == INVALID    # K % 128
+    assert q(P_ODD, None, 4, 256, 128, P16, P16, None) == INVALID  # alignment
     assert lib.moe_quant_fp8_block(P16, 100, 256, 128, P16, P16, None) == INVALID  # R % 128
     assert lib.moe_quant_fp8_block(P16, 128, 256, 128, None, P16, None) == INVALID
 
@@ -121,10 +128,14 @@ def test_gemm_calls_reject_bad_arguments(lib):
     assert g(P16, None, P16, 8, 2, 8, 128, 256, None, None, 0, P16, None, None, None) == INVALID
     d = lib.moe_grouped_gemm_down
     assert d(P16, None, P16, P16, P16, 8, 2, 8, 128, 256, P16, None, 1, P16, None, None) == INVALID
-    assert d(P16, None, P16, P16, None, 8, 2, 8, 128, 256, P16, None, 0, P16, None, None) == INVALID
-    assert lib.moe_permute_rows(P16, None, P16, P16, 8, 2, 8, 256, 9, P16, None, None) == UNSUPPORTED
-    assert lib.moe_permute_rows(P16, None, P16, P16, 8, 2, 8, 200, 0, P16, None, None) == INVALID
-    assert lib.moe_permute_rows(None, None, P16, P16, 8, 2, 8, 256, 0, P16, None, None) == INVALID
+    assert d(P16, None, None, P16, None, 8, 2, 8, 128, 256, P16, None, 0, P16, None, None) == INVALID  # no sorted ids
+    pr = lib.moe_permute_rows
+    #         x   xs    rw    srt  off  M  k  E  K    dt A    As   s
+    assert pr(P16, None, None, P16, P16, 8, 2, 8, 256, 9, P16, None, None) == UNSUPPORTED
+    assert pr(P16, None, None, P16, P16, 8, 2, 8, 200, 0, P16, None, None) == INVALID
+    assert pr(None, None, None, P16, P16, 8, 2, 8, 256, 0, P16, None, None) == INVALID
+    # FP8 rows take the router weight in the quantiser, not in the gather
+    assert pr(P16, P16, P16, P16, P16, 8, 1, 8, 256, 1, P16, P16, None) == INVALID
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 2, 12, P16, None) == INVALID
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 33, 256, P16, None) == INVALID
     b = lib.moe_batched_masked_experts
@@ -136,17 +147,19 @@ def test_gemm_calls_reject_bad_arguments(lib):
 
 def test_forward_rejects_bad_arguments(lib):
     f = lib.moe_forward
-    args = [P16, P16, None, 64, 256, 128, 8, 2, 0, 1, 1, 1, 0, P16, None, P16, None,
-            P16, None, None, P16, 1 << 30, None, None]
-    small = list(args)
-    small[21] = 1024  # workspace too small
-    assert f(*small) == INVALID
-    with_bias = list(args)
-    with_bias[2] = P16  # bias with a softmax router
-    assert f(*with_bias) == INVALID
-    odd = list(args)
-    odd[17] = P_ODD  # misaligned output
-    assert f(*odd) == INVALID
-    fp8 = list(args)
-    fp8[12] = 1  # FP8 weights without their scales
-    assert f(*fp8) == INVALID
+    #       x    lg   bias  M   K    N    Eg map   E  k  fn ng tg rn woi dt
+    args = [P16, P16, None, 64, 256, 128, 8, None, 8, 2, 0, 1, 1, 1, 0, 0,
+            P16, None, P16, None, P16, None, None, P16, 1 << 30, None, None]
+    #       w1   w1s   w2   w2s   out  ids   wts   ws   wsb      err   s
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a24=1024) == INVALID          # workspace too small
+    assert call(a2=P16) == INVALID            # bias with a softmax router
+    assert call(a20=P_ODD) == INVALID         # misaligned output
+    assert call(a15=1) == INVALID             # FP8 weights without their scales
+    assert call(a14=1) == INVALID             # weight on input needs topk 1
+    assert call(a6=16) == INVALID             # 16 routed experts, 8 local, no map
+    assert call(a15=3) == UNSUPPORTED         # dtype
