@@ -29,6 +29,7 @@ _lib = None
 
 BF16, FP8 = 0, 1
 SOFTMAX, SIGMOID = 0, 1
+SILU, GELU = 0, 1
 
 
 def build(force: bool = False) -> str:
@@ -72,7 +73,7 @@ def _load():
             lib.orc_moe_forward_ep.restype = None
             lib.orc_moe_forward_ep.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I,
                                                I, I, P, I, I, P, P, P, P, P, I,
-                                               P, P, P, I]
+                                               P, P, P, I, I]
             lib.orc_permute_rows.restype = None
             lib.orc_permute_rows.argtypes = [P, P, I, I, I, P]
             lib.orc_unpermute_reduce.restype = None
@@ -83,13 +84,13 @@ def _load():
             lib.orc_quant_fp8_block.argtypes = [P, I, I, I, P, P]
             lib.orc_expert_row.restype = None
             lib.orc_expert_row.argtypes = [I, P, I, I, I, I, I, P, P, P, P, I,
-                                           P, P]
+                                           P, P, I]
             lib.orc_moe_forward.restype = None
             lib.orc_moe_forward.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I,
                                             I, I, P, P, P, P, P, I, P, P, P, I]
             lib.orc_batched_experts.restype = I
             lib.orc_batched_experts.argtypes = [P, P, I, I, I, I, I, I, P, P,
-                                                P, P, P, I, P, I]
+                                                P, P, P, I, P, I, I]
             lib.orc_max_threads.restype = I
             lib.orc_max_threads.argtypes = []
             _lib = lib
@@ -230,8 +231,9 @@ class Weights:
     absent; routing a computed token to one of them is a caller error)."""
 
     def __init__(self, dtype, w1=None, w2=None, w1s=None, w2s=None,
-                 experts=None, E=None, N=None, K=None):
+                 experts=None, E=None, N=None, K=None, act=SILU):
         self.dtype = dtype
+        self.act = act  # the experts' gated activation: SILU or GELU
         bits = np.uint16 if dtype == BF16 else np.uint8
         if experts is None:
             w1 = _c(w1, bits)
@@ -275,7 +277,7 @@ def expert_row(x_bf16_bits, t, e, W: Weights, requant_h=False):
     y = np.empty((W.K,), np.float64)
     lib.orc_expert_row(W.dtype, _p(x), int(t), int(e), W.E, W.N, W.K,
                        _p(W.w1), _p(W.w1s), _p(W.w2), _p(W.w2s),
-                       int(requant_h), _p(h), _p(y))
+                       int(requant_h), _p(h), _p(y), int(W.act))
     return h, y
 
 
@@ -307,7 +309,7 @@ def moe_forward(x_bf16_bits, logits, bias, topk, score_fn, W: Weights,
                            score_fn, n_groups, topk_groups, int(renorm), W.dtype,
                            int(requant_h), _p(emap), W.E, int(weight_on_input),
                            _p(W.w1), _p(W.w1s), _p(W.w2), _p(W.w2s), _p(tok), n,
-                           _p(ids), _p(w), _p(out), int(nthreads))
+                           _p(ids), _p(w), _p(out), int(nthreads), int(W.act))
     return out, ids, w
 
 
@@ -326,5 +328,5 @@ def batched_experts(xb_bf16_bits, counts, W: Weights, rows=None,
     n = lib.orc_batched_experts(_p(xb), _p(counts), E, T, W.N, K, W.dtype,
                                 int(requant_h), _p(W.w1), _p(W.w1s), _p(W.w2),
                                 _p(W.w2s), _p(r), 0 if r is None else r.shape[0],
-                                _p(out), int(nthreads))
+                                _p(out), int(nthreads), int(W.act))
     return out, int(n)

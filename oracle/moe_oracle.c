@@ -73,6 +73,9 @@
 
 enum { ORC_BF16 = 0, ORC_FP8 = 1 };
 enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
+/* FusedMoEPermuteExpertsUnpermute.activation: "silu" -> silu_and_mul,
+ * "gelu" -> gelu_and_mul */
+enum { ORC_SILU = 0, ORC_GELU = 1 };
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */
@@ -521,6 +524,7 @@ void orc_quant_fp8_block(const uint16_t *w, int R, int C, int block,
  * hold the 128 x 128 block scales. */
 typedef struct {
     int dtype, E, N, K;
+    int act; /* ORC_SILU or ORC_GELU: the gated activation of the experts */
     const void *const *w1, *const *w2;
     const float *const *w1s, *const *w2s;
 } orc_weights;
@@ -554,7 +558,10 @@ static void expert_row(const orc_weights *W, int e, const double *x,
             g += x[k] * weight_at(W, 1, e, n, k);
             u += x[k] * weight_at(W, 1, e, N + n, k);
         }
-        h[n] = g / (1.0 + exp(-g)) * u;
+        if (W->act == ORC_GELU)
+            h[n] = 0.5 * g * (1.0 + erf(g / sqrt(2.0))) * u; /* exact GELU */
+        else
+            h[n] = g / (1.0 + exp(-g)) * u;                  /* SiLU */
     }
     if (requant_h) {
         int gi;
@@ -613,12 +620,12 @@ static void input_row(int dtype, const uint16_t *x, int t, int K, double *xr)
 void orc_expert_row(int dtype, const uint16_t *x, int t, int e, int E, int N,
                     int K, const void *const *w1, const float *const *w1s,
                     const void *const *w2, const float *const *w2s,
-                    int requant_h, double *h, double *y)
+                    int requant_h, double *h, double *y, int act)
 {
     orc_weights W;
     double *xr = (double *)malloc(sizeof(double) * (size_t)K);
     fill_e4m3_table();
-    W.dtype = dtype; W.E = E; W.N = N; W.K = K;
+    W.dtype = dtype; W.E = E; W.N = N; W.K = K; W.act = act;
     W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
     input_row(dtype, x, t, K, xr);
     expert_row(&W, e, xr, requant_h, h, y);
@@ -651,12 +658,12 @@ void orc_moe_forward_ep(const uint16_t *x, const float *logits,
                         const float *const *w1s, const void *const *w2,
                         const float *const *w2s, const int32_t *tokens,
                         int n_tok, int32_t *ids_out, double *w_out,
-                        double *out, int nthreads)
+                        double *out, int nthreads, int act)
 {
     int i;
     orc_weights W;
     fill_e4m3_table();
-    W.dtype = dtype; W.E = E_local; W.N = N; W.K = K;
+    W.dtype = dtype; W.E = E_local; W.N = N; W.K = K; W.act = act;
     W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
     if (!tokens)
         n_tok = M;
@@ -714,7 +721,7 @@ void orc_moe_forward(const uint16_t *x, const float *logits, const float *bias,
     orc_moe_forward_ep(x, logits, bias, M, K, N, E, topk, score_fn, n_groups,
                        topk_groups, renorm, dtype, requant_h, NULL, E, 0, w1,
                        w1s, w2, w2s, tokens, n_tok, ids_out, w_out, out,
-                       nthreads);
+                       nthreads, ORC_SILU);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -730,13 +737,13 @@ int orc_batched_experts(const uint16_t *xb, const int32_t *counts, int E,
                         const void *const *w1, const float *const *w1s,
                         const void *const *w2, const float *const *w2s,
                         const int32_t *rows, int n_rows,
-                        double *yb, int nthreads)
+                        double *yb, int nthreads, int act)
 {
     int e, i, n = 0;
     int32_t *list;
     orc_weights W;
     fill_e4m3_table();
-    W.dtype = dtype; W.E = E; W.N = N; W.K = K;
+    W.dtype = dtype; W.E = E; W.N = N; W.K = K; W.act = act;
     W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
     if (rows) {
         list = (int32_t *)rows;

@@ -423,3 +423,20 @@ def test_quant_with_row_weights_is_cast_of_the_fp32_product(orc):
     assert np.array_equal(s, (v.abs().amax(-1) / 448.0).numpy())
     ref = (v / torch.from_numpy(s).view(17, 2, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
     assert np.array_equal(q, ref.view(17, 256).numpy())
+
+
+def test_gelu_experts_are_dense_geglu(orc):
+    """activation "gelu" (gelu_and_mul): h = gelu(gate) * up with the exact
+    erf GELU, checked against torch's gelu on a dense E = 1 layer."""
+    cfg = WL.MoEConfig("gelu", M=11, K=64, N=32, E=1, topk=1, seed=34)
+    d = WL.make_inputs(cfg)
+    W = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"]), act=orc.GELU)
+    out, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1, orc.SOFTMAX, W)
+    x = d["x"].double()
+    w1 = d["w1"][0].double()
+    h = torch.nn.functional.gelu(x @ w1[:32].T) * (x @ w1[32:].T)
+    ref = (h @ d["w2"][0].double().T).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    Ws = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"]))
+    silu, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1, orc.SOFTMAX, Ws)
+    assert np.abs(silu - out).max() > 1e-3 * np.abs(out).max()
