@@ -60,6 +60,11 @@ typedef enum {
 enum { GBMOE_BF16 = 0, GBMOE_FP8_E4M3 = 1 };
 /* router score function */
 enum { GBMOE_SOFTMAX = 0, GBMOE_SIGMOID = 1 };
+/* gated activation of the experts (FusedMoEPermuteExpertsUnpermute.activation):
+ * "silu" -> silu_and_mul, h = silu(g) * u with silu(z) = z / (1 + exp(-z));
+ * "gelu" -> gelu_and_mul, h = gelu(g) * u with the exact
+ * gelu(z) = z / 2 * (1 + erf(z / sqrt 2)) */
+enum { GBMOE_ACT_SILU = 0, GBMOE_ACT_GELU = 1 };
 /* which call a workspace is sized for (moe_workspace_size) */
 enum {
     GBMOE_WS_ALIGN = 0,    /* moe_align_permute                       */
@@ -221,6 +226,14 @@ gbmoe_status_t moe_grouped_gemm_gate_up_silu(
     int dtype, void *H, float *H_scales, int32_t *err_word,
     gbmoe_stream_t stream);
 
+/* The same GEMM with activation "gelu" (gelu_and_mul):
+ * H[i, n] = gelu(g[n]) * u[n], gelu the exact erf form above. */
+gbmoe_status_t moe_grouped_gemm_gate_up_gelu(
+    const void *A, const float *A_scales, const int32_t *offsets, int M,
+    int topk, int E, int N, int K, const void *w1, const float *w1_scales,
+    int dtype, void *H, float *H_scales, int32_t *err_word,
+    gbmoe_stream_t stream);
+
 /* Second expert GEMM with the router weight fused into its epilogue
  * (the experts own the weight application, which
  * FusedMoEPermuteExpertsUnpermute.finalize_weight_and_reduce_impl hands to
@@ -259,6 +272,7 @@ gbmoe_status_t moe_unpermute_weighted_reduce(const uint16_t *y_slot,
  * c_e = min(max(expert_num_tokens[e], 0), T),
  *   h = silu(x_b[e,r] . w1[e, 0:N]^T) * (x_b[e,r] . w1[e, N:2N]^T)
  *   y_b[e, r, :] = h . w2[e]^T           (unweighted; no reduction)
+ * (gelu in place of silu when activation is GBMOE_ACT_GELU).
  * Rows r >= c_e of x_b are never read and rows r >= c_e of y_b are never
  * written.  A count outside [0, T] is clamped and sets GBMOE_ERR_COUNT_RANGE.
  * No count is read on the host, so the call can be captured in a CUDA graph
@@ -270,7 +284,7 @@ gbmoe_status_t moe_batched_masked_experts(
     const void *x_b, const float *x_b_scales,
     const int32_t *expert_num_tokens, int E, int T, int N, int K,
     const void *w1, const float *w1_scales, const void *w2,
-    const float *w2_scales, int dtype, uint16_t *y_b, void *ws,
+    const float *w2_scales, int dtype, int activation, uint16_t *y_b, void *ws,
     size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream);
 
 /* The whole layer in the Standard format, FusedMoEModularKernel.forward
@@ -283,6 +297,7 @@ gbmoe_status_t moe_batched_masked_experts(
  * apply_router_weight_on_input != 0 (topk must be 1): the router weight
  * multiplies the activations (before FP8 quantisation) instead of the expert
  * output, out[t] = expert(w[t] * x[t]);
+ * activation: GBMOE_ACT_SILU or GBMOE_ACT_GELU;
  * dtype GBMOE_BF16: w1 (E, 2N, K) / w2 (E, K, N) bf16, scales NULL;
  * dtype GBMOE_FP8_E4M3: w1/w2 e4m3 with their block scales; the activations
  *   are quantised per token in groups of 128 and H is requantised.
@@ -295,7 +310,8 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                            const int32_t *expert_map, int E, int topk,
                            int score_fn, int n_groups, int topk_groups,
                            int renormalize, int apply_router_weight_on_input,
-                           int dtype, const void *w1, const float *w1_scales,
+                           int activation, int dtype, const void *w1,
+                           const float *w1_scales,
                            const void *w2, const float *w2_scales,
                            uint16_t *out, int32_t *topk_ids,
                            float *topk_weights, void *ws, size_t ws_bytes,

@@ -19,6 +19,7 @@ from . import build as _build
 
 BF16, FP8_E4M3 = 0, 1
 SOFTMAX, SIGMOID = 0, 1
+ACT_SILU, ACT_GELU = 0, 1
 WS_ALIGN, WS_BATCHED, WS_FORWARD = 0, 2, 3
 ERR_BAD_EXPERT_ID, ERR_COUNT_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4
 
@@ -53,13 +54,15 @@ _SIGS = {
     "moe_permute_rows": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm_gate_up_silu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                                            _I, _P, _P, _P, _P]),
+    "moe_grouped_gemm_gate_up_gelu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
+                                           _I, _P, _P, _P, _P]),
     "moe_grouped_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                                    _I, _P, _P, _P]),
     "moe_unpermute_weighted_reduce": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_batched_masked_experts": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
-                                        _I, _P, _P, _Z, _P, _P]),
+                                        _I, _I, _P, _P, _Z, _P, _P]),
     "moe_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
-                         _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P]),
+                         _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P]),
 }
 
 
@@ -184,6 +187,15 @@ def moe_grouped_gemm_gate_up_silu(A, A_scales, offsets, M, topk, E, N, K, w1,
         _stream(stream)))
 
 
+def moe_grouped_gemm_gate_up_gelu(A, A_scales, offsets, M, topk, E, N, K, w1,
+                                  w1_scales, dtype, H, H_scales, err_word=None,
+                                  stream=None):
+    _check("moe_grouped_gemm_gate_up_gelu", load().moe_grouped_gemm_gate_up_gelu(
+        _ptr(A), _ptr(A_scales), _ptr(offsets), M, topk, E, N, K, _ptr(w1),
+        _ptr(w1_scales), dtype, _ptr(H), _ptr(H_scales), _ptr(err_word),
+        _stream(stream)))
+
+
 def moe_grouped_gemm_down(H, H_scales, sorted_pair_ids, offsets, topk_weights,
                           M, topk, E, N, K, w2, w2_scales, dtype, y_slot,
                           err_word=None, stream=None):
@@ -200,11 +212,13 @@ def moe_unpermute_weighted_reduce(y_slot, inv, M, topk, K, out, stream=None):
 
 def moe_batched_masked_experts(x_b, expert_num_tokens, N, w1, w2, y_b, ws,
                                dtype=BF16, x_b_scales=None, w1_scales=None,
-                               w2_scales=None, err_word=None, stream=None):
+                               w2_scales=None, err_word=None, stream=None,
+                               activation=ACT_SILU):
     E, T, K = x_b.shape
     _check("moe_batched_masked_experts", load().moe_batched_masked_experts(
         _ptr(x_b), _ptr(x_b_scales), _ptr(expert_num_tokens), E, T, N, K,
-        _ptr(w1), _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), dtype, _ptr(y_b),
+        _ptr(w1), _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), dtype,
+        int(activation), _ptr(y_b),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
         _stream(stream)))
 
@@ -212,7 +226,8 @@ def moe_batched_masked_experts(x_b, expert_num_tokens, N, w1, w2, y_b, ws,
 def moe_forward(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
                 renormalize, dtype, w1, w1_scales, w2, w2_scales, out, ws,
                 topk_ids=None, topk_weights=None, err_word=None, stream=None,
-                expert_map=None, apply_router_weight_on_input=False):
+                expert_map=None, apply_router_weight_on_input=False,
+                activation=ACT_SILU):
     """The whole Standard layer.  E is the number of local experts (w1.shape[0]);
     the router picks among logits.shape[1] experts, mapped to local ones by
     expert_map when given."""
@@ -221,7 +236,8 @@ def moe_forward(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
     _check("moe_forward", load().moe_forward(
         _ptr(x), _ptr(logits), _ptr(bias), M, K, N, E_global, _ptr(expert_map), E,
         topk, score_fn, n_groups, topk_groups, int(renormalize),
-        int(apply_router_weight_on_input), dtype, _ptr(w1), _ptr(w1_scales),
+        int(apply_router_weight_on_input), int(activation), dtype, _ptr(w1),
+        _ptr(w1_scales),
         _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
         _stream(stream)))

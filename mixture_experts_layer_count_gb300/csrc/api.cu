@@ -128,10 +128,11 @@ bool route_args_ok(int M, int E, int topk, int score_fn, const float *bias,
 gbmoe_status_t gate_up_impl(const void *A, const float *A_scales,
                             const int32_t *offsets, int M, int topk, int E,
                             int N, int K, const void *w1, const float *w1_scales,
-                            int dtype, void *H, float *H_scales, int32_t *err,
-                            int num_sms, cudaStream_t s) {
+                            int dtype, int act, void *H, float *H_scales,
+                            int32_t *err, int num_sms, cudaStream_t s) {
   GroupedGemmArgs a{};
   a.mode = kGateUp;
+  a.act = act;
   a.fp8 = dtype == GBMOE_FP8_E4M3;
   a.offsets = offsets;
   a.E = E;
@@ -350,10 +351,10 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
                       dtype, A, A_scales, sms, (cudaStream_t)stream);
 }
 
-gbmoe_status_t moe_grouped_gemm_gate_up_silu(
+static gbmoe_status_t gate_up_entry(
     const void *A, const float *A_scales, const int32_t *offsets, int M,
     int topk, int E, int N, int K, const void *w1, const float *w1_scales,
-    int dtype, void *H, float *H_scales, int32_t *err_word,
+    int dtype, int act, void *H, float *H_scales, int32_t *err_word,
     gbmoe_stream_t stream) {
   if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
   if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
@@ -366,8 +367,26 @@ gbmoe_status_t moe_grouped_gemm_gate_up_silu(
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK || M == 0) return st;
-  return gate_up_impl(A, A_scales, offsets, M, topk, E, N, K, w1, w1_scales, dtype, H,
+  return gate_up_impl(A, A_scales, offsets, M, topk, E, N, K, w1, w1_scales, dtype, act, H,
                       H_scales, err_word, sms, (cudaStream_t)stream);
+}
+
+gbmoe_status_t moe_grouped_gemm_gate_up_silu(
+    const void *A, const float *A_scales, const int32_t *offsets, int M,
+    int topk, int E, int N, int K, const void *w1, const float *w1_scales,
+    int dtype, void *H, float *H_scales, int32_t *err_word,
+    gbmoe_stream_t stream) {
+  return gate_up_entry(A, A_scales, offsets, M, topk, E, N, K, w1, w1_scales, dtype,
+                       GBMOE_ACT_SILU, H, H_scales, err_word, stream);
+}
+
+gbmoe_status_t moe_grouped_gemm_gate_up_gelu(
+    const void *A, const float *A_scales, const int32_t *offsets, int M,
+    int topk, int E, int N, int K, const void *w1, const float *w1_scales,
+    int dtype, void *H, float *H_scales, int32_t *err_word,
+    gbmoe_stream_t stream) {
+  return gate_up_entry(A, A_scales, offsets, M, topk, E, N, K, w1, w1_scales, dtype,
+                       GBMOE_ACT_GELU, H, H_scales, err_word, stream);
 }
 
 gbmoe_status_t moe_grouped_gemm_down(
@@ -411,9 +430,10 @@ gbmoe_status_t moe_batched_masked_experts(
     const void *x_b, const float *x_b_scales,
     const int32_t *expert_num_tokens, int E, int T, int N, int K,
     const void *w1, const float *w1_scales, const void *w2,
-    const float *w2_scales, int dtype, uint16_t *y_b, void *ws,
+    const float *w2_scales, int dtype, int activation, uint16_t *y_b, void *ws,
     size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream) {
   (void)x_b_scales;
+  if (activation != GBMOE_ACT_SILU && activation != GBMOE_ACT_GELU) return GBMOE_INVALID_ARG;
   (void)w1_scales;
   (void)w2_scales;
   if (dtype != GBMOE_BF16) return GBMOE_UNSUPPORTED;
@@ -435,6 +455,7 @@ gbmoe_status_t moe_batched_masked_experts(
   void *Hb = ws;
   GroupedGemmArgs a{};
   a.mode = kGateUp;
+  a.act = activation;
   a.counts = expert_num_tokens;
   a.E = E;
   a.T = T;
@@ -459,7 +480,8 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                            const int32_t *expert_map, int E, int topk,
                            int score_fn, int n_groups, int topk_groups,
                            int renormalize, int apply_router_weight_on_input,
-                           int dtype, const void *w1, const float *w1_scales,
+                           int activation, int dtype, const void *w1,
+                           const float *w1_scales,
                            const void *w2, const float *w2_scales,
                            uint16_t *out, int32_t *topk_ids,
                            float *topk_weights, void *ws, size_t ws_bytes,
@@ -470,6 +492,7 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   if (!route_args_ok(M, E_global, topk, score_fn, bias, n_groups, topk_groups))
     return GBMOE_INVALID_ARG;
   if (apply_router_weight_on_input && topk != 1) return GBMOE_INVALID_ARG;
+  if (activation != GBMOE_ACT_SILU && activation != GBMOE_ACT_GELU) return GBMOE_INVALID_ARG;
   const bool fp8 = dtype == GBMOE_FP8_E4M3;
   if (M > 0) {
     if (!x || !logits || !w1 || !w2 || !out || !ws) return GBMOE_INVALID_ARG;
@@ -510,8 +533,8 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   st = permute_impl(a_src, a_src_s, fp8 ? nullptr : in_w, w.sorted, w.offsets, M, topk, E, K,
                     dtype, w.A, w.As, sms, s);
   if (st != GBMOE_OK) return st;
-  st = gate_up_impl(w.A, w.As, w.offsets, M, topk, E, N, K, w1, w1_scales, dtype, w.H,
-                    w.Hs, err_word, sms, s);
+  st = gate_up_impl(w.A, w.As, w.offsets, M, topk, E, N, K, w1, w1_scales, dtype, activation,
+                    w.H, w.Hs, err_word, sms, s);
   if (st != GBMOE_OK) return st;
   st = down_impl(w.H, w.Hs, w.sorted, w.offsets, in_w ? nullptr : wts, M, topk, E, N, K, w2,
                  w2_scales, dtype, w.y_slot, err_word, sms, s);

@@ -70,7 +70,7 @@ struct KParams {
   int32_t *err;
 };
 
-template <int MODE>
+template <int MODE, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -227,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float h0 = silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-            const float h1 = silu_f(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+            const float h0 = gate_act<ACT>(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+            const float h1 = gate_act<ACT>(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
             pk[i] = pack_bf16x2(h0, h1);
           }
           if (valid) {
@@ -304,11 +304,11 @@ bool resolve_encode() {
   return g_encode != nullptr;
 }
 
-template <int MODE>
+template <int MODE, int ACT>
 cudaError_t launch_bf16(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, ACT>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           kSmemBytes);
     if (st != cudaSuccess) return st;
@@ -343,7 +343,7 @@ cudaError_t launch_bf16(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   long long tiles = mtiles * p.n_tiles;
   int grid = (int)(tiles < num_sms ? tiles : num_sms);
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
+  grouped_gemm_kernel<MODE, ACT><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
   return cudaGetLastError();
 }
 
@@ -371,8 +371,9 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int kind, uint64_t cols,
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,
                                 cudaStream_t s) {
   if (a.fp8) return launch_grouped_gemm_fp8(a, num_sms, s);
-  return a.mode == kGateUp ? launch_bf16<kGateUpMode>(a, num_sms, s)
-                           : launch_bf16<kDownMode>(a, num_sms, s);
+  if (a.mode == kDown) return launch_bf16<kDownMode, kActSilu>(a, num_sms, s);
+  return a.act == GBMOE_ACT_GELU ? launch_bf16<kGateUpMode, kActGelu>(a, num_sms, s)
+                                 : launch_bf16<kGateUpMode, kActSilu>(a, num_sms, s);
 }
 
 }  // namespace gbmoe

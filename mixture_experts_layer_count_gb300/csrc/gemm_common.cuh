@@ -86,6 +86,19 @@ __device__ __forceinline__ void decode_tile(const int *prefix, int E,
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// exact (erf) GELU, the "gelu" of gelu_and_mul
+__device__ __forceinline__ float gelu_f(float g) {
+  return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f));
+}
+
+constexpr int kActSilu = 0;
+constexpr int kActGelu = 1;
+
+template <int ACT>
+__device__ __forceinline__ float gate_act(float g) {
+  return ACT == kActGelu ? gelu_f(g) : silu_f(g);
+}
+
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3) |
          ((uint32_t)__nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3) << 8) |

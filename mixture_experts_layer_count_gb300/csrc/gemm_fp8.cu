@@ -98,7 +98,7 @@ __device__ __forceinline__ void promote16(float *acc, const uint32_t (&v)[16], f
   }
 }
 
-template <int MODE>
+template <int MODE, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          acc[i] = silu_f(acc[i]) * acc[32 + i];
+          acc[i] = gate_act<ACT>(acc[i]) * acc[32 + i];
           amax = fmaxf(amax, fabsf(acc[i]));
         }
         const int xb = tile_no & 1;
@@ -400,11 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc<512>(tmem_base);
 }
 
-template <int MODE>
+template <int MODE, int ACT>
 cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_fp8_kernel<MODE>,
+    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_fp8_kernel<MODE, ACT>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           kSmemBytes);
     if (st != cudaSuccess) return st;
@@ -442,7 +442,7 @@ cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   long long tiles = ((a.a_rows + kBM - 1) / kBM + a.E) * (long long)p.n_tiles;
   int grid = (int)(tiles < num_sms ? tiles : num_sms);
   if (grid < 1) grid = 1;
-  grouped_gemm_fp8_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmAS, p);
+  grouped_gemm_fp8_kernel<MODE, ACT><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmAS, p);
   return cudaGetLastError();
 }
 
@@ -450,8 +450,9 @@ cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
 
 cudaError_t launch_grouped_gemm_fp8(const GroupedGemmArgs &a, int num_sms,
                                     cudaStream_t s) {
-  return a.mode == kGateUp ? launch_fp8<kGateUpMode>(a, num_sms, s)
-                           : launch_fp8<kDownMode>(a, num_sms, s);
+  if (a.mode == kDown) return launch_fp8<kDownMode, kActSilu>(a, num_sms, s);
+  return a.act == GBMOE_ACT_GELU ? launch_fp8<kGateUpMode, kActGelu>(a, num_sms, s)
+                                 : launch_fp8<kGateUpMode, kActSilu>(a, num_sms, s);
 }
 
 }  // namespace gbmoe

@@ -51,6 +51,7 @@ enum GemmMode { kGateUp = 0, kDown = 1 };
 struct GroupedGemmArgs {
   int mode;                  // kGateUp or kDown
   int fp8;                   // 0: bf16 operands, 1: e4m3 with fp32 block scales
+  int act;                   // gate/up: GBMOE_ACT_SILU or GBMOE_ACT_GELU
   // row groups: Standard (offsets != nullptr): expert e owns rows
   // [offsets[e], offsets[e+1]) of A.  Batched: rows [e*T, e*T + min(counts[e], T)).
   const int32_t *offsets;

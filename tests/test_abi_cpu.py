@@ -139,16 +139,17 @@ def test_gemm_calls_reject_bad_arguments(lib):
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 2, 12, P16, None) == INVALID
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 33, 256, P16, None) == INVALID
     b = lib.moe_batched_masked_experts
-    #        xb  xbs   cnt E  T   N    K    w1   w1s  w2   w2s  dt yb   ws   wsb  err  s
-    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 1, P16, P16, 1 << 30, None, None) == UNSUPPORTED
-    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 0, P16, P16, 16, None, None) == INVALID
-    assert b(P16, None, None, 4, 16, 128, 256, P16, None, P16, None, 0, P16, P16, 1 << 30, None, None) == INVALID
+    #        xb  xbs   cnt E  T   N    K    w1   w1s  w2   w2s  dt ac yb   ws   wsb  err  s
+    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 1, 0, P16, P16, 1 << 30, None, None) == UNSUPPORTED
+    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 0, 0, P16, P16, 16, None, None) == INVALID
+    assert b(P16, None, None, 4, 16, 128, 256, P16, None, P16, None, 0, 0, P16, P16, 1 << 30, None, None) == INVALID
+    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 0, 5, P16, P16, 1 << 30, None, None) == INVALID
 
 
 def test_forward_rejects_bad_arguments(lib):
     f = lib.moe_forward
-    #       x    lg   bias  M   K    N    Eg map   E  k  fn ng tg rn woi dt
-    args = [P16, P16, None, 64, 256, 128, 8, None, 8, 2, 0, 1, 1, 1, 0, 0,
+    #       x    lg   bias  M   K    N    Eg map   E  k  fn ng tg rn woi act dt
+    args = [P16, P16, None, 64, 256, 128, 8, None, 8, 2, 0, 1, 1, 1, 0, 0, 0,
             P16, None, P16, None, P16, None, None, P16, 1 << 30, None, None]
     #       w1   w1s   w2   w2s   out  ids   wts   ws   wsb      err   s
     def call(**kw):
@@ -156,10 +157,11 @@ def test_forward_rejects_bad_arguments(lib):
         for i, v in kw.items():
             a[int(i[1:])] = v
         return f(*a)
-    assert call(a24=1024) == INVALID          # workspace too small
+    assert call(a25=1024) == INVALID          # workspace too small
     assert call(a2=P16) == INVALID            # bias with a softmax router
-    assert call(a20=P_ODD) == INVALID         # misaligned output
-    assert call(a15=1) == INVALID             # FP8 weights without their scales
+    assert call(a21=P_ODD) == INVALID         # misaligned output
+    assert call(a16=1) == INVALID             # FP8 weights without their scales
     assert call(a14=1) == INVALID             # weight on input needs topk 1
     assert call(a6=16) == INVALID             # 16 routed experts, 8 local, no map
-    assert call(a15=3) == UNSUPPORTED         # dtype
+    assert call(a15=7) == INVALID             # activation
+    assert call(a16=3) == UNSUPPORTED         # dtype
