@@ -69,7 +69,8 @@ enum { GBMOE_ACT_SILU = 0, GBMOE_ACT_GELU = 1 };
 enum {
     GBMOE_WS_ALIGN = 0,    /* moe_align_permute                       */
     GBMOE_WS_BATCHED = 2,  /* moe_batched_masked_experts              */
-    GBMOE_WS_FORWARD = 3   /* moe_forward (the whole Standard layer)  */
+    GBMOE_WS_FORWARD = 3,  /* moe_forward (the whole Standard layer)  */
+    GBMOE_WS_SHARED = 4    /* moe_shared_expert_forward (N = shared intermediate size) */
 };
 
 /* bits OR-ed into *err_word by the kernels */
@@ -316,6 +317,55 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                            uint16_t *out, int32_t *topk_ids,
                            float *topk_weights, void *ws, size_t ws_bytes,
                            int32_t *err_word, gbmoe_stream_t stream);
+
+/* The shared experts of the layer: a dense gated MLP applied to every token
+ * (the shared_experts of FusedMoEModularKernel.forward, whose output it
+ * returns beside the routed one; the SharedExperts page runs them on an
+ * auxiliary stream).  For every token t:
+ *   h = act(x[t] . w1s[0:Ns]^T) * (x[t] . w1s[Ns:2Ns]^T),
+ *   out_shared[t] = h . w2s^T
+ * x (M, K) bf16; w1s (2Ns, K), w2s (K, Ns) bf16 (the shared experts stacked
+ * along Ns); out_shared (M, K) bf16; activation GBMOE_ACT_*; dtype GBMOE_BF16
+ * only.  Runs the two grouped-GEMM kernels with one expert holding all M
+ * rows.  ws: moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1, dtype). */
+gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K,
+                                         int Ns, const void *w1s,
+                                         const void *w2s, int dtype,
+                                         int activation, uint16_t *out_shared,
+                                         void *ws, size_t ws_bytes,
+                                         int32_t *err_word,
+                                         gbmoe_stream_t stream);
+
+/* moe_forward with the shared experts overlapped on an auxiliary stream
+ * (the MULTI_STREAM_OVERLAPPED order of the SharedExperts page): records
+ * ev_input_ready on `stream`, makes aux_stream wait for it, enqueues
+ * moe_shared_expert_forward on aux_stream and records ev_output_ready
+ * there, enqueues the routed layer (moe_forward) on `stream`, and makes
+ * `stream` wait for ev_output_ready -- so work enqueued on `stream` after
+ * the call sees both out (routed) and out_shared.  The events are created by
+ * the caller (cudaEvent_t; timing may be disabled).  aux_stream NULL: both
+ * run on `stream` one after the other.  The fork/join is capturable in a
+ * CUDA graph when `stream` is being captured.
+ * Arguments as moe_forward, plus Ns, w1s, w2s, out_shared as
+ * moe_shared_expert_forward; ws_shared: moe_workspace_size(GBMOE_WS_SHARED,
+ * ...) bytes, separate from ws. */
+gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
+                                  const float *bias, int M, int K, int N,
+                                  int E_global, const int32_t *expert_map,
+                                  int E, int topk, int score_fn, int n_groups,
+                                  int topk_groups, int renormalize,
+                                  int apply_router_weight_on_input,
+                                  int activation, int dtype, const void *w1,
+                                  const float *w1_scales, const void *w2,
+                                  const float *w2_scales, uint16_t *out,
+                                  void *ws, size_t ws_bytes, int Ns,
+                                  const void *w1s, const void *w2s,
+                                  uint16_t *out_shared, void *ws_shared,
+                                  size_t ws_shared_bytes, int32_t *err_word,
+                                  gbmoe_stream_t stream,
+                                  gbmoe_stream_t aux_stream,
+                                  struct CUevent_st *ev_input_ready,
+                                  struct CUevent_st *ev_output_ready);
 
 /* moe_align_permute without a workspace argument.  The pages have no
  * counterpart of this call: it exists for callers that cannot give the

@@ -20,7 +20,7 @@ from . import build as _build
 BF16, FP8_E4M3 = 0, 1
 SOFTMAX, SIGMOID = 0, 1
 ACT_SILU, ACT_GELU = 0, 1
-WS_ALIGN, WS_BATCHED, WS_FORWARD = 0, 2, 3
+WS_ALIGN, WS_BATCHED, WS_FORWARD, WS_SHARED = 0, 2, 3, 4
 ERR_BAD_EXPERT_ID, ERR_COUNT_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype or device",
@@ -48,6 +48,10 @@ _SIGS = {
     "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_count_expert_tokens": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_align_permute": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
+    "moe_shared_expert_forward": (_I, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _Z, _P, _P]),
+    "moe_forward_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
+                                _I, _I, _P, _P, _P, _P, _P, _P, _Z, _I, _P, _P, _P, _P,
+                                _Z, _P, _P, _P, _P, _P]),
     "moe_align_permute_no_ws": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_group": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
@@ -241,6 +245,47 @@ def moe_forward(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
         _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
         _stream(stream)))
+
+
+def moe_shared_expert_forward(x, Ns, w1s, w2s, out_shared, ws, dtype=BF16,
+                              activation=ACT_SILU, err_word=None, stream=None):
+    """The shared experts (dense gated MLP) on every token of x."""
+    M, K = x.shape
+    _check("moe_shared_expert_forward", load().moe_shared_expert_forward(
+        _ptr(x), M, K, Ns, _ptr(w1s), _ptr(w2s), dtype, int(activation),
+        _ptr(out_shared), _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
+        _stream(stream)))
+
+
+def _event(ev):
+    """Raw cudaEvent_t of a torch.cuda.Event (recorded once if torch has not
+    created it yet)."""
+    if ev is None:
+        return None
+    if ev.cuda_event == 0:
+        ev.record()
+    return ev.cuda_event
+
+
+def moe_forward_shared(x, logits, bias, N, E, topk, score_fn, n_groups,
+                       topk_groups, renormalize, dtype, w1, w1_scales, w2,
+                       w2_scales, out, ws, Ns, w1s, w2s, out_shared, ws_shared,
+                       aux_stream=None, ev_input_ready=None, ev_output_ready=None,
+                       err_word=None, stream=None, expert_map=None,
+                       apply_router_weight_on_input=False, activation=ACT_SILU):
+    """moe_forward with the shared experts overlapped on aux_stream (a
+    torch.cuda.Stream) through two torch.cuda.Event objects."""
+    M, K = x.shape
+    E_global = logits.shape[1]
+    _check("moe_forward_shared", load().moe_forward_shared(
+        _ptr(x), _ptr(logits), _ptr(bias), M, K, N, E_global, _ptr(expert_map), E,
+        topk, score_fn, n_groups, topk_groups, int(renormalize),
+        int(apply_router_weight_on_input), int(activation), dtype, _ptr(w1),
+        _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(ws),
+        ws.numel() * ws.element_size(), Ns, _ptr(w1s), _ptr(w2s), _ptr(out_shared),
+        _ptr(ws_shared), ws_shared.numel() * ws_shared.element_size(), _ptr(err_word),
+        _stream(stream), None if aux_stream is None else aux_stream.cuda_stream,
+        _event(ev_input_ready), _event(ev_output_ready)))
 
 
 def workspace(which, M_or_T, E, N, K, topk, dtype, device="cuda"):

@@ -238,6 +238,10 @@ size_t moe_workspace_size(int which, int M_or_T, int E, int N, int K, int topk,
       if (!gemm_shape_ok(M_or_T, topk, E, N, K, dtype)) return 0;
       carve_forward(c, M_or_T, E, N, K, topk, dtype);
       return c.off;
+    case GBMOE_WS_SHARED:
+      if (!gemm_shape_ok(M_or_T, 1, 1, N, K, dtype) || dtype != GBMOE_BF16) return 0;
+      c.take((size_t)M_or_T * N * 2);
+      return c.off > 0 ? c.off : kWsAlign;
   }
   return 0;
 }
@@ -475,17 +479,16 @@ gbmoe_status_t moe_batched_masked_experts(
   return from_cuda(launch_grouped_gemm(a, sms, s));
 }
 
-gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
-                           const float *bias, int M, int K, int N, int E_global,
-                           const int32_t *expert_map, int E, int topk,
-                           int score_fn, int n_groups, int topk_groups,
-                           int renormalize, int apply_router_weight_on_input,
-                           int activation, int dtype, const void *w1,
-                           const float *w1_scales,
-                           const void *w2, const float *w2_scales,
-                           uint16_t *out, int32_t *topk_ids,
-                           float *topk_weights, void *ws, size_t ws_bytes,
-                           int32_t *err_word, gbmoe_stream_t stream) {
+// every argument check of moe_forward (no launch, no device query)
+static gbmoe_status_t forward_validate(const uint16_t *x, const float *logits,
+                                       const float *bias, int M, int K, int N,
+                                       int E_global, const int32_t *expert_map, int E,
+                                       int topk, int score_fn, int n_groups,
+                                       int topk_groups, int apply_router_weight_on_input,
+                                       int activation, int dtype, const void *w1,
+                                       const float *w1_scales, const void *w2,
+                                       const float *w2_scales, const uint16_t *out,
+                                       const void *ws, size_t ws_bytes) {
   if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
   if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
   if (!map_args_ok(E_global, expert_map, E)) return GBMOE_INVALID_ARG;
@@ -502,6 +505,26 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
     if (ws_bytes < moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype))
       return GBMOE_INVALID_ARG;
   }
+  return GBMOE_OK;
+}
+
+gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
+                           const float *bias, int M, int K, int N, int E_global,
+                           const int32_t *expert_map, int E, int topk,
+                           int score_fn, int n_groups, int topk_groups,
+                           int renormalize, int apply_router_weight_on_input,
+                           int activation, int dtype, const void *w1,
+                           const float *w1_scales,
+                           const void *w2, const float *w2_scales,
+                           uint16_t *out, int32_t *topk_ids,
+                           float *topk_weights, void *ws, size_t ws_bytes,
+                           int32_t *err_word, gbmoe_stream_t stream) {
+  gbmoe_status_t vst = forward_validate(x, logits, bias, M, K, N, E_global, expert_map, E,
+                                        topk, score_fn, n_groups, topk_groups,
+                                        apply_router_weight_on_input, activation, dtype, w1,
+                                        w1_scales, w2, w2_scales, out, ws, ws_bytes);
+  if (vst != GBMOE_OK) return vst;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK) return st;
@@ -540,6 +563,118 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                  w2_scales, dtype, w.y_slot, err_word, sms, s);
   if (st != GBMOE_OK) return st;
   return from_cuda(launch_reduce(w.y_slot, w.inv, M, topk, K, out, sms, s));
+}
+
+gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K,
+                                         int Ns, const void *w1s,
+                                         const void *w2s, int dtype,
+                                         int activation, uint16_t *out_shared,
+                                         void *ws, size_t ws_bytes,
+                                         int32_t *err_word,
+                                         gbmoe_stream_t stream) {
+  if (dtype != GBMOE_BF16) return GBMOE_UNSUPPORTED;
+  if (!gemm_shape_ok(M, 1, 1, Ns, K, dtype)) return GBMOE_INVALID_ARG;
+  if (activation != GBMOE_ACT_SILU && activation != GBMOE_ACT_GELU) return GBMOE_INVALID_ARG;
+  if (M > 0) {
+    if (!x || !w1s || !w2s || !out_shared || !ws) return GBMOE_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w1s) || !aligned16(w2s) || !aligned16(out_shared) ||
+        !aligned16(ws))
+      return GBMOE_INVALID_ARG;
+    if (ws_bytes < moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1, dtype))
+      return GBMOE_INVALID_ARG;
+  }
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK || M == 0) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  // one expert owning all M rows ("dense": neither offsets nor counts)
+  GroupedGemmArgs a{};
+  a.mode = kGateUp;
+  a.act = activation;
+  a.E = 1;
+  a.T = M;
+  a.N = Ns;
+  a.K = K;
+  a.A = x;
+  a.a_rows = M;
+  a.B = w1s;
+  a.out = ws;
+  a.err = err_word;
+  cudaError_t ce = launch_grouped_gemm(a, sms, s);
+  if (ce != cudaSuccess) return from_cuda(ce);
+  a.mode = kDown;
+  a.A = ws;
+  a.B = w2s;
+  a.out = out_shared;
+  return from_cuda(launch_grouped_gemm(a, sms, s));
+}
+
+gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
+                                  const float *bias, int M, int K, int N,
+                                  int E_global, const int32_t *expert_map,
+                                  int E, int topk, int score_fn, int n_groups,
+                                  int topk_groups, int renormalize,
+                                  int apply_router_weight_on_input,
+                                  int activation, int dtype, const void *w1,
+                                  const float *w1_scales, const void *w2,
+                                  const float *w2_scales, uint16_t *out,
+                                  void *ws, size_t ws_bytes, int Ns,
+                                  const void *w1s, const void *w2s,
+                                  uint16_t *out_shared, void *ws_shared,
+                                  size_t ws_shared_bytes, int32_t *err_word,
+                                  gbmoe_stream_t stream,
+                                  gbmoe_stream_t aux_stream,
+                                  struct CUevent_st *ev_input_ready,
+                                  struct CUevent_st *ev_output_ready) {
+  // every argument is checked before anything is enqueued
+  gbmoe_status_t st = forward_validate(x, logits, bias, M, K, N, E_global, expert_map, E,
+                                       topk, score_fn, n_groups, topk_groups,
+                                       apply_router_weight_on_input, activation, dtype, w1,
+                                       w1_scales, w2, w2_scales, out, ws, ws_bytes);
+  if (st != GBMOE_OK) return st;
+  if (!gemm_shape_ok(M, 1, 1, Ns, K, GBMOE_BF16)) return GBMOE_INVALID_ARG;
+  if (M > 0) {
+    if (!w1s || !w2s || !out_shared || !ws_shared || !aligned16(w1s) || !aligned16(w2s) ||
+        !aligned16(out_shared) || !aligned16(ws_shared))
+      return GBMOE_INVALID_ARG;
+    if (ws_shared_bytes < moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1, GBMOE_BF16))
+      return GBMOE_INVALID_ARG;
+  }
+  if (aux_stream && (!ev_input_ready || !ev_output_ready)) return GBMOE_INVALID_ARG;
+  int sms;
+  st = device_info(&sms);
+  if (st != GBMOE_OK || M == 0) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaStream_t aux = (cudaStream_t)aux_stream;
+  cudaEvent_t ev_in = (cudaEvent_t)ev_input_ready, ev_out = (cudaEvent_t)ev_output_ready;
+  if (aux) {
+    // fork: the shared experts on aux_stream once `stream` reaches this point
+    cudaError_t ce = cudaEventRecord(ev_in, s);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(aux, ev_in, 0);
+    if (ce != cudaSuccess) return from_cuda(ce);
+    gbmoe_status_t st1 = moe_shared_expert_forward(x, M, K, Ns, w1s, w2s, GBMOE_BF16,
+                                                   activation, out_shared, ws_shared,
+                                                   ws_shared_bytes, err_word, aux_stream);
+    cudaError_t ce1 = cudaEventRecord(ev_out, aux);
+    // the routed experts on `stream` meanwhile
+    gbmoe_status_t st2 = moe_forward(x, logits, bias, M, K, N, E_global, expert_map, E, topk,
+                                     score_fn, n_groups, topk_groups, renormalize,
+                                     apply_router_weight_on_input, activation, dtype, w1,
+                                     w1_scales, w2, w2_scales, out, nullptr, nullptr, ws,
+                                     ws_bytes, err_word, stream);
+    // join (always, so that `stream` never runs ahead of aux_stream's work)
+    cudaError_t ce2 = ce1 == cudaSuccess ? cudaStreamWaitEvent(s, ev_out, 0) : ce1;
+    if (st1 != GBMOE_OK) return st1;
+    if (st2 != GBMOE_OK) return st2;
+    return from_cuda(ce2);
+  }
+  st = moe_shared_expert_forward(x, M, K, Ns, w1s, w2s, GBMOE_BF16, activation, out_shared,
+                                 ws_shared, ws_shared_bytes, err_word, stream);
+  if (st != GBMOE_OK) return st;
+  return moe_forward(x, logits, bias, M, K, N, E_global, expert_map, E, topk, score_fn,
+                     n_groups, topk_groups, renormalize, apply_router_weight_on_input,
+                     activation, dtype, w1, w1_scales, w2, w2_scales, out, nullptr, nullptr,
+                     ws, ws_bytes, err_word, stream);
 }
 
 }  // extern "C"

@@ -339,7 +339,7 @@ cudaError_t launch_bf16(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   p.err = a.err;
   // upper bound on the tiles: every expert may end with a partial m-tile
   long long mtiles = a.offsets ? (a.a_rows + kBM - 1) / kBM + a.E
-                               : (long long)a.E * ((a.T + kBM - 1) / kBM);
+                               : (long long)a.E * ((a.T + kBM - 1) / kBM);  // batched / dense
   long long tiles = mtiles * p.n_tiles;
   int grid = (int)(tiles < num_sms ? tiles : num_sms);
   if (grid < 1) grid = 1;

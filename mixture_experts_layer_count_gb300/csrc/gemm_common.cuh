@@ -22,7 +22,9 @@ constexpr int kBStage = kBN * kBKB;  // 32 KB
 constexpr int kMaxE = 512;
 
 // Rows of expert e: Standard format [offsets[e], offsets[e+1]); Batched
-// format [e*T, e*T + min(max(counts[e], 0), T)).  Fills rbase / rcnt and
+// format [e*T, e*T + min(max(counts[e], 0), T)); dense (offsets and counts
+// both NULL: every expert has all T rows, as the shared expert does)
+// [e*T, e*T + T).  Fills rbase / rcnt and
 // prefix[e+1] = tiles of expert e (m-tiles x n_tiles).  All threads of the
 // block take part; a __syncthreads must follow before tile_table_scan.
 __device__ __forceinline__ void tile_table_fill(const int32_t *offsets,
@@ -36,7 +38,7 @@ __device__ __forceinline__ void tile_table_fill(const int32_t *offsets,
       b = offsets[e];
       r = offsets[e + 1] - b;
     } else {
-      r = counts[e];
+      r = counts ? counts[e] : T;
       if (r < 0 || r > T) {
         if (blockIdx.x == 0) set_err(err, GBMOE_ERR_COUNT_RANGE);
         r = r < 0 ? 0 : T;
