@@ -318,6 +318,27 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                            float *topk_weights, void *ws, size_t ws_bytes,
                            int32_t *err_word, gbmoe_stream_t stream);
 
+/* moe_forward in chunks of at most chunk_size tokens, one after the other on
+ * `stream`, as FusedMoEModularKernel._maybe_chunk_fused_experts does to bound
+ * its workspaces -- but with every chunk's counts computed on the device (the
+ * pages copy them to the host per chunk), so the whole loop stays
+ * capturable.  Each token's result is the same as unchunked, bit for bit.
+ * Arguments as moe_forward (topk_ids / topk_weights may be NULL);
+ * ws: moe_workspace_size(GBMOE_WS_FORWARD, min(M, chunk_size), E, N, K,
+ * topk, dtype) bytes. */
+gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
+                                   const float *bias, int M, int K, int N,
+                                   int E_global, const int32_t *expert_map,
+                                   int E, int topk, int score_fn, int n_groups,
+                                   int topk_groups, int renormalize,
+                                   int apply_router_weight_on_input,
+                                   int activation, int dtype, const void *w1,
+                                   const float *w1_scales, const void *w2,
+                                   const float *w2_scales, uint16_t *out,
+                                   int32_t *topk_ids, float *topk_weights,
+                                   int chunk_size, void *ws, size_t ws_bytes,
+                                   int32_t *err_word, gbmoe_stream_t stream);
+
 /* The shared experts of the layer: a dense gated MLP applied to every token
  * (the shared_experts of FusedMoEModularKernel.forward, whose output it
  * returns beside the routed one; the SharedExperts page runs them on an

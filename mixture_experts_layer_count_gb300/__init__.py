@@ -48,6 +48,8 @@ _SIGS = {
     "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_count_expert_tokens": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_align_permute": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
+    "moe_forward_chunked": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
+                                 _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
     "moe_shared_expert_forward": (_I, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _Z, _P, _P]),
     "moe_forward_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
                                 _I, _I, _P, _P, _P, _P, _P, _P, _Z, _I, _P, _P, _P, _P,
@@ -245,6 +247,23 @@ def moe_forward(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
         _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
         _stream(stream)))
+
+
+def moe_forward_chunked(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
+                        renormalize, dtype, w1, w1_scales, w2, w2_scales, out, ws,
+                        chunk_size, topk_ids=None, topk_weights=None, err_word=None,
+                        stream=None, expert_map=None, apply_router_weight_on_input=False,
+                        activation=ACT_SILU):
+    """moe_forward in chunks of chunk_size tokens (ws sized for one chunk)."""
+    M, K = x.shape
+    E_global = logits.shape[1]
+    _check("moe_forward_chunked", load().moe_forward_chunked(
+        _ptr(x), _ptr(logits), _ptr(bias), M, K, N, E_global, _ptr(expert_map), E,
+        topk, score_fn, n_groups, topk_groups, int(renormalize),
+        int(apply_router_weight_on_input), int(activation), dtype, _ptr(w1),
+        _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids),
+        _ptr(topk_weights), int(chunk_size), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(err_word), _stream(stream)))
 
 
 def moe_shared_expert_forward(x, Ns, w1s, w2s, out_shared, ws, dtype=BF16,

@@ -565,6 +565,41 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   return from_cuda(launch_reduce(w.y_slot, w.inv, M, topk, K, out, sms, s));
 }
 
+gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
+                                   const float *bias, int M, int K, int N,
+                                   int E_global, const int32_t *expert_map,
+                                   int E, int topk, int score_fn, int n_groups,
+                                   int topk_groups, int renormalize,
+                                   int apply_router_weight_on_input,
+                                   int activation, int dtype, const void *w1,
+                                   const float *w1_scales, const void *w2,
+                                   const float *w2_scales, uint16_t *out,
+                                   int32_t *topk_ids, float *topk_weights,
+                                   int chunk_size, void *ws, size_t ws_bytes,
+                                   int32_t *err_word, gbmoe_stream_t stream) {
+  if (chunk_size < 1) return GBMOE_INVALID_ARG;
+  const int CS = M < chunk_size ? M : chunk_size;
+  // validate once with the chunk's size (the workspace is sized for it)
+  gbmoe_status_t st = forward_validate(x, logits, bias, CS, K, N, E_global, expert_map, E,
+                                       topk, score_fn, n_groups, topk_groups,
+                                       apply_router_weight_on_input, activation, dtype, w1,
+                                       w1_scales, w2, w2_scales, out, ws, ws_bytes);
+  if (st != GBMOE_OK) return st;
+  if (M < 0) return GBMOE_INVALID_ARG;
+  for (int t0 = 0; t0 < M; t0 += CS) {
+    const int m = M - t0 < CS ? M - t0 : CS;
+    st = moe_forward(x + (size_t)t0 * K, logits + (size_t)t0 * E_global, bias, m, K, N,
+                     E_global, expert_map, E, topk, score_fn, n_groups, topk_groups,
+                     renormalize, apply_router_weight_on_input, activation, dtype, w1,
+                     w1_scales, w2, w2_scales, out + (size_t)t0 * K,
+                     topk_ids ? topk_ids + (size_t)t0 * topk : nullptr,
+                     topk_weights ? topk_weights + (size_t)t0 * topk : nullptr, ws, ws_bytes,
+                     err_word, stream);
+    if (st != GBMOE_OK) return st;
+  }
+  return GBMOE_OK;
+}
+
 gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K,
                                          int Ns, const void *w1s,
                                          const void *w2s, int dtype,
