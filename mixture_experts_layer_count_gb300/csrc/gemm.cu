@@ -368,9 +368,21 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int kind, uint64_t cols,
   return r == CUDA_SUCCESS;
 }
 
+bool bf16_uses_cta_pairs(const GroupedGemmArgs &a) {
+  // Row capacity the launch covers: Standard format the M*topk permuted rows,
+  // BatchedExperts / dense E*T.  CTA pairs (256-row tiles) when the experts
+  // average 128 rows or more; below that a pair tile is mostly padding, and
+  // the 1-SM kernel keeps more weight bytes in flight per SM (4 stages x
+  // 32 KB of B against 6 x 16 KB), which is what a weight-streaming launch
+  // (decode) needs.
+  const long long rows = a.offsets ? (long long)a.a_rows : (long long)a.T * a.E;
+  return rows >= 128LL * a.E;
+}
+
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,
                                 cudaStream_t s) {
   if (a.fp8) return launch_grouped_gemm_fp8(a, num_sms, s);
+  if (bf16_uses_cta_pairs(a)) return launch_grouped_gemm_pair(a, num_sms, s);
   if (a.mode == kDown) return launch_bf16<kDownMode, kActSilu>(a, num_sms, s);
   return a.act == GBMOE_ACT_GELU ? launch_bf16<kGateUpMode, kActGelu>(a, num_sms, s)
                                  : launch_bf16<kGateUpMode, kActSilu>(a, num_sms, s);

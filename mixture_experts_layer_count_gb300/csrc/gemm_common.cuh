@@ -31,7 +31,7 @@ __device__ __forceinline__ void tile_table_fill(const int32_t *offsets,
                                                 const int32_t *counts, int E,
                                                 int T, int n_tiles, int *prefix,
                                                 int *rbase, int *rcnt,
-                                                int32_t *err) {
+                                                int32_t *err, int bm = kBM) {
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int b, r;
     if (offsets) {
@@ -47,7 +47,7 @@ __device__ __forceinline__ void tile_table_fill(const int32_t *offsets,
     }
     rbase[e] = b;
     rcnt[e] = r;
-    prefix[e + 1] = ((r + kBM - 1) / kBM) * n_tiles;
+    prefix[e + 1] = ((r + bm - 1) / bm) * n_tiles;
   }
 }
 

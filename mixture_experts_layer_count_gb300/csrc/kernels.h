@@ -75,6 +75,11 @@ struct GroupedGemmArgs {
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,
                                 cudaStream_t s);
+// whether launch_grouped_gemm runs a bf16 launch on CTA pairs (gemm2sm.cu)
+bool bf16_uses_cta_pairs(const GroupedGemmArgs &a);
+// gemm2sm.cu: bf16 on CTA pairs (cta_group::2, 256 x 256 tiles)
+cudaError_t launch_grouped_gemm_pair(const GroupedGemmArgs &a, int num_sms,
+                                     cudaStream_t s);
 // gemm_fp8.cu
 cudaError_t launch_grouped_gemm_fp8(const GroupedGemmArgs &a, int num_sms,
                                     cudaStream_t s);

@@ -47,8 +47,9 @@ def _check_rows(cfg, d, yb, W, rows=None):
         assert np.all(bits[e, c:] == np.int16(SENTINEL)), f"padded rows of expert {e} written"
 
 
-def test_batched_small_all_rows():
-    cfg = WL.SMALL_BATCHED
+@pytest.mark.parametrize("cfg", [WL.SMALL_BATCHED, WL.SMALL_BATCHED_SHORT],
+                         ids=lambda c: c.name)
+def test_batched_small_all_rows(cfg):
     d = WL.make_inputs(cfg, DEV)
     g = gbmoe()
     yb = _fresh(cfg)

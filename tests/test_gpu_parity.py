@@ -165,8 +165,11 @@ def _stage_inputs(cfg):
     return d, rid, rw, ids, wts, offsets, srt, inv
 
 
-@pytest.mark.parametrize("cfg", [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.SMALL_FP8],
-                         ids=lambda c: c.name)
+SMALL_STANDARD = [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.SMALL_FP8, WL.SMALL_PAIR,
+                  WL.SMALL_PAIR_TOP2]
+
+
+@pytest.mark.parametrize("cfg", SMALL_STANDARD, ids=lambda c: c.name)
 def test_gate_up_then_down_stages(cfg):
     """Each grouped GEMM against the oracle's expert rows."""
     g = gbmoe()
@@ -223,8 +226,7 @@ def test_gate_up_then_down_stages(cfg):
     assert_close_rel(ygot, yref, TOL[cfg.dtype], "weighted y")
 
 
-@pytest.mark.parametrize("cfg", [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.SMALL_FP8],
-                         ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", SMALL_STANDARD, ids=lambda c: c.name)
 def test_forward_parity_small(cfg):
     d = WL.make_inputs(cfg, DEV)
     gw = GpuWeights(cfg, d["w1"], d["w2"])
@@ -270,11 +272,14 @@ def test_forward_edge_sizes(M):
     assert_close_rel(out.float().cpu().numpy(), ref, TOL[cfg.dtype], f"M={M}")
 
 
-def test_one_expert_takes_every_token_matches_torch_matmul():
+@pytest.mark.parametrize("M", [300, 600])
+def test_one_expert_takes_every_token_matches_torch_matmul(M):
     """All tokens on one expert: the grouped GEMMs reduce to dense matmuls,
-    checked against torch's own bf16 matmul on the GPU (a second reference)."""
+    checked against torch's own bf16 matmul on the GPU (a second reference).
+    M = 600 over 4 experts runs on CTA pairs (two full 256-row tiles and a
+    tail of 88), M = 300 on the 1-SM kernel."""
     g = gbmoe()
-    cfg = WL.MoEConfig("one", M=300, K=512, N=256, E=4, topk=1, seed=6)
+    cfg = WL.MoEConfig("one", M=M, K=512, N=256, E=4, topk=1, seed=6)
     d = WL.make_inputs(cfg, DEV)
     d["logits"][:, 2] += 100.0  # every token picks expert 2
     out, ids, wts, err = run_forward(cfg, d, GpuWeights(cfg, d["w1"], d["w2"]))

@@ -86,6 +86,18 @@ SMALL_FP8 = MoEConfig("small_fp8_M256_K512_N256_E16_top4", M=256, K=512, N=256,
 SMALL_BATCHED = MoEConfig("small_batched_bf16_E6_T200_K256_N256", M=200, K=256,
                           N=256, E=6, topk=1, batched=True, seed=14)
 
+# Small cases whose experts average 128 rows or more (M*topk >= 128*E, or
+# T >= 128 for the batched format): the bf16 GEMMs run on CTA pairs with
+# 256-row tiles, here with ragged last tiles in M and, for K = 640, a down
+# n-tile of 128 columns.  SMALL_BATCHED_SHORT (T < 128) stays on the 1-SM
+# kernel.
+SMALL_PAIR = MoEConfig("small_pair_bf16_M300_K384_N256_E2_top1", M=300, K=384,
+                       N=256, E=2, topk=1, seed=15)
+SMALL_PAIR_TOP2 = MoEConfig("small_pair_bf16_M520_K640_N384_E4_top2", M=520, K=640,
+                            N=384, E=4, topk=2, seed=16)
+SMALL_BATCHED_SHORT = MoEConfig("small_batched_bf16_E5_T100_K384_N256", M=100, K=384,
+                                N=256, E=5, topk=1, batched=True, seed=17)
+
 ALL = [TINY, MIXTRAL_PREFILL, DSV3_PREFILL_FP8, DSV3_DECODE, BATCHED_MASKED]
 
 # Small cases of the same kernels for profiler captures: operands larger than
@@ -100,7 +112,8 @@ PROFILE_DECODE = MoEConfig("profile_decode_bf16_M16_K7168_N2048_E32_top4", M=16,
                            n_groups=4, topk_groups=2, seed=23)
 
 BY_NAME = {c.name: c for c in ALL + [SMALL_BF16, SMALL_SIGMOID, SMALL_FP8,
-                                     PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE]}
+                                     SMALL_BATCHED, SMALL_PAIR, SMALL_PAIR_TOP2,
+                                     SMALL_BATCHED_SHORT, PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE]}
 
 
 def _gen(seed: int, device) -> torch.Generator:
