@@ -21,7 +21,8 @@ def _lib():
     gbmoe()
 
 
-@pytest.mark.parametrize("cfg", [WL.SMALL_BF16, WL.SMALL_FP8, WL.SMALL_PAIR_TOP2],
+@pytest.mark.parametrize("cfg", [WL.SMALL_BF16, WL.SMALL_FP8, WL.SMALL_PAIR_TOP2,
+                                 WL.SMALL_FP8_K640],
                          ids=lambda c: c.name)
 def test_forward_gelu(cfg):
     g = gbmoe()

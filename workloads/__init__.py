@@ -95,6 +95,9 @@ SMALL_PAIR = MoEConfig("small_pair_bf16_M300_K384_N256_E2_top1", M=300, K=384,
                        N=256, E=2, topk=1, seed=15)
 SMALL_PAIR_TOP2 = MoEConfig("small_pair_bf16_M520_K640_N384_E4_top2", M=520, K=640,
                             N=384, E=4, topk=2, seed=16)
+# e4m3 with a down n-tile of 128 columns (K = 640) and 150 rows per expert
+SMALL_FP8_K640 = MoEConfig("small_fp8_M300_K640_N256_E4_top2", M=300, K=640, N=256,
+                           E=4, topk=2, dtype=FP8, seed=18)
 SMALL_BATCHED_SHORT = MoEConfig("small_batched_bf16_E5_T100_K384_N256", M=100, K=384,
                                 N=256, E=5, topk=1, batched=True, seed=17)
 
@@ -112,7 +115,7 @@ PROFILE_DECODE = MoEConfig("profile_decode_bf16_M16_K7168_N2048_E32_top4", M=16,
                            n_groups=4, topk_groups=2, seed=23)
 
 BY_NAME = {c.name: c for c in ALL + [SMALL_BF16, SMALL_SIGMOID, SMALL_FP8,
-                                     SMALL_BATCHED, SMALL_PAIR, SMALL_PAIR_TOP2,
+                                     SMALL_BATCHED, SMALL_PAIR, SMALL_PAIR_TOP2, SMALL_FP8_K640,
                                      SMALL_BATCHED_SHORT, PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE]}
 
 
