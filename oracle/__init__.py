@@ -27,7 +27,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-BF16, FP8 = 0, 1
+BF16, FP8, FP8_CHANNEL = 0, 1, 2  # FP8: 1x128 / 128x128 scales; FP8_CHANNEL: per token / per row
 SOFTMAX, SIGMOID = 0, 1
 SILU, GELU = 0, 1
 
@@ -222,13 +222,15 @@ def quant_fp8_block(w_bf16_bits, block=128):
 
 
 class Weights:
-    """Expert weights as the oracle reads them: bf16 bits (dtype BF16) or
-    e4m3 codes plus 128 x 128 block scales (dtype FP8), one block per expert.
+    """Expert weights as the oracle reads them: bf16 bits (dtype BF16), or
+    e4m3 codes plus 128 x 128 block scales (dtype FP8), or e4m3 codes plus
+    one scale per row (dtype FP8_CHANNEL), one block per expert.
 
     Either pass full arrays w1 (E, 2N, K), w2 (E, K, N) [+ w1s (E, 2N/128,
-    K/128), w2s (E, K/128, N/128)], or ``experts={e: (w1e, w2e[, w1se,
-    w2se])}`` with ``E, N, K`` for a subset of the experts (the rest are
-    absent; routing a computed token to one of them is a caller error)."""
+    K/128), w2s (E, K/128, N/128) for FP8; w1s (E, 2N), w2s (E, K) for
+    FP8_CHANNEL], or ``experts={e: (w1e, w2e[, w1se, w2se])}`` with
+    ``E, N, K`` for a subset of the experts (the rest are absent; routing a
+    computed token to one of them is a caller error)."""
 
     def __init__(self, dtype, w1=None, w2=None, w1s=None, w2s=None,
                  experts=None, E=None, N=None, K=None, act=SILU):
@@ -244,7 +246,7 @@ class Weights:
             experts = {}
             for e in range(self.E):
                 blk = (w1[e], w2[e])
-                if dtype == FP8:
+                if dtype != BF16:
                     blk = blk + (_c(w1s, np.float32)[e], _c(w2s, np.float32)[e])
                 experts[e] = blk
         else:
@@ -258,7 +260,7 @@ class Weights:
             blk[1] = _c(blk[1], bits)
             assert blk[0].shape == (2 * self.N, self.K), blk[0].shape
             assert blk[1].shape == (self.K, self.N), blk[1].shape
-            if dtype == FP8:
+            if dtype != BF16:
                 blk[2] = _c(blk[2], np.float32)
                 blk[3] = _c(blk[3], np.float32)
             self._keep.append(blk)

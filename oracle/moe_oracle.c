@@ -61,6 +61,13 @@
  *      ids of this shard, -1 = not here (the pair adds nothing);
  *      apply_router_weight_on_input (prepare, forward; topk 1): the router
  *      weight multiplies the expert's input, not its output.
+ *   Q6 per_act_token_quant with per_out_ch_quant (the quant config's
+ *      properties on FusedMoEPermuteExpertsUnpermute): the Q1 rule with one
+ *      group per row -- one scale per token over its K values, one scale per
+ *      output channel (row) of w1 and w2.  The hidden row h is kept in
+ *      bf16 between the GEMMs (the activations' dtype) and quantised per
+ *      token over its N values before the second GEMM, as prepare
+ *      quantises the input of the experts.
  */
 #include <math.h>
 #include <stdint.h>
@@ -71,7 +78,9 @@
 #include <omp.h>
 #endif
 
-enum { ORC_BF16 = 0, ORC_FP8 = 1 };
+/* ORC_FP8: 1 x 128 activation groups, 128 x 128 weight blocks (Q1, Q2);
+ * ORC_FP8_CHANNEL: one scale per token and one per weight row (Q6) */
+enum { ORC_BF16 = 0, ORC_FP8 = 1, ORC_FP8_CHANNEL = 2 };
 enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
 /* FusedMoEPermuteExpertsUnpermute.activation: "silu" -> silu_and_mul,
  * "gelu" -> gelu_and_mul */
@@ -521,7 +530,8 @@ void orc_quant_fp8_block(const uint16_t *w, int R, int C, int block,
  * caller did not supply; using one is an error the caller must avoid).
  * dtype ORC_BF16: w1[e] (2N, K) and w2[e] (K, N) hold bf16 bits.  ORC_FP8:
  * they hold e4m3 codes, and w1s[e] (2N/128, K/128), w2s[e] (K/128, N/128)
- * hold the 128 x 128 block scales. */
+ * hold the 128 x 128 block scales.  ORC_FP8_CHANNEL: e4m3 codes with one
+ * scale per row, w1s[e] (2N), w2s[e] (K). */
 typedef struct {
     int dtype, E, N, K;
     int act; /* ORC_SILU or ORC_GELU: the gated activation of the experts */
@@ -541,13 +551,28 @@ static double weight_at(const orc_weights *W, int which, int e, int row,
     } else {
         const uint8_t *q = (const uint8_t *)(which == 1 ? W->w1[e] : W->w2[e]);
         const float *sc = which == 1 ? W->w1s[e] : W->w2s[e];
-        size_t sidx = (size_t)(row / 128) * (C / 128) + col / 128;
+        size_t sidx = W->dtype == ORC_FP8_CHANNEL
+                          ? (size_t)row
+                          : (size_t)(row / 128) * (C / 128) + col / 128;
         return e4m3_table[q[idx]] * (double)sc[sidx];
     }
 }
 
-/* h (N) = silu(x W1[e][0:N]^T) * (x W1[e][N:2N]^T); optional Q5 requant of
- * h; y (K) = h W2[e]^T.  x is the (dequantised) input row of K values. */
+/* bf16 rounding (nearest, ties to even) of the fp32 rounding of v */
+static double bf16_round(double v)
+{
+    float f = (float)v;
+    uint32_t u;
+    uint16_t h;
+    memcpy(&u, &f, 4);
+    h = (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+    return bf16_value(h);
+}
+
+/* h (N) = silu(x W1[e][0:N]^T) * (x W1[e][N:2N]^T); optional requant of h
+ * (Q5: 128-wide groups of the fp32 h; Q6 for ORC_FP8_CHANNEL: h rounded to
+ * bf16, then one group of N); y (K) = h W2[e]^T.  x is the (dequantised)
+ * input row of K values. */
 static void expert_row(const orc_weights *W, int e, const double *x,
                        int requant_h, double *h, double *y)
 {
@@ -564,16 +589,19 @@ static void expert_row(const orc_weights *W, int e, const double *x,
             h[n] = g / (1.0 + exp(-g)) * u;                  /* SiLU */
     }
     if (requant_h) {
-        int gi;
-        for (gi = 0; gi < N / 128; ++gi) {
+        int gi, gw = W->dtype == ORC_FP8_CHANNEL ? N : 128;
+        if (W->dtype == ORC_FP8_CHANNEL)
+            for (n = 0; n < N; ++n)
+                h[n] = bf16_round(h[n]);
+        for (gi = 0; gi < N / gw; ++gi) {
             float amax = 0.0f, s;
-            for (n = gi * 128; n < (gi + 1) * 128; ++n) {
+            for (n = gi * gw; n < (gi + 1) * gw; ++n) {
                 float v = (float)fabs((float)h[n]);
                 if (v > amax)
                     amax = v;
             }
             s = group_scale(amax);
-            for (n = gi * 128; n < (gi + 1) * 128; ++n)
+            for (n = gi * gw; n < (gi + 1) * gw; ++n)
                 h[n] = orc_e4m3_value(orc_e4m3_encode((float)h[n] / s)) *
                        (double)s;
         }
@@ -588,8 +616,8 @@ static void expert_row(const orc_weights *W, int e, const double *x,
 
 /* Input row t of x (M, K) bf16 times `scale`, as the experts see it: the
  * product as is for bf16, or through Q1 (groups of 128, with the product
- * formed in fp32) for FP8.  scale is 1 except with
- * apply_router_weight_on_input. */
+ * formed in fp32) for FP8, or through Q6 (one group of K) for
+ * ORC_FP8_CHANNEL.  scale is 1 except with apply_router_weight_on_input. */
 static void input_row_scaled(int dtype, const uint16_t *x, int t, int K,
                              double scale, double *xr)
 {
@@ -600,11 +628,12 @@ static void input_row_scaled(int dtype, const uint16_t *x, int t, int K,
             xr[k] = bf16_value(row[k]) * scale;
     } else {
         float fs = (float)scale;
+        int group = dtype == ORC_FP8_CHANNEL ? K : 128;
         uint8_t *q = (uint8_t *)malloc((size_t)K);
-        float *s = (float *)malloc(sizeof(float) * (size_t)(K / 128));
-        orc_quant_fp8_group_w(row, &fs, 1, K, 128, q, s);
+        float *s = (float *)malloc(sizeof(float) * (size_t)(K / group));
+        orc_quant_fp8_group_w(row, &fs, 1, K, group, q, s);
         for (k = 0; k < K; ++k)
-            xr[k] = orc_e4m3_value(q[k]) * (double)s[k / 128];
+            xr[k] = orc_e4m3_value(q[k]) * (double)s[k / group];
         free(q);
         free(s);
     }

@@ -440,3 +440,58 @@ def test_gelu_experts_are_dense_geglu(orc):
     Ws = orc.Weights(orc.BF16, _bits(d["w1"]), _bits(d["w2"]))
     silu, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1, orc.SOFTMAX, Ws)
     assert np.abs(silu - out).max() > 1e-3 * np.abs(out).max()
+
+
+def _rowwise_quant_torch(a32):
+    """Per-row e4m3 quantisation written with numpy and torch's cast:
+    s = max(amax, 1e-12) / 448 in fp32, codes = cast of the fp32 quotient."""
+    a32 = np.asarray(a32, np.float32)
+    s = (np.maximum(np.abs(a32).max(axis=1), np.float32(1e-12)) / np.float32(448)).astype(np.float32)
+    q = torch.from_numpy(a32 / s[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return q, s
+
+
+def test_fp8_channel_quant_is_one_group_per_row(orc):
+    """Per-token activations and per-channel weights: the group rule with a
+    group as wide as the row equals the per-row formula and torch's cast."""
+    g = torch.Generator().manual_seed(41)
+    x = (torch.randn((7, 384), generator=g) * torch.linspace(0.01, 30, 384)).to(torch.bfloat16)
+    q, s = orc.quant_fp8_group(_bits(x), group=384)
+    qr, sr = _rowwise_quant_torch(x.float().numpy())
+    assert s.shape == (7, 1)
+    np.testing.assert_array_equal(s[:, 0], sr)
+    np.testing.assert_array_equal(q, qr)
+
+
+def test_fp8_channel_single_expert_is_dequantised_swiglu(orc):
+    """FP8 with one scale per token and per weight row: with E = 1 the layer
+    is the dense SwiGLU MLP of the dequantised operands; with requantisation
+    the hidden row goes to bf16 and then through one scale over its N
+    values (the per-row rule applied by torch's casts)."""
+    cfg = WL.MoEConfig("f8c", M=6, K=256, N=256, E=1, topk=1, seed=25)  # N > 128: a row is not one 128-group
+    d = WL.make_inputs(cfg)
+    q1, s1 = _rowwise_quant_torch(d["w1"][0].float().numpy())
+    q2, s2 = _rowwise_quant_torch(d["w2"][0].float().numpy())
+    W = orc.Weights(orc.FP8_CHANNEL, q1[None], q2[None], s1[None], s2[None])
+
+    def deq(q, s):
+        return torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy() * s.astype(np.float64)[:, None]
+
+    qx, sx = _rowwise_quant_torch(d["x"].float().numpy())
+    x = deq(qx, sx)
+    w1, w2 = deq(q1, s1), deq(q2, s2)
+    N = cfg.N
+    h = _silu(x @ w1[:N].T) * (x @ w1[N:].T)
+    out, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1,
+                                orc.SOFTMAX, W, requant_h=False)
+    np.testing.assert_allclose(out, h @ w2.T, rtol=1e-10, atol=1e-12)
+
+    hb = torch.from_numpy(h.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    qh, sh = _rowwise_quant_torch(hb)
+    hd = deq(qh, sh)
+    for t in (0, 3, 5):
+        hq, y = orc.expert_row(_bits(d["x"]), t, 0, W, requant_h=True)
+        assert np.mean(np.abs(hq - hd[t]) <= 1e-12) > 0.99
+        np.testing.assert_allclose(hq, hd[t], rtol=0, atol=float(sh[t]) * 2 ** -3 + 1e-12)
+        ref = hd[t] @ w2.T
+        np.testing.assert_allclose(y, ref, rtol=0, atol=2e-3 * np.abs(ref).max())
