@@ -157,8 +157,20 @@ class Layer:
         self.x, self.logits, self.bias = d["x"], d["logits"], d["bias"]
         M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
         P = M * k
-        self.fp8 = cfg.dtype == WL.FP8
-        if self.fp8:
+        self.fp8 = cfg.dtype != WL.BF16
+        self.ch = cfg.dtype == WL.FP8_CHANNEL  # one scale per token / per weight row
+        if self.ch:
+            self.w1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=device)
+            self.w2 = torch.empty((E, K, N), dtype=torch.uint8, device=device)
+            self.w1s = torch.empty((E, 2 * N), dtype=torch.float32, device=device)
+            self.w2s = torch.empty((E, K), dtype=torch.float32, device=device)
+            g.moe_quant_fp8_group(d["w1"].view(E * 2 * N, K), self.w1.view(E * 2 * N, K),
+                                  self.w1s.view(E * 2 * N, 1), group=K)
+            g.moe_quant_fp8_group(d["w2"].view(E * K, N), self.w2.view(E * K, N),
+                                  self.w2s.view(E * K, 1), group=N)
+            del d
+            torch.cuda.empty_cache()
+        elif self.fp8:
             self.w1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=device)
             self.w2 = torch.empty((E, K, N), dtype=torch.uint8, device=device)
             self.w1s = torch.empty((E, 2 * N // 128, K // 128), dtype=torch.float32, device=device)
@@ -178,18 +190,26 @@ class Layer:
         self.inv = torch.empty(P, dtype=i32, device=device)
         self.align_ws = g.workspace(g.WS_ALIGN, M, E, 0, 0, k, 0, device=device)
         adt = torch.uint8 if self.fp8 else torch.bfloat16
+        sk = 1 if self.ch else K // 128   # scales per row of x / A
         self.xq = torch.empty((M, K), dtype=torch.uint8, device=device) if self.fp8 else None
-        self.xs = torch.empty((M, K // 128), dtype=f32, device=device) if self.fp8 else None
+        self.xs = torch.empty((M, sk), dtype=f32, device=device) if self.fp8 else None
         self.A = torch.empty((P, K), dtype=adt, device=device)
         ld = (P + 3) // 4 * 4  # group-major FP8 row scales
-        self.As = torch.empty((K // 128, ld), dtype=f32, device=device) if self.fp8 else None
-        self.H = torch.empty((P, N), dtype=adt, device=device)
-        self.Hs = torch.empty((N // 128, ld), dtype=f32, device=device) if self.fp8 else None
+        self.As = torch.empty((sk, ld), dtype=f32, device=device) if self.fp8 else None
+        if self.ch:  # H in bf16 from gate/up, then its per-token e4m3 codes
+            self.Hb = torch.empty((P, N), dtype=torch.bfloat16, device=device)
+            self.H = torch.empty((P, N), dtype=torch.uint8, device=device)
+            self.Hs = torch.empty((P, 1), dtype=f32, device=device)
+        else:
+            self.Hb = None
+            self.H = torch.empty((P, N), dtype=adt, device=device)
+            self.Hs = torch.empty((N // 128, ld), dtype=f32, device=device) if self.fp8 else None
         self.y = torch.empty((M, k, K), dtype=torch.bfloat16, device=device)
         self.out = torch.empty((M, K), dtype=torch.bfloat16, device=device)
         self.err = torch.zeros(1, dtype=i32, device=device)
         self.fwd_ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype, device=device)
-        self.launches_per_step = 8 + (1 if self.fp8 else 0)  # route, 3 align, [quant], gather, 2 GEMMs, reduce
+        # route, 3 align, [quant x], gather, gate/up, [quant H], down, reduce
+        self.launches_per_step = 8 + (1 if self.fp8 else 0) + (1 if self.ch else 0)
 
     def step(self, ev_gemm=None):
         g, c = self.g, self.cfg
@@ -200,15 +220,18 @@ class Layer:
                             self.align_ws, self.err)
         src, src_s = self.x, None
         if self.fp8:
-            g.moe_quant_fp8_group(self.x, self.xq, self.xs)
+            g.moe_quant_fp8_group(self.x, self.xq, self.xs, group=K if self.ch else 128)
             src, src_s = self.xq, self.xs
         g.moe_permute_rows(src, src_s, self.sorted, self.offsets, k, E, c.dtype, self.A, self.As)
         if ev_gemm is not None:
             ev_gemm[0].record()
         g.moe_grouped_gemm_gate_up_silu(self.A, self.As, self.offsets, M, k, E, N, K, self.w1,
-                                        self.w1s, c.dtype, self.H, self.Hs, self.err)
+                                        self.w1s, c.dtype, self.Hb if self.ch else self.H,
+                                        self.Hs, self.err)
         if ev_gemm is not None:
             ev_gemm[1].record()
+        if self.ch:
+            g.moe_quant_fp8_group(self.Hb, self.H, self.Hs, group=N)
         g.moe_grouped_gemm_down(self.H, self.Hs, self.sorted, self.offsets, self.wts, M, k, E,
                                 N, K, self.w2, self.w2s, c.dtype, self.y, self.err)
         g.moe_unpermute_weighted_reduce(self.y, self.inv, M, k, K, self.out)
@@ -330,19 +353,40 @@ def run_gpu(args, cfg):
         pg.destroy_process_group()
 
 
+def _scales_desc(cfg):
+    return {WL.BF16: "none", WL.FP8: "fp32, 1x128 activations / 128x128 weights",
+            WL.FP8_CHANNEL: "fp32, per token / per output channel"}[cfg.dtype]
+
+
+def _gate_up_kernel_name(cfg):
+    """Which kernel runs the gate/up GEMM of a Standard-format workload: the
+    library's dispatch (block-scaled e4m3 on the FP8 kernel, per-channel e4m3
+    on the 1-SM kernel; bf16 on CTA pairs when the experts average 128 rows
+    or more)."""
+    if cfg.dtype == WL.FP8:
+        return "grouped_gemm_fp8_kernel"
+    if cfg.dtype == WL.FP8_CHANNEL:
+        return "grouped_gemm_kernel"
+    pairs = cfg.M * cfg.topk >= 128 * cfg.E
+    return "grouped_gemm_pair_kernel" if pairs else "grouped_gemm_kernel"
+
+
 def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
     """The JSON result line (value fields filled in by the caller)."""
     peaks, src = _peaks()
     P = cfg.M * cfg.topk
-    fp8 = cfg.dtype == WL.FP8
+    fp8 = cfg.dtype != WL.BF16
+    ch = cfg.dtype == WL.FP8_CHANNEL
     eb = 1 if fp8 else 2
     # the dominant kernel: the gate/up grouped GEMM (2/3 of the layer's FLOPs)
     gemm_flop = 4.0 * cfg.K * cfg.N * P
     counts = layer.counts.cpu().numpy()
     touched = int((counts > 0).sum())
+    w1_scales = (2 * cfg.N if ch else (2 * cfg.N // 128) * (cfg.K // 128)) * 4 if fp8 else 0
     gemm_bytes = (touched * 2 * cfg.N * cfg.K * eb            # w1 of the experts with rows
-                  + (touched * (2 * cfg.N // 128) * (cfg.K // 128) * 4 if fp8 else 0)
-                  + P * cfg.K * eb + P * cfg.N * eb)          # A rows read, H written
+                  + touched * w1_scales
+                  + P * cfg.K * eb                            # A rows read
+                  + P * cfg.N * (2 if ch else eb))            # H written (bf16 before its quant)
     tc_time = gemm_flop / (peaks.get("bf16_tflops", 1900.0) * (2 if fp8 else 1) * 1e12)
     hbm_time = gemm_bytes / (peaks.get("hbm_gbs", 6800.0) * 1e9)
     timed_s = ms / 1e3
@@ -360,7 +404,7 @@ def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": f"{src} hbm_gbs (copy)"}
     roof.update({"traffic": _kernel_traffic(cfg, "gate_up"),
-                 "kernel": "grouped_gemm_kernel, gate/up + SiLU*mul",
+                 "kernel": _gate_up_kernel_name(cfg) + ", gate/up + SiLU*mul",
                  "kernel_ms": gemm_avg, "flop_per_launch": gemm_flop,
                  "alg_bytes_per_launch": gemm_bytes, "experts_with_rows": touched})
     layer_flop = 6.0 * cfg.K * cfg.N * P
@@ -378,7 +422,7 @@ def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
         "dtype": "fp8_e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) activations and logits; N(0,1/K), N(0,1/N) weights)",
         "config": {"workload": cfg.name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "E": cfg.E,
-                   "topk": cfg.topk, "format": "standard",
+                   "topk": cfg.topk, "format": "standard", "scales": _scales_desc(cfg),
                    "l2": "no flush; working set > L2 (%.2f GB of expert weights read per step)" %
                          (touched * 3 * cfg.N * cfg.K * eb / 1e9),
                    "parallelism": f"{world} independent replica(s)"},
@@ -519,6 +563,10 @@ def _oracle_inputs(cfg, d, tokens):
         b2 = WL.bf16_bits(d["w2"][e])
         if cfg.dtype == WL.BF16:
             blocks[int(e)] = (b1, b2)
+        elif cfg.dtype == WL.FP8_CHANNEL:
+            q1, s1 = orc.quant_fp8_group(b1, group=cfg.K)
+            q2, s2 = orc.quant_fp8_group(b2, group=cfg.N)
+            blocks[int(e)] = (q1, q2, s1[:, 0], s2[:, 0])
         else:
             q1, s1 = orc.quant_fp8_block(b1)
             q2, s2 = orc.quant_fp8_block(b2)
@@ -582,9 +630,9 @@ def run_reference(args, cfg):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp8_e4m3" if cfg.dtype == WL.FP8 else "bf16", "data": "synthetic",
+            "dtype": "bf16" if cfg.dtype == WL.BF16 else "fp8_e4m3", "data": "synthetic",
             "config": {"workload": cfg.name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "E": cfg.E,
-                       "topk": cfg.topk, "format": "standard",
+                       "topk": cfg.topk, "format": "standard", "scales": _scales_desc(cfg),
                        "sample_tokens_per_step": tokens_per_step},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{tokens_per_step} tokens per step of {cfg.name}"},

@@ -56,8 +56,18 @@ typedef enum {
     GBMOE_CUDA_ERROR = 3
 } gbmoe_status_t;
 
-/* element type of activations / weights fed to the expert GEMMs */
-enum { GBMOE_BF16 = 0, GBMOE_FP8_E4M3 = 1 };
+/* element type of activations / weights fed to the expert GEMMs:
+ * GBMOE_FP8_E4M3          e4m3 with fp32 block scales: 1 x 128 groups of a
+ *                         token's activations, 128 x 128 blocks of weights;
+ * GBMOE_FP8_E4M3_CHANNEL  e4m3 with one fp32 scale per token of the
+ *                         activations and one per output channel (row) of
+ *                         w1 and w2 -- the quant config's
+ *                         per_act_token_quant and per_out_ch_quant
+ *                         (FusedMoEPermuteExpertsUnpermute's quant
+ *                         properties); the scale rule is that of
+ *                         moe_quant_fp8_group with a group as wide as the
+ *                         row. */
+enum { GBMOE_BF16 = 0, GBMOE_FP8_E4M3 = 1, GBMOE_FP8_E4M3_CHANNEL = 2 };
 /* router score function */
 enum { GBMOE_SOFTMAX = 0, GBMOE_SIGMOID = 1 };
 /* gated activation of the experts (FusedMoEPermuteExpertsUnpermute.activation):
@@ -166,7 +176,9 @@ gbmoe_status_t moe_align_permute(const int32_t *topk_ids, int M, int topk,
  *   s = max(max_k |v[t,k]|, 1e-12) / 448   (fp32, IEEE division)
  *   q[t,k] = e4m3(v[t,k] / s)               (round to nearest even, saturating at 448)
  * x (M, K) bf16; row_weights (M) fp32 or NULL; q (M, K) e4m3 out;
- * scales (M, K/group) fp32 out.  group must be 128 and K % 128 == 0. */
+ * scales (M, K/group) fp32 out.  group must be 128 or K (one group per row:
+ * the per-token scales of GBMOE_FP8_E4M3_CHANNEL, and with x = a weight
+ * tensor viewed as (E*R, C), its per-channel scales); K % 128 == 0. */
 gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, const float *row_weights,
                                    int M, int K, int group, uint8_t *q,
                                    float *scales, gbmoe_stream_t stream);
@@ -194,6 +206,9 @@ gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
  *   of consecutive rows are contiguous for the GEMM's TMA loads.
  *   row_weights must be NULL (the FP8 rows take the weight in
  *   moe_quant_fp8_group, before the codes are chosen).
+ * dtype GBMOE_FP8_E4M3_CHANNEL: x (M, K) e4m3 with x_scales (M) fp32 ->
+ *   A (M*topk, K) e4m3 with A_scales (M*topk) fp32, one per row; row_weights
+ *   must be NULL.
  * K % 128 == 0; x and A 16-byte aligned. */
 gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
                                 const float *row_weights,
@@ -220,6 +235,12 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
  *   before it is added.  H is written as e4m3 with group-major H_scales
  *   (N/128, ld) fp32, requantised per 128-group of a row with the
  *   moe_quant_fp8_group rule.
+ * dtype GBMOE_FP8_E4M3_CHANNEL: A e4m3 with A_scales (M*topk) fp32, w1 e4m3
+ *   with w1_scales (E, 2N) fp32; the whole K is accumulated in fp32 and
+ *   scaled once, g[n] = A_scale[i] * w1_scale[e, n] * (codes dot product).
+ *   H (M*topk, N) is written in bf16 (H_scales unused): a per-token scale
+ *   spans the whole row, so the caller quantises H with moe_quant_fp8_group
+ *   (group = N) before moe_grouped_gemm_down.
  * Accumulation is fp32.  N % 128 == 0, K % 128 == 0.  err_word may be NULL. */
 gbmoe_status_t moe_grouped_gemm_gate_up_silu(
     const void *A, const float *A_scales, const int32_t *offsets, int M,
@@ -248,7 +269,10 @@ gbmoe_status_t moe_grouped_gemm_gate_up_gelu(
  * dtype GBMOE_BF16: H (M*topk, N) bf16, w2 (E, K, N) bf16.
  * dtype GBMOE_FP8_E4M3: H e4m3 + group-major H_scales (N/128, ld), ld =
  *   M*topk rounded up to 4 (as written by the gate/up call); w2 e4m3 +
- *   w2_scales (E, K/128, N/128).  Accumulation fp32.  err_word may be NULL. */
+ *   w2_scales (E, K/128, N/128).
+ * dtype GBMOE_FP8_E4M3_CHANNEL: H e4m3 + H_scales (M*topk) fp32, one per
+ *   row; w2 e4m3 + w2_scales (E, K) fp32, one per output channel.
+ * Accumulation fp32.  err_word may be NULL. */
 gbmoe_status_t moe_grouped_gemm_down(
     const void *H, const float *H_scales, const int32_t *sorted_pair_ids,
     const int32_t *offsets, const float *topk_weights, int M, int topk, int E,
@@ -302,6 +326,9 @@ gbmoe_status_t moe_batched_masked_experts(
  * dtype GBMOE_BF16: w1 (E, 2N, K) / w2 (E, K, N) bf16, scales NULL;
  * dtype GBMOE_FP8_E4M3: w1/w2 e4m3 with their block scales; the activations
  *   are quantised per token in groups of 128 and H is requantised.
+ * dtype GBMOE_FP8_E4M3_CHANNEL: w1/w2 e4m3 with their per-channel scales
+ *   (E, 2N) / (E, K); the activations are quantised with one scale per
+ *   token, H is kept in bf16 and quantised per token before the second GEMM.
  * out (M, K) bf16.  topk_ids / topk_weights (M, topk) may be NULL; when given
  * they receive the router's output (global ids).
  * ws: moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype) bytes.

@@ -17,7 +17,7 @@ import torch
 
 from . import build as _build
 
-BF16, FP8_E4M3 = 0, 1
+BF16, FP8_E4M3, FP8_E4M3_CHANNEL = 0, 1, 2  # dtype codes of include/gbmoe.h
 SOFTMAX, SIGMOID = 0, 1
 ACT_SILU, ACT_GELU = 0, 1
 WS_ALIGN, WS_BATCHED, WS_FORWARD, WS_SHARED = 0, 2, 3, 4

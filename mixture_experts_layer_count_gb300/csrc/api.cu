@@ -65,12 +65,16 @@ struct Carver {
   }
 };
 
-size_t elem_bytes(int dtype) { return dtype == GBMOE_FP8_E4M3 ? 1 : 2; }
+bool is_fp8(int dtype) { return dtype == GBMOE_FP8_E4M3 || dtype == GBMOE_FP8_E4M3_CHANNEL; }
+size_t elem_bytes(int dtype) { return is_fp8(dtype) ? 1 : 2; }
+// fp32 scales per row of a (rows, cols) e4m3 operand: one per 128 columns,
+// or one per row (GBMOE_FP8_E4M3_CHANNEL)
+int scales_per_row(int dtype, int cols) { return dtype == GBMOE_FP8_E4M3_CHANNEL ? 1 : cols / 128; }
 
 // leading dimension of the group-major FP8 row scales of M*topk rows
 int64_t scale_ld(size_t P) { return (int64_t)((P + 3) / 4 * 4); }
 
-bool valid_dtype(int dtype) { return dtype == GBMOE_BF16 || dtype == GBMOE_FP8_E4M3; }
+bool valid_dtype(int dtype) { return dtype == GBMOE_BF16 || is_fp8(dtype); }
 
 struct ForwardWs {
   int32_t *ids, *counts, *offsets, *sorted, *inv, *chunk_hist;
@@ -81,6 +85,7 @@ struct ForwardWs {
   float *As;
   void *H;
   float *Hs;
+  uint16_t *Hb;  // GBMOE_FP8_E4M3_CHANNEL: H in bf16 before its per-token quantisation
   uint16_t *y_slot;
 };
 ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dtype) {
@@ -93,13 +98,16 @@ ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dty
   w.sorted = static_cast<int32_t *>(c.take(P * 4));
   w.inv = static_cast<int32_t *>(c.take(P * 4));
   w.chunk_hist = static_cast<int32_t *>(c.take((size_t)align_num_chunks((int)P) * E * 4));
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  const bool fp8 = is_fp8(dtype);
+  const int sk = scales_per_row(dtype, K), sn = scales_per_row(dtype, N);
   w.xq = fp8 ? static_cast<uint8_t *>(c.take((size_t)M * K)) : nullptr;
-  w.xs = fp8 ? static_cast<float *>(c.take((size_t)M * (K / 128) * 4)) : nullptr;
+  w.xs = fp8 ? static_cast<float *>(c.take((size_t)M * sk * 4)) : nullptr;
   w.A = c.take(P * (size_t)K * elem_bytes(dtype));
-  w.As = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * (K / 128) * 4)) : nullptr;
+  w.As = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * sk * 4)) : nullptr;
   w.H = c.take(P * (size_t)N * elem_bytes(dtype));
-  w.Hs = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * (N / 128) * 4)) : nullptr;
+  w.Hs = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * sn * 4)) : nullptr;
+  w.Hb = dtype == GBMOE_FP8_E4M3_CHANNEL ? static_cast<uint16_t *>(c.take(P * (size_t)N * 2))
+                                         : nullptr;
   w.y_slot = static_cast<uint16_t *>(c.take(P * (size_t)K * 2));
   return w;
 }
@@ -134,6 +142,7 @@ gbmoe_status_t gate_up_impl(const void *A, const float *A_scales,
   a.mode = kGateUp;
   a.act = act;
   a.fp8 = dtype == GBMOE_FP8_E4M3;
+  a.fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
   a.offsets = offsets;
   a.E = E;
   a.N = N;
@@ -155,10 +164,11 @@ gbmoe_status_t permute_impl(const void *x, const float *x_scales,
                             const int32_t *offsets, int M, int topk, int E, int K,
                             int dtype, void *A, float *A_scales, int num_sms,
                             cudaStream_t s) {
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  const bool fp8 = is_fp8(dtype);
   return from_cuda(launch_gather_rows(x, fp8 ? x_scales : nullptr,
                                       fp8 ? nullptr : row_weights,
-                                      (int)(K * elem_bytes(dtype)), K / 128, sorted,
+                                      (int)(K * elem_bytes(dtype)), scales_per_row(dtype, K),
+                                      sorted,
                                       offsets + E, M * topk, topk, A,
                                       fp8 ? A_scales : nullptr,
                                       scale_ld((size_t)M * topk), num_sms, s));
@@ -173,6 +183,7 @@ gbmoe_status_t down_impl(const void *H, const float *H_scales,
   GroupedGemmArgs a{};
   a.mode = kDown;
   a.fp8 = dtype == GBMOE_FP8_E4M3;
+  a.fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
   a.offsets = offsets;
   a.E = E;
   a.N = N;
@@ -305,13 +316,16 @@ gbmoe_status_t moe_align_permute(const int32_t *topk_ids, int M, int topk,
 gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, const float *row_weights,
                                    int M, int K, int group, uint8_t *q,
                                    float *scales, gbmoe_stream_t stream) {
-  if (M < 0 || K < 128 || K % 128 != 0 || group != 128) return GBMOE_INVALID_ARG;
+  if (M < 0 || K < 128 || K % 128 != 0 || (group != 128 && group != K))
+    return GBMOE_INVALID_ARG;
   if (M > 0 && (!x || !q || !scales || !aligned16(x) || !aligned16(q)))
     return GBMOE_INVALID_ARG;
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK) return st;
   if (M == 0) return GBMOE_OK;
+  if (group == K && K != 128)  // one group per row
+    return from_cuda(launch_quant_row(x, row_weights, M, K, q, scales, (cudaStream_t)stream));
   return from_cuda(launch_quant_group(x, row_weights, M, K, q, scales, (cudaStream_t)stream));
 }
 
@@ -340,7 +354,7 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
   if (M < 0 || topk < 1 || topk > kMaxTopk || E < 1 || E > kMaxExperts || K < 128 ||
       K % 128 != 0 || (size_t)M * topk > (size_t)INT32_MAX)
     return GBMOE_INVALID_ARG;
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  const bool fp8 = is_fp8(dtype);
   if (M > 0) {
     if (!x || !sorted_pair_ids || !offsets || !A || !aligned16(x) || !aligned16(A))
       return GBMOE_INVALID_ARG;
@@ -363,9 +377,11 @@ static gbmoe_status_t gate_up_entry(
   if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
   if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
   const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  const bool fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
   if (M > 0) {
     if (!A || !offsets || !w1 || !H) return GBMOE_INVALID_ARG;
     if (fp8 && (!A_scales || !w1_scales || !H_scales)) return GBMOE_INVALID_ARG;
+    if (fp8ch && (!A_scales || !w1_scales || !aligned16(w1_scales))) return GBMOE_INVALID_ARG;
     if (!aligned16(A) || !aligned16(w1) || !aligned16(H)) return GBMOE_INVALID_ARG;
   }
   int sms;
@@ -404,9 +420,10 @@ gbmoe_status_t moe_grouped_gemm_down(
     int sms;
     return device_info(&sms);
   }
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  const bool fp8 = is_fp8(dtype);
   if (!H || !sorted_pair_ids || !offsets || !w2 || !y_slot) return GBMOE_INVALID_ARG;
   if (fp8 && (!H_scales || !w2_scales)) return GBMOE_INVALID_ARG;
+  if (dtype == GBMOE_FP8_E4M3_CHANNEL && !aligned16(w2_scales)) return GBMOE_INVALID_ARG;
   if (!aligned16(H) || !aligned16(w2) || !aligned16(y_slot)) return GBMOE_INVALID_ARG;
   int sms;
   gbmoe_status_t st = device_info(&sms);
@@ -496,10 +513,12 @@ static gbmoe_status_t forward_validate(const uint16_t *x, const float *logits,
     return GBMOE_INVALID_ARG;
   if (apply_router_weight_on_input && topk != 1) return GBMOE_INVALID_ARG;
   if (activation != GBMOE_ACT_SILU && activation != GBMOE_ACT_GELU) return GBMOE_INVALID_ARG;
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  const bool fp8 = is_fp8(dtype);
   if (M > 0) {
     if (!x || !logits || !w1 || !w2 || !out || !ws) return GBMOE_INVALID_ARG;
     if (fp8 && (!w1_scales || !w2_scales)) return GBMOE_INVALID_ARG;
+    if (dtype == GBMOE_FP8_E4M3_CHANNEL && (!aligned16(w1_scales) || !aligned16(w2_scales)))
+      return GBMOE_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(ws))
       return GBMOE_INVALID_ARG;
     if (ws_bytes < moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype))
@@ -524,7 +543,8 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                                         apply_router_weight_on_input, activation, dtype, w1,
                                         w1_scales, w2, w2_scales, out, ws, ws_bytes);
   if (vst != GBMOE_OK) return vst;
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  const bool fp8 = is_fp8(dtype);
+  const bool fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK) return st;
@@ -548,7 +568,8 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   const void *a_src = x;
   const float *a_src_s = nullptr;
   if (fp8) {
-    ce = launch_quant_group(x, in_w, M, K, w.xq, w.xs, s);
+    ce = fp8ch ? launch_quant_row(x, in_w, M, K, w.xq, w.xs, s)
+               : launch_quant_group(x, in_w, M, K, w.xq, w.xs, s);
     if (ce != cudaSuccess) return from_cuda(ce);
     a_src = w.xq;
     a_src_s = w.xs;
@@ -556,9 +577,15 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   st = permute_impl(a_src, a_src_s, fp8 ? nullptr : in_w, w.sorted, w.offsets, M, topk, E, K,
                     dtype, w.A, w.As, sms, s);
   if (st != GBMOE_OK) return st;
+  // per-token scales span a whole row of H: it is written in bf16 and
+  // quantised per row before the second GEMM
   st = gate_up_impl(w.A, w.As, w.offsets, M, topk, E, N, K, w1, w1_scales, dtype, activation,
-                    w.H, w.Hs, err_word, sms, s);
+                    fp8ch ? static_cast<void *>(w.Hb) : w.H, w.Hs, err_word, sms, s);
   if (st != GBMOE_OK) return st;
+  if (fp8ch) {
+    ce = launch_quant_row(w.Hb, nullptr, P, N, static_cast<uint8_t *>(w.H), w.Hs, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+  }
   st = down_impl(w.H, w.Hs, w.sorted, w.offsets, in_w ? nullptr : wts, M, topk, E, N, K, w2,
                  w2_scales, dtype, w.y_slot, err_word, sms, s);
   if (st != GBMOE_OK) return st;

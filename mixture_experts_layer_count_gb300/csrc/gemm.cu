@@ -1,7 +1,11 @@
-// gemm.cu -- the two expert GEMMs of [Permute-Experts-Unpermute] in bf16 as
-// grouped GEMMs on the sm_103a tensor cores (tcgen05.mma, fp32 accumulators
-// in TMEM), operands staged in shared memory by TMA; plus the tensor-map
-// encoder and the dispatch between the bf16 and FP8 kernels.
+// gemm.cu -- the two expert GEMMs of [Permute-Experts-Unpermute] in bf16, or
+// in e4m3 with one scale per row of each operand (per-token activations,
+// per-channel weights), as grouped GEMMs on the sm_103a tensor cores
+// (tcgen05.mma, fp32 accumulators in TMEM), operands staged in shared memory
+// by TMA; plus the tensor-map encoder and the dispatch between the kernels.
+// With per-row scales the whole K accumulates in TMEM and the epilogue
+// applies s_a[row] * s_w[column] once (the 1 x 128 / 128 x 128 block-scaled
+// e4m3 GEMMs are in gemm_fp8.cu).
 //
 // FusedMoEPermuteExpertsUnpermute.apply in
 // "vllm/model_executor/layers/fused_moe/modular_kernel.py" is "matmul +
@@ -41,9 +45,13 @@ using namespace gemm;
 
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kBK = kBKB / 2;               // bf16 elements per stage row
-constexpr int kMmaPerStage = kBK / 16;      // tcgen05.mma kind::f16 has K = 16
-constexpr uint32_t kIdesc = umma_idesc(kBM, kBN, kFmtBF16);
+// a stage row is kBKB = 128 bytes of K: 64 bf16 or 128 e4m3 elements, four
+// MMAs either way (kind::f16 has K = 16, kind::f8f6f4 K = 32)
+template <bool F8>
+__host__ __device__ constexpr int stage_k() { return F8 ? kBKB : kBKB / 2; }
+constexpr int kMmaPerStage = 4;
+template <bool F8>
+__host__ __device__ constexpr uint32_t idesc_of() { return umma_idesc(kBM, kBN, F8 ? kFmtE4M3 : kFmtBF16); }
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
 constexpr int kOffA = 0;
@@ -67,10 +75,26 @@ struct KParams {
   void *out;
   const int32_t *sorted;    // down, Standard
   const float *topk_w;      // down, Standard
+  const float *a_scales;    // e4m3: one per row of A
+  const float *b_scales;    // e4m3: one per row of B (E * b_rows)
   int32_t *err;
 };
 
-template <int MODE, int ACT>
+// the 32 per-row weight scales of output columns [col, col + 32) of expert e
+// (every lane reads the same addresses: broadcast loads)
+__device__ __forceinline__ void load_scales32(const float *b_scales, size_t first, float (&w)[32]) {
+  const float4 *p4 = reinterpret_cast<const float4 *>(b_scales + first);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = __ldg(p4 + i);
+    w[4 * i] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
+  }
+}
+
+template <int MODE, int ACT, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -149,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(s), kAStage + kBStage);
-          const int x = kb * kBK;
+          const int x = kb * stage_k<F8>();
           tma_load_2d(sA + s * kAStage, &tmA, full_bar(s), x, a_row);
           tma_load_2d(sB + s * kBStage, &tmB, full_bar(s), x, b_row0);
           tma_load_2d(sB + s * kBStage + kBStage / 2, &tmB, full_bar(s), x, b_row1);
@@ -185,8 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t da = umma_desc_sw128(sA + s * kAStage);
           const uint64_t db = umma_desc_sw128(sB + s * kBStage);
 #pragma unroll
-          for (int k = 0; k < kMmaPerStage; ++k)
-            umma_f16(d, da + 2 * k, db + 2 * k, kIdesc, (kb | k) != 0);
+          for (int k = 0; k < kMmaPerStage; ++k) {
+            if (F8)
+              umma_f8(d, da + 2 * k, db + 2 * k, idesc_of<F8>(), (kb | k) != 0);
+            else
+              umma_f16(d, da + 2 * k, db + 2 * k, idesc_of<F8>(), (kb | k) != 0);
+          }
           umma_commit(empty_bar(s));
         }
         if (!ok) break;
@@ -216,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + t_lane + buf * kBN;
+      const float sa = F8 && valid ? p.a_scales[arow] : 1.0f;
       if (MODE == kGateUpMode) {
         uint16_t *hrow = static_cast<uint16_t *>(p.out) + (size_t)arow * p.N + nt * 128;
 #pragma unroll 1
@@ -224,6 +253,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tb + c * 32, g);
           tmem_ld32(tb + 128 + c * 32, u);
           tmem_ld_wait();
+          if (F8) {  // g, u *= s_a[row] * s_w[column]
+            float sw[32];
+            const size_t col = (size_t)e * p.b_rows + nt * 128 + c * 32;
+            load_scales32(p.b_scales, col, sw);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = __float_as_uint(__uint_as_float(g[i]) * (sa * sw[i]));
+            load_scales32(p.b_scales, col + p.N, sw);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * (sa * sw[i]));
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -257,6 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld32(tb + c * 32, v);
           tmem_ld_wait();
+          if (F8) {  // y *= s_a[row] * s_w[column]
+            float sw[32];
+            load_scales32(p.b_scales, (size_t)e * p.b_rows + nt * kBN + c * 32, sw);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * (sa * sw[i]));
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -304,11 +349,11 @@ bool resolve_encode() {
   return g_encode != nullptr;
 }
 
-template <int MODE, int ACT>
+template <int MODE, int ACT, bool F8>
 cudaError_t launch_bf16(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, ACT>,
+    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, ACT, F8>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           kSmemBytes);
     if (st != cudaSuccess) return st;
@@ -317,11 +362,13 @@ cudaError_t launch_bf16(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   const bool gate_up = MODE == kGateUpMode;
   const int Kd = gate_up ? a.K : a.N;          // contraction length
   const int b_rows = gate_up ? 2 * a.N : a.K;  // rows of B per expert
+  const int esz = F8 ? 1 : 2;                  // bytes per element
+  const int kind = F8 ? kTmapU8 : kTmapBF16;
   CUtensorMap tmA, tmB;
-  if (!encode_tmap_2d(&tmA, a.A, kTmapBF16, (uint64_t)Kd, (uint64_t)a.a_rows,
-                      (uint64_t)Kd * 2, kBK, kBM, true) ||
-      !encode_tmap_2d(&tmB, a.B, kTmapBF16, (uint64_t)Kd, (uint64_t)a.E * b_rows,
-                      (uint64_t)Kd * 2, kBK, 128, true))
+  if (!encode_tmap_2d(&tmA, a.A, kind, (uint64_t)Kd, (uint64_t)a.a_rows,
+                      (uint64_t)Kd * esz, stage_k<F8>(), kBM, true) ||
+      !encode_tmap_2d(&tmB, a.B, kind, (uint64_t)Kd, (uint64_t)a.E * b_rows,
+                      (uint64_t)Kd * esz, stage_k<F8>(), 128, true))
     return cudaErrorInvalidValue;
   KParams p;
   p.offsets = a.offsets;
@@ -331,11 +378,13 @@ cudaError_t launch_bf16(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   p.N = a.N;
   p.K = a.K;
   p.n_tiles = gate_up ? a.N / 128 : (a.K + kBN - 1) / kBN;
-  p.num_kb = Kd / kBK;
+  p.num_kb = Kd / stage_k<F8>();
   p.b_rows = b_rows;
   p.out = a.out;
   p.sorted = a.sorted_pair_ids;
   p.topk_w = a.topk_weights;
+  p.a_scales = a.A_scales;
+  p.b_scales = a.B_scales;
   p.err = a.err;
   // upper bound on the tiles: every expert may end with a partial m-tile
   long long mtiles = a.offsets ? (a.a_rows + kBM - 1) / kBM + a.E
@@ -343,7 +392,7 @@ cudaError_t launch_bf16(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   long long tiles = mtiles * p.n_tiles;
   int grid = (int)(tiles < num_sms ? tiles : num_sms);
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<MODE, ACT><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
+  grouped_gemm_kernel<MODE, ACT, F8><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
   return cudaGetLastError();
 }
 
@@ -374,18 +423,27 @@ bool bf16_uses_cta_pairs(const GroupedGemmArgs &a) {
   // average 128 rows or more; below that a pair tile is mostly padding, and
   // the 1-SM kernel keeps more weight bytes in flight per SM (4 stages x
   // 32 KB of B against 6 x 16 KB), which is what a weight-streaming launch
-  // (decode) needs.
+  // (decode) needs.  e4m3 operands stay on one SM: a 128-byte K block is
+  // twice the MMA work of a bf16 one, so the 1-SM stage traffic (48 KB per
+  // 512 MMA cycles) is already below what shared memory delivers, and the
+  // weight tiles mostly stream from HBM.
+  if (a.fp8ch) return false;
   const long long rows = a.offsets ? (long long)a.a_rows : (long long)a.T * a.E;
   return rows >= 128LL * a.E;
+}
+
+template <bool F8>
+cudaError_t launch_one_sm(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
+  if (a.mode == kDown) return launch_bf16<kDownMode, kActSilu, F8>(a, num_sms, s);
+  return a.act == GBMOE_ACT_GELU ? launch_bf16<kGateUpMode, kActGelu, F8>(a, num_sms, s)
+                                 : launch_bf16<kGateUpMode, kActSilu, F8>(a, num_sms, s);
 }
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,
                                 cudaStream_t s) {
   if (a.fp8) return launch_grouped_gemm_fp8(a, num_sms, s);
   if (bf16_uses_cta_pairs(a)) return launch_grouped_gemm_pair(a, num_sms, s);
-  if (a.mode == kDown) return launch_bf16<kDownMode, kActSilu>(a, num_sms, s);
-  return a.act == GBMOE_ACT_GELU ? launch_bf16<kGateUpMode, kActGelu>(a, num_sms, s)
-                                 : launch_bf16<kGateUpMode, kActSilu>(a, num_sms, s);
+  return a.fp8ch ? launch_one_sm<true>(a, num_sms, s) : launch_one_sm<false>(a, num_sms, s);
 }
 
 }  // namespace gbmoe

@@ -42,6 +42,8 @@ cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
 // row_w (M) or NULL: rows multiplied by their weight (fp32) before quantising
 cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int K,
                                uint8_t *q, float *scales, cudaStream_t s);
+cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K,
+                             uint8_t *q, float *scales, cudaStream_t s);
 cudaError_t launch_quant_block(const uint16_t *w, int64_t R, int C, uint8_t *q,
                                float *scales, cudaStream_t s);
 
@@ -51,6 +53,8 @@ enum GemmMode { kGateUp = 0, kDown = 1 };
 struct GroupedGemmArgs {
   int mode;                  // kGateUp or kDown
   int fp8;                   // 0: bf16 operands, 1: e4m3 with fp32 block scales
+  int fp8ch;                 // 1: e4m3 with one fp32 scale per row of A and per row of B
+                             //    (A_scales (a_rows), B_scales (E * rows of B per expert))
   int act;                   // gate/up: GBMOE_ACT_SILU or GBMOE_ACT_GELU
   // row groups: Standard (offsets != nullptr): expert e owns rows
   // [offsets[e], offsets[e+1]) of A.  Batched: rows [e*T, e*T + min(counts[e], T)).

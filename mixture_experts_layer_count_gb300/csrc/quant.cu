@@ -8,7 +8,11 @@
 //     s = max(amax, 1e-12) / 448       (fp32, IEEE division)
 //     q = e4m3(x / s)                  (IEEE division, round to nearest even,
 //                                       saturating at +-448)
-// HBM-bound: each kernel reads its input once and writes q and s once.
+// The group is 128 values, or a whole row (one scale per token of the
+// activations, per_act_token_quant; per output channel of a weight matrix,
+// per_out_ch_quant).
+// HBM-bound: each kernel reads its input once (the row kernel a second time
+// from L1/L2) and writes q and s once.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -61,6 +65,56 @@ __global__ void __launch_bounds__(256)
                       (e4m3_of(__fdiv_rn(f[3], s)) << 24);
     q[base / 4] = packed;
     if (lane == 0) scales[t * G + g] = s;
+  }
+}
+
+// one warp per row, the group being the whole row: the row maximum, then
+// the codes (the row is read again, from L1/L2); 8 values per 16-byte load
+__global__ void __launch_bounds__(256)
+    quant_row_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w, int M,
+                     int K, uint2 *__restrict__ q, float *__restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int vecs = K / 8;
+  for (size_t t = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; t < (size_t)M;
+       t += ((size_t)gridDim.x * blockDim.x) >> 5) {
+    const float w = row_w ? row_w[t] : 1.0f;
+    const uint4 *xr = x + t * vecs;
+    float amax = 0.0f;
+    for (int v = lane; v < vecs; v += 32) {
+      const uint4 raw = xr[v];
+      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a = bf16_bits_to_float(u[i] & 0xffffu), b = bf16_bits_to_float(u[i] >> 16);
+        if (row_w) {
+          a = __fmul_rn(a, w);
+          b = __fmul_rn(b, w);
+        }
+        amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = group_scale(amax);
+    for (int v = lane; v < vecs; v += 32) {
+      const uint4 raw = xr[v];
+      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t c[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a = bf16_bits_to_float(u[i] & 0xffffu), b = bf16_bits_to_float(u[i] >> 16);
+        if (row_w) {
+          a = __fmul_rn(a, w);
+          b = __fmul_rn(b, w);
+        }
+        c[2 * i] = e4m3_of(__fdiv_rn(a, s));
+        c[2 * i + 1] = e4m3_of(__fdiv_rn(b, s));
+      }
+      q[t * vecs + v] = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                                   c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+    }
+    if (lane == 0) scales[t] = s;
   }
 }
 
@@ -121,6 +175,16 @@ cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int
   if (blocks > 65535u * 16u) blocks = 65535u * 16u;
   quant_group_kernel<<<(unsigned)blocks, 256, 0, s>>>(
       reinterpret_cast<const uint2 *>(x), row_w, M, K, reinterpret_cast<uint32_t *>(q),
+      scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K,
+                             uint8_t *q, float *scales, cudaStream_t s) {
+  size_t blocks = ((size_t)M + 7) / 8;
+  if (blocks > 65535u * 16u) blocks = 65535u * 16u;
+  quant_row_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), row_w, M, K, reinterpret_cast<uint2 *>(q),
       scales);
   return cudaGetLastError();
 }

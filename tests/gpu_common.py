@@ -8,7 +8,7 @@ import torch
 import oracle as orc
 import workloads as WL
 
-TOL = {WL.BF16: 2e-2, WL.FP8: 5e-2}  # max|d| <= tol * max|ref|
+TOL = {WL.BF16: 2e-2, WL.FP8: 5e-2, WL.FP8_CHANNEL: 5e-2}  # max|d| <= tol * max|ref|
 
 
 def gbmoe():
@@ -30,13 +30,24 @@ def assert_close_rel(got, ref, tol, what=""):
 
 class GpuWeights:
     """The expert weights as the CUDA path takes them: bf16 tensors, or e4m3
-    codes + 128 x 128 block scales made by the library's own quantiser."""
+    codes + 128 x 128 block scales (FP8) or one scale per row (FP8_CHANNEL)
+    made by the library's own quantiser."""
 
     def __init__(self, cfg, w1, w2):
         g = gbmoe()
         self.dtype = cfg.dtype
         if cfg.dtype == WL.BF16:
             self.w1, self.w2, self.w1s, self.w2s = w1, w2, None, None
+        elif cfg.dtype == WL.FP8_CHANNEL:
+            E, N, K = cfg.E, cfg.N, cfg.K
+            self.w1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=w1.device)
+            self.w2 = torch.empty((E, K, N), dtype=torch.uint8, device=w1.device)
+            self.w1s = torch.empty((E, 2 * N), dtype=torch.float32, device=w1.device)
+            self.w2s = torch.empty((E, K), dtype=torch.float32, device=w1.device)
+            g.moe_quant_fp8_group(w1.view(E * 2 * N, K), self.w1.view(E * 2 * N, K),
+                                  self.w1s.view(E * 2 * N, 1), group=K)
+            g.moe_quant_fp8_group(w2.view(E * K, N), self.w2.view(E * K, N),
+                                  self.w2s.view(E * K, 1), group=N)
         else:
             E, N, K = cfg.E, cfg.N, cfg.K
             self.w1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=w1.device)
@@ -57,6 +68,10 @@ def oracle_weights(cfg, w1, w2, experts=None):
         b2 = WL.bf16_bits(w2[e])
         if cfg.dtype == WL.BF16:
             blocks[e] = (b1, b2)
+        elif cfg.dtype == WL.FP8_CHANNEL:  # one scale per row: a group as wide as the row
+            q1, s1 = orc.quant_fp8_group(b1, group=cfg.K)
+            q2, s2 = orc.quant_fp8_group(b2, group=cfg.N)
+            blocks[e] = (q1, q2, s1[:, 0], s2[:, 0])
         else:
             q1, s1 = orc.quant_fp8_block(b1)
             q2, s2 = orc.quant_fp8_block(b2)

@@ -22,7 +22,7 @@ def _lib():
 
 
 @pytest.mark.parametrize("cfg", [WL.SMALL_BF16, WL.SMALL_FP8, WL.SMALL_PAIR_TOP2,
-                                 WL.SMALL_FP8_K640],
+                                 WL.SMALL_FP8_K640, WL.SMALL_FP8CH_PAIR],
                          ids=lambda c: c.name)
 def test_forward_gelu(cfg):
     g = gbmoe()

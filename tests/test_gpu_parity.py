@@ -130,6 +130,27 @@ def test_quant_fp8_group_bit_exact():
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
+@pytest.mark.parametrize("K,weighted", [(1024, False), (7168, True), (640, False)])
+def test_quant_fp8_rowwise_bit_exact(K, weighted):
+    """One scale per row (per-token activations, per-channel weights): codes
+    and scales bit-exact against the oracle, with and without row weights."""
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(43 + K)
+    M = 301
+    x = (torch.randn((M, K), generator=gen, device=DEV) *
+         torch.logspace(-3, 2, K, device=DEV)).to(torch.bfloat16)
+    x[5] = 0
+    x[7] = x[7].abs() * -1
+    rw = (torch.rand(M, generator=gen, device=DEV) + 0.05) if weighted else None
+    q = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    s = torch.empty((M, 1), dtype=torch.float32, device=DEV)
+    g.moe_quant_fp8_group(x, q, s, group=K, row_weights=rw)
+    rq, rs = orc.quant_fp8_group(WL.bf16_bits(x), group=K,
+                                 row_weights=None if rw is None else rw.cpu().numpy())
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
 def test_quant_fp8_block_bit_exact():
     g = gbmoe()
     gen = torch.Generator(device=DEV).manual_seed(42)
@@ -166,7 +187,7 @@ def _stage_inputs(cfg):
 
 
 SMALL_STANDARD = [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.SMALL_FP8, WL.SMALL_PAIR,
-                  WL.SMALL_PAIR_TOP2, WL.SMALL_FP8_K640]
+                  WL.SMALL_PAIR_TOP2, WL.SMALL_FP8_K640, WL.SMALL_FP8CH, WL.SMALL_FP8CH_PAIR]
 
 
 @pytest.mark.parametrize("cfg", SMALL_STANDARD, ids=lambda c: c.name)
@@ -178,8 +199,16 @@ def test_gate_up_then_down_stages(cfg):
     W = oracle_weights(cfg, d["w1"], d["w2"])
     M, E, N, K, k, P = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk, cfg.P
     fp8 = cfg.dtype == WL.FP8
+    ch = cfg.dtype == WL.FP8_CHANNEL
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    if fp8:
+    if ch:  # one scale per token; H in bf16, then one scale per row of H
+        xq = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+        xs = torch.empty((M, 1), dtype=torch.float32, device=DEV)
+        g.moe_quant_fp8_group(d["x"], xq, xs, group=K)
+        xin, xin_s = xq, xs
+        H = torch.empty((P, N), dtype=torch.bfloat16, device=DEV)
+        Hs = None
+    elif fp8:
         xq = torch.empty((M, K), dtype=torch.uint8, device=DEV)
         xs = torch.empty((M, K // 128), dtype=torch.float32, device=DEV)
         g.moe_quant_fp8_group(d["x"], xq, xs)
@@ -192,18 +221,27 @@ def test_gate_up_then_down_stages(cfg):
         H = torch.empty((P, N), dtype=torch.bfloat16, device=DEV)
         Hs = None
     A = torch.empty((P, K), dtype=xin.dtype, device=DEV)
-    As = torch.empty((K // 128, (P + 3) // 4 * 4), dtype=torch.float32, device=DEV) if fp8 else None
+    ld = (P + 3) // 4 * 4
+    As = (torch.empty((K // 128, ld), dtype=torch.float32, device=DEV) if fp8 else
+          torch.empty((1, ld), dtype=torch.float32, device=DEV) if ch else None)
     g.moe_permute_rows(xin, xin_s, srt, offsets, k, E, cfg.dtype, A, As)
     g.moe_grouped_gemm_gate_up_silu(A, As, offsets, M, k, E, N, K, gw.w1, gw.w1s,
                                     cfg.dtype, H, Hs, err)
     y = torch.empty((M, k, K), dtype=torch.bfloat16, device=DEV)
-    g.moe_grouped_gemm_down(H, Hs, srt, offsets, wts, M, k, E, N, K, gw.w2, gw.w2s,
+    Hd, Hds = H, Hs
+    if ch:
+        Hd = torch.empty((P, N), dtype=torch.uint8, device=DEV)
+        Hds = torch.empty((P, 1), dtype=torch.float32, device=DEV)
+        g.moe_quant_fp8_group(H, Hd, Hds, group=N)
+    g.moe_grouped_gemm_down(Hd, Hds, srt, offsets, wts, M, k, E, N, K, gw.w2, gw.w2s,
                             cfg.dtype, y, err)
     torch.cuda.synchronize()
     assert err.item() == 0
     if fp8:
         Hf = (H.view(torch.float8_e4m3fn).float().view(P, N // 128, 128) *
               Hs[:, :P].t().reshape(P, N // 128, 1)).view(P, N).cpu().numpy()
+    elif ch:  # the codes the down GEMM read, dequantised
+        Hf = (Hd.view(torch.float8_e4m3fn).float() * Hds).cpu().numpy()
     else:
         Hf = H.float().cpu().numpy()
     yf = y.float().cpu().numpy()
@@ -294,7 +332,7 @@ def test_one_expert_takes_every_token_matches_torch_matmul(M):
 
 # ------------------------------------------------- full-size, sampled ------
 
-FULL_CFGS = [WL.MIXTRAL_PREFILL, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8]
+FULL_CFGS = [WL.MIXTRAL_PREFILL, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8, WL.DSV3_PREFILL_FP8CH]
 
 
 @pytest.mark.parametrize("cfg", FULL_CFGS, ids=lambda c: c.name)

@@ -28,7 +28,7 @@ from typing import Optional
 import torch
 
 SOFTMAX, SIGMOID = 0, 1
-BF16, FP8 = 0, 1
+BF16, FP8, FP8_CHANNEL = 0, 1, 2
 
 
 @dataclasses.dataclass(frozen=True)
@@ -39,7 +39,8 @@ class MoEConfig:
     N: int                 # intermediate size (w1 has 2N rows per expert)
     E: int                 # experts
     topk: int
-    dtype: int = BF16      # BF16 or FP8 (e4m3, 1x128 activation / 128x128 weight scales)
+    dtype: int = BF16      # BF16, FP8 (e4m3, 1x128 activation / 128x128 weight scales) or
+                           # FP8_CHANNEL (e4m3, one scale per token / per weight row)
     score_fn: int = SOFTMAX
     n_groups: int = 1
     topk_groups: int = 1
@@ -54,7 +55,7 @@ class MoEConfig:
 
     @property
     def requant_h(self) -> bool:
-        return self.dtype == FP8
+        return self.dtype != BF16
 
 
 # The workloads the layer is specified on.
@@ -101,6 +102,19 @@ SMALL_FP8_K640 = MoEConfig("small_fp8_M300_K640_N256_E4_top2", M=300, K=640, N=2
 SMALL_BATCHED_SHORT = MoEConfig("small_batched_bf16_E5_T100_K384_N256", M=100, K=384,
                                 N=256, E=5, topk=1, batched=True, seed=17)
 
+# e4m3 with per-token / per-channel scales: a small sigmoid-routed case with
+# 64 rows per expert, one with 150 rows per expert and K = 640, and the
+# DeepSeek-V3-shaped prefill in this format.
+SMALL_FP8CH = MoEConfig("small_fp8ch_M256_K512_N256_E16_top4", M=256, K=512, N=256,
+                        E=16, topk=4, dtype=FP8_CHANNEL, score_fn=SIGMOID, n_groups=4,
+                        topk_groups=2, zipf_bias=True, seed=19)
+SMALL_FP8CH_PAIR = MoEConfig("small_fp8ch_M300_K640_N384_E4_top2", M=300, K=640, N=384,
+                             E=4, topk=2, dtype=FP8_CHANNEL, seed=20)
+DSV3_PREFILL_FP8CH = MoEConfig("dsv3_prefill_fp8ch_M8192_K7168_N2048_E256_top8",
+                               M=8192, K=7168, N=2048, E=256, topk=8, dtype=FP8_CHANNEL,
+                               score_fn=SIGMOID, n_groups=8, topk_groups=4, zipf_bias=True,
+                               seed=3)
+
 ALL = [TINY, MIXTRAL_PREFILL, DSV3_PREFILL_FP8, DSV3_DECODE, BATCHED_MASKED]
 
 # Small cases of the same kernels for profiler captures: operands larger than
@@ -110,12 +124,17 @@ PROFILE_BF16 = MoEConfig("profile_bf16_M2048_K4096_N14336_E2_top1", M=2048, K=40
 PROFILE_FP8 = MoEConfig("profile_fp8_M2048_K7168_N2048_E16_top2", M=2048, K=7168,
                         N=2048, E=16, topk=2, dtype=FP8, score_fn=SIGMOID,
                         n_groups=4, topk_groups=2, seed=22)
+PROFILE_FP8CH = MoEConfig("profile_fp8ch_M2048_K7168_N2048_E16_top2", M=2048, K=7168,
+                          N=2048, E=16, topk=2, dtype=FP8_CHANNEL, score_fn=SIGMOID,
+                          n_groups=4, topk_groups=2, seed=22)
 PROFILE_DECODE = MoEConfig("profile_decode_bf16_M16_K7168_N2048_E32_top4", M=16,
                            K=7168, N=2048, E=32, topk=4, score_fn=SIGMOID,
                            n_groups=4, topk_groups=2, seed=23)
 
 BY_NAME = {c.name: c for c in ALL + [SMALL_BF16, SMALL_SIGMOID, SMALL_FP8,
                                      SMALL_BATCHED, SMALL_PAIR, SMALL_PAIR_TOP2, SMALL_FP8_K640,
+                                     SMALL_FP8CH, SMALL_FP8CH_PAIR, DSV3_PREFILL_FP8CH,
+                                     PROFILE_FP8CH,
                                      SMALL_BATCHED_SHORT, PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE]}
 
 
