@@ -27,7 +27,9 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-BF16, FP8, FP8_CHANNEL = 0, 1, 2  # FP8: 1x128 / 128x128 scales; FP8_CHANNEL: per token / per row
+# FP8: 1x128 / 128x128 scales; FP8_CHANNEL: per token / per weight row;
+# FP8_TENSOR: one scale per activation tensor / per weight row
+BF16, FP8, FP8_CHANNEL, FP8_TENSOR = 0, 1, 2, 3
 SOFTMAX, SIGMOID = 0, 1
 SILU, GELU = 0, 1
 
@@ -82,6 +84,8 @@ def _load():
             lib.orc_quant_fp8_group.argtypes = [P, I, I, I, P, P]
             lib.orc_quant_fp8_block.restype = None
             lib.orc_quant_fp8_block.argtypes = [P, I, I, I, P, P]
+            lib.orc_quant_fp8_tensor.restype = None
+            lib.orc_quant_fp8_tensor.argtypes = [P, P, I, I, P, P]
             lib.orc_expert_row.restype = None
             lib.orc_expert_row.argtypes = [I, P, I, I, I, I, I, P, P, P, P, I,
                                            P, P, I]
@@ -210,6 +214,19 @@ def quant_fp8_group(x_bf16_bits, group=128, row_weights=None):
     return q, s
 
 
+def quant_fp8_tensor(x_bf16_bits, row_weights=None):
+    """x (M, K) bf16 bits -> q (M, K) codes and the one scale of the tensor
+    (rows multiplied by row_weights in fp32 first when given)."""
+    lib = _load()
+    x = _c(x_bf16_bits, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((1,), np.float32)
+    rw = _c(row_weights, np.float32)
+    lib.orc_quant_fp8_tensor(_p(x), _p(rw), M, K, _p(q), _p(s))
+    return q, s[0]
+
+
 def quant_fp8_block(w_bf16_bits, block=128):
     """w (R, C) bf16 bits -> q (R, C) codes, scales (R/block, C/block)."""
     lib = _load()
@@ -224,11 +241,12 @@ def quant_fp8_block(w_bf16_bits, block=128):
 class Weights:
     """Expert weights as the oracle reads them: bf16 bits (dtype BF16), or
     e4m3 codes plus 128 x 128 block scales (dtype FP8), or e4m3 codes plus
-    one scale per row (dtype FP8_CHANNEL), one block per expert.
+    one scale per row (dtypes FP8_CHANNEL and FP8_TENSOR), one block per
+    expert.
 
     Either pass full arrays w1 (E, 2N, K), w2 (E, K, N) [+ w1s (E, 2N/128,
     K/128), w2s (E, K/128, N/128) for FP8; w1s (E, 2N), w2s (E, K) for
-    FP8_CHANNEL], or ``experts={e: (w1e, w2e[, w1se, w2se])}`` with
+    FP8_CHANNEL and FP8_TENSOR], or ``experts={e: (w1e, w2e[, w1se, w2se])}`` with
     ``E, N, K`` for a subset of the experts (the rest are absent; routing a
     computed token to one of them is a caller error)."""
 

@@ -68,6 +68,11 @@
  *      bf16 between the GEMMs (the activations' dtype) and quantised per
  *      token over its N values before the second GEMM, as prepare
  *      quantises the input of the experts.
+ *   Q7 per-tensor activation scales (per_act_token_quant off, no block
+ *      shape): the Q1 rule with one group holding the whole tensor -- one
+ *      scale for the layer's input x (all M tokens) and one for H (every
+ *      routed pair's hidden row, kept in bf16 as in Q6); weights as in Q6
+ *      (per-tensor weight scales are equal per-row scales).
  */
 #include <math.h>
 #include <stdint.h>
@@ -79,8 +84,9 @@
 #endif
 
 /* ORC_FP8: 1 x 128 activation groups, 128 x 128 weight blocks (Q1, Q2);
- * ORC_FP8_CHANNEL: one scale per token and one per weight row (Q6) */
-enum { ORC_BF16 = 0, ORC_FP8 = 1, ORC_FP8_CHANNEL = 2 };
+ * ORC_FP8_CHANNEL: one scale per token and one per weight row (Q6);
+ * ORC_FP8_TENSOR: one scale per activation tensor, one per weight row (Q7) */
+enum { ORC_BF16 = 0, ORC_FP8 = 1, ORC_FP8_CHANNEL = 2, ORC_FP8_TENSOR = 3 };
 enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
 /* FusedMoEPermuteExpertsUnpermute.activation: "silu" -> silu_and_mul,
  * "gelu" -> gelu_and_mul */
@@ -492,6 +498,31 @@ void orc_quant_fp8_group(const uint16_t *x, int M, int K, int group,
     orc_quant_fp8_group_w(x, NULL, M, K, group, q, scales);
 }
 
+/* Q7: one group holding all M rows of x (times row_w[t] in fp32 when given):
+ * *scale = max(amax, 1e-12) / 448, q = e4m3(v / scale). */
+void orc_quant_fp8_tensor(const uint16_t *x, const float *row_w, int M, int K,
+                          uint8_t *q, float *scale)
+{
+    int t, k;
+    float amax = 0.0f, s;
+    for (t = 0; t < M; ++t) {
+        const float rw = row_w ? row_w[t] : 1.0f;
+        for (k = 0; k < K; ++k) {
+            float v = (float)fabs((float)bf16_value(x[(size_t)t * K + k]) * rw);
+            if (v > amax)
+                amax = v;
+        }
+    }
+    s = group_scale(amax);
+    *scale = s;
+    for (t = 0; t < M; ++t) {
+        const float rw = row_w ? row_w[t] : 1.0f;
+        for (k = 0; k < K; ++k)
+            q[(size_t)t * K + k] =
+                orc_e4m3_encode(((float)bf16_value(x[(size_t)t * K + k]) * rw) / s);
+    }
+}
+
 /* w (R, C) bf16 -> q (R, C) e4m3, scales (R / block, C / block) fp32; one
  * scale per block x block tile from the tile's largest magnitude. */
 void orc_quant_fp8_block(const uint16_t *w, int R, int C, int block,
@@ -551,7 +582,7 @@ static double weight_at(const orc_weights *W, int which, int e, int row,
     } else {
         const uint8_t *q = (const uint8_t *)(which == 1 ? W->w1[e] : W->w2[e]);
         const float *sc = which == 1 ? W->w1s[e] : W->w2s[e];
-        size_t sidx = W->dtype == ORC_FP8_CHANNEL
+        size_t sidx = W->dtype == ORC_FP8_CHANNEL || W->dtype == ORC_FP8_TENSOR
                           ? (size_t)row
                           : (size_t)(row / 128) * (C / 128) + col / 128;
         return e4m3_table[q[idx]] * (double)sc[sidx];
@@ -573,8 +604,8 @@ static double bf16_round(double v)
  * (Q5: 128-wide groups of the fp32 h; Q6 for ORC_FP8_CHANNEL: h rounded to
  * bf16, then one group of N); y (K) = h W2[e]^T.  x is the (dequantised)
  * input row of K values. */
-static void expert_row(const orc_weights *W, int e, const double *x,
-                       int requant_h, double *h, double *y)
+/* h (N) = act(x W1[e][0:N]^T) * (x W1[e][N:2N]^T) */
+static void expert_h(const orc_weights *W, int e, const double *x, double *h)
 {
     int n, k, N = W->N, K = W->K;
     for (n = 0; n < N; ++n) {
@@ -588,6 +619,25 @@ static void expert_row(const orc_weights *W, int e, const double *x,
         else
             h[n] = g / (1.0 + exp(-g)) * u;                  /* SiLU */
     }
+}
+
+/* y (K) = h W2[e]^T */
+static void expert_y(const orc_weights *W, int e, const double *h, double *y)
+{
+    int n, k, N = W->N, K = W->K;
+    for (k = 0; k < K; ++k) {
+        double acc = 0.0;
+        for (n = 0; n < N; ++n)
+            acc += h[n] * weight_at(W, 2, e, k, n);
+        y[k] = acc;
+    }
+}
+
+static void expert_row(const orc_weights *W, int e, const double *x,
+                       int requant_h, double *h, double *y)
+{
+    int n, N = W->N;
+    expert_h(W, e, x, h);
     if (requant_h) {
         int gi, gw = W->dtype == ORC_FP8_CHANNEL ? N : 128;
         if (W->dtype == ORC_FP8_CHANNEL)
@@ -606,12 +656,7 @@ static void expert_row(const orc_weights *W, int e, const double *x,
                        (double)s;
         }
     }
-    for (k = 0; k < K; ++k) {
-        double acc = 0.0;
-        for (n = 0; n < N; ++n)
-            acc += h[n] * weight_at(W, 2, e, k, n);
-        y[k] = acc;
-    }
+    expert_y(W, e, h, y);
 }
 
 /* Input row t of x (M, K) bf16 times `scale`, as the experts see it: the
@@ -678,6 +723,86 @@ void orc_expert_row(int dtype, const uint16_t *x, int t, int e, int E, int N,
  * (apply_router_weight_on_input, meant for topk == 1): the router weight
  * multiplies the expert's input instead of its output,
  *   out[t] = sum_j expert(w[t,j] * x[t]). */
+/* The layer with per-tensor activation scales (Q7).  The scale of H spans
+ * every routed pair, so this takes two passes: first x's scale and every
+ * local pair's hidden row (all M tokens, whatever `tokens` lists), then the
+ * scale of H and the outputs of the listed tokens.  Arguments as
+ * orc_moe_forward_ep. */
+static void forward_tensor(const uint16_t *x, const float *logits,
+                           const float *bias, int M, int K, int N, int E,
+                           int topk, int score_fn, int n_groups,
+                           int topk_groups, int renorm, int requant_h,
+                           const int32_t *expert_map, int E_local,
+                           int weight_on_input, const orc_weights *W,
+                           const int32_t *tokens, int n_tok, int32_t *ids_out,
+                           double *w_out, double *out)
+{
+    const size_t P = (size_t)M * topk;
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (P ? P : 1));
+    double *w = (double *)malloc(sizeof(double) * (P ? P : 1));
+    float *rw = (float *)malloc(sizeof(float) * (size_t)(M ? M : 1));
+    uint8_t *xq = (uint8_t *)malloc((size_t)M * K + 1);
+    double *h = (double *)malloc(sizeof(double) * (P * N + 1));
+    char *local = (char *)malloc(P + 1);
+    double *xr = (double *)malloc(sizeof(double) * (size_t)K);
+    double *hq = (double *)malloc(sizeof(double) * (size_t)N);
+    double *y = (double *)malloc(sizeof(double) * (size_t)K);
+    float sx, sh = 1.0f, amax = 0.0f;
+    int t, j, k, n, i;
+    for (t = 0; t < M; ++t) {
+        orc_route(logits + (size_t)t * E, bias, 1, E, topk, score_fn, n_groups,
+                  topk_groups, renorm, ids + (size_t)t * topk,
+                  w + (size_t)t * topk, NULL);
+        rw[t] = (float)w[(size_t)t * topk]; /* weight on input: topk is 1 */
+    }
+    orc_quant_fp8_tensor(x, weight_on_input ? rw : NULL, M, K, xq, &sx);
+    for (t = 0; t < M; ++t) {
+        for (k = 0; k < K; ++k)
+            xr[k] = orc_e4m3_value(xq[(size_t)t * K + k]) * (double)sx;
+        for (j = 0; j < topk; ++j) {
+            size_t p = (size_t)t * topk + j;
+            int l = local_expert(ids[p], E, expert_map, E_local);
+            local[p] = l >= 0;
+            if (l < 0)
+                continue;
+            expert_h(W, l, xr, h + p * N);
+            for (n = 0; n < N; ++n) {
+                float v;
+                h[p * N + n] = bf16_round(h[p * N + n]);
+                v = (float)fabs((float)h[p * N + n]);
+                if (v > amax)
+                    amax = v;
+            }
+        }
+    }
+    if (requant_h)
+        sh = group_scale(amax);
+    if (!tokens)
+        n_tok = M;
+    for (i = 0; i < n_tok; ++i) {
+        double *o = out + (size_t)i * K;
+        t = tokens ? tokens[i] : i;
+        for (k = 0; k < K; ++k)
+            o[k] = 0.0;
+        for (j = 0; j < topk; ++j) {
+            size_t p = (size_t)t * topk + j;
+            ids_out[(size_t)i * topk + j] = ids[p];
+            w_out[(size_t)i * topk + j] = w[p];
+            if (!local[p])
+                continue;
+            for (n = 0; n < N; ++n)
+                hq[n] = requant_h ? orc_e4m3_value(orc_e4m3_encode(
+                                        (float)h[p * N + n] / sh)) * (double)sh
+                                  : h[p * N + n];
+            expert_y(W, local_expert(ids[p], E, expert_map, E_local), hq, y);
+            for (k = 0; k < K; ++k)
+                o[k] += (weight_on_input ? 1.0 : w[p]) * y[k];
+        }
+    }
+    free(ids); free(w); free(rw); free(xq); free(h); free(local);
+    free(xr); free(hq); free(y);
+}
+
 void orc_moe_forward_ep(const uint16_t *x, const float *logits,
                         const float *bias, int M, int K, int N, int E,
                         int topk, int score_fn, int n_groups, int topk_groups,
@@ -694,6 +819,12 @@ void orc_moe_forward_ep(const uint16_t *x, const float *logits,
     fill_e4m3_table();
     W.dtype = dtype; W.E = E_local; W.N = N; W.K = K; W.act = act;
     W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
+    if (dtype == ORC_FP8_TENSOR) {
+        forward_tensor(x, logits, bias, M, K, N, E, topk, score_fn, n_groups,
+                       topk_groups, renorm, requant_h, expert_map, E_local,
+                       weight_on_input, &W, tokens, n_tok, ids_out, w_out, out);
+        return;
+    }
     if (!tokens)
         n_tok = M;
 #ifdef _OPENMP

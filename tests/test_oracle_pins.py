@@ -495,3 +495,57 @@ def test_fp8_channel_single_expert_is_dequantised_swiglu(orc):
         np.testing.assert_allclose(hq, hd[t], rtol=0, atol=float(sh[t]) * 2 ** -3 + 1e-12)
         ref = hd[t] @ w2.T
         np.testing.assert_allclose(y, ref, rtol=0, atol=2e-3 * np.abs(ref).max())
+
+
+def test_fp8_tensor_quant_is_one_group_for_the_whole_tensor(orc):
+    """Per-tensor activation scale: the max over every element (of the fp32
+    product with the row weights), codes = torch's cast of the quotient."""
+    g = torch.Generator().manual_seed(44)
+    x = (torch.randn((9, 256), generator=g) * torch.linspace(0.1, 5, 9)[:, None]).to(torch.bfloat16)
+    rw = (torch.rand(9, generator=g) + 0.1).numpy().astype(np.float32)
+    for w in (None, rw):
+        v = x.float().numpy() * (1.0 if w is None else w[:, None])
+        v = v.astype(np.float32)
+        s = np.float32(max(np.abs(v).max(), np.float32(1e-12))) / np.float32(448)
+        q, sc = orc.quant_fp8_tensor(_bits(x), row_weights=w)
+        assert sc == s
+        np.testing.assert_array_equal(
+            q, torch.from_numpy(v / s).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+
+
+def test_fp8_tensor_layer_uses_one_scale_for_all_hidden_rows(orc):
+    """Per-tensor activations (two experts, top-1): x quantised with one scale,
+    every routed hidden row rounded to bf16, then one scale for all of H;
+    written with numpy, torch's casts and the routing's argmax."""
+    cfg = WL.MoEConfig("f8t", M=10, K=256, N=256, E=2, topk=1, seed=26)
+    d = WL.make_inputs(cfg)
+    N = cfg.N
+    q1, s1, q2, s2 = [], [], [], []
+    for e in range(2):
+        a, b = _rowwise_quant_torch(d["w1"][e].float().numpy())
+        c, dd = _rowwise_quant_torch(d["w2"][e].float().numpy())
+        q1.append(a); s1.append(b); q2.append(c); s2.append(dd)
+    W = orc.Weights(orc.FP8_TENSOR, np.stack(q1), np.stack(q2), np.stack(s1), np.stack(s2))
+    out, ids, w = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1, orc.SOFTMAX,
+                                  W, requant_h=True)
+    ref_ids = np.argmax(d["logits"].numpy(), axis=1)
+    assert np.array_equal(ids[:, 0], ref_ids)
+
+    def deq(q, s):
+        return torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy() * s
+
+    x32 = d["x"].float().numpy()
+    sx = np.float32(np.abs(x32).max()) / np.float32(448)
+    xd = deq(torch.from_numpy(x32 / sx).to(torch.float8_e4m3fn).view(torch.uint8).numpy(), float(sx))
+    hs = []
+    for t in range(cfg.M):
+        e = ref_ids[t]
+        w1d = deq(q1[e], s1[e].astype(np.float64)[:, None])
+        g_, u_ = xd[t] @ w1d[:N].T, xd[t] @ w1d[N:].T
+        hs.append(_silu(g_) * u_)
+    hb = torch.from_numpy(np.stack(hs).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    sh = np.float32(np.abs(hb).max()) / np.float32(448)
+    hd = deq(torch.from_numpy(hb / sh).to(torch.float8_e4m3fn).view(torch.uint8).numpy(), float(sh))
+    ref = np.stack([hd[t] @ deq(q2[ref_ids[t]], s2[ref_ids[t]].astype(np.float64)[:, None]).T
+                    for t in range(cfg.M)])
+    np.testing.assert_allclose(out, ref, rtol=0, atol=2e-3 * np.abs(ref).max())
