@@ -158,7 +158,10 @@ class Layer:
         M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
         P = M * k
         self.fp8 = cfg.dtype != WL.BF16
-        self.ch = cfg.dtype == WL.FP8_CHANNEL  # one scale per token / per weight row
+        # one scale per weight row; per token (FP8_CHANNEL) or per tensor
+        # (FP8_TENSOR) for the activations
+        self.ch = cfg.dtype in (WL.FP8_CHANNEL, WL.FP8_TENSOR)
+        self.tensor = cfg.dtype == WL.FP8_TENSOR
         if self.ch:
             self.w1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=device)
             self.w2 = torch.empty((E, K, N), dtype=torch.uint8, device=device)
@@ -207,9 +210,12 @@ class Layer:
         self.y = torch.empty((M, k, K), dtype=torch.bfloat16, device=device)
         self.out = torch.empty((M, K), dtype=torch.bfloat16, device=device)
         self.err = torch.zeros(1, dtype=i32, device=device)
+        self.amax = torch.zeros(2, dtype=i32, device=device) if self.tensor else None
         self.fwd_ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype, device=device)
-        # route, 3 align, [quant x], gather, gate/up, [quant H], down, reduce
-        self.launches_per_step = 8 + (1 if self.fp8 else 0) + (1 if self.ch else 0)
+        # route, 3 align, [quant x], gather, gate/up, [quant H], down, reduce;
+        # a per-tensor quant is a clear, a maximum and the codes
+        self.launches_per_step = (8 + (1 if self.fp8 else 0) + (1 if self.ch else 0)
+                                  + (4 if self.tensor else 0))
 
     def step(self, ev_gemm=None):
         g, c = self.g, self.cfg
@@ -219,7 +225,10 @@ class Layer:
         g.moe_align_permute(self.ids, E, self.counts, self.offsets, self.sorted, self.inv,
                             self.align_ws, self.err)
         src, src_s = self.x, None
-        if self.fp8:
+        if self.tensor:
+            g.moe_quant_fp8_tensor(self.x, self.xq, self.xs, self.amax[0:1])
+            src, src_s = self.xq, self.xs
+        elif self.fp8:
             g.moe_quant_fp8_group(self.x, self.xq, self.xs, group=K if self.ch else 128)
             src, src_s = self.xq, self.xs
         g.moe_permute_rows(src, src_s, self.sorted, self.offsets, k, E, c.dtype, self.A, self.As)
@@ -230,7 +239,10 @@ class Layer:
                                         self.Hs, self.err)
         if ev_gemm is not None:
             ev_gemm[1].record()
-        if self.ch:
+        if self.tensor:  # rows of pairs computed here: offsets[E]
+            g.moe_quant_fp8_tensor(self.Hb, self.H, self.Hs, self.amax[1:2],
+                                   n_rows=self.offsets[E:])
+        elif self.ch:
             g.moe_quant_fp8_group(self.Hb, self.H, self.Hs, group=N)
         g.moe_grouped_gemm_down(self.H, self.Hs, self.sorted, self.offsets, self.wts, M, k, E,
                                 N, K, self.w2, self.w2s, c.dtype, self.y, self.err)
@@ -355,7 +367,8 @@ def run_gpu(args, cfg):
 
 def _scales_desc(cfg):
     return {WL.BF16: "none", WL.FP8: "fp32, 1x128 activations / 128x128 weights",
-            WL.FP8_CHANNEL: "fp32, per token / per output channel"}[cfg.dtype]
+            WL.FP8_CHANNEL: "fp32, per token / per output channel",
+            WL.FP8_TENSOR: "fp32, per activation tensor / per output channel"}[cfg.dtype]
 
 
 def _gate_up_kernel_name(cfg):
@@ -365,7 +378,7 @@ def _gate_up_kernel_name(cfg):
     or more)."""
     if cfg.dtype == WL.FP8:
         return "grouped_gemm_fp8_kernel"
-    if cfg.dtype == WL.FP8_CHANNEL:
+    if cfg.dtype in (WL.FP8_CHANNEL, WL.FP8_TENSOR):
         return "grouped_gemm_kernel"
     pairs = cfg.M * cfg.topk >= 128 * cfg.E
     return "grouped_gemm_pair_kernel" if pairs else "grouped_gemm_kernel"
@@ -376,7 +389,7 @@ def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
     peaks, src = _peaks()
     P = cfg.M * cfg.topk
     fp8 = cfg.dtype != WL.BF16
-    ch = cfg.dtype == WL.FP8_CHANNEL
+    ch = cfg.dtype in (WL.FP8_CHANNEL, WL.FP8_TENSOR)
     eb = 1 if fp8 else 2
     # the dominant kernel: the gate/up grouped GEMM (2/3 of the layer's FLOPs)
     gemm_flop = 4.0 * cfg.K * cfg.N * P
@@ -563,7 +576,7 @@ def _oracle_inputs(cfg, d, tokens):
         b2 = WL.bf16_bits(d["w2"][e])
         if cfg.dtype == WL.BF16:
             blocks[int(e)] = (b1, b2)
-        elif cfg.dtype == WL.FP8_CHANNEL:
+        elif cfg.dtype in (WL.FP8_CHANNEL, WL.FP8_TENSOR):
             q1, s1 = orc.quant_fp8_group(b1, group=cfg.K)
             q2, s2 = orc.quant_fp8_group(b2, group=cfg.N)
             blocks[int(e)] = (q1, q2, s1[:, 0], s2[:, 0])
@@ -584,8 +597,15 @@ def _time_oracle(cfg, d, W, tokens, threads):
     return time.perf_counter() - t
 
 
+_TENSOR_UNBOUNDED = ("per-tensor activation scales couple every token: the oracle computes "
+                     "all tokens' hidden rows before any output, so no bounded token sample "
+                     "of this workload exists")
+
+
 def cpu_baseline(cfg, layer, budget_s):
     """The oracle as it stands on the host cores, on a bounded token sample."""
+    if cfg.dtype == WL.FP8_TENSOR:
+        return {"unavailable": _TENSOR_UNBOUNDED}
     import oracle as orc
     orc.build()
     cores = os.cpu_count() or 1
@@ -610,6 +630,9 @@ def run_reference(args, cfg):
     per step on a bounded token sample of the same workload."""
     world, rank, _ = _dist()
     if rank != 0:
+        return
+    if cfg.dtype == WL.FP8_TENSOR:
+        print(json.dumps({"impl": "reference", "unavailable": _TENSOR_UNBOUNDED}), flush=True)
         return
     import torch
     import oracle as orc

@@ -66,8 +66,14 @@ typedef enum {
  *                         (FusedMoEPermuteExpertsUnpermute's quant
  *                         properties); the scale rule is that of
  *                         moe_quant_fp8_group with a group as wide as the
- *                         row. */
-enum { GBMOE_BF16 = 0, GBMOE_FP8_E4M3 = 1, GBMOE_FP8_E4M3_CHANNEL = 2 };
+ *                         row;
+ * GBMOE_FP8_E4M3_TENSOR   e4m3 with one fp32 scale for a whole activation
+ *                         tensor (the layer's input; H) -- per_act_token_quant
+ *                         off, no block shape -- and per-channel weight
+ *                         scales as above (per-tensor weight scales are
+ *                         per-channel scales of equal value). */
+enum { GBMOE_BF16 = 0, GBMOE_FP8_E4M3 = 1, GBMOE_FP8_E4M3_CHANNEL = 2,
+       GBMOE_FP8_E4M3_TENSOR = 3 };
 /* router score function */
 enum { GBMOE_SOFTMAX = 0, GBMOE_SIGMOID = 1 };
 /* gated activation of the experts (FusedMoEPermuteExpertsUnpermute.activation):
@@ -183,6 +189,22 @@ gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, const float *row_weights,
                                    int M, int K, int group, uint8_t *q,
                                    float *scales, gbmoe_stream_t stream);
 
+/* The quantiser with one group holding a whole tensor (dynamic per-tensor
+ * scale): over rows t < n (n = *n_rows when n_rows is given, a device
+ * int32 -- the row count a previous kernel wrote, e.g. offsets[E] -- else M),
+ * with v[t,k] = x[t,k] * row_weights[t] as above,
+ *   s = max(max_{t<n,k} |v[t,k]|, 1e-12) / 448,  q[t,k] = e4m3(v[t,k] / s),
+ * and row_scales[t] = s for every t < n, so that the permute and GEMM calls
+ * take the tensor's scale as a per-row one (dtype GBMOE_FP8_E4M3_TENSOR).
+ * Rows t >= n are left unwritten.  amax_ws: 4 bytes of caller device
+ * memory, overwritten (the maximum is reduced there; max is order-free, so
+ * the result is deterministic).  Three launches on `stream` (a 4-byte
+ * clear, the maximum, the codes).  K % 128 == 0; x, q 16-byte aligned. */
+gbmoe_status_t moe_quant_fp8_tensor(const uint16_t *x, const float *row_weights,
+                                    int M, int K, const int32_t *n_rows,
+                                    uint8_t *q, float *row_scales,
+                                    uint32_t *amax_ws, gbmoe_stream_t stream);
+
 /* The same quantiser over block x block tiles of a weight matrix, for
  * preparing FP8 expert weights (not part of the timed layer):
  * w (R, C) bf16 -> q (R, C) e4m3 and scales (R/block, C/block) fp32, one
@@ -206,9 +228,9 @@ gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
  *   of consecutive rows are contiguous for the GEMM's TMA loads.
  *   row_weights must be NULL (the FP8 rows take the weight in
  *   moe_quant_fp8_group, before the codes are chosen).
- * dtype GBMOE_FP8_E4M3_CHANNEL: x (M, K) e4m3 with x_scales (M) fp32 ->
- *   A (M*topk, K) e4m3 with A_scales (M*topk) fp32, one per row; row_weights
- *   must be NULL.
+ * dtype GBMOE_FP8_E4M3_CHANNEL or GBMOE_FP8_E4M3_TENSOR: x (M, K) e4m3 with
+ *   x_scales (M) fp32 -> A (M*topk, K) e4m3 with A_scales (M*topk) fp32, one
+ *   per row; row_weights must be NULL.
  * K % 128 == 0; x and A 16-byte aligned. */
 gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
                                 const float *row_weights,
@@ -235,12 +257,14 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
  *   before it is added.  H is written as e4m3 with group-major H_scales
  *   (N/128, ld) fp32, requantised per 128-group of a row with the
  *   moe_quant_fp8_group rule.
- * dtype GBMOE_FP8_E4M3_CHANNEL: A e4m3 with A_scales (M*topk) fp32, w1 e4m3
- *   with w1_scales (E, 2N) fp32; the whole K is accumulated in fp32 and
- *   scaled once, g[n] = A_scale[i] * w1_scale[e, n] * (codes dot product).
- *   H (M*topk, N) is written in bf16 (H_scales unused): a per-token scale
- *   spans the whole row, so the caller quantises H with moe_quant_fp8_group
- *   (group = N) before moe_grouped_gemm_down.
+ * dtype GBMOE_FP8_E4M3_CHANNEL or GBMOE_FP8_E4M3_TENSOR: A e4m3 with
+ *   A_scales (M*topk) fp32, w1 e4m3 with w1_scales (E, 2N) fp32; the whole K
+ *   is accumulated in fp32 and scaled once,
+ *   g[n] = A_scale[i] * w1_scale[e, n] * (codes dot product).
+ *   H (M*topk, N) is written in bf16 (H_scales unused): its scale spans at
+ *   least a whole row, so the caller quantises H with moe_quant_fp8_group
+ *   (group = N; CHANNEL) or moe_quant_fp8_tensor (n_rows = offsets + E;
+ *   TENSOR) before moe_grouped_gemm_down.
  * Accumulation is fp32.  N % 128 == 0, K % 128 == 0.  err_word may be NULL. */
 gbmoe_status_t moe_grouped_gemm_gate_up_silu(
     const void *A, const float *A_scales, const int32_t *offsets, int M,
@@ -270,8 +294,9 @@ gbmoe_status_t moe_grouped_gemm_gate_up_gelu(
  * dtype GBMOE_FP8_E4M3: H e4m3 + group-major H_scales (N/128, ld), ld =
  *   M*topk rounded up to 4 (as written by the gate/up call); w2 e4m3 +
  *   w2_scales (E, K/128, N/128).
- * dtype GBMOE_FP8_E4M3_CHANNEL: H e4m3 + H_scales (M*topk) fp32, one per
- *   row; w2 e4m3 + w2_scales (E, K) fp32, one per output channel.
+ * dtype GBMOE_FP8_E4M3_CHANNEL or GBMOE_FP8_E4M3_TENSOR: H e4m3 + H_scales
+ *   (M*topk) fp32, one per row; w2 e4m3 + w2_scales (E, K) fp32, one per
+ *   output channel.
  * Accumulation fp32.  err_word may be NULL. */
 gbmoe_status_t moe_grouped_gemm_down(
     const void *H, const float *H_scales, const int32_t *sorted_pair_ids,
@@ -329,6 +354,8 @@ gbmoe_status_t moe_batched_masked_experts(
  * dtype GBMOE_FP8_E4M3_CHANNEL: w1/w2 e4m3 with their per-channel scales
  *   (E, 2N) / (E, K); the activations are quantised with one scale per
  *   token, H is kept in bf16 and quantised per token before the second GEMM.
+ * dtype GBMOE_FP8_E4M3_TENSOR: the same weights; x is quantised with one
+ *   scale for all M tokens and H with one for all its computed rows.
  * out (M, K) bf16.  topk_ids / topk_weights (M, topk) may be NULL; when given
  * they receive the router's output (global ids).
  * ws: moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype) bytes.
@@ -349,7 +376,9 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
  * `stream`, as FusedMoEModularKernel._maybe_chunk_fused_experts does to bound
  * its workspaces -- but with every chunk's counts computed on the device (the
  * pages copy them to the host per chunk), so the whole loop stays
- * capturable.  Each token's result is the same as unchunked, bit for bit.
+ * capturable.  Each token's result is the same as unchunked, bit for bit --
+ * except with GBMOE_FP8_E4M3_TENSOR, whose activation scales are then taken
+ * per chunk (as the chunk loop quantises each chunk on its own).
  * Arguments as moe_forward (topk_ids / topk_weights may be NULL);
  * ws: moe_workspace_size(GBMOE_WS_FORWARD, min(M, chunk_size), E, N, K,
  * topk, dtype) bytes. */

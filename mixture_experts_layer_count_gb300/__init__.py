@@ -17,7 +17,7 @@ import torch
 
 from . import build as _build
 
-BF16, FP8_E4M3, FP8_E4M3_CHANNEL = 0, 1, 2  # dtype codes of include/gbmoe.h
+BF16, FP8_E4M3, FP8_E4M3_CHANNEL, FP8_E4M3_TENSOR = 0, 1, 2, 3  # dtype codes of include/gbmoe.h
 SOFTMAX, SIGMOID = 0, 1
 ACT_SILU, ACT_GELU = 0, 1
 WS_ALIGN, WS_BATCHED, WS_FORWARD, WS_SHARED = 0, 2, 3, 4
@@ -56,6 +56,7 @@ _SIGS = {
                                 _Z, _P, _P, _P, _P, _P]),
     "moe_align_permute_no_ws": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_group": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "moe_quant_fp8_tensor": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
     "moe_permute_rows": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm_gate_up_silu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
@@ -166,6 +167,17 @@ def moe_quant_fp8_group(x, q, scales, group=128, stream=None, row_weights=None):
     _check("moe_quant_fp8_group", load().moe_quant_fp8_group(
         _ptr(x), _ptr(row_weights), M, K, group, _ptr(q), _ptr(scales),
         _stream(stream)))
+
+
+def moe_quant_fp8_tensor(x, q, row_scales, amax_ws, n_rows=None, stream=None,
+                         row_weights=None):
+    """One scale for the whole tensor (rows < *n_rows when n_rows, a device
+    int32, is given); row_scales (M) receives it for every such row;
+    amax_ws: a 4-byte device buffer."""
+    M, K = x.shape
+    _check("moe_quant_fp8_tensor", load().moe_quant_fp8_tensor(
+        _ptr(x), _ptr(row_weights), M, K, _ptr(n_rows), _ptr(q), _ptr(row_scales),
+        _ptr(amax_ws), _stream(stream)))
 
 
 def moe_quant_fp8_block(w, q, scales, block=128, stream=None):

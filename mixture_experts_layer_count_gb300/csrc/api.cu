@@ -65,11 +65,16 @@ struct Carver {
   }
 };
 
-bool is_fp8(int dtype) { return dtype == GBMOE_FP8_E4M3 || dtype == GBMOE_FP8_E4M3_CHANNEL; }
+// e4m3 with one scale per row of each GEMM operand (per token or per tensor
+// for the activations, per channel for the weights)
+bool row_scaled(int dtype) {
+  return dtype == GBMOE_FP8_E4M3_CHANNEL || dtype == GBMOE_FP8_E4M3_TENSOR;
+}
+bool is_fp8(int dtype) { return dtype == GBMOE_FP8_E4M3 || row_scaled(dtype); }
 size_t elem_bytes(int dtype) { return is_fp8(dtype) ? 1 : 2; }
 // fp32 scales per row of a (rows, cols) e4m3 operand: one per 128 columns,
-// or one per row (GBMOE_FP8_E4M3_CHANNEL)
-int scales_per_row(int dtype, int cols) { return dtype == GBMOE_FP8_E4M3_CHANNEL ? 1 : cols / 128; }
+// or one per row (row-scaled e4m3)
+int scales_per_row(int dtype, int cols) { return row_scaled(dtype) ? 1 : cols / 128; }
 
 // leading dimension of the group-major FP8 row scales of M*topk rows
 int64_t scale_ld(size_t P) { return (int64_t)((P + 3) / 4 * 4); }
@@ -85,7 +90,8 @@ struct ForwardWs {
   float *As;
   void *H;
   float *Hs;
-  uint16_t *Hb;  // GBMOE_FP8_E4M3_CHANNEL: H in bf16 before its per-token quantisation
+  uint16_t *Hb;     // row-scaled e4m3: H in bf16 before its quantisation
+  uint32_t *amax;   // GBMOE_FP8_E4M3_TENSOR: the maxima of x and of H
   uint16_t *y_slot;
 };
 ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dtype) {
@@ -106,7 +112,8 @@ ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dty
   w.As = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * sk * 4)) : nullptr;
   w.H = c.take(P * (size_t)N * elem_bytes(dtype));
   w.Hs = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * sn * 4)) : nullptr;
-  w.Hb = dtype == GBMOE_FP8_E4M3_CHANNEL ? static_cast<uint16_t *>(c.take(P * (size_t)N * 2))
+  w.Hb = row_scaled(dtype) ? static_cast<uint16_t *>(c.take(P * (size_t)N * 2)) : nullptr;
+  w.amax = dtype == GBMOE_FP8_E4M3_TENSOR ? static_cast<uint32_t *>(c.take(2 * sizeof(uint32_t)))
                                          : nullptr;
   w.y_slot = static_cast<uint16_t *>(c.take(P * (size_t)K * 2));
   return w;
@@ -142,7 +149,7 @@ gbmoe_status_t gate_up_impl(const void *A, const float *A_scales,
   a.mode = kGateUp;
   a.act = act;
   a.fp8 = dtype == GBMOE_FP8_E4M3;
-  a.fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
+  a.fp8ch = row_scaled(dtype);
   a.offsets = offsets;
   a.E = E;
   a.N = N;
@@ -183,7 +190,7 @@ gbmoe_status_t down_impl(const void *H, const float *H_scales,
   GroupedGemmArgs a{};
   a.mode = kDown;
   a.fp8 = dtype == GBMOE_FP8_E4M3;
-  a.fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
+  a.fp8ch = row_scaled(dtype);
   a.offsets = offsets;
   a.E = E;
   a.N = N;
@@ -329,6 +336,22 @@ gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, const float *row_weights,
   return from_cuda(launch_quant_group(x, row_weights, M, K, q, scales, (cudaStream_t)stream));
 }
 
+gbmoe_status_t moe_quant_fp8_tensor(const uint16_t *x, const float *row_weights,
+                                    int M, int K, const int32_t *n_rows,
+                                    uint8_t *q, float *row_scales,
+                                    uint32_t *amax_ws, gbmoe_stream_t stream) {
+  if (M < 0 || K < 128 || K % 128 != 0) return GBMOE_INVALID_ARG;
+  if (M > 0 && (!x || !q || !row_scales || !amax_ws || !aligned16(x) || !aligned16(q) ||
+                reinterpret_cast<uintptr_t>(amax_ws) % 4 != 0))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  if (M == 0) return GBMOE_OK;
+  return from_cuda(launch_quant_tensor(x, row_weights, M, K, n_rows, q, row_scales, amax_ws,
+                                       sms, (cudaStream_t)stream));
+}
+
 gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
                                    int block, uint8_t *q, float *scales,
                                    gbmoe_stream_t stream) {
@@ -377,7 +400,7 @@ static gbmoe_status_t gate_up_entry(
   if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
   if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
   const bool fp8 = dtype == GBMOE_FP8_E4M3;
-  const bool fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
+  const bool fp8ch = row_scaled(dtype);
   if (M > 0) {
     if (!A || !offsets || !w1 || !H) return GBMOE_INVALID_ARG;
     if (fp8 && (!A_scales || !w1_scales || !H_scales)) return GBMOE_INVALID_ARG;
@@ -423,7 +446,7 @@ gbmoe_status_t moe_grouped_gemm_down(
   const bool fp8 = is_fp8(dtype);
   if (!H || !sorted_pair_ids || !offsets || !w2 || !y_slot) return GBMOE_INVALID_ARG;
   if (fp8 && (!H_scales || !w2_scales)) return GBMOE_INVALID_ARG;
-  if (dtype == GBMOE_FP8_E4M3_CHANNEL && !aligned16(w2_scales)) return GBMOE_INVALID_ARG;
+  if (row_scaled(dtype) && !aligned16(w2_scales)) return GBMOE_INVALID_ARG;
   if (!aligned16(H) || !aligned16(w2) || !aligned16(y_slot)) return GBMOE_INVALID_ARG;
   int sms;
   gbmoe_status_t st = device_info(&sms);
@@ -517,7 +540,7 @@ static gbmoe_status_t forward_validate(const uint16_t *x, const float *logits,
   if (M > 0) {
     if (!x || !logits || !w1 || !w2 || !out || !ws) return GBMOE_INVALID_ARG;
     if (fp8 && (!w1_scales || !w2_scales)) return GBMOE_INVALID_ARG;
-    if (dtype == GBMOE_FP8_E4M3_CHANNEL && (!aligned16(w1_scales) || !aligned16(w2_scales)))
+    if (row_scaled(dtype) && (!aligned16(w1_scales) || !aligned16(w2_scales)))
       return GBMOE_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(ws))
       return GBMOE_INVALID_ARG;
@@ -544,7 +567,8 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                                         w1_scales, w2, w2_scales, out, ws, ws_bytes);
   if (vst != GBMOE_OK) return vst;
   const bool fp8 = is_fp8(dtype);
-  const bool fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
+  const bool fp8ch = row_scaled(dtype);
+  const bool fp8t = dtype == GBMOE_FP8_E4M3_TENSOR;
   int sms;
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK) return st;
@@ -568,8 +592,9 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   const void *a_src = x;
   const float *a_src_s = nullptr;
   if (fp8) {
-    ce = fp8ch ? launch_quant_row(x, in_w, M, K, w.xq, w.xs, s)
-               : launch_quant_group(x, in_w, M, K, w.xq, w.xs, s);
+    ce = fp8t    ? launch_quant_tensor(x, in_w, M, K, nullptr, w.xq, w.xs, w.amax, sms, s)
+         : fp8ch ? launch_quant_row(x, in_w, M, K, w.xq, w.xs, s)
+                 : launch_quant_group(x, in_w, M, K, w.xq, w.xs, s);
     if (ce != cudaSuccess) return from_cuda(ce);
     a_src = w.xq;
     a_src_s = w.xs;
@@ -577,12 +602,16 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   st = permute_impl(a_src, a_src_s, fp8 ? nullptr : in_w, w.sorted, w.offsets, M, topk, E, K,
                     dtype, w.A, w.As, sms, s);
   if (st != GBMOE_OK) return st;
-  // per-token scales span a whole row of H: it is written in bf16 and
-  // quantised per row before the second GEMM
+  // per-token (per-tensor) scales span a whole row (all computed rows) of
+  // H: it is written in bf16 and quantised before the second GEMM
   st = gate_up_impl(w.A, w.As, w.offsets, M, topk, E, N, K, w1, w1_scales, dtype, activation,
                     fp8ch ? static_cast<void *>(w.Hb) : w.H, w.Hs, err_word, sms, s);
   if (st != GBMOE_OK) return st;
-  if (fp8ch) {
+  if (fp8t) {  // rows at and beyond offsets[E] (pairs not computed here) do not count
+    ce = launch_quant_tensor(w.Hb, nullptr, P, N, w.offsets + E, static_cast<uint8_t *>(w.H),
+                             w.Hs, w.amax + 1, sms, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+  } else if (fp8ch) {
     ce = launch_quant_row(w.Hb, nullptr, P, N, static_cast<uint8_t *>(w.H), w.Hs, s);
     if (ce != cudaSuccess) return from_cuda(ce);
   }

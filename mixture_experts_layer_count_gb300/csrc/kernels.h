@@ -44,6 +44,9 @@ cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int
                                uint8_t *q, float *scales, cudaStream_t s);
 cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K,
                              uint8_t *q, float *scales, cudaStream_t s);
+cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, int K,
+                                const int32_t *n_rows, uint8_t *q, float *row_scales,
+                                uint32_t *amax, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_block(const uint16_t *w, int64_t R, int C, uint8_t *q,
                                float *scales, cudaStream_t s);
 

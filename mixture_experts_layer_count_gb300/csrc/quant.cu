@@ -10,7 +10,8 @@
 //                                       saturating at +-448)
 // The group is 128 values, or a whole row (one scale per token of the
 // activations, per_act_token_quant; per output channel of a weight matrix,
-// per_out_ch_quant).
+// per_out_ch_quant), or a whole tensor (per-tensor activation scale: a
+// grid-wide maximum first, then the codes).
 // HBM-bound: each kernel reads its input once (the row kernel a second time
 // from L1/L2) and writes q and s once.
 #include <cuda_bf16.h>
@@ -118,6 +119,78 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// 8 values of a 16-byte vector, times the row weight (an fp32 product)
+__device__ __forceinline__ void unpack8(uint4 raw, const float *row_w, size_t t, float (&v)[8]) {
+  const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+  const float w = row_w ? row_w[t] : 1.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_float(u[i] & 0xffffu);
+    v[2 * i + 1] = bf16_bits_to_float(u[i] >> 16);
+    if (row_w) {
+      v[2 * i] = __fmul_rn(v[2 * i], w);
+      v[2 * i + 1] = __fmul_rn(v[2 * i + 1], w);
+    }
+  }
+}
+
+__device__ __forceinline__ int tensor_rows(const int32_t *n_rows, int M) {
+  if (!n_rows) return M;
+  const int n = *n_rows;
+  return n < 0 ? 0 : (n > M ? M : n);
+}
+
+// per-tensor maximum of |v| over rows t < n: each block reduces its share,
+// then one integer atomicMax on the bit pattern (a float >= 0 orders like
+// its bits; max does not depend on the order of the updates)
+__global__ void __launch_bounds__(256)
+    quant_tensor_max_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w,
+                            int M, int K, const int32_t *__restrict__ n_rows,
+                            unsigned int *__restrict__ amax) {
+  __shared__ float red[8];
+  const int vecs = K / 8;
+  const size_t total = (size_t)tensor_rows(n_rows, M) * vecs;
+  float m = 0.0f;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float v[8];
+    unpack8(x[i], row_w, i / vecs, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) b = fmaxf(b, red[w]);
+    atomicMax(amax, __float_as_uint(b));
+  }
+}
+
+// the codes with the tensor's scale; row_scales[t] = s for every row t < n
+__global__ void __launch_bounds__(256)
+    quant_tensor_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w, int M,
+                        int K, const int32_t *__restrict__ n_rows,
+                        const unsigned int *__restrict__ amax, uint2 *__restrict__ q,
+                        float *__restrict__ row_scales) {
+  const int vecs = K / 8;
+  const size_t total = (size_t)tensor_rows(n_rows, M) * vecs;
+  const float s = group_scale(__uint_as_float(*amax));
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float v[8];
+    unpack8(x[i], row_w, i / vecs, v);
+    uint32_t c[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c[j] = e4m3_of(__fdiv_rn(v[j], s));
+    q[i] = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                      c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+    if (i % vecs == 0) row_scales[i / vecs] = s;
+  }
+}
+
 // one block of 256 threads per 128 x 128 tile; thread i reads rows
 // (i / 16) + 16 r, r < 8, columns (i % 16) * 8 .. + 8
 __global__ void __launch_bounds__(256)
@@ -186,6 +259,26 @@ cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K
   quant_row_kernel<<<(unsigned)blocks, 256, 0, s>>>(
       reinterpret_cast<const uint4 *>(x), row_w, M, K, reinterpret_cast<uint2 *>(q),
       scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, int K,
+                                const int32_t *n_rows, uint8_t *q, float *row_scales,
+                                uint32_t *amax, int num_sms, cudaStream_t s) {
+  cudaError_t st = cudaMemsetAsync(amax, 0, sizeof(uint32_t), s);
+  if (st != cudaSuccess) return st;
+  const size_t vecs = (size_t)M * (K / 8);
+  size_t blocks = (vecs + 255) / 256;
+  const size_t cap = (size_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  quant_tensor_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x),
+                                                          row_w, M, K, n_rows, amax);
+  st = cudaGetLastError();
+  if (st != cudaSuccess) return st;
+  quant_tensor_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x), row_w,
+                                                      M, K, n_rows, amax,
+                                                      reinterpret_cast<uint2 *>(q), row_scales);
   return cudaGetLastError();
 }
 

@@ -8,7 +8,7 @@ import torch
 import oracle as orc
 import workloads as WL
 
-TOL = {WL.BF16: 2e-2, WL.FP8: 5e-2, WL.FP8_CHANNEL: 5e-2}  # max|d| <= tol * max|ref|
+TOL = {WL.BF16: 2e-2, WL.FP8: 5e-2, WL.FP8_CHANNEL: 5e-2, WL.FP8_TENSOR: 5e-2}  # max|d| <= tol * max|ref|
 
 
 def gbmoe():
@@ -30,15 +30,15 @@ def assert_close_rel(got, ref, tol, what=""):
 
 class GpuWeights:
     """The expert weights as the CUDA path takes them: bf16 tensors, or e4m3
-    codes + 128 x 128 block scales (FP8) or one scale per row (FP8_CHANNEL)
-    made by the library's own quantiser."""
+    codes + 128 x 128 block scales (FP8) or one scale per row (FP8_CHANNEL,
+    FP8_TENSOR) made by the library's own quantiser."""
 
     def __init__(self, cfg, w1, w2):
         g = gbmoe()
         self.dtype = cfg.dtype
         if cfg.dtype == WL.BF16:
             self.w1, self.w2, self.w1s, self.w2s = w1, w2, None, None
-        elif cfg.dtype == WL.FP8_CHANNEL:
+        elif cfg.dtype in (WL.FP8_CHANNEL, WL.FP8_TENSOR):  # per-row weight scales
             E, N, K = cfg.E, cfg.N, cfg.K
             self.w1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=w1.device)
             self.w2 = torch.empty((E, K, N), dtype=torch.uint8, device=w1.device)
@@ -68,7 +68,7 @@ def oracle_weights(cfg, w1, w2, experts=None):
         b2 = WL.bf16_bits(w2[e])
         if cfg.dtype == WL.BF16:
             blocks[e] = (b1, b2)
-        elif cfg.dtype == WL.FP8_CHANNEL:  # one scale per row: a group as wide as the row
+        elif cfg.dtype in (WL.FP8_CHANNEL, WL.FP8_TENSOR):  # one scale per weight row
             q1, s1 = orc.quant_fp8_group(b1, group=cfg.K)
             q2, s2 = orc.quant_fp8_group(b2, group=cfg.N)
             blocks[e] = (q1, q2, s1[:, 0], s2[:, 0])

@@ -164,4 +164,4 @@ def test_forward_rejects_bad_arguments(lib):
     assert call(a14=1) == INVALID             # weight on input needs topk 1
     assert call(a6=16) == INVALID             # 16 routed experts, 8 local, no map
     assert call(a15=7) == INVALID             # activation
-    assert call(a16=3) == UNSUPPORTED         # dtype
+    assert call(a16=9) == UNSUPPORTED         # dtype

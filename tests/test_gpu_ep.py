@@ -58,7 +58,8 @@ def test_count_align_with_expert_map_bit_exact():
     assert np.array_equal(inv.cpu().numpy(), ri)
 
 
-@pytest.mark.parametrize("dtype", [WL.BF16, WL.FP8], ids=["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", [WL.BF16, WL.FP8, WL.FP8_CHANNEL, WL.FP8_TENSOR],
+                         ids=["bf16", "fp8", "fp8ch", "fp8t"])
 def test_forward_on_an_expert_parallel_shard(dtype):
     """The shard holding 24 of 64 routed experts: its output is the local
     part of the layer (non-local slots add nothing)."""
@@ -91,7 +92,8 @@ def test_forward_on_an_expert_parallel_shard(dtype):
     assert_close_rel(out.float().cpu().numpy(), ref, TOL[dtype], "shard")
 
 
-@pytest.mark.parametrize("dtype", [WL.BF16, WL.FP8], ids=["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", [WL.BF16, WL.FP8, WL.FP8_CHANNEL, WL.FP8_TENSOR],
+                         ids=["bf16", "fp8", "fp8ch", "fp8t"])
 def test_forward_with_router_weight_on_input(dtype):
     """Top-1, unrenormalised softmax weights p < 1: out = expert(p x)."""
     g = gbmoe()

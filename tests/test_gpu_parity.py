@@ -151,6 +151,45 @@ def test_quant_fp8_rowwise_bit_exact(K, weighted):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
+@pytest.mark.parametrize("weighted,partial", [(False, False), (True, False), (False, True)])
+def test_quant_fp8_tensor_bit_exact(weighted, partial):
+    """One scale for the whole tensor: the scale, every code and every row's
+    copy of the scale bit-exact; with a device row count only the first rows
+    count and the rest are left as they were."""
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(47)
+    M, K = 333, 1024
+    x = (torch.randn((M, K), generator=gen, device=DEV) *
+         torch.logspace(-2, 1, M, device=DEV)[:, None]).to(torch.bfloat16)
+    rw = (torch.rand(M, generator=gen, device=DEV) + 0.05) if weighted else None
+    n = 200 if partial else M
+    n_rows = torch.tensor([n], dtype=torch.int32, device=DEV) if partial else None
+    q = torch.full((M, K), 0xAB, dtype=torch.uint8, device=DEV)
+    s = torch.full((M,), -1.0, dtype=torch.float32, device=DEV)
+    amax = torch.empty(1, dtype=torch.int32, device=DEV)
+    g.moe_quant_fp8_tensor(x, q, s, amax, n_rows=n_rows, row_weights=rw)
+    rq, rs = orc.quant_fp8_tensor(WL.bf16_bits(x[:n]),
+                                  row_weights=None if rw is None else rw[:n].cpu().numpy())
+    assert np.all(s[:n].cpu().numpy() == rs)
+    assert np.array_equal(q[:n].cpu().numpy(), rq)
+    assert torch.all(q[n:] == 0xAB) and torch.all(s[n:] == -1.0)
+
+
+@pytest.mark.parametrize("cfg", [WL.SMALL_FP8T, WL.MID_FP8T], ids=lambda c: c.name)
+def test_forward_parity_fp8_tensor(cfg):
+    """Per-tensor activation scales: every token against the oracle's
+    two-pass layer (the scales of x and H span all tokens)."""
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    out, ids, wts, err = run_forward(cfg, d, gw)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    W = oracle_weights(cfg, d["w1"], d["w2"])
+    ref, rid, rw = oracle_forward(cfg, d, W)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert_close_rel(out.float().cpu().numpy(), ref, TOL[cfg.dtype], cfg.name)
+
+
 def test_quant_fp8_block_bit_exact():
     g = gbmoe()
     gen = torch.Generator(device=DEV).manual_seed(42)

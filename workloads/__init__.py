@@ -28,7 +28,7 @@ from typing import Optional
 import torch
 
 SOFTMAX, SIGMOID = 0, 1
-BF16, FP8, FP8_CHANNEL = 0, 1, 2
+BF16, FP8, FP8_CHANNEL, FP8_TENSOR = 0, 1, 2, 3
 
 
 @dataclasses.dataclass(frozen=True)
@@ -40,7 +40,8 @@ class MoEConfig:
     E: int                 # experts
     topk: int
     dtype: int = BF16      # BF16, FP8 (e4m3, 1x128 activation / 128x128 weight scales) or
-                           # FP8_CHANNEL (e4m3, one scale per token / per weight row)
+                           # FP8_CHANNEL (e4m3, one scale per token / per weight row) or
+                           # FP8_TENSOR (e4m3, one scale per activation tensor / per weight row)
     score_fn: int = SOFTMAX
     n_groups: int = 1
     topk_groups: int = 1
@@ -115,6 +116,20 @@ DSV3_PREFILL_FP8CH = MoEConfig("dsv3_prefill_fp8ch_M8192_K7168_N2048_E256_top8",
                                score_fn=SIGMOID, n_groups=8, topk_groups=4, zipf_bias=True,
                                seed=3)
 
+# e4m3 with one scale per activation tensor: cases small enough for the
+# oracle's two passes over every token, and the DeepSeek-V3-shaped prefill
+# in this format (timed; its parity is covered by the smaller cases, since a
+# per-tensor scale couples every token)
+SMALL_FP8T = MoEConfig("small_fp8t_M256_K512_N256_E8_top2", M=256, K=512, N=256, E=8,
+                       topk=2, dtype=FP8_TENSOR, seed=27)
+MID_FP8T = MoEConfig("mid_fp8t_M384_K768_N384_E16_top4", M=384, K=768, N=384, E=16,
+                     topk=4, dtype=FP8_TENSOR, score_fn=SIGMOID, n_groups=4, topk_groups=2,
+                     zipf_bias=True, seed=28)
+DSV3_PREFILL_FP8T = MoEConfig("dsv3_prefill_fp8t_M8192_K7168_N2048_E256_top8",
+                              M=8192, K=7168, N=2048, E=256, topk=8, dtype=FP8_TENSOR,
+                              score_fn=SIGMOID, n_groups=8, topk_groups=4, zipf_bias=True,
+                              seed=3)
+
 ALL = [TINY, MIXTRAL_PREFILL, DSV3_PREFILL_FP8, DSV3_DECODE, BATCHED_MASKED]
 
 # Small cases of the same kernels for profiler captures: operands larger than
@@ -134,7 +149,7 @@ PROFILE_DECODE = MoEConfig("profile_decode_bf16_M16_K7168_N2048_E32_top4", M=16,
 BY_NAME = {c.name: c for c in ALL + [SMALL_BF16, SMALL_SIGMOID, SMALL_FP8,
                                      SMALL_BATCHED, SMALL_PAIR, SMALL_PAIR_TOP2, SMALL_FP8_K640,
                                      SMALL_FP8CH, SMALL_FP8CH_PAIR, DSV3_PREFILL_FP8CH,
-                                     PROFILE_FP8CH,
+                                     PROFILE_FP8CH, SMALL_FP8T, MID_FP8T, DSV3_PREFILL_FP8T,
                                      SMALL_BATCHED_SHORT, PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE]}
 
 
