@@ -280,6 +280,47 @@ def _dist():
     return ws, rank, local
 
 
+def pipelined_e2e(steps, h2d, compute, d2h):
+    """End-to-end steps as a serving loop runs them: step i's host-to-device
+    copy (h2d(b)), the layer (compute(b)) and the device-to-host copy of its
+    result (d2h(b)) go to three streams, on buffer set b = i % 2, so the
+    copies of one step overlap the layer of its neighbour.  Events order a
+    buffer's reuse: the copy into set b waits until the layer of step i - 2
+    has read it, the layer waits for its inputs and for the copy-out of step
+    i - 2.  Returns the milliseconds from the first copy-in to the last
+    copy-out (events on both streams)."""
+    import torch
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    for st in (s_in, s_run, s_out):
+        st.wait_stream(torch.cuda.current_stream())
+    t0.record(s_in)
+    for i in range(steps):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["done"][b])
+            h2d(b)
+            ev["in"][b].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(ev["in"][b])
+            if i >= 2:
+                s_run.wait_event(ev["out"][b])
+            compute(b)
+            ev["done"][b].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["done"][b])
+            d2h(b)
+            ev["out"][b].record(s_out)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_run)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
 def run_gpu(args, cfg):
     import torch
     world, rank, local = _dist()
@@ -321,31 +362,28 @@ def run_gpu(args, cfg):
     gemm_ms = [a.elapsed_time(b) for a, b in ev]
     assert layer.err.item() == 0, f"device error word {layer.err.item()}"
 
-    # end to end through the public one-call API: pinned host inputs copied in,
-    # the output copied back, every step inside the timed region
+    # end to end through the public one-call API: every step copies its inputs
+    # in from pinned host memory and its output back, inside the timed region
     x_h = layer.x.cpu().pin_memory()
     lg_h = layer.logits.cpu().pin_memory()
-    out_h = torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory()
-    x_d = torch.empty_like(layer.x)
-    lg_d = torch.empty_like(layer.logits)
-    out_d = torch.empty_like(layer.out)
-    for _ in range(max(1, args.warmup)):
-        x_d.copy_(x_h, non_blocking=True)
-        lg_d.copy_(lg_h, non_blocking=True)
-        layer.forward_public(x_d, lg_d, out_d)
-        out_h.copy_(out_d, non_blocking=True)
+    out_h = [torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(layer.x) for _ in range(2)]
+    lg_d = [torch.empty_like(layer.logits) for _ in range(2)]
+    out_d = [torch.empty_like(layer.out) for _ in range(2)]
+
+    def h2d(b):
+        x_d[b].copy_(x_h, non_blocking=True)
+        lg_d[b].copy_(lg_h, non_blocking=True)
+
+    def d2h(b):
+        out_h[b].copy_(out_d[b], non_blocking=True)
+
+    pipelined_e2e(max(2, args.warmup), h2d, lambda b: layer.forward_public(x_d[b], lg_d[b], out_d[b]),
+                  d2h)
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        x_d.copy_(x_h, non_blocking=True)
-        lg_d.copy_(lg_h, non_blocking=True)
-        layer.forward_public(x_d, lg_d, out_d)
-        out_h.copy_(out_d, non_blocking=True)
-    e1.record()
+    e2e_ms = pipelined_e2e(steps, h2d,
+                           lambda b: layer.forward_public(x_d[b], lg_d[b], out_d[b]), d2h)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
     assert layer.err.item() == 0
 
     # max over ranks
@@ -443,7 +481,9 @@ def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
         "roofline": roof,
         "e2e": {"value": None, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(layer.x.numel() * 2 + layer.logits.numel() * 4),
-                "d2h_bytes_per_step": int(layer.out.numel() * 2)},
+                "d2h_bytes_per_step": int(layer.out.numel() * 2),
+                "pipeline": "copy-in, moe_forward and copy-out of consecutive steps on three "
+                            "streams, two buffer sets"},
         "gpu_launches": layer.launches_per_step * steps,
         "clocks": clocks,
     }
@@ -507,23 +547,33 @@ def run_gpu_batched(args, cfg):
         wall1 = time.time()
     ms = t0.elapsed_time(t1)
     assert err.item() == 0, f"device error word {err.item()}"
-    # end to end: pinned host inputs in, the result out, every step
+    # end to end: every step copies x_b and the counts in from pinned host
+    # memory and y_b back, inside the timed region; a second graph over a
+    # second buffer set lets the copies of one step overlap its neighbour
     xh = xb.cpu().pin_memory()
     ch = counts.cpu().pin_memory()
-    yh = torch.empty(yb.shape, dtype=yb.dtype).pin_memory()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(steps, 20))
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(e2e_steps):
-        xb.copy_(xh, non_blocking=True)
-        counts.copy_(ch, non_blocking=True)
-        graph.replay()
-        yh.copy_(yb, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    yh = [torch.empty(yb.shape, dtype=yb.dtype).pin_memory() for _ in range(2)]
+    xb2, counts2, yb2 = torch.empty_like(xb), counts.clone(), torch.empty_like(yb)
+    xb2.copy_(xb)
+    with torch.cuda.stream(s):
+        call(xb2, counts2, yb2)
+    torch.cuda.current_stream().wait_stream(s)
+    graph2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph2):
+        call(xb2, counts2, yb2)
+    sets = [(xb, counts, yb, graph), (xb2, counts2, yb2, graph2)]
+
+    def h2d(b):
+        sets[b][0].copy_(xh, non_blocking=True)
+        sets[b][1].copy_(ch, non_blocking=True)
+
+    def d2h(b):
+        yh[b].copy_(sets[b][2], non_blocking=True)
+
+    e2e_steps = max(2, min(steps, 50))
+    pipelined_e2e(2, h2d, lambda b: sets[b][3].replay(), d2h)
+    e2e_ms = pipelined_e2e(e2e_steps, h2d, lambda b: sets[b][3].replay(), d2h)
+    assert err.item() == 0
     ms, e2e_ms = reduce_max([ms, e2e_ms], pg, device=dev)
     if rank != 0:
         return
@@ -548,12 +598,15 @@ def run_gpu_batched(args, cfg):
                    "parallelism": f"{world} independent replica(s)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "grouped_gemm_kernel, gate/up + down (one graph replay)",
+                     "kernel": ("grouped_gemm_pair_kernel" if T >= 128 else "grouped_gemm_kernel")
+                               + ", gate/up + down (one graph replay)",
                      "peak_source": f"{src} {key} (timed region {timed_s:.2f} s)",
                      "flop_per_launch": flop},
         "e2e": {"value": rows * e2e_steps * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(xb.numel() * 2 + counts.numel() * 4),
-                "d2h_bytes_per_step": int(yb.numel() * 2)},
+                "d2h_bytes_per_step": int(yb.numel() * 2),
+                "pipeline": "copy-in, graph replay and copy-out of consecutive steps on three "
+                            "streams, two buffer sets (two captured graphs)"},
         "gpu_launches": 2 * steps,
         "clocks": clk.summary(wall0, wall1),
     }
