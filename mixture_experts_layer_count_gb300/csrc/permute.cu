@@ -230,7 +230,11 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------------ reduce --
 
 // out[t, :] = bf16(sum_j y_slot[t, j, :]) in slot order, fp32 sums; one thread
-// per 8 output columns.
+// per 8 output columns.  The slots of a token are loaded eight at a time,
+// all loads issued before the first add (a slot of a pair not computed on
+// this shard -- inv < 0 -- is not loaded and adds +0.0, which leaves the sum
+// bit for bit as skipping it would: the sum starts at +0.0 and never becomes
+// -0.0), then added in slot order.
 __global__ void __launch_bounds__(256)
     reduce_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ inv,
                   int M, int topk, int kvec, uint4 *__restrict__ out) {
@@ -242,16 +246,24 @@ __global__ void __launch_bounds__(256)
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < topk; ++j) {
-      const int p = t * topk + j;
-      if (inv && inv[p] < 0) continue;
-      uint4 v = y[(size_t)p * kvec + c];
-      const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+    for (int j0 = 0; j0 < topk; j0 += 8) {
+      uint4 v[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 f = __bfloat1622float2(h[i]);
-        acc[2 * i] += f.x;
-        acc[2 * i + 1] += f.y;
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        const int p = t * topk + j;
+        const bool take = j < topk && (!inv || __ldg(inv + p) >= 0);
+        v[u] = take ? __ldg(y + (size_t)p * kvec + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[u]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          acc[2 * i] += f.x;
+          acc[2 * i + 1] += f.y;
+        }
       }
     }
     uint4 o;

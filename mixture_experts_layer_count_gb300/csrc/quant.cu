@@ -36,36 +36,52 @@ __device__ __forceinline__ float group_scale(float amax) {
   return __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
 }
 
-// one warp per (token, 128-group): 4 values per lane
+// one half-warp per (token, 128-group): 8 values (one 16-byte load) per lane,
+// two groups per warp
 __global__ void __launch_bounds__(256)
-    quant_group_kernel(const uint2 *__restrict__ x, const float *__restrict__ row_w,
-                       int M, int K, uint32_t *__restrict__ q,
+    quant_group_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w,
+                       int M, int K, uint2 *__restrict__ q,
                        float *__restrict__ scales) {
   const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
   const int G = K / 128;
-  const size_t n = (size_t)M * G;
-  for (size_t w = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; w < n;
+  const size_t n = (size_t)M * G;  // groups
+  for (size_t w = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; 2 * w < n;
        w += ((size_t)gridDim.x * blockDim.x) >> 5) {
-    const size_t t = w / G, g = w % G;
-    const size_t base = t * K + g * 128 + lane * 4;  // element index
-    uint2 raw = x[base / 4];
-    float f[4] = {bf16_bits_to_float(raw.x & 0xffffu), bf16_bits_to_float(raw.x >> 16),
-                  bf16_bits_to_float(raw.y & 0xffffu), bf16_bits_to_float(raw.y >> 16)};
-    if (row_w) {  // apply_router_weight_on_input: the fp32 product is quantised
-      const float w = row_w[t];
+    const size_t gi = 2 * w + half;  // this half-warp's group
+    const bool live = gi < n;
+    const size_t t = live ? gi / G : 0, g = live ? gi % G : 0;
+    const size_t vec = (t * K + g * 128) / 8 + hl;  // 16-byte vector index
+    float f[8];
+    float amax = 0.0f;
+    if (live) {
+      const uint4 raw = x[vec];
+      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+      const float w8 = row_w ? row_w[t] : 1.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) f[i] = __fmul_rn(f[i], w);
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = bf16_bits_to_float(u[i] & 0xffffu);
+        f[2 * i + 1] = bf16_bits_to_float(u[i] >> 16);
+      }
+      if (row_w) {  // apply_router_weight_on_input: the fp32 product is quantised
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], w8);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
     }
-    float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
+    for (int off = 8; off > 0; off >>= 1)  // within each half-warp
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float s = group_scale(amax);
-    uint32_t packed = e4m3_of(__fdiv_rn(f[0], s)) | (e4m3_of(__fdiv_rn(f[1], s)) << 8) |
-                      (e4m3_of(__fdiv_rn(f[2], s)) << 16) |
-                      (e4m3_of(__fdiv_rn(f[3], s)) << 24);
-    q[base / 4] = packed;
-    if (lane == 0) scales[t * G + g] = s;
+    if (live) {
+      const float s = group_scale(amax);
+      uint32_t c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = e4m3_of(__fdiv_rn(f[i], s));
+      q[vec] = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                          c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+      if (hl == 0) scales[t * G + g] = s;
+    }
   }
 }
 
@@ -243,12 +259,12 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int K,
                                uint8_t *q, float *scales, cudaStream_t s) {
-  const size_t warps = (size_t)M * (K / 128);
+  const size_t warps = ((size_t)M * (K / 128) + 1) / 2;  // two groups per warp
   size_t blocks = (warps + 7) / 8;
   if (blocks > 65535u * 16u) blocks = 65535u * 16u;
+  if (blocks < 1) blocks = 1;
   quant_group_kernel<<<(unsigned)blocks, 256, 0, s>>>(
-      reinterpret_cast<const uint2 *>(x), row_w, M, K, reinterpret_cast<uint32_t *>(q),
-      scales);
+      reinterpret_cast<const uint4 *>(x), row_w, M, K, reinterpret_cast<uint2 *>(q), scales);
   return cudaGetLastError();
 }
 
