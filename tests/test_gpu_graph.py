@@ -21,7 +21,8 @@ def _lib():
     gbmoe()
 
 
-@pytest.mark.parametrize("cfg", [WL.SMALL_SIGMOID, WL.SMALL_FP8], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [WL.SMALL_SIGMOID, WL.SMALL_FP8, WL.SMALL_PAIR_TOP2,
+                                 WL.SMALL_FP8CH, WL.SMALL_FP8T], ids=lambda c: c.name)
 def test_forward_graph_replay_equals_eager(cfg):
     g = gbmoe()
     d0 = WL.make_inputs(cfg, DEV)
