@@ -230,11 +230,13 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------------ reduce --
 
 // out[t, :] = bf16(sum_j y_slot[t, j, :]) in slot order, fp32 sums; one thread
-// per 8 output columns.  The slots of a token are loaded eight at a time,
-// all loads issued before the first add (a slot of a pair not computed on
-// this shard -- inv < 0 -- is not loaded and adds +0.0, which leaves the sum
-// bit for bit as skipping it would: the sum starts at +0.0 and never becomes
-// -0.0), then added in slot order.
+// per 8 output columns.  The slots of a token are loaded B at a time (B =
+// 2, 4 or 8, the smallest that covers topk, up to 8), all loads issued
+// before the first add (a slot of a pair not computed on this shard -- inv
+// < 0 -- is not loaded and adds +0.0, which leaves the sum bit for bit as
+// skipping it would: the sum starts at +0.0 and never becomes -0.0), then
+// added in slot order.
+template <int B>
 __global__ void __launch_bounds__(256)
     reduce_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ inv,
                   int M, int topk, int kvec, uint4 *__restrict__ out) {
@@ -246,17 +248,17 @@ __global__ void __launch_bounds__(256)
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j0 = 0; j0 < topk; j0 += 8) {
-      uint4 v[8];
+    for (int j0 = 0; j0 < topk; j0 += B) {
+      uint4 v[B];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < B; ++u) {
         const int j = j0 + u;
         const int p = t * topk + j;
         const bool take = j < topk && (!inv || __ldg(inv + p) >= 0);
         v[u] = take ? __ldg(y + (size_t)p * kvec + c) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < B; ++u) {
         const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[u]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -332,9 +334,14 @@ cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
   size_t blocks = (n + 255) / 256;
   if (blocks > (size_t)8 * num_sms) blocks = (size_t)8 * num_sms;
   if (blocks < 1) blocks = 1;
-  reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(
-      reinterpret_cast<const uint4 *>(y_slot), inv, M, topk, kvec,
-      reinterpret_cast<uint4 *>(out));
+  const uint4 *y = reinterpret_cast<const uint4 *>(y_slot);
+  uint4 *o = reinterpret_cast<uint4 *>(out);
+  if (topk <= 2)
+    reduce_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(y, inv, M, topk, kvec, o);
+  else if (topk <= 4)
+    reduce_kernel<4><<<(unsigned)blocks, 256, 0, s>>>(y, inv, M, topk, kvec, o);
+  else
+    reduce_kernel<8><<<(unsigned)blocks, 256, 0, s>>>(y, inv, M, topk, kvec, o);
   return cudaGetLastError();
 }
 
