@@ -332,8 +332,10 @@ gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, const float *row_weights,
   if (st != GBMOE_OK) return st;
   if (M == 0) return GBMOE_OK;
   if (group == K && K != 128)  // one group per row
-    return from_cuda(launch_quant_row(x, row_weights, M, K, q, scales, (cudaStream_t)stream));
-  return from_cuda(launch_quant_group(x, row_weights, M, K, q, scales, (cudaStream_t)stream));
+    return from_cuda(
+        launch_quant_row(x, row_weights, M, K, q, scales, sms, (cudaStream_t)stream));
+  return from_cuda(
+      launch_quant_group(x, row_weights, M, K, q, scales, sms, (cudaStream_t)stream));
 }
 
 gbmoe_status_t moe_quant_fp8_tensor(const uint16_t *x, const float *row_weights,
@@ -593,8 +595,8 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   const float *a_src_s = nullptr;
   if (fp8) {
     ce = fp8t    ? launch_quant_tensor(x, in_w, M, K, nullptr, w.xq, w.xs, w.amax, sms, s)
-         : fp8ch ? launch_quant_row(x, in_w, M, K, w.xq, w.xs, s)
-                 : launch_quant_group(x, in_w, M, K, w.xq, w.xs, s);
+         : fp8ch ? launch_quant_row(x, in_w, M, K, w.xq, w.xs, sms, s)
+                 : launch_quant_group(x, in_w, M, K, w.xq, w.xs, sms, s);
     if (ce != cudaSuccess) return from_cuda(ce);
     a_src = w.xq;
     a_src_s = w.xs;
@@ -612,7 +614,7 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                              w.Hs, w.amax + 1, sms, s);
     if (ce != cudaSuccess) return from_cuda(ce);
   } else if (fp8ch) {
-    ce = launch_quant_row(w.Hb, nullptr, P, N, static_cast<uint8_t *>(w.H), w.Hs, s);
+    ce = launch_quant_row(w.Hb, nullptr, P, N, static_cast<uint8_t *>(w.H), w.Hs, sms, s);
     if (ce != cudaSuccess) return from_cuda(ce);
   }
   st = down_impl(w.H, w.Hs, w.sorted, w.offsets, in_w ? nullptr : wts, M, topk, E, N, K, w2,

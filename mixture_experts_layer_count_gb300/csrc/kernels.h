@@ -41,9 +41,9 @@ cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
 // quant.cu
 // row_w (M) or NULL: rows multiplied by their weight (fp32) before quantising
 cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int K,
-                               uint8_t *q, float *scales, cudaStream_t s);
+                               uint8_t *q, float *scales, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K,
-                             uint8_t *q, float *scales, cudaStream_t s);
+                             uint8_t *q, float *scales, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, int K,
                                 const int32_t *n_rows, uint8_t *q, float *row_scales,
                                 uint32_t *amax, int num_sms, cudaStream_t s);

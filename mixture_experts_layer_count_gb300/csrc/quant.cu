@@ -37,7 +37,42 @@ __device__ __forceinline__ float group_scale(float amax) {
 }
 
 // one half-warp per (token, 128-group): 8 values (one 16-byte load) per lane,
-// two groups per warp
+// two groups per warp; each warp takes two pairs of groups per loop turn
+// with both loads issued first (more bytes in flight per SM)
+__device__ __forceinline__ void quant_group_pair(const uint4 &raw, bool live, const float *row_w,
+                                                 size_t t, size_t g, size_t vec, int hl, int G,
+                                                 uint2 *__restrict__ q, float *__restrict__ scales) {
+  float f[8];
+  float amax = 0.0f;
+  const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_bits_to_float(u[i] & 0xffffu);
+    f[2 * i + 1] = bf16_bits_to_float(u[i] >> 16);
+  }
+  if (row_w) {  // apply_router_weight_on_input: the fp32 product is quantised
+    const float w8 = live ? row_w[t] : 1.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], w8);
+  }
+  if (live) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1)  // within each half-warp
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (live) {
+    const float s = group_scale(amax);
+    uint32_t c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = e4m3_of(__fdiv_rn(f[i], s));
+    q[vec] = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                        c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+    if (hl == 0) scales[t * G + g] = s;
+  }
+}
+
 __global__ void __launch_bounds__(256)
     quant_group_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w,
                        int M, int K, uint2 *__restrict__ q,
@@ -46,42 +81,19 @@ __global__ void __launch_bounds__(256)
   const int half = lane >> 4, hl = lane & 15;
   const int G = K / 128;
   const size_t n = (size_t)M * G;  // groups
-  for (size_t w = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; 2 * w < n;
-       w += ((size_t)gridDim.x * blockDim.x) >> 5) {
-    const size_t gi = 2 * w + half;  // this half-warp's group
-    const bool live = gi < n;
-    const size_t t = live ? gi / G : 0, g = live ? gi % G : 0;
-    const size_t vec = (t * K + g * 128) / 8 + hl;  // 16-byte vector index
-    float f[8];
-    float amax = 0.0f;
-    if (live) {
-      const uint4 raw = x[vec];
-      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
-      const float w8 = row_w ? row_w[t] : 1.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f[2 * i] = bf16_bits_to_float(u[i] & 0xffffu);
-        f[2 * i + 1] = bf16_bits_to_float(u[i] >> 16);
-      }
-      if (row_w) {  // apply_router_weight_on_input: the fp32 product is quantised
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], w8);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    }
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1)  // within each half-warp
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (live) {
-      const float s = group_scale(amax);
-      uint32_t c[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = e4m3_of(__fdiv_rn(f[i], s));
-      q[vec] = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
-                          c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
-      if (hl == 0) scales[t * G + g] = s;
-    }
+  const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
+  for (size_t w = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; 2 * w < n; w += 2 * nw) {
+    const size_t gi0 = 2 * w + half, gi1 = 2 * (w + nw) + half;
+    const bool live0 = gi0 < n, live1 = gi1 < n;
+    const size_t t0 = live0 ? gi0 / G : 0, g0 = live0 ? gi0 % G : 0;
+    const size_t t1 = live1 ? gi1 / G : 0, g1 = live1 ? gi1 % G : 0;
+    const size_t v0 = (t0 * K + g0 * 128) / 8 + hl, v1 = (t1 * K + g1 * 128) / 8 + hl;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 r0 = live0 ? x[v0] : z;
+    const uint4 r1 = live1 ? x[v1] : z;
+    quant_group_pair(r0, live0, row_w, t0, g0, v0, hl, G, q, scales);
+    if (2 * (w + nw) < n)  // uniform over the warp
+      quant_group_pair(r1, live1, row_w, t1, g1, v1, hl, G, q, scales);
   }
 }
 
@@ -258,10 +270,11 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int K,
-                               uint8_t *q, float *scales, cudaStream_t s) {
+                               uint8_t *q, float *scales, int num_sms, cudaStream_t s) {
   const size_t warps = ((size_t)M * (K / 128) + 1) / 2;  // two groups per warp
   size_t blocks = (warps + 7) / 8;
-  if (blocks > 65535u * 16u) blocks = 65535u * 16u;
+  const size_t resident = (size_t)num_sms * 8;  // grid-stride over what is left
+  if (blocks > resident) blocks = resident;
   if (blocks < 1) blocks = 1;
   quant_group_kernel<<<(unsigned)blocks, 256, 0, s>>>(
       reinterpret_cast<const uint4 *>(x), row_w, M, K, reinterpret_cast<uint2 *>(q), scales);
@@ -269,9 +282,11 @@ cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int
 }
 
 cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K,
-                             uint8_t *q, float *scales, cudaStream_t s) {
+                             uint8_t *q, float *scales, int num_sms, cudaStream_t s) {
   size_t blocks = ((size_t)M + 7) / 8;
-  if (blocks > 65535u * 16u) blocks = 65535u * 16u;
+  const size_t resident = (size_t)num_sms * 8;
+  if (blocks > resident) blocks = resident;
+  if (blocks < 1) blocks = 1;
   quant_row_kernel<<<(unsigned)blocks, 256, 0, s>>>(
       reinterpret_cast<const uint4 *>(x), row_w, M, K, reinterpret_cast<uint2 *>(q),
       scales);
