@@ -7,7 +7,9 @@
 // contiguous groups; a group's key is the fp32 sum of the fp32-rounded fp64
 // sigmoids of its two largest v; the topk_groups best groups are kept and the
 // topk best experts among them chosen; weight sigmoid(v_e), renormalised on
-// request.  Equal keys go to the lower index everywhere.
+// request.  Equal keys go to the lower index everywhere.  The group choice
+// is made on fp32 estimates of the keys and confirmed by their margin; the
+// fp64 keys are computed only for a token whose cut is closer than that.
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -26,6 +28,16 @@ __device__ __forceinline__ float key_sigmoid(float v) {
   return (float)(1.0 / (1.0 + exp(-(double)v)));
 }
 
+// an fp32 estimate of key_sigmoid: expf (within its documented few-ulp
+// bound), one add, one IEEE division -- within ~4e-7 of key_sigmoid, so a
+// key (a sum of two scores, rounded) is within ~1.1e-6 of the exact key
+__device__ __forceinline__ float key_sigmoid_fp32(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+// the group selection taken from the fp32 keys stands when the last kept
+// key leads the best dropped one by more than this (several times twice the
+// estimate's error); otherwise the keys are recomputed exactly
+constexpr float kKeyMargin = 8e-6f;
+
 // warp-wide argmax; equal values go to the lower index
 __device__ __forceinline__ void warp_argmax(float &v, int &i) {
 #pragma unroll
@@ -43,6 +55,28 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
   return v;
+}
+
+// the topk_groups best groups by key (lanes < n_groups hold one key each);
+// *margin = last kept key minus best dropped key
+__device__ __forceinline__ uint32_t select_groups(float my_key, int lane, int n_groups,
+                                                  int topk_groups, float *margin) {
+  uint32_t gmask = 0;
+  float last = INFINITY;
+  for (int r = 0; r < topk_groups; ++r) {
+    const bool cand = lane < n_groups && !((gmask >> lane) & 1u);
+    float kv = cand ? my_key : -INFINITY;
+    int ki = cand ? lane : INT_MAX;
+    warp_argmax(kv, ki);
+    if (ki < 32) gmask |= 1u << ki;
+    last = kv;
+  }
+  const bool rest = lane < n_groups && !((gmask >> lane) & 1u);
+  float kv = rest ? my_key : -INFINITY;
+  int ki = rest ? lane : INT_MAX;
+  warp_argmax(kv, ki);
+  *margin = last - kv;
+  return gmask;
 }
 
 // VPL values per lane: expert e = i * 32 + lane lives in lane (e & 31), slot
@@ -73,6 +107,9 @@ __global__ void __launch_bounds__(256)
   // pipe is narrow: a warp-wide fp64 instruction costs the same with one
   // lane active as with 32)
   const int gs = E / (n_groups > 0 ? n_groups : 1);
+  int grp[VPL];  // the group of each value this lane holds (one division each)
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) grp[i] = (i * 32 + lane) / gs;
   uint32_t gmask = kFull;
   if (sigmoid && n_groups > 1 && topk_groups < n_groups) {
     float my_t1 = -INFINITY, my_t2 = -INFINITY;
@@ -81,7 +118,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         int e = i * 32 + lane;
-        if (e < E && e / gs == g) {
+        if (e < E && grp[i] == g) {
           float x = v[i];
           if (x > t1) {
             t2 = t1;
@@ -105,16 +142,18 @@ __global__ void __launch_bounds__(256)
         my_t2 = t2;
       }
     }
+    // fp32 keys first; the fp64 keys (the definition) only when two groups
+    // at the cut are too close for the estimate to order them
     float my_key = -INFINITY;
     if (lane < n_groups)
-      my_key = gs >= 2 ? key_sigmoid(my_t1) + key_sigmoid(my_t2) : key_sigmoid(my_t1);
-    gmask = 0;
-    for (int r = 0; r < topk_groups; ++r) {
-      bool cand = lane < n_groups && !((gmask >> lane) & 1u);
-      float kv = cand ? my_key : -INFINITY;
-      int ki = cand ? lane : INT_MAX;
-      warp_argmax(kv, ki);
-      if (ki < 32) gmask |= 1u << ki;
+      my_key = gs >= 2 ? key_sigmoid_fp32(my_t1) + key_sigmoid_fp32(my_t2)
+                       : key_sigmoid_fp32(my_t1);
+    float margin;
+    gmask = select_groups(my_key, lane, n_groups, topk_groups, &margin);
+    if (!(margin > kKeyMargin)) {  // uniform over the warp (also for NaN)
+      if (lane < n_groups)
+        my_key = gs >= 2 ? key_sigmoid(my_t1) + key_sigmoid(my_t2) : key_sigmoid(my_t1);
+      gmask = select_groups(my_key, lane, n_groups, topk_groups, &margin);
     }
   }
 
@@ -128,7 +167,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       int e = i * 32 + lane;
-      if (e < E && !((taken >> i) & 1u) && ((gmask >> (e / gs)) & 1u)) {
+      if (e < E && !((taken >> i) & 1u) && ((gmask >> grp[i]) & 1u)) {
         if (bi == INT_MAX || v[i] > bv) {  // i ascending: keeps the lower e on ties
           bv = v[i];
           bi = e;
