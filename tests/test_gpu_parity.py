@@ -62,6 +62,24 @@ def test_route_unrenormalised_and_ungrouped():
         np.testing.assert_allclose(w.cpu().numpy(), rw, atol=2e-6, rtol=0)
 
 
+def test_route_grouped_exact_key_ties():
+    """Sigmoid grouped routing with logits on a 0.5 grid: many groups share
+    their two best values, so their keys tie exactly and the group choice
+    falls to the lower group index (keys closer than the fp32 estimate's
+    margin are recomputed exactly).  Keys that differ are far apart on this
+    grid, so the ids must equal the oracle's on every token."""
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(53)
+    for E, n_groups, topk_groups, k in ((64, 8, 4, 6), (256, 8, 4, 8), (32, 4, 2, 3)):
+        lg = (torch.randint(-4, 5, (333, E), generator=gen, device=DEV).float() * 0.5)
+        ids = torch.empty((333, k), dtype=torch.int32, device=DEV)
+        w = torch.empty((333, k), dtype=torch.float32, device=DEV)
+        g.moe_topk_route(lg, None, k, orc.SIGMOID, n_groups, topk_groups, True, ids, w)
+        rid, rw, _ = orc.route(lg.cpu().numpy(), None, k, orc.SIGMOID, n_groups, topk_groups, True)
+        assert np.array_equal(ids.cpu().numpy(), rid), f"E={E}"
+        np.testing.assert_allclose(w.cpu().numpy(), rw, atol=2e-6, rtol=0)
+
+
 # -------------------------------------------------------- count / permute --
 
 @pytest.mark.parametrize("E,M,k,skew", [(8, 64, 2, 0.0), (256, 8192, 8, 1.1),
