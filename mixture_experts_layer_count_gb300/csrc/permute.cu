@@ -187,9 +187,11 @@ __global__ void __launch_bounds__(kAlignThreads)
 // out[i] = x[sorted[i] / topk] for i < *total (one warp per row, 16-byte
 // vectors); FP8 also carries the row's group scales, written group-major
 // (out_s[g * out_s_ld + i]) so that a GEMM tile's scales of one K block are
-// contiguous.  row_w (bf16 rows only, per pair or NULL): the row is scaled by
-// the pair's router weight in fp32 and rounded back to bf16
-// (apply_router_weight_on_input).
+// contiguous.  The scales are copied after the rows by every thread of the
+// grid, one (row, 8 groups) unit at a time with the rows fastest, so that a
+// warp's stores of one group cover 32 consecutive rows.  row_w (bf16 rows
+// only, per pair or NULL): the row is scaled by the pair's router weight in
+// fp32 and rounded back to bf16 (apply_router_weight_on_input).
 __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint4 *__restrict__ x, const float *__restrict__ xs,
                        const float *__restrict__ row_w, int row_vecs, int n_scales,
@@ -221,9 +223,17 @@ __global__ void __launch_bounds__(256)
     } else {
       for (int v = lane; v < row_vecs; v += 32) dst[v] = src[v];
     }
-    if (xs)
-      for (int g = lane; g < n_scales; g += 32)
-        out_s[(size_t)g * out_s_ld + i] = xs[(size_t)t * n_scales + g];
+  }
+  if (xs) {
+    const int n_units = n * ((n_scales + 7) >> 3);
+    for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
+      const int g0 = (u / n) << 3, i = u % n;
+      const float *src = xs + (size_t)(sorted[i] / topk) * n_scales;
+      float *dst = out_s + (size_t)g0 * out_s_ld + i;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        if (g0 + g < n_scales) dst[(size_t)g * out_s_ld] = src[g0 + g];
+    }
   }
 }
 
