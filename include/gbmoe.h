@@ -471,6 +471,19 @@ gbmoe_status_t moe_align_permute_no_ws(const int32_t *topk_ids, int M,
                                        int32_t *err_word,
                                        gbmoe_stream_t stream);
 
+/* Self-test of the failure path of the pipeline waits.  Every wait of the
+ * GEMM kernels on a pipeline barrier is bounded: after its limit it gives
+ * up, ORs GBMOE_ERR_TIMEOUT into err_word and the kernel leaves its loops
+ * instead of hanging.  This call runs that same bounded wait, with a limit of
+ * limit_us microseconds (1 .. 1000000), on a shared-memory barrier that
+ * nothing ever completes: once the stream reaches it, *err_word has the
+ * GBMOE_ERR_TIMEOUT bit set after about limit_us, and the context stays
+ * usable.  One launch of one 32-thread block; err_word is caller-owned
+ * device memory (not cleared here).  GBMOE_INVALID_ARG for a NULL err_word
+ * or a limit outside the range, before any launch. */
+gbmoe_status_t gbmoe_selftest_bounded_wait(int32_t *err_word, int limit_us,
+                                           gbmoe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

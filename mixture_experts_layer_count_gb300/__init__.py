@@ -55,6 +55,7 @@ _SIGS = {
                                 _I, _I, _P, _P, _P, _P, _P, _P, _Z, _I, _P, _P, _P, _P,
                                 _Z, _P, _P, _P, _P, _P]),
     "moe_align_permute_no_ws": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "gbmoe_selftest_bounded_wait": (_I, [_P, _I, _P]),
     "moe_quant_fp8_group": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_quant_fp8_tensor": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
@@ -160,6 +161,13 @@ def moe_align_permute_no_ws(topk_ids, E, counts, offsets, sorted_pair_ids, inv,
     _check("moe_align_permute_no_ws", load().moe_align_permute_no_ws(
         _ptr(topk_ids), M, topk, E, _ptr(counts), _ptr(offsets),
         _ptr(sorted_pair_ids), _ptr(inv), _ptr(err_word), _stream(stream)))
+
+
+def gbmoe_selftest_bounded_wait(err_word, limit_us, stream=None):
+    """Runs the GEMM kernels' bounded pipeline wait on a barrier nothing
+    completes: GBMOE_ERR_TIMEOUT lands in err_word after about limit_us."""
+    _check("gbmoe_selftest_bounded_wait", load().gbmoe_selftest_bounded_wait(
+        _ptr(err_word), int(limit_us), _stream(stream)))
 
 
 def moe_quant_fp8_group(x, q, scales, group=128, stream=None, row_weights=None):

@@ -165,3 +165,10 @@ def test_forward_rejects_bad_arguments(lib):
     assert call(a6=16) == INVALID             # 16 routed experts, 8 local, no map
     assert call(a15=7) == INVALID             # activation
     assert call(a16=9) == UNSUPPORTED         # dtype
+
+
+def test_selftest_rejects_bad_arguments(lib):
+    s = lib.gbmoe_selftest_bounded_wait
+    assert s(None, 1000, None) == INVALID          # no error word
+    assert s(P16, 0, None) == INVALID              # limit below 1 us
+    assert s(P16, 1000001, None) == INVALID        # limit above 1 s
