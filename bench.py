@@ -217,21 +217,30 @@ class Layer:
         self.launches_per_step = (8 + (1 if self.fp8 else 0) + (1 if self.ch else 0)
                                   + (4 if self.tensor else 0))
 
-    def step(self, ev_gemm=None):
+    def step(self, ev_gemm=None, mark=None):
+        """One layer pass as its separate calls.  ev_gemm: a pair of events
+        recorded around the gate/up GEMM; mark(name): called after each
+        stage (the per-stage breakdown records an event there)."""
         g, c = self.g, self.cfg
         M, E, N, K, k = c.M, c.E, c.N, c.K, c.topk
+        mark = mark or (lambda name: None)
         g.moe_topk_route(self.logits, self.bias, k, c.score_fn, c.n_groups, c.topk_groups,
                          c.renorm, self.ids, self.wts)
+        mark("a1_route")
         g.moe_align_permute(self.ids, E, self.counts, self.offsets, self.sorted, self.inv,
                             self.align_ws, self.err)
+        mark("a2_a3_count_align")
         src, src_s = self.x, None
         if self.tensor:
             g.moe_quant_fp8_tensor(self.x, self.xq, self.xs, self.amax[0:1])
             src, src_s = self.xq, self.xs
+            mark("a4_quant_x")
         elif self.fp8:
             g.moe_quant_fp8_group(self.x, self.xq, self.xs, group=K if self.ch else 128)
             src, src_s = self.xq, self.xs
+            mark("a4_quant_x")
         g.moe_permute_rows(src, src_s, self.sorted, self.offsets, k, E, c.dtype, self.A, self.As)
+        mark("a3_gather")
         if ev_gemm is not None:
             ev_gemm[0].record()
         g.moe_grouped_gemm_gate_up_silu(self.A, self.As, self.offsets, M, k, E, N, K, self.w1,
@@ -239,14 +248,19 @@ class Layer:
                                         self.Hs, self.err)
         if ev_gemm is not None:
             ev_gemm[1].record()
+        mark("a5_gate_up")
         if self.tensor:  # rows of pairs computed here: offsets[E]
             g.moe_quant_fp8_tensor(self.Hb, self.H, self.Hs, self.amax[1:2],
                                    n_rows=self.offsets[E:])
+            mark("a4_quant_h")
         elif self.ch:
             g.moe_quant_fp8_group(self.Hb, self.H, self.Hs, group=N)
+            mark("a4_quant_h")
         g.moe_grouped_gemm_down(self.H, self.Hs, self.sorted, self.offsets, self.wts, M, k, E,
                                 N, K, self.w2, self.w2s, c.dtype, self.y, self.err)
+        mark("a6_down")
         g.moe_unpermute_weighted_reduce(self.y, self.inv, M, k, K, self.out)
+        mark("a7_reduce")
 
     def forward_public(self, x, logits, out):
         """The public one-call API on device tensors."""
@@ -254,6 +268,61 @@ class Layer:
         self.g.moe_forward(x, logits, self.bias, c.N, c.E, c.topk, c.score_fn, c.n_groups,
                            c.topk_groups, c.renorm, c.dtype, self.w1, self.w1s, self.w2,
                            self.w2s, out, self.fwd_ws, err_word=self.err)
+
+
+def stage_breakdown(layer, steps):
+    """Mean device milliseconds of each stage of the separate-call layer over
+    `steps` passes (events between consecutive calls on the launching
+    stream; a pass apart from the timed region)."""
+    import torch
+    acc = {}
+    for _ in range(steps):
+        evs = []
+        start = torch.cuda.Event(enable_timing=True)
+        start.record()
+
+        def mark(name, evs=evs):
+            e = torch.cuda.Event(enable_timing=True)
+            e.record()
+            evs.append((name, e))
+        layer.step(mark=mark)
+        torch.cuda.synchronize()
+        prev = start
+        for name, e in evs:
+            acc[name] = acc.get(name, 0.0) + prev.elapsed_time(e)
+            prev = e
+    return {k: v / steps for k, v in acc.items()}
+
+
+def graph_time(layer, steps):
+    """Milliseconds per step of the one-call layer (moe_forward) captured
+    once in a CUDA graph and replayed `steps` times, and of the same call
+    launched eagerly."""
+    import torch
+    out = torch.empty_like(layer.out)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            layer.forward_public(layer.x, layer.logits, out)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward_public(layer.x, layer.logits, out)
+    for _ in range(3):
+        graph.replay()
+    t = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    torch.cuda.synchronize()
+    t[0].record()
+    for _ in range(steps):
+        graph.replay()
+    t[1].record()
+    for _ in range(steps):
+        layer.forward_public(layer.x, layer.logits, out)
+    t[2].record()
+    torch.cuda.synchronize()
+    assert layer.err.item() == 0
+    return t[0].elapsed_time(t[1]) / steps, t[1].elapsed_time(t[2]) / steps
 
 
 def reduce_max(values, dist=None, device="cpu"):
@@ -386,6 +455,11 @@ def run_gpu(args, cfg):
     barrier()
     assert layer.err.item() == 0
 
+    # per-stage breakdown and one-call graph / eager timing (outside the
+    # timed region, on this rank)
+    kernels_ms = stage_breakdown(layer, min(steps, 20))
+    graph_ms, eager_call_ms = graph_time(layer, min(steps, 100))
+
     # max over ranks
     ms, e2e_ms, gemm_avg = reduce_max([ms, e2e_ms, float(np.mean(gemm_ms))], pg, device=dev)
     value = replica_throughput(cfg.M, steps, world, ms)
@@ -394,13 +468,155 @@ def run_gpu(args, cfg):
                  clk.summary(wall0, wall1))
     line["value"] = value
     line["e2e"]["value"] = e2e_value
+    line["kernels_ms"] = kernels_ms
+    line["graph_ms_per_step"] = graph_ms
+    line["one_call_eager_ms_per_step"] = eager_call_ms
     if rank != 0:
         return
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, layer, args.cpu_seconds)
+    if world == 1 and not args.no_extras:
+        del layer
+        torch.cuda.empty_cache()
+        line["per_workload"] = run_extras(args, dev, skip=cfg.name)
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+EXTRA_WORKLOADS = [WL.TINY, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8, WL.BATCHED_MASKED]
+
+
+def run_extras(args, dev, skip=None):
+    """The other workloads of the layer, each timed as the default one is
+    (event-timed steps over resident inputs, clocks sampled inside the timed
+    region) but without the end-to-end and CPU legs, so that they add well
+    under a minute: tiny (launch-bound), DeepSeek-V3 decode (weight-streaming,
+    HBM-bound), DeepSeek-V3 prefill with e4m3 block scales, and the batched
+    masked format replayed from a CUDA graph."""
+    import torch
+    steps = max(20, min(args.steps, 200))
+    warmup = max(3, min(args.warmup, 10))
+    out = {}
+    for cfg in EXTRA_WORKLOADS:
+        if cfg.name == skip:
+            continue
+        t = time.time()
+        if cfg.batched:
+            entry = measure_batched_entry(cfg, dev, steps, warmup)
+        else:
+            entry = measure_standard_entry(cfg, dev, steps, warmup)
+        entry["wall_s"] = time.time() - t
+        out[cfg.name] = entry
+        torch.cuda.empty_cache()
+    return out
+
+
+def measure_standard_entry(cfg, dev, steps, warmup):
+    import torch
+    layer = Layer(cfg, dev)
+    for _ in range(warmup):
+        layer.step()
+    torch.cuda.synchronize()
+    assert layer.err.item() == 0, f"device error word {layer.err.item()}"
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        t0.record()
+        for i in range(steps):
+            layer.step(ev[i])
+        t1.record()
+        torch.cuda.synchronize()
+        wall1 = time.time()
+    ms = t0.elapsed_time(t1)
+    assert layer.err.item() == 0, f"device error word {layer.err.item()}"
+    gemm_avg = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    roof, touched = _roofline(cfg, layer, gemm_avg, ms / 1e3)
+    graph_ms, eager_call_ms = graph_time(layer, min(steps, 100))
+    eb = 1 if cfg.dtype != WL.BF16 else 2
+    wbytes = touched * 3 * cfg.N * cfg.K * eb
+    entry = {"unit": "tokens/s", "value": cfg.M * steps / (ms / 1e3), "steps": steps,
+             "ms_per_step": ms / steps, "graph_ms_per_step": graph_ms,
+             "one_call_eager_ms_per_step": eager_call_ms,
+             "graph_tokens_per_s": cfg.M / (graph_ms / 1e3),
+             "kernel_ms": gemm_avg, "kernels_ms": stage_breakdown(layer, min(steps, 20)),
+             "layer_tflops": 6.0 * cfg.K * cfg.N * cfg.P / (ms / steps / 1e3) / 1e12,
+             "roofline": roof, "clocks": clk.summary(wall0, wall1),
+             "config": {"M": cfg.M, "K": cfg.K, "N": cfg.N, "E": cfg.E, "topk": cfg.topk,
+                        "scales": _scales_desc(cfg),
+                        "l2": ("no flush; working set > L2 (%.2f GB of expert weights per step)"
+                               % (wbytes / 1e9)) if wbytes > L2_BYTES else
+                              ("L2-resident: %.1f MB of expert weights, no flush (a "
+                               "launch-latency case)" % (wbytes / 1e6))},
+             "gpu_launches_per_step": layer.launches_per_step}
+    del layer
+    return entry
+
+
+def measure_batched_entry(cfg, dev, steps, warmup):
+    """One CUDA graph of moe_batched_masked_experts replayed over resident
+    inputs; the roofline covers both grouped GEMM launches."""
+    import torch
+    import mixture_experts_layer_count_gb300 as g
+    g.load()
+    d = WL.make_inputs(cfg, dev)
+    E, T, N, K = cfg.E, cfg.M, cfg.N, cfg.K
+    xb, counts, w1, w2 = d["x_b"], d["counts"], d["w1"], d["w2"]
+    yb = torch.empty_like(xb)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = g.workspace(g.WS_BATCHED, T, E, N, K, 1, WL.BF16, device=dev)
+    rows = int(counts.clamp(0, T).sum().item())
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            g.moe_batched_masked_experts(xb, counts, N, w1, w2, yb, ws, err_word=err)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.moe_batched_masked_experts(xb, counts, N, w1, w2, yb, ws, err_word=err)
+    for _ in range(warmup):
+        graph.replay()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        t0.record()
+        for _ in range(steps):
+            graph.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        wall1 = time.time()
+    ms = t0.elapsed_time(t1)
+    assert err.item() == 0, f"device error word {err.item()}"
+    peaks, src = _peaks()
+    key = "bf16_tflops" if ms / 1e3 < 2.0 else "bf16_tflops_sustained"
+    peak = peaks.get(key, FALLBACK_PEAKS[key])
+    flop = 6.0 * K * N * rows
+    achieved = flop / (ms / steps / 1e3) / 1e12
+    touched = int((counts > 0).sum().item())
+    wbytes = touched * 3 * N * K * 2
+    hbm = (wbytes + 2 * rows * K * 2) / (ms / steps / 1e3) / 1e9
+    return {"unit": "rows/s", "value": rows * steps / (ms / 1e3), "steps": steps,
+            "ms_per_step": ms / steps, "graph_ms_per_step": ms / steps,
+            "kernel_ms": ms / steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "tensor_frac": achieved / peak,
+                         "hbm_frac": hbm / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
+                         "traffic": None, "flop_per_launch": flop,
+                         "kernel": "grouped GEMM gate/up + down (one graph replay)",
+                         "peak_source": f"{src} {key} (timed region {ms / 1e3:.2f} s)"},
+            "clocks": clk.summary(wall0, wall1),
+            "config": {"E": E, "T": T, "K": K, "N": N, "valid_rows": rows,
+                       "experts_with_rows": touched,
+                       "l2": "no flush; working set > L2 (%.2f GB of expert weights per "
+                             "step)" % (wbytes / 1e9)}}
 
 
 def _scales_desc(cfg):
@@ -422,14 +638,17 @@ def _gate_up_kernel_name(cfg):
     return "grouped_gemm_pair_kernel" if pairs else "grouped_gemm_kernel"
 
 
-def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
-    """The JSON result line (value fields filled in by the caller)."""
+def _roofline(cfg, layer, gemm_avg, timed_s):
+    """Roofline of the dominant kernel, the gate/up grouped GEMM (2/3 of the
+    layer's FLOPs), from its mean event-timed duration gemm_avg (ms).
+    Algorithmic bytes per launch: w1 (+ scales) of the experts with rows, the
+    gathered A rows read and H written.  Both the tensor and the HBM
+    fractions are given; `bound` names the larger roofline time."""
     peaks, src = _peaks()
     P = cfg.M * cfg.topk
     fp8 = cfg.dtype != WL.BF16
     ch = cfg.dtype in (WL.FP8_CHANNEL, WL.FP8_TENSOR)
     eb = 1 if fp8 else 2
-    # the dominant kernel: the gate/up grouped GEMM (2/3 of the layer's FLOPs)
     gemm_flop = 4.0 * cfg.K * cfg.N * P
     counts = layer.counts.cpu().numpy()
     touched = int((counts > 0).sum())
@@ -438,26 +657,35 @@ def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
                   + touched * w1_scales
                   + P * cfg.K * eb                            # A rows read
                   + P * cfg.N * (2 if ch else eb))            # H written (bf16 before its quant)
-    tc_time = gemm_flop / (peaks.get("bf16_tflops", 1900.0) * (2 if fp8 else 1) * 1e12)
-    hbm_time = gemm_bytes / (peaks.get("hbm_gbs", 6800.0) * 1e9)
-    timed_s = ms / 1e3
+    key = "bf16_tflops" if timed_s < 2.0 else "bf16_tflops_sustained"
+    tc_peak = peaks.get(key, FALLBACK_PEAKS[key]) * (2.0 if fp8 else 1.0)
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tc_time = gemm_flop / (tc_peak * 1e12)
+    hbm_time = gemm_bytes / (hbm_peak * 1e9)
+    tflops = gemm_flop / (gemm_avg / 1e3) / 1e12
+    gbs = gemm_bytes / (gemm_avg / 1e3) / 1e9
     if tc_time >= hbm_time:
-        key = "bf16_tflops" if timed_s < 2.0 else "bf16_tflops_sustained"
-        peak = peaks.get(key, FALLBACK_PEAKS[key]) * (2.0 if fp8 else 1.0)
-        achieved = gemm_flop / (gemm_avg / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
+        roof = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": tflops / tc_peak,
                 "peak_source": f"{src} {key}" + (" x2 (nominal fp8:bf16 dense ratio)" if fp8 else "")
                                + f" (timed region {timed_s:.2f} s)"}
     else:
-        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-        achieved = gemm_bytes / (gemm_avg / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"{src} hbm_gbs (copy)"}
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gbs / hbm_peak, "peak_source": f"{src} hbm_gbs (copy)"}
     roof.update({"traffic": _kernel_traffic(cfg, "gate_up"),
                  "kernel": _gate_up_kernel_name(cfg) + ", gate/up + SiLU*mul",
                  "kernel_ms": gemm_avg, "flop_per_launch": gemm_flop,
-                 "alg_bytes_per_launch": gemm_bytes, "experts_with_rows": touched})
+                 "alg_bytes_per_launch": gemm_bytes, "experts_with_rows": touched,
+                 "tensor_frac": tflops / tc_peak, "hbm_frac": gbs / hbm_peak})
+    return roof, touched
+
+
+def _line(args, cfg, layer, world, steps, ms, gemm_avg, e2e_ms, clocks):
+    """The JSON result line (value fields filled in by the caller)."""
+    P = cfg.M * cfg.topk
+    fp8 = cfg.dtype != WL.BF16
+    eb = 1 if fp8 else 2
+    roof, touched = _roofline(cfg, layer, gemm_avg, ms / 1e3)
     layer_flop = 6.0 * cfg.K * cfg.N * P
     return {
         "metric": METRIC,
@@ -726,6 +954,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time only the chosen workload (no per_workload object)")
     args = ap.parse_args()
     cfg = WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -36,6 +36,9 @@
  *     GBMOE_ERR_* bit into the caller's device word `err_word` (may be NULL
  *     where noted); read it after synchronising.  No kernel traps.
  *   - M == 0 (or E * T == 0) is a valid no-op and returns GBMOE_OK.
+ *   - `stream` must belong to the device that is current on the calling
+ *     thread (cudaSetDevice); calls that keep per-device state refuse a
+ *     stream of another device with GBMOE_INVALID_ARG.
  */
 #ifndef GBMOE_H
 #define GBMOE_H
@@ -240,9 +243,10 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
                                 gbmoe_stream_t stream);
 
 /* First expert GEMM with the gated activation fused into its epilogue:
- * FusedMoEPermuteExpertsUnpermute.apply ("matmul + act_mul + optionally
- * quant") with activation "silu" (silu_and_mul: the output is half as wide as
- * the GEMM).  For every sorted position i in [offsets[e], offsets[e+1]):
+ * the first GEMM of FusedMoEPermuteExpertsUnpermute.apply followed by its
+ * gated activation (and, for block-scaled e4m3, the requantisation of the
+ * result), with activation "silu" (silu_and_mul: the output is half as wide
+ * as the GEMM).  For every sorted position i in [offsets[e], offsets[e+1]):
  *   g[n] = A[i] . w1[e, n, :],   u[n] = A[i] . w1[e, N + n, :]   (n < N)
  *   H[i, n] = silu(g[n]) * u[n],  silu(z) = z / (1 + exp(-z))
  * Rows [0, N) of w1[e] are the gate, rows [N, 2N) the up projection.
@@ -449,9 +453,12 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
  * library scratch memory -- for instance a plugin interface that hands an
  * operator only its input and output buffers, or a serving engine that has
  * carved up all device memory in advance and has no spare buffer to lend
- * per call.  It computes exactly what moe_align_permute computes (same
- * arguments and results, minus ws / ws_bytes) and allocates nothing: no
- * cudaMalloc, cudaFree or allocating library routine.
+ * per call.  It computes exactly what moe_align_permute computes with
+ * expert_map = NULL and E_global = E (the routed ids are this GPU's expert
+ * ids; there is no expert-map argument, so an id outside [0, E) is skipped
+ * and flagged GBMOE_ERR_BAD_EXPERT_ID, never treated as off-shard), minus
+ * ws / ws_bytes, and allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
  * Its scratch (one int32 histogram of E entries per chunk of 2048 pairs) is a
  * fixed 256 KiB array in device memory that belongs to the library: every
  * GPU that loads the library keeps it until the process exits.  Limit:
@@ -463,7 +470,10 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
  * All calls share the one array and it keeps the last call's contents; every
  * entry a call reads is first written by the same call, so nothing needs
  * clearing.  Two calls that overlap on the GPU (different streams without
- * ordering between them) race on the array and give wrong results. */
+ * ordering between them) race on the array and give wrong results.
+ * `stream` must belong to the current device: the array's address is looked
+ * up for the current device, and a stream of another device is refused with
+ * GBMOE_INVALID_ARG before anything is enqueued. */
 gbmoe_status_t moe_align_permute_no_ws(const int32_t *topk_ids, int M,
                                        int topk, int E, int32_t *counts,
                                        int32_t *offsets,

@@ -17,19 +17,19 @@ namespace {
 // entries per chunk of 2048 pairs, so chunks * E must stay within this.
 constexpr int kNoWsHistEntries = 65536;
 constexpr int kMaxExpertsNoWs = 512;
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevicesNoWs = 64;
 
 __device__ __align__(256) int32_t g_align_hist[kNoWsHistEntries];
 
 // Device address of g_align_hist, looked up once per device.  In host code
 // the symbol name is only a host-side stand-in for the array, not a device
 // address, so the kernels are given the address cudaGetSymbolAddress returns.
-int32_t *g_hist_addr[kMaxDevices] = {};
+int32_t *g_hist_addr[kMaxDevicesNoWs] = {};
 std::mutex g_hist_mu;
 
 gbmoe_status_t hist_address(int32_t **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesNoWs)
     return GBMOE_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_hist_mu);
   if (g_hist_addr[dev] == nullptr) {
@@ -64,6 +64,14 @@ extern "C" gbmoe_status_t moe_align_permute_no_ws(const int32_t *topk_ids, int M
   int32_t *hist = nullptr;
   gbmoe_status_t st = hist_address(&hist);
   if (st != GBMOE_OK) return st;
+  // the address above is the current device's copy of the array: a stream
+  // of another device would have its kernels write through it
+  if (stream != nullptr) {
+    int cur = -1, sdev = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess ||
+        cudaStreamGetDevice((cudaStream_t)stream, &sdev) != cudaSuccess || sdev != cur)
+      return GBMOE_INVALID_ARG;
+  }
   return status_from_cuda(launch_align(topk_ids, P, E, nullptr, E, counts, offsets,
                                        sorted_pair_ids, inv, hist, err_word,
                                        (cudaStream_t)stream));

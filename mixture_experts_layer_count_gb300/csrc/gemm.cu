@@ -7,10 +7,11 @@
 // applies s_a[row] * s_w[column] once (the 1 x 128 / 128 x 128 block-scaled
 // e4m3 GEMMs are in gemm_fp8.cu).
 //
-// FusedMoEPermuteExpertsUnpermute.apply in
-// "vllm/model_executor/layers/fused_moe/modular_kernel.py" is "matmul +
-// act_mul + optionally quant + matmul": the gate/up GEMM with w1 (E, 2N, K)
-// feeds the gated activation (silu_and_mul, output half as wide), the down
+// In "vllm/model_executor/layers/fused_moe/modular_kernel.py"
+// (FusedMoEPermuteExpertsUnpermute, its apply), the experts stage is two
+// GEMMs with the gated activation and an optional requantisation between
+// them: the gate/up GEMM with w1 (E, 2N, K) feeds the gated activation
+// (silu_and_mul, output half as wide), the down
 // GEMM with w2 (E, K, N) gives the per-pair expert output that [Finalize]
 // weights and reduces.  Here:
 //   gate/up: H[i, n] = silu(A[i] . w1[e, n]) * (A[i] . w1[e, N + n])
@@ -34,8 +35,11 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "gemm_common.cuh"
 #include "kernels.h"
+#include "per_device.h"
 
 namespace gbmoe {
 
@@ -334,31 +338,27 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
 
+// looked up once per process (the driver entry point is not per device);
+// std::call_once makes concurrent first calls from several threads safe
 bool resolve_encode() {
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  std::call_once(g_encode_once, [] {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-  }
+  });
   return g_encode != nullptr;
 }
 
 template <int MODE, int ACT, bool F8>
 cudaError_t launch_bf16(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, ACT, F8>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          kSmemBytes);
-    if (st != cudaSuccess) return st;
-    attr_set = true;
-  }
+  static PerDeviceInt smem_set;
+  cudaError_t st = set_smem_once(smem_set, grouped_gemm_kernel<MODE, ACT, F8>, kSmemBytes);
+  if (st != cudaSuccess) return st;
   const bool gate_up = MODE == kGateUpMode;
   const int Kd = gate_up ? a.K : a.N;          // contraction length
   const int b_rows = gate_up ? 2 * a.N : a.K;  // rows of B per expert

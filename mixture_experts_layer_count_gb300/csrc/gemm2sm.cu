@@ -25,6 +25,7 @@
 
 #include "gemm_common.cuh"
 #include "kernels.h"
+#include "per_device.h"
 
 namespace gbmoe {
 
@@ -124,6 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =========================== TMA producer ===========================
     if (lane == 0) {
       int it = 0;
+      int last_round[kStages2];
+#pragma unroll
+      for (int s = 0; s < kStages2; ++s) last_round[s] = -1;
       bool ok = true;
       for (int tile = pair_id; tile < total && ok; tile += n_pairs) {
         int e, mt, nt;
@@ -146,7 +150,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int x = kb * kBK;
           tma_load_2d_pair(sA + s * kAHalf, &tmA, fb, x, a_row);
           tma_load_2d_pair(sB + s * kBHalf, &tmB, fb, x, b_row);
+          last_round[s] = round;
         }
+      }
+      // Copies still in flight land before the CTA can leave.  The odd CTA's
+      // copies complete the even CTA's full barrier, which it cannot wait
+      // on, so both CTAs wait (bounded) until the pair's MMA has released
+      // each stage they loaded last: the MMA issuer waited for those bytes
+      // first.  The even CTA also waits for its full barriers, which count
+      // the bytes of both CTAs; it stays resident (final cluster barrier)
+      // until it has.  After a timeout these waits end within their own
+      // limit, by which time copies issued before the stall have landed.
+#pragma unroll
+      for (int s = 0; s < kStages2; ++s) {
+        if (last_round[s] < 0) continue;
+        if (leader) mbar_wait(full_bar(s), last_round[s] & 1, 100000000ull);
+        mbar_wait(empty_bar(s), last_round[s] & 1, 100000000ull);
       }
     }
   } else if (warp == 1) {
@@ -273,14 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MODE, int ACT>
 cudaError_t launch_pair(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE, ACT>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          kSmemBytes);
-    if (st != cudaSuccess) return st;
-    attr_set = true;
-  }
+  static PerDeviceInt smem_set;
+  cudaError_t st = set_smem_once(smem_set, grouped_gemm_pair_kernel<MODE, ACT>, kSmemBytes);
+  if (st != cudaSuccess) return st;
   const bool gate_up = MODE == kGateUpMode;
   const int Kd = gate_up ? a.K : a.N;
   const int b_rows = gate_up ? 2 * a.N : a.K;
@@ -317,16 +331,21 @@ cudaError_t launch_pair(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   cfg.numAttrs = 1;
   // persistent: as many pairs as can be resident at once (an SM left without
   // a partner in its GPC hosts none)
-  static int resident_pairs = 0;
-  if (resident_pairs == 0) {
+  static PerDeviceInt resident;
+  int resident_pairs = 0;
+  st = resident.get(&resident_pairs, [&](int *v) {
     cfg.gridDim = dim3(2 * (num_sms / 2));
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<MODE, ACT>, &cfg) !=
             cudaSuccess ||
-        n < 1)
+        n < 1) {
+      cudaGetLastError();  // the query's error, if any, is not a launch error
       n = num_sms / 2;
-    resident_pairs = n;
-  }
+    }
+    *v = n;
+    return cudaSuccess;
+  });
+  if (st != cudaSuccess) return st;
   const long long mtiles = a.offsets ? (a.a_rows + kPairBM - 1) / kPairBM + a.E
                                      : (long long)a.E * ((a.T + kPairBM - 1) / kPairBM);
   const long long tiles = mtiles * p.n_tiles;

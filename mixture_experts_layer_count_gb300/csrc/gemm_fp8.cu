@@ -26,6 +26,7 @@
 
 #include "gemm_common.cuh"
 #include "kernels.h"
+#include "per_device.h"
 
 namespace gbmoe {
 
@@ -402,14 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MODE, int ACT>
 cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t st = cudaFuncSetAttribute(grouped_gemm_fp8_kernel<MODE, ACT>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          kSmemBytes);
-    if (st != cudaSuccess) return st;
-    attr_set = true;
-  }
+  static PerDeviceInt smem_set;
+  cudaError_t st = set_smem_once(smem_set, grouped_gemm_fp8_kernel<MODE, ACT>, kSmemBytes);
+  if (st != cudaSuccess) return st;
   const bool gate_up = MODE == kGateUpMode;
   const int Kd = gate_up ? a.K : a.N;
   const int b_rows = gate_up ? 2 * a.N : a.K;

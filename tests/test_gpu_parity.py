@@ -8,7 +8,8 @@ import torch
 import oracle as orc
 import workloads as WL
 from gpu_common import (TOL, GpuWeights, assert_close_rel, check_ids, gbmoe,
-                        oracle_forward, oracle_weights, run_forward)
+                        oracle_forward, oracle_pair_rows, oracle_weights, run_forward,
+                        run_stages)
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +43,8 @@ def test_route_parity(cfg):
                                 cfg.topk, cfg.score_fn, cfg.n_groups, cfg.topk_groups,
                                 cfg.renorm)
     gid = ids.cpu().numpy()
-    diff = check_ids(gid, rid, margin, cfg.name)
+    diff = check_ids(gid, rid, margin, cfg.name, cfg, d["logits"].cpu().numpy(),
+                     None if d["bias"] is None else d["bias"].cpu().numpy())
     same = np.setdiff1d(np.arange(cfg.M), diff)
     np.testing.assert_allclose(w.cpu().numpy()[same], rw[same], atol=2e-6, rtol=0)
 
@@ -387,37 +389,84 @@ def test_one_expert_takes_every_token_matches_torch_matmul(M):
     assert_close_rel(out.float().cpu().numpy(), ref.cpu().numpy(), 2e-2, "dense")
 
 
-# ------------------------------------------------- full-size, sampled ------
+# ------------------------------------------------------------- full-size ---
 
 FULL_CFGS = [WL.MIXTRAL_PREFILL, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8, WL.DSV3_PREFILL_FP8CH]
+N_SAMPLE = 512
 
 
 @pytest.mark.parametrize("cfg", FULL_CFGS, ids=lambda c: c.name)
-def test_forward_parity_full_size_sampled(cfg):
-    """The bench's workloads at full size: routing, counts and permutation of
-    every token against the oracle; output values on a seeded sample of
-    tokens, plus tokens of the most loaded expert (tokens are independent, so
-    a sample is computed exactly as in the full run)."""
+def test_forward_parity_full_size(cfg):
+    """The bench's workloads at full size, checked as follows (tokens are
+    independent, so every checked row is computed exactly as in the full
+    run):
+      * routing: the ids of every token bit for bit (a near-tie token must be
+        one of the valid choices), the weights of the others;
+      * counts, offsets, sorted pair ids and inv of the workload's own routing
+        (the oracle's ids, aligned on the GPU) bit for bit;
+      * the weighted expert row of every pair routed to the two most loaded
+        experts (the heavy experts' tiles), against the oracle;
+      * the output of a seeded sample of 512 tokens (every token when there
+        are fewer), against the oracle's layer;
+      * the one-call layer bit for bit equal, on every token, to the same
+        layer run as its separate calls on the same routing."""
+    g = gbmoe()
     d = WL.make_inputs(cfg, DEV)
     gw = GpuWeights(cfg, d["w1"], d["w2"])
     out, ids, wts, err = run_forward(cfg, d, gw)
     torch.cuda.synchronize()
     assert err.item() == 0
-    rid, rw, margin = orc.route(d["logits"].cpu().numpy(),
-                                None if d["bias"] is None else d["bias"].cpu().numpy(),
-                                cfg.topk, cfg.score_fn, cfg.n_groups, cfg.topk_groups,
-                                cfg.renorm)
-    diff = check_ids(ids.cpu().numpy(), rid, margin, cfg.name)
+    lg = d["logits"].cpu().numpy()
+    bias = None if d["bias"] is None else d["bias"].cpu().numpy()
+    rid, rw, margin = orc.route(lg, bias, cfg.topk, cfg.score_fn, cfg.n_groups,
+                                cfg.topk_groups, cfg.renorm)
+    gid = ids.cpu().numpy()
+    diff = check_ids(gid, rid, margin, cfg.name, cfg, lg, bias)
+    same = np.setdiff1d(np.arange(cfg.M), diff)
+    np.testing.assert_allclose(wts.cpu().numpy()[same], rw[same], atol=2e-6, rtol=0)
+
+    # the permutation of the workload's routing, every pair
+    E, P = cfg.E, cfg.P
+    counts = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    srt = torch.full((P,), -5, dtype=torch.int32, device=DEV)
+    inv = torch.empty(P, dtype=torch.int32, device=DEV)
+    aerr = torch.zeros(1, dtype=torch.int32, device=DEV)
+    g.moe_align_permute(torch.from_numpy(rid).to(DEV), E, counts, offsets, srt, inv,
+                        g.workspace(g.WS_ALIGN, cfg.M, E, 0, 0, cfg.topk, 0), aerr)
+    rc, bad = orc.count(rid, E)
+    ro, rs, ri = orc.align(rid, E)
+    torch.cuda.synchronize()
+    assert bad == 0 and aerr.item() == 0 and rc.sum() == P
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(srt.cpu().numpy(), rs)
+    assert np.array_equal(inv.cpu().numpy(), ri)
+    del counts, offsets, srt, inv
+
+    # the layer as separate calls on the path's own routing
+    st = run_stages(cfg, d, gw, ids, wts)
+    torch.cuda.synchronize()
+    assert st["err"].item() == 0
+    assert torch.equal(out.view(torch.int16), st["out"].view(torch.int16)), \
+        "one-call layer differs from its separate calls"
+
+    # every pair of the two most loaded experts (tokens with a near-tie route
+    # left out: their experts differ from the oracle's)
+    top2 = np.argsort(-rc, kind="stable")[:2]
+    pairs = np.concatenate([rs[ro[e]:ro[e + 1]] for e in top2])
+    pairs = pairs[~np.isin(pairs // cfg.topk, diff)]
+    yref = oracle_pair_rows(cfg, d, d["w1"], d["w2"], rid, pairs) * rw.ravel()[pairs][:, None]
+    ygot = st["y_slot"].view(P, cfg.K)[torch.from_numpy(pairs).to(DEV)].float().cpu().numpy()
+    assert_close_rel(ygot, yref, TOL[cfg.dtype], f"{cfg.name}: pairs of experts {top2}")
+    del st
+
+    # a seeded sample of tokens through the whole layer
     rng = np.random.default_rng(1)
-    n_sample = 24 if cfg.M > 64 else 16
-    counts = np.bincount(rid.ravel(), minlength=cfg.E)
-    top = int(np.argmax(counts))
-    on_top = np.flatnonzero((rid == top).any(1))
-    tokens = np.unique(np.concatenate([rng.choice(cfg.M, n_sample, replace=False),
-                                       on_top[:4]]))
+    tokens = (np.arange(cfg.M) if cfg.M <= N_SAMPLE
+              else np.sort(rng.choice(cfg.M, N_SAMPLE, replace=False)))
     tokens = np.setdiff1d(tokens, diff)
-    experts = np.unique(rid[tokens])
-    W = oracle_weights(cfg, d["w1"], d["w2"], experts)
+    W = oracle_weights(cfg, d["w1"], d["w2"], np.unique(rid[tokens]))
     ref, rid_s, _ = oracle_forward(cfg, d, W, tokens=tokens)
     assert np.array_equal(rid_s, rid[tokens])
     assert_close_rel(out[torch.from_numpy(tokens).to(DEV)].float().cpu().numpy(), ref,

@@ -21,7 +21,9 @@ def g():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import mixture_experts_layer_count_gb300 as lib
+    import oracle
     lib.load()
+    oracle.build()
     return lib
 
 
@@ -52,6 +54,15 @@ def test_no_ws_matches_workspace_version_on_two_calls_in_a_row(g):
         assert err.item() == 0
         for a, b, name in zip(ref, got, ("counts", "offsets", "sorted", "inv")):
             assert torch.equal(a, b), f"{name} differs (M={M}, E={E})"
+        # and against the oracle's stable counting sort
+        import oracle
+        rc, bad = oracle.count(ids.cpu().numpy(), E)
+        ro, rs, ri = oracle.align(ids.cpu().numpy(), E)
+        assert bad == 0
+        assert np.array_equal(got[0].cpu().numpy(), rc)
+        assert np.array_equal(got[1].cpu().numpy(), ro)
+        assert np.array_equal(got[2].cpu().numpy(), rs)
+        assert np.array_equal(got[3].cpu().numpy(), ri)
 
 
 def test_no_ws_refuses_sizes_beyond_its_fixed_array(g):
