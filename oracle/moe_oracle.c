@@ -472,8 +472,13 @@ void orc_unpermute_reduce(const double *yperm, const int32_t *inv,
 void orc_quant_fp8_group_w(const uint16_t *x, const float *row_w, int M,
                            int K, int group, uint8_t *q, float *scales)
 {
-    int t, g, k, G = K / group;
+    int t, G = K / group;
+    /* rows are independent: each one is quantised by one thread */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (t = 0; t < M; ++t) {
+        int g, k;
         const float rw = row_w ? row_w[t] : 1.0f;
         for (g = 0; g < G; ++g) {
             const uint16_t *xg = x + (size_t)t * K + (size_t)g * group;
