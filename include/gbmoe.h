@@ -89,7 +89,10 @@ enum {
     GBMOE_WS_ALIGN = 0,    /* moe_align_permute                       */
     GBMOE_WS_BATCHED = 2,  /* moe_batched_masked_experts              */
     GBMOE_WS_FORWARD = 3,  /* moe_forward (the whole Standard layer)  */
-    GBMOE_WS_SHARED = 4    /* moe_shared_expert_forward (N = shared intermediate size) */
+    GBMOE_WS_SHARED = 4,   /* moe_shared_expert_forward (N = shared intermediate size) */
+    GBMOE_WS_DOWN_REDUCE = 5, /* moe_grouped_gemm_down_reduce          */
+    GBMOE_WS_EP_DISPATCH = 6  /* moe_ep_dispatch: M_or_T = M tokens per shard, E = all
+                                 routed experts, N = the number of shards G  */
 };
 
 /* bits OR-ed into *err_word by the kernels */
@@ -320,6 +323,33 @@ gbmoe_status_t moe_unpermute_weighted_reduce(const uint16_t *y_slot,
                                              int topk, int K, uint16_t *out,
                                              gbmoe_stream_t stream);
 
+/* The second expert GEMM and [Finalize] in one call: what
+ * moe_grouped_gemm_down followed by moe_unpermute_weighted_reduce (with the
+ * same inv) computes, bit for bit -- y_slot (M, topk, K) holds the weighted
+ * slot rows and out (M, K) their ordered fp32 sum rounded once to bf16 --
+ * with the reduce done inside the GEMM's epilogue ("experts own the weight
+ * application", FusedMoEPermuteExpertsUnpermute.finalize_weight_and_reduce_impl,
+ * and TopKWeightAndReduce.apply of the modular kernel): for each token and
+ * block of output columns, the thread that stores the token's last computed
+ * slot row sums the token's rows in slot order j = 0 .. topk-1.  No thread
+ * waits for another and no floating-point atomic is used, so the result is
+ * deterministic.  A token with no computed slot (inv < 0 for every slot,
+ * e.g. all its experts on other shards) gets a zero row.  Block-scaled e4m3
+ * (GBMOE_FP8_E4M3) runs the reduce as a separate pass after the GEMM, with
+ * the same result.
+ * inv (M*topk) is the inverse map of moe_align_permute (-1: pair not computed
+ * here); other arguments as in moe_grouped_gemm_down.
+ * ws: moe_workspace_size(GBMOE_WS_DOWN_REDUCE, M, E, N, K, topk, dtype)
+ * bytes (per-token arrival counters, cleared by the call itself), 16-byte
+ * aligned.  Launches: a counter-clearing kernel and the GEMM (or the GEMM and
+ * the reduce for block-scaled e4m3).  err_word may be NULL. */
+gbmoe_status_t moe_grouped_gemm_down_reduce(
+    const void *H, const float *H_scales, const int32_t *sorted_pair_ids,
+    const int32_t *inv, const int32_t *offsets, const float *topk_weights, int M,
+    int topk, int E, int N, int K, const void *w2, const float *w2_scales, int dtype,
+    uint16_t *y_slot, uint16_t *out, void *ws, size_t ws_bytes, int32_t *err_word,
+    gbmoe_stream_t stream);
+
 /* Both expert GEMMs in the BatchedExperts format (E, T, K), masked by the
  * device-resident expert_num_tokens as the masked grouped GEMM of the
  * worst-tokens mode reads it: for every expert e and row r < c_e,
@@ -447,6 +477,59 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
                                   gbmoe_stream_t aux_stream,
                                   struct CUevent_st *ev_input_ready,
                                   struct CUevent_st *ev_output_ready);
+
+/* Expert-parallel dispatch in the worst-tokens mode of "EP: CUDA-graph-safe
+ * HT internode dispatch+combine (worst-tokens mode)" (uccl pull request 7 and
+ * the vLLM commit message under it), for G shards whose buffers are in this
+ * GPU's memory.  Shard r (r < G) holds tokens x[r] (M, K) bf16, of which the
+ * first num_tokens[r] (a DEVICE int32, clamped to [0, M]) are valid, with
+ * their routed expert ids topk_ids[r] (M, topk) int32 in [0, E).  Shard g
+ * owns the E / G experts [g*E/G, (g+1)*E/G).  Each valid (token, slot) pair
+ * goes to the receive block of its expert:
+ *   recv_x (E, worst_tokens, K) bf16: recv_x[e, pos] = x[r, t] for the pos-th
+ *     pair routed to e, pairs taken in ascending order of (r, t, slot);
+ *     the E/G experts of shard g are rows [g*E/G, (g+1)*E/G): that shard's
+ *     static worst-case receive buffer, in the BatchedExperts layout;
+ *   recv_counts (E) int32, device: rows received per expert (the per-expert
+ *     count tensor the masked grouped GEMM reads inside a graph: pass
+ *     recv_x + g*(E/G)*worst_tokens*K and recv_counts + g*(E/G) to
+ *     moe_batched_masked_experts for shard g);
+ *   recv_pos (G, M, topk) int32: pos of each pair, -1 for pairs of padded
+ *     tokens and of invalid ids (those are skipped; invalid ids also set
+ *     GBMOE_ERR_BAD_EXPERT_ID).
+ * worst_tokens is the static per-expert capacity, G * M covers every case
+ * (the pages size it as the padded step tokens times the number of
+ * dispatchers); pairs beyond it are dropped (pos -1), the count clamped and
+ * GBMOE_ERR_COUNT_RANGE set.  Rows of recv_x at and beyond a count are not
+ * written.  No count is read on the host and no loop runs over the padded
+ * shapes: the whole call is capturable.
+ * ws: moe_workspace_size(GBMOE_WS_EP_DISPATCH, M, E, G, K, topk, 0) bytes,
+ * 16-byte aligned.  K a multiple of 8, E a multiple of G; x and recv_x
+ * 16-byte aligned.  err_word may be NULL.  On several GPUs each shard's
+ * receive block would live on its own GPU and the row copies would be
+ * peer stores; this call is the single-GPU form. */
+gbmoe_status_t moe_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
+                               const int32_t *topk_ids, int G, int M, int K, int E,
+                               int topk, int worst_tokens, uint16_t *recv_x,
+                               int32_t *recv_counts, int32_t *recv_pos, void *ws,
+                               size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream);
+
+/* Expert-parallel combine of the same mode: for every shard r and valid token
+ * t < num_tokens[r] (device),
+ *   out[r, t, :] = bf16( sum_{j = 0 .. topk-1} topk_weights[r, t, j] *
+ *                        recv_y[e_j, recv_pos[r, t, j], :] )
+ * with e_j = topk_ids[r, t, j], in fp32, in slot order, skipping pairs with
+ * recv_pos < 0 (TopKWeightAndReduce.apply of the modular kernel: weights
+ * applied, then the reduce).  recv_y (E, worst_tokens, K) bf16 holds the
+ * experts' unweighted outputs at the rows dispatch gave them (the y_b of
+ * moe_batched_masked_experts).  Rows of out of padded tokens are not
+ * written; the token loop is bounded by num_tokens on the device, never by M.
+ * out (G, M, K) bf16, 16-byte aligned. */
+gbmoe_status_t moe_ep_combine(const uint16_t *recv_y, const int32_t *topk_ids,
+                              const int32_t *recv_pos, const float *topk_weights,
+                              const int32_t *num_tokens, int G, int M, int K, int E,
+                              int topk, int worst_tokens, uint16_t *out,
+                              gbmoe_stream_t stream);
 
 /* moe_align_permute without a workspace argument.  The pages have no
  * counterpart of this call: it exists for callers that cannot give the

@@ -20,7 +20,7 @@ from . import build as _build
 BF16, FP8_E4M3, FP8_E4M3_CHANNEL, FP8_E4M3_TENSOR = 0, 1, 2, 3  # dtype codes of include/gbmoe.h
 SOFTMAX, SIGMOID = 0, 1
 ACT_SILU, ACT_GELU = 0, 1
-WS_ALIGN, WS_BATCHED, WS_FORWARD, WS_SHARED = 0, 2, 3, 4
+WS_ALIGN, WS_BATCHED, WS_FORWARD, WS_SHARED, WS_DOWN_REDUCE, WS_EP_DISPATCH = 0, 2, 3, 4, 5, 6
 ERR_BAD_EXPERT_ID, ERR_COUNT_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype or device",
@@ -66,7 +66,11 @@ _SIGS = {
                                            _I, _P, _P, _P, _P]),
     "moe_grouped_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                                    _I, _P, _P, _P]),
+    "moe_grouped_gemm_down_reduce": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
+                                          _I, _P, _P, _P, _Z, _P, _P]),
     "moe_unpermute_weighted_reduce": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "moe_ep_dispatch": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P, _P]),
+    "moe_ep_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_batched_masked_experts": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                         _I, _I, _P, _P, _Z, _P, _P]),
     "moe_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
@@ -229,6 +233,38 @@ def moe_grouped_gemm_down(H, H_scales, sorted_pair_ids, offsets, topk_weights,
         _ptr(H), _ptr(H_scales), _ptr(sorted_pair_ids), _ptr(offsets),
         _ptr(topk_weights), M, topk, E, N, K, _ptr(w2), _ptr(w2_scales), dtype,
         _ptr(y_slot), _ptr(err_word), _stream(stream)))
+
+
+def moe_grouped_gemm_down_reduce(H, H_scales, sorted_pair_ids, inv, offsets, topk_weights,
+                                 M, topk, E, N, K, w2, w2_scales, dtype, y_slot, out, ws,
+                                 err_word=None, stream=None):
+    _check("moe_grouped_gemm_down_reduce", load().moe_grouped_gemm_down_reduce(
+        _ptr(H), _ptr(H_scales), _ptr(sorted_pair_ids), _ptr(inv), _ptr(offsets),
+        _ptr(topk_weights), M, topk, E, N, K, _ptr(w2), _ptr(w2_scales), dtype,
+        _ptr(y_slot), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
+        _stream(stream)))
+
+
+def moe_ep_dispatch(x, num_tokens, topk_ids, E, worst_tokens, recv_x, recv_counts, recv_pos,
+                    ws, err_word=None, stream=None):
+    """x (G, M, K) bf16, num_tokens (G) int32, topk_ids (G, M, topk) int32;
+    recv_x (E, worst_tokens, K), recv_counts (E), recv_pos (G, M, topk)."""
+    G, M, K = x.shape
+    topk = topk_ids.shape[-1]
+    _check("moe_ep_dispatch", load().moe_ep_dispatch(
+        _ptr(x), _ptr(num_tokens), _ptr(topk_ids), G, M, K, E, topk, worst_tokens,
+        _ptr(recv_x), _ptr(recv_counts), _ptr(recv_pos), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(err_word), _stream(stream)))
+
+
+def moe_ep_combine(recv_y, topk_ids, recv_pos, topk_weights, num_tokens, out, stream=None):
+    """recv_y (E, worst_tokens, K); topk_ids / recv_pos / topk_weights
+    (G, M, topk); num_tokens (G); out (G, M, K)."""
+    E, worst, K = recv_y.shape
+    G, M, topk = topk_ids.shape
+    _check("moe_ep_combine", load().moe_ep_combine(
+        _ptr(recv_y), _ptr(topk_ids), _ptr(recv_pos), _ptr(topk_weights), _ptr(num_tokens),
+        G, M, K, E, topk, worst, _ptr(out), _stream(stream)))
 
 
 def moe_unpermute_weighted_reduce(y_slot, inv, M, topk, K, out, stream=None):

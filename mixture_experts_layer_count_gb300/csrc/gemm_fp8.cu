@@ -5,12 +5,14 @@
 //
 // Both scales change every 128 elements of K, so a K block's products cannot
 // be accumulated across blocks inside the tensor core.  Each K block (4 MMAs
-// of K 32) is accumulated alone into one of two 256-column TMEM buffers; 16
+// of K 32) is accumulated alone into one of two 256-column TMEM buffers; 8
 // epilogue warps then add it into fp32 registers,
 //     acc += (s_a[row, kb] * s_w[blk, kb]) * partial,
 // while the tensor core fills the other buffer.  Each epilogue thread owns one
-// row and 64 columns (4 lane quarters x 4 column quarters cover the 128 x 256
-// tile), so the promotion is 32 packed FFMA2 per thread per K block.  The
+// row and 128 columns (4 lane quarters x 2 column halves cover the 128 x 256
+// tile: for gate/up the gate and up columns of 64 outputs), so the promotion
+// is 64 packed FFMA2 per thread per K block, in 16-column TMEM loads; at 320
+// threads a thread has 168 registers, enough for its 128 accumulators.  The
 // per-row scales of a K block travel with the operand tiles: the producer
 // loads them by TMA from the group-major scale array (one contiguous run of
 // rows per K block) into the stage's shared memory; the weight-block scales
@@ -18,8 +20,11 @@
 //
 // gate/up ends with h = silu(gate) * up and the e4m3 requantisation of h in
 // 128-wide groups (one scale per row and n-tile; the row maximum is
-// exchanged between the four warps holding that row); down ends with the
-// router weight and bf16 stores into the (token, slot) rows.
+// exchanged between the two warps holding that row); down ends with the
+// router weight and bf16 stores into the (token, slot) rows (the ordered
+// top-k reduce is a pass of its own after this kernel: added to this
+// epilogue it stalled the per-K-block pipeline, 1.8 -> 4.3 ms on the
+// DeepSeek-V3-shaped prefill).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -34,9 +39,9 @@ namespace {
 
 using namespace gemm;
 
-constexpr int kEpiWarps = 16;
+constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 64 + kEpiThreads;      // 576
+constexpr int kThreads = 64 + kEpiThreads;      // 320
 constexpr int kBK = kBKB;                       // e4m3 elements per stage row
 constexpr int kMmaPerStage = kBK / 32;          // kind::f8f6f4 has K = 32
 constexpr uint32_t kIdesc = umma_idesc(kBM, kBN, kFmtE4M3);
@@ -86,17 +91,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
-// acc[0..16) += f * v[0..16) with packed fp32x2 FMAs
-__device__ __forceinline__ void promote16(float *acc, const uint32_t (&v)[16], float f) {
+
+// acc[0..8) += f * v[0..16) (as 8 float2) with packed fp32x2 FMAs
+__device__ __forceinline__ void promote8(float2 *acc, const uint32_t (&v)[16], float f) {
   const float2 f2 = make_float2(f, f);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float2 a = make_float2(acc[2 * j], acc[2 * j + 1]);
-    const float2 x = make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-    a = __ffma2_rn(x, f2, a);
-    acc[2 * j] = a.x;
-    acc[2 * j + 1] = a.y;
-  }
+  for (int j = 0; j < 8; ++j)
+    acc[j] = __ffma2_rn(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), f2, acc[j]);
 }
 
 template <int MODE, int ACT>
@@ -249,10 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================= epilogue =============================
-    const int ew = warp - 2;           // 0..15
+    const int ew = warp - 2;           // 0..7
     const int q = warp & 3;            // TMEM lane quarter of this warp
-    const int cq = ew >> 2;            // column quarter of this warp
-    const int etid = ew * 32 + lane;   // 0..511
+    const int hh = ew >> 2;            // column half of this warp
+    const int etid = ew * 32 + lane;   // 0..255
     const int row_in_tile = q * 32 + lane;
     const uint32_t t_lane = (uint32_t)(q * 32) << 16;
     const int b_blk_rows = p.b_rows / 128;
@@ -282,13 +283,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         set_err(p.err, GBMOE_ERR_TIMEOUT);
         break;
       }
-      const float *bs_g = bsc;                     // gate / this quarter's block (down)
+      const float *bs_g = bsc;                     // gate
       const float *bs_u = bsc + kMaxKB;            // up
-      const float *bs_d = bsc + (cq >> 1) * kMaxKB;
+      const float *bs_d = bsc + hh * kMaxKB;       // down: this half's weight block
 
-      float acc[64];
+      // gate/up: [0, 32) the gate of columns [64 hh, 64 hh + 64), [32, 64)
+      // their up; down: columns [128 hh, 128 hh + 128)
+      float2 acc[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const int buf = it & 1, use = it >> 1;
@@ -308,33 +311,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t tbuf = tmem_base + t_lane + buf * kBN;
-        uint32_t v0[16], v1[16];
+        uint32_t v[16];
         if (MODE == kGateUpMode) {
           const float fg = sa * bs_g[kb], fu = sa * bs_u[kb];
-          const uint32_t cg = tbuf + cq * 32, cu = tbuf + 128 + cq * 32;
-          tmem_ld16(cg, v0);
-          tmem_ld16(cg + 16, v1);
-          tmem_ld_wait();
-          promote16(acc, v0, fg);
-          promote16(acc + 16, v1, fg);
-          tmem_ld16(cu, v0);
-          tmem_ld16(cu + 16, v1);
-          tmem_ld_wait();
-          promote16(acc + 32, v0, fu);
-          promote16(acc + 48, v1, fu);
+          const uint32_t cg = tbuf + hh * 64, cu = tbuf + 128 + hh * 64;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld16(cg + 16 * c, v);
+            tmem_ld_wait();
+            promote8(acc + 8 * c, v, fg);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld16(cu + 16 * c, v);
+            tmem_ld_wait();
+            promote8(acc + 32 + 8 * c, v, fu);
+          }
         } else {
           const float f = sa * bs_d[kb];
-          const uint32_t c0 = tbuf + cq * 64;
-          tmem_ld16(c0, v0);
-          tmem_ld16(c0 + 16, v1);
-          tmem_ld_wait();
-          promote16(acc, v0, f);
-          promote16(acc + 16, v1, f);
-          tmem_ld16(c0 + 32, v0);
-          tmem_ld16(c0 + 48, v1);
-          tmem_ld_wait();
-          promote16(acc + 32, v0, f);
-          promote16(acc + 48, v1, f);
+          const uint32_t c0 = tbuf + hh * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            tmem_ld16(c0 + 16 * c, v);
+            tmem_ld_wait();
+            promote8(acc + 8 * c, v, f);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -343,53 +344,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       if (MODE == kGateUpMode) {
-        // h on this thread's 32 columns, then one e4m3 scale per 128-wide
-        // group: the row maximum over the four column quarters
+        // h on this thread's 64 columns, then one e4m3 scale per 128-wide
+        // group: the row maximum over the two column halves
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          acc[i] = gate_act<ACT>(acc[i]) * acc[32 + i];
-          amax = fmaxf(amax, fabsf(acc[i]));
+          acc[i].x = gate_act<ACT>(acc[i].x) * acc[32 + i].x;
+          acc[i].y = gate_act<ACT>(acc[i].y) * acc[32 + i].y;
+          amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
         }
         const int xb = tile_no & 1;
-        amax_x[(xb * 4 + cq) * 128 + row_in_tile] = amax;
+        amax_x[(xb * 2 + hh) * 128 + row_in_tile] = amax;
         mbar_arrive(xchg_bar(xb));
         if (!mbar_wait(xchg_bar(xb), (tile_no >> 1) & 1)) {
           set_err(p.err, GBMOE_ERR_TIMEOUT);
           break;
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) amax = fmaxf(amax, amax_x[(xb * 4 + c) * 128 + row_in_tile]);
+        amax = fmaxf(amax_x[(xb * 2) * 128 + row_in_tile], amax_x[(xb * 2 + 1) * 128 + row_in_tile]);
         const float sc = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
         if (valid) {
           uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
-                                                 (size_t)arow * p.N + nt * 128 + cq * 32);
+                                                 (size_t)arow * p.N + nt * 128 + hh * 64);
 #pragma unroll
-          for (int v = 0; v < 2; ++v) {
+          for (int v = 0; v < 4; ++v) {
             uint32_t w4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const int i0 = v * 16 + j * 4;
-              w4[j] = e4m3x4(__fdiv_rn(acc[i0], sc), __fdiv_rn(acc[i0 + 1], sc),
-                             __fdiv_rn(acc[i0 + 2], sc), __fdiv_rn(acc[i0 + 3], sc));
+              const float2 a = acc[v * 8 + j * 2], b = acc[v * 8 + j * 2 + 1];
+              w4[j] = e4m3x4(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc), __fdiv_rn(b.x, sc),
+                             __fdiv_rn(b.y, sc));
             }
             dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          if (cq == 0) p.out_scales[(size_t)nt * p.scale_ld + arow] = sc;
+          if (hh == 0) p.out_scales[(size_t)nt * p.scale_ld + arow] = sc;
         }
       } else {
-        const int col0 = nt * kBN + cq * 64;
+        const int col0 = nt * kBN + hh * 128;
         if (valid && col0 < p.K) {
           const int pair = p.sorted[arow];
           const float w = p.topk_w ? p.topk_w[pair] : 1.0f;
           uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
                                                  (size_t)pair * p.K + col0);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_uint4(pack_bf16x2(w * acc[8 * v], w * acc[8 * v + 1]),
-                                pack_bf16x2(w * acc[8 * v + 2], w * acc[8 * v + 3]),
-                                pack_bf16x2(w * acc[8 * v + 4], w * acc[8 * v + 5]),
-                                pack_bf16x2(w * acc[8 * v + 6], w * acc[8 * v + 7]));
+          for (int v = 0; v < 16; ++v)
+            dst[v] = make_uint4(pack_bf16x2(w * acc[4 * v].x, w * acc[4 * v].y),
+                                pack_bf16x2(w * acc[4 * v + 1].x, w * acc[4 * v + 1].y),
+                                pack_bf16x2(w * acc[4 * v + 2].x, w * acc[4 * v + 2].y),
+                                pack_bf16x2(w * acc[4 * v + 3].x, w * acc[4 * v + 3].y));
         }
       }
     }

@@ -34,9 +34,34 @@ cudaError_t launch_gather_rows(const void *x, const float *xs, const float *row_
                                const int32_t *total, int P, int topk,
                                void *out, float *out_s, int64_t out_s_ld,
                                int num_sms, cudaStream_t s);
+// clears the fused reduce's arrival counters (M * units) and zeroes the
+// output rows of tokens with no slot computed here (inv < 0 for all)
+cudaError_t launch_fused_reduce_prep(const int32_t *inv, int M, int topk, int K,
+                                     int32_t *arrive, int units, uint16_t *out,
+                                     int num_sms, cudaStream_t s);
 cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
                           int topk, int K, uint16_t *out, int num_sms,
                           cudaStream_t s);
+
+// ep.cu -- worst-tokens dispatch / combine over G shards in this GPU's memory
+struct EpWorkspace {
+  int32_t *ids_eff;     // (G*M*topk): the pairs' expert ids, E for padded tokens
+  int32_t *map;         // (E + 1): e -> e, E -> -1 (skipped)
+  int32_t *counts;      // (E)
+  int32_t *offsets;     // (E + 1)
+  int32_t *sorted;      // (G*M*topk)
+  int32_t *inv;         // (G*M*topk)
+  int32_t *chunk_hist;  // (align_num_chunks(G*M*topk) * E)
+};
+cudaError_t launch_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
+                               const int32_t *topk_ids, int G, int M, int K, int E, int topk,
+                               int worst, uint16_t *recv_x, int32_t *recv_counts,
+                               int32_t *recv_pos, const EpWorkspace &w, int32_t *err,
+                               int num_sms, cudaStream_t s);
+cudaError_t launch_ep_combine(const uint16_t *recv_y, const int32_t *topk_ids,
+                              const int32_t *recv_pos, const float *topk_weights,
+                              const int32_t *num_tokens, int G, int M, int K, int E, int topk,
+                              int worst, uint16_t *out, int num_sms, cudaStream_t s);
 
 // quant.cu
 // row_w (M) or NULL: rows multiplied by their weight (fp32) before quantising
@@ -78,6 +103,17 @@ struct GroupedGemmArgs {
   const int32_t *sorted_pair_ids;  // down, Standard: output row = pair id
   const float *topk_weights;       // down, Standard: row scale
   int32_t *err;
+  // down, Standard, optional: the ordered top-k reduce fused into the
+  // epilogue (fused_out != NULL): out (M, K) bf16, inv (M*topk) of the
+  // sort, topk, and per-(token, column unit) arrival counters
+  // (M * arrive_units int32, zero at launch; arrive_units >= the kernel's
+  // units per row: ceil(K / 256)); the bf16 and per-row-scaled e4m3
+  // kernels only
+  uint16_t *fused_out;
+  const int32_t *inv;
+  int topk;
+  int32_t *arrive;
+  int arrive_units;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,

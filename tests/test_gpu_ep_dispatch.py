@@ -1,0 +1,175 @@
+"""Expert-parallel dispatch / combine in the worst-tokens mode, G = 2 and 4
+shards in this GPU's memory: route -> dispatch -> per-shard masked grouped
+GEMMs reading the device counts -> combine, captured once in a CUDA graph and
+replayed with fresh data, routing and valid-token counts per replay (50 for
+G = 2, 20 for G = 4).  Every replay equals the eager run bit for bit; the
+per-expert counts and every pair's receive row equal the oracle's stable
+counting sort of the valid pairs (bit-exact); the outputs of the valid tokens
+match the oracle's layer over all experts within the bf16 tolerance; rows of
+padded tokens are never written."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads as WL
+from gpu_common import TOL, assert_close_rel, gbmoe, oracle_weights
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+SENTINEL = 0x7E7E
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gbmoe()
+
+
+class EpLayer:
+    """Static buffers of the sharded layer and its launch sequence."""
+
+    def __init__(self, cfg, w1, w2):
+        g = gbmoe()
+        self.cfg, self.g = cfg, g
+        G, M, K, N, E, k = cfg.G, cfg.M, cfg.K, cfg.N, cfg.E, cfg.topk
+        W = cfg.worst_tokens
+        i32 = torch.int32
+        self.x = torch.empty((G, M, K), dtype=torch.bfloat16, device=DEV)
+        self.logits = torch.empty((G, M, E), dtype=torch.float32, device=DEV)
+        self.num_tokens = torch.empty(G, dtype=i32, device=DEV)
+        self.ids = torch.empty((G, M, k), dtype=i32, device=DEV)
+        self.wts = torch.empty((G, M, k), dtype=torch.float32, device=DEV)
+        self.recv_x = torch.empty((E, W, K), dtype=torch.bfloat16, device=DEV)
+        self.recv_y = torch.empty((E, W, K), dtype=torch.bfloat16, device=DEV)
+        self.recv_counts = torch.empty(E, dtype=i32, device=DEV)
+        self.recv_pos = torch.empty((G, M, k), dtype=i32, device=DEV)
+        self.out = torch.empty((G, M, K), dtype=torch.bfloat16, device=DEV)
+        self.err = torch.zeros(1, dtype=i32, device=DEV)
+        self.ws = g.workspace(g.WS_EP_DISPATCH, M, E, G, K, k, 0)
+        El = E // G
+        self.El = El
+        self.w1 = [w1[s * El:(s + 1) * El] for s in range(G)]
+        self.w2 = [w2[s * El:(s + 1) * El] for s in range(G)]
+        self.bws = [g.workspace(g.WS_BATCHED, W, El, N, K, 1, WL.BF16) for _ in range(G)]
+
+    def step(self):
+        c, g = self.cfg, self.g
+        G, M, E, k = c.G, c.M, c.E, c.topk
+        g.moe_topk_route(self.logits.view(G * M, E), None, k, c.score_fn, c.n_groups,
+                         c.topk_groups, True, self.ids.view(G * M, k), self.wts.view(G * M, k))
+        g.moe_ep_dispatch(self.x, self.num_tokens, self.ids, E, c.worst_tokens, self.recv_x,
+                          self.recv_counts, self.recv_pos, self.ws, self.err)
+        for s in range(G):  # each shard's masked grouped GEMMs on its own receive block
+            sl = slice(s * self.El, (s + 1) * self.El)
+            g.moe_batched_masked_experts(self.recv_x[sl], self.recv_counts[sl], c.N, self.w1[s],
+                                         self.w2[s], self.recv_y[sl], self.bws[s],
+                                         err_word=self.err)
+        g.moe_ep_combine(self.recv_y, self.ids, self.recv_pos, self.wts, self.num_tokens,
+                         self.out)
+
+    def load(self, d):
+        self.x.copy_(d["x"])
+        self.logits.copy_(d["logits"])
+        self.num_tokens.copy_(d["num_tokens"])
+        self.out.view(torch.int16).fill_(SENTINEL)
+
+
+def _oracle_check(cfg, layer, d, W):
+    n = d["num_tokens"].cpu().numpy()
+    G, M, E, k = cfg.G, cfg.M, cfg.E, cfg.topk
+    xv = torch.cat([d["x"][r, :n[r]] for r in range(G)])
+    lv = torch.cat([d["logits"][r, :n[r]] for r in range(G)]).cpu().numpy()
+    rid, rw, _ = orc.route(lv, None, k, cfg.score_fn, cfg.n_groups, cfg.topk_groups, True)
+    # per-expert counts and the receive row of every valid pair
+    rc, bad = orc.count(rid, E)
+    ro, rs, ri = orc.align(rid, E)
+    assert bad == 0
+    assert np.array_equal(layer.recv_counts.cpu().numpy(), rc)
+    pos_ref = ri - ro[rid.ravel()]
+    gpos = layer.recv_pos.cpu().numpy()
+    gids = layer.ids.cpu().numpy()
+    got_pos = np.concatenate([gpos[r, :n[r]].ravel() for r in range(G)])
+    got_ids = np.concatenate([gids[r, :n[r]] for r in range(G)])
+    assert np.array_equal(got_ids, rid)
+    assert np.array_equal(got_pos, pos_ref)
+    for r in range(G):  # pairs of padded tokens are not dispatched
+        assert np.all(gpos[r, n[r]:] == -1)
+    # values: the layer over all experts, token by token
+    ref, rid2, _ = orc.moe_forward(WL.bf16_bits(xv), lv, None, k, cfg.score_fn, W,
+                                   cfg.n_groups, cfg.topk_groups, True)
+    got = torch.cat([layer.out[r, :n[r]] for r in range(G)]).float().cpu().numpy()
+    assert_close_rel(got, ref, TOL[WL.BF16], cfg.name)
+    bits = layer.out.view(torch.int16).cpu().numpy()
+    for r in range(G):
+        assert np.all(bits[r, n[r]:] == np.int16(SENTINEL)), f"shard {r}: padded rows written"
+
+
+@pytest.mark.parametrize("cfg,replays", [(WL.EP2, 50), (WL.EP4, 20)], ids=["G2", "G4"])
+def test_ep_worst_tokens_graph_replays(cfg, replays):
+    d0 = WL.make_ep_inputs(cfg, DEV)
+    layer = EpLayer(cfg, d0["w1"], d0["w2"])
+    W = oracle_weights(WL.MoEConfig("ep_all", M=1, K=cfg.K, N=cfg.N, E=cfg.E, topk=cfg.topk),
+                       d0["w1"], d0["w2"])
+    layer.load(d0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.step()  # warm up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.step()
+    eager = EpLayer(cfg, d0["w1"], d0["w2"])
+    for r in range(replays):
+        dr = WL.make_ep_inputs(cfg, DEV, seed=cfg.seed * 1000 + r + 1, with_weights=False)
+        layer.load(dr)
+        graph.replay()
+        eager.load(dr)
+        eager.step()
+        torch.cuda.synchronize()
+        assert layer.err.item() == 0 and eager.err.item() == 0, f"replay {r}"
+        for name in ("out", "recv_counts", "recv_pos", "ids"):
+            a, b = getattr(layer, name), getattr(eager, name)
+            if a.dtype == torch.bfloat16:
+                a, b = a.view(torch.int16), b.view(torch.int16)
+            assert torch.equal(a, b), f"replay {r}: {name} differs from the eager run"
+        if r % 5 == 0:
+            _oracle_check(cfg, layer, dr, W)
+
+
+def test_ep_dispatch_flags_overflow_of_the_static_shape():
+    """A receive capacity below the real per-expert count: the count is
+    clamped, the extra pairs are dropped (pos -1) and the error bit is set;
+    nothing is written past the static shape."""
+    g = gbmoe()
+    cfg = WL.EP2
+    d = WL.make_ep_inputs(cfg, DEV, with_weights=False)
+    G, M, E, k, K = cfg.G, cfg.M, cfg.E, cfg.topk, cfg.K
+    ids = torch.zeros((G, M, k), dtype=torch.int32, device=DEV)
+    ids[..., 1] = 1
+    ids[..., 2] = 2
+    ids[..., 3] = 3   # every token on experts 0..3: counts = sum(num_tokens)
+    worst = 16
+    flat = torch.empty(E * worst * K + 4096, dtype=torch.bfloat16, device=DEV)
+    flat.view(torch.int16).fill_(SENTINEL)
+    recv_x = flat[:E * worst * K].view(E, worst, K)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    pos = torch.empty((G, M, k), dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = g.workspace(g.WS_EP_DISPATCH, M, E, G, K, k, 0)
+    g.moe_ep_dispatch(d["x"], d["num_tokens"], ids, E, worst, recv_x, counts, pos, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() & g.ERR_COUNT_RANGE
+    assert torch.all(counts[:4] == worst) and torch.all(counts[4:] == 0)
+    assert int((pos >= 0).sum()) == 4 * worst
+    assert int(pos.max()) == worst - 1
+    # the first `worst` valid tokens (in shard, token order) fill each block
+    n = d["num_tokens"].cpu().numpy()
+    xv = torch.cat([d["x"][r, :n[r]] for r in range(G)])
+    for e in range(4):
+        assert torch.equal(recv_x[e].view(torch.int16), xv[:worst].view(torch.int16))
+    assert torch.all(recv_x[4:].view(torch.int16) == SENTINEL)      # experts with no rows
+    assert torch.all(flat[E * worst * K:].view(torch.int16) == SENTINEL)  # past the shape

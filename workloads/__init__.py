@@ -241,6 +241,61 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
     return make_standard(cfg, device, seed, with_weights)
 
 
+@dataclasses.dataclass(frozen=True)
+class EpConfig:
+    """Expert-parallel worst-tokens layout: G shards of up to M tokens each
+    (a device count of valid ones per shard), E routed experts split evenly
+    over the shards (E / G each), top-k routing; worst_tokens rows of static
+    receive capacity per expert (G * M: every token of every shard)."""
+    name: str
+    G: int
+    M: int
+    K: int
+    N: int
+    E: int
+    topk: int
+    score_fn: int = SOFTMAX
+    n_groups: int = 1
+    topk_groups: int = 1
+    seed: int = 0
+
+    @property
+    def worst_tokens(self) -> int:
+        return self.G * self.M
+
+
+EP2 = EpConfig("ep_worst_tokens_G2_M96_K512_N256_E32_top4", G=2, M=96, K=512, N=256, E=32,
+               topk=4, seed=71)
+EP4 = EpConfig("ep_worst_tokens_G4_M64_K384_N256_E64_top6", G=4, M=64, K=384, N=256, E=64,
+               topk=6, score_fn=SIGMOID, n_groups=8, topk_groups=4, seed=72)
+
+
+def make_ep_inputs(cfg: EpConfig, device="cpu", seed: Optional[int] = None,
+                   with_weights: bool = True) -> dict:
+    """x (G, M, K) bf16 and logits (G, M, E) fp32 with N(0, 1) valid rows and
+    N(0, 10^2) garbage in the padded rows of each shard, num_tokens (G) int32
+    ~ U{M/2..M} with one shard at M; then w1 (E, 2N, K), w2 (E, K, N) as for
+    the Standard workloads."""
+    g = _gen(cfg.seed if seed is None else seed, device)
+    G, M = cfg.G, cfg.M
+    n = torch.randint(M // 2, M + 1, (G,), generator=g, device=device, dtype=torch.int64)
+    n[int(torch.randint(0, G, (1,), generator=g, device=device).item())] = M
+    rows = torch.arange(M, device=device).view(1, M, 1)
+    pad = rows >= n.view(G, 1, 1)
+    x = torch.where(pad, _randn((G, M, cfg.K), g, device, std=10.0),
+                    _randn((G, M, cfg.K), g, device))
+    logits = torch.where(pad, _randn((G, M, cfg.E), g, device, std=10.0),
+                         _randn((G, M, cfg.E), g, device))
+    out = {"x": x.to(torch.bfloat16), "logits": logits.contiguous(),
+           "num_tokens": n.to(torch.int32)}
+    if with_weights:
+        out["w1"] = _randn((cfg.E, 2 * cfg.N, cfg.K), g, device, std=1.0 / math.sqrt(cfg.K),
+                           dtype=torch.bfloat16)
+        out["w2"] = _randn((cfg.E, cfg.K, cfg.N), g, device, std=1.0 / math.sqrt(cfg.N),
+                           dtype=torch.bfloat16)
+    return out
+
+
 def bf16_bits(t: torch.Tensor):
     """numpy uint16 view of a bf16 tensor's bits (on the host)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
