@@ -2,8 +2,8 @@
 
 One step = one pass of the whole hot path over one batch of synthetic tokens:
 route -> align/permute -> [FP8 quantise] -> gather -> gate/up GEMM + SiLU*mul
--> down GEMM + router weight with the ordered top-k reduce in its epilogue,
-each a CUDA kernel of libgbmoe.so launched through its C ABI.
+-> down GEMM + router weight -> ordered top-k reduce, each a CUDA kernel of
+libgbmoe.so launched through its C ABI.
 
 Default workload: the Mixtral-8x7B-shaped prefill layer in bf16 (M=4096 tokens,
 K=4096, N=14336, E=8, top-2), synthetic seeded inputs resident in HBM.
@@ -212,10 +212,8 @@ class Layer:
         self.err = torch.zeros(1, dtype=i32, device=device)
         self.amax = torch.zeros(2, dtype=i32, device=device) if self.tensor else None
         self.fwd_ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype, device=device)
-        self.dr_ws = g.workspace(g.WS_DOWN_REDUCE, M, E, N, K, k, cfg.dtype, device=device)
-        # route, 3 align, [quant x], gather, gate/up, [quant H], counter
-        # clear + down with the fused reduce (block-scaled e4m3: down, then
-        # the reduce); a per-tensor quant is a clear, a maximum and the codes
+        # route, 3 align, [quant x], gather, gate/up, [quant H], down, reduce;
+        # a per-tensor quant is a clear, a maximum and the codes
         self.launches_per_step = (8 + (1 if self.fp8 else 0) + (1 if self.ch else 0)
                                   + (4 if self.tensor else 0))
 
@@ -258,12 +256,11 @@ class Layer:
         elif self.ch:
             g.moe_quant_fp8_group(self.Hb, self.H, self.Hs, group=N)
             mark("a4_quant_h")
-        # down GEMM + [Finalize]: the ordered reduce runs in the GEMM's
-        # epilogue (a separate pass after it for block-scaled e4m3)
-        g.moe_grouped_gemm_down_reduce(self.H, self.Hs, self.sorted, self.inv, self.offsets,
-                                       self.wts, M, k, E, N, K, self.w2, self.w2s, c.dtype,
-                                       self.y, self.out, self.dr_ws, self.err)
-        mark("a6_a7_down_reduce")
+        g.moe_grouped_gemm_down(self.H, self.Hs, self.sorted, self.offsets, self.wts, M, k, E,
+                                N, K, self.w2, self.w2s, c.dtype, self.y, self.err)
+        mark("a6_down")
+        g.moe_unpermute_weighted_reduce(self.y, self.inv, M, k, K, self.out)
+        mark("a7_reduce")
 
     def forward_public(self, x, logits, out):
         """The public one-call API on device tensors."""

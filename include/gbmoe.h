@@ -90,7 +90,6 @@ enum {
     GBMOE_WS_BATCHED = 2,  /* moe_batched_masked_experts              */
     GBMOE_WS_FORWARD = 3,  /* moe_forward (the whole Standard layer)  */
     GBMOE_WS_SHARED = 4,   /* moe_shared_expert_forward (N = shared intermediate size) */
-    GBMOE_WS_DOWN_REDUCE = 5, /* moe_grouped_gemm_down_reduce          */
     GBMOE_WS_EP_DISPATCH = 6  /* moe_ep_dispatch: M_or_T = M tokens per shard, E = all
                                  routed experts, N = the number of shards G  */
 };
@@ -322,33 +321,6 @@ gbmoe_status_t moe_unpermute_weighted_reduce(const uint16_t *y_slot,
                                              const int32_t *inv, int M,
                                              int topk, int K, uint16_t *out,
                                              gbmoe_stream_t stream);
-
-/* The second expert GEMM and [Finalize] in one call: what
- * moe_grouped_gemm_down followed by moe_unpermute_weighted_reduce (with the
- * same inv) computes, bit for bit -- y_slot (M, topk, K) holds the weighted
- * slot rows and out (M, K) their ordered fp32 sum rounded once to bf16 --
- * with the reduce done inside the GEMM's epilogue ("experts own the weight
- * application", FusedMoEPermuteExpertsUnpermute.finalize_weight_and_reduce_impl,
- * and TopKWeightAndReduce.apply of the modular kernel): for each token and
- * block of output columns, the thread that stores the token's last computed
- * slot row sums the token's rows in slot order j = 0 .. topk-1.  No thread
- * waits for another and no floating-point atomic is used, so the result is
- * deterministic.  A token with no computed slot (inv < 0 for every slot,
- * e.g. all its experts on other shards) gets a zero row.  Block-scaled e4m3
- * (GBMOE_FP8_E4M3) runs the reduce as a separate pass after the GEMM, with
- * the same result.
- * inv (M*topk) is the inverse map of moe_align_permute (-1: pair not computed
- * here); other arguments as in moe_grouped_gemm_down.
- * ws: moe_workspace_size(GBMOE_WS_DOWN_REDUCE, M, E, N, K, topk, dtype)
- * bytes (per-token arrival counters, cleared by the call itself), 16-byte
- * aligned.  Launches: a counter-clearing kernel and the GEMM (or the GEMM and
- * the reduce for block-scaled e4m3).  err_word may be NULL. */
-gbmoe_status_t moe_grouped_gemm_down_reduce(
-    const void *H, const float *H_scales, const int32_t *sorted_pair_ids,
-    const int32_t *inv, const int32_t *offsets, const float *topk_weights, int M,
-    int topk, int E, int N, int K, const void *w2, const float *w2_scales, int dtype,
-    uint16_t *y_slot, uint16_t *out, void *ws, size_t ws_bytes, int32_t *err_word,
-    gbmoe_stream_t stream);
 
 /* Both expert GEMMs in the BatchedExperts format (E, T, K), masked by the
  * device-resident expert_num_tokens as the masked grouped GEMM of the

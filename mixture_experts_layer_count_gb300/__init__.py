@@ -20,7 +20,7 @@ from . import build as _build
 BF16, FP8_E4M3, FP8_E4M3_CHANNEL, FP8_E4M3_TENSOR = 0, 1, 2, 3  # dtype codes of include/gbmoe.h
 SOFTMAX, SIGMOID = 0, 1
 ACT_SILU, ACT_GELU = 0, 1
-WS_ALIGN, WS_BATCHED, WS_FORWARD, WS_SHARED, WS_DOWN_REDUCE, WS_EP_DISPATCH = 0, 2, 3, 4, 5, 6
+WS_ALIGN, WS_BATCHED, WS_FORWARD, WS_SHARED, WS_EP_DISPATCH = 0, 2, 3, 4, 6
 ERR_BAD_EXPERT_ID, ERR_COUNT_RANGE, ERR_TIMEOUT = 0x1, 0x2, 0x4
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype or device",
@@ -66,8 +66,6 @@ _SIGS = {
                                            _I, _P, _P, _P, _P]),
     "moe_grouped_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                                    _I, _P, _P, _P]),
-    "moe_grouped_gemm_down_reduce": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
-                                          _I, _P, _P, _P, _Z, _P, _P]),
     "moe_unpermute_weighted_reduce": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_ep_dispatch": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P, _P]),
     "moe_ep_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
@@ -233,16 +231,6 @@ def moe_grouped_gemm_down(H, H_scales, sorted_pair_ids, offsets, topk_weights,
         _ptr(H), _ptr(H_scales), _ptr(sorted_pair_ids), _ptr(offsets),
         _ptr(topk_weights), M, topk, E, N, K, _ptr(w2), _ptr(w2_scales), dtype,
         _ptr(y_slot), _ptr(err_word), _stream(stream)))
-
-
-def moe_grouped_gemm_down_reduce(H, H_scales, sorted_pair_ids, inv, offsets, topk_weights,
-                                 M, topk, E, N, K, w2, w2_scales, dtype, y_slot, out, ws,
-                                 err_word=None, stream=None):
-    _check("moe_grouped_gemm_down_reduce", load().moe_grouped_gemm_down_reduce(
-        _ptr(H), _ptr(H_scales), _ptr(sorted_pair_ids), _ptr(inv), _ptr(offsets),
-        _ptr(topk_weights), M, topk, E, N, K, _ptr(w2), _ptr(w2_scales), dtype,
-        _ptr(y_slot), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
-        _stream(stream)))
 
 
 def moe_ep_dispatch(x, num_tokens, topk_ids, E, worst_tokens, recv_x, recv_counts, recv_pos,

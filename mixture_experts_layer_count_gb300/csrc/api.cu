@@ -93,12 +93,7 @@ struct ForwardWs {
   uint16_t *Hb;     // row-scaled e4m3: H in bf16 before its quantisation
   uint32_t *amax;   // GBMOE_FP8_E4M3_TENSOR: the maxima of x and of H
   uint16_t *y_slot;
-  int32_t *arrive;  // arrival counters of the reduce fused into the down GEMM
 };
-
-// arrival counters per token of the fused reduce: one per 64 output columns
-// (enough for every kernel's column unit)
-int arrive_units(int K) { return (K + 63) / 64; }
 ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dtype) {
   const size_t P = (size_t)M * topk;
   ForwardWs w;
@@ -121,7 +116,6 @@ ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dty
   w.amax = dtype == GBMOE_FP8_E4M3_TENSOR ? static_cast<uint32_t *>(c.take(2 * sizeof(uint32_t)))
                                          : nullptr;
   w.y_slot = static_cast<uint16_t *>(c.take(P * (size_t)K * 2));
-  w.arrive = static_cast<int32_t *>(c.take((size_t)M * arrive_units(K) * 4));
   return w;
 }
 
@@ -206,16 +200,12 @@ gbmoe_status_t permute_impl(const void *x, const float *x_scales,
                                       scale_ld((size_t)M * topk), num_sms, s));
 }
 
-// fused_out (optional): the ordered top-k reduce runs in the down GEMM's
-// epilogue and writes out (M, K); inv and arrive (zeroed here) as in
-// GroupedGemmArgs
 gbmoe_status_t down_impl(const void *H, const float *H_scales,
                          const int32_t *sorted, const int32_t *offsets,
                          const float *topk_weights, int M, int topk, int E,
                          int N, int K, const void *w2, const float *w2_scales,
                          int dtype, uint16_t *y_slot, int32_t *err, int num_sms,
-                         cudaStream_t s, uint16_t *fused_out = nullptr,
-                         const int32_t *inv = nullptr, int32_t *arrive = nullptr) {
+                         cudaStream_t s) {
   GroupedGemmArgs a{};
   a.mode = kDown;
   a.fp8 = dtype == GBMOE_FP8_E4M3;
@@ -234,24 +224,8 @@ gbmoe_status_t down_impl(const void *H, const float *H_scales,
   a.sorted_pair_ids = sorted;
   a.topk_weights = topk_weights;
   a.err = err;
-  if (fused_out) {
-    cudaError_t ce = launch_fused_reduce_prep(inv, M, topk, K, arrive, arrive_units(K), fused_out,
-                                              num_sms, s);
-    if (ce != cudaSuccess) return from_cuda(ce);
-    a.fused_out = fused_out;
-    a.inv = inv;
-    a.topk = topk;
-    a.arrive = arrive;
-    a.arrive_units = arrive_units(K);
-  }
   return from_cuda(launch_grouped_gemm(a, num_sms, s));
 }
-
-// whether the down GEMM's kernel carries the ordered reduce in its epilogue:
-// bf16 and per-row-scaled e4m3 (one epilogue per tile); the block-scaled e4m3
-// kernel promotes every K block in its epilogue, which then sets the pace, so
-// its reduce is a pass of its own after the GEMM
-bool down_fuses_reduce(int dtype) { return dtype != GBMOE_FP8_E4M3; }
 
 bool gemm_shape_ok(int M, int topk, int E, int N, int K, int dtype) {
   return M >= 0 && topk >= 1 && topk <= kMaxTopk && E >= 1 && E <= kMaxExperts &&
@@ -301,10 +275,6 @@ size_t moe_workspace_size(int which, int M_or_T, int E, int N, int K, int topk,
       if (!gemm_shape_ok(M_or_T, topk, E, N, K, dtype)) return 0;
       carve_forward(c, M_or_T, E, N, K, topk, dtype);
       return c.off;
-    case GBMOE_WS_DOWN_REDUCE:
-      if (!gemm_shape_ok(M_or_T, topk, E, N, K, dtype)) return 0;
-      c.take((size_t)M_or_T * arrive_units(K) * 4);
-      return c.off > 0 ? c.off : kWsAlign;
     case GBMOE_WS_EP_DISPATCH:
       // M_or_T: tokens per shard (M), E: all routed experts, N: the number of
       // shards G
@@ -514,39 +484,6 @@ gbmoe_status_t moe_grouped_gemm_down(
                    (cudaStream_t)stream);
 }
 
-gbmoe_status_t moe_grouped_gemm_down_reduce(
-    const void *H, const float *H_scales, const int32_t *sorted_pair_ids,
-    const int32_t *inv, const int32_t *offsets, const float *topk_weights, int M,
-    int topk, int E, int N, int K, const void *w2, const float *w2_scales, int dtype,
-    uint16_t *y_slot, uint16_t *out, void *ws, size_t ws_bytes, int32_t *err_word,
-    gbmoe_stream_t stream) {
-  if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
-  if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
-  if (M == 0) {
-    int sms;
-    return device_info(&sms);
-  }
-  const bool fp8 = is_fp8(dtype);
-  if (!H || !sorted_pair_ids || !inv || !offsets || !w2 || !y_slot || !out || !ws)
-    return GBMOE_INVALID_ARG;
-  if (fp8 && (!H_scales || !w2_scales)) return GBMOE_INVALID_ARG;
-  if (row_scaled(dtype) && !aligned16(w2_scales)) return GBMOE_INVALID_ARG;
-  if (!aligned16(H) || !aligned16(w2) || !aligned16(y_slot) || !aligned16(out) || !aligned16(ws))
-    return GBMOE_INVALID_ARG;
-  if (ws_bytes < moe_workspace_size(GBMOE_WS_DOWN_REDUCE, M, E, N, K, topk, dtype))
-    return GBMOE_INVALID_ARG;
-  int sms;
-  gbmoe_status_t st = device_info(&sms);
-  if (st != GBMOE_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  const bool fuse = down_fuses_reduce(dtype);
-  st = down_impl(H, H_scales, sorted_pair_ids, offsets, topk_weights, M, topk, E, N, K, w2,
-                 w2_scales, dtype, y_slot, err_word, sms, s, fuse ? out : nullptr, inv,
-                 static_cast<int32_t *>(ws));
-  if (st != GBMOE_OK || fuse) return st;
-  return from_cuda(launch_reduce(y_slot, inv, M, topk, K, out, sms, s));
-}
-
 gbmoe_status_t moe_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
                                const int32_t *topk_ids, int G, int M, int K, int E,
                                int topk, int worst_tokens, uint16_t *recv_x,
@@ -749,11 +686,9 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
     ce = launch_quant_row(w.Hb, nullptr, P, N, static_cast<uint8_t *>(w.H), w.Hs, sms, s);
     if (ce != cudaSuccess) return from_cuda(ce);
   }
-  const bool fuse = down_fuses_reduce(dtype);
   st = down_impl(w.H, w.Hs, w.sorted, w.offsets, in_w ? nullptr : wts, M, topk, E, N, K, w2,
-                 w2_scales, dtype, w.y_slot, err_word, sms, s, fuse ? out : nullptr, w.inv,
-                 w.arrive);
-  if (st != GBMOE_OK || fuse) return st;
+                 w2_scales, dtype, w.y_slot, err_word, sms, s);
+  if (st != GBMOE_OK) return st;
   return from_cuda(launch_reduce(w.y_slot, w.inv, M, topk, K, out, sms, s));
 }
 

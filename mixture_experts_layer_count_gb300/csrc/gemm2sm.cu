@@ -64,11 +64,6 @@ struct KParams {
   void *out;
   const int32_t *sorted;
   const float *topk_w;
-  uint16_t *fused_out;      // down, Standard: fused ordered reduce (or NULL)
-  const int32_t *inv;
-  int topk;
-  int32_t *arrive;
-  int arrive_units;
   int32_t *err;
 };
 
@@ -227,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + t_lane + buf * kBN;
-      int reduce_pair = -1;  // down with the fused reduce: this row's pair
       if (MODE == kGateUpMode) {
         uint16_t *hrow = static_cast<uint16_t *>(p.out) + (size_t)arow * p.N + nt * 128;
 #pragma unroll 1
@@ -259,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pair = p.sorted[arow];
             orow = (size_t)pair;
             w = p.topk_w ? p.topk_w[pair] : 1.0f;
-            if (p.fused_out) reduce_pair = pair;
           } else {
             orow = (size_t)arow;
           }
@@ -286,11 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
-      // the ordered top-k reduce of this row's token, after TMEM is released
-      if (MODE == kDownMode && reduce_pair >= 0)
-        fused_slot_reduce(static_cast<const uint16_t *>(p.out), p.inv, p.arrive, p.fused_out,
-                          reduce_pair, p.topk, p.K, nt, p.arrive_units, nt * kBN,
-                          p.K < nt * kBN + kBN ? p.K : nt * kBN + kBN);
       ++acc_it;
     }
   }
@@ -329,11 +317,6 @@ cudaError_t launch_pair(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   p.out = a.out;
   p.sorted = a.sorted_pair_ids;
   p.topk_w = a.topk_weights;
-  p.fused_out = a.fused_out;
-  p.inv = a.inv;
-  p.topk = a.topk;
-  p.arrive = a.arrive;
-  p.arrive_units = a.arrive_units;
   p.err = a.err;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);

@@ -101,63 +101,6 @@ __device__ __forceinline__ float gate_act(float g) {
   return ACT == kActGelu ? gelu_f(g) : silu_f(g);
 }
 
-// [Finalize] (TopKWeightAndReduce.apply / FusedMoEPrepareAndFinalize.finalize
-// in "vllm/model_executor/layers/fused_moe/modular_kernel.py") fused into the
-// down GEMM's epilogue.  The calling thread has just stored the weighted
-// bf16 slot row of `pair` for output columns [c0, c1) into y_slot (M, topk,
-// K).  It counts itself in on the token's arrival counter of that column
-// unit; the thread that arrives last for the token (the number of its slots
-// computed in this launch: inv >= 0) sums the token's slot rows over
-// [c0, c1) in slot order j = 0..topk-1 in fp32 and stores one bf16 rounding
-// into out (M, K).  The sum reads the stored bf16 rows, so it is bit for bit
-// the separate ordered reduce, whichever thread arrives last; nothing waits
-// and no floating-point atomic is used.  Counters start at zero (cleared
-// before the launch); stores are published by a device-scope fence before
-// the counter increment, and the last arriver fences again and reads the
-// rows through L2 (ld.global.cg), bypassing its SM's L1.
-__device__ __forceinline__ void fused_slot_reduce(const uint16_t *y_slot, const int32_t *inv,
-                                                  int32_t *arrive, uint16_t *out, int pair,
-                                                  int topk, int K, int unit, int n_units,
-                                                  int c0, int c1) {
-  const int t = pair / topk;
-  const int32_t *iv = inv + (size_t)t * topk;
-  int target = 0;
-  for (int j = 0; j < topk; ++j) target += __ldg(iv + j) >= 0 ? 1 : 0;
-  __threadfence();
-  const int old = atomicAdd(arrive + (size_t)t * n_units + unit, 1);
-  if (old != target - 1) return;
-  __threadfence();
-  const uint16_t *yt = y_slot + (size_t)t * topk * K;
-  for (int c = c0; c < c1; c += 8) {
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j0 = 0; j0 < topk; j0 += 8) {
-      uint4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u;
-        const bool take = j < topk && __ldg(iv + j) >= 0;
-        v[u] = take ? __ldcg(reinterpret_cast<const uint4 *>(yt + (size_t)j * K + c))
-                    : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[u]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(h[i]);
-          acc[2 * i] += f.x;
-          acc[2 * i + 1] += f.y;
-        }
-      }
-    }
-    *reinterpret_cast<uint4 *>(out + (size_t)t * K + c) =
-        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-  }
-}
-
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3) |
          ((uint32_t)__nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3) << 8) |

@@ -34,11 +34,6 @@ cudaError_t launch_gather_rows(const void *x, const float *xs, const float *row_
                                const int32_t *total, int P, int topk,
                                void *out, float *out_s, int64_t out_s_ld,
                                int num_sms, cudaStream_t s);
-// clears the fused reduce's arrival counters (M * units) and zeroes the
-// output rows of tokens with no slot computed here (inv < 0 for all)
-cudaError_t launch_fused_reduce_prep(const int32_t *inv, int M, int topk, int K,
-                                     int32_t *arrive, int units, uint16_t *out,
-                                     int num_sms, cudaStream_t s);
 cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
                           int topk, int K, uint16_t *out, int num_sms,
                           cudaStream_t s);
@@ -103,17 +98,6 @@ struct GroupedGemmArgs {
   const int32_t *sorted_pair_ids;  // down, Standard: output row = pair id
   const float *topk_weights;       // down, Standard: row scale
   int32_t *err;
-  // down, Standard, optional: the ordered top-k reduce fused into the
-  // epilogue (fused_out != NULL): out (M, K) bf16, inv (M*topk) of the
-  // sort, topk, and per-(token, column unit) arrival counters
-  // (M * arrive_units int32, zero at launch; arrive_units >= the kernel's
-  // units per row: ceil(K / 256)); the bf16 and per-row-scaled e4m3
-  // kernels only
-  uint16_t *fused_out;
-  const int32_t *inv;
-  int topk;
-  int32_t *arrive;
-  int arrive_units;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs &a, int num_sms,

@@ -287,40 +287,7 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Before a down GEMM that carries the fused ordered reduce: one warp per
-// token clears the token's arrival counters (units int32) and, for a token
-// none of whose slots is computed here (every inv < 0: all its experts are
-// on other shards), writes its output row as zeros, as the separate reduce
-// would (a sum of no slot).
-__global__ void __launch_bounds__(256)
-    fused_reduce_prep_kernel(const int32_t *__restrict__ inv, int M, int topk, int kvec,
-                             int32_t *__restrict__ arrive, int units,
-                             uint4 *__restrict__ out) {
-  const int lane = threadIdx.x & 31;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < M;
-       t += (gridDim.x * blockDim.x) >> 5) {
-    for (int u = lane; u < units; u += 32) arrive[(size_t)t * units + u] = 0;
-    const bool mine = lane < topk && __ldg(inv + (size_t)t * topk + lane) >= 0;
-    bool any = __any_sync(0xffffffffu, mine);
-    for (int j = 32 + lane; j < topk && !any; j += 32) any = __ldg(inv + (size_t)t * topk + j) >= 0;
-    any = __any_sync(0xffffffffu, any);
-    if (!any)
-      for (int v = lane; v < kvec; v += 32) out[(size_t)t * kvec + v] = make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
 }  // namespace
-
-cudaError_t launch_fused_reduce_prep(const int32_t *inv, int M, int topk, int K,
-                                     int32_t *arrive, int units, uint16_t *out,
-                                     int num_sms, cudaStream_t s) {
-  int blocks = (M + 7) / 8;
-  if (blocks > 8 * num_sms) blocks = 8 * num_sms;
-  if (blocks < 1) blocks = 1;
-  fused_reduce_prep_kernel<<<blocks, 256, 0, s>>>(inv, M, topk, K / 8, arrive, units,
-                                                  reinterpret_cast<uint4 *>(out));
-  return cudaGetLastError();
-}
 
 cudaError_t launch_count(const int32_t *ids, int P, int Eg, const int32_t *map,
                          int E, int32_t *counts, int32_t *err, int num_sms,

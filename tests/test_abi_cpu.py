@@ -37,17 +37,14 @@ def test_binding_covers_every_entry_point():
 def test_workspace_sizes():
     import mixture_experts_layer_count_gb300 as g
     # Standard layer: ids, weights, counts, offsets, sorted, inv, chunk
-    # histograms, gathered rows, H, the weighted slots and the fused
-    # reduce's arrival counters (one per token and 64 output columns), each
-    # 256-aligned
+    # histograms, gathered rows, H and the weighted slots, each 256-aligned
     M, E, N, K, k = 64, 8, 128, 256, 2
     n = g.moe_workspace_size(g.WS_FORWARD, M, E, N, K, k, g.BF16)
     P = M * k
     expect = sum(-(-b // 256) * 256 for b in (
         P * 4, P * 4, E * 4, (E + 1) * 4, P * 4, P * 4, 1 * E * 4,
-        P * K * 2, P * N * 2, P * K * 2, M * (K // 64) * 4))  # A, H, y_slot, counters
+        P * K * 2, P * N * 2, P * K * 2))  # A, H, y_slot
     assert n == expect
-    assert g.moe_workspace_size(g.WS_DOWN_REDUCE, M, E, N, K, k, g.BF16) == M * (K // 64) * 4
     assert g.moe_workspace_size(g.WS_FORWARD, M, E, 100, K, k, g.BF16) == 0  # N % 128
     assert g.moe_workspace_size(g.WS_BATCHED, 16, 4, 128, 256, 1, g.FP8_E4M3) == 0
     assert g.moe_workspace_size(g.WS_ALIGN, 8192, 256, 0, 0, 8, 0) == 32 * 256 * 4
@@ -139,12 +136,6 @@ def test_gemm_calls_reject_bad_arguments(lib):
     assert pr(None, None, None, P16, P16, 8, 2, 8, 256, 0, P16, None, None) == INVALID
     # FP8 rows take the router weight in the quantiser, not in the gather
     assert pr(P16, P16, P16, P16, P16, 8, 1, 8, 256, 1, P16, P16, None) == INVALID
-    dr = lib.moe_grouped_gemm_down_reduce
-    #         H    Hs    srt  inv   off  w    M  k  E  N    K    w2   w2s  dt ys   out  ws   wsb      err   s
-    assert dr(P16, None, P16, None, P16, P16, 8, 2, 8, 128, 256, P16, None, 0, P16, P16, P16, 1 << 20, None, None) == INVALID  # no inv
-    assert dr(P16, None, P16, P16, P16, P16, 8, 2, 8, 128, 256, P16, None, 0, P16, P16, P16, 16, None, None) == INVALID  # ws too small
-    assert dr(P16, None, P16, P16, P16, P16, 8, 2, 8, 128, 256, P16, None, 0, P16, P_ODD, P16, 1 << 20, None, None) == INVALID
-    assert dr(P16, None, P16, P16, P16, P16, 8, 2, 8, 128, 256, P16, None, 1, P16, P16, P16, 1 << 20, None, None) == INVALID  # fp8 w/o scales
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 2, 12, P16, None) == INVALID
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 33, 256, P16, None) == INVALID
     b = lib.moe_batched_masked_experts
