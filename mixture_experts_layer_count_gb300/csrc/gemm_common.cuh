@@ -101,6 +101,14 @@ __device__ __forceinline__ float gate_act(float g) {
   return ACT == kActGelu ? gelu_f(g) : silu_f(g);
 }
 
+// the same with SiLU's division by the approximate __fdividef (within 2 ulp;
+// 0 for a denominator above 2^126, the limit of z / (1 + e^-z) there), for
+// epilogues whose result is requantised to e4m3 next
+template <int ACT>
+__device__ __forceinline__ float gate_act_fast(float g) {
+  return ACT == kActGelu ? gelu_f(g) : __fdividef(g, 1.0f + __expf(-g));
+}
+
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return (uint32_t)__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3) |
          ((uint32_t)__nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3) << 8) |

@@ -257,6 +257,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_in_tile = q * 32 + lane;
     const uint32_t t_lane = (uint32_t)(q * 32) << 16;
     const int b_blk_rows = p.b_rows / 128;
+    // The weight-block scales of a tile, [0] gate (or the first 128
+    // columns), [1] up (or the second 128 columns), for every K block:
+    // 2 * num_kb <= 256 values, one per epilogue thread.  Each thread loads
+    // its value of the next tile while the current one runs and stores it
+    // into the other half of the double buffer at the tile's end, so a tile
+    // starts with its scales in shared memory.
+    auto tile_scale = [&](int tile_idx) -> float {
+      if (etid >= 2 * num_kb || tile_idx >= total) return 0.0f;
+      int te, tmt, tnt;
+      decode_tile(prefix, E, p.n_tiles, tile_idx, te, tmt, tnt);
+      const int h = etid / num_kb, kb = etid - h * num_kb;
+      int blk = MODE == kGateUpMode ? (h == 0 ? tnt : p.N / 128 + tnt) : tnt * 2 + h;
+      if (blk >= b_blk_rows) blk = b_blk_rows - 1;  // columns past K: masked
+      return __ldg(p.b_scales + ((size_t)te * b_blk_rows + blk) * num_kb + kb);
+    };
+    auto put_scale = [&](int tno, float v) {
+      if (etid < 2 * num_kb) {
+        const int h = etid / num_kb, kb = etid - h * num_kb;
+        bsc_smem[(tno & 1) * 2 * kMaxKB + h * kMaxKB + kb] = v;
+      }
+      mbar_arrive(bsc_bar(tno & 1));
+    };
+    if (blockIdx.x < total) put_scale(0, tile_scale(blockIdx.x));
     int it = 0, tile_no = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tile_no) {
@@ -267,18 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = r < rcnt[e];
       const int arow = a_row + row_in_tile;
       const int as_idx = (a_row & 3) + row_in_tile;
-
-      // weight-block scales of this tile: [0] gate (or the first 128
-      // columns), [1] up (or the second 128 columns), for every K block
-      const int tb = tile_no & 1;
-      float *bsc = bsc_smem + tb * 2 * kMaxKB;
-      for (int i = etid; i < 2 * num_kb; i += kEpiThreads) {
-        const int h = i / num_kb, kb = i - h * num_kb;
-        int blk = MODE == kGateUpMode ? (h == 0 ? nt : p.N / 128 + nt) : nt * 2 + h;
-        if (blk >= b_blk_rows) blk = b_blk_rows - 1;  // columns past K: masked
-        bsc[h * kMaxKB + kb] = p.b_scales[((size_t)e * b_blk_rows + blk) * num_kb + kb];
+      const float next_scale = tile_scale(tile + gridDim.x);  // used at the tile's end
+      // down: the output row (pair) and its router weight, needed at the end
+      int pair = 0;
+      float wgt = 1.0f;
+      if (MODE == kDownMode && valid) {
+        pair = __ldg(p.sorted + arow);
+        wgt = p.topk_w ? __ldg(p.topk_w + pair) : 1.0f;
       }
-      mbar_arrive(bsc_bar(tb));
+
+      const int tb = tile_no & 1;
+      const float *bsc = bsc_smem + tb * 2 * kMaxKB;
       if (!mbar_wait(bsc_bar(tb), (tile_no >> 1) & 1)) {
         set_err(p.err, GBMOE_ERR_TIMEOUT);
         break;
@@ -349,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          acc[i].x = gate_act<ACT>(acc[i].x) * acc[32 + i].x;
-          acc[i].y = gate_act<ACT>(acc[i].y) * acc[32 + i].y;
+          acc[i].x = gate_act_fast<ACT>(acc[i].x) * acc[32 + i].x;
+          acc[i].y = gate_act_fast<ACT>(acc[i].y) * acc[32 + i].y;
           amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
         }
         const int xb = tile_no & 1;
@@ -362,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         amax = fmaxf(amax_x[(xb * 2) * 128 + row_in_tile], amax_x[(xb * 2 + 1) * 128 + row_in_tile]);
         const float sc = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
+        const float inv_sc = __frcp_rn(sc);  // codes of h * (1 / s): one division per row group
         if (valid) {
           uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
                                                  (size_t)arow * p.N + nt * 128 + hh * 64);
@@ -371,8 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float2 a = acc[v * 8 + j * 2], b = acc[v * 8 + j * 2 + 1];
-              w4[j] = e4m3x4(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc), __fdiv_rn(b.x, sc),
-                             __fdiv_rn(b.y, sc));
+              w4[j] = e4m3x4(a.x * inv_sc, a.y * inv_sc, b.x * inv_sc, b.y * inv_sc);
             }
             dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
@@ -381,8 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const int col0 = nt * kBN + hh * 128;
         if (valid && col0 < p.K) {
-          const int pair = p.sorted[arow];
-          const float w = p.topk_w ? p.topk_w[pair] : 1.0f;
+          const float w = wgt;
           uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
                                                  (size_t)pair * p.K + col0);
 #pragma unroll
@@ -393,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pack_bf16x2(w * acc[4 * v + 3].x, w * acc[4 * v + 3].y));
         }
       }
+      if (tile + gridDim.x < total) put_scale(tile_no + 1, next_scale);
     }
   }
 
