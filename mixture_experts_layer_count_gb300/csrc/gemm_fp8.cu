@@ -58,8 +58,11 @@ constexpr int kOffBar = kOffAS + kASStages * kASStage;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 2 + 2 + 2 * kASStages;
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kOffBsc = kOffTmem + 16;                       // [2 bufs][2][kMaxKB] f32
-constexpr int kOffAmax = kOffBsc + 2 * 2 * kMaxKB * 4;       // [2 bufs][4][128] f32
-constexpr int kOffPrefix = kOffAmax + 2 * 4 * 128 * 4;
+constexpr int kOffAmax = kOffBsc + 2 * 2 * kMaxKB * 4;       // [2 bufs][2 halves][128] f32
+constexpr int kStgRow = 272;                                 // staged output row: 256 B + 16 B pad
+constexpr int kStgWarp = 8 * kStgRow;                        // 8 rows per epilogue warp
+constexpr int kOffStg = (kOffAmax + 2 * 2 * 128 * 4 + 127) / 128 * 128;  // [8 warps][8 rows][272 B]
+constexpr int kOffPrefix = kOffStg + 8 * kStgWarp;
 constexpr int kOffRBase = kOffPrefix + (kMaxE + 1) * 4;
 constexpr int kOffRCnt = kOffRBase + kMaxE * 4;
 constexpr int kSmemUsed = kOffRCnt + kMaxE * 4;
@@ -263,10 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // its value of the next tile while the current one runs and stores it
     // into the other half of the double buffer at the tile's end, so a tile
     // starts with its scales in shared memory.
-    auto tile_scale = [&](int tile_idx) -> float {
-      if (etid >= 2 * num_kb || tile_idx >= total) return 0.0f;
-      int te, tmt, tnt;
-      decode_tile(prefix, E, p.n_tiles, tile_idx, te, tmt, tnt);
+    auto tile_scale = [&](int te, int tnt) -> float {
+      if (etid >= 2 * num_kb) return 0.0f;
       const int h = etid / num_kb, kb = etid - h * num_kb;
       int blk = MODE == kGateUpMode ? (h == 0 ? tnt : p.N / 128 + tnt) : tnt * 2 + h;
       if (blk >= b_blk_rows) blk = b_blk_rows - 1;  // columns past K: masked
@@ -279,25 +280,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(bsc_bar(tno & 1));
     };
-    if (blockIdx.x < total) put_scale(0, tile_scale(blockIdx.x));
+    // down: the output row (pair) of this thread's row and its router weight
+    auto row_pair = [&](int te, int tmt) -> int {
+      return tmt * kBM + row_in_tile < rcnt[te] ? __ldg(p.sorted + rbase[te] + tmt * kBM + row_in_tile)
+                                                : -1;
+    };
+    // a tile is decoded once, as the next tile of the previous iteration
+    int ce = 0, cmt = 0, cnt = 0;
+    int cur_pair = 0;
+    float cur_wgt = 1.0f;
+    if (blockIdx.x < total) {
+      decode_tile(prefix, E, p.n_tiles, blockIdx.x, ce, cmt, cnt);
+      put_scale(0, tile_scale(ce, cnt));
+      if (MODE == kDownMode) {
+        cur_pair = row_pair(ce, cmt);
+        cur_wgt = cur_pair >= 0 && p.topk_w ? __ldg(p.topk_w + cur_pair) : 1.0f;
+      }
+    }
     int it = 0, tile_no = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tile_no) {
-      int e, mt, nt;
-      decode_tile(prefix, E, p.n_tiles, tile, e, mt, nt);
+      const int e = ce, mt = cmt, nt = cnt;
       const int a_row = rbase[e] + mt * kBM;
       const int r = mt * kBM + row_in_tile;
       const bool valid = r < rcnt[e];
       const int arow = a_row + row_in_tile;
       const int as_idx = (a_row & 3) + row_in_tile;
-      const float next_scale = tile_scale(tile + gridDim.x);  // used at the tile's end
-      // down: the output row (pair) and its router weight, needed at the end
-      int pair = 0;
-      float wgt = 1.0f;
-      if (MODE == kDownMode && valid) {
-        pair = __ldg(p.sorted + arow);
-        wgt = p.topk_w ? __ldg(p.topk_w + pair) : 1.0f;
-      }
+      // the next tile: its decode, its weight-block scale (stored at this
+      // tile's end) and, for down, its row's pair (the weight of that pair
+      // is loaded halfway through this tile's K loop)
+      const bool has_next = tile + (int)gridDim.x < total;
+      int ne = 0, nmt = 0, nnt = 0;
+      if (has_next) decode_tile(prefix, E, p.n_tiles, tile + gridDim.x, ne, nmt, nnt);
+      const float next_scale = has_next ? tile_scale(ne, nnt) : 0.0f;
+      const int pair = cur_pair;
+      const float wgt = cur_wgt;
+      const int nxt_pair = MODE == kDownMode && has_next ? row_pair(ne, nmt) : -1;
+      float nxt_wgt = 1.0f;
 
       const int tb = tile_no & 1;
       const float *bsc = bsc_smem + tb * 2 * kMaxKB;
@@ -316,6 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if (MODE == kDownMode && kb == num_kb / 2 && nxt_pair >= 0 && p.topk_w)
+          nxt_wgt = __ldg(p.topk_w + nxt_pair);
         const int buf = it & 1, use = it >> 1;
         const int s8 = it % kASStages, round8 = it / kASStages;
         if (!mbar_wait(as_full_bar(s8), round8 & 1)) {
@@ -401,20 +422,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (hh == 0) p.out_scales[(size_t)nt * p.scale_ld + arow] = sc;
         }
       } else {
+        // Each thread holds 128 columns (256 bytes of bf16) of its row.  A
+        // warp's 32 rows go out through shared memory, 8 rows at a time, so
+        // that every global store instruction writes one row's 256 bytes
+        // (32 lanes x 8 bytes) instead of 16 bytes of 32 different rows.
         const int col0 = nt * kBN + hh * 128;
-        if (valid && col0 < p.K) {
-          const float w = wgt;
-          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                                 (size_t)pair * p.K + col0);
+        if (col0 < p.K) {  // uniform over the CTA
+          uint32_t pk[64];
 #pragma unroll
-          for (int v = 0; v < 16; ++v)
-            dst[v] = make_uint4(pack_bf16x2(w * acc[4 * v].x, w * acc[4 * v].y),
-                                pack_bf16x2(w * acc[4 * v + 1].x, w * acc[4 * v + 1].y),
-                                pack_bf16x2(w * acc[4 * v + 2].x, w * acc[4 * v + 2].y),
-                                pack_bf16x2(w * acc[4 * v + 3].x, w * acc[4 * v + 3].y));
+          for (int j = 0; j < 64; ++j) pk[j] = pack_bf16x2(wgt * acc[j].x, wgt * acc[j].y);
+          uint8_t *stg = sbase + kOffStg + ew * kStgWarp;
+          uint16_t *ybase = static_cast<uint16_t *>(p.out) + col0 + lane * 4;
+#pragma unroll 1
+          for (int b = 0; b < 4; ++b) {
+            if ((lane >> 3) == b) {
+              uint4 *dst = reinterpret_cast<uint4 *>(stg + (lane & 7) * kStgRow);
+#pragma unroll
+              for (int v = 0; v < 16; ++v)
+                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+              const int src = b * 8 + rr;
+              const int rpair = __shfl_sync(0xffffffffu, pair, src);
+              const int rvalid = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
+              if (rvalid) {
+                const uint2 val = *reinterpret_cast<const uint2 *>(stg + rr * kStgRow + lane * 8);
+                *reinterpret_cast<uint2 *>(ybase + (size_t)rpair * p.K) = val;
+              }
+            }
+            __syncwarp();
+          }
         }
       }
-      if (tile + gridDim.x < total) put_scale(tile_no + 1, next_scale);
+      if (has_next) put_scale(tile_no + 1, next_scale);
+      cur_pair = nxt_pair;
+      cur_wgt = nxt_wgt;
+      ce = ne;
+      cmt = nmt;
+      cnt = nnt;
     }
   }
 
