@@ -246,7 +246,8 @@ def _stage_inputs(cfg):
 
 
 SMALL_STANDARD = [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.SMALL_FP8, WL.SMALL_PAIR,
-                  WL.SMALL_PAIR_TOP2, WL.SMALL_FP8_K640, WL.SMALL_FP8CH, WL.SMALL_FP8CH_PAIR]
+                  WL.SMALL_PAIR_TOP2, WL.SMALL_FP8_K640, WL.SMALL_FP8_NARROW, WL.SMALL_FP8CH,
+                  WL.SMALL_FP8CH_PAIR]
 
 
 @pytest.mark.parametrize("cfg", SMALL_STANDARD, ids=lambda c: c.name)

@@ -100,6 +100,10 @@ SMALL_PAIR_TOP2 = MoEConfig("small_pair_bf16_M520_K640_N384_E4_top2", M=520, K=6
 # e4m3 with a down n-tile of 128 columns (K = 640) and 150 rows per expert
 SMALL_FP8_K640 = MoEConfig("small_fp8_M300_K640_N256_E4_top2", M=300, K=640, N=256,
                            E=4, topk=2, dtype=FP8, seed=18)
+# e4m3 with every expert at 1..64 rows (the operand-swapped narrow tile) and
+# K = 640 (the last down tile's second half lies past K)
+SMALL_FP8_NARROW = MoEConfig("small_fp8_narrow_M48_K640_N256_E8_top2", M=48, K=640, N=256,
+                             E=8, topk=2, dtype=FP8, seed=29)
 SMALL_BATCHED_SHORT = MoEConfig("small_batched_bf16_E5_T100_K384_N256", M=100, K=384,
                                 N=256, E=5, topk=1, batched=True, seed=17)
 
@@ -142,6 +146,8 @@ PROFILE_FP8 = MoEConfig("profile_fp8_M2048_K7168_N2048_E16_top2", M=2048, K=7168
 PROFILE_FP8CH = MoEConfig("profile_fp8ch_M2048_K7168_N2048_E16_top2", M=2048, K=7168,
                           N=2048, E=16, topk=2, dtype=FP8_CHANNEL, score_fn=SIGMOID,
                           n_groups=4, topk_groups=2, seed=22)
+PROFILE_BATCHED = MoEConfig("profile_batched_bf16_E8_T512_K7168_N2048", M=512, K=7168,
+                            N=2048, E=8, topk=1, batched=True, seed=24)
 PROFILE_DECODE = MoEConfig("profile_decode_bf16_M16_K7168_N2048_E32_top4", M=16,
                            K=7168, N=2048, E=32, topk=4, score_fn=SIGMOID,
                            n_groups=4, topk_groups=2, seed=23)
@@ -150,7 +156,8 @@ BY_NAME = {c.name: c for c in ALL + [SMALL_BF16, SMALL_SIGMOID, SMALL_FP8,
                                      SMALL_BATCHED, SMALL_PAIR, SMALL_PAIR_TOP2, SMALL_FP8_K640,
                                      SMALL_FP8CH, SMALL_FP8CH_PAIR, DSV3_PREFILL_FP8CH,
                                      PROFILE_FP8CH, SMALL_FP8T, MID_FP8T, DSV3_PREFILL_FP8T,
-                                     SMALL_BATCHED_SHORT, PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE]}
+                                     SMALL_BATCHED_SHORT, PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE,
+                                     PROFILE_BATCHED, SMALL_FP8_NARROW]}
 
 
 def _gen(seed: int, device) -> torch.Generator:
