@@ -48,6 +48,14 @@ def test_workspace_sizes():
     assert g.moe_workspace_size(g.WS_FORWARD, M, E, 100, K, k, g.BF16) == 0  # N % 128
     assert g.moe_workspace_size(g.WS_BATCHED, 16, 4, 128, 256, 1, g.FP8_E4M3) == 0
     assert g.moe_workspace_size(g.WS_ALIGN, 8192, 256, 0, 0, 8, 0) == 32 * 256 * 4
+    # EP dispatch (M tokens per shard, E routed experts, N = G shards): the
+    # pairs' ids, the map, counts, offsets, sorted, inv, chunk histograms
+    G, M, E, k = 4, 100, 64, 6
+    P = G * M * k
+    expect = sum(-(-b // 256) * 256 for b in (P * 4, (E + 1) * 4, E * 4, (E + 1) * 4, P * 4,
+                                               P * 4, -(-P // 2048) * E * 4))
+    assert g.moe_workspace_size(g.WS_EP_DISPATCH, M, E, G, 256, k, 0) == expect
+    assert g.moe_workspace_size(g.WS_EP_DISPATCH, M, E, 5, 256, k, 0) == 0  # E % G
 
 
 def test_status_strings():
@@ -137,6 +145,19 @@ def test_gemm_calls_reject_bad_arguments(lib):
     # FP8 rows take the router weight in the quantiser, not in the gather
     assert pr(P16, P16, P16, P16, P16, 8, 1, 8, 256, 1, P16, P16, None) == INVALID
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 2, 12, P16, None) == INVALID
+    ed = lib.moe_ep_dispatch
+    #         x    ntok ids  G  M   K    E   k  worst rx   rc   rp   ws   wsb      err   s
+    assert ed(P16, P16, P16, 3, 16, 256, 32, 4, 48, P16, P16, P16, P16, 1 << 20, None, None) == INVALID  # E % G
+    assert ed(P16, P16, P16, 2, 16, 250, 32, 4, 32, P16, P16, P16, P16, 1 << 20, None, None) == INVALID  # K % 8
+    assert ed(P16, P16, P16, 2, 16, 256, 32, 4, 32, P16, P16, P16, P16, 16, None, None) == INVALID       # ws too small
+    assert ed(P16, None, P16, 2, 16, 256, 32, 4, 32, P16, P16, P16, P16, 1 << 20, None, None) == INVALID  # no counts
+    assert ed(P_ODD, P16, P16, 2, 16, 256, 32, 4, 32, P16, P16, P16, P16, 1 << 20, None, None) == INVALID
+    assert ed(P16, P16, P16, 2, 16, 256, 32, 33, 32, P16, P16, P16, P16, 1 << 20, None, None) == INVALID  # topk
+    ec = lib.moe_ep_combine
+    #         ry   ids  pos  w    ntok G  M   K    E   k  worst out  s
+    assert ec(P16, P16, P16, P16, P16, 2, 16, 256, 32, 4, 0, P16, None) == INVALID    # worst < 1
+    assert ec(P16, P16, P16, None, P16, 2, 16, 256, 32, 4, 32, P16, None) == INVALID  # no weights
+    assert ec(P16, P16, P16, P16, P16, 2, 16, 256, 32, 4, 32, P_ODD, None) == INVALID
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 33, 256, P16, None) == INVALID
     b = lib.moe_batched_masked_experts
     #        xb  xbs   cnt E  T   N    K    w1   w1s  w2   w2s  dt ac yb   ws   wsb  err  s
