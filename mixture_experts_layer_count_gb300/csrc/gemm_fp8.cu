@@ -25,6 +25,15 @@
 // top-k reduce is a pass of its own after this kernel: added to this
 // epilogue it stalled the per-K-block pipeline, 1.8 -> 4.3 ms on the
 // DeepSeek-V3-shaped prefill).
+//
+// The epilogue keeps its accumulators in registers, so the tensor core can
+// run only two K blocks into the next tile while the epilogue finishes the
+// current one.  Down tiles are short (K = N, 16 K blocks for N = 2048), and
+// writing 128 scattered output rows per tile from the epilogue stalled the
+// next tile's MMAs for about a third of the tile's time.  So in down mode
+// the epilogue only packs its rows into a shared-memory stage of the whole
+// tile and a store warp writes them out during the next tile; the stage
+// costs the operand ring one of its four stages.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -41,7 +50,6 @@ using namespace gemm;
 
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 64 + kEpiThreads;      // 320
 constexpr int kBK = kBKB;                       // e4m3 elements per stage row
 constexpr int kMmaPerStage = kBK / 32;          // kind::f8f6f4 has K = 32
 constexpr uint32_t kIdesc = umma_idesc(kBM, kBN, kFmtE4M3);
@@ -50,23 +58,35 @@ constexpr int kASBox = kBM + 4;                 // row scales per K block (rows 
 constexpr int kASStage = 640;                   // bytes per ring slot (528 used)
 constexpr int kASStages = 8;                    // row-scale ring, deeper than the operand ring
 
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kAStage;
-constexpr int kOffAS = kOffB + kStages * kBStage;            // 196608
-constexpr int kOffBar = kOffAS + kASStages * kASStage;
 // full[4], empty[4], tfull[2], tempty[2], done, bsc[2], xchg[2], as_full[8], as_empty[8]
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 2 + 2 + 2 * kASStages;
-constexpr int kOffTmem = kOffBar + 8 * kNumBars;
-constexpr int kOffBsc = kOffTmem + 16;                       // [2 bufs][2][kMaxKB] f32
-constexpr int kOffAmax = kOffBsc + 2 * 2 * kMaxKB * 4;       // [2 bufs][2 halves][128] f32
-constexpr int kStgRow = 272;                                 // staged output row: 256 B + 16 B pad
-constexpr int kStgWarp = 8 * kStgRow;                        // 8 rows per epilogue warp
-constexpr int kOffStg = (kOffAmax + 2 * 2 * 128 * 4 + 127) / 128 * 128;  // [8 warps][8 rows][272 B]
-constexpr int kOffPrefix = kOffStg + 8 * kStgWarp;
-constexpr int kOffRBase = kOffPrefix + (kMaxE + 1) * 4;
-constexpr int kOffRCnt = kOffRBase + kMaxE * 4;
-constexpr int kSmemUsed = kOffRCnt + kMaxE * 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;
+constexpr int kTileRow = 528;  // a staged down-output row: 256 bf16 + 16 B of padding
+
+// Shared-memory layout per mode.  Down keeps three operand stages and a
+// stage of the whole output tile (128 rows of 256 bf16 plus the rows' pair
+// ids) that a store warp drains while the epilogue moves on to the next
+// tile; gate/up keeps four operand stages and the row-maximum exchange.
+template <int MODE>
+struct Layout {
+  static constexpr bool kDown = MODE == kDownMode;
+  static constexpr int S = kDown ? 3 : kStages;
+  static constexpr int threads = 64 + kEpiThreads + (kDown ? 32 : 0);
+  static constexpr int offA = 0;
+  static constexpr int offB = offA + S * kAStage;
+  static constexpr int offAS = offB + S * kBStage;
+  static constexpr int offBar = offAS + kASStages * kASStage;
+  static constexpr int nbars = 2 * S + 2 + 2 + 1 + 2 + 2 + 2 * kASStages + (kDown ? 2 : 0);
+  static constexpr int offTmem = offBar + 8 * nbars;
+  static constexpr int offBsc = offTmem + 16;                      // [2 bufs][2][kMaxKB] f32
+  static constexpr int offAmax = offBsc + 2 * 2 * kMaxKB * 4;      // gate/up: [2][2][128] f32
+  static constexpr int offStg = (offAmax + (kDown ? 0 : 2 * 2 * 128 * 4) + 127) / 128 * 128;
+  static constexpr int offStgPair = offStg + (kDown ? kBM * kTileRow : 0);
+  static constexpr int offPrefix = offStgPair + (kDown ? kBM * 4 : 0);
+  static constexpr int offRBase = offPrefix + (kMaxE + 1) * 4;
+  static constexpr int offRCnt = offRBase + kMaxE * 4;
+  static constexpr int used = offRCnt + kMaxE * 4;
+  static constexpr int smem = used + 1024;
+  static_assert(smem <= 232448, "shared memory");
+};
 
 struct KParams {
   const int32_t *offsets;
@@ -104,7 +124,7 @@ __device__ __forceinline__ void promote8(float2 *acc, const uint32_t (&v)[16], f
 }
 
 template <int MODE, int ACT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Layout<MODE>::threads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmAS,
@@ -114,33 +134,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t *sbase = smem_raw + (base - raw_u32);
 
-  const uint32_t sA = base + kOffA;
-  const uint32_t sB = base + kOffB;
-  const uint32_t sAS = base + kOffAS;
-  const uint32_t bar0 = base + kOffBar;
+  using L = Layout<MODE>;
+  constexpr int S = L::S;
+  const uint32_t sA = base + L::offA;
+  const uint32_t sB = base + L::offB;
+  const uint32_t sAS = base + L::offAS;
+  const uint32_t bar0 = base + L::offBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-  const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
-  auto bsc_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 5 + b); };
-  auto xchg_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 7 + b); };
-  auto as_full_bar = [&](int s) { return bar0 + 8u * (2 * kStages + 9 + s); };
-  auto as_empty_bar = [&](int s) { return bar0 + 8u * (2 * kStages + 9 + kASStages + s); };
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + kOffTmem);
-  const float *as_smem = reinterpret_cast<const float *>(sbase + kOffAS);
-  float *bsc_smem = reinterpret_cast<float *>(sbase + kOffBsc);
-  float *amax_x = reinterpret_cast<float *>(sbase + kOffAmax);
-  int *prefix = reinterpret_cast<int *>(sbase + kOffPrefix);
-  int *rbase = reinterpret_cast<int *>(sbase + kOffRBase);
-  int *rcnt = reinterpret_cast<int *>(sbase + kOffRCnt);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
+  auto bsc_bar = [&](int b) { return bar0 + 8u * (2 * S + 5 + b); };
+  auto xchg_bar = [&](int b) { return bar0 + 8u * (2 * S + 7 + b); };
+  auto as_full_bar = [&](int s) { return bar0 + 8u * (2 * S + 9 + s); };
+  auto as_empty_bar = [&](int s) { return bar0 + 8u * (2 * S + 9 + kASStages + s); };
+  const uint32_t stg_full_bar = bar0 + 8u * (2 * S + 9 + 2 * kASStages);
+  const uint32_t stg_empty_bar = stg_full_bar + 8u;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + L::offTmem);
+  const float *as_smem = reinterpret_cast<const float *>(sbase + L::offAS);
+  float *bsc_smem = reinterpret_cast<float *>(sbase + L::offBsc);
+  float *amax_x = reinterpret_cast<float *>(sbase + L::offAmax);
+  uint8_t *stg = sbase + L::offStg;
+  int *stg_pair = reinterpret_cast<int *>(sbase + L::offStgPair);
+  int *prefix = reinterpret_cast<int *>(sbase + L::offPrefix);
+  int *rbase = reinterpret_cast<int *>(sbase + L::offRBase);
+  int *rcnt = reinterpret_cast<int *>(sbase + L::offRCnt);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
 
   tile_table_fill(p.offsets, nullptr, E, 0, p.n_tiles, prefix, rbase, rcnt, p.err);
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -155,6 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(xchg_bar(b), kEpiThreads);
     }
     mbar_init(done_bar, 1);
+    if constexpr (MODE == kDownMode) {
+      mbar_init(stg_full_bar, kEpiWarps);  // every epilogue warp staged its rows
+      mbar_init(stg_empty_bar, 1);         // the store warp drained the stage
+    }
     fence_barrier_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -174,9 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =========================== TMA producer ===========================
     if (lane == 0) {
       int it = 0;
-      int last_round[kStages], last_as_round[kASStages];
+      int last_round[S], last_as_round[kASStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
+      for (int s = 0; s < S; ++s) last_round[s] = -1;
 #pragma unroll
       for (int s = 0; s < kASStages; ++s) last_as_round[s] = -1;
       bool ok = true;
@@ -193,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           b_row1 = b_row0 + 128;
         }
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = it % kStages, round = it / kStages;
+          const int s = it % S, round = it / S;
           const int s8 = it % kASStages, round8 = it / kASStages;
           if (!mbar_wait(empty_bar(s), (round & 1) ^ 1) ||
               !mbar_wait(as_empty_bar(s8), (round8 & 1) ^ 1)) {
@@ -216,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // copies still in flight land before the CTA can leave
 #pragma unroll
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < S; ++s)
         if (last_round[s] >= 0) mbar_wait(full_bar(s), last_round[s] & 1, 100000000ull);
 #pragma unroll
       for (int s = 0; s < kASStages; ++s)
@@ -230,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int buf = it & 1, use = it >> 1;
-          const int s = it % kStages, round = it / kStages;
+          const int s = it % S, round = it / S;
           if (!mbar_wait(tempty_bar(buf), (use & 1) ^ 1) ||
               !mbar_wait(full_bar(s), round & 1)) {
             set_err(p.err, GBMOE_ERR_TIMEOUT);
@@ -250,6 +280,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit(done_bar);
       mbar_wait(done_bar, 0, 100000000ull);
+    }
+  } else if (MODE == kDownMode && warp == 2 + kEpiWarps) {
+    // ========================= down-output stores =======================
+    // Each staged row goes out as one 512-byte store (32 lanes x 16 B) to
+    // its (token, slot) row; the stage is handed back once read.
+    int tile_no = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tile_no) {
+      int e, mt, nt;
+      decode_tile(prefix, E, p.n_tiles, tile, e, mt, nt);
+      if (!mbar_wait(stg_full_bar, tile_no & 1)) {
+        set_err(p.err, GBMOE_ERR_TIMEOUT);
+        break;
+      }
+      const int col = nt * kBN + lane * 8;
+      const bool in_k = col < p.K;
+      uint16_t *ycol = static_cast<uint16_t *>(p.out) + col;
+#pragma unroll 8
+      for (int r = 0; r < kBM; ++r) {
+        const int pr = stg_pair[r];
+        if (pr >= 0 && in_k) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * kTileRow + lane * 16);
+          *reinterpret_cast<uint4 *>(ycol + (size_t)pr * p.K) = v;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stg_empty_bar);
     }
   } else {
     // ============================= epilogue =============================
@@ -422,39 +478,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (hh == 0) p.out_scales[(size_t)nt * p.scale_ld + arow] = sc;
         }
       } else {
-        // Each thread holds 128 columns (256 bytes of bf16) of its row.  A
-        // warp's 32 rows go out through shared memory, 8 rows at a time, so
-        // that every global store instruction writes one row's 256 bytes
-        // (32 lanes x 8 bytes) instead of 16 bytes of 32 different rows.
-        const int col0 = nt * kBN + hh * 128;
-        if (col0 < p.K) {  // uniform over the CTA
-          uint32_t pk[64];
-#pragma unroll
-          for (int j = 0; j < 64; ++j) pk[j] = pack_bf16x2(wgt * acc[j].x, wgt * acc[j].y);
-          uint8_t *stg = sbase + kOffStg + ew * kStgWarp;
-          uint16_t *ybase = static_cast<uint16_t *>(p.out) + col0 + lane * 4;
-#pragma unroll 1
-          for (int b = 0; b < 4; ++b) {
-            if ((lane >> 3) == b) {
-              uint4 *dst = reinterpret_cast<uint4 *>(stg + (lane & 7) * kStgRow);
-#pragma unroll
-              for (int v = 0; v < 16; ++v)
-                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-              const int src = b * 8 + rr;
-              const int rpair = __shfl_sync(0xffffffffu, pair, src);
-              const int rvalid = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
-              if (rvalid) {
-                const uint2 val = *reinterpret_cast<const uint2 *>(stg + rr * kStgRow + lane * 8);
-                *reinterpret_cast<uint2 *>(ybase + (size_t)rpair * p.K) = val;
-              }
-            }
-            __syncwarp();
-          }
+        // This thread's 128 columns (256 bytes of bf16) of its row go into
+        // the tile's stage; the store warp writes them out while this warp
+        // starts on the next tile.
+        if (!mbar_wait(stg_empty_bar, (tile_no & 1) ^ 1)) {
+          set_err(p.err, GBMOE_ERR_TIMEOUT);
+          break;
         }
+        if (nt * kBN + hh * 128 < p.K) {  // uniform over the warp
+          uint4 *dst = reinterpret_cast<uint4 *>(stg + row_in_tile * kTileRow + hh * 256);
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            dst[v] = make_uint4(pack_bf16x2(wgt * acc[4 * v].x, wgt * acc[4 * v].y),
+                                pack_bf16x2(wgt * acc[4 * v + 1].x, wgt * acc[4 * v + 1].y),
+                                pack_bf16x2(wgt * acc[4 * v + 2].x, wgt * acc[4 * v + 2].y),
+                                pack_bf16x2(wgt * acc[4 * v + 3].x, wgt * acc[4 * v + 3].y));
+        }
+        if (hh == 0) stg_pair[row_in_tile] = valid ? pair : -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stg_full_bar);
       }
       if (has_next) put_scale(tile_no + 1, next_scale);
       cur_pair = nxt_pair;
@@ -474,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int MODE, int ACT>
 cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   static PerDeviceInt smem_set;
-  cudaError_t st = set_smem_once(smem_set, grouped_gemm_fp8_kernel<MODE, ACT>, kSmemBytes);
+  cudaError_t st = set_smem_once(smem_set, grouped_gemm_fp8_kernel<MODE, ACT>, Layout<MODE>::smem);
   if (st != cudaSuccess) return st;
   const bool gate_up = MODE == kGateUpMode;
   const int Kd = gate_up ? a.K : a.N;
@@ -508,7 +550,7 @@ cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   long long tiles = ((a.a_rows + kBM - 1) / kBM + a.E) * (long long)p.n_tiles;
   int grid = (int)(tiles < num_sms ? tiles : num_sms);
   if (grid < 1) grid = 1;
-  grouped_gemm_fp8_kernel<MODE, ACT><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmAS, p);
+  grouped_gemm_fp8_kernel<MODE, ACT><<<grid, Layout<MODE>::threads, Layout<MODE>::smem, s>>>(tmA, tmB, tmAS, p);
   return cudaGetLastError();
 }
 
