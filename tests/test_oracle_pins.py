@@ -338,6 +338,49 @@ def test_batched_equals_standard_on_the_same_routing(orc):
                 assert np.all(np.isnan(yb[e, r]))
 
 
+def test_fp8_batched_rows_are_dequantised_swiglu_with_requantised_h(orc):
+    """FP8 BatchedExperts: each valid row (e, r) is expert e's SwiGLU of the
+    dequantised row (1 x 128 group scales) and dequantised weights (128 x 128
+    block scales), with h requantised per 128-group by the library e4m3 cast
+    before the down projection; padded rows are never written."""
+    E, T, K, N = 3, 5, 256, 256
+    rng = np.random.default_rng(31)
+    xb = torch.from_numpy(rng.standard_normal((E, T, K)).astype(np.float32)).to(torch.bfloat16)
+    w1 = torch.from_numpy((rng.standard_normal((E, 2 * N, K)) / np.sqrt(K)).astype(np.float32)).to(torch.bfloat16)
+    w2 = torch.from_numpy((rng.standard_normal((E, K, N)) / np.sqrt(N)).astype(np.float32)).to(torch.bfloat16)
+    q1, s1, q2, s2 = [], [], [], []
+    for e in range(E):
+        a, b = orc.quant_fp8_block(_bits(w1[e])); q1.append(a); s1.append(b)
+        a, b = orc.quant_fp8_block(_bits(w2[e])); q2.append(a); s2.append(b)
+    W = orc.Weights(orc.FP8, np.stack(q1), np.stack(q2), np.stack(s1), np.stack(s2))
+    counts = np.array([5, 0, 2], np.int32)
+    yb, n = orc.batched_experts(_bits(xb), counts, W, requant_h=True)
+    assert n == 7
+
+    def deq(q, s, rows, cols):
+        v = torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy()
+        return v * np.kron(s.astype(np.float64), np.ones((rows, cols)))
+
+    for e in range(E):
+        wd1 = deq(q1[e], s1[e], 128, 128)
+        wd2 = deq(q2[e], s2[e], 128, 128)
+        for r in range(T):
+            if r >= counts[e]:
+                assert np.all(np.isnan(yb[e, r]))
+                continue
+            qx, sx = orc.quant_fp8_group(_bits(xb[e, r:r + 1]))
+            x = deq(qx, sx, 1, 128)[0]
+            h = (_silu(x @ wd1[:N].T) * (x @ wd1[N:].T)).astype(np.float32)
+            hq = np.empty(N)
+            for g in range(N // 128):
+                hg = h[g * 128:(g + 1) * 128]
+                sc = np.float32(np.abs(hg).max()) / np.float32(448)
+                hq[g * 128:(g + 1) * 128] = (torch.from_numpy(hg / sc).to(torch.float8_e4m3fn)
+                                             .double().numpy() * float(sc))
+            ref = hq @ wd2.T
+            np.testing.assert_allclose(yb[e, r], ref, rtol=0, atol=1e-10 * np.abs(ref).max())
+
+
 # ------------------------------------------- expert_map / weight on input ----
 
 def _swiglu_np(x, w1, w2, N):
