@@ -484,7 +484,8 @@ def run_gpu(args, cfg):
         pg.destroy_process_group()
 
 
-EXTRA_WORKLOADS = [WL.TINY, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8, WL.BATCHED_MASKED]
+EXTRA_WORKLOADS = [WL.TINY, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8, WL.BATCHED_MASKED,
+                   WL.BATCHED_MASKED_FP8]
 
 
 def run_extras(args, dev, skip=None):
@@ -559,7 +560,9 @@ def measure_standard_entry(cfg, dev, steps, warmup):
 
 def measure_batched_entry(cfg, dev, steps, warmup):
     """One CUDA graph of moe_batched_masked_experts replayed over resident
-    inputs; the roofline covers both grouped GEMM launches."""
+    inputs; the roofline covers both grouped GEMM launches.  e4m3: x_b comes
+    quantised (1 x 128 group scales, as the prepare step hands it to the
+    experts) and the weights block-quantised, both before the timed region."""
     import torch
     import mixture_experts_layer_count_gb300 as g
     g.load()
@@ -567,18 +570,35 @@ def measure_batched_entry(cfg, dev, steps, warmup):
     E, T, N, K = cfg.E, cfg.M, cfg.N, cfg.K
     xb, counts, w1, w2 = d["x_b"], d["counts"], d["w1"], d["w2"]
     yb = torch.empty_like(xb)
+    fp8 = cfg.dtype == WL.FP8
+    kw = {}
+    if fp8:
+        q1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=dev)
+        q2 = torch.empty((E, K, N), dtype=torch.uint8, device=dev)
+        s1 = torch.empty((E, 2 * N // 128, K // 128), dtype=torch.float32, device=dev)
+        s2 = torch.empty((E, K // 128, N // 128), dtype=torch.float32, device=dev)
+        g.moe_quant_fp8_block(w1, q1, s1)
+        g.moe_quant_fp8_block(w2, q2, s2)
+        xq = torch.empty((E, T, K), dtype=torch.uint8, device=dev)
+        xs = torch.empty((E * T, K // 128), dtype=torch.float32, device=dev)
+        g.moe_quant_fp8_group(xb.view(E * T, K), xq.view(E * T, K), xs)
+        del d["w1"], d["w2"]
+        w1, w2, xb = q1, q2, xq
+        kw = dict(dtype=WL.FP8, x_b_scales=xs, w1_scales=s1, w2_scales=s2)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = g.workspace(g.WS_BATCHED, T, E, N, K, 1, WL.BF16, device=dev)
+    ws = g.workspace(g.WS_BATCHED, T, E, N, K, 1, cfg.dtype, device=dev)
     rows = int(counts.clamp(0, T).sum().item())
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         for _ in range(warmup):
-            g.moe_batched_masked_experts(xb, counts, N, w1, w2, yb, ws, err_word=err)
+            g.moe_batched_masked_experts(xb, counts, N, w1, w2, yb, ws, err_word=err, **kw)
     torch.cuda.current_stream().wait_stream(s)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        g.moe_batched_masked_experts(xb, counts, N, w1, w2, yb, ws, err_word=err)
+        g.moe_batched_masked_experts(xb, counts, N, w1, w2, yb, ws, err_word=err, **kw)
     for _ in range(warmup):
         graph.replay()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -596,12 +616,13 @@ def measure_batched_entry(cfg, dev, steps, warmup):
     assert err.item() == 0, f"device error word {err.item()}"
     peaks, src = _peaks()
     key = "bf16_tflops" if ms / 1e3 < 2.0 else "bf16_tflops_sustained"
-    peak = peaks.get(key, FALLBACK_PEAKS[key])
+    peak = peaks.get(key, FALLBACK_PEAKS[key]) * (2.0 if fp8 else 1.0)
     flop = 6.0 * K * N * rows
     achieved = flop / (ms / steps / 1e3) / 1e12
     touched = int((counts > 0).sum().item())
-    wbytes = touched * 3 * N * K * 2
-    hbm = (wbytes + 2 * rows * K * 2) / (ms / steps / 1e3) / 1e9
+    eb = 1 if fp8 else 2
+    wbytes = touched * 3 * N * K * eb
+    hbm = (wbytes + rows * K * (eb + 2)) / (ms / steps / 1e3) / 1e9
     return {"unit": "rows/s", "value": rows * steps / (ms / 1e3), "steps": steps,
             "ms_per_step": ms / steps, "graph_ms_per_step": ms / steps,
             "kernel_ms": ms / steps,
@@ -611,9 +632,11 @@ def measure_batched_entry(cfg, dev, steps, warmup):
                          "hbm_frac": hbm / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
                          "traffic": None, "flop_per_launch": flop,
                          "kernel": "grouped GEMM gate/up + down (one graph replay)",
-                         "peak_source": f"{src} {key} (timed region {ms / 1e3:.2f} s)"},
+                         "peak_source": f"{src} {key} (timed region {ms / 1e3:.2f} s)"
+                                        + (" x2 (nominal fp8:bf16 dense ratio)" if fp8 else "")},
             "clocks": clk.summary(wall0, wall1),
             "config": {"E": E, "T": T, "K": K, "N": N, "valid_rows": rows,
+                       "scales": _scales_desc(cfg),
                        "experts_with_rows": touched,
                        "l2": "no flush; working set > L2 (%.2f GB of expert weights per "
                              "step)" % (wbytes / 1e9)}}
@@ -963,6 +986,9 @@ def main():
             raise SystemExit("the reference arm times the Standard workloads")
         run_reference(args, cfg)
     elif cfg.batched:
+        if cfg.dtype != WL.BF16:
+            raise SystemExit("the e4m3 BatchedExperts workload is timed in the per_workload "
+                             "object of the default line")
         run_gpu_batched(args, cfg)
     else:
         run_gpu(args, cfg)

@@ -333,8 +333,18 @@ gbmoe_status_t moe_unpermute_weighted_reduce(const uint16_t *y_slot,
  * written.  A count outside [0, T] is clamped and sets GBMOE_ERR_COUNT_RANGE.
  * No count is read on the host, so the call can be captured in a CUDA graph
  * and replayed with new counts.
- * dtype GBMOE_BF16 only: x_b (E, T, K) bf16, w1 (E, 2N, K), w2 (E, K, N)
- * bf16, y_b (E, T, K) bf16; x_b_scales, w1_scales, w2_scales NULL.
+ * dtype GBMOE_BF16: x_b (E, T, K) bf16, w1 (E, 2N, K), w2 (E, K, N) bf16;
+ *   x_b_scales, w1_scales, w2_scales ignored.
+ * dtype GBMOE_FP8_E4M3 (the experts' side of the prepare step's per-token-
+ *   group quantisation): x_b (E, T, K) e4m3 codes with x_b_scales
+ *   (E*T, K/128) fp32 row-major, one scale per row and 128-group (the layout
+ *   moe_quant_fp8_group writes for x_b viewed as (E*T, K)); w1/w2 e4m3 with
+ *   their 128 x 128 block scales w1_scales (E, 2N/128, K/128) and
+ *   w2_scales (E, K/128, N/128).  The products are promoted per 128-wide K
+ *   block, h is requantised to e4m3 per row and 128-group inside ws, and the
+ *   down projection reads it back with those scales.  Scales of padded rows
+ *   are never used.  The other e4m3 dtypes return GBMOE_UNSUPPORTED.
+ * y_b (E, T, K) bf16 in both cases.
  * ws: moe_workspace_size(GBMOE_WS_BATCHED, T, E, N, K, 1, dtype) bytes. */
 gbmoe_status_t moe_batched_masked_experts(
     const void *x_b, const float *x_b_scales,

@@ -119,6 +119,24 @@ ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dty
   return w;
 }
 
+// BatchedExperts scratch: H (E*T, N) (bf16, or e4m3 with its group-major
+// scales), and for e4m3 the activations' scales moved to the group-major
+// layout the GEMM's scale loads read
+struct BatchedWs {
+  void *H;
+  float *Hs;
+  float *xs;
+};
+BatchedWs carve_batched(Carver &c, int T, int E, int N, int K, int dtype) {
+  const size_t R = (size_t)E * T;
+  BatchedWs w;
+  w.H = c.take(R * (size_t)N * elem_bytes(dtype));
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  w.Hs = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(R) * (N / 128) * 4)) : nullptr;
+  w.xs = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(R) * (K / 128) * 4)) : nullptr;
+  return w;
+}
+
 EpWorkspace carve_ep(Carver &c, int G, int M, int E, int topk) {
   const size_t P = (size_t)G * M * topk;
   EpWorkspace w;
@@ -268,8 +286,10 @@ size_t moe_workspace_size(int which, int M_or_T, int E, int N, int K, int topk,
       return c.off > 0 ? c.off : kWsAlign;
     }
     case GBMOE_WS_BATCHED:
-      if (!gemm_shape_ok(M_or_T, 1, E, N, K, dtype) || dtype != GBMOE_BF16) return 0;
-      c.take((size_t)E * M_or_T * N * 2);
+      if (!gemm_shape_ok(M_or_T, 1, E, N, K, dtype) ||
+          (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3) || (size_t)E * M_or_T > (size_t)INT32_MAX)
+        return 0;
+      carve_batched(c, M_or_T, E, N, K, dtype);
       return c.off > 0 ? c.off : kWsAlign;
     case GBMOE_WS_FORWARD:
       if (!gemm_shape_ok(M_or_T, topk, E, N, K, dtype)) return 0;
@@ -547,11 +567,9 @@ gbmoe_status_t moe_batched_masked_experts(
     const void *w1, const float *w1_scales, const void *w2,
     const float *w2_scales, int dtype, int activation, uint16_t *y_b, void *ws,
     size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream) {
-  (void)x_b_scales;
   if (activation != GBMOE_ACT_SILU && activation != GBMOE_ACT_GELU) return GBMOE_INVALID_ARG;
-  (void)w1_scales;
-  (void)w2_scales;
-  if (dtype != GBMOE_BF16) return GBMOE_UNSUPPORTED;
+  if (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3) return GBMOE_UNSUPPORTED;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
   if (!gemm_shape_ok(T, 1, E, N, K, dtype)) return GBMOE_INVALID_ARG;
   if ((size_t)E * T > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
   if (T == 0) {
@@ -559,6 +577,8 @@ gbmoe_status_t moe_batched_masked_experts(
     return device_info(&sms);
   }
   if (!x_b || !expert_num_tokens || !w1 || !w2 || !y_b || !ws) return GBMOE_INVALID_ARG;
+  if (fp8 && (!x_b_scales || !w1_scales || !w2_scales)) return GBMOE_INVALID_ARG;
+  if (fp8 && (reinterpret_cast<uintptr_t>(x_b_scales) & 3u)) return GBMOE_INVALID_ARG;
   if (!aligned16(x_b) || !aligned16(w1) || !aligned16(w2) || !aligned16(y_b) || !aligned16(ws))
     return GBMOE_INVALID_ARG;
   if (ws_bytes < moe_workspace_size(GBMOE_WS_BATCHED, T, E, N, K, 1, dtype))
@@ -567,9 +587,12 @@ gbmoe_status_t moe_batched_masked_experts(
   gbmoe_status_t st = device_info(&sms);
   if (st != GBMOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  void *Hb = ws;
+  Carver c(ws);
+  const BatchedWs w = carve_batched(c, T, E, N, K, dtype);
+  const int64_t R = (int64_t)E * T;
   GroupedGemmArgs a{};
   a.mode = kGateUp;
+  a.fp8 = fp8;
   a.act = activation;
   a.counts = expert_num_tokens;
   a.E = E;
@@ -577,15 +600,28 @@ gbmoe_status_t moe_batched_masked_experts(
   a.N = N;
   a.K = K;
   a.A = x_b;
-  a.a_rows = (int64_t)E * T;
+  a.a_rows = R;
   a.B = w1;
-  a.out = Hb;
+  a.out = w.H;
   a.err = err_word;
-  cudaError_t ce = launch_grouped_gemm(a, sms, s);
+  cudaError_t ce;
+  if (fp8) {
+    // the caller's (E*T, K/128) row-major scales -> (K/128, ld) group-major
+    ce = launch_scales_group_major(x_b_scales, R, K / 128, w.xs, scale_ld((size_t)R), sms, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+    a.A_scales = w.xs;
+    a.scale_ld = scale_ld((size_t)R);
+    a.B_scales = w1_scales;
+    a.out_scales = w.Hs;
+  }
+  ce = launch_grouped_gemm(a, sms, s);
   if (ce != cudaSuccess) return from_cuda(ce);
   a.mode = kDown;
-  a.A = Hb;
+  a.A = w.H;
+  a.A_scales = w.Hs;
   a.B = w2;
+  a.B_scales = w2_scales;
+  a.out_scales = nullptr;
   a.out = y_b;
   return from_cuda(launch_grouped_gemm(a, sms, s));
 }

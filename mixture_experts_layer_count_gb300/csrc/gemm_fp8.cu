@@ -89,7 +89,9 @@ struct Layout {
 };
 
 struct KParams {
-  const int32_t *offsets;
+  const int32_t *offsets;   // Standard: expert e owns rows [offsets[e], offsets[e+1])
+  const int32_t *counts;    // Batched (offsets NULL): rows [e*T, e*T + min(counts[e], T))
+  int T;
   int E, N, K;
   int n_tiles;
   int num_kb;
@@ -98,7 +100,7 @@ struct KParams {
   float *out_scales;        // gate/up: H scales (N/128, scale_ld)
   int64_t scale_ld;
   const float *b_scales;    // (E, b_rows/128, num_kb)
-  const int32_t *sorted;
+  const int32_t *sorted;    // down: output row of each row of A (NULL: the row itself)
   const float *topk_w;
   int32_t *err;
 };
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(Layout<MODE>::threads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
 
-  tile_table_fill(p.offsets, nullptr, E, 0, p.n_tiles, prefix, rbase, rcnt, p.err);
+  tile_table_fill(p.offsets, p.counts, E, p.T, p.n_tiles, prefix, rbase, rcnt, p.err);
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
@@ -338,8 +340,9 @@ __global__ void __launch_bounds__(Layout<MODE>::threads, 1)
     };
     // down: the output row (pair) of this thread's row and its router weight
     auto row_pair = [&](int te, int tmt) -> int {
-      return tmt * kBM + row_in_tile < rcnt[te] ? __ldg(p.sorted + rbase[te] + tmt * kBM + row_in_tile)
-                                                : -1;
+      if (tmt * kBM + row_in_tile >= rcnt[te]) return -1;
+      const int r = rbase[te] + tmt * kBM + row_in_tile;
+      return p.sorted ? __ldg(p.sorted + r) : r;
     };
     // a tile is decoded once, as the next tile of the previous iteration
     int ce = 0, cmt = 0, cnt = 0;
@@ -522,7 +525,7 @@ cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
   const int Kd = gate_up ? a.K : a.N;
   const int b_rows = gate_up ? 2 * a.N : a.K;
   const int num_kb = Kd / kBK;
-  if (num_kb > kMaxKB || !a.offsets || a.scale_ld % 4 != 0 || a.scale_ld < a.a_rows)
+  if (num_kb > kMaxKB || a.scale_ld % 4 != 0 || a.scale_ld < a.a_rows)
     return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB, tmAS;
   if (!encode_tmap_2d(&tmA, a.A, kTmapU8, (uint64_t)Kd, (uint64_t)a.a_rows, (uint64_t)Kd,
@@ -534,6 +537,8 @@ cudaError_t launch_fp8(const GroupedGemmArgs &a, int num_sms, cudaStream_t s) {
     return cudaErrorInvalidValue;
   KParams p;
   p.offsets = a.offsets;
+  p.counts = a.counts;
+  p.T = a.T;
   p.E = a.E;
   p.N = a.N;
   p.K = a.K;

@@ -34,6 +34,9 @@ cudaError_t launch_gather_rows(const void *x, const float *xs, const float *row_
                                const int32_t *total, int P, int topk,
                                void *out, float *out_s, int64_t out_s_ld,
                                int num_sms, cudaStream_t s);
+// row-major (rows, G) fp32 -> group-major (G, ld), ld >= rows; G <= 128
+cudaError_t launch_scales_group_major(const float *in, int64_t rows, int G, float *out,
+                                      int64_t ld, int num_sms, cudaStream_t s);
 cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
                           int topk, int K, uint16_t *out, int num_sms,
                           cudaStream_t s);

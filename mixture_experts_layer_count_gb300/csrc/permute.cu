@@ -287,6 +287,27 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Row-major scales (rows, G) -> group-major (G, ld): 32 rows at a time
+// through shared memory, so both the reads (a run of 32 * G floats) and the
+// writes (32 consecutive floats of each of the G groups) are coalesced.
+__global__ void __launch_bounds__(256)
+    scales_group_major_kernel(const float *__restrict__ in, int64_t rows, int G,
+                              float *__restrict__ out, int64_t ld) {
+  extern __shared__ float tile[];  // [32][G + 1]
+  const int gp = G + 1;
+  for (int64_t r0 = (int64_t)blockIdx.x * 32; r0 < rows; r0 += (int64_t)gridDim.x * 32) {
+    const int nr = (int)(rows - r0 < 32 ? rows - r0 : 32);
+    for (int i = threadIdx.x; i < nr * G; i += blockDim.x)
+      tile[(i / G) * gp + i % G] = in[r0 * G + i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < 32 * G; i += blockDim.x) {
+      const int g = i >> 5, r = i & 31;
+      if (r < nr) out[(int64_t)g * ld + r0 + r] = tile[r * gp + g];
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_count(const int32_t *ids, int P, int Eg, const int32_t *map,
@@ -352,6 +373,15 @@ cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
     reduce_kernel<4><<<(unsigned)blocks, 256, 0, s>>>(y, inv, M, topk, kvec, o);
   else
     reduce_kernel<8><<<(unsigned)blocks, 256, 0, s>>>(y, inv, M, topk, kvec, o);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scales_group_major(const float *in, int64_t rows, int G, float *out,
+                                      int64_t ld, int num_sms, cudaStream_t s) {
+  int64_t blocks = (rows + 31) / 32;
+  if (blocks > 4 * num_sms) blocks = 4 * num_sms;
+  if (blocks < 1) blocks = 1;
+  scales_group_major_kernel<<<(int)blocks, 256, (size_t)32 * (G + 1) * 4, s>>>(in, rows, G, out, ld);
   return cudaGetLastError();
 }
 

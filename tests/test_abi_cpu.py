@@ -46,7 +46,14 @@ def test_workspace_sizes():
         P * K * 2, P * N * 2, P * K * 2))  # A, H, y_slot
     assert n == expect
     assert g.moe_workspace_size(g.WS_FORWARD, M, E, 100, K, k, g.BF16) == 0  # N % 128
-    assert g.moe_workspace_size(g.WS_BATCHED, 16, 4, 128, 256, 1, g.FP8_E4M3) == 0
+    # batched: H (E*T, N) in the operand type; for e4m3 also H's and x_b's
+    # group-major scales with E*T rounded up to 4 rows
+    T, E, N, K = 15, 4, 256, 384
+    R, ld = E * T, (E * T + 3) // 4 * 4
+    assert g.moe_workspace_size(g.WS_BATCHED, T, E, N, K, 1, g.BF16) == -(-R * N * 2 // 256) * 256
+    assert g.moe_workspace_size(g.WS_BATCHED, T, E, N, K, 1, g.FP8_E4M3) == sum(
+        -(-b // 256) * 256 for b in (R * N, ld * (N // 128) * 4, ld * (K // 128) * 4))
+    assert g.moe_workspace_size(g.WS_BATCHED, T, E, N, K, 1, g.FP8_E4M3_CHANNEL) == 0
     assert g.moe_workspace_size(g.WS_ALIGN, 8192, 256, 0, 0, 8, 0) == 32 * 256 * 4
     # EP dispatch (M tokens per shard, E routed experts, N = G shards): the
     # pairs' ids, the map, counts, offsets, sorted, inv, chunk histograms
@@ -161,7 +168,13 @@ def test_gemm_calls_reject_bad_arguments(lib):
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 33, 256, P16, None) == INVALID
     b = lib.moe_batched_masked_experts
     #        xb  xbs   cnt E  T   N    K    w1   w1s  w2   w2s  dt ac yb   ws   wsb  err  s
-    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 1, 0, P16, P16, 1 << 30, None, None) == UNSUPPORTED
+    assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 2, 0, P16, P16, 1 << 30, None, None) == UNSUPPORTED
+    # e4m3 with block scales: all three scale arrays are required, x_b's 4-byte aligned
+    assert b(P16, None, P16, 4, 16, 128, 256, P16, P16, P16, P16, 1, 0, P16, P16, 1 << 30, None, None) == INVALID
+    assert b(P16, P16, P16, 4, 16, 128, 256, P16, None, P16, P16, 1, 0, P16, P16, 1 << 30, None, None) == INVALID
+    assert b(P16, P16, P16, 4, 16, 128, 256, P16, P16, P16, None, 1, 0, P16, P16, 1 << 30, None, None) == INVALID
+    assert b(P16, P16 + 2, P16, 4, 16, 128, 256, P16, P16, P16, P16, 1, 0, P16, P16, 1 << 30, None, None) == INVALID
+    assert b(P16, P16, P16, 4, 16, 128, 256, P16, P16, P16, P16, 1, 0, P16, P16, 1000, None, None) == INVALID
     assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 0, 0, P16, P16, 16, None, None) == INVALID
     assert b(P16, None, None, 4, 16, 128, 256, P16, None, P16, None, 0, 0, P16, P16, 1 << 30, None, None) == INVALID
     assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 0, 5, P16, P16, 1 << 30, None, None) == INVALID

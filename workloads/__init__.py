@@ -74,6 +74,10 @@ DSV3_DECODE = MoEConfig("dsv3_decode_bf16_M64_K7168_N2048_E256_top8",
 BATCHED_MASKED = MoEConfig("batched_masked_bf16_E32_T1024_K7168_N2048",
                            M=1024, K=7168, N=2048, E=32, topk=1, batched=True,
                            seed=5000)
+# the same shapes with e4m3 activations and block-scaled weights
+BATCHED_MASKED_FP8 = MoEConfig("batched_masked_fp8_E32_T1024_K7168_N2048",
+                               M=1024, K=7168, N=2048, E=32, topk=1, batched=True,
+                               dtype=FP8, seed=6000)
 
 # Smaller cases of the same kinds, for parity tests that the oracle finishes in
 # seconds while still spanning several tiles and a ragged tail.
@@ -106,6 +110,13 @@ SMALL_FP8_NARROW = MoEConfig("small_fp8_narrow_M48_K640_N256_E8_top2", M=48, K=6
                              E=8, topk=2, dtype=FP8, seed=29)
 SMALL_BATCHED_SHORT = MoEConfig("small_batched_bf16_E5_T100_K384_N256", M=100, K=384,
                                 N=256, E=5, topk=1, batched=True, seed=17)
+# the BatchedExperts format with e4m3 activations (1 x 128 group scales) and
+# block-scaled weights: several m-tiles per expert, and T < 128 with K = 640
+# (the last down tile's second half lies past K)
+SMALL_BATCHED_FP8 = MoEConfig("small_batched_fp8_E6_T300_K256_N256", M=300, K=256,
+                              N=256, E=6, topk=1, batched=True, dtype=FP8, seed=41)
+SMALL_BATCHED_FP8_K640 = MoEConfig("small_batched_fp8_E5_T100_K640_N256", M=100, K=640,
+                                   N=256, E=5, topk=1, batched=True, dtype=FP8, seed=42)
 
 # e4m3 with per-token / per-channel scales: a small sigmoid-routed case with
 # 64 rows per expert, one with 150 rows per expert and K = 640, and the
@@ -157,7 +168,8 @@ BY_NAME = {c.name: c for c in ALL + [SMALL_BF16, SMALL_SIGMOID, SMALL_FP8,
                                      SMALL_FP8CH, SMALL_FP8CH_PAIR, DSV3_PREFILL_FP8CH,
                                      PROFILE_FP8CH, SMALL_FP8T, MID_FP8T, DSV3_PREFILL_FP8T,
                                      SMALL_BATCHED_SHORT, PROFILE_BF16, PROFILE_FP8, PROFILE_DECODE,
-                                     PROFILE_BATCHED, SMALL_FP8_NARROW]}
+                                     PROFILE_BATCHED, SMALL_FP8_NARROW, SMALL_BATCHED_FP8,
+                                     SMALL_BATCHED_FP8_K640, BATCHED_MASKED_FP8]}
 
 
 def _gen(seed: int, device) -> torch.Generator:
