@@ -12,7 +12,8 @@
 // row and 128 columns (4 lane quarters x 2 column halves cover the 128 x 256
 // tile: for gate/up the gate and up columns of 64 outputs), so the promotion
 // is 64 packed FFMA2 per thread per K block, in 16-column TMEM loads; at 320
-// threads a thread has 168 registers, enough for its 128 accumulators.  The
+// threads (352 in down mode, with the store warp below) a thread has 168
+// registers, enough for its 128 accumulators.  The
 // per-row scales of a K block travel with the operand tiles: the producer
 // loads them by TMA from the group-major scale array (one contiguous run of
 // rows per K block) into the stage's shared memory; the weight-block scales
@@ -21,7 +22,9 @@
 // gate/up ends with h = silu(gate) * up and the e4m3 requantisation of h in
 // 128-wide groups (one scale per row and n-tile; the row maximum is
 // exchanged between the two warps holding that row); down ends with the
-// router weight and bf16 stores into the (token, slot) rows (the ordered
+// router weight and bf16 stores into the (token, slot) rows, or unweighted
+// into the row itself in the BatchedExperts format (row groups from the
+// device counts, e*T + [0, count)) (the ordered
 // top-k reduce is a pass of its own after this kernel: added to this
 // epilogue it stalled the per-K-block pipeline, 1.8 -> 4.3 ms on the
 // DeepSeek-V3-shaped prefill).
