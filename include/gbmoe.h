@@ -463,12 +463,12 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
 /* Expert-parallel dispatch in the worst-tokens mode of "EP: CUDA-graph-safe
  * HT internode dispatch+combine (worst-tokens mode)" (uccl pull request 7 and
  * the vLLM commit message under it), for G shards whose buffers are in this
- * GPU's memory.  Shard r (r < G) holds tokens x[r] (M, K) bf16, of which the
+ * GPU's memory.  Shard r (r < G) holds tokens x[r] (M, K), of which the
  * first num_tokens[r] (a DEVICE int32, clamped to [0, M]) are valid, with
  * their routed expert ids topk_ids[r] (M, topk) int32 in [0, E).  Shard g
  * owns the E / G experts [g*E/G, (g+1)*E/G).  Each valid (token, slot) pair
  * goes to the receive block of its expert:
- *   recv_x (E, worst_tokens, K) bf16: recv_x[e, pos] = x[r, t] for the pos-th
+ *   recv_x (E, worst_tokens, K): recv_x[e, pos] = x[r, t] for the pos-th
  *     pair routed to e, pairs taken in ascending order of (r, t, slot);
  *     the E/G experts of shard g are rows [g*E/G, (g+1)*E/G): that shard's
  *     static worst-case receive buffer, in the BatchedExperts layout;
@@ -485,14 +485,24 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
  * GBMOE_ERR_COUNT_RANGE set.  Rows of recv_x at and beyond a count are not
  * written.  No count is read on the host and no loop runs over the padded
  * shapes: the whole call is capturable.
+ * dtype GBMOE_BF16: x (G, M, K) and recv_x bf16; x_scales, recv_scales
+ *   ignored.
+ * dtype GBMOE_FP8_E4M3 (the tokens quantised before the dispatch, as the
+ *   prepare step does): x (G, M, K) e4m3 codes with x_scales (G*M, K/128)
+ *   fp32, one per token and 128-group (moe_quant_fp8_group's layout), and
+ *   recv_x (E, worst_tokens, K) e4m3 with recv_scales (E*worst_tokens,
+ *   K/128) fp32: each row's scales travel with its codes, in the layout
+ *   moe_batched_masked_experts takes for e4m3 (pass recv_scales +
+ *   g*(E/G)*worst_tokens*(K/128) for shard g).  K a multiple of 128.
  * ws: moe_workspace_size(GBMOE_WS_EP_DISPATCH, M, E, G, K, topk, 0) bytes,
  * 16-byte aligned.  K a multiple of 8, E a multiple of G; x and recv_x
- * 16-byte aligned.  err_word may be NULL.  On several GPUs each shard's
- * receive block would live on its own GPU and the row copies would be
- * peer stores; this call is the single-GPU form. */
-gbmoe_status_t moe_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
-                               const int32_t *topk_ids, int G, int M, int K, int E,
-                               int topk, int worst_tokens, uint16_t *recv_x,
+ * 16-byte aligned, the scales 4-byte aligned.  err_word may be NULL.  On
+ * several GPUs each shard's receive block would live on its own GPU and the
+ * row copies would be peer stores; this call is the single-GPU form. */
+gbmoe_status_t moe_ep_dispatch(const void *x, const float *x_scales,
+                               const int32_t *num_tokens, const int32_t *topk_ids,
+                               int G, int M, int K, int E, int topk, int worst_tokens,
+                               int dtype, void *recv_x, float *recv_scales,
                                int32_t *recv_counts, int32_t *recv_pos, void *ws,
                                size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream);
 

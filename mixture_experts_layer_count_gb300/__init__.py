@@ -67,7 +67,8 @@ _SIGS = {
     "moe_grouped_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                                    _I, _P, _P, _P]),
     "moe_unpermute_weighted_reduce": (_I, [_P, _P, _I, _I, _I, _P, _P]),
-    "moe_ep_dispatch": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P, _P]),
+    "moe_ep_dispatch": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                             _Z, _P, _P]),
     "moe_ep_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_batched_masked_experts": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                         _I, _I, _P, _P, _Z, _P, _P]),
@@ -234,15 +235,19 @@ def moe_grouped_gemm_down(H, H_scales, sorted_pair_ids, offsets, topk_weights,
 
 
 def moe_ep_dispatch(x, num_tokens, topk_ids, E, worst_tokens, recv_x, recv_counts, recv_pos,
-                    ws, err_word=None, stream=None):
-    """x (G, M, K) bf16, num_tokens (G) int32, topk_ids (G, M, topk) int32;
-    recv_x (E, worst_tokens, K), recv_counts (E), recv_pos (G, M, topk)."""
+                    ws, err_word=None, stream=None, dtype=BF16, x_scales=None,
+                    recv_scales=None):
+    """x (G, M, K) bf16, or e4m3 codes with x_scales (G*M, K/128); num_tokens
+    (G) int32, topk_ids (G, M, topk) int32; recv_x (E, worst_tokens, K)
+    [+ recv_scales (E*worst_tokens, K/128)], recv_counts (E), recv_pos
+    (G, M, topk)."""
     G, M, K = x.shape
     topk = topk_ids.shape[-1]
     _check("moe_ep_dispatch", load().moe_ep_dispatch(
-        _ptr(x), _ptr(num_tokens), _ptr(topk_ids), G, M, K, E, topk, worst_tokens,
-        _ptr(recv_x), _ptr(recv_counts), _ptr(recv_pos), _ptr(ws),
-        ws.numel() * ws.element_size(), _ptr(err_word), _stream(stream)))
+        _ptr(x), _ptr(x_scales), _ptr(num_tokens), _ptr(topk_ids), G, M, K, E, topk,
+        worst_tokens, dtype, _ptr(recv_x), _ptr(recv_scales), _ptr(recv_counts),
+        _ptr(recv_pos), _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
+        _stream(stream)))
 
 
 def moe_ep_combine(recv_y, topk_ids, recv_pos, topk_weights, num_tokens, out, stream=None):

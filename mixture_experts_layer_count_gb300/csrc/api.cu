@@ -504,14 +504,21 @@ gbmoe_status_t moe_grouped_gemm_down(
                    (cudaStream_t)stream);
 }
 
-gbmoe_status_t moe_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
-                               const int32_t *topk_ids, int G, int M, int K, int E,
-                               int topk, int worst_tokens, uint16_t *recv_x,
+gbmoe_status_t moe_ep_dispatch(const void *x, const float *x_scales,
+                               const int32_t *num_tokens, const int32_t *topk_ids,
+                               int G, int M, int K, int E, int topk, int worst_tokens,
+                               int dtype, void *recv_x, float *recv_scales,
                                int32_t *recv_counts, int32_t *recv_pos, void *ws,
                                size_t ws_bytes, int32_t *err_word, gbmoe_stream_t stream) {
-  if (!ep_shape_ok(G, M, K, E, topk, worst_tokens)) return GBMOE_INVALID_ARG;
+  if (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3) return GBMOE_UNSUPPORTED;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  if (!ep_shape_ok(G, M, K, E, topk, worst_tokens) || (fp8 && K % 128 != 0))
+    return GBMOE_INVALID_ARG;
   if (M > 0) {
     if (!x || !num_tokens || !topk_ids || !recv_x || !recv_counts || !recv_pos || !ws)
+      return GBMOE_INVALID_ARG;
+    if (fp8 && (!x_scales || !recv_scales || (reinterpret_cast<uintptr_t>(x_scales) & 3u) ||
+                (reinterpret_cast<uintptr_t>(recv_scales) & 3u)))
       return GBMOE_INVALID_ARG;
     if (!aligned16(x) || !aligned16(recv_x) || !aligned16(ws)) return GBMOE_INVALID_ARG;
     if (ws_bytes < moe_workspace_size(GBMOE_WS_EP_DISPATCH, M, E, G, K, topk, 0))
@@ -525,8 +532,10 @@ gbmoe_status_t moe_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
     return from_cuda(cudaMemsetAsync(recv_counts, 0, (size_t)E * 4, s));
   Carver c(ws);
   EpWorkspace w = carve_ep(c, G, M, E, topk);
-  return from_cuda(launch_ep_dispatch(x, num_tokens, topk_ids, G, M, K, E, topk, worst_tokens,
-                                      recv_x, recv_counts, recv_pos, w, err_word, sms, s));
+  return from_cuda(launch_ep_dispatch(x, fp8 ? x_scales : nullptr, num_tokens, topk_ids, G, M, K,
+                                      (int)elem_bytes(dtype) * K, E, topk, worst_tokens, recv_x,
+                                      fp8 ? recv_scales : nullptr, recv_counts, recv_pos, w,
+                                      err_word, sms, s));
 }
 
 gbmoe_status_t moe_ep_combine(const uint16_t *recv_y, const int32_t *topk_ids,

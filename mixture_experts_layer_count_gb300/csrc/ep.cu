@@ -18,6 +18,10 @@
 // num_tokens), and nothing waits on another launch or on the host, so both
 // calls can be captured in a CUDA graph and replayed with fresh data.
 //
+// With e4m3 tokens (quantised before the dispatch, as the prepare step does)
+// each row's 1 x 128 group scales travel with its codes into a receive block
+// of scales laid out like the rows.
+//
 // The counting sort is the one of moe_align_permute (permute.cu), run over
 // the concatenated pairs of all shards with padded tokens mapped to "not
 // routed here" (skipped without an error).
@@ -81,12 +85,15 @@ __global__ void __launch_bounds__(256)
 }
 
 // recv_x[e, pos] = x[token of pair] for the sorted positions below the
-// device total offsets[E]: one warp per row, 16-byte vectors.
+// device total offsets[E]: one warp per row, 16-byte vectors; e4m3 rows
+// bring their n_scales group scales along (xs NULL: none).
 __global__ void __launch_bounds__(256)
-    ep_dispatch_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ sorted,
+    ep_dispatch_rows_kernel(const uint4 *__restrict__ x, const float *__restrict__ xs,
+                            const int32_t *__restrict__ sorted,
                             const int32_t *__restrict__ ids_eff,
                             const int32_t *__restrict__ offsets, int E, int topk, int worst,
-                            int row_vecs, uint4 *__restrict__ recv_x) {
+                            int row_vecs, int n_scales, uint4 *__restrict__ recv_x,
+                            float *__restrict__ recv_s) {
   const int lane = threadIdx.x & 31;
   const int total = offsets[E];
   for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < total;
@@ -95,9 +102,12 @@ __global__ void __launch_bounds__(256)
     const int e = ids_eff[p];
     const int pos = i - offsets[e];
     if (pos >= worst) continue;  // beyond the static shape: dropped (flagged)
-    const uint4 *src = x + (size_t)(p / topk) * row_vecs;
-    uint4 *dst = recv_x + ((size_t)e * worst + pos) * row_vecs;
+    const size_t tok = (size_t)(p / topk), slot = (size_t)e * worst + pos;
+    const uint4 *src = x + tok * row_vecs;
+    uint4 *dst = recv_x + slot * row_vecs;
     for (int v = lane; v < row_vecs; v += 32) dst[v] = src[v];
+    if (xs)
+      for (int j = lane; j < n_scales; j += 32) recv_s[slot * n_scales + j] = xs[tok * n_scales + j];
   }
 }
 
@@ -147,11 +157,11 @@ int grid_for(size_t work, int per_block, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
-                               const int32_t *topk_ids, int R, int M, int K, int E, int topk,
-                               int worst, uint16_t *recv_x, int32_t *recv_counts,
-                               int32_t *recv_pos, const EpWorkspace &w, int32_t *err,
-                               int num_sms, cudaStream_t s) {
+cudaError_t launch_ep_dispatch(const void *x, const float *xs, const int32_t *num_tokens,
+                               const int32_t *topk_ids, int R, int M, int K, int row_bytes,
+                               int E, int topk, int worst, void *recv_x, float *recv_s,
+                               int32_t *recv_counts, int32_t *recv_pos, const EpWorkspace &w,
+                               int32_t *err, int num_sms, cudaStream_t s) {
   const size_t P = (size_t)R * M * topk;
   ep_mask_kernel<<<grid_for(P, 256, num_sms), 256, 0, s>>>(topk_ids, num_tokens, R, M, topk, E,
                                                           w.ids_eff, w.map);
@@ -165,8 +175,8 @@ cudaError_t launch_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
   st = cudaGetLastError();
   if (st != cudaSuccess) return st;
   ep_dispatch_rows_kernel<<<grid_for(P, 8, num_sms), 256, 0, s>>>(
-      reinterpret_cast<const uint4 *>(x), w.sorted, w.ids_eff, w.offsets, E, topk, worst, K / 8,
-      reinterpret_cast<uint4 *>(recv_x));
+      static_cast<const uint4 *>(x), xs, w.sorted, w.ids_eff, w.offsets, E, topk, worst,
+      row_bytes / 16, K / 128, static_cast<uint4 *>(recv_x), recv_s);
   return cudaGetLastError();
 }
 

@@ -51,11 +51,13 @@ struct EpWorkspace {
   int32_t *inv;         // (G*M*topk)
   int32_t *chunk_hist;  // (align_num_chunks(G*M*topk) * E)
 };
-cudaError_t launch_ep_dispatch(const uint16_t *x, const int32_t *num_tokens,
-                               const int32_t *topk_ids, int G, int M, int K, int E, int topk,
-                               int worst, uint16_t *recv_x, int32_t *recv_counts,
-                               int32_t *recv_pos, const EpWorkspace &w, int32_t *err,
-                               int num_sms, cudaStream_t s);
+// rows of row_bytes (a multiple of 16); xs / recv_s: e4m3 group scales
+// (K/128 per row) carried with the rows, or NULL
+cudaError_t launch_ep_dispatch(const void *x, const float *xs, const int32_t *num_tokens,
+                               const int32_t *topk_ids, int G, int M, int K, int row_bytes,
+                               int E, int topk, int worst, void *recv_x, float *recv_s,
+                               int32_t *recv_counts, int32_t *recv_pos, const EpWorkspace &w,
+                               int32_t *err, int num_sms, cudaStream_t s);
 cudaError_t launch_ep_combine(const uint16_t *recv_y, const int32_t *topk_ids,
                               const int32_t *recv_pos, const float *topk_weights,
                               const int32_t *num_tokens, int G, int M, int K, int E, int topk,

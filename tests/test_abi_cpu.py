@@ -153,13 +153,18 @@ def test_gemm_calls_reject_bad_arguments(lib):
     assert pr(P16, P16, P16, P16, P16, 8, 1, 8, 256, 1, P16, P16, None) == INVALID
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 2, 12, P16, None) == INVALID
     ed = lib.moe_ep_dispatch
-    #         x    ntok ids  G  M   K    E   k  worst rx   rc   rp   ws   wsb      err   s
-    assert ed(P16, P16, P16, 3, 16, 256, 32, 4, 48, P16, P16, P16, P16, 1 << 20, None, None) == INVALID  # E % G
-    assert ed(P16, P16, P16, 2, 16, 250, 32, 4, 32, P16, P16, P16, P16, 1 << 20, None, None) == INVALID  # K % 8
-    assert ed(P16, P16, P16, 2, 16, 256, 32, 4, 32, P16, P16, P16, P16, 16, None, None) == INVALID       # ws too small
-    assert ed(P16, None, P16, 2, 16, 256, 32, 4, 32, P16, P16, P16, P16, 1 << 20, None, None) == INVALID  # no counts
-    assert ed(P_ODD, P16, P16, 2, 16, 256, 32, 4, 32, P16, P16, P16, P16, 1 << 20, None, None) == INVALID
-    assert ed(P16, P16, P16, 2, 16, 256, 32, 33, 32, P16, P16, P16, P16, 1 << 20, None, None) == INVALID  # topk
+    #         x    xs    ntok ids  G  M   K    E   k  worst dt rx   rs    rc   rp   ws   wsb      err   s
+    assert ed(P16, None, P16, P16, 3, 16, 256, 32, 4, 48, 0, P16, None, P16, P16, P16, 1 << 20, None, None) == INVALID  # E % G
+    assert ed(P16, None, P16, P16, 2, 16, 250, 32, 4, 32, 0, P16, None, P16, P16, P16, 1 << 20, None, None) == INVALID  # K % 8
+    assert ed(P16, None, P16, P16, 2, 16, 256, 32, 4, 32, 0, P16, None, P16, P16, P16, 16, None, None) == INVALID       # ws too small
+    assert ed(P16, None, None, P16, 2, 16, 256, 32, 4, 32, 0, P16, None, P16, P16, P16, 1 << 20, None, None) == INVALID  # no counts
+    assert ed(P_ODD, None, P16, P16, 2, 16, 256, 32, 4, 32, 0, P16, None, P16, P16, P16, 1 << 20, None, None) == INVALID
+    assert ed(P16, None, P16, P16, 2, 16, 256, 32, 33, 32, 0, P16, None, P16, P16, P16, 1 << 20, None, None) == INVALID  # topk
+    assert ed(P16, None, P16, P16, 2, 16, 256, 32, 4, 32, 2, P16, None, P16, P16, P16, 1 << 20, None, None) == UNSUPPORTED
+    # e4m3: both scale arrays, K a multiple of 128
+    assert ed(P16, None, P16, P16, 2, 16, 256, 32, 4, 32, 1, P16, P16, P16, P16, P16, 1 << 20, None, None) == INVALID
+    assert ed(P16, P16, P16, P16, 2, 16, 256, 32, 4, 32, 1, P16, None, P16, P16, P16, 1 << 20, None, None) == INVALID
+    assert ed(P16, P16, P16, P16, 2, 16, 192, 32, 4, 32, 1, P16, P16, P16, P16, P16, 1 << 20, None, None) == INVALID
     ec = lib.moe_ep_combine
     #         ry   ids  pos  w    ntok G  M   K    E   k  worst out  s
     assert ec(P16, P16, P16, P16, P16, 2, 16, 256, 32, 4, 0, P16, None) == INVALID    # worst < 1

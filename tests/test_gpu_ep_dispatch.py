@@ -29,11 +29,13 @@ def _lib():
 
 
 class EpLayer:
-    """Static buffers of the sharded layer and its launch sequence."""
+    """Static buffers of the sharded layer and its launch sequence (bf16, or
+    e4m3: tokens quantised per 128-group before the dispatch, block-scaled
+    weights)."""
 
-    def __init__(self, cfg, w1, w2):
+    def __init__(self, cfg, w1, w2, dtype=WL.BF16):
         g = gbmoe()
-        self.cfg, self.g = cfg, g
+        self.cfg, self.g, self.dtype = cfg, g, dtype
         G, M, K, N, E, k = cfg.G, cfg.M, cfg.K, cfg.N, cfg.E, cfg.topk
         W = cfg.worst_tokens
         i32 = torch.int32
@@ -42,7 +44,20 @@ class EpLayer:
         self.num_tokens = torch.empty(G, dtype=i32, device=DEV)
         self.ids = torch.empty((G, M, k), dtype=i32, device=DEV)
         self.wts = torch.empty((G, M, k), dtype=torch.float32, device=DEV)
-        self.recv_x = torch.empty((E, W, K), dtype=torch.bfloat16, device=DEV)
+        fp8 = dtype == WL.FP8
+        self.recv_x = torch.empty((E, W, K), dtype=torch.uint8 if fp8 else torch.bfloat16,
+                                  device=DEV)
+        if fp8:
+            self.xq = torch.empty((G, M, K), dtype=torch.uint8, device=DEV)
+            self.xs = torch.empty((G * M, K // 128), dtype=torch.float32, device=DEV)
+            self.recv_s = torch.empty((E * W, K // 128), dtype=torch.float32, device=DEV)
+            q1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=DEV)
+            q2 = torch.empty((E, K, N), dtype=torch.uint8, device=DEV)
+            s1 = torch.empty((E, 2 * N // 128, K // 128), dtype=torch.float32, device=DEV)
+            s2 = torch.empty((E, K // 128, N // 128), dtype=torch.float32, device=DEV)
+            g.moe_quant_fp8_block(w1, q1, s1)
+            g.moe_quant_fp8_block(w2, q2, s2)
+            w1, w2 = q1, q2
         self.recv_y = torch.empty((E, W, K), dtype=torch.bfloat16, device=DEV)
         self.recv_counts = torch.empty(E, dtype=i32, device=DEV)
         self.recv_pos = torch.empty((G, M, k), dtype=i32, device=DEV)
@@ -53,20 +68,32 @@ class EpLayer:
         self.El = El
         self.w1 = [w1[s * El:(s + 1) * El] for s in range(G)]
         self.w2 = [w2[s * El:(s + 1) * El] for s in range(G)]
-        self.bws = [g.workspace(g.WS_BATCHED, W, El, N, K, 1, WL.BF16) for _ in range(G)]
+        self.kw = [{} for _ in range(G)]
+        if fp8:
+            for s_ in range(G):
+                self.kw[s_] = dict(dtype=WL.FP8, x_b_scales=self.recv_s[s_ * El * W:(s_ + 1) * El * W],
+                                   w1_scales=s1[s_ * El:(s_ + 1) * El],
+                                   w2_scales=s2[s_ * El:(s_ + 1) * El])
+        self.bws = [g.workspace(g.WS_BATCHED, W, El, N, K, 1, dtype) for _ in range(G)]
 
     def step(self):
         c, g = self.cfg, self.g
         G, M, E, k = c.G, c.M, c.E, c.topk
         g.moe_topk_route(self.logits.view(G * M, E), None, k, c.score_fn, c.n_groups,
                          c.topk_groups, True, self.ids.view(G * M, k), self.wts.view(G * M, k))
-        g.moe_ep_dispatch(self.x, self.num_tokens, self.ids, E, c.worst_tokens, self.recv_x,
-                          self.recv_counts, self.recv_pos, self.ws, self.err)
+        if self.dtype == WL.FP8:
+            g.moe_quant_fp8_group(self.x.view(G * M, c.K), self.xq.view(G * M, c.K), self.xs)
+            g.moe_ep_dispatch(self.xq, self.num_tokens, self.ids, E, c.worst_tokens, self.recv_x,
+                              self.recv_counts, self.recv_pos, self.ws, self.err, dtype=WL.FP8,
+                              x_scales=self.xs, recv_scales=self.recv_s)
+        else:
+            g.moe_ep_dispatch(self.x, self.num_tokens, self.ids, E, c.worst_tokens, self.recv_x,
+                              self.recv_counts, self.recv_pos, self.ws, self.err)
         for s in range(G):  # each shard's masked grouped GEMMs on its own receive block
             sl = slice(s * self.El, (s + 1) * self.El)
             g.moe_batched_masked_experts(self.recv_x[sl], self.recv_counts[sl], c.N, self.w1[s],
                                          self.w2[s], self.recv_y[sl], self.bws[s],
-                                         err_word=self.err)
+                                         err_word=self.err, **self.kw[s])
         g.moe_ep_combine(self.recv_y, self.ids, self.recv_pos, self.wts, self.num_tokens,
                          self.out)
 
@@ -77,7 +104,7 @@ class EpLayer:
         self.out.view(torch.int16).fill_(SENTINEL)
 
 
-def _oracle_check(cfg, layer, d, W):
+def _oracle_check(cfg, layer, d, W, dtype=WL.BF16):
     n = d["num_tokens"].cpu().numpy()
     G, M, E, k = cfg.G, cfg.M, cfg.E, cfg.topk
     xv = torch.cat([d["x"][r, :n[r]] for r in range(G)])
@@ -99,9 +126,10 @@ def _oracle_check(cfg, layer, d, W):
         assert np.all(gpos[r, n[r]:] == -1)
     # values: the layer over all experts, token by token
     ref, rid2, _ = orc.moe_forward(WL.bf16_bits(xv), lv, None, k, cfg.score_fn, W,
-                                   cfg.n_groups, cfg.topk_groups, True)
+                                   cfg.n_groups, cfg.topk_groups, True,
+                                   requant_h=dtype == WL.FP8)
     got = torch.cat([layer.out[r, :n[r]] for r in range(G)]).float().cpu().numpy()
-    assert_close_rel(got, ref, TOL[WL.BF16], cfg.name)
+    assert_close_rel(got, ref, TOL[dtype], cfg.name)
     bits = layer.out.view(torch.int16).cpu().numpy()
     for r in range(G):
         assert np.all(bits[r, n[r]:] == np.int16(SENTINEL)), f"shard {r}: padded rows written"
@@ -138,6 +166,58 @@ def test_ep_worst_tokens_graph_replays(cfg, replays):
             assert torch.equal(a, b), f"replay {r}: {name} differs from the eager run"
         if r % 5 == 0:
             _oracle_check(cfg, layer, dr, W)
+
+
+def test_ep_worst_tokens_fp8_graph_replays():
+    """The same sharded layer with the tokens quantised to e4m3 (1 x 128
+    group scales) before the dispatch, the scales carried with the rows, and
+    block-scaled e4m3 experts on each shard: 20 replays, each equal to the
+    eager run bit for bit (receive rows and scales included), every fifth
+    against the oracle's e4m3 layer (h requantised)."""
+    cfg = WL.EP2
+    d0 = WL.make_ep_inputs(cfg, DEV)
+    layer = EpLayer(cfg, d0["w1"], d0["w2"], WL.FP8)
+    W = oracle_weights(WL.MoEConfig("ep_all_fp8", M=1, K=cfg.K, N=cfg.N, E=cfg.E, topk=cfg.topk,
+                                    dtype=WL.FP8), d0["w1"], d0["w2"])
+    layer.load(d0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.step()
+    eager = EpLayer(cfg, d0["w1"], d0["w2"], WL.FP8)
+    for r in range(20):
+        dr = WL.make_ep_inputs(cfg, DEV, seed=cfg.seed * 1000 + 500 + r, with_weights=False)
+        layer.load(dr)
+        graph.replay()
+        eager.load(dr)
+        eager.step()
+        torch.cuda.synchronize()
+        assert layer.err.item() == 0 and eager.err.item() == 0, f"replay {r}"
+        for name in ("out", "recv_counts", "recv_pos", "ids"):
+            a, b = getattr(layer, name), getattr(eager, name)
+            if a.dtype == torch.bfloat16:
+                a, b = a.view(torch.int16), b.view(torch.int16)
+            assert torch.equal(a, b), f"replay {r}: {name} differs from the eager run"
+        # the received rows (codes and scales) below each count agree too
+        cnt = layer.recv_counts.cpu().numpy()
+        for e in range(cfg.E):
+            c = int(cnt[e])
+            assert torch.equal(layer.recv_x[e, :c], eager.recv_x[e, :c]), f"replay {r} expert {e}"
+            row0 = e * cfg.worst_tokens
+            assert torch.equal(layer.recv_s[row0:row0 + c], eager.recv_s[row0:row0 + c])
+        if r % 5 == 0:
+            # every dispatched pair's receive row holds its token's codes and
+            # scales, byte for byte
+            pos, ids = layer.recv_pos, layer.ids
+            sh, tk, _ = torch.nonzero(pos >= 0, as_tuple=True)
+            pe, pp = ids[pos >= 0].long(), pos[pos >= 0].long()
+            assert torch.equal(layer.recv_x[pe, pp], layer.xq[sh, tk])
+            assert torch.equal(layer.recv_s[pe * cfg.worst_tokens + pp], layer.xs[sh * cfg.M + tk])
+            _oracle_check(cfg, layer, dr, W, WL.FP8)
 
 
 def test_ep_dispatch_flags_overflow_of_the_static_shape():
