@@ -61,7 +61,8 @@ typedef enum {
 
 /* element type of activations / weights fed to the expert GEMMs:
  * GBMOE_FP8_E4M3          e4m3 with fp32 block scales: 1 x 128 groups of a
- *                         token's activations, 128 x 128 blocks of weights;
+ *                         token's activations, 128 x 128 blocks of weights
+ *                         (K and N at most 16384 for the GEMMs);
  * GBMOE_FP8_E4M3_CHANNEL  e4m3 with one fp32 scale per token of the
  *                         activations and one per output channel (row) of
  *                         w1 and w2 -- the quant config's

@@ -245,9 +245,14 @@ gbmoe_status_t down_impl(const void *H, const float *H_scales,
   return from_cuda(launch_grouped_gemm(a, num_sms, s));
 }
 
+// K and N of the block-scaled e4m3 GEMMs: the weight-block scales of a tile
+// (two rows of K/128 or N/128 values) are staged in shared memory, 128 each
+constexpr int kMaxFp8BlockK = 16384;
+
 bool gemm_shape_ok(int M, int topk, int E, int N, int K, int dtype) {
   return M >= 0 && topk >= 1 && topk <= kMaxTopk && E >= 1 && E <= kMaxExperts &&
          N >= 128 && K >= 128 && N % 128 == 0 && K % 128 == 0 && valid_dtype(dtype) &&
+         (dtype != GBMOE_FP8_E4M3 || (K <= kMaxFp8BlockK && N <= kMaxFp8BlockK)) &&
          (size_t)M * topk <= (size_t)INT32_MAX && (size_t)E * 2 * N <= (size_t)INT32_MAX &&
          (size_t)E * K <= (size_t)INT32_MAX;
 }

@@ -54,6 +54,11 @@ def test_workspace_sizes():
     assert g.moe_workspace_size(g.WS_BATCHED, T, E, N, K, 1, g.FP8_E4M3) == sum(
         -(-b // 256) * 256 for b in (R * N, ld * (N // 128) * 4, ld * (K // 128) * 4))
     assert g.moe_workspace_size(g.WS_BATCHED, T, E, N, K, 1, g.FP8_E4M3_CHANNEL) == 0
+    # block-scaled e4m3 GEMMs take K and N up to 16384 (128 scale blocks)
+    assert g.moe_workspace_size(g.WS_FORWARD, 4, 2, 128, 16384, 1, g.FP8_E4M3) > 0
+    assert g.moe_workspace_size(g.WS_FORWARD, 4, 2, 128, 16512, 1, g.FP8_E4M3) == 0
+    assert g.moe_workspace_size(g.WS_FORWARD, 4, 2, 16512, 128, 1, g.FP8_E4M3) == 0
+    assert g.moe_workspace_size(g.WS_FORWARD, 4, 2, 16512, 128, 1, g.BF16) > 0
     assert g.moe_workspace_size(g.WS_ALIGN, 8192, 256, 0, 0, 8, 0) == 32 * 256 * 4
     # EP dispatch (M tokens per shard, E routed experts, N = G shards): the
     # pairs' ids, the map, counts, offsets, sorted, inv, chunk histograms
