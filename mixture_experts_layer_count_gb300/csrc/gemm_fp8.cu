@@ -20,8 +20,8 @@
 // of a tile (two rows of K blocks) are staged in shared memory once per tile.
 //
 // gate/up ends with h = silu(gate) * up and the e4m3 requantisation of h in
-// 128-wide groups (one scale per row and n-tile; the row maximum is
-// exchanged between the two warps holding that row); down ends with the
+// 128-wide groups (one scale per row and n-tile, from the maximum of the two
+// half-rows that two warps hold); down ends with the
 // router weight and bf16 stores into the (token, slot) rows, or unweighted
 // into the row itself in the BatchedExperts format (row groups from the
 // device counts, e*T + [0, count)) (the ordered
@@ -33,10 +33,12 @@
 // run only two K blocks into the next tile while the epilogue finishes the
 // current one.  Down tiles are short (K = N, 16 K blocks for N = 2048), and
 // writing 128 scattered output rows per tile from the epilogue stalled the
-// next tile's MMAs for about a third of the tile's time.  So in down mode
-// the epilogue only packs its rows into a shared-memory stage of the whole
-// tile and a store warp writes them out during the next tile; the stage
-// costs the operand ring one of its four stages.
+// next tile's MMAs for about a third of the tile's time.  So the epilogue
+// only puts its rows into a shared-memory stage of the whole tile (down:
+// bf16 rows times the router weight; gate/up: h in fp32 and each half-row's
+// maximum) and an output warp stores them (gate/up: after the scales and the
+// e4m3 codes) during the next tile; the stage costs the operand ring one of
+// four stages.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -61,28 +63,31 @@ constexpr int kASBox = kBM + 4;                 // row scales per K block (rows 
 constexpr int kASStage = 640;                   // bytes per ring slot (528 used)
 constexpr int kASStages = 8;                    // row-scale ring, deeper than the operand ring
 
-// full[4], empty[4], tfull[2], tempty[2], done, bsc[2], xchg[2], as_full[8], as_empty[8]
-constexpr int kTileRow = 528;  // a staged down-output row: 256 bf16 + 16 B of padding
+// a staged output row: 128 fp32 h values (gate/up) or 256 bf16 (down), plus
+// 16 bytes of padding so that 32 rows' 16-byte accesses spread over the banks
+constexpr int kTileRow = 528;
 
-// Shared-memory layout per mode.  Down keeps three operand stages and a
-// stage of the whole output tile (128 rows of 256 bf16 plus the rows' pair
-// ids) that a store warp drains while the epilogue moves on to the next
-// tile; gate/up keeps four operand stages and the row-maximum exchange.
+// Shared-memory layout per mode: three operand stages, then the stage of the
+// whole output tile that the output warp drains while the epilogue moves on
+// to the next tile (gate/up: h in fp32 with the two half-rows' maxima and
+// the rows' 1/scale; down: the bf16 rows with their pair ids).
+// Barriers: full[S], empty[S], tfull[2], tempty[2], done, bsc[2], (2 unused),
+// as_full[8], as_empty[8], stg_full, stg_empty.
 template <int MODE>
 struct Layout {
   static constexpr bool kDown = MODE == kDownMode;
-  static constexpr int S = kDown ? 3 : kStages;
-  static constexpr int threads = 64 + kEpiThreads + (kDown ? 32 : 0);
+  static constexpr int S = 3;
+  static constexpr int threads = 64 + kEpiThreads + 32;  // + the output warp
   static constexpr int offA = 0;
   static constexpr int offB = offA + S * kAStage;
   static constexpr int offAS = offB + S * kBStage;
   static constexpr int offBar = offAS + kASStages * kASStage;
-  static constexpr int nbars = 2 * S + 2 + 2 + 1 + 2 + 2 + 2 * kASStages + (kDown ? 2 : 0);
+  static constexpr int nbars = 2 * S + 2 + 2 + 1 + 2 + 2 + 2 * kASStages + 2;
   static constexpr int offTmem = offBar + 8 * nbars;
   static constexpr int offBsc = offTmem + 16;                      // [2 bufs][2][kMaxKB] f32
-  static constexpr int offAmax = offBsc + 2 * 2 * kMaxKB * 4;      // gate/up: [2][2][128] f32
-  static constexpr int offStg = (offAmax + (kDown ? 0 : 2 * 2 * 128 * 4) + 127) / 128 * 128;
-  static constexpr int offStgPair = offStg + (kDown ? kBM * kTileRow : 0);
+  static constexpr int offRowMax = offBsc + 2 * 2 * kMaxKB * 4;    // gate/up: [2 halves][128], [128] 1/s
+  static constexpr int offStg = (offRowMax + (kDown ? 0 : 3 * 128 * 4) + 127) / 128 * 128;
+  static constexpr int offStgPair = offStg + kBM * kTileRow;
   static constexpr int offPrefix = offStgPair + (kDown ? kBM * 4 : 0);
   static constexpr int offRBase = offPrefix + (kMaxE + 1) * 4;
   static constexpr int offRCnt = offRBase + kMaxE * 4;
@@ -151,7 +156,6 @@ __global__ void __launch_bounds__(Layout<MODE>::threads, 1)
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
   auto bsc_bar = [&](int b) { return bar0 + 8u * (2 * S + 5 + b); };
-  auto xchg_bar = [&](int b) { return bar0 + 8u * (2 * S + 7 + b); };
   auto as_full_bar = [&](int s) { return bar0 + 8u * (2 * S + 9 + s); };
   auto as_empty_bar = [&](int s) { return bar0 + 8u * (2 * S + 9 + kASStages + s); };
   const uint32_t stg_full_bar = bar0 + 8u * (2 * S + 9 + 2 * kASStages);
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(Layout<MODE>::threads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + L::offTmem);
   const float *as_smem = reinterpret_cast<const float *>(sbase + L::offAS);
   float *bsc_smem = reinterpret_cast<float *>(sbase + L::offBsc);
-  float *amax_x = reinterpret_cast<float *>(sbase + L::offAmax);
+  float *rowmax = reinterpret_cast<float *>(sbase + L::offRowMax);
   uint8_t *stg = sbase + L::offStg;
   int *stg_pair = reinterpret_cast<int *>(sbase + L::offStgPair);
   int *prefix = reinterpret_cast<int *>(sbase + L::offPrefix);
@@ -183,13 +187,10 @@ __global__ void __launch_bounds__(Layout<MODE>::threads, 1)
       mbar_init(tfull_bar(b), 1);
       mbar_init(tempty_bar(b), kEpiWarps);
       mbar_init(bsc_bar(b), kEpiThreads);
-      mbar_init(xchg_bar(b), kEpiThreads);
     }
     mbar_init(done_bar, 1);
-    if constexpr (MODE == kDownMode) {
-      mbar_init(stg_full_bar, kEpiWarps);  // every epilogue warp staged its rows
-      mbar_init(stg_empty_bar, 1);         // the store warp drained the stage
-    }
+    mbar_init(stg_full_bar, kEpiWarps);  // every epilogue warp staged its rows
+    mbar_init(stg_empty_bar, 1);         // the store / quant warp drained the stage
     fence_barrier_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -312,6 +313,43 @@ __global__ void __launch_bounds__(Layout<MODE>::threads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(stg_empty_bar);
     }
+  } else if (MODE == kGateUpMode && warp == 2 + kEpiWarps) {
+    // ===================== h requantisation and stores ==================
+    // A staged row holds h of the tile's 128 outputs in fp32 and the maxima
+    // of its two halves.  Lane l first turns rows l, l + 32, ... into their
+    // scales (s = max / 448) and 1/s; then every row's codes go out as one
+    // 128-byte store, lane l coding outputs [4l, 4l + 4).
+    const float *hst = reinterpret_cast<const float *>(stg);
+    float *rinv = rowmax + 2 * 128;  // [128] 1 / scale of each staged row
+    int tile_no = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tile_no) {
+      int e, mt, nt;
+      decode_tile(prefix, E, p.n_tiles, tile, e, mt, nt);
+      if (!mbar_wait(stg_full_bar, tile_no & 1)) {
+        set_err(p.err, GBMOE_ERR_TIMEOUT);
+        break;
+      }
+      const int rows = min(rcnt[e] - mt * kBM, kBM);
+      const int arow0 = rbase[e] + mt * kBM;
+      // one row's scale per lane: the maximum of its two halves' maxima
+      for (int r = lane; r < rows; r += 32) {
+        const float amax = fmaxf(rowmax[r], rowmax[128 + r]);
+        const float sc = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
+        rinv[r] = __frcp_rn(sc);  // codes of h * (1 / s)
+        p.out_scales[(size_t)nt * p.scale_ld + arow0 + r] = sc;
+      }
+      __syncwarp();
+      uint8_t *hrow = static_cast<uint8_t *>(p.out) + (size_t)arow0 * p.N + nt * 128;
+#pragma unroll 4
+      for (int r = 0; r < rows; ++r) {
+        const float4 h = *reinterpret_cast<const float4 *>(hst + r * (kTileRow / 4) + lane * 4);
+        const float inv_sc = rinv[r];
+        reinterpret_cast<uint32_t *>(hrow + (size_t)r * p.N)[lane] =
+            e4m3x4(h.x * inv_sc, h.y * inv_sc, h.z * inv_sc, h.w * inv_sc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stg_empty_bar);
+    }
   } else {
     // ============================= epilogue =============================
     const int ew = warp - 2;           // 0..7
@@ -366,7 +404,6 @@ __global__ void __launch_bounds__(Layout<MODE>::threads, 1)
       const int a_row = rbase[e] + mt * kBM;
       const int r = mt * kBM + row_in_tile;
       const bool valid = r < rcnt[e];
-      const int arow = a_row + row_in_tile;
       const int as_idx = (a_row & 3) + row_in_tile;
       // the next tile: its decode, its weight-block scale (stored at this
       // tile's end) and, for down, its row's pair (the weight of that pair
@@ -449,40 +486,26 @@ __global__ void __launch_bounds__(Layout<MODE>::threads, 1)
       if (!ok) break;
 
       if (MODE == kGateUpMode) {
-        // h on this thread's 64 columns, then one e4m3 scale per 128-wide
-        // group: the row maximum over the two column halves
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          acc[i].x = gate_act_fast<ACT>(acc[i].x) * acc[32 + i].x;
-          acc[i].y = gate_act_fast<ACT>(acc[i].y) * acc[32 + i].y;
-          amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
-        }
-        const int xb = tile_no & 1;
-        amax_x[(xb * 2 + hh) * 128 + row_in_tile] = amax;
-        mbar_arrive(xchg_bar(xb));
-        if (!mbar_wait(xchg_bar(xb), (tile_no >> 1) & 1)) {
+        // h on this thread's 64 columns into the tile's stage; the quant
+        // warp requantises and stores it while this warp starts the next tile
+        if (!mbar_wait(stg_empty_bar, (tile_no & 1) ^ 1)) {
           set_err(p.err, GBMOE_ERR_TIMEOUT);
           break;
         }
-        amax = fmaxf(amax_x[(xb * 2) * 128 + row_in_tile], amax_x[(xb * 2 + 1) * 128 + row_in_tile]);
-        const float sc = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
-        const float inv_sc = __frcp_rn(sc);  // codes of h * (1 / s): one division per row group
-        if (valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
-                                                 (size_t)arow * p.N + nt * 128 + hh * 64);
+        float4 *dst = reinterpret_cast<float4 *>(stg + row_in_tile * kTileRow + hh * 256);
+        float amax = 0.0f;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 a = acc[v * 8 + j * 2], b = acc[v * 8 + j * 2 + 1];
-              w4[j] = e4m3x4(a.x * inv_sc, a.y * inv_sc, b.x * inv_sc, b.y * inv_sc);
-            }
-            dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
-          if (hh == 0) p.out_scales[(size_t)nt * p.scale_ld + arow] = sc;
+        for (int v = 0; v < 16; ++v) {
+          const float2 g0 = acc[2 * v], g1 = acc[2 * v + 1];
+          const float2 u0 = acc[32 + 2 * v], u1 = acc[32 + 2 * v + 1];
+          const float4 h = make_float4(gate_act_fast<ACT>(g0.x) * u0.x, gate_act_fast<ACT>(g0.y) * u0.y,
+                                       gate_act_fast<ACT>(g1.x) * u1.x, gate_act_fast<ACT>(g1.y) * u1.y);
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
+          dst[v] = h;
         }
+        rowmax[hh * 128 + row_in_tile] = amax;  // this half-row's maximum
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stg_full_bar);
       } else {
         // This thread's 128 columns (256 bytes of bf16) of its row go into
         // the tile's stage; the store warp writes them out while this warp
