@@ -61,6 +61,7 @@ constexpr uint32_t kIdesc = umma_idesc(kBM, kBN, kFmtE4M3);
 constexpr int kMaxKB = 128;                     // K up to 16384
 constexpr int kASBox = kBM + 4;                 // row scales per K block (rows from a 4-aligned start)
 constexpr int kASStage = 640;                   // bytes per ring slot (528 used)
+static_assert(kASStage % 128 == 0, "a TMA destination in shared memory is 128-byte aligned");
 constexpr int kASStages = 8;                    // row-scale ring, deeper than the operand ring
 
 // a staged output row: 128 fp32 h values (gate/up) or 256 bf16 (down), plus
