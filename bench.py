@@ -213,8 +213,9 @@ class Layer:
         self.amax = torch.zeros(2, dtype=i32, device=device) if self.tensor else None
         self.fwd_ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype, device=device)
         # route, 3 align, [quant x], gather, gate/up, [quant H], down, reduce;
-        # a per-tensor quant is a clear, a maximum and the codes
-        self.launches_per_step = (8 + (1 if self.fp8 else 0) + (1 if self.ch else 0)
+        # 1 x 128 e4m3 quantises and gathers in one launch; a per-tensor
+        # quant is a clear, a maximum and the codes
+        self.launches_per_step = (8 + (1 if self.ch else 0) + (1 if self.ch else 0)
                                   + (4 if self.tensor else 0))
 
     def step(self, ev_gemm=None, mark=None):
@@ -235,12 +236,19 @@ class Layer:
             g.moe_quant_fp8_tensor(self.x, self.xq, self.xs, self.amax[0:1])
             src, src_s = self.xq, self.xs
             mark("a4_quant_x")
-        elif self.fp8:
-            g.moe_quant_fp8_group(self.x, self.xq, self.xs, group=K if self.ch else 128)
+        elif self.ch:
+            g.moe_quant_fp8_group(self.x, self.xq, self.xs, group=K)
             src, src_s = self.xq, self.xs
             mark("a4_quant_x")
-        g.moe_permute_rows(src, src_s, self.sorted, self.offsets, k, E, c.dtype, self.A, self.As)
-        mark("a3_gather")
+        if self.fp8 and not self.ch and not self.tensor:
+            # 1 x 128 groups: quantised once, codes and scales written to the
+            # permuted rows in the same pass
+            g.moe_quant_fp8_group_permute(self.x, self.inv, k, self.A, self.As)
+            mark("a4_a3_quant_permute")
+        else:
+            g.moe_permute_rows(src, src_s, self.sorted, self.offsets, k, E, c.dtype, self.A,
+                               self.As)
+            mark("a3_gather")
         if ev_gemm is not None:
             ev_gemm[0].record()
         g.moe_grouped_gemm_gate_up_silu(self.A, self.As, self.offsets, M, k, E, N, K, self.w1,

@@ -245,6 +245,23 @@ gbmoe_status_t moe_permute_rows(const void *x, const float *x_scales,
                                 int K, int dtype, void *A, float *A_scales,
                                 gbmoe_stream_t stream);
 
+/* moe_quant_fp8_group (group 128) and moe_permute_rows (dtype
+ * GBMOE_FP8_E4M3) in one pass: each token's 1 x 128 groups are quantised
+ * once and their codes and scales written straight to the permuted rows of
+ * the token's pairs, A[inv[p]] for p = t*topk + j (pairs with inv[p] < 0,
+ * not routed to a local expert, are skipped).  The results equal the two
+ * calls' bit for bit.
+ * x (M, K) bf16; row_weights (M) fp32 or NULL (apply_router_weight_on_input,
+ * topk 1: the fp32 product of a row and its weight is quantised); inv
+ * (M*topk) int32 from moe_align_permute; A (M*topk, K) e4m3 and A_scales
+ * group-major (K/128, ld), ld = M*topk rounded up to 4, as
+ * moe_permute_rows writes them.  K % 128 == 0; x and A 16-byte aligned. */
+gbmoe_status_t moe_quant_fp8_group_permute(const uint16_t *x,
+                                           const float *row_weights, int M,
+                                           int K, const int32_t *inv, int topk,
+                                           uint8_t *A, float *A_scales,
+                                           gbmoe_stream_t stream);
+
 /* First expert GEMM with the gated activation fused into its epilogue:
  * the first GEMM of FusedMoEPermuteExpertsUnpermute.apply followed by its
  * gated activation (and, for block-scaled e4m3, the requantisation of the

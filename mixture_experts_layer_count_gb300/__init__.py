@@ -67,6 +67,7 @@ _SIGS = {
     "moe_grouped_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
                                    _I, _P, _P, _P]),
     "moe_unpermute_weighted_reduce": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "moe_quant_fp8_group_permute": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P]),
     "moe_ep_dispatch": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                              _Z, _P, _P]),
     "moe_ep_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
@@ -177,6 +178,15 @@ def moe_quant_fp8_group(x, q, scales, group=128, stream=None, row_weights=None):
     M, K = x.shape
     _check("moe_quant_fp8_group", load().moe_quant_fp8_group(
         _ptr(x), _ptr(row_weights), M, K, group, _ptr(q), _ptr(scales),
+        _stream(stream)))
+
+
+def moe_quant_fp8_group_permute(x, inv, topk, A, A_scales, row_weights=None, stream=None):
+    """x (M, K) bf16, inv (M*topk) int32 -> A (M*topk, K) e4m3 codes in
+    permuted order, A_scales group-major (K/128, ld) fp32."""
+    M, K = x.shape
+    _check("moe_quant_fp8_group_permute", load().moe_quant_fp8_group_permute(
+        _ptr(x), _ptr(row_weights), M, K, _ptr(inv), topk, _ptr(A), _ptr(A_scales),
         _stream(stream)))
 
 

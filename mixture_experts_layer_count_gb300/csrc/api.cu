@@ -389,6 +389,23 @@ gbmoe_status_t moe_quant_fp8_group(const uint16_t *x, const float *row_weights,
       launch_quant_group(x, row_weights, M, K, q, scales, sms, (cudaStream_t)stream));
 }
 
+gbmoe_status_t moe_quant_fp8_group_permute(const uint16_t *x, const float *row_weights,
+                                           int M, int K, const int32_t *inv, int topk,
+                                           uint8_t *A, float *A_scales, gbmoe_stream_t stream) {
+  if (M < 0 || K < 128 || K % 128 != 0 || topk < 1 || topk > kMaxTopk) return GBMOE_INVALID_ARG;
+  if (row_weights && topk != 1) return GBMOE_INVALID_ARG;
+  if ((size_t)M * topk > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
+  if (M > 0 && (!x || !inv || !A || !A_scales || !aligned16(x) || !aligned16(A) ||
+                (reinterpret_cast<uintptr_t>(A_scales) & 3u)))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK || M == 0) return st;
+  return from_cuda(launch_quant_group_scatter(x, row_weights, M, K, inv, topk, A, A_scales,
+                                              scale_ld((size_t)M * topk), sms,
+                                              (cudaStream_t)stream));
+}
+
 gbmoe_status_t moe_quant_fp8_tensor(const uint16_t *x, const float *row_weights,
                                     int M, int K, const int32_t *n_rows,
                                     uint8_t *q, float *row_scales,
@@ -712,17 +729,23 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   const float *in_w = apply_router_weight_on_input ? wts : nullptr;
   const void *a_src = x;
   const float *a_src_s = nullptr;
-  if (fp8) {
-    ce = fp8t    ? launch_quant_tensor(x, in_w, M, K, nullptr, w.xq, w.xs, w.amax, sms, s)
-         : fp8ch ? launch_quant_row(x, in_w, M, K, w.xq, w.xs, sms, s)
-                 : launch_quant_group(x, in_w, M, K, w.xq, w.xs, sms, s);
+  if (fp8 && !fp8t && !fp8ch) {
+    // 1 x 128 groups: the codes and scales go straight to the permuted rows
+    ce = launch_quant_group_scatter(x, in_w, M, K, w.inv, topk, static_cast<uint8_t *>(w.A),
+                                    w.As, scale_ld((size_t)P), sms, s);
     if (ce != cudaSuccess) return from_cuda(ce);
-    a_src = w.xq;
-    a_src_s = w.xs;
+  } else {
+    if (fp8) {
+      ce = fp8t ? launch_quant_tensor(x, in_w, M, K, nullptr, w.xq, w.xs, w.amax, sms, s)
+                : launch_quant_row(x, in_w, M, K, w.xq, w.xs, sms, s);
+      if (ce != cudaSuccess) return from_cuda(ce);
+      a_src = w.xq;
+      a_src_s = w.xs;
+    }
+    st = permute_impl(a_src, a_src_s, fp8 ? nullptr : in_w, w.sorted, w.offsets, M, topk, E, K,
+                      dtype, w.A, w.As, sms, s);
+    if (st != GBMOE_OK) return st;
   }
-  st = permute_impl(a_src, a_src_s, fp8 ? nullptr : in_w, w.sorted, w.offsets, M, topk, E, K,
-                    dtype, w.A, w.As, sms, s);
-  if (st != GBMOE_OK) return st;
   // per-token (per-tensor) scales span a whole row (all computed rows) of
   // H: it is written in bf16 and quantised before the second GEMM
   st = gate_up_impl(w.A, w.As, w.offsets, M, topk, E, N, K, w1, w1_scales, dtype, activation,

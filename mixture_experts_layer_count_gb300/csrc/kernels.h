@@ -67,6 +67,11 @@ cudaError_t launch_ep_combine(const uint16_t *recv_y, const int32_t *topk_ids,
 // row_w (M) or NULL: rows multiplied by their weight (fp32) before quantising
 cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int K,
                                uint8_t *q, float *scales, int num_sms, cudaStream_t s);
+// launch_quant_group writing its codes and scales straight to the permuted
+// rows: A row inv[t*topk + j] (skipped when negative), As group-major (K/128, ld)
+cudaError_t launch_quant_group_scatter(const uint16_t *x, const float *row_w, int M, int K,
+                                       const int32_t *inv, int topk, uint8_t *A, float *As,
+                                       int64_t ld, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K,
                              uint8_t *q, float *scales, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, int K,

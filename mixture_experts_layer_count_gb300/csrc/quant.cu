@@ -39,9 +39,9 @@ __device__ __forceinline__ float group_scale(float amax) {
 // one half-warp per (token, 128-group): 8 values (one 16-byte load) per lane,
 // two groups per warp; each warp takes two pairs of groups per loop turn
 // with both loads issued first (more bytes in flight per SM)
-__device__ __forceinline__ void quant_group_pair(const uint4 &raw, bool live, const float *row_w,
-                                                 size_t t, size_t g, size_t vec, int hl, int G,
-                                                 uint2 *__restrict__ q, float *__restrict__ scales) {
+// the codes of one lane's 8 values and the group's scale (valid when live)
+__device__ __forceinline__ void quant_group_codes(const uint4 &raw, bool live, const float *row_w,
+                                                  size_t t, uint2 &code, float &scale) {
   float f[8];
   float amax = 0.0f;
   const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -62,14 +62,49 @@ __device__ __forceinline__ void quant_group_pair(const uint4 &raw, bool live, co
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1)  // within each half-warp
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  scale = 1.0f;
+  code = make_uint2(0u, 0u);
   if (live) {
     const float s = group_scale(amax);
     uint32_t c[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = e4m3_of(__fdiv_rn(f[i], s));
-    q[vec] = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
-                        c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+    code = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                      c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+    scale = s;
+  }
+}
+
+__device__ __forceinline__ void quant_group_pair(const uint4 &raw, bool live, const float *row_w,
+                                                 size_t t, size_t g, size_t vec, int hl, int G,
+                                                 uint2 *__restrict__ q, float *__restrict__ scales) {
+  uint2 code;
+  float s;
+  quant_group_codes(raw, live, row_w, t, code, s);
+  if (live) {
+    q[vec] = code;
     if (hl == 0) scales[t * G + g] = s;
+  }
+}
+
+// the same codes sent straight to the permuted rows of the token's pairs
+// (the gather of moe_permute_rows folded in): row inv[t * topk + j] of A,
+// skipped when negative, gets the group's 128 codes and As[g * ld + row]
+// its scale
+__device__ __forceinline__ void quant_group_scatter(const uint4 &raw, bool live,
+                                                    const float *row_w, size_t t, size_t g,
+                                                    int hl, int K, const int32_t *__restrict__ inv,
+                                                    int topk, uint2 *__restrict__ A,
+                                                    float *__restrict__ As, int64_t ld) {
+  uint2 code;
+  float s;
+  quant_group_codes(raw, live, row_w, t, code, s);
+  if (!live) return;
+  for (int j = 0; j < topk; ++j) {
+    const int i = __ldg(inv + t * topk + j);
+    if (i < 0) continue;
+    A[((size_t)i * K + g * 128) / 8 + hl] = code;
+    if (hl == 0) As[(size_t)g * ld + i] = s;
   }
 }
 
@@ -94,6 +129,30 @@ __global__ void __launch_bounds__(256)
     quant_group_pair(r0, live0, row_w, t0, g0, v0, hl, G, q, scales);
     if (2 * (w + nw) < n)  // uniform over the warp
       quant_group_pair(r1, live1, row_w, t1, g1, v1, hl, G, q, scales);
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    quant_group_scatter_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w,
+                               int M, int K, const int32_t *__restrict__ inv, int topk,
+                               uint2 *__restrict__ A, float *__restrict__ As, int64_t ld) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  const int G = K / 128;
+  const size_t n = (size_t)M * G;  // groups
+  const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
+  for (size_t w = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; 2 * w < n; w += 2 * nw) {
+    const size_t gi0 = 2 * w + half, gi1 = 2 * (w + nw) + half;
+    const bool live0 = gi0 < n, live1 = gi1 < n;
+    const size_t t0 = live0 ? gi0 / G : 0, g0 = live0 ? gi0 % G : 0;
+    const size_t t1 = live1 ? gi1 / G : 0, g1 = live1 ? gi1 % G : 0;
+    const size_t v0 = (t0 * K + g0 * 128) / 8 + hl, v1 = (t1 * K + g1 * 128) / 8 + hl;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 r0 = live0 ? x[v0] : z;
+    const uint4 r1 = live1 ? x[v1] : z;
+    quant_group_scatter(r0, live0, row_w, t0, g0, hl, K, inv, topk, A, As, ld);
+    if (2 * (w + nw) < n)  // uniform over the warp
+      quant_group_scatter(r1, live1, row_w, t1, g1, hl, K, inv, topk, A, As, ld);
   }
 }
 
@@ -278,6 +337,20 @@ cudaError_t launch_quant_group(const uint16_t *x, const float *row_w, int M, int
   if (blocks < 1) blocks = 1;
   quant_group_kernel<<<(unsigned)blocks, 256, 0, s>>>(
       reinterpret_cast<const uint4 *>(x), row_w, M, K, reinterpret_cast<uint2 *>(q), scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_group_scatter(const uint16_t *x, const float *row_w, int M, int K,
+                                       const int32_t *inv, int topk, uint8_t *A, float *As,
+                                       int64_t ld, int num_sms, cudaStream_t s) {
+  const size_t warps = ((size_t)M * (K / 128) + 1) / 2;
+  size_t blocks = (warps + 7) / 8;
+  const size_t resident = (size_t)num_sms * 8;
+  if (blocks > resident) blocks = resident;
+  if (blocks < 1) blocks = 1;
+  quant_group_scatter_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), row_w, M, K, inv, topk, reinterpret_cast<uint2 *>(A),
+      As, ld);
   return cudaGetLastError();
 }
 

@@ -176,6 +176,13 @@ def test_gemm_calls_reject_bad_arguments(lib):
     assert ec(P16, P16, P16, None, P16, 2, 16, 256, 32, 4, 32, P16, None) == INVALID  # no weights
     assert ec(P16, P16, P16, P16, P16, 2, 16, 256, 32, 4, 32, P_ODD, None) == INVALID
     assert lib.moe_unpermute_weighted_reduce(P16, None, 8, 33, 256, P16, None) == INVALID
+    qp = lib.moe_quant_fp8_group_permute
+    #         x    rw    M   K    inv  k  A    As   s
+    assert qp(P16, None, 16, 200, P16, 4, P16, P16, None) == INVALID   # K % 128
+    assert qp(P16, P16, 16, 256, P16, 2, P16, P16, None) == INVALID    # row weights need top-1
+    assert qp(P16, None, 16, 256, None, 4, P16, P16, None) == INVALID  # no inverse map
+    assert qp(P_ODD, None, 16, 256, P16, 4, P16, P16, None) == INVALID
+    assert qp(P16, None, 16, 256, P16, 4, P16, P16 + 2, None) == INVALID
     b = lib.moe_batched_masked_experts
     #        xb  xbs   cnt E  T   N    K    w1   w1s  w2   w2s  dt ac yb   ws   wsb  err  s
     assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 2, 0, P16, P16, 1 << 30, None, None) == UNSUPPORTED

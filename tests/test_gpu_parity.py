@@ -150,6 +150,56 @@ def test_quant_fp8_group_bit_exact():
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
+@pytest.mark.parametrize("case", ["all_local", "expert_map", "weight_on_input"])
+def test_quant_fp8_group_permute_bit_exact(case):
+    """Quantisation and permutation in one pass: codes and group-major scales
+    of every permuted row bit-exact against the oracle's group quantiser and
+    stable sort (A[i] = codes of token sorted[i] / topk), pairs not routed to
+    a local expert skipped, rows at and beyond the local total untouched;
+    with a row weight (top-1) the product is quantised."""
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(43)
+    M, K, E = 300, 640, 16
+    topk = 1 if case == "weight_on_input" else 4
+    x = (torch.randn((M, K), generator=gen, device=DEV) *
+         torch.logspace(-3, 2, K, device=DEV)).to(torch.bfloat16)
+    ids = torch.stack([torch.randperm(E, generator=gen, device=DEV)[:topk] for _ in range(M)]).int()
+    emap = None
+    E_loc = E
+    if case == "expert_map":  # experts 4..11 are local (as 0..7), the rest elsewhere
+        emap = torch.full((E,), -1, dtype=torch.int32, device=DEV)
+        emap[4:12] = torch.arange(8, dtype=torch.int32, device=DEV)
+        E_loc = 8
+    rw = (torch.rand((M,), generator=gen, device=DEV) + 0.25) if case == "weight_on_input" else None
+    P = M * topk
+    counts = torch.empty(E_loc, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E_loc + 1, dtype=torch.int32, device=DEV)
+    srt = torch.empty(P, dtype=torch.int32, device=DEV)
+    inv = torch.empty(P, dtype=torch.int32, device=DEV)
+    ws = g.workspace(g.WS_ALIGN, M, E, 0, 0, topk, 0)
+    g.moe_align_permute(ids, E_loc, counts, offsets, srt, inv, ws, expert_map=emap,
+                        E_global=E if emap is not None else None)
+    ld = (P + 3) // 4 * 4
+    A = torch.full((P, K), 0xA5, dtype=torch.uint8, device=DEV)
+    As = torch.full((K // 128, ld), -7.0, dtype=torch.float32, device=DEV)
+    g.moe_quant_fp8_group_permute(x, inv, topk, A, As, row_weights=rw)
+    torch.cuda.synchronize()
+    rq, rs = orc.quant_fp8_group(WL.bf16_bits(x),
+                                 row_weights=None if rw is None else rw.cpu().numpy())
+    ro, rsrt, rinv = orc.align(ids.cpu().numpy(), E,
+                               expert_map=None if emap is None else emap.cpu().numpy(),
+                               E_local=E_loc)
+    total = int(ro[E_loc])
+    assert total == int(offsets[E_loc].item())
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+    tok = rsrt[:total] // topk
+    a = A.cpu().numpy()
+    a_s = As.cpu().numpy()
+    assert np.array_equal(a[:total], rq[tok])
+    assert np.array_equal(a_s[:, :total], rs[tok].T)
+    assert np.all(a[total:] == 0xA5) and np.all(a_s[:, total:] == -7.0)
+
+
 @pytest.mark.parametrize("K,weighted", [(1024, False), (7168, True), (640, False)])
 def test_quant_fp8_rowwise_bit_exact(K, weighted):
     """One scale per row (per-token activations, per-channel weights): codes
