@@ -29,7 +29,10 @@
  *     K or N not a multiple of 128, topk > E, workspace too small,
  *     misaligned pointer), GBMOE_UNSUPPORTED (dtype, or a device that is not
  *     sm_103), GBMOE_CUDA_ERROR (a launch failed; see gbmoe_last_cuda_error).
- *     Nothing is enqueued when a call returns an error.
+ *     Nothing is enqueued when a call returns GBMOE_INVALID_ARG or
+ *     GBMOE_UNSUPPORTED (arguments are checked before the first launch); a
+ *     call of several launches that returns GBMOE_CUDA_ERROR may have
+ *     enqueued the launches before the failing one.
  *   - Errors in the DATA (an expert id outside [0, E), a batched count
  *     outside [0, T], a device wait that ran out of time) cannot be seen on
  *     the host without a sync.  Kernels skip the offending element and OR a
