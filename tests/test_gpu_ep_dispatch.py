@@ -168,13 +168,13 @@ def test_ep_worst_tokens_graph_replays(cfg, replays):
             _oracle_check(cfg, layer, dr, W)
 
 
-def test_ep_worst_tokens_fp8_graph_replays():
+@pytest.mark.parametrize("cfg,replays", [(WL.EP2, 20), (WL.EP4, 10)], ids=["G2", "G4"])
+def test_ep_worst_tokens_fp8_graph_replays(cfg, replays):
     """The same sharded layer with the tokens quantised to e4m3 (1 x 128
     group scales) before the dispatch, the scales carried with the rows, and
-    block-scaled e4m3 experts on each shard: 20 replays, each equal to the
-    eager run bit for bit (receive rows and scales included), every fifth
-    against the oracle's e4m3 layer (h requantised)."""
-    cfg = WL.EP2
+    block-scaled e4m3 experts on each shard: 20 (G = 2) or 10 (G = 4)
+    replays, each equal to the eager run bit for bit (receive rows and scales
+    included), every fifth against the oracle's e4m3 layer (h requantised)."""
     d0 = WL.make_ep_inputs(cfg, DEV)
     layer = EpLayer(cfg, d0["w1"], d0["w2"], WL.FP8)
     W = oracle_weights(WL.MoEConfig("ep_all_fp8", M=1, K=cfg.K, N=cfg.N, E=cfg.E, topk=cfg.topk,
@@ -189,7 +189,7 @@ def test_ep_worst_tokens_fp8_graph_replays():
     with torch.cuda.graph(graph):
         layer.step()
     eager = EpLayer(cfg, d0["w1"], d0["w2"], WL.FP8)
-    for r in range(20):
+    for r in range(replays):
         dr = WL.make_ep_inputs(cfg, DEV, seed=cfg.seed * 1000 + 500 + r, with_weights=False)
         layer.load(dr)
         graph.replay()

@@ -70,17 +70,29 @@ def test_gate_up_gelu_entry_point():
     assert_close_rel(H.float().cpu().numpy(), href, TOL[WL.BF16], "H (gelu)")
 
 
-def test_batched_gelu():
+@pytest.mark.parametrize("cfg", [WL.SMALL_BATCHED, WL.SMALL_BATCHED_FP8],
+                         ids=lambda c: c.name)
+def test_batched_gelu(cfg):
     g = gbmoe()
-    cfg = WL.SMALL_BATCHED
     d = WL.make_inputs(cfg, DEV)
     yb = torch.full((cfg.E, cfg.M, cfg.K), 5.0, dtype=torch.bfloat16, device=DEV)
-    ws = g.workspace(g.WS_BATCHED, cfg.M, cfg.E, cfg.N, cfg.K, 1, WL.BF16)
-    g.moe_batched_masked_experts(d["x_b"], d["counts"], cfg.N, d["w1"], d["w2"], yb, ws,
-                                 activation=g.ACT_GELU)
+    ws = g.workspace(g.WS_BATCHED, cfg.M, cfg.E, cfg.N, cfg.K, 1, cfg.dtype)
+    if cfg.dtype == WL.FP8:
+        gw = GpuWeights(cfg, d["w1"], d["w2"])
+        E, T, K = cfg.E, cfg.M, cfg.K
+        q = torch.empty((E, T, K), dtype=torch.uint8, device=DEV)
+        sc = torch.empty((E * T, K // 128), dtype=torch.float32, device=DEV)
+        g.moe_quant_fp8_group(d["x_b"].reshape(E * T, K), q.view(E * T, K), sc)
+        g.moe_batched_masked_experts(q, d["counts"], cfg.N, gw.w1, gw.w2, yb, ws, dtype=WL.FP8,
+                                     x_b_scales=sc, w1_scales=gw.w1s, w2_scales=gw.w2s,
+                                     activation=g.ACT_GELU)
+    else:
+        g.moe_batched_masked_experts(d["x_b"], d["counts"], cfg.N, d["w1"], d["w2"], yb, ws,
+                                     activation=g.ACT_GELU)
     torch.cuda.synchronize()
     W = oracle_weights(cfg, d["w1"], d["w2"])
     W.act = orc.GELU
-    ref, n = orc.batched_experts(WL.bf16_bits(d["x_b"]), d["counts"].cpu().numpy(), W)
+    ref, n = orc.batched_experts(WL.bf16_bits(d["x_b"]), d["counts"].cpu().numpy(), W,
+                                 requant_h=cfg.dtype == WL.FP8)
     mask = ~np.isnan(ref[..., 0])
-    assert_close_rel(yb.float().cpu().numpy()[mask], ref[mask], TOL[WL.BF16], "batched gelu")
+    assert_close_rel(yb.float().cpu().numpy()[mask], ref[mask], TOL[cfg.dtype], f"{cfg.name} gelu")
