@@ -93,7 +93,8 @@ enum {
     GBMOE_WS_ALIGN = 0,    /* moe_align_permute                       */
     GBMOE_WS_BATCHED = 2,  /* moe_batched_masked_experts              */
     GBMOE_WS_FORWARD = 3,  /* moe_forward (the whole Standard layer)  */
-    GBMOE_WS_SHARED = 4,   /* moe_shared_expert_forward (N = shared intermediate size) */
+    GBMOE_WS_SHARED = 4,   /* moe_shared_expert_forward (N = shared intermediate size;
+                              dtype GBMOE_BF16 or GBMOE_FP8_E4M3) */
     GBMOE_WS_EP_DISPATCH = 6  /* moe_ep_dispatch: M_or_T = M tokens per shard, E = all
                                  routed experts, N = the number of shards G  */
 };
@@ -438,16 +439,23 @@ gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
  * auxiliary stream).  For every token t:
  *   h = act(x[t] . w1s[0:Ns]^T) * (x[t] . w1s[Ns:2Ns]^T),
  *   out_shared[t] = h . w2s^T
- * x (M, K) bf16; w1s (2Ns, K), w2s (K, Ns) bf16 (the shared experts stacked
- * along Ns); out_shared (M, K) bf16; activation GBMOE_ACT_*; dtype GBMOE_BF16
- * only.  Runs the two grouped-GEMM kernels with one expert holding all M
- * rows.  ws: moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1, dtype). */
-gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K,
-                                         int Ns, const void *w1s,
-                                         const void *w2s, int dtype,
-                                         int activation, uint16_t *out_shared,
-                                         void *ws, size_t ws_bytes,
-                                         int32_t *err_word,
+ * x (M, K) bf16; w1s (2Ns, K), w2s (K, Ns) (the shared experts stacked
+ * along Ns); out_shared (M, K) bf16; activation GBMOE_ACT_*.
+ * dtype GBMOE_BF16: w1s, w2s bf16, the scale pointers unused (may be NULL).
+ * dtype GBMOE_FP8_E4M3: w1s, w2s e4m3 with 128 x 128 block scales
+ * w1s_scales (2Ns/128, K/128) and w2s_scales (K/128, Ns/128) fp32 (4-byte
+ * aligned; moe_quant_fp8_block makes them); x is quantised inside the call
+ * in 1 x 128 groups and h in 1 x 128 groups along Ns, as moe_forward does
+ * for the routed experts; K and Ns at most 16384.
+ * Other dtypes: GBMOE_UNSUPPORTED.  Runs the grouped-GEMM kernels with one
+ * expert holding all M rows (e4m3: after the group quantisation of x and a
+ * transpose of its scales).  ws: moe_workspace_size(GBMOE_WS_SHARED, M, 1,
+ * Ns, K, 1, dtype). */
+gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K, int Ns,
+                                         const void *w1s, const float *w1s_scales,
+                                         const void *w2s, const float *w2s_scales,
+                                         int dtype, int activation, uint16_t *out_shared,
+                                         void *ws, size_t ws_bytes, int32_t *err_word,
                                          gbmoe_stream_t stream);
 
 /* moe_forward with the shared experts overlapped on an auxiliary stream
@@ -460,9 +468,12 @@ gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K,
  * the caller (cudaEvent_t; timing may be disabled).  aux_stream NULL: both
  * run on `stream` one after the other.  The fork/join is capturable in a
  * CUDA graph when `stream` is being captured.
- * Arguments as moe_forward, plus Ns, w1s, w2s, out_shared as
- * moe_shared_expert_forward; ws_shared: moe_workspace_size(GBMOE_WS_SHARED,
- * ...) bytes, separate from ws. */
+ * Arguments as moe_forward, plus Ns, w1s, w1s_scales, w2s, w2s_scales and
+ * out_shared as moe_shared_expert_forward, whose dtype is shared_dtype
+ * (GBMOE_BF16 or GBMOE_FP8_E4M3, independent of the routed experts' dtype);
+ * ws_shared: moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1,
+ * shared_dtype) bytes, separate from ws.  Both calls' arguments are checked
+ * before anything is enqueued. */
 gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
                                   const float *bias, int M, int K, int N,
                                   int E_global, const int32_t *expert_map,
@@ -473,8 +484,9 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
                                   const float *w1_scales, const void *w2,
                                   const float *w2_scales, uint16_t *out,
                                   void *ws, size_t ws_bytes, int Ns,
-                                  const void *w1s, const void *w2s,
-                                  uint16_t *out_shared, void *ws_shared,
+                                  const void *w1s, const float *w1s_scales,
+                                  const void *w2s, const float *w2s_scales,
+                                  int shared_dtype, uint16_t *out_shared, void *ws_shared,
                                   size_t ws_shared_bytes, int32_t *err_word,
                                   gbmoe_stream_t stream,
                                   gbmoe_stream_t aux_stream,

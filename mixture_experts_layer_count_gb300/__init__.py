@@ -50,10 +50,11 @@ _SIGS = {
     "moe_align_permute": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
     "moe_forward_chunked": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
                                  _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
-    "moe_shared_expert_forward": (_I, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _Z, _P, _P]),
+    "moe_shared_expert_forward": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _Z,
+                                       _P, _P]),
     "moe_forward_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
-                                _I, _I, _P, _P, _P, _P, _P, _P, _Z, _I, _P, _P, _P, _P,
-                                _Z, _P, _P, _P, _P, _P]),
+                                _I, _I, _P, _P, _P, _P, _P, _P, _Z, _I, _P, _P, _P, _P, _I,
+                                _P, _P, _Z, _P, _P, _P, _P, _P]),
     "moe_align_permute_no_ws": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "gbmoe_selftest_bounded_wait": (_I, [_P, _I, _P]),
     "moe_quant_fp8_group": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
@@ -326,13 +327,15 @@ def moe_forward_chunked(x, logits, bias, N, E, topk, score_fn, n_groups, topk_gr
 
 
 def moe_shared_expert_forward(x, Ns, w1s, w2s, out_shared, ws, dtype=BF16,
-                              activation=ACT_SILU, err_word=None, stream=None):
-    """The shared experts (dense gated MLP) on every token of x."""
+                              activation=ACT_SILU, err_word=None, stream=None,
+                              w1s_scales=None, w2s_scales=None):
+    """The shared experts (dense gated MLP) on every token of x; bf16, or e4m3
+    weights with their 128 x 128 block scales (dtype FP8_E4M3)."""
     M, K = x.shape
     _check("moe_shared_expert_forward", load().moe_shared_expert_forward(
-        _ptr(x), M, K, Ns, _ptr(w1s), _ptr(w2s), dtype, int(activation),
-        _ptr(out_shared), _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
-        _stream(stream)))
+        _ptr(x), M, K, Ns, _ptr(w1s), _ptr(w1s_scales), _ptr(w2s), _ptr(w2s_scales), dtype,
+        int(activation), _ptr(out_shared), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(err_word), _stream(stream)))
 
 
 def _event(ev):
@@ -350,9 +353,11 @@ def moe_forward_shared(x, logits, bias, N, E, topk, score_fn, n_groups,
                        w2_scales, out, ws, Ns, w1s, w2s, out_shared, ws_shared,
                        aux_stream=None, ev_input_ready=None, ev_output_ready=None,
                        err_word=None, stream=None, expert_map=None,
-                       apply_router_weight_on_input=False, activation=ACT_SILU):
+                       apply_router_weight_on_input=False, activation=ACT_SILU,
+                       shared_dtype=BF16, w1s_scales=None, w2s_scales=None):
     """moe_forward with the shared experts overlapped on aux_stream (a
-    torch.cuda.Stream) through two torch.cuda.Event objects."""
+    torch.cuda.Stream) through two torch.cuda.Event objects; the shared
+    experts in shared_dtype (BF16, or FP8_E4M3 with block scales)."""
     M, K = x.shape
     E_global = logits.shape[1]
     _check("moe_forward_shared", load().moe_forward_shared(
@@ -360,7 +365,8 @@ def moe_forward_shared(x, logits, bias, N, E, topk, score_fn, n_groups,
         topk, score_fn, n_groups, topk_groups, int(renormalize),
         int(apply_router_weight_on_input), int(activation), dtype, _ptr(w1),
         _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(ws),
-        ws.numel() * ws.element_size(), Ns, _ptr(w1s), _ptr(w2s), _ptr(out_shared),
+        ws.numel() * ws.element_size(), Ns, _ptr(w1s), _ptr(w1s_scales), _ptr(w2s),
+        _ptr(w2s_scales), int(shared_dtype), _ptr(out_shared),
         _ptr(ws_shared), ws_shared.numel() * ws_shared.element_size(), _ptr(err_word),
         _stream(stream), None if aux_stream is None else aux_stream.cuda_stream,
         _event(ev_input_ready), _event(ev_output_ready)))

@@ -137,6 +137,29 @@ BatchedWs carve_batched(Carver &c, int T, int E, int N, int K, int dtype) {
   return w;
 }
 
+// moe_shared_expert_forward: H (M, Ns); e4m3 adds the codes of x, x's
+// scales row-major (the quantiser's output) and group-major (the GEMM's
+// operand), and H's group-major scales
+struct SharedWs {
+  void *H;
+  float *Hs;
+  void *xq;
+  float *xs_rows;
+  float *xs;
+};
+SharedWs carve_shared(Carver &c, int M, int Ns, int K, int dtype) {
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  SharedWs w{};
+  w.H = c.take((size_t)M * Ns * elem_bytes(dtype));
+  if (fp8) {
+    w.Hs = static_cast<float *>(c.take((size_t)scale_ld(M) * (Ns / 128) * 4));
+    w.xq = c.take((size_t)M * K);
+    w.xs_rows = static_cast<float *>(c.take((size_t)M * (K / 128) * 4));
+    w.xs = static_cast<float *>(c.take((size_t)scale_ld(M) * (K / 128) * 4));
+  }
+  return w;
+}
+
 EpWorkspace carve_ep(Carver &c, int G, int M, int E, int topk) {
   const size_t P = (size_t)G * M * topk;
   EpWorkspace w;
@@ -308,8 +331,9 @@ size_t moe_workspace_size(int which, int M_or_T, int E, int N, int K, int topk,
       carve_ep(c, N, M_or_T, E, topk);
       return c.off;
     case GBMOE_WS_SHARED:
-      if (!gemm_shape_ok(M_or_T, 1, 1, N, K, dtype) || dtype != GBMOE_BF16) return 0;
-      c.take((size_t)M_or_T * N * 2);
+      if (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3) return 0;
+      if (!gemm_shape_ok(M_or_T, 1, 1, N, K, dtype)) return 0;
+      carve_shared(c, M_or_T, N, K, dtype);
       return c.off > 0 ? c.off : kWsAlign;
   }
   return 0;
@@ -800,14 +824,13 @@ gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
   return GBMOE_OK;
 }
 
-gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K,
-                                         int Ns, const void *w1s,
-                                         const void *w2s, int dtype,
-                                         int activation, uint16_t *out_shared,
-                                         void *ws, size_t ws_bytes,
-                                         int32_t *err_word,
-                                         gbmoe_stream_t stream) {
-  if (dtype != GBMOE_BF16) return GBMOE_UNSUPPORTED;
+// every argument check of moe_shared_expert_forward (no launch, no device query)
+static gbmoe_status_t shared_validate(const uint16_t *x, int M, int K, int Ns, const void *w1s,
+                                      const float *w1s_scales, const void *w2s,
+                                      const float *w2s_scales, int dtype, int activation,
+                                      const uint16_t *out_shared, const void *ws,
+                                      size_t ws_bytes) {
+  if (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3) return GBMOE_UNSUPPORTED;
   if (!gemm_shape_ok(M, 1, 1, Ns, K, dtype)) return GBMOE_INVALID_ARG;
   if (activation != GBMOE_ACT_SILU && activation != GBMOE_ACT_GELU) return GBMOE_INVALID_ARG;
   if (M > 0) {
@@ -815,16 +838,36 @@ gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K,
     if (!aligned16(x) || !aligned16(w1s) || !aligned16(w2s) || !aligned16(out_shared) ||
         !aligned16(ws))
       return GBMOE_INVALID_ARG;
+    if (dtype == GBMOE_FP8_E4M3 &&
+        (!w1s_scales || !w2s_scales || (reinterpret_cast<uintptr_t>(w1s_scales) & 3u) ||
+         (reinterpret_cast<uintptr_t>(w2s_scales) & 3u)))
+      return GBMOE_INVALID_ARG;
     if (ws_bytes < moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1, dtype))
       return GBMOE_INVALID_ARG;
   }
+  return GBMOE_OK;
+}
+
+gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K, int Ns,
+                                         const void *w1s, const float *w1s_scales,
+                                         const void *w2s, const float *w2s_scales,
+                                         int dtype, int activation, uint16_t *out_shared,
+                                         void *ws, size_t ws_bytes, int32_t *err_word,
+                                         gbmoe_stream_t stream) {
+  gbmoe_status_t st = shared_validate(x, M, K, Ns, w1s, w1s_scales, w2s, w2s_scales, dtype,
+                                      activation, out_shared, ws, ws_bytes);
+  if (st != GBMOE_OK) return st;
   int sms;
-  gbmoe_status_t st = device_info(&sms);
+  st = device_info(&sms);
   if (st != GBMOE_OK || M == 0) return st;
   cudaStream_t s = (cudaStream_t)stream;
+  const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  Carver c(ws);
+  const SharedWs w = carve_shared(c, M, Ns, K, dtype);
   // one expert owning all M rows ("dense": neither offsets nor counts)
   GroupedGemmArgs a{};
   a.mode = kGateUp;
+  a.fp8 = fp8;
   a.act = activation;
   a.E = 1;
   a.T = M;
@@ -833,13 +876,29 @@ gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K,
   a.A = x;
   a.a_rows = M;
   a.B = w1s;
-  a.out = ws;
+  a.out = w.H;
   a.err = err_word;
-  cudaError_t ce = launch_grouped_gemm(a, sms, s);
+  cudaError_t ce;
+  if (fp8) {
+    // x in 1 x 128 groups, its scales moved to the GEMM's group-major layout
+    ce = launch_quant_group(x, nullptr, M, K, static_cast<uint8_t *>(w.xq), w.xs_rows, sms, s);
+    if (ce == cudaSuccess)
+      ce = launch_scales_group_major(w.xs_rows, M, K / 128, w.xs, scale_ld((size_t)M), sms, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+    a.A = w.xq;
+    a.A_scales = w.xs;
+    a.scale_ld = scale_ld((size_t)M);
+    a.B_scales = w1s_scales;
+    a.out_scales = w.Hs;
+  }
+  ce = launch_grouped_gemm(a, sms, s);
   if (ce != cudaSuccess) return from_cuda(ce);
   a.mode = kDown;
-  a.A = ws;
+  a.A = w.H;
+  a.A_scales = w.Hs;
   a.B = w2s;
+  a.B_scales = w2s_scales;
+  a.out_scales = nullptr;
   a.out = out_shared;
   return from_cuda(launch_grouped_gemm(a, sms, s));
 }
@@ -854,8 +913,9 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
                                   const float *w1_scales, const void *w2,
                                   const float *w2_scales, uint16_t *out,
                                   void *ws, size_t ws_bytes, int Ns,
-                                  const void *w1s, const void *w2s,
-                                  uint16_t *out_shared, void *ws_shared,
+                                  const void *w1s, const float *w1s_scales,
+                                  const void *w2s, const float *w2s_scales,
+                                  int shared_dtype, uint16_t *out_shared, void *ws_shared,
                                   size_t ws_shared_bytes, int32_t *err_word,
                                   gbmoe_stream_t stream,
                                   gbmoe_stream_t aux_stream,
@@ -867,14 +927,9 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
                                        apply_router_weight_on_input, activation, dtype, w1,
                                        w1_scales, w2, w2_scales, out, ws, ws_bytes);
   if (st != GBMOE_OK) return st;
-  if (!gemm_shape_ok(M, 1, 1, Ns, K, GBMOE_BF16)) return GBMOE_INVALID_ARG;
-  if (M > 0) {
-    if (!w1s || !w2s || !out_shared || !ws_shared || !aligned16(w1s) || !aligned16(w2s) ||
-        !aligned16(out_shared) || !aligned16(ws_shared))
-      return GBMOE_INVALID_ARG;
-    if (ws_shared_bytes < moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1, GBMOE_BF16))
-      return GBMOE_INVALID_ARG;
-  }
+  st = shared_validate(x, M, K, Ns, w1s, w1s_scales, w2s, w2s_scales, shared_dtype, activation,
+                       out_shared, ws_shared, ws_shared_bytes);
+  if (st != GBMOE_OK) return st;
   if (aux_stream && (!ev_input_ready || !ev_output_ready)) return GBMOE_INVALID_ARG;
   int sms;
   st = device_info(&sms);
@@ -887,9 +942,10 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
     cudaError_t ce = cudaEventRecord(ev_in, s);
     if (ce == cudaSuccess) ce = cudaStreamWaitEvent(aux, ev_in, 0);
     if (ce != cudaSuccess) return from_cuda(ce);
-    gbmoe_status_t st1 = moe_shared_expert_forward(x, M, K, Ns, w1s, w2s, GBMOE_BF16,
-                                                   activation, out_shared, ws_shared,
-                                                   ws_shared_bytes, err_word, aux_stream);
+    gbmoe_status_t st1 = moe_shared_expert_forward(x, M, K, Ns, w1s, w1s_scales, w2s,
+                                                   w2s_scales, shared_dtype, activation,
+                                                   out_shared, ws_shared, ws_shared_bytes,
+                                                   err_word, aux_stream);
     cudaError_t ce1 = cudaEventRecord(ev_out, aux);
     // the routed experts on `stream` meanwhile
     gbmoe_status_t st2 = moe_forward(x, logits, bias, M, K, N, E_global, expert_map, E, topk,
@@ -903,8 +959,9 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
     if (st2 != GBMOE_OK) return st2;
     return from_cuda(ce2);
   }
-  st = moe_shared_expert_forward(x, M, K, Ns, w1s, w2s, GBMOE_BF16, activation, out_shared,
-                                 ws_shared, ws_shared_bytes, err_word, stream);
+  st = moe_shared_expert_forward(x, M, K, Ns, w1s, w1s_scales, w2s, w2s_scales, shared_dtype,
+                                 activation, out_shared, ws_shared, ws_shared_bytes, err_word,
+                                 stream);
   if (st != GBMOE_OK) return st;
   return moe_forward(x, logits, bias, M, K, N, E_global, expert_map, E, topk, score_fn,
                      n_groups, topk_groups, renormalize, apply_router_weight_on_input,

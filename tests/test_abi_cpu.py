@@ -60,6 +60,15 @@ def test_workspace_sizes():
     assert g.moe_workspace_size(g.WS_FORWARD, 4, 2, 16512, 128, 1, g.FP8_E4M3) == 0
     assert g.moe_workspace_size(g.WS_FORWARD, 4, 2, 16512, 128, 1, g.BF16) > 0
     assert g.moe_workspace_size(g.WS_ALIGN, 8192, 256, 0, 0, 8, 0) == 32 * 256 * 4
+    # shared experts (M rows, Ns = N): H; e4m3 also H's group-major scales,
+    # the codes of x, x's scales row-major and group-major
+    M, Ns, K = 100, 256, 384
+    ld = (M + 3) // 4 * 4
+    assert g.moe_workspace_size(g.WS_SHARED, M, 1, Ns, K, 1, g.BF16) == -(-M * Ns * 2 // 256) * 256
+    assert g.moe_workspace_size(g.WS_SHARED, M, 1, Ns, K, 1, g.FP8_E4M3) == sum(
+        -(-b // 256) * 256 for b in (M * Ns, ld * (Ns // 128) * 4, M * K, M * (K // 128) * 4,
+                                     ld * (K // 128) * 4))
+    assert g.moe_workspace_size(g.WS_SHARED, M, 1, Ns, K, 1, g.FP8_E4M3_CHANNEL) == 0
     # EP dispatch (M tokens per shard, E routed experts, N = G shards): the
     # pairs' ids, the map, counts, offsets, sorted, inv, chunk histograms
     G, M, E, k = 4, 100, 64, 6
@@ -216,6 +225,45 @@ def test_forward_rejects_bad_arguments(lib):
     assert call(a6=16) == INVALID             # 16 routed experts, 8 local, no map
     assert call(a15=7) == INVALID             # activation
     assert call(a16=9) == UNSUPPORTED         # dtype
+
+
+def test_shared_experts_reject_bad_arguments(lib):
+    f = lib.moe_shared_expert_forward
+    #       x    M   K    Ns   w1s  w1ss  w2s  w2ss  dt act out  ws   wsb      err   s
+    args = [P16, 64, 256, 128, P16, None, P16, None, 0, 0, P16, P16, 1 << 30, None, None]
+
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a8=2) == UNSUPPORTED                  # per-channel e4m3
+    assert call(a8=1) == INVALID                      # e4m3 weights without scales
+    assert call(a8=1, a5=P16) == INVALID              # ... without w2s's scales
+    assert call(a8=1, a5=P16 + 2, a7=P16) == INVALID  # scales not 4-byte aligned
+    assert call(a3=100) == INVALID                    # Ns % 128
+    assert call(a2=16512, a8=1, a5=P16, a7=P16) == INVALID  # block-scaled K above 16384
+    assert call(a12=256) == INVALID                   # workspace too small
+    assert call(a9=3) == INVALID                      # activation
+    assert call(a4=P_ODD) == INVALID                  # misaligned weights
+    fs = lib.moe_forward_shared
+    #       x    lg   bias  M   K    N    Eg map   E  k  fn ng tg rn woi act dt
+    fargs = [P16, P16, None, 64, 256, 128, 8, None, 8, 2, 0, 1, 1, 1, 0, 0, 0,
+             P16, None, P16, None, P16, P16, 1 << 30, 128, P16, None, P16, None, 0,
+             P16, P16, 1 << 30, None, None, None, None, None]
+    #        w1   w1s   w2   w2s   out  ws   wsb     Ns   w1sh  ss   w2sh  ss   sdt
+    #        outsh wssh wsshb    err   s     aux   ev    ev
+
+    def fcall(**kw):
+        a = list(fargs)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return fs(*a)
+    assert fcall(a29=2) == UNSUPPORTED          # shared experts in per-channel e4m3
+    assert fcall(a29=1) == INVALID              # e4m3 shared experts without scales
+    assert fcall(a32=64) == INVALID             # shared workspace too small
+    assert fcall(a35=P16) == INVALID            # aux stream without its events
+    assert fcall(a16=9) == UNSUPPORTED          # routed dtype
 
 
 def test_selftest_rejects_bad_arguments(lib):

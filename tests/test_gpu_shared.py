@@ -1,6 +1,7 @@
 """Shared experts (a dense gated MLP on every token, returned beside the
-routed output) and their overlap with the routed experts on an auxiliary
-stream, the MULTI_STREAM_OVERLAPPED order of the SharedExperts page."""
+routed output), in bf16 or in e4m3 with block-scaled weights, and their
+overlap with the routed experts on an auxiliary stream, the
+MULTI_STREAM_OVERLAPPED order of the SharedExperts page."""
 import numpy as np
 import pytest
 import torch
@@ -46,22 +47,73 @@ def test_shared_expert_is_the_dense_mlp(act):
     assert_close_rel(out_s.float().cpu().numpy(), ref[0], TOL[WL.BF16], "shared")
 
 
-def test_overlapped_shared_experts_equal_the_separate_calls_and_replay():
+def _shared_e4m3(w1s, w2s):
+    """The library's 128 x 128 block quantisation of the shared weights:
+    (w1 codes, w1 scales, w2 codes, w2 scales)."""
     g = gbmoe()
-    cfg = WL.SMALL_SIGMOID
+    (Ns2, K), Ns = w1s.shape, w2s.shape[1]
+    q1 = torch.empty((Ns2, K), dtype=torch.uint8, device=DEV)
+    s1 = torch.empty((Ns2 // 128, K // 128), dtype=torch.float32, device=DEV)
+    q2 = torch.empty((K, Ns), dtype=torch.uint8, device=DEV)
+    s2 = torch.empty((K // 128, Ns // 128), dtype=torch.float32, device=DEV)
+    g.moe_quant_fp8_block(w1s, q1, s1)
+    g.moe_quant_fp8_block(w2s, q2, s2)
+    return q1, s1, q2, s2
+
+
+@pytest.mark.parametrize("cfg,act", [(WL.SMALL_BF16, 0), (WL.SMALL_BF16, 1),
+                                     (WL.SMALL_FP8_K640, 0)],
+                         ids=["M300_K512_silu", "M300_K512_gelu", "M300_K640_silu"])
+def test_shared_expert_e4m3_is_the_oracles_e4m3_mlp(cfg, act):
+    """e4m3 shared experts: x quantised in 1 x 128 groups inside the call,
+    128 x 128 weight blocks, h requantised -- against the oracle's e4m3
+    experts with one expert holding every token (ragged last m-tile; K = 640
+    leaves the second half of the last down tile past K)."""
+    g = gbmoe()
+    d = WL.make_inputs(cfg, DEV, with_weights=False)
+    M, K = cfg.M, cfg.K
+    w1s, w2s = _shared_weights(K, NS, 52)
+    q1, s1, q2, s2 = _shared_e4m3(w1s, w2s)
+    out_s = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = g.workspace(g.WS_SHARED, M, 1, NS, K, 1, g.FP8_E4M3)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    g.moe_shared_expert_forward(d["x"], NS, q1, q2, out_s, ws, dtype=g.FP8_E4M3, activation=act,
+                                err_word=err, w1s_scales=s1, w2s_scales=s2)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    oq1, os1 = orc.quant_fp8_block(WL.bf16_bits(w1s))
+    oq2, os2 = orc.quant_fp8_block(WL.bf16_bits(w2s))
+    # the weights the GPU ran with are the oracle's own block quantisation
+    assert np.array_equal(q1.cpu().numpy(), oq1) and np.array_equal(q2.cpu().numpy(), oq2)
+    assert np.array_equal(s1.cpu().numpy(), os1) and np.array_equal(s2.cpu().numpy(), os2)
+    W = orc.Weights(WL.FP8, experts={0: (oq1, oq2, os1, os2)}, E=1, N=NS, K=K, act=act)
+    ref, n = orc.batched_experts(WL.bf16_bits(d["x"])[None], np.array([M], np.int32), W,
+                                 requant_h=True)
+    assert n == M
+    assert_close_rel(out_s.float().cpu().numpy(), ref[0], TOL[WL.FP8], "shared e4m3")
+
+
+@pytest.mark.parametrize("cfg,shared_dtype", [(WL.SMALL_SIGMOID, WL.BF16), (WL.SMALL_FP8, WL.FP8)],
+                         ids=["bf16", "e4m3"])
+def test_overlapped_shared_experts_equal_the_separate_calls_and_replay(cfg, shared_dtype):
+    g = gbmoe()
     d = WL.make_inputs(cfg, DEV)
     gw = GpuWeights(cfg, d["w1"], d["w2"])
     w1s, w2s = _shared_weights(cfg.K, NS, 51)
+    s1 = s2 = None
+    if shared_dtype == WL.FP8:
+        w1s, s1, w2s, s2 = _shared_e4m3(w1s, w2s)
+    sh = dict(dtype=shared_dtype, w1s_scales=s1, w2s_scales=s2)
     M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
     ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype)
-    ws_s = g.workspace(g.WS_SHARED, M, 1, NS, K, 1, g.BF16)
+    ws_s = g.workspace(g.WS_SHARED, M, 1, NS, K, 1, shared_dtype)
     args = (d["logits"], d["bias"], N, E, k, cfg.score_fn, cfg.n_groups, cfg.topk_groups,
             cfg.renorm, cfg.dtype, gw.w1, gw.w1s, gw.w2, gw.w2s)
     # separate calls on one stream
     ref_out = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
     ref_sh = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
     g.moe_forward(d["x"], *args, ref_out, ws)
-    g.moe_shared_expert_forward(d["x"], NS, w1s, w2s, ref_sh, ws_s)
+    g.moe_shared_expert_forward(d["x"], NS, w1s, w2s, ref_sh, ws_s, **sh)
     # overlapped
     aux = torch.cuda.Stream()
     ev_in = torch.cuda.Event()
@@ -70,11 +122,12 @@ def test_overlapped_shared_experts_equal_the_separate_calls_and_replay():
     out = torch.empty_like(ref_out)
     out_sh = torch.empty_like(ref_sh)
     ws2 = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype)
-    ws2_s = g.workspace(g.WS_SHARED, M, 1, NS, K, 1, g.BF16)
+    ws2_s = g.workspace(g.WS_SHARED, M, 1, NS, K, 1, shared_dtype)
 
     def run():
         g.moe_forward_shared(x, *args, out, ws2, NS, w1s, w2s, out_sh, ws2_s,
-                             aux_stream=aux, ev_input_ready=ev_in, ev_output_ready=ev_out)
+                             aux_stream=aux, ev_input_ready=ev_in, ev_output_ready=ev_out,
+                             shared_dtype=shared_dtype, w1s_scales=s1, w2s_scales=s2)
 
     run()
     torch.cuda.synchronize()
@@ -94,7 +147,38 @@ def test_overlapped_shared_experts_equal_the_separate_calls_and_replay():
     graph.replay()
     torch.cuda.synchronize()
     g.moe_forward(x2, *args, ref_out, ws)
-    g.moe_shared_expert_forward(x2, NS, w1s, w2s, ref_sh, ws_s)
+    g.moe_shared_expert_forward(x2, NS, w1s, w2s, ref_sh, ws_s, **sh)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(out_sh.view(torch.int16), ref_sh.view(torch.int16))
+
+
+def test_shared_expert_e4m3_full_size_sampled():
+    """The DeepSeek-V3-shaped shared expert (K = 7168, Ns = 2048) on 8192
+    tokens in e4m3: 512 seeded rows plus the first and the last against the
+    oracle's e4m3 expert, and the whole output finite."""
+    g = gbmoe()
+    M, K, Ns = 8192, 7168, 2048
+    gen = torch.Generator(device=DEV).manual_seed(53)
+    x = torch.randn((M, K), generator=gen, device=DEV).to(torch.bfloat16)
+    w1s, w2s = _shared_weights(K, Ns, 54)
+    q1, s1, q2, s2 = _shared_e4m3(w1s, w2s)
+    out_s = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    ws = g.workspace(g.WS_SHARED, M, 1, Ns, K, 1, g.FP8_E4M3)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    g.moe_shared_expert_forward(x, Ns, q1, q2, out_s, ws, dtype=g.FP8_E4M3, err_word=err,
+                                w1s_scales=s1, w2s_scales=s2)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert bool(torch.isfinite(out_s.float()).all())
+    rows = np.unique(np.concatenate([[0, M - 1],
+                                     np.random.default_rng(55).choice(M, 512, replace=False)]))
+    oq1, os1 = orc.quant_fp8_block(WL.bf16_bits(w1s))
+    oq2, os2 = orc.quant_fp8_block(WL.bf16_bits(w2s))
+    W = orc.Weights(WL.FP8, experts={0: (oq1, oq2, os1, os2)}, E=1, N=Ns, K=K)
+    sel = np.stack([np.zeros_like(rows), rows], 1)
+    ref, n = orc.batched_experts(WL.bf16_bits(x)[None], np.array([M], np.int32), W,
+                                 rows=sel, requant_h=True)
+    assert n == len(rows)
+    got = out_s.float().cpu().numpy()
+    assert_close_rel(got[rows], ref[0][rows], TOL[WL.FP8], "shared e4m3 full size")
