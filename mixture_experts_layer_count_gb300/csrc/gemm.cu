@@ -340,7 +340,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
 
-// looked up once per process (the driver entry point is not per device);
+// looked up once per process (the CUDA driver API entry point is not per
+// device);
 // std::call_once makes concurrent first calls from several threads safe
 bool resolve_encode() {
   std::call_once(g_encode_once, [] {

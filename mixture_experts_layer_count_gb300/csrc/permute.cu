@@ -130,9 +130,9 @@ __global__ void __launch_bounds__(1024)
   if (e == E - 1) offsets[E] = incl;
 }
 
-// pass 3: each block walks its chunk in order, 256 pairs per round; a pair's
-// position = chunk base of its expert + pairs of that expert in earlier rounds
-// + in earlier warps of this round + in lower lanes of its warp.
+// pass 3: each block walks its chunk in order, 256 pairs per step; a pair's
+// position = chunk base of its expert + pairs of that expert in earlier steps
+// + in earlier warps of this step + in lower lanes of its warp.
 __global__ void __launch_bounds__(kAlignThreads)
     align_scatter_kernel(const int32_t *__restrict__ ids, int P, int Eg,
                          const int32_t *__restrict__ map, int E,
