@@ -75,7 +75,7 @@ def _load():
             lib.orc_moe_forward_ep.restype = None
             lib.orc_moe_forward_ep.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I,
                                                I, I, P, I, I, P, P, P, P, P, I,
-                                               P, P, P, I, I]
+                                               P, P, P, I, I, P]
             lib.orc_permute_rows.restype = None
             lib.orc_permute_rows.argtypes = [P, P, I, I, I, P]
             lib.orc_unpermute_reduce.restype = None
@@ -86,6 +86,8 @@ def _load():
             lib.orc_quant_fp8_block.argtypes = [P, I, I, I, P, P]
             lib.orc_quant_fp8_tensor.restype = None
             lib.orc_quant_fp8_tensor.argtypes = [P, P, I, I, P, P]
+            lib.orc_quant_fp8_tensor_static.restype = None
+            lib.orc_quant_fp8_tensor_static.argtypes = [P, P, I, I, ctypes.c_float, P]
             lib.orc_expert_row.restype = None
             lib.orc_expert_row.argtypes = [I, P, I, I, I, I, I, P, P, P, P, I,
                                            P, P, I]
@@ -214,15 +216,20 @@ def quant_fp8_group(x_bf16_bits, group=128, row_weights=None):
     return q, s
 
 
-def quant_fp8_tensor(x_bf16_bits, row_weights=None):
+def quant_fp8_tensor(x_bf16_bits, row_weights=None, scale=None):
     """x (M, K) bf16 bits -> q (M, K) codes and the one scale of the tensor
-    (rows multiplied by row_weights in fp32 first when given)."""
+    (rows multiplied by row_weights in fp32 first when given).  With `scale`
+    (a static activation scale, Q8) the codes use it instead of the
+    tensor's maximum (saturating at +-448) and it is returned."""
     lib = _load()
     x = _c(x_bf16_bits, np.uint16)
     M, K = x.shape
     q = np.empty((M, K), np.uint8)
-    s = np.empty((1,), np.float32)
     rw = _c(row_weights, np.float32)
+    if scale is not None:
+        lib.orc_quant_fp8_tensor_static(_p(x), _p(rw), M, K, float(np.float32(scale)), _p(q))
+        return q, np.float32(scale)
+    s = np.empty((1,), np.float32)
     lib.orc_quant_fp8_tensor(_p(x), _p(rw), M, K, _p(q), _p(s))
     return q, s[0]
 
@@ -304,12 +311,13 @@ def expert_row(x_bf16_bits, t, e, W: Weights, requant_h=False):
 def moe_forward(x_bf16_bits, logits, bias, topk, score_fn, W: Weights,
                 n_groups=1, topk_groups=1, renorm=True, requant_h=False,
                 tokens=None, nthreads=0, expert_map=None,
-                weight_on_input=False):
+                weight_on_input=False, static_scales=None):
     """The layer in the Standard format for the listed tokens (all when None).
     logits (M, E) cover the E routed (global) experts; W holds W.E local
     experts, reached through expert_map (E) when given (-1: not local, the
     pair adds nothing).  weight_on_input: the router weight scales the
-    expert's input instead of its output.
+    expert's input instead of its output.  static_scales (FP8_TENSOR only):
+    (scale of x, scale of H) given instead of the tensors' maxima (Q8).
     Returns out (n, K) fp64, ids (n, topk) int32 (global), weights (n, topk)."""
     lib = _load()
     x = _c(x_bf16_bits, np.uint16)
@@ -325,11 +333,13 @@ def moe_forward(x_bf16_bits, logits, bias, topk, score_fn, W: Weights,
     out = np.empty((n, K), np.float64)
     ids = np.empty((n, topk), np.int32)
     w = np.empty((n, topk), np.float64)
+    assert static_scales is None or W.dtype == FP8_TENSOR
+    ss = None if static_scales is None else np.asarray(static_scales, np.float32).reshape(2)
     lib.orc_moe_forward_ep(_p(x), _p(logits), _p(bias), M, K, W.N, E, topk,
                            score_fn, n_groups, topk_groups, int(renorm), W.dtype,
                            int(requant_h), _p(emap), W.E, int(weight_on_input),
                            _p(W.w1), _p(W.w1s), _p(W.w2), _p(W.w2s), _p(tok), n,
-                           _p(ids), _p(w), _p(out), int(nthreads), int(W.act))
+                           _p(ids), _p(w), _p(out), int(nthreads), int(W.act), _p(ss))
     return out, ids, w
 
 

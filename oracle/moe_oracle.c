@@ -73,6 +73,10 @@
  *      scale for the layer's input x (all M tokens) and one for H (every
  *      routed pair's hidden row, kept in bf16 as in Q6); weights as in Q6
  *      (per-tensor weight scales are equal per-row scales).
+ *   Q8 static per-tensor activation scales (the quant config's a1_scale and
+ *      a2_scale, FusedMoEPrepareAndFinalize.prepare): as Q7, but the scale of
+ *      x and the scale of H are given instead of taken from the tensors'
+ *      maxima; q = e4m3(v / scale), saturating at +-448 like every code.
  */
 #include <math.h>
 #include <stdint.h>
@@ -503,6 +507,20 @@ void orc_quant_fp8_group(const uint16_t *x, int M, int K, int group,
     orc_quant_fp8_group_w(x, NULL, M, K, group, q, scales);
 }
 
+/* Q8: the codes of x (times row_w[t] in fp32 when given) with a given
+ * scale: q = e4m3(v / scale), saturating. */
+void orc_quant_fp8_tensor_static(const uint16_t *x, const float *row_w, int M,
+                                 int K, float scale, uint8_t *q)
+{
+    int t, k;
+    for (t = 0; t < M; ++t) {
+        const float rw = row_w ? row_w[t] : 1.0f;
+        for (k = 0; k < K; ++k)
+            q[(size_t)t * K + k] =
+                orc_e4m3_encode(((float)bf16_value(x[(size_t)t * K + k]) * rw) / scale);
+    }
+}
+
 /* Q7: one group holding all M rows of x (times row_w[t] in fp32 when given):
  * *scale = max(amax, 1e-12) / 448, q = e4m3(v / scale). */
 void orc_quant_fp8_tensor(const uint16_t *x, const float *row_w, int M, int K,
@@ -731,8 +749,9 @@ void orc_expert_row(int dtype, const uint16_t *x, int t, int e, int E, int N,
 /* The layer with per-tensor activation scales (Q7).  The scale of H spans
  * every routed pair, so this takes two passes: first x's scale and every
  * local pair's hidden row (all M tokens, whatever `tokens` lists), then the
- * scale of H and the outputs of the listed tokens.  Arguments as
- * orc_moe_forward_ep. */
+ * scale of H and the outputs of the listed tokens.  static_scales (Q8):
+ * NULL, or {scale of x, scale of H} given instead of the maxima's.
+ * Arguments as orc_moe_forward_ep. */
 static void forward_tensor(const uint16_t *x, const float *logits,
                            const float *bias, int M, int K, int N, int E,
                            int topk, int score_fn, int n_groups,
@@ -740,7 +759,7 @@ static void forward_tensor(const uint16_t *x, const float *logits,
                            const int32_t *expert_map, int E_local,
                            int weight_on_input, const orc_weights *W,
                            const int32_t *tokens, int n_tok, int32_t *ids_out,
-                           double *w_out, double *out)
+                           double *w_out, double *out, const float *static_scales)
 {
     const size_t P = (size_t)M * topk;
     int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (P ? P : 1));
@@ -760,7 +779,12 @@ static void forward_tensor(const uint16_t *x, const float *logits,
                   w + (size_t)t * topk, NULL);
         rw[t] = (float)w[(size_t)t * topk]; /* weight on input: topk is 1 */
     }
-    orc_quant_fp8_tensor(x, weight_on_input ? rw : NULL, M, K, xq, &sx);
+    if (static_scales) {
+        sx = static_scales[0];
+        orc_quant_fp8_tensor_static(x, weight_on_input ? rw : NULL, M, K, sx, xq);
+    } else {
+        orc_quant_fp8_tensor(x, weight_on_input ? rw : NULL, M, K, xq, &sx);
+    }
     for (t = 0; t < M; ++t) {
         for (k = 0; k < K; ++k)
             xr[k] = orc_e4m3_value(xq[(size_t)t * K + k]) * (double)sx;
@@ -781,7 +805,7 @@ static void forward_tensor(const uint16_t *x, const float *logits,
         }
     }
     if (requant_h)
-        sh = group_scale(amax);
+        sh = static_scales ? static_scales[1] : group_scale(amax);
     if (!tokens)
         n_tok = M;
     for (i = 0; i < n_tok; ++i) {
@@ -817,7 +841,8 @@ void orc_moe_forward_ep(const uint16_t *x, const float *logits,
                         const float *const *w1s, const void *const *w2,
                         const float *const *w2s, const int32_t *tokens,
                         int n_tok, int32_t *ids_out, double *w_out,
-                        double *out, int nthreads, int act)
+                        double *out, int nthreads, int act,
+                        const float *static_scales)
 {
     int i;
     orc_weights W;
@@ -827,7 +852,8 @@ void orc_moe_forward_ep(const uint16_t *x, const float *logits,
     if (dtype == ORC_FP8_TENSOR) {
         forward_tensor(x, logits, bias, M, K, N, E, topk, score_fn, n_groups,
                        topk_groups, renorm, requant_h, expert_map, E_local,
-                       weight_on_input, &W, tokens, n_tok, ids_out, w_out, out);
+                       weight_on_input, &W, tokens, n_tok, ids_out, w_out, out,
+                       static_scales);
         return;
     }
     if (!tokens)
@@ -886,7 +912,7 @@ void orc_moe_forward(const uint16_t *x, const float *logits, const float *bias,
     orc_moe_forward_ep(x, logits, bias, M, K, N, E, topk, score_fn, n_groups,
                        topk_groups, renorm, dtype, requant_h, NULL, E, 0, w1,
                        w1s, w2, w2s, tokens, n_tok, ids_out, w_out, out,
-                       nthreads, ORC_SILU);
+                       nthreads, ORC_SILU, NULL);
 }
 
 /* ------------------------------------------------------------------------ */

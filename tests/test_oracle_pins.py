@@ -592,3 +592,76 @@ def test_fp8_tensor_layer_uses_one_scale_for_all_hidden_rows(orc):
     ref = np.stack([hd[t] @ deq(q2[ref_ids[t]], s2[ref_ids[t]].astype(np.float64)[:, None]).T
                     for t in range(cfg.M)])
     np.testing.assert_allclose(out, ref, rtol=0, atol=2e-3 * np.abs(ref).max())
+
+
+def _clamped_cast(v32, s):
+    """e4m3 codes of v / s saturating at +-448: numpy's fp32 quotient,
+    clamped, then torch's cast (which itself saturates only up to 464)."""
+    qv = np.clip((v32 / np.float32(s)).astype(np.float32), -448.0, 448.0)
+    return torch.from_numpy(qv).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_fp8_tensor_static_quant_is_the_clamped_cast(orc):
+    """Static per-tensor activation scale (the quant config's a1_scale): the
+    codes of x / s for the given s, values beyond 448 s saturating; with s
+    the tensor's own max / 448 they are the dynamic quantiser's codes."""
+    g = torch.Generator().manual_seed(45)
+    x = (torch.randn((9, 256), generator=g) * torch.linspace(0.1, 5, 9)[:, None]).to(torch.bfloat16)
+    rw = (torch.rand(9, generator=g) + 0.1).numpy().astype(np.float32)
+    for w in (None, rw):
+        v = (x.float().numpy() * (1.0 if w is None else w[:, None])).astype(np.float32)
+        s_dyn = np.float32(np.abs(v).max()) / np.float32(448)
+        for s in (s_dyn, s_dyn * np.float32(0.25), s_dyn * np.float32(3.0)):
+            q, sc = orc.quant_fp8_tensor(_bits(x), row_weights=w, scale=s)
+            assert sc == np.float32(s)
+            np.testing.assert_array_equal(q, _clamped_cast(v, s))
+        # a quarter of the dynamic scale saturates the largest values
+        q, _ = orc.quant_fp8_tensor(_bits(x), row_weights=w, scale=s_dyn * np.float32(0.25))
+        assert np.any((q & 0x7f) == 0x7e)
+        qd, sd = orc.quant_fp8_tensor(_bits(x), row_weights=w)
+        qs, _ = orc.quant_fp8_tensor(_bits(x), row_weights=w, scale=sd)
+        np.testing.assert_array_equal(qs, qd)
+
+
+def test_fp8_tensor_static_layer_uses_the_given_scales(orc):
+    """Static per-tensor activation scales a1 (for x) and a2 (for H), two
+    experts, top-1: x coded with a1, every routed hidden row rounded to bf16
+    and coded with a2, both saturating -- written with numpy, torch's casts
+    and the routing's argmax."""
+    cfg = WL.MoEConfig("f8s", M=10, K=256, N=256, E=2, topk=1, seed=27)
+    d = WL.make_inputs(cfg)
+    N = cfg.N
+    q1, s1, q2, s2 = [], [], [], []
+    for e in range(2):
+        a, b = _rowwise_quant_torch(d["w1"][e].float().numpy())
+        c, dd = _rowwise_quant_torch(d["w2"][e].float().numpy())
+        q1.append(a); s1.append(b); q2.append(c); s2.append(dd)
+    W = orc.Weights(orc.FP8_TENSOR, np.stack(q1), np.stack(q2), np.stack(s1), np.stack(s2))
+    ref_ids = np.argmax(d["logits"].numpy(), axis=1)
+    x32 = d["x"].float().numpy()
+    a1 = np.float32(np.abs(x32).max()) / np.float32(448) * np.float32(0.5)  # saturates x's tail
+
+    def deq(q, s):
+        return torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy() * s
+
+    xd = deq(_clamped_cast(x32, a1), float(a1))
+    hs = []
+    for t in range(cfg.M):
+        e = ref_ids[t]
+        w1d = deq(q1[e], s1[e].astype(np.float64)[:, None])
+        hs.append(_silu(xd[t] @ w1d[:N].T) * (xd[t] @ w1d[N:].T))
+    hb = torch.from_numpy(np.stack(hs).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    a2 = np.float32(np.abs(hb).max()) / np.float32(448) * np.float32(0.7)  # saturates H's tail
+    hq = _clamped_cast(hb, a2)
+    assert np.any((hq & 0x7f) == 0x7e)
+    hd = deq(hq, float(a2))
+    ref = np.stack([hd[t] @ deq(q2[ref_ids[t]], s2[ref_ids[t]].astype(np.float64)[:, None]).T
+                    for t in range(cfg.M)])
+    out, ids, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1, orc.SOFTMAX,
+                                  W, requant_h=True, static_scales=(a1, a2))
+    assert np.array_equal(ids[:, 0], ref_ids)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=2e-3 * np.abs(ref).max())
+    # and not the layer with the tensors' own scales
+    dyn, _, _ = orc.moe_forward(_bits(d["x"]), d["logits"].numpy(), None, 1, orc.SOFTMAX,
+                                W, requant_h=True)
+    assert np.abs(dyn - out).max() > 1e-3 * np.abs(ref).max()
