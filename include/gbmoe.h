@@ -215,6 +215,17 @@ gbmoe_status_t moe_quant_fp8_tensor(const uint16_t *x, const float *row_weights,
                                     uint8_t *q, float *row_scales,
                                     uint32_t *amax_ws, gbmoe_stream_t stream);
 
+/* The same quantiser with a static per-tensor scale (the quant config's
+ * a1_scale / a2_scale): scale is a DEVICE fp32 scalar (4-byte aligned), and
+ *   q[t,k] = e4m3(v[t,k] / scale)   (IEEE division, saturating at +-448),
+ *   row_scales[t] = scale            for every t < n,
+ * with v, n_rows, x, q, row_scales as in moe_quant_fp8_tensor.  One launch
+ * on `stream`.  K % 128 == 0; x, q 16-byte aligned. */
+gbmoe_status_t moe_quant_fp8_tensor_static(const uint16_t *x, const float *row_weights,
+                                           int M, int K, const int32_t *n_rows,
+                                           const float *scale, uint8_t *q, float *row_scales,
+                                           gbmoe_stream_t stream);
+
 /* The same quantiser over block x block tiles of a weight matrix, for
  * preparing FP8 expert weights (not part of the timed layer):
  * w (R, C) bf16 -> q (R, C) e4m3 and scales (R/block, C/block) fp32, one
@@ -393,7 +404,13 @@ gbmoe_status_t moe_batched_masked_experts(
  *   (E, 2N) / (E, K); the activations are quantised with one scale per
  *   token, H is kept in bf16 and quantised per token before the second GEMM.
  * dtype GBMOE_FP8_E4M3_TENSOR: the same weights; x is quantised with one
- *   scale for all M tokens and H with one for all its computed rows.
+ *   scale for all M tokens and H with one for all its computed rows.  The
+ *   scales are the tensors' own maxima / 448 (dynamic), or the caller's
+ *   static scales: a1_scale for x and a2_scale for H (the quant config's
+ *   a1_scale / a2_scale, FusedMoEPrepareAndFinalize.prepare), each a DEVICE
+ *   fp32 scalar (4-byte aligned) or NULL for the dynamic scale; codes are
+ *   e4m3(v / scale), saturating at +-448.  With any other dtype both must be
+ *   NULL (GBMOE_INVALID_ARG otherwise).
  * out (M, K) bf16.  topk_ids / topk_weights (M, topk) may be NULL; when given
  * they receive the router's output (global ids).
  * ws: moe_workspace_size(GBMOE_WS_FORWARD, M, E, N, K, topk, dtype) bytes.
@@ -406,6 +423,7 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                            int activation, int dtype, const void *w1,
                            const float *w1_scales,
                            const void *w2, const float *w2_scales,
+                           const float *a1_scale, const float *a2_scale,
                            uint16_t *out, int32_t *topk_ids,
                            float *topk_weights, void *ws, size_t ws_bytes,
                            int32_t *err_word, gbmoe_stream_t stream);
@@ -415,8 +433,9 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
  * its workspaces -- but with every chunk's counts computed on the device (the
  * pages copy them to the host per chunk), so the whole loop stays
  * capturable.  Each token's result is the same as unchunked, bit for bit --
- * except with GBMOE_FP8_E4M3_TENSOR, whose activation scales are then taken
- * per chunk (as the chunk loop quantises each chunk on its own).
+ * except with GBMOE_FP8_E4M3_TENSOR and dynamic scales, which are then taken
+ * per chunk (as the chunk loop quantises each chunk on its own); static
+ * scales (a1_scale, a2_scale) give the unchunked result.
  * Arguments as moe_forward (topk_ids / topk_weights may be NULL);
  * ws: moe_workspace_size(GBMOE_WS_FORWARD, min(M, chunk_size), E, N, K,
  * topk, dtype) bytes. */
@@ -428,7 +447,8 @@ gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
                                    int apply_router_weight_on_input,
                                    int activation, int dtype, const void *w1,
                                    const float *w1_scales, const void *w2,
-                                   const float *w2_scales, uint16_t *out,
+                                   const float *w2_scales, const float *a1_scale,
+                                   const float *a2_scale, uint16_t *out,
                                    int32_t *topk_ids, float *topk_weights,
                                    int chunk_size, void *ws, size_t ws_bytes,
                                    int32_t *err_word, gbmoe_stream_t stream);
@@ -482,7 +502,8 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
                                   int apply_router_weight_on_input,
                                   int activation, int dtype, const void *w1,
                                   const float *w1_scales, const void *w2,
-                                  const float *w2_scales, uint16_t *out,
+                                  const float *w2_scales, const float *a1_scale,
+                                  const float *a2_scale, uint16_t *out,
                                   void *ws, size_t ws_bytes, int Ns,
                                   const void *w1s, const float *w1s_scales,
                                   const void *w2s, const float *w2s_scales,

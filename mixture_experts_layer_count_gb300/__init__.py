@@ -49,16 +49,18 @@ _SIGS = {
     "moe_count_expert_tokens": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_align_permute": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
     "moe_forward_chunked": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
-                                 _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
+                                 _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P,
+                                 _P]),
     "moe_shared_expert_forward": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _Z,
                                        _P, _P]),
     "moe_forward_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
-                                _I, _I, _P, _P, _P, _P, _P, _P, _Z, _I, _P, _P, _P, _P, _I,
-                                _P, _P, _Z, _P, _P, _P, _P, _P]),
+                                _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _P, _P, _P,
+                                _P, _I, _P, _P, _Z, _P, _P, _P, _P, _P]),
     "moe_align_permute_no_ws": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "gbmoe_selftest_bounded_wait": (_I, [_P, _I, _P]),
     "moe_quant_fp8_group": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_quant_fp8_tensor": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_quant_fp8_tensor_static": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
     "moe_permute_rows": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm_gate_up_silu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
@@ -75,7 +77,7 @@ _SIGS = {
     "moe_batched_masked_experts": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                         _I, _I, _P, _P, _Z, _P, _P]),
     "moe_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I,
-                         _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P]),
+                         _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P, _P]),
 }
 
 
@@ -202,6 +204,17 @@ def moe_quant_fp8_tensor(x, q, row_scales, amax_ws, n_rows=None, stream=None,
         _ptr(amax_ws), _stream(stream)))
 
 
+def moe_quant_fp8_tensor_static(x, scale, q, row_scales, n_rows=None, stream=None,
+                                row_weights=None):
+    """The per-tensor quantiser with a static scale (a device fp32 scalar):
+    q = e4m3(x / scale) saturating, row_scales (M) = scale for every row
+    (rows < *n_rows when n_rows is given)."""
+    M, K = x.shape
+    _check("moe_quant_fp8_tensor_static", load().moe_quant_fp8_tensor_static(
+        _ptr(x), _ptr(row_weights), M, K, _ptr(n_rows), _ptr(scale), _ptr(q), _ptr(row_scales),
+        _stream(stream)))
+
+
 def moe_quant_fp8_block(w, q, scales, block=128, stream=None):
     R = w.numel() // w.shape[-1]
     C = w.shape[-1]
@@ -293,10 +306,11 @@ def moe_forward(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
                 renormalize, dtype, w1, w1_scales, w2, w2_scales, out, ws,
                 topk_ids=None, topk_weights=None, err_word=None, stream=None,
                 expert_map=None, apply_router_weight_on_input=False,
-                activation=ACT_SILU):
+                activation=ACT_SILU, a1_scale=None, a2_scale=None):
     """The whole Standard layer.  E is the number of local experts (w1.shape[0]);
     the router picks among logits.shape[1] experts, mapped to local ones by
-    expert_map when given."""
+    expert_map when given.  a1_scale / a2_scale: static activation scales
+    (device fp32 scalars) for FP8_E4M3_TENSOR, None for the dynamic ones."""
     M, K = x.shape
     E_global = logits.shape[1]
     _check("moe_forward", load().moe_forward(
@@ -304,7 +318,8 @@ def moe_forward(x, logits, bias, N, E, topk, score_fn, n_groups, topk_groups,
         topk, score_fn, n_groups, topk_groups, int(renormalize),
         int(apply_router_weight_on_input), int(activation), dtype, _ptr(w1),
         _ptr(w1_scales),
-        _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
+        _ptr(w2), _ptr(w2_scales), _ptr(a1_scale), _ptr(a2_scale), _ptr(out), _ptr(topk_ids),
+        _ptr(topk_weights),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(err_word),
         _stream(stream)))
 
@@ -313,7 +328,7 @@ def moe_forward_chunked(x, logits, bias, N, E, topk, score_fn, n_groups, topk_gr
                         renormalize, dtype, w1, w1_scales, w2, w2_scales, out, ws,
                         chunk_size, topk_ids=None, topk_weights=None, err_word=None,
                         stream=None, expert_map=None, apply_router_weight_on_input=False,
-                        activation=ACT_SILU):
+                        activation=ACT_SILU, a1_scale=None, a2_scale=None):
     """moe_forward in chunks of chunk_size tokens (ws sized for one chunk)."""
     M, K = x.shape
     E_global = logits.shape[1]
@@ -321,8 +336,8 @@ def moe_forward_chunked(x, logits, bias, N, E, topk, score_fn, n_groups, topk_gr
         _ptr(x), _ptr(logits), _ptr(bias), M, K, N, E_global, _ptr(expert_map), E,
         topk, score_fn, n_groups, topk_groups, int(renormalize),
         int(apply_router_weight_on_input), int(activation), dtype, _ptr(w1),
-        _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(topk_ids),
-        _ptr(topk_weights), int(chunk_size), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), _ptr(a1_scale), _ptr(a2_scale), _ptr(out),
+        _ptr(topk_ids), _ptr(topk_weights), int(chunk_size), _ptr(ws), ws.numel() * ws.element_size(),
         _ptr(err_word), _stream(stream)))
 
 
@@ -354,7 +369,8 @@ def moe_forward_shared(x, logits, bias, N, E, topk, score_fn, n_groups,
                        aux_stream=None, ev_input_ready=None, ev_output_ready=None,
                        err_word=None, stream=None, expert_map=None,
                        apply_router_weight_on_input=False, activation=ACT_SILU,
-                       shared_dtype=BF16, w1s_scales=None, w2s_scales=None):
+                       shared_dtype=BF16, w1s_scales=None, w2s_scales=None, a1_scale=None,
+                       a2_scale=None):
     """moe_forward with the shared experts overlapped on aux_stream (a
     torch.cuda.Stream) through two torch.cuda.Event objects; the shared
     experts in shared_dtype (BF16, or FP8_E4M3 with block scales)."""
@@ -364,7 +380,8 @@ def moe_forward_shared(x, logits, bias, N, E, topk, score_fn, n_groups,
         _ptr(x), _ptr(logits), _ptr(bias), M, K, N, E_global, _ptr(expert_map), E,
         topk, score_fn, n_groups, topk_groups, int(renormalize),
         int(apply_router_weight_on_input), int(activation), dtype, _ptr(w1),
-        _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), _ptr(out), _ptr(ws),
+        _ptr(w1_scales), _ptr(w2), _ptr(w2_scales), _ptr(a1_scale), _ptr(a2_scale), _ptr(out),
+        _ptr(ws),
         ws.numel() * ws.element_size(), Ns, _ptr(w1s), _ptr(w1s_scales), _ptr(w2s),
         _ptr(w2s_scales), int(shared_dtype), _ptr(out_shared),
         _ptr(ws_shared), ws_shared.numel() * ws_shared.element_size(), _ptr(err_word),

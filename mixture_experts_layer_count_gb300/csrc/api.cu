@@ -443,7 +443,23 @@ gbmoe_status_t moe_quant_fp8_tensor(const uint16_t *x, const float *row_weights,
   if (st != GBMOE_OK) return st;
   if (M == 0) return GBMOE_OK;
   return from_cuda(launch_quant_tensor(x, row_weights, M, K, n_rows, q, row_scales, amax_ws,
-                                       sms, (cudaStream_t)stream));
+                                       nullptr, sms, (cudaStream_t)stream));
+}
+
+gbmoe_status_t moe_quant_fp8_tensor_static(const uint16_t *x, const float *row_weights,
+                                           int M, int K, const int32_t *n_rows,
+                                           const float *scale, uint8_t *q, float *row_scales,
+                                           gbmoe_stream_t stream) {
+  if (M < 0 || K < 128 || K % 128 != 0) return GBMOE_INVALID_ARG;
+  if (M > 0 && (!x || !q || !row_scales || !scale || !aligned16(x) || !aligned16(q) ||
+                reinterpret_cast<uintptr_t>(scale) % 4 != 0))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK) return st;
+  if (M == 0) return GBMOE_OK;
+  return from_cuda(launch_quant_tensor(x, row_weights, M, K, n_rows, q, row_scales, nullptr,
+                                       scale, sms, (cudaStream_t)stream));
 }
 
 gbmoe_status_t moe_quant_fp8_block(const uint16_t *w, int64_t R, int C,
@@ -689,9 +705,14 @@ static gbmoe_status_t forward_validate(const uint16_t *x, const float *logits,
                                        int topk_groups, int apply_router_weight_on_input,
                                        int activation, int dtype, const void *w1,
                                        const float *w1_scales, const void *w2,
-                                       const float *w2_scales, const uint16_t *out,
+                                       const float *w2_scales, const float *a1_scale,
+                                       const float *a2_scale, const uint16_t *out,
                                        const void *ws, size_t ws_bytes) {
   if (!valid_dtype(dtype)) return GBMOE_UNSUPPORTED;
+  // static activation scales: per-tensor e4m3 only, each a device fp32
+  if ((a1_scale || a2_scale) && dtype != GBMOE_FP8_E4M3_TENSOR) return GBMOE_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a1_scale) & 3u) || (reinterpret_cast<uintptr_t>(a2_scale) & 3u))
+    return GBMOE_INVALID_ARG;
   if (!gemm_shape_ok(M, topk, E, N, K, dtype)) return GBMOE_INVALID_ARG;
   if (!map_args_ok(E_global, expert_map, E)) return GBMOE_INVALID_ARG;
   if (!route_args_ok(M, E_global, topk, score_fn, bias, n_groups, topk_groups))
@@ -720,13 +741,15 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
                            int activation, int dtype, const void *w1,
                            const float *w1_scales,
                            const void *w2, const float *w2_scales,
+                           const float *a1_scale, const float *a2_scale,
                            uint16_t *out, int32_t *topk_ids,
                            float *topk_weights, void *ws, size_t ws_bytes,
                            int32_t *err_word, gbmoe_stream_t stream) {
   gbmoe_status_t vst = forward_validate(x, logits, bias, M, K, N, E_global, expert_map, E,
                                         topk, score_fn, n_groups, topk_groups,
                                         apply_router_weight_on_input, activation, dtype, w1,
-                                        w1_scales, w2, w2_scales, out, ws, ws_bytes);
+                                        w1_scales, w2, w2_scales, a1_scale, a2_scale, out, ws,
+                                        ws_bytes);
   if (vst != GBMOE_OK) return vst;
   const bool fp8 = is_fp8(dtype);
   const bool fp8ch = row_scaled(dtype);
@@ -760,7 +783,8 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
     if (ce != cudaSuccess) return from_cuda(ce);
   } else {
     if (fp8) {
-      ce = fp8t ? launch_quant_tensor(x, in_w, M, K, nullptr, w.xq, w.xs, w.amax, sms, s)
+      ce = fp8t ? launch_quant_tensor(x, in_w, M, K, nullptr, w.xq, w.xs, w.amax, a1_scale, sms,
+                                      s)
                 : launch_quant_row(x, in_w, M, K, w.xq, w.xs, sms, s);
       if (ce != cudaSuccess) return from_cuda(ce);
       a_src = w.xq;
@@ -777,7 +801,7 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   if (st != GBMOE_OK) return st;
   if (fp8t) {  // rows at and beyond offsets[E] (pairs not computed here) do not count
     ce = launch_quant_tensor(w.Hb, nullptr, P, N, w.offsets + E, static_cast<uint8_t *>(w.H),
-                             w.Hs, w.amax + 1, sms, s);
+                             w.Hs, w.amax + 1, a2_scale, sms, s);
     if (ce != cudaSuccess) return from_cuda(ce);
   } else if (fp8ch) {
     ce = launch_quant_row(w.Hb, nullptr, P, N, static_cast<uint8_t *>(w.H), w.Hs, sms, s);
@@ -797,7 +821,8 @@ gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
                                    int apply_router_weight_on_input,
                                    int activation, int dtype, const void *w1,
                                    const float *w1_scales, const void *w2,
-                                   const float *w2_scales, uint16_t *out,
+                                   const float *w2_scales, const float *a1_scale,
+                                   const float *a2_scale, uint16_t *out,
                                    int32_t *topk_ids, float *topk_weights,
                                    int chunk_size, void *ws, size_t ws_bytes,
                                    int32_t *err_word, gbmoe_stream_t stream) {
@@ -807,7 +832,8 @@ gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
   gbmoe_status_t st = forward_validate(x, logits, bias, CS, K, N, E_global, expert_map, E,
                                        topk, score_fn, n_groups, topk_groups,
                                        apply_router_weight_on_input, activation, dtype, w1,
-                                       w1_scales, w2, w2_scales, out, ws, ws_bytes);
+                                       w1_scales, w2, w2_scales, a1_scale, a2_scale, out, ws,
+                                       ws_bytes);
   if (st != GBMOE_OK) return st;
   if (M < 0) return GBMOE_INVALID_ARG;
   for (int t0 = 0; t0 < M; t0 += CS) {
@@ -815,7 +841,7 @@ gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
     st = moe_forward(x + (size_t)t0 * K, logits + (size_t)t0 * E_global, bias, m, K, N,
                      E_global, expert_map, E, topk, score_fn, n_groups, topk_groups,
                      renormalize, apply_router_weight_on_input, activation, dtype, w1,
-                     w1_scales, w2, w2_scales, out + (size_t)t0 * K,
+                     w1_scales, w2, w2_scales, a1_scale, a2_scale, out + (size_t)t0 * K,
                      topk_ids ? topk_ids + (size_t)t0 * topk : nullptr,
                      topk_weights ? topk_weights + (size_t)t0 * topk : nullptr, ws, ws_bytes,
                      err_word, stream);
@@ -911,7 +937,8 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
                                   int apply_router_weight_on_input,
                                   int activation, int dtype, const void *w1,
                                   const float *w1_scales, const void *w2,
-                                  const float *w2_scales, uint16_t *out,
+                                  const float *w2_scales, const float *a1_scale,
+                                  const float *a2_scale, uint16_t *out,
                                   void *ws, size_t ws_bytes, int Ns,
                                   const void *w1s, const float *w1s_scales,
                                   const void *w2s, const float *w2s_scales,
@@ -925,7 +952,8 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
   gbmoe_status_t st = forward_validate(x, logits, bias, M, K, N, E_global, expert_map, E,
                                        topk, score_fn, n_groups, topk_groups,
                                        apply_router_weight_on_input, activation, dtype, w1,
-                                       w1_scales, w2, w2_scales, out, ws, ws_bytes);
+                                       w1_scales, w2, w2_scales, a1_scale, a2_scale, out, ws,
+                                       ws_bytes);
   if (st != GBMOE_OK) return st;
   st = shared_validate(x, M, K, Ns, w1s, w1s_scales, w2s, w2s_scales, shared_dtype, activation,
                        out_shared, ws_shared, ws_shared_bytes);
@@ -951,8 +979,8 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
     gbmoe_status_t st2 = moe_forward(x, logits, bias, M, K, N, E_global, expert_map, E, topk,
                                      score_fn, n_groups, topk_groups, renormalize,
                                      apply_router_weight_on_input, activation, dtype, w1,
-                                     w1_scales, w2, w2_scales, out, nullptr, nullptr, ws,
-                                     ws_bytes, err_word, stream);
+                                     w1_scales, w2, w2_scales, a1_scale, a2_scale, out, nullptr,
+                                     nullptr, ws, ws_bytes, err_word, stream);
     // join (always, so that `stream` never runs ahead of aux_stream's work)
     cudaError_t ce2 = ce1 == cudaSuccess ? cudaStreamWaitEvent(s, ev_out, 0) : ce1;
     if (st1 != GBMOE_OK) return st1;
@@ -965,8 +993,8 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
   if (st != GBMOE_OK) return st;
   return moe_forward(x, logits, bias, M, K, N, E_global, expert_map, E, topk, score_fn,
                      n_groups, topk_groups, renormalize, apply_router_weight_on_input,
-                     activation, dtype, w1, w1_scales, w2, w2_scales, out, nullptr, nullptr,
-                     ws, ws_bytes, err_word, stream);
+                     activation, dtype, w1, w1_scales, w2, w2_scales, a1_scale, a2_scale, out,
+                     nullptr, nullptr, ws, ws_bytes, err_word, stream);
 }
 
 }  // extern "C"

@@ -74,9 +74,12 @@ cudaError_t launch_quant_group_scatter(const uint16_t *x, const float *row_w, in
                                        int64_t ld, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K,
                              uint8_t *q, float *scales, int num_sms, cudaStream_t s);
+// static_scale (device fp32) or NULL: the codes use that scale instead of the
+// tensor's maximum (amax then unused)
 cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, int K,
                                 const int32_t *n_rows, uint8_t *q, float *row_scales,
-                                uint32_t *amax, int num_sms, cudaStream_t s);
+                                uint32_t *amax, const float *static_scale, int num_sms,
+                                cudaStream_t s);
 cudaError_t launch_quant_block(const uint16_t *w, int64_t R, int C, uint8_t *q,
                                float *scales, cudaStream_t s);
 

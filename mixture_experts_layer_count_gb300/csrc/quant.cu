@@ -256,15 +256,17 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// the codes with the tensor's scale; row_scales[t] = s for every row t < n
+// the codes with the tensor's scale -- from its maximum, or the caller's
+// static scale when given; row_scales[t] = s for every row t < n
 __global__ void __launch_bounds__(256)
     quant_tensor_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w, int M,
                         int K, const int32_t *__restrict__ n_rows,
-                        const unsigned int *__restrict__ amax, uint2 *__restrict__ q,
+                        const unsigned int *__restrict__ amax,
+                        const float *__restrict__ static_scale, uint2 *__restrict__ q,
                         float *__restrict__ row_scales) {
   const int vecs = K / 8;
   const size_t total = (size_t)tensor_rows(n_rows, M) * vecs;
-  const float s = group_scale(__uint_as_float(*amax));
+  const float s = static_scale ? *static_scale : group_scale(__uint_as_float(*amax));
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x) {
     float v[8];
@@ -368,20 +370,24 @@ cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K
 
 cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, int K,
                                 const int32_t *n_rows, uint8_t *q, float *row_scales,
-                                uint32_t *amax, int num_sms, cudaStream_t s) {
-  cudaError_t st = cudaMemsetAsync(amax, 0, sizeof(uint32_t), s);
-  if (st != cudaSuccess) return st;
+                                uint32_t *amax, const float *static_scale, int num_sms,
+                                cudaStream_t s) {
   const size_t vecs = (size_t)M * (K / 8);
   size_t blocks = (vecs + 255) / 256;
   const size_t cap = (size_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  quant_tensor_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x),
-                                                          row_w, M, K, n_rows, amax);
-  st = cudaGetLastError();
-  if (st != cudaSuccess) return st;
+  cudaError_t st;
+  if (!static_scale) {  // the dynamic scale: the tensor's maximum first
+    st = cudaMemsetAsync(amax, 0, sizeof(uint32_t), s);
+    if (st != cudaSuccess) return st;
+    quant_tensor_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+        reinterpret_cast<const uint4 *>(x), row_w, M, K, n_rows, amax);
+    st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+  }
   quant_tensor_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x), row_w,
-                                                      M, K, n_rows, amax,
+                                                      M, K, n_rows, amax, static_scale,
                                                       reinterpret_cast<uint2 *>(q), row_scales);
   return cudaGetLastError();
 }

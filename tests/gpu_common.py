@@ -85,8 +85,10 @@ def oracle_blocks(cfg, w1, w2, experts=None):
     return blocks
 
 
-def run_forward(cfg, d, gw, stream=None):
-    """The whole Standard layer on the GPU; returns out, ids, weights, err."""
+def run_forward(cfg, d, gw, stream=None, a1_scale=None, a2_scale=None):
+    """The whole Standard layer on the GPU (per-tensor e4m3: static activation
+    scales a1_scale / a2_scale, device fp32 scalars, when given); returns
+    out, ids, weights, err."""
     g = gbmoe()
     dev = d["x"].device
     M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
@@ -98,16 +100,16 @@ def run_forward(cfg, d, gw, stream=None):
     g.moe_forward(d["x"], d["logits"], d["bias"], N, E, k, cfg.score_fn,
                   cfg.n_groups, cfg.topk_groups, cfg.renorm, cfg.dtype, gw.w1,
                   gw.w1s, gw.w2, gw.w2s, out, ws, topk_ids=ids, topk_weights=wts,
-                  err_word=err, stream=stream)
+                  err_word=err, stream=stream, a1_scale=a1_scale, a2_scale=a2_scale)
     return out, ids, wts, err
 
 
-def oracle_forward(cfg, d, W, tokens=None, nthreads=0):
+def oracle_forward(cfg, d, W, tokens=None, nthreads=0, static_scales=None):
     return orc.moe_forward(WL.bf16_bits(d["x"]), d["logits"].cpu().numpy(),
                            None if d["bias"] is None else d["bias"].cpu().numpy(),
                            cfg.topk, cfg.score_fn, W, cfg.n_groups, cfg.topk_groups,
                            cfg.renorm, cfg.requant_h, tokens=tokens,
-                           nthreads=nthreads)
+                           nthreads=nthreads, static_scales=static_scales)
 
 
 def _grouped_choice_is_valid(v, ids_row, topk, n_groups, topk_groups, tol):

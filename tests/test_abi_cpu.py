@@ -210,21 +210,36 @@ def test_forward_rejects_bad_arguments(lib):
     f = lib.moe_forward
     #       x    lg   bias  M   K    N    Eg map   E  k  fn ng tg rn woi act dt
     args = [P16, P16, None, 64, 256, 128, 8, None, 8, 2, 0, 1, 1, 1, 0, 0, 0,
-            P16, None, P16, None, P16, None, None, P16, 1 << 30, None, None]
-    #       w1   w1s   w2   w2s   out  ids   wts   ws   wsb      err   s
+            P16, None, P16, None, None, None, P16, None, None, P16, 1 << 30, None, None]
+    #       w1   w1s   w2   w2s   a1s   a2s   out  ids   wts   ws   wsb      err   s
     def call(**kw):
         a = list(args)
         for i, v in kw.items():
             a[int(i[1:])] = v
         return f(*a)
-    assert call(a25=1024) == INVALID          # workspace too small
+    assert call(a27=1024) == INVALID          # workspace too small
     assert call(a2=P16) == INVALID            # bias with a softmax router
-    assert call(a21=P_ODD) == INVALID         # misaligned output
+    assert call(a23=P_ODD) == INVALID         # misaligned output
     assert call(a16=1) == INVALID             # FP8 weights without their scales
     assert call(a14=1) == INVALID             # weight on input needs topk 1
     assert call(a6=16) == INVALID             # 16 routed experts, 8 local, no map
     assert call(a15=7) == INVALID             # activation
     assert call(a16=9) == UNSUPPORTED         # dtype
+    # static activation scales: per-tensor e4m3 only, 4-byte aligned
+    assert call(a21=P16) == INVALID                                  # with bf16
+    assert call(a16=1, a18=P16, a20=P16, a22=P16) == INVALID        # with 1 x 128 groups
+    assert call(a16=3, a18=P16, a20=P16, a21=P16 + 2) == INVALID    # misaligned a1_scale
+    c = lib.moe_forward_chunked
+    #         x    lg   bias  M   K    N    Eg map   E  k  fn ng tg rn woi act dt
+    assert c(P16, P16, None, 64, 256, 128, 8, None, 8, 2, 0, 1, 1, 1, 0, 0, 0,
+             P16, None, P16, None, P16, None, P16, None, None, 32, P16, 1 << 30, None,
+             None) == INVALID                                       # a1_scale with bf16
+    #        w1   w1s   w2   w2s   a1s  a2s   out  ids   wts   cs  ws   wsb      err
+    q = lib.moe_quant_fp8_tensor_static
+    #        x    rw    M  K    n    scale q    rs   s
+    assert q(P16, None, 4, 256, None, None, P16, P16, None) == INVALID      # no scale
+    assert q(P16, None, 4, 256, None, P16 + 2, P16, P16, None) == INVALID   # misaligned
+    assert q(P16, None, 4, 200, None, P16, P16, P16, None) == INVALID       # K % 128
 
 
 def test_shared_experts_reject_bad_arguments(lib):
@@ -249,9 +264,9 @@ def test_shared_experts_reject_bad_arguments(lib):
     fs = lib.moe_forward_shared
     #       x    lg   bias  M   K    N    Eg map   E  k  fn ng tg rn woi act dt
     fargs = [P16, P16, None, 64, 256, 128, 8, None, 8, 2, 0, 1, 1, 1, 0, 0, 0,
-             P16, None, P16, None, P16, P16, 1 << 30, 128, P16, None, P16, None, 0,
+             P16, None, P16, None, None, None, P16, P16, 1 << 30, 128, P16, None, P16, None, 0,
              P16, P16, 1 << 30, None, None, None, None, None]
-    #        w1   w1s   w2   w2s   out  ws   wsb     Ns   w1sh  ss   w2sh  ss   sdt
+    #        w1   w1s   w2   w2s   a1s   a2s   out  ws   wsb     Ns   w1sh  ss   w2sh  ss  sdt
     #        outsh wssh wsshb    err   s     aux   ev    ev
 
     def fcall(**kw):
@@ -259,11 +274,12 @@ def test_shared_experts_reject_bad_arguments(lib):
         for i, v in kw.items():
             a[int(i[1:])] = v
         return fs(*a)
-    assert fcall(a29=2) == UNSUPPORTED          # shared experts in per-channel e4m3
-    assert fcall(a29=1) == INVALID              # e4m3 shared experts without scales
-    assert fcall(a32=64) == INVALID             # shared workspace too small
-    assert fcall(a35=P16) == INVALID            # aux stream without its events
+    assert fcall(a31=2) == UNSUPPORTED          # shared experts in per-channel e4m3
+    assert fcall(a31=1) == INVALID              # e4m3 shared experts without scales
+    assert fcall(a34=64) == INVALID             # shared workspace too small
+    assert fcall(a37=P16) == INVALID            # aux stream without its events
     assert fcall(a16=9) == UNSUPPORTED          # routed dtype
+    assert fcall(a22=P16) == INVALID            # a2_scale with bf16
 
 
 def test_selftest_rejects_bad_arguments(lib):

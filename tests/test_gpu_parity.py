@@ -260,6 +260,66 @@ def test_forward_parity_fp8_tensor(cfg):
     assert_close_rel(out.float().cpu().numpy(), ref, TOL[cfg.dtype], cfg.name)
 
 
+@pytest.mark.parametrize("partial", [False, True], ids=["all_rows", "device_row_count"])
+def test_quant_fp8_tensor_static_bit_exact(partial):
+    """A static per-tensor scale (the quant config's a1_scale): every code of
+    x / scale bit-exact with the oracle's, the largest values saturated at
+    +-448, the scale copied to every counted row, the other rows untouched."""
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(48)
+    M, K = 333, 1024
+    x = (torch.randn((M, K), generator=gen, device=DEV) *
+         torch.logspace(-2, 1, M, device=DEV)[:, None]).to(torch.bfloat16)
+    rw = torch.rand(M, generator=gen, device=DEV) + 0.05
+    n = 200 if partial else M
+    n_rows = torch.tensor([n], dtype=torch.int32, device=DEV) if partial else None
+    v = (x[:n].float() * rw[:n, None]).abs().max().item()  # the counted rows' largest |x w|
+    s_host = np.float32(v) / np.float32(448) * np.float32(0.3)
+    scale = torch.tensor([s_host], dtype=torch.float32, device=DEV)
+    q = torch.full((M, K), 0xAB, dtype=torch.uint8, device=DEV)
+    s = torch.full((M,), -1.0, dtype=torch.float32, device=DEV)
+    g.moe_quant_fp8_tensor_static(x, scale, q, s, n_rows=n_rows, row_weights=rw)
+    rq, rs = orc.quant_fp8_tensor(WL.bf16_bits(x[:n]), row_weights=rw[:n].cpu().numpy(),
+                                  scale=s_host)
+    assert np.all(s[:n].cpu().numpy() == rs)
+    assert np.array_equal(q[:n].cpu().numpy(), rq)
+    assert np.any((rq & 0x7f) == 0x7e)  # saturated codes among them
+    assert torch.all(q[n:] == 0xAB) and torch.all(s[n:] == -1.0)
+
+
+@pytest.mark.parametrize("cfg", [WL.SMALL_FP8T, WL.MID_FP8T], ids=lambda c: c.name)
+def test_forward_parity_fp8_tensor_static_scales(cfg):
+    """Static per-tensor activation scales a1 (x) and a2 (H), small enough
+    that both saturate their largest values: every token against the
+    oracle's layer with the same scales; chunked equals unchunked bit for
+    bit (no scale depends on the chunk)."""
+    g = gbmoe()
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    a1 = np.float32(d["x"].float().abs().max().item()) / np.float32(448) * np.float32(0.5)
+    a2 = np.float32(0.01)
+    a1_t = torch.tensor([a1], dtype=torch.float32, device=DEV)
+    a2_t = torch.tensor([a2], dtype=torch.float32, device=DEV)
+    out, ids, wts, err = run_forward(cfg, d, gw, a1_scale=a1_t, a2_scale=a2_t)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    W = oracle_weights(cfg, d["w1"], d["w2"])
+    ref, rid, rw = oracle_forward(cfg, d, W, static_scales=(a1, a2))
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert_close_rel(out.float().cpu().numpy(), ref, TOL[cfg.dtype], cfg.name + " static")
+    dyn, _, _, _ = run_forward(cfg, d, gw)
+    assert not torch.equal(dyn.view(torch.int16), out.view(torch.int16))
+    M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
+    chunk = 100
+    outc = torch.empty_like(out)
+    g.moe_forward_chunked(d["x"], d["logits"], d["bias"], N, E, k, cfg.score_fn, cfg.n_groups,
+                          cfg.topk_groups, cfg.renorm, cfg.dtype, gw.w1, gw.w1s, gw.w2, gw.w2s,
+                          outc, g.workspace(g.WS_FORWARD, chunk, E, N, K, k, cfg.dtype), chunk,
+                          a1_scale=a1_t, a2_scale=a2_t)
+    torch.cuda.synchronize()
+    assert torch.equal(outc.view(torch.int16), out.view(torch.int16))
+
+
 def test_quant_fp8_block_bit_exact():
     g = gbmoe()
     gen = torch.Generator(device=DEV).manual_seed(42)
