@@ -746,12 +746,11 @@ void orc_expert_row(int dtype, const uint16_t *x, int t, int e, int E, int N,
  * (apply_router_weight_on_input, meant for topk == 1): the router weight
  * multiplies the expert's input instead of its output,
  *   out[t] = sum_j expert(w[t,j] * x[t]). */
-/* The layer with per-tensor activation scales (Q7).  The scale of H spans
- * every routed pair, so this takes two passes: first x's scale and every
- * local pair's hidden row (all M tokens, whatever `tokens` lists), then the
- * scale of H and the outputs of the listed tokens.  static_scales (Q8):
- * NULL, or {scale of x, scale of H} given instead of the maxima's.
- * Arguments as orc_moe_forward_ep. */
+/* The layer with dynamic per-tensor activation scales (Q7).  The scale of H
+ * spans every routed pair, so this takes two passes: first x's scale and
+ * every local pair's hidden row (all M tokens, whatever `tokens` lists),
+ * then the scale of H and the outputs of the listed tokens.  Arguments as
+ * orc_moe_forward_ep. */
 static void forward_tensor(const uint16_t *x, const float *logits,
                            const float *bias, int M, int K, int N, int E,
                            int topk, int score_fn, int n_groups,
@@ -759,7 +758,7 @@ static void forward_tensor(const uint16_t *x, const float *logits,
                            const int32_t *expert_map, int E_local,
                            int weight_on_input, const orc_weights *W,
                            const int32_t *tokens, int n_tok, int32_t *ids_out,
-                           double *w_out, double *out, const float *static_scales)
+                           double *w_out, double *out)
 {
     const size_t P = (size_t)M * topk;
     int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (P ? P : 1));
@@ -779,12 +778,7 @@ static void forward_tensor(const uint16_t *x, const float *logits,
                   w + (size_t)t * topk, NULL);
         rw[t] = (float)w[(size_t)t * topk]; /* weight on input: topk is 1 */
     }
-    if (static_scales) {
-        sx = static_scales[0];
-        orc_quant_fp8_tensor_static(x, weight_on_input ? rw : NULL, M, K, sx, xq);
-    } else {
-        orc_quant_fp8_tensor(x, weight_on_input ? rw : NULL, M, K, xq, &sx);
-    }
+    orc_quant_fp8_tensor(x, weight_on_input ? rw : NULL, M, K, xq, &sx);
     for (t = 0; t < M; ++t) {
         for (k = 0; k < K; ++k)
             xr[k] = orc_e4m3_value(xq[(size_t)t * K + k]) * (double)sx;
@@ -805,7 +799,7 @@ static void forward_tensor(const uint16_t *x, const float *logits,
         }
     }
     if (requant_h)
-        sh = static_scales ? static_scales[1] : group_scale(amax);
+        sh = group_scale(amax);
     if (!tokens)
         n_tok = M;
     for (i = 0; i < n_tok; ++i) {
@@ -832,6 +826,67 @@ static void forward_tensor(const uint16_t *x, const float *logits,
     free(xr); free(hq); free(y);
 }
 
+/* The layer with static per-tensor activation scales (Q8): sx codes x, sh
+ * codes H (each routed hidden row rounded to bf16 first, as in Q7).  No scale
+ * depends on other tokens, so each listed token is computed on its own, in
+ * the steps of the Q7 layer: its row of x (times its router weight in fp32
+ * with weight_on_input) coded with sx, each local pair's hidden row rounded
+ * to bf16 and (requant_h) coded with sh, the down projection, the weighted
+ * sum in slot order.  Arguments as orc_moe_forward_ep. */
+static void forward_tensor_static(const uint16_t *x, const float *logits,
+                                  const float *bias, int K, int N, int E,
+                                  int topk, int score_fn, int n_groups,
+                                  int topk_groups, int renorm, int requant_h,
+                                  const int32_t *expert_map, int E_local,
+                                  int weight_on_input, const orc_weights *W,
+                                  const int32_t *tokens, int n_tok,
+                                  int32_t *ids_out, double *w_out, double *out,
+                                  float sx, float sh, int nthreads)
+{
+    int i;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (i = 0; i < n_tok; ++i) {
+        int t = tokens ? tokens[i] : i;
+        int j, k, n;
+        int32_t *ids = ids_out + (size_t)i * topk;
+        double *w = w_out + (size_t)i * topk;
+        uint8_t *xq = (uint8_t *)malloc((size_t)K);
+        double *xr = (double *)malloc(sizeof(double) * (size_t)K);
+        double *h = (double *)malloc(sizeof(double) * (size_t)N);
+        double *y = (double *)malloc(sizeof(double) * (size_t)K);
+        double *o = out + (size_t)i * K;
+        float rw;
+        orc_route(logits + (size_t)t * E, bias, 1, E, topk, score_fn, n_groups,
+                  topk_groups, renorm, ids, w, NULL);
+        rw = (float)w[0]; /* weight on input: topk is 1 */
+        orc_quant_fp8_tensor_static(x + (size_t)t * K, weight_on_input ? &rw : NULL,
+                                    1, K, sx, xq);
+        for (k = 0; k < K; ++k) {
+            xr[k] = orc_e4m3_value(xq[k]) * (double)sx;
+            o[k] = 0.0;
+        }
+        for (j = 0; j < topk; ++j) {
+            int l = local_expert(ids[j], E, expert_map, E_local);
+            if (l < 0)
+                continue;
+            expert_h(W, l, xr, h);
+            for (n = 0; n < N; ++n) {
+                h[n] = bf16_round(h[n]);
+                if (requant_h)
+                    h[n] = orc_e4m3_value(orc_e4m3_encode((float)h[n] / sh)) * (double)sh;
+            }
+            expert_y(W, l, h, y);
+            for (k = 0; k < K; ++k)
+                o[k] += (weight_on_input ? 1.0 : w[j]) * y[k];
+        }
+        free(xq); free(xr); free(h); free(y);
+    }
+}
+
 void orc_moe_forward_ep(const uint16_t *x, const float *logits,
                         const float *bias, int M, int K, int N, int E,
                         int topk, int score_fn, int n_groups, int topk_groups,
@@ -849,11 +904,18 @@ void orc_moe_forward_ep(const uint16_t *x, const float *logits,
     fill_e4m3_table();
     W.dtype = dtype; W.E = E_local; W.N = N; W.K = K; W.act = act;
     W.w1 = w1; W.w2 = w2; W.w1s = w1s; W.w2s = w2s;
+    if (dtype == ORC_FP8_TENSOR && static_scales) {
+        forward_tensor_static(x, logits, bias, K, N, E, topk, score_fn, n_groups,
+                              topk_groups, renorm, requant_h, expert_map, E_local,
+                              weight_on_input, &W, tokens, tokens ? n_tok : M,
+                              ids_out, w_out, out, static_scales[0],
+                              static_scales[1], nthreads);
+        return;
+    }
     if (dtype == ORC_FP8_TENSOR) {
         forward_tensor(x, logits, bias, M, K, N, E, topk, score_fn, n_groups,
                        topk_groups, renorm, requant_h, expert_map, E_local,
-                       weight_on_input, &W, tokens, n_tok, ids_out, w_out, out,
-                       static_scales);
+                       weight_on_input, &W, tokens, n_tok, ids_out, w_out, out);
         return;
     }
     if (!tokens)

@@ -582,3 +582,34 @@ def test_forward_parity_full_size(cfg):
     assert np.array_equal(rid_s, rid[tokens])
     assert_close_rel(out[torch.from_numpy(tokens).to(DEV)].float().cpu().numpy(), ref,
                      TOL[cfg.dtype], cfg.name)
+
+
+def test_forward_parity_fp8_tensor_static_full_size_sampled():
+    """The DeepSeek-V3-shaped prefill with per-tensor e4m3 activations and
+    static scales for x and H (small enough that both saturate their largest
+    values) at full size: the ids and outputs of a seeded sample of 512
+    tokens against the oracle's layer with the same scales (no scale depends
+    on other tokens, so the sampled tokens are computed exactly as in the
+    full run)."""
+    cfg = WL.DSV3_PREFILL_FP8T
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    a1 = np.float32(d["x"].float().abs().max().item()) / np.float32(448) * np.float32(0.8)
+    a2 = np.float32(0.03)
+    out, ids, wts, err = run_forward(
+        cfg, d, gw, a1_scale=torch.tensor([a1], dtype=torch.float32, device=DEV),
+        a2_scale=torch.tensor([a2], dtype=torch.float32, device=DEV))
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    lg = d["logits"].cpu().numpy()
+    bias = None if d["bias"] is None else d["bias"].cpu().numpy()
+    rid, _, margin = orc.route(lg, bias, cfg.topk, cfg.score_fn, cfg.n_groups,
+                               cfg.topk_groups, cfg.renorm)
+    diff = check_ids(ids.cpu().numpy(), rid, margin, cfg.name, cfg, lg, bias)
+    rng = np.random.default_rng(2)
+    tokens = np.setdiff1d(np.sort(rng.choice(cfg.M, N_SAMPLE, replace=False)), diff)
+    W = oracle_weights(cfg, d["w1"], d["w2"], np.unique(rid[tokens]))
+    ref, rid_s, _ = oracle_forward(cfg, d, W, tokens=tokens, static_scales=(a1, a2))
+    assert np.array_equal(rid_s, rid[tokens])
+    assert_close_rel(out[torch.from_numpy(tokens).to(DEV)].float().cpu().numpy(), ref,
+                     TOL[cfg.dtype], cfg.name + " static scales")
