@@ -94,7 +94,8 @@ enum {
     GBMOE_WS_BATCHED = 2,  /* moe_batched_masked_experts              */
     GBMOE_WS_FORWARD = 3,  /* moe_forward (the whole Standard layer)  */
     GBMOE_WS_SHARED = 4,   /* moe_shared_expert_forward (N = shared intermediate size;
-                              dtype GBMOE_BF16 or GBMOE_FP8_E4M3) */
+                              dtype GBMOE_BF16, GBMOE_FP8_E4M3 or
+                              GBMOE_FP8_E4M3_CHANNEL) */
     GBMOE_WS_EP_DISPATCH = 6  /* moe_ep_dispatch: M_or_T = M tokens per shard, E = all
                                  routed experts, N = the number of shards G  */
 };
@@ -467,6 +468,10 @@ gbmoe_status_t moe_forward_chunked(const uint16_t *x, const float *logits,
  * aligned; moe_quant_fp8_block makes them); x is quantised inside the call
  * in 1 x 128 groups and h in 1 x 128 groups along Ns, as moe_forward does
  * for the routed experts; K and Ns at most 16384.
+ * dtype GBMOE_FP8_E4M3_CHANNEL: w1s, w2s e4m3 with one fp32 scale per row,
+ * w1s_scales (2Ns) and w2s_scales (K), 16-byte aligned (moe_quant_fp8_group
+ * with a group as wide as the row makes them); x is quantised with one scale
+ * per token and h, kept in bf16, with one scale per row, as moe_forward does.
  * Other dtypes: GBMOE_UNSUPPORTED.  Runs the grouped-GEMM kernels with one
  * expert holding all M rows (e4m3: after the group quantisation of x and a
  * transpose of its scales).  ws: moe_workspace_size(GBMOE_WS_SHARED, M, 1,
@@ -490,7 +495,8 @@ gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K, int Ns
  * CUDA graph when `stream` is being captured.
  * Arguments as moe_forward, plus Ns, w1s, w1s_scales, w2s, w2s_scales and
  * out_shared as moe_shared_expert_forward, whose dtype is shared_dtype
- * (GBMOE_BF16 or GBMOE_FP8_E4M3, independent of the routed experts' dtype);
+ * (GBMOE_BF16, GBMOE_FP8_E4M3 or GBMOE_FP8_E4M3_CHANNEL, independent of the
+ * routed experts' dtype);
  * ws_shared: moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1,
  * shared_dtype) bytes, separate from ws.  Both calls' arguments are checked
  * before anything is enqueued. */

@@ -137,25 +137,32 @@ BatchedWs carve_batched(Carver &c, int T, int E, int N, int K, int dtype) {
   return w;
 }
 
-// moe_shared_expert_forward: H (M, Ns); e4m3 adds the codes of x, x's
-// scales row-major (the quantiser's output) and group-major (the GEMM's
-// operand), and H's group-major scales
+// moe_shared_expert_forward: H (M, Ns), the down GEMM's operand.  Block
+// e4m3 adds the codes of x, x's scales row-major (the quantiser's output)
+// and group-major (the GEMM's operand), and H's group-major scales;
+// per-channel e4m3 adds H's scale per row, H in bf16 before its quantisation,
+// the codes of x and x's scale per row.
 struct SharedWs {
   void *H;
   float *Hs;
+  void *Hb;
   void *xq;
   float *xs_rows;
   float *xs;
 };
 SharedWs carve_shared(Carver &c, int M, int Ns, int K, int dtype) {
-  const bool fp8 = dtype == GBMOE_FP8_E4M3;
   SharedWs w{};
   w.H = c.take((size_t)M * Ns * elem_bytes(dtype));
-  if (fp8) {
+  if (dtype == GBMOE_FP8_E4M3) {
     w.Hs = static_cast<float *>(c.take((size_t)scale_ld(M) * (Ns / 128) * 4));
     w.xq = c.take((size_t)M * K);
     w.xs_rows = static_cast<float *>(c.take((size_t)M * (K / 128) * 4));
     w.xs = static_cast<float *>(c.take((size_t)scale_ld(M) * (K / 128) * 4));
+  } else if (dtype == GBMOE_FP8_E4M3_CHANNEL) {
+    w.Hs = static_cast<float *>(c.take((size_t)M * 4));
+    w.Hb = c.take((size_t)M * Ns * 2);
+    w.xq = c.take((size_t)M * K);
+    w.xs_rows = static_cast<float *>(c.take((size_t)M * 4));
   }
   return w;
 }
@@ -331,7 +338,8 @@ size_t moe_workspace_size(int which, int M_or_T, int E, int N, int K, int topk,
       carve_ep(c, N, M_or_T, E, topk);
       return c.off;
     case GBMOE_WS_SHARED:
-      if (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3) return 0;
+      if (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3 && dtype != GBMOE_FP8_E4M3_CHANNEL)
+        return 0;
       if (!gemm_shape_ok(M_or_T, 1, 1, N, K, dtype)) return 0;
       carve_shared(c, M_or_T, N, K, dtype);
       return c.off > 0 ? c.off : kWsAlign;
@@ -856,7 +864,8 @@ static gbmoe_status_t shared_validate(const uint16_t *x, int M, int K, int Ns, c
                                       const float *w2s_scales, int dtype, int activation,
                                       const uint16_t *out_shared, const void *ws,
                                       size_t ws_bytes) {
-  if (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3) return GBMOE_UNSUPPORTED;
+  if (dtype != GBMOE_BF16 && dtype != GBMOE_FP8_E4M3 && dtype != GBMOE_FP8_E4M3_CHANNEL)
+    return GBMOE_UNSUPPORTED;
   if (!gemm_shape_ok(M, 1, 1, Ns, K, dtype)) return GBMOE_INVALID_ARG;
   if (activation != GBMOE_ACT_SILU && activation != GBMOE_ACT_GELU) return GBMOE_INVALID_ARG;
   if (M > 0) {
@@ -867,6 +876,10 @@ static gbmoe_status_t shared_validate(const uint16_t *x, int M, int K, int Ns, c
     if (dtype == GBMOE_FP8_E4M3 &&
         (!w1s_scales || !w2s_scales || (reinterpret_cast<uintptr_t>(w1s_scales) & 3u) ||
          (reinterpret_cast<uintptr_t>(w2s_scales) & 3u)))
+      return GBMOE_INVALID_ARG;
+    // per-channel weight scales are read 16 bytes at a time
+    if (dtype == GBMOE_FP8_E4M3_CHANNEL &&
+        (!w1s_scales || !w2s_scales || !aligned16(w1s_scales) || !aligned16(w2s_scales)))
       return GBMOE_INVALID_ARG;
     if (ws_bytes < moe_workspace_size(GBMOE_WS_SHARED, M, 1, Ns, K, 1, dtype))
       return GBMOE_INVALID_ARG;
@@ -888,6 +901,7 @@ gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K, int Ns
   if (st != GBMOE_OK || M == 0) return st;
   cudaStream_t s = (cudaStream_t)stream;
   const bool fp8 = dtype == GBMOE_FP8_E4M3;
+  const bool fp8ch = dtype == GBMOE_FP8_E4M3_CHANNEL;
   Carver c(ws);
   const SharedWs w = carve_shared(c, M, Ns, K, dtype);
   // one expert owning all M rows ("dense": neither offsets nor counts)
@@ -905,6 +919,29 @@ gbmoe_status_t moe_shared_expert_forward(const uint16_t *x, int M, int K, int Ns
   a.out = w.H;
   a.err = err_word;
   cudaError_t ce;
+  if (fp8ch) {
+    // one scale per token; h in bf16, then one scale per row of H
+    ce = launch_quant_row(x, nullptr, M, K, static_cast<uint8_t *>(w.xq), w.xs_rows, sms, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+    a.fp8ch = true;
+    a.A = w.xq;
+    a.A_scales = w.xs_rows;
+    a.scale_ld = scale_ld((size_t)M);
+    a.B_scales = w1s_scales;
+    a.out = w.Hb;
+    ce = launch_grouped_gemm(a, sms, s);
+    if (ce == cudaSuccess)
+      ce = launch_quant_row(static_cast<const uint16_t *>(w.Hb), nullptr, M, Ns,
+                            static_cast<uint8_t *>(w.H), w.Hs, sms, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+    a.mode = kDown;
+    a.A = w.H;
+    a.A_scales = w.Hs;
+    a.B = w2s;
+    a.B_scales = w2s_scales;
+    a.out = out_shared;
+    return from_cuda(launch_grouped_gemm(a, sms, s));
+  }
   if (fp8) {
     // x in 1 x 128 groups, its scales moved to the GEMM's group-major layout
     ce = launch_quant_group(x, nullptr, M, K, static_cast<uint8_t *>(w.xq), w.xs_rows, sms, s);

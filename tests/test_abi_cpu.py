@@ -68,7 +68,10 @@ def test_workspace_sizes():
     assert g.moe_workspace_size(g.WS_SHARED, M, 1, Ns, K, 1, g.FP8_E4M3) == sum(
         -(-b // 256) * 256 for b in (M * Ns, ld * (Ns // 128) * 4, M * K, M * (K // 128) * 4,
                                      ld * (K // 128) * 4))
-    assert g.moe_workspace_size(g.WS_SHARED, M, 1, Ns, K, 1, g.FP8_E4M3_CHANNEL) == 0
+    # per-channel e4m3: H, H's scale per row, H in bf16, the codes of x, x's scale per row
+    assert g.moe_workspace_size(g.WS_SHARED, M, 1, Ns, K, 1, g.FP8_E4M3_CHANNEL) == sum(
+        -(-b // 256) * 256 for b in (M * Ns, M * 4, M * Ns * 2, M * K, M * 4))
+    assert g.moe_workspace_size(g.WS_SHARED, M, 1, Ns, K, 1, g.FP8_E4M3_TENSOR) == 0
     # EP dispatch (M tokens per shard, E routed experts, N = G shards): the
     # pairs' ids, the map, counts, offsets, sorted, inv, chunk histograms
     G, M, E, k = 4, 100, 64, 6
@@ -252,7 +255,9 @@ def test_shared_experts_reject_bad_arguments(lib):
         for i, v in kw.items():
             a[int(i[1:])] = v
         return f(*a)
-    assert call(a8=2) == UNSUPPORTED                  # per-channel e4m3
+    assert call(a8=3) == UNSUPPORTED                  # per-tensor e4m3
+    assert call(a8=2) == INVALID                      # per-channel e4m3 without scales
+    assert call(a8=2, a5=P16, a7=P16 + 4) == INVALID  # per-channel scales not 16-byte aligned
     assert call(a8=1) == INVALID                      # e4m3 weights without scales
     assert call(a8=1, a5=P16) == INVALID              # ... without w2s's scales
     assert call(a8=1, a5=P16 + 2, a7=P16) == INVALID  # scales not 4-byte aligned
@@ -274,7 +279,7 @@ def test_shared_experts_reject_bad_arguments(lib):
         for i, v in kw.items():
             a[int(i[1:])] = v
         return fs(*a)
-    assert fcall(a31=2) == UNSUPPORTED          # shared experts in per-channel e4m3
+    assert fcall(a31=3) == UNSUPPORTED          # shared experts in per-tensor e4m3
     assert fcall(a31=1) == INVALID              # e4m3 shared experts without scales
     assert fcall(a34=64) == INVALID             # shared workspace too small
     assert fcall(a37=P16) == INVALID            # aux stream without its events

@@ -61,40 +61,66 @@ def _shared_e4m3(w1s, w2s):
     return q1, s1, q2, s2
 
 
-@pytest.mark.parametrize("cfg,act", [(WL.SMALL_BF16, 0), (WL.SMALL_BF16, 1),
-                                     (WL.SMALL_FP8_K640, 0)],
-                         ids=["M300_K512_silu", "M300_K512_gelu", "M300_K640_silu"])
-def test_shared_expert_e4m3_is_the_oracles_e4m3_mlp(cfg, act):
-    """e4m3 shared experts: x quantised in 1 x 128 groups inside the call,
-    128 x 128 weight blocks, h requantised -- against the oracle's e4m3
-    experts with one expert holding every token (ragged last m-tile; K = 640
-    leaves the second half of the last down tile past K)."""
+def _shared_e4m3_channel(w1s, w2s):
+    """The library's per-row (per output channel) quantisation of the shared
+    weights: (w1 codes, w1 scales (2Ns), w2 codes, w2 scales (K))."""
+    g = gbmoe()
+    (Ns2, K), Ns = w1s.shape, w2s.shape[1]
+    q1 = torch.empty((Ns2, K), dtype=torch.uint8, device=DEV)
+    s1 = torch.empty((Ns2, 1), dtype=torch.float32, device=DEV)
+    q2 = torch.empty((K, Ns), dtype=torch.uint8, device=DEV)
+    s2 = torch.empty((K, 1), dtype=torch.float32, device=DEV)
+    g.moe_quant_fp8_group(w1s, q1, s1, group=K)
+    g.moe_quant_fp8_group(w2s, q2, s2, group=Ns)
+    return q1, s1.view(-1), q2, s2.view(-1)
+
+
+@pytest.mark.parametrize("cfg,act,dtype",
+                         [(WL.SMALL_BF16, 0, WL.FP8), (WL.SMALL_BF16, 1, WL.FP8),
+                          (WL.SMALL_FP8_K640, 0, WL.FP8), (WL.SMALL_BF16, 0, WL.FP8_CHANNEL),
+                          (WL.SMALL_FP8_K640, 1, WL.FP8_CHANNEL)],
+                         ids=["block_M300_K512_silu", "block_M300_K512_gelu", "block_M300_K640_silu",
+                              "channel_M300_K512_silu", "channel_M300_K640_gelu"])
+def test_shared_expert_e4m3_is_the_oracles_e4m3_mlp(cfg, act, dtype):
+    """e4m3 shared experts against the oracle's e4m3 experts with one expert
+    holding every token (ragged last m-tile; K = 640 leaves the second half
+    of the last down tile past K).  Block scales: x quantised in 1 x 128
+    groups inside the call, 128 x 128 weight blocks, h requantised in 1 x 128
+    groups.  Per-channel: one scale per token of x and per weight row, h kept
+    in bf16 and quantised per row."""
     g = gbmoe()
     d = WL.make_inputs(cfg, DEV, with_weights=False)
     M, K = cfg.M, cfg.K
     w1s, w2s = _shared_weights(K, NS, 52)
-    q1, s1, q2, s2 = _shared_e4m3(w1s, w2s)
+    block = dtype == WL.FP8
+    q1, s1, q2, s2 = _shared_e4m3(w1s, w2s) if block else _shared_e4m3_channel(w1s, w2s)
     out_s = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device=DEV)
-    ws = g.workspace(g.WS_SHARED, M, 1, NS, K, 1, g.FP8_E4M3)
+    ws = g.workspace(g.WS_SHARED, M, 1, NS, K, 1, dtype)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    g.moe_shared_expert_forward(d["x"], NS, q1, q2, out_s, ws, dtype=g.FP8_E4M3, activation=act,
+    g.moe_shared_expert_forward(d["x"], NS, q1, q2, out_s, ws, dtype=dtype, activation=act,
                                 err_word=err, w1s_scales=s1, w2s_scales=s2)
     torch.cuda.synchronize()
     assert err.item() == 0
-    oq1, os1 = orc.quant_fp8_block(WL.bf16_bits(w1s))
-    oq2, os2 = orc.quant_fp8_block(WL.bf16_bits(w2s))
-    # the weights the GPU ran with are the oracle's own block quantisation
+    if block:
+        oq1, os1 = orc.quant_fp8_block(WL.bf16_bits(w1s))
+        oq2, os2 = orc.quant_fp8_block(WL.bf16_bits(w2s))
+    else:
+        oq1, os1 = orc.quant_fp8_group(WL.bf16_bits(w1s), group=K)
+        oq2, os2 = orc.quant_fp8_group(WL.bf16_bits(w2s), group=NS)
+        os1, os2 = os1[:, 0], os2[:, 0]
+    # the weights the GPU ran with are the oracle's own quantisation
     assert np.array_equal(q1.cpu().numpy(), oq1) and np.array_equal(q2.cpu().numpy(), oq2)
     assert np.array_equal(s1.cpu().numpy(), os1) and np.array_equal(s2.cpu().numpy(), os2)
-    W = orc.Weights(WL.FP8, experts={0: (oq1, oq2, os1, os2)}, E=1, N=NS, K=K, act=act)
+    W = orc.Weights(dtype, experts={0: (oq1, oq2, os1, os2)}, E=1, N=NS, K=K, act=act)
     ref, n = orc.batched_experts(WL.bf16_bits(d["x"])[None], np.array([M], np.int32), W,
                                  requant_h=True)
     assert n == M
-    assert_close_rel(out_s.float().cpu().numpy(), ref[0], TOL[WL.FP8], "shared e4m3")
+    assert_close_rel(out_s.float().cpu().numpy(), ref[0], TOL[dtype], f"shared e4m3 ({dtype})")
 
 
-@pytest.mark.parametrize("cfg,shared_dtype", [(WL.SMALL_SIGMOID, WL.BF16), (WL.SMALL_FP8, WL.FP8)],
-                         ids=["bf16", "e4m3"])
+@pytest.mark.parametrize("cfg,shared_dtype", [(WL.SMALL_SIGMOID, WL.BF16), (WL.SMALL_FP8, WL.FP8),
+                                              (WL.SMALL_FP8CH, WL.FP8_CHANNEL)],
+                         ids=["bf16", "e4m3", "e4m3_channel"])
 def test_overlapped_shared_experts_equal_the_separate_calls_and_replay(cfg, shared_dtype):
     g = gbmoe()
     d = WL.make_inputs(cfg, DEV)
@@ -103,6 +129,8 @@ def test_overlapped_shared_experts_equal_the_separate_calls_and_replay(cfg, shar
     s1 = s2 = None
     if shared_dtype == WL.FP8:
         w1s, s1, w2s, s2 = _shared_e4m3(w1s, w2s)
+    elif shared_dtype == WL.FP8_CHANNEL:
+        w1s, s1, w2s, s2 = _shared_e4m3_channel(w1s, w2s)
     sh = dict(dtype=shared_dtype, w1s_scales=s1, w2s_scales=s2)
     M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
     ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype)
