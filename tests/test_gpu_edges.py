@@ -1,8 +1,8 @@
 """The layer at the edges of its argument ranges, against the oracle: the
 largest expert count (512) with grouped sigmoid routing, the largest top-k
-(32), every expert picked by every token (topk = E), a single expert, and
-the largest K and N of the block-scaled e4m3 GEMMs (16384: 128 scale blocks,
-the whole per-tile scale table)."""
+(32), every expert picked by every token (topk = E), a single expert, the
+largest K and N of the block-scaled e4m3 GEMMs (16384: 128 scale blocks,
+the whole per-tile scale table), and a single token in every dtype."""
 import numpy as np
 import pytest
 import torch
@@ -39,6 +39,13 @@ CASES = [
     # block-scaled e4m3 at the largest K (gate/up: 128 K blocks) and N (down)
     WL.MoEConfig("edge_fp8_K16384", M=40, K=16384, N=256, E=4, topk=2, dtype=WL.FP8, seed=56),
     WL.MoEConfig("edge_fp8_N16384", M=24, K=256, N=16384, E=2, topk=1, dtype=WL.FP8, seed=57),
+    # a single token (a decode step of batch one) in every dtype
+    WL.MoEConfig("edge_M1_bf16", M=1, K=512, N=256, E=8, topk=2, seed=58),
+    WL.MoEConfig("edge_M1_fp8_grouped", M=1, K=512, N=256, E=64, topk=8, dtype=WL.FP8,
+                 score_fn=WL.SIGMOID, n_groups=8, topk_groups=4, zipf_bias=True, seed=59),
+    WL.MoEConfig("edge_M1_fp8ch", M=1, K=512, N=256, E=16, topk=4, dtype=WL.FP8_CHANNEL,
+                 seed=60),
+    WL.MoEConfig("edge_M1_fp8t", M=1, K=512, N=256, E=16, topk=4, dtype=WL.FP8_TENSOR, seed=61),
 ]
 
 
