@@ -499,13 +499,16 @@ EXTRA_WORKLOADS = [WL.TINY, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8, WL.BATCHED_MASK
 def run_extras(args, dev, skip=None):
     """The other workloads of the layer, each timed as the default one is
     (event-timed steps over resident inputs, clocks sampled inside the timed
-    region) but without the end-to-end and CPU legs, so that they add well
-    under a minute: tiny (launch-bound), DeepSeek-V3 decode (weight-streaming,
-    HBM-bound), DeepSeek-V3 prefill with e4m3 block scales, and the batched
-    masked format replayed from a CUDA graph."""
+    region) but without the end-to-end leg: tiny (launch-bound), DeepSeek-V3
+    decode (weight-streaming, HBM-bound), DeepSeek-V3 prefill with e4m3 block
+    scales, and the batched masked format replayed from a CUDA graph.  Only
+    the tiny and decode entries carry a CPU leg: the oracle on all their
+    tokens (seconds), the tiny one also on one thread."""
     import torch
     steps = max(20, min(args.steps, 200))
     warmup = max(3, min(args.warmup, 10))
+    # the whole-workload oracle timings ride along where they take seconds
+    cpu_full = not args.no_cpu_baseline and _dist()[0] == 1
     out = {}
     for cfg in EXTRA_WORKLOADS:
         if cfg.name == skip:
@@ -514,14 +517,14 @@ def run_extras(args, dev, skip=None):
         if cfg.batched:
             entry = measure_batched_entry(cfg, dev, steps, warmup)
         else:
-            entry = measure_standard_entry(cfg, dev, steps, warmup)
+            entry = measure_standard_entry(cfg, dev, steps, warmup, cpu_full)
         entry["wall_s"] = time.time() - t
         out[cfg.name] = entry
         torch.cuda.empty_cache()
     return out
 
 
-def measure_standard_entry(cfg, dev, steps, warmup):
+def measure_standard_entry(cfg, dev, steps, warmup, cpu_full=False):
     import torch
     layer = Layer(cfg, dev)
     for _ in range(warmup):
@@ -562,6 +565,8 @@ def measure_standard_entry(cfg, dev, steps, warmup):
                               ("L2-resident: %.1f MB of expert weights, no flush (a "
                                "launch-latency case)" % (wbytes / 1e6))},
              "gpu_launches_per_step": layer.launches_per_step}
+    if cpu_full and cfg.name in FULL_ORACLE_WORKLOADS:
+        entry["cpu_baseline"] = cpu_baseline_full(cfg, layer)
     del layer
     return entry
 
@@ -912,6 +917,35 @@ def _time_oracle(cfg, d, W, tokens, threads):
 _TENSOR_UNBOUNDED = ("per-tensor activation scales couple every token: the oracle computes "
                      "all tokens' hidden rows before any output, so no bounded token sample "
                      "of this workload exists")
+
+
+# small enough for the whole oracle layer in seconds: every token, on all
+# host cores and (the tiny one) on one
+FULL_ORACLE_WORKLOADS = {WL.TINY.name: (0, 1), WL.DSV3_DECODE.name: (0,)}
+
+
+def cpu_baseline_full(cfg, layer):
+    """The oracle on every token of the workload, on the listed thread counts
+    (0 = all host cores); weights copied to the host before the clock
+    starts."""
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    d = {"x": layer.x, "logits": layer.logits, "bias": layer.bias}
+    d.update(WL.make_weights(cfg, layer.x.device))
+    tokens = np.arange(cfg.M)
+    W = _oracle_inputs(cfg, d, tokens)
+    res = {"kind": "oracle", "unit": "tokens/s",
+           "sample": f"all {cfg.M} tokens of {cfg.name}, fp64 per-token loops"}
+    for threads in FULL_ORACLE_WORKLOADS[cfg.name]:
+        n = cores if threads == 0 else threads
+        _time_oracle(cfg, d, W, tokens[:1], n)  # page the weights in
+        dt = _time_oracle(cfg, d, W, tokens, n)
+        if threads == 0:
+            res.update({"value": cfg.M / dt, "cores": n, "seconds": dt})
+        else:
+            res[f"threads_{n}"] = {"value": cfg.M / dt, "cores": n, "seconds": dt}
+    return res
 
 
 def cpu_baseline(cfg, layer, budget_s):
