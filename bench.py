@@ -515,7 +515,7 @@ def run_extras(args, dev, skip=None):
             continue
         t = time.time()
         if cfg.batched:
-            entry = measure_batched_entry(cfg, dev, steps, warmup)
+            entry = measure_batched_entry(cfg, dev, steps, warmup, cpu_full)
         else:
             entry = measure_standard_entry(cfg, dev, steps, warmup, cpu_full)
         entry["wall_s"] = time.time() - t
@@ -567,11 +567,13 @@ def measure_standard_entry(cfg, dev, steps, warmup, cpu_full=False):
              "gpu_launches_per_step": layer.launches_per_step}
     if cpu_full and cfg.name in FULL_ORACLE_WORKLOADS:
         entry["cpu_baseline"] = cpu_baseline_full(cfg, layer)
+    elif cpu_full and cfg.dtype != WL.FP8_TENSOR:
+        entry["cpu_baseline"] = cpu_baseline_pairs(cfg, layer)
     del layer
     return entry
 
 
-def measure_batched_entry(cfg, dev, steps, warmup):
+def measure_batched_entry(cfg, dev, steps, warmup, cpu_full=False):
     """One CUDA graph of moe_batched_masked_experts replayed over resident
     inputs; the roofline covers both grouped GEMM launches.  e4m3: x_b comes
     quantised (1 x 128 group scales, as the prepare step hands it to the
@@ -581,6 +583,7 @@ def measure_batched_entry(cfg, dev, steps, warmup):
     g.load()
     d = WL.make_inputs(cfg, dev)
     E, T, N, K = cfg.E, cfg.M, cfg.N, cfg.K
+    cpu = cpu_baseline_batched(cfg, d) if cpu_full else None
     xb, counts, w1, w2 = d["x_b"], d["counts"], d["w1"], d["w2"]
     yb = torch.empty_like(xb)
     fp8 = cfg.dtype == WL.FP8
@@ -647,6 +650,7 @@ def measure_batched_entry(cfg, dev, steps, warmup):
                          "kernel": "grouped GEMM gate/up + down (one graph replay)",
                          "peak_source": f"{src} {key} (timed region {ms / 1e3:.2f} s)"
                                         + (" x2 (nominal fp8:bf16 dense ratio)" if fp8 else "")},
+            **({"cpu_baseline": cpu} if cpu else {}),
             "clocks": clk.summary(wall0, wall1),
             "config": {"E": E, "T": T, "K": K, "N": N, "valid_rows": rows,
                        "scales": _scales_desc(cfg),
@@ -946,6 +950,95 @@ def cpu_baseline_full(cfg, layer):
         else:
             res[f"threads_{n}"] = {"value": cfg.M / dt, "cores": n, "seconds": dt}
     return res
+
+
+def cpu_baseline_pairs(cfg, layer, n_experts=4, rows_per_expert=32):
+    """The oracle's expert rows -- the per-pair work of the layer, each routed
+    row through its expert (e4m3: h requantised) -- on the first rows routed
+    to a few experts with rows, all host cores; pairs/s, tokens/s = pairs/s /
+    topk, and the whole run extrapolated.  Only those experts' weights are
+    prepared, so the sample stays seconds on a 256-expert layer."""
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    x = layer.x
+    rid, _, _ = orc.route(layer.logits.cpu().numpy(),
+                          None if layer.bias is None else layer.bias.cpu().numpy(),
+                          cfg.topk, cfg.score_fn, cfg.n_groups, cfg.topk_groups, cfg.renorm)
+    rng = np.random.default_rng(0)
+    present = np.unique(rid)
+    experts = np.sort(rng.choice(present, min(n_experts, len(present)), replace=False))
+    wd = WL.make_weights(cfg, x.device)  # the workload's weights (on the device)
+    T = rows_per_expert
+    xb = np.zeros((len(experts), T, cfg.K), np.uint16)
+    counts = np.zeros(len(experts), np.int32)
+    blocks = {}
+    for i, e in enumerate(experts):
+        toks = np.flatnonzero((rid == e).any(axis=1))[:T]
+        counts[i] = len(toks)
+        xb[i, :len(toks)] = WL.bf16_bits(x[torch_index(toks, x.device)])
+        b1, b2 = WL.bf16_bits(wd["w1"][int(e)]), WL.bf16_bits(wd["w2"][int(e)])
+        if cfg.dtype == WL.FP8:
+            q1, s1 = orc.quant_fp8_block(b1)
+            q2, s2 = orc.quant_fp8_block(b2)
+            blocks[i] = (q1, q2, s1, s2)
+        elif cfg.dtype == WL.FP8_CHANNEL:
+            q1, s1 = orc.quant_fp8_group(b1, group=cfg.K)
+            q2, s2 = orc.quant_fp8_group(b2, group=cfg.N)
+            blocks[i] = (q1, q2, s1[:, 0], s2[:, 0])
+        else:
+            blocks[i] = (b1, b2)
+    W = orc.Weights(cfg.dtype, experts=blocks, E=len(experts), N=cfg.N, K=cfg.K)
+    out = np.empty((len(experts), T, cfg.K), np.float64)
+    t = time.perf_counter()
+    _, n = orc.batched_experts(xb, counts, W, requant_h=cfg.requant_h, nthreads=cores, out=out)
+    dt = time.perf_counter() - t
+    del wd
+    pairs_s = n / dt
+    return {"value": pairs_s / cfg.topk, "unit": "tokens/s", "pairs_per_s": pairs_s,
+            "cores": cores, "kind": "oracle",
+            "sample": f"{n} routed rows of experts {experts.tolist()} of {cfg.name} through "
+                      f"their experts (the per-pair work; routing and the reduce left out), "
+                      f"fp64 loops, {cores} OpenMP threads, {dt:.2f} s",
+            "full_run_s_extrapolated": cfg.P / pairs_s}
+
+
+def torch_index(idx, device):
+    import torch
+    return torch.from_numpy(np.asarray(idx, np.int64)).to(device)
+
+
+def cpu_baseline_batched(cfg, d, n_rows=128):
+    """The oracle's BatchedExperts rows (each valid row through its expert)
+    on a seeded sample of valid rows, all host cores; rows/s, and the whole
+    run extrapolated."""
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    counts = d["counts"].clamp(0, cfg.M).cpu().numpy()
+    valid = np.array([(e, r) for e in range(cfg.E) for r in range(int(counts[e]))], np.int32)
+    rng = np.random.default_rng(0)
+    rows = valid[np.sort(rng.choice(len(valid), min(n_rows, len(valid)), replace=False))]
+    blocks = {}
+    for e in np.unique(rows[:, 0]):
+        b1, b2 = WL.bf16_bits(d["w1"][e]), WL.bf16_bits(d["w2"][e])
+        if cfg.dtype == WL.FP8:
+            q1, s1 = orc.quant_fp8_block(b1)
+            q2, s2 = orc.quant_fp8_block(b2)
+            blocks[int(e)] = (q1, q2, s1, s2)
+        else:
+            blocks[int(e)] = (b1, b2)
+    W = orc.Weights(cfg.dtype, experts=blocks, E=cfg.E, N=cfg.N, K=cfg.K)
+    xb = WL.bf16_bits(d["x_b"])
+    out = np.empty((cfg.E, cfg.M, cfg.K), np.float64)  # only the sampled rows are written
+    t = time.perf_counter()
+    orc.batched_experts(xb, counts, W, rows=rows, requant_h=cfg.dtype == WL.FP8,
+                        nthreads=cores, out=out)
+    dt = time.perf_counter() - t
+    return {"value": len(rows) / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} of {len(valid)} valid rows of {cfg.name}, fp64 loops, "
+                      f"{cores} OpenMP threads, {dt:.1f} s",
+            "full_run_s_extrapolated": len(valid) * dt / len(rows)}
 
 
 def cpu_baseline(cfg, layer, budget_s):
