@@ -487,6 +487,8 @@ def run_gpu(args, cfg):
         del layer
         torch.cuda.empty_cache()
         line["per_workload"] = run_extras(args, dev, skip=cfg.name)
+        if not args.no_next_rows:
+            line["next_rows"] = run_next_rows(args, dev)
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
@@ -522,6 +524,253 @@ def run_extras(args, dev, skip=None):
         out[cfg.name] = entry
         torch.cuda.empty_cache()
     return out
+
+
+def _timed(fn, steps, warmup, dev):
+    """Milliseconds per call of fn (whatever it enqueues, on any streams that
+    join the current one), CUDA events over `steps` calls after `warmup`,
+    with the clocks sampled in between."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        t0.record()
+        for _ in range(steps):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        wall1 = time.time()
+    return t0.elapsed_time(t1) / steps, clk.summary(wall0, wall1)
+
+
+def _tc_roof(flop, ms, fp8, timed_s, what):
+    peaks, src = _peaks()
+    key = "bf16_tflops" if timed_s < 2.0 else "bf16_tflops_sustained"
+    peak = peaks.get(key, FALLBACK_PEAKS[key]) * (2.0 if fp8 else 1.0)
+    achieved = flop / (ms / 1e3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None, "kernel": what,
+            "peak_source": f"{src} {key}" + (" x2 (nominal fp8:bf16 dense ratio)" if fp8 else "")
+                           + f" (timed region {timed_s:.2f} s)"}
+
+
+# the NEXT rows, each measured on a DeepSeek-V3-shaped workload
+NEXT_STANDARD = [(WL.DSV3_PREFILL_FP8CH, "NEXT-2: e4m3, one scale per token and per weight row"),
+                 (WL.DSV3_PREFILL_FP8T, "NEXT-2: e4m3, one dynamic scale per activation tensor")]
+SHARED_NS = 2048          # DeepSeek-V3's shared expert: intermediate size 2048
+CHUNK = 2048              # tokens per chunk of the chunked layer
+
+
+def run_next_rows(args, dev):
+    """The NEXT rows timed like the workloads above (event-timed calls over
+    resident inputs, clocks sampled inside the timed region): the per-channel
+    and per-tensor e4m3 layers; the block-scaled e4m3 layer with its shared
+    expert overlapped on an auxiliary stream (and the same calls one after
+    the other); that layer in chunks of 2048 tokens; and the worst-tokens EP
+    layer of eight shards (route, e4m3 dispatch, eight masked expert GEMM
+    pairs, combine) replayed from one CUDA graph."""
+    import torch
+    steps = max(20, min(args.steps, 100))
+    warmup = max(3, min(args.warmup, 10))
+    cpu_full = not args.no_cpu_baseline and _dist()[0] == 1
+    out = {}
+    for cfg, row in NEXT_STANDARD:
+        t = time.time()
+        e = measure_standard_entry(cfg, dev, steps, warmup, cpu_full)
+        e["row"] = row
+        e["wall_s"] = time.time() - t
+        out[cfg.name] = e
+        torch.cuda.empty_cache()
+    t = time.time()
+    sh, ch = measure_shared_and_chunked(WL.DSV3_PREFILL_FP8, dev, steps, warmup)
+    sh["wall_s"] = ch["wall_s"] = time.time() - t
+    out[WL.DSV3_PREFILL_FP8.name + "_shared_expert_overlapped"] = sh
+    out[WL.DSV3_PREFILL_FP8.name + f"_chunked_{CHUNK}"] = ch
+    torch.cuda.empty_cache()
+    t = time.time()
+    e = measure_ep_entry(WL.EP8_DSV3, dev, steps, warmup)
+    e["wall_s"] = time.time() - t
+    out[WL.EP8_DSV3.name + "_fp8"] = e
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_shared_and_chunked(cfg, dev, steps, warmup):
+    """The one-call e4m3 layer (moe_forward) with a shared expert of
+    intermediate size SHARED_NS in block-scaled e4m3: routed alone, shared
+    alone, both one after the other on one stream, and overlapped (the
+    shared expert on an auxiliary stream, moe_forward_shared); then the
+    routed layer in chunks of CHUNK tokens (moe_forward_chunked, a workspace
+    sized for one chunk)."""
+    import torch
+    layer = Layer(cfg, dev)
+    g = layer.g
+    M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
+    Ns = SHARED_NS
+    gen = torch.Generator(device=dev).manual_seed(cfg.seed + 100)
+    w1s = (torch.randn((2 * Ns, K), generator=gen, device=dev) / K ** 0.5).to(torch.bfloat16)
+    w2s = (torch.randn((K, Ns), generator=gen, device=dev) / Ns ** 0.5).to(torch.bfloat16)
+    q1 = torch.empty((2 * Ns, K), dtype=torch.uint8, device=dev)
+    q2 = torch.empty((K, Ns), dtype=torch.uint8, device=dev)
+    s1 = torch.empty((2 * Ns // 128, K // 128), dtype=torch.float32, device=dev)
+    s2 = torch.empty((K // 128, Ns // 128), dtype=torch.float32, device=dev)
+    g.moe_quant_fp8_block(w1s, q1, s1)
+    g.moe_quant_fp8_block(w2s, q2, s2)
+    del w1s, w2s
+    out_sh = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    ws = layer.fwd_ws
+    ws_sh = g.workspace(g.WS_SHARED, M, 1, Ns, K, 1, WL.FP8, device=dev)
+    args = (layer.x, layer.logits, layer.bias, N, E, k, cfg.score_fn, cfg.n_groups,
+            cfg.topk_groups, cfg.renorm, cfg.dtype, layer.w1, layer.w1s, layer.w2, layer.w2s)
+    shk = dict(shared_dtype=WL.FP8, w1s_scales=s1, w2s_scales=s2, err_word=layer.err)
+    aux = torch.cuda.Stream()
+    ev_in, ev_out = torch.cuda.Event(), torch.cuda.Event()
+
+    def routed():
+        g.moe_forward(*args, layer.out, ws, err_word=layer.err)
+
+    def shared():
+        g.moe_shared_expert_forward(layer.x, Ns, q1, q2, out_sh, ws_sh, dtype=WL.FP8,
+                                    w1s_scales=s1, w2s_scales=s2, err_word=layer.err)
+
+    def serial():
+        g.moe_forward_shared(*args, layer.out, ws, Ns, q1, q2, out_sh, ws_sh, **shk)
+
+    def overlapped():
+        g.moe_forward_shared(*args, layer.out, ws, Ns, q1, q2, out_sh, ws_sh, aux_stream=aux,
+                             ev_input_ready=ev_in, ev_output_ready=ev_out, **shk)
+
+    t_r, _ = _timed(routed, steps, warmup, dev)
+    t_s, _ = _timed(shared, steps, warmup, dev)
+    t_ser, _ = _timed(serial, steps, warmup, dev)
+    t_ovl, clk = _timed(overlapped, steps, warmup, dev)
+    routed_flop = 6.0 * K * N * cfg.P
+    shared_flop = 6.0 * K * Ns * M
+    sh = {"row": "NEXT-3: shared expert (block-scaled e4m3) overlapped on an auxiliary stream",
+          "unit": "tokens/s", "value": M / (t_ovl / 1e3), "steps": steps,
+          "ms_per_step": t_ovl, "serial_ms_per_step": t_ser, "routed_alone_ms": t_r,
+          "shared_alone_ms": t_s, "overlap_saved_ms": t_ser - t_ovl,
+          "layer_tflops": (routed_flop + shared_flop) / (t_ovl / 1e3) / 1e12,
+          "roofline": _tc_roof(routed_flop + shared_flop, t_ovl, True, t_ovl * steps / 1e3,
+                               "whole layer: routed experts + shared expert"),
+          "clocks": clk, "config": {"M": M, "K": K, "N": N, "E": E, "topk": k,
+                                    "shared_intermediate": Ns,
+                                    "scales": _scales_desc(cfg)}}
+    ws_c = g.workspace(g.WS_FORWARD, CHUNK, E, N, K, k, cfg.dtype, device=dev)
+
+    def chunked():
+        g.moe_forward_chunked(*args, layer.out, ws_c, CHUNK, err_word=layer.err)
+
+    t_c, clk_c = _timed(chunked, steps, warmup, dev)
+    torch.cuda.synchronize()
+    assert layer.err.item() == 0, f"device error word {layer.err.item()}"
+    ch = {"row": "NEXT-3: in-graph chunking (device-side counts per chunk)",
+          "unit": "tokens/s", "value": M / (t_c / 1e3), "steps": steps,
+          "ms_per_step": t_c, "unchunked_ms_per_step": t_r, "chunk_tokens": CHUNK,
+          "workspace_bytes": ws_c.numel(), "unchunked_workspace_bytes": ws.numel(),
+          "roofline": _tc_roof(routed_flop, t_c, True, t_c * steps / 1e3,
+                               "whole layer, all chunks"),
+          "clocks": clk_c, "config": {"M": M, "K": K, "N": N, "E": E, "topk": k,
+                                      "scales": _scales_desc(cfg)}}
+    del layer
+    return sh, ch
+
+
+def measure_ep_entry(cfg, dev, steps, warmup):
+    """The worst-tokens EP layer of cfg.G shards in this GPU's memory, e4m3:
+    route every shard's tokens, quantise them in 1 x 128 groups, dispatch
+    the valid pairs into the experts' static receive blocks (device counts),
+    run each shard's masked expert GEMMs on its block, combine -- captured
+    once in a CUDA graph and replayed; the same sequence launched eagerly
+    for comparison.  The roofline counts the valid pairs' expert work and
+    the e4m3 weights of the experts that received rows."""
+    import torch
+    import mixture_experts_layer_count_gb300 as g
+    g.load()
+    G, M, K, N, E, k = cfg.G, cfg.M, cfg.K, cfg.N, cfg.E, cfg.topk
+    W = cfg.worst_tokens
+    El = E // G
+    d = WL.make_ep_inputs(cfg, dev)
+    q1 = torch.empty((E, 2 * N, K), dtype=torch.uint8, device=dev)
+    q2 = torch.empty((E, K, N), dtype=torch.uint8, device=dev)
+    s1 = torch.empty((E, 2 * N // 128, K // 128), dtype=torch.float32, device=dev)
+    s2 = torch.empty((E, K // 128, N // 128), dtype=torch.float32, device=dev)
+    g.moe_quant_fp8_block(d["w1"], q1, s1)
+    g.moe_quant_fp8_block(d["w2"], q2, s2)
+    del d["w1"], d["w2"]
+    torch.cuda.empty_cache()
+    i32, f32 = torch.int32, torch.float32
+    x, logits, num_tokens = d["x"], d["logits"], d["num_tokens"]
+    ids = torch.empty((G, M, k), dtype=i32, device=dev)
+    wts = torch.empty((G, M, k), dtype=f32, device=dev)
+    xq = torch.empty((G, M, K), dtype=torch.uint8, device=dev)
+    xs = torch.empty((G * M, K // 128), dtype=f32, device=dev)
+    recv_x = torch.empty((E, W, K), dtype=torch.uint8, device=dev)
+    recv_s = torch.empty((E * W, K // 128), dtype=f32, device=dev)
+    recv_y = torch.empty((E, W, K), dtype=torch.bfloat16, device=dev)
+    recv_counts = torch.empty(E, dtype=i32, device=dev)
+    recv_pos = torch.empty((G, M, k), dtype=i32, device=dev)
+    out = torch.empty((G, M, K), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=i32, device=dev)
+    ws = g.workspace(g.WS_EP_DISPATCH, M, E, G, K, k, 0, device=dev)
+    bws = [g.workspace(g.WS_BATCHED, W, El, N, K, 1, WL.FP8, device=dev) for _ in range(G)]
+
+    def step():
+        g.moe_topk_route(logits.view(G * M, E), None, k, cfg.score_fn, cfg.n_groups,
+                         cfg.topk_groups, True, ids.view(G * M, k), wts.view(G * M, k))
+        g.moe_quant_fp8_group(x.view(G * M, K), xq.view(G * M, K), xs)
+        g.moe_ep_dispatch(xq, num_tokens, ids, E, W, recv_x, recv_counts, recv_pos, ws, err,
+                          dtype=WL.FP8, x_scales=xs, recv_scales=recv_s)
+        for r in range(G):
+            sl = slice(r * El, (r + 1) * El)
+            g.moe_batched_masked_experts(recv_x[sl], recv_counts[sl], N, q1[sl], q2[sl],
+                                         recv_y[sl], bws[r], dtype=WL.FP8,
+                                         x_b_scales=recv_s[r * El * W:(r + 1) * El * W],
+                                         w1_scales=s1[sl], w2_scales=s2[sl], err_word=err)
+        g.moe_ep_combine(recv_y, ids, recv_pos, wts, num_tokens, out)
+
+    t_eager, _ = _timed(step, min(steps, 20), warmup, dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    t_graph, clk = _timed(graph.replay, steps, warmup, dev)
+    torch.cuda.synchronize()
+    assert err.item() == 0, f"device error word {err.item()}"
+    counts = recv_counts.cpu().numpy()
+    tokens = int(num_tokens.sum().item())
+    pairs = int(counts.sum())
+    flop = 6.0 * K * N * pairs
+    touched = int((counts > 0).sum())
+    wbytes = touched * (3 * N * K + (2 * N // 128 * (K // 128) + (K // 128) * (N // 128)) * 4)
+    gbs = wbytes / (t_graph / 1e3) / 1e9
+    peaks, src = _peaks()
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tc = _tc_roof(flop, t_graph, True, t_graph * steps / 1e3,
+                  "EP layer: route, dispatch, 8 shards' masked e4m3 GEMMs, combine")
+    roof = tc if tc["achieved"] / tc["peak"] >= gbs / hbm_peak else {
+        "bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+        "frac": gbs / hbm_peak, "traffic": None, "kernel": tc["kernel"],
+        "peak_source": f"{src} hbm_gbs (copy)"}
+    roof["tensor_frac"] = tc["frac"]
+    roof["hbm_frac"] = gbs / hbm_peak
+    del graph
+    return {"row": "NEXT-4: worst-tokens EP dispatch/combine, single-GPU form (8 shards)",
+            "unit": "tokens/s", "value": tokens / (t_graph / 1e3), "steps": steps,
+            "ms_per_step": t_graph, "graph_ms_per_step": t_graph,
+            "eager_ms_per_step": t_eager, "valid_tokens": tokens, "valid_pairs": pairs,
+            "experts_with_rows": touched, "roofline": roof, "clocks": clk,
+            "config": {"G": G, "M_per_shard": M, "K": K, "N": N, "E": E, "topk": k,
+                       "worst_tokens": W, "scales": "fp32, 1x128 activations / 128x128 weights"}}
 
 
 def measure_standard_entry(cfg, dev, steps, warmup, cpu_full=False):
@@ -1112,6 +1361,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="leave out the next_rows object (shared experts, chunking, EP, "
+                         "per-channel and per-tensor e4m3)")
     ap.add_argument("--no-extras", action="store_true",
                     help="time only the chosen workload (no per_workload object)")
     args = ap.parse_args()

@@ -287,6 +287,10 @@ EP2 = EpConfig("ep_worst_tokens_G2_M96_K512_N256_E32_top4", G=2, M=96, K=512, N=
                topk=4, seed=71)
 EP4 = EpConfig("ep_worst_tokens_G4_M64_K384_N256_E64_top6", G=4, M=64, K=384, N=256, E=64,
                topk=6, score_fn=SIGMOID, n_groups=8, topk_groups=4, seed=72)
+# DeepSeek-V3-shaped experts split over eight shards (an EP8 layer's shards
+# emulated in one GPU's memory), 256 tokens per shard
+EP8_DSV3 = EpConfig("ep_worst_tokens_G8_M256_K7168_N2048_E256_top8", G=8, M=256, K=7168,
+                    N=2048, E=256, topk=8, score_fn=SIGMOID, n_groups=8, topk_groups=4, seed=73)
 
 
 def make_ep_inputs(cfg: EpConfig, device="cpu", seed: Optional[int] = None,
