@@ -487,8 +487,8 @@ def run_gpu(args, cfg):
         del layer
         torch.cuda.empty_cache()
         line["per_workload"] = run_extras(args, dev, skip=cfg.name)
-        if not args.no_next_rows:
-            line["next_rows"] = run_next_rows(args, dev)
+        if not args.no_features:
+            line["features"] = run_features(args, dev)
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
@@ -559,15 +559,15 @@ def _tc_roof(flop, ms, fp8, timed_s, what):
                            + f" (timed region {timed_s:.2f} s)"}
 
 
-# the NEXT rows, each measured on a DeepSeek-V3-shaped workload
-NEXT_STANDARD = [(WL.DSV3_PREFILL_FP8CH, "NEXT-2: e4m3, one scale per token and per weight row"),
-                 (WL.DSV3_PREFILL_FP8T, "NEXT-2: e4m3, one dynamic scale per activation tensor")]
+# the wider features, each measured on a DeepSeek-V3-shaped workload
+FEATURE_STANDARD = [(WL.DSV3_PREFILL_FP8CH, "e4m3, one scale per token and per weight row"),
+                    (WL.DSV3_PREFILL_FP8T, "e4m3, one dynamic scale per activation tensor")]
 SHARED_NS = 2048          # DeepSeek-V3's shared expert: intermediate size 2048
 CHUNK = 2048              # tokens per chunk of the chunked layer
 
 
-def run_next_rows(args, dev):
-    """The NEXT rows timed like the workloads above (event-timed calls over
+def run_features(args, dev):
+    """The layer's wider features timed like the workloads above (event-timed calls over
     resident inputs, clocks sampled inside the timed region): the per-channel
     and per-tensor e4m3 layers; the block-scaled e4m3 layer with its shared
     expert overlapped on an auxiliary stream (and the same calls one after
@@ -579,10 +579,10 @@ def run_next_rows(args, dev):
     warmup = max(3, min(args.warmup, 10))
     cpu_full = not args.no_cpu_baseline and _dist()[0] == 1
     out = {}
-    for cfg, row in NEXT_STANDARD:
+    for cfg, feature in FEATURE_STANDARD:
         t = time.time()
         e = measure_standard_entry(cfg, dev, steps, warmup, cpu_full)
-        e["row"] = row
+        e["feature"] = feature
         e["wall_s"] = time.time() - t
         out[cfg.name] = e
         torch.cuda.empty_cache()
@@ -651,7 +651,7 @@ def measure_shared_and_chunked(cfg, dev, steps, warmup):
     t_ovl, clk = _timed(overlapped, steps, warmup, dev)
     routed_flop = 6.0 * K * N * cfg.P
     shared_flop = 6.0 * K * Ns * M
-    sh = {"row": "NEXT-3: shared expert (block-scaled e4m3) overlapped on an auxiliary stream",
+    sh = {"feature": "shared expert (block-scaled e4m3) overlapped on an auxiliary stream",
           "unit": "tokens/s", "value": M / (t_ovl / 1e3), "steps": steps,
           "ms_per_step": t_ovl, "serial_ms_per_step": t_ser, "routed_alone_ms": t_r,
           "shared_alone_ms": t_s, "overlap_saved_ms": t_ser - t_ovl,
@@ -669,7 +669,7 @@ def measure_shared_and_chunked(cfg, dev, steps, warmup):
     t_c, clk_c = _timed(chunked, steps, warmup, dev)
     torch.cuda.synchronize()
     assert layer.err.item() == 0, f"device error word {layer.err.item()}"
-    ch = {"row": "NEXT-3: in-graph chunking (device-side counts per chunk)",
+    ch = {"feature": "in-graph chunking (device-side counts per chunk)",
           "unit": "tokens/s", "value": M / (t_c / 1e3), "steps": steps,
           "ms_per_step": t_c, "unchunked_ms_per_step": t_r, "chunk_tokens": CHUNK,
           "workspace_bytes": ws_c.numel(), "unchunked_workspace_bytes": ws.numel(),
@@ -764,7 +764,7 @@ def measure_ep_entry(cfg, dev, steps, warmup):
     roof["tensor_frac"] = tc["frac"]
     roof["hbm_frac"] = gbs / hbm_peak
     del graph
-    return {"row": "NEXT-4: worst-tokens EP dispatch/combine, single-GPU form (8 shards)",
+    return {"feature": "worst-tokens EP dispatch/combine, single-GPU form (8 shards)",
             "unit": "tokens/s", "value": tokens / (t_graph / 1e3), "steps": steps,
             "ms_per_step": t_graph, "graph_ms_per_step": t_graph,
             "eager_ms_per_step": t_eager, "valid_tokens": tokens, "valid_pairs": pairs,
@@ -1361,8 +1361,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-next-rows", action="store_true",
-                    help="leave out the next_rows object (shared experts, chunking, EP, "
+    ap.add_argument("--no-features", action="store_true",
+                    help="leave out the features object (shared experts, chunking, EP, "
                          "per-channel and per-tensor e4m3)")
     ap.add_argument("--no-extras", action="store_true",
                     help="time only the chosen workload (no per_workload object)")
