@@ -213,9 +213,9 @@ class Layer:
         self.amax = torch.zeros(2, dtype=i32, device=device) if self.tensor else None
         self.fwd_ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype, device=device)
         # route, 3 align, [quant x], gather, gate/up, [quant H], down, reduce;
-        # 1 x 128 e4m3 quantises and gathers in one launch; a per-tensor
-        # quant is a clear, a maximum and the codes
-        self.launches_per_step = (8 + (1 if self.ch else 0) + (1 if self.ch else 0)
+        # 1 x 128 and per-token e4m3 quantise and gather in one launch; a
+        # per-tensor quant is a clear, a maximum and the codes
+        self.launches_per_step = (8 + (1 if self.ch else 0) + (1 if self.tensor else 0)
                                   + (4 if self.tensor else 0))
 
     def step(self, ev_gemm=None, mark=None):
@@ -236,14 +236,14 @@ class Layer:
             g.moe_quant_fp8_tensor(self.x, self.xq, self.xs, self.amax[0:1])
             src, src_s = self.xq, self.xs
             mark("a4_quant_x")
-        elif self.ch:
-            g.moe_quant_fp8_group(self.x, self.xq, self.xs, group=K)
-            src, src_s = self.xq, self.xs
-            mark("a4_quant_x")
         if self.fp8 and not self.ch and not self.tensor:
             # 1 x 128 groups: quantised once, codes and scales written to the
             # permuted rows in the same pass
             g.moe_quant_fp8_group_permute(self.x, self.inv, k, self.A, self.As)
+            mark("a4_a3_quant_permute")
+        elif self.ch and not self.tensor:
+            # one scale per token: likewise
+            g.moe_quant_fp8_row_permute(self.x, self.inv, k, self.A, self.As.view(-1))
             mark("a4_a3_quant_permute")
         else:
             g.moe_permute_rows(src, src_s, self.sorted, self.offsets, k, E, c.dtype, self.A,

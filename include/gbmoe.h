@@ -278,6 +278,18 @@ gbmoe_status_t moe_quant_fp8_group_permute(const uint16_t *x,
                                            uint8_t *A, float *A_scales,
                                            gbmoe_stream_t stream);
 
+/* The same for one scale per token (moe_quant_fp8_group with group = K, and
+ * moe_permute_rows with dtype GBMOE_FP8_E4M3_CHANNEL) in one pass: a row's
+ * codes and its scale go to every permuted row of the token's pairs,
+ * A[inv[p]] and A_scales[inv[p]] (pairs with inv[p] < 0 skipped); equal to
+ * the two calls bit for bit.  Arguments as moe_quant_fp8_group_permute, with
+ * A_scales (M*topk) fp32 (4-byte aligned). */
+gbmoe_status_t moe_quant_fp8_row_permute(const uint16_t *x,
+                                         const float *row_weights, int M,
+                                         int K, const int32_t *inv, int topk,
+                                         uint8_t *A, float *A_scales,
+                                         gbmoe_stream_t stream);
+
 /* First expert GEMM with the gated activation fused into its epilogue:
  * the first GEMM of FusedMoEPermuteExpertsUnpermute.apply followed by its
  * gated activation (and, for block-scaled e4m3, the requantisation of the

@@ -61,6 +61,7 @@ _SIGS = {
     "moe_quant_fp8_group": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_quant_fp8_tensor": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_tensor_static": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_quant_fp8_row_permute": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P]),
     "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
     "moe_permute_rows": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm_gate_up_silu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
@@ -202,6 +203,15 @@ def moe_quant_fp8_tensor(x, q, row_scales, amax_ws, n_rows=None, stream=None,
     _check("moe_quant_fp8_tensor", load().moe_quant_fp8_tensor(
         _ptr(x), _ptr(row_weights), M, K, _ptr(n_rows), _ptr(q), _ptr(row_scales),
         _ptr(amax_ws), _stream(stream)))
+
+
+def moe_quant_fp8_row_permute(x, inv, topk, A, A_scales, row_weights=None, stream=None):
+    """One scale per token, quantised and written to the permuted rows in one
+    pass: A[inv[p]] gets its token's codes and A_scales[inv[p]] its scale."""
+    M, K = x.shape
+    _check("moe_quant_fp8_row_permute", load().moe_quant_fp8_row_permute(
+        _ptr(x), _ptr(row_weights), M, K, _ptr(inv), topk, _ptr(A), _ptr(A_scales),
+        _stream(stream)))
 
 
 def moe_quant_fp8_tensor_static(x, scale, q, row_scales, n_rows=None, stream=None,

@@ -438,6 +438,22 @@ gbmoe_status_t moe_quant_fp8_group_permute(const uint16_t *x, const float *row_w
                                               (cudaStream_t)stream));
 }
 
+gbmoe_status_t moe_quant_fp8_row_permute(const uint16_t *x, const float *row_weights,
+                                         int M, int K, const int32_t *inv, int topk,
+                                         uint8_t *A, float *A_scales, gbmoe_stream_t stream) {
+  if (M < 0 || K < 128 || K % 128 != 0 || topk < 1 || topk > kMaxTopk) return GBMOE_INVALID_ARG;
+  if (row_weights && topk != 1) return GBMOE_INVALID_ARG;
+  if ((size_t)M * topk > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
+  if (M > 0 && (!x || !inv || !A || !A_scales || !aligned16(x) || !aligned16(A) ||
+                (reinterpret_cast<uintptr_t>(A_scales) & 3u)))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK || M == 0) return st;
+  return from_cuda(launch_quant_row_scatter(x, row_weights, M, K, inv, topk, A, A_scales, sms,
+                                            (cudaStream_t)stream));
+}
+
 gbmoe_status_t moe_quant_fp8_tensor(const uint16_t *x, const float *row_weights,
                                     int M, int K, const int32_t *n_rows,
                                     uint8_t *q, float *row_scales,
@@ -788,6 +804,12 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
     // 1 x 128 groups: the codes and scales go straight to the permuted rows
     ce = launch_quant_group_scatter(x, in_w, M, K, w.inv, topk, static_cast<uint8_t *>(w.A),
                                     w.As, scale_ld((size_t)P), sms, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+  } else if (fp8ch && !fp8t) {
+    // one scale per token: likewise, the row's codes and its scale to every
+    // permuted row of the token's pairs
+    ce = launch_quant_row_scatter(x, in_w, M, K, w.inv, topk, static_cast<uint8_t *>(w.A), w.As,
+                                  sms, s);
     if (ce != cudaSuccess) return from_cuda(ce);
   } else {
     if (fp8) {

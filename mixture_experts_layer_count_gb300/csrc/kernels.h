@@ -74,6 +74,11 @@ cudaError_t launch_quant_group_scatter(const uint16_t *x, const float *row_w, in
                                        int64_t ld, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K,
                              uint8_t *q, float *scales, int num_sms, cudaStream_t s);
+// launch_quant_row writing codes and the row's scale straight to the permuted
+// rows: A row inv[t*topk + j] (skipped when negative), As[that row]; topk <= 32
+cudaError_t launch_quant_row_scatter(const uint16_t *x, const float *row_w, int M, int K,
+                                     const int32_t *inv, int topk, uint8_t *A, float *As,
+                                     int num_sms, cudaStream_t s);
 // static_scale (device fp32) or NULL: the codes use that scale instead of the
 // tensor's maximum (amax then unused)
 cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, int K,

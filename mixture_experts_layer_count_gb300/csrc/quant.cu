@@ -157,10 +157,15 @@ __global__ void __launch_bounds__(256)
 }
 
 // one warp per row, the group being the whole row: the row maximum, then
-// the codes (the row is read again, from L1/L2); 8 values per 16-byte load
+// the codes (the row is read again, from L1/L2); 8 values per 16-byte load.
+// SCATTER: the codes and the scale go straight to the permuted rows of the
+// token's pairs (the gather of moe_permute_rows folded in): row
+// inv[t * topk + j] of q, skipped when negative, and scales[that row].
+template <bool SCATTER>
 __global__ void __launch_bounds__(256)
     quant_row_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w, int M,
-                     int K, uint2 *__restrict__ q, float *__restrict__ scales) {
+                     int K, uint2 *__restrict__ q, float *__restrict__ scales,
+                     const int32_t *__restrict__ inv, int topk) {
   const int lane = threadIdx.x & 31;
   const int vecs = K / 8;
   for (size_t t = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; t < (size_t)M;
@@ -185,24 +190,43 @@ __global__ void __launch_bounds__(256)
     for (int off = 16; off > 0; off >>= 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const float s = group_scale(amax);
-    for (int v = lane; v < vecs; v += 32) {
-      const uint4 raw = xr[v];
-      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t c[8];
+    // SCATTER: lane j < topk holds the row of pair j (topk <= 32)
+    const int my_dst = SCATTER && lane < topk ? __ldg(inv + t * topk + lane) : -1;
+    for (int v0 = 0; v0 < vecs; v0 += 32) {  // uniform over the warp (the shuffles below)
+      const int v = v0 + lane;
+      const bool live = v < vecs;
+      uint2 code = make_uint2(0u, 0u);
+      if (live) {
+        const uint4 raw = xr[v];
+        const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t c[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float a = bf16_bits_to_float(u[i] & 0xffffu), b = bf16_bits_to_float(u[i] >> 16);
-        if (row_w) {
-          a = __fmul_rn(a, w);
-          b = __fmul_rn(b, w);
+        for (int i = 0; i < 4; ++i) {
+          float a = bf16_bits_to_float(u[i] & 0xffffu), b = bf16_bits_to_float(u[i] >> 16);
+          if (row_w) {
+            a = __fmul_rn(a, w);
+            b = __fmul_rn(b, w);
+          }
+          c[2 * i] = e4m3_of(__fdiv_rn(a, s));
+          c[2 * i + 1] = e4m3_of(__fdiv_rn(b, s));
         }
-        c[2 * i] = e4m3_of(__fdiv_rn(a, s));
-        c[2 * i + 1] = e4m3_of(__fdiv_rn(b, s));
+        code = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                          c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
       }
-      q[t * vecs + v] = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
-                                   c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+      if (SCATTER) {
+        for (int j = 0; j < topk; ++j) {
+          const int dst = __shfl_sync(0xffffffffu, my_dst, j);
+          if (live && dst >= 0) q[(size_t)dst * vecs + v] = code;
+        }
+      } else if (live) {
+        q[t * vecs + v] = code;
+      }
     }
-    if (lane == 0) scales[t] = s;
+    if (SCATTER) {
+      if (my_dst >= 0) scales[my_dst] = s;
+    } else if (lane == 0) {
+      scales[t] = s;
+    }
   }
 }
 
@@ -362,9 +386,23 @@ cudaError_t launch_quant_row(const uint16_t *x, const float *row_w, int M, int K
   const size_t resident = (size_t)num_sms * 8;
   if (blocks > resident) blocks = resident;
   if (blocks < 1) blocks = 1;
-  quant_row_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+  quant_row_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(
       reinterpret_cast<const uint4 *>(x), row_w, M, K, reinterpret_cast<uint2 *>(q),
-      scales);
+      scales, nullptr, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_row_scatter(const uint16_t *x, const float *row_w, int M, int K,
+                                     const int32_t *inv, int topk, uint8_t *A, float *As,
+                                     int num_sms, cudaStream_t s) {
+  if (topk < 1 || topk > 32) return cudaErrorInvalidValue;
+  size_t blocks = ((size_t)M + 7) / 8;
+  const size_t resident = (size_t)num_sms * 8;
+  if (blocks > resident) blocks = resident;
+  if (blocks < 1) blocks = 1;
+  quant_row_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), row_w, M, K, reinterpret_cast<uint2 *>(A), As, inv,
+      topk);
   return cudaGetLastError();
 }
 

@@ -195,6 +195,13 @@ def test_gemm_calls_reject_bad_arguments(lib):
     assert qp(P16, None, 16, 256, None, 4, P16, P16, None) == INVALID  # no inverse map
     assert qp(P_ODD, None, 16, 256, P16, 4, P16, P16, None) == INVALID
     assert qp(P16, None, 16, 256, P16, 4, P16, P16 + 2, None) == INVALID
+    rp = lib.moe_quant_fp8_row_permute
+    #         x    rw    M   K    inv  k  A    As   s
+    assert rp(P16, None, 16, 200, P16, 4, P16, P16, None) == INVALID   # K % 128
+    assert rp(P16, P16, 16, 256, P16, 2, P16, P16, None) == INVALID    # row weights need top-1
+    assert rp(P16, None, 16, 256, P16, 33, P16, P16, None) == INVALID  # topk > 32
+    assert rp(P16, None, 16, 256, None, 4, P16, P16, None) == INVALID  # no inverse map
+    assert rp(P_ODD, None, 16, 256, P16, 4, P16, P16, None) == INVALID
     b = lib.moe_batched_masked_experts
     #        xb  xbs   cnt E  T   N    K    w1   w1s  w2   w2s  dt ac yb   ws   wsb  err  s
     assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 2, 0, P16, P16, 1 << 30, None, None) == UNSUPPORTED

@@ -151,8 +151,10 @@ def test_quant_fp8_group_bit_exact():
 
 
 @pytest.mark.parametrize("case", ["all_local", "expert_map", "weight_on_input"])
-def test_quant_fp8_group_permute_bit_exact(case):
-    """Quantisation and permutation in one pass: codes and group-major scales
+@pytest.mark.parametrize("per_row", [False, True], ids=["groups_of_128", "one_scale_per_row"])
+def test_quant_fp8_group_permute_bit_exact(case, per_row):
+    """Quantisation and permutation in one pass (1 x 128 groups, or one scale
+    per row): codes and group-major scales
     of every permuted row bit-exact against the oracle's group quantiser and
     stable sort (A[i] = codes of token sorted[i] / topk), pairs not routed to
     a local expert skipped, rows at and beyond the local total untouched;
@@ -181,10 +183,13 @@ def test_quant_fp8_group_permute_bit_exact(case):
                         E_global=E if emap is not None else None)
     ld = (P + 3) // 4 * 4
     A = torch.full((P, K), 0xA5, dtype=torch.uint8, device=DEV)
-    As = torch.full((K // 128, ld), -7.0, dtype=torch.float32, device=DEV)
-    g.moe_quant_fp8_group_permute(x, inv, topk, A, As, row_weights=rw)
+    As = torch.full((1 if per_row else K // 128, ld), -7.0, dtype=torch.float32, device=DEV)
+    if per_row:  # moe_quant_fp8_row_permute: one scale per token (A_scales[row])
+        g.moe_quant_fp8_row_permute(x, inv, topk, A, As.view(-1), row_weights=rw)
+    else:
+        g.moe_quant_fp8_group_permute(x, inv, topk, A, As, row_weights=rw)
     torch.cuda.synchronize()
-    rq, rs = orc.quant_fp8_group(WL.bf16_bits(x),
+    rq, rs = orc.quant_fp8_group(WL.bf16_bits(x), group=K if per_row else 128,
                                  row_weights=None if rw is None else rw.cpu().numpy())
     ro, rsrt, rinv = orc.align(ids.cpu().numpy(), E,
                                expert_map=None if emap is None else emap.cpu().numpy(),
