@@ -194,8 +194,6 @@ class Layer:
         self.align_ws = g.workspace(g.WS_ALIGN, M, E, 0, 0, k, 0, device=device)
         adt = torch.uint8 if self.fp8 else torch.bfloat16
         sk = 1 if self.ch else K // 128   # scales per row of x / A
-        self.xq = torch.empty((M, K), dtype=torch.uint8, device=device) if self.fp8 else None
-        self.xs = torch.empty((M, sk), dtype=f32, device=device) if self.fp8 else None
         self.A = torch.empty((P, K), dtype=adt, device=device)
         ld = (P + 3) // 4 * 4  # group-major FP8 row scales
         self.As = torch.empty((sk, ld), dtype=f32, device=device) if self.fp8 else None
@@ -212,11 +210,10 @@ class Layer:
         self.err = torch.zeros(1, dtype=i32, device=device)
         self.amax = torch.zeros(2, dtype=i32, device=device) if self.tensor else None
         self.fwd_ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype, device=device)
-        # route, 3 align, [quant x], gather, gate/up, [quant H], down, reduce;
-        # 1 x 128 and per-token e4m3 quantise and gather in one launch; a
-        # per-tensor quant is a clear, a maximum and the codes
-        self.launches_per_step = (8 + (1 if self.ch else 0) + (1 if self.tensor else 0)
-                                  + (4 if self.tensor else 0))
+        # route, 3 align, gather, gate/up, [quant H], down, reduce; e4m3
+        # quantises x and gathers in one launch (per tensor: after a clear
+        # and a maximum, as its H quant is a clear, a maximum and the codes)
+        self.launches_per_step = 8 + (1 if self.ch else 0) + (4 if self.tensor else 0)
 
     def step(self, ev_gemm=None, mark=None):
         """One layer pass as its separate calls.  ev_gemm: a pair of events
@@ -231,11 +228,6 @@ class Layer:
         g.moe_align_permute(self.ids, E, self.counts, self.offsets, self.sorted, self.inv,
                             self.align_ws, self.err)
         mark("a2_a3_count_align")
-        src, src_s = self.x, None
-        if self.tensor:
-            g.moe_quant_fp8_tensor(self.x, self.xq, self.xs, self.amax[0:1])
-            src, src_s = self.xq, self.xs
-            mark("a4_quant_x")
         if self.fp8 and not self.ch and not self.tensor:
             # 1 x 128 groups: quantised once, codes and scales written to the
             # permuted rows in the same pass
@@ -245,8 +237,14 @@ class Layer:
             # one scale per token: likewise
             g.moe_quant_fp8_row_permute(self.x, self.inv, k, self.A, self.As.view(-1))
             mark("a4_a3_quant_permute")
+        elif self.tensor:
+            # one scale for the tensor: its maximum first, then the codes
+            # written to the permuted rows
+            g.moe_quant_fp8_tensor_permute(self.x, self.inv, k, self.A, self.As.view(-1),
+                                           amax_ws=self.amax[0:1])
+            mark("a4_a3_quant_permute")
         else:
-            g.moe_permute_rows(src, src_s, self.sorted, self.offsets, k, E, c.dtype, self.A,
+            g.moe_permute_rows(self.x, None, self.sorted, self.offsets, k, E, c.dtype, self.A,
                                self.As)
             mark("a3_gather")
         if ev_gemm is not None:

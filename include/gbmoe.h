@@ -290,6 +290,21 @@ gbmoe_status_t moe_quant_fp8_row_permute(const uint16_t *x,
                                          uint8_t *A, float *A_scales,
                                          gbmoe_stream_t stream);
 
+/* The same for one scale for the whole of x (dtype GBMOE_FP8_E4M3_TENSOR):
+ * the scale is scale[0] (a DEVICE fp32, static) or, when scale is NULL, the
+ * maximum over all M rows / 448 (reduced in amax_ws, 4 bytes of caller
+ * device memory, overwritten); every token's codes and the scale go to the
+ * permuted rows of its pairs, A[inv[p]] and A_scales[inv[p]], as
+ * moe_quant_fp8_tensor(_static) followed by moe_permute_rows would write
+ * them, bit for bit.  Arguments otherwise as moe_quant_fp8_row_permute;
+ * three launches with a dynamic scale, one with a static one. */
+gbmoe_status_t moe_quant_fp8_tensor_permute(const uint16_t *x,
+                                            const float *row_weights, int M,
+                                            int K, const int32_t *inv, int topk,
+                                            const float *scale, uint8_t *A,
+                                            float *A_scales, uint32_t *amax_ws,
+                                            gbmoe_stream_t stream);
+
 /* First expert GEMM with the gated activation fused into its epilogue:
  * the first GEMM of FusedMoEPermuteExpertsUnpermute.apply followed by its
  * gated activation (and, for block-scaled e4m3, the requantisation of the

@@ -62,6 +62,7 @@ _SIGS = {
     "moe_quant_fp8_tensor": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_tensor_static": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_row_permute": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_quant_fp8_tensor_permute": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P]),
     "moe_quant_fp8_block": (_I, [_P, _L, _I, _I, _P, _P, _P]),
     "moe_permute_rows": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm_gate_up_silu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
@@ -212,6 +213,17 @@ def moe_quant_fp8_row_permute(x, inv, topk, A, A_scales, row_weights=None, strea
     _check("moe_quant_fp8_row_permute", load().moe_quant_fp8_row_permute(
         _ptr(x), _ptr(row_weights), M, K, _ptr(inv), topk, _ptr(A), _ptr(A_scales),
         _stream(stream)))
+
+
+def moe_quant_fp8_tensor_permute(x, inv, topk, A, A_scales, scale=None, amax_ws=None,
+                                 row_weights=None, stream=None):
+    """One scale for all of x -- the static `scale` (a device fp32), else its
+    maximum / 448 (amax_ws: a 4-byte device buffer) -- quantised and written
+    to the permuted rows in one pass (A[inv[p]], A_scales[inv[p]])."""
+    M, K = x.shape
+    _check("moe_quant_fp8_tensor_permute", load().moe_quant_fp8_tensor_permute(
+        _ptr(x), _ptr(row_weights), M, K, _ptr(inv), topk, _ptr(scale), _ptr(A),
+        _ptr(A_scales), _ptr(amax_ws), _stream(stream)))
 
 
 def moe_quant_fp8_tensor_static(x, scale, q, row_scales, n_rows=None, stream=None,

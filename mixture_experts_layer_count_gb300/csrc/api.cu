@@ -84,8 +84,6 @@ bool valid_dtype(int dtype) { return dtype == GBMOE_BF16 || is_fp8(dtype); }
 struct ForwardWs {
   int32_t *ids, *counts, *offsets, *sorted, *inv, *chunk_hist;
   float *weights;
-  uint8_t *xq;
-  float *xs;
   void *A;
   float *As;
   void *H;
@@ -106,8 +104,6 @@ ForwardWs carve_forward(Carver &c, int M, int E, int N, int K, int topk, int dty
   w.chunk_hist = static_cast<int32_t *>(c.take((size_t)align_num_chunks((int)P) * E * 4));
   const bool fp8 = is_fp8(dtype);
   const int sk = scales_per_row(dtype, K), sn = scales_per_row(dtype, N);
-  w.xq = fp8 ? static_cast<uint8_t *>(c.take((size_t)M * K)) : nullptr;
-  w.xs = fp8 ? static_cast<float *>(c.take((size_t)M * sk * 4)) : nullptr;
   w.A = c.take(P * (size_t)K * elem_bytes(dtype));
   w.As = fp8 ? static_cast<float *>(c.take((size_t)scale_ld(P) * sk * 4)) : nullptr;
   w.H = c.take(P * (size_t)N * elem_bytes(dtype));
@@ -454,6 +450,25 @@ gbmoe_status_t moe_quant_fp8_row_permute(const uint16_t *x, const float *row_wei
                                             (cudaStream_t)stream));
 }
 
+gbmoe_status_t moe_quant_fp8_tensor_permute(const uint16_t *x, const float *row_weights,
+                                            int M, int K, const int32_t *inv, int topk,
+                                            const float *scale, uint8_t *A, float *A_scales,
+                                            uint32_t *amax_ws, gbmoe_stream_t stream) {
+  if (M < 0 || K < 128 || K % 128 != 0 || topk < 1 || topk > kMaxTopk) return GBMOE_INVALID_ARG;
+  if (row_weights && topk != 1) return GBMOE_INVALID_ARG;
+  if ((size_t)M * topk > (size_t)INT32_MAX) return GBMOE_INVALID_ARG;
+  if (M > 0 && (!x || !inv || !A || !A_scales || !aligned16(x) || !aligned16(A) ||
+                (reinterpret_cast<uintptr_t>(A_scales) & 3u) ||
+                (reinterpret_cast<uintptr_t>(scale) & 3u) ||
+                (!scale && (!amax_ws || (reinterpret_cast<uintptr_t>(amax_ws) & 3u)))))
+    return GBMOE_INVALID_ARG;
+  int sms;
+  gbmoe_status_t st = device_info(&sms);
+  if (st != GBMOE_OK || M == 0) return st;
+  return from_cuda(launch_quant_tensor_scatter(x, row_weights, M, K, inv, topk, A, A_scales,
+                                               amax_ws, scale, sms, (cudaStream_t)stream));
+}
+
 gbmoe_status_t moe_quant_fp8_tensor(const uint16_t *x, const float *row_weights,
                                     int M, int K, const int32_t *n_rows,
                                     uint8_t *q, float *row_scales,
@@ -798,8 +813,6 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
   // apply_router_weight_on_input (top-1): the weight scales the activations
   // (before the FP8 codes are chosen) and not the expert output
   const float *in_w = apply_router_weight_on_input ? wts : nullptr;
-  const void *a_src = x;
-  const float *a_src_s = nullptr;
   if (fp8 && !fp8t && !fp8ch) {
     // 1 x 128 groups: the codes and scales go straight to the permuted rows
     ce = launch_quant_group_scatter(x, in_w, M, K, w.inv, topk, static_cast<uint8_t *>(w.A),
@@ -811,17 +824,15 @@ gbmoe_status_t moe_forward(const uint16_t *x, const float *logits,
     ce = launch_quant_row_scatter(x, in_w, M, K, w.inv, topk, static_cast<uint8_t *>(w.A), w.As,
                                   sms, s);
     if (ce != cudaSuccess) return from_cuda(ce);
-  } else {
-    if (fp8) {
-      ce = fp8t ? launch_quant_tensor(x, in_w, M, K, nullptr, w.xq, w.xs, w.amax, a1_scale, sms,
-                                      s)
-                : launch_quant_row(x, in_w, M, K, w.xq, w.xs, sms, s);
-      if (ce != cudaSuccess) return from_cuda(ce);
-      a_src = w.xq;
-      a_src_s = w.xs;
-    }
-    st = permute_impl(a_src, a_src_s, fp8 ? nullptr : in_w, w.sorted, w.offsets, M, topk, E, K,
-                      dtype, w.A, w.As, sms, s);
+  } else if (fp8t) {
+    // one scale for the tensor (its maximum, or a1_scale): the codes pass
+    // writes the permuted rows
+    ce = launch_quant_tensor_scatter(x, in_w, M, K, w.inv, topk, static_cast<uint8_t *>(w.A),
+                                     w.As, w.amax, a1_scale, sms, s);
+    if (ce != cudaSuccess) return from_cuda(ce);
+  } else {  // bf16: the rows gathered (times the weight on input)
+    st = permute_impl(x, nullptr, in_w, w.sorted, w.offsets, M, topk, E, K, dtype, w.A, w.As,
+                      sms, s);
     if (st != GBMOE_OK) return st;
   }
   // per-token (per-tensor) scales span a whole row (all computed rows) of

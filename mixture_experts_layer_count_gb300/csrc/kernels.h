@@ -85,6 +85,12 @@ cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, in
                                 const int32_t *n_rows, uint8_t *q, float *row_scales,
                                 uint32_t *amax, const float *static_scale, int num_sms,
                                 cudaStream_t s);
+// launch_quant_tensor over all M rows of x with row t's codes and scale
+// written to the permuted rows A / As [inv[t*topk + j]] (skipped when negative)
+cudaError_t launch_quant_tensor_scatter(const uint16_t *x, const float *row_w, int M, int K,
+                                        const int32_t *inv, int topk, uint8_t *A, float *As,
+                                        uint32_t *amax, const float *static_scale, int num_sms,
+                                        cudaStream_t s);
 cudaError_t launch_quant_block(const uint16_t *w, int64_t R, int C, uint8_t *q,
                                float *scales, cudaStream_t s);
 

@@ -281,26 +281,42 @@ __global__ void __launch_bounds__(256)
 }
 
 // the codes with the tensor's scale -- from its maximum, or the caller's
-// static scale when given; row_scales[t] = s for every row t < n
+// static scale when given; row_scales[t] = s for every row t < n.
+// SCATTER: row t's codes and scale go to the permuted rows of its pairs
+// instead, q / row_scales [inv[t * topk + j]] (skipped when negative).
+template <bool SCATTER>
 __global__ void __launch_bounds__(256)
     quant_tensor_kernel(const uint4 *__restrict__ x, const float *__restrict__ row_w, int M,
                         int K, const int32_t *__restrict__ n_rows,
                         const unsigned int *__restrict__ amax,
                         const float *__restrict__ static_scale, uint2 *__restrict__ q,
-                        float *__restrict__ row_scales) {
+                        float *__restrict__ row_scales, const int32_t *__restrict__ inv,
+                        int topk) {
   const int vecs = K / 8;
   const size_t total = (size_t)tensor_rows(n_rows, M) * vecs;
   const float s = static_scale ? *static_scale : group_scale(__uint_as_float(*amax));
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = i / vecs;
     float v[8];
-    unpack8(x[i], row_w, i / vecs, v);
+    unpack8(x[i], row_w, t, v);
     uint32_t c[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) c[j] = e4m3_of(__fdiv_rn(v[j], s));
-    q[i] = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
-                      c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
-    if (i % vecs == 0) row_scales[i / vecs] = s;
+    const uint2 code = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                                  c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+    if (SCATTER) {
+      const size_t vi = i - t * vecs;
+      for (int j = 0; j < topk; ++j) {
+        const int dst = __ldg(inv + t * topk + j);
+        if (dst < 0) continue;
+        q[(size_t)dst * vecs + vi] = code;
+        if (vi == 0) row_scales[dst] = s;
+      }
+    } else {
+      q[i] = code;
+      if (i % vecs == 0) row_scales[t] = s;
+    }
   }
 }
 
@@ -424,9 +440,33 @@ cudaError_t launch_quant_tensor(const uint16_t *x, const float *row_w, int M, in
     st = cudaGetLastError();
     if (st != cudaSuccess) return st;
   }
-  quant_tensor_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x), row_w,
-                                                      M, K, n_rows, amax, static_scale,
-                                                      reinterpret_cast<uint2 *>(q), row_scales);
+  quant_tensor_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), row_w, M, K, n_rows, amax, static_scale,
+      reinterpret_cast<uint2 *>(q), row_scales, nullptr, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tensor_scatter(const uint16_t *x, const float *row_w, int M, int K,
+                                        const int32_t *inv, int topk, uint8_t *A, float *As,
+                                        uint32_t *amax, const float *static_scale, int num_sms,
+                                        cudaStream_t s) {
+  const size_t vecs = (size_t)M * (K / 8);
+  size_t blocks = (vecs + 255) / 256;
+  const size_t cap = (size_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  cudaError_t st;
+  if (!static_scale) {
+    st = cudaMemsetAsync(amax, 0, sizeof(uint32_t), s);
+    if (st != cudaSuccess) return st;
+    quant_tensor_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+        reinterpret_cast<const uint4 *>(x), row_w, M, K, nullptr, amax);
+    st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+  }
+  quant_tensor_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), row_w, M, K, nullptr, amax, static_scale,
+      reinterpret_cast<uint2 *>(A), As, inv, topk);
   return cudaGetLastError();
 }
 

@@ -172,11 +172,12 @@ def check_ids(gpu_ids, ref_ids, margin, what="", cfg=None, logits=None, bias=Non
     return diff
 
 
-def run_stages(cfg, d, gw, ids, wts):
+def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None):
     """The Standard layer as its separate calls, on the given routing (ids
     (M, topk) int32 and weights (M, topk) fp32 on the device): align, [FP8
     quantise], gather, gate/up GEMM, [quantise H], down GEMM into the
-    (M, topk, K) slots, and the ordered reduce.  Returns the device tensors
+    (M, topk, K) slots, and the ordered reduce (per-tensor e4m3: static
+    scales a1_scale / a2_scale when given).  Returns the device tensors
     counts, offsets, sorted, inv, y_slot, out and err."""
     g = gbmoe()
     dev = d["x"].device
@@ -191,14 +192,20 @@ def run_stages(cfg, d, gw, ids, wts):
     g.moe_align_permute(ids, E, counts, offsets, srt, inv,
                         g.workspace(g.WS_ALIGN, M, E, 0, 0, k, 0, device=dev), err)
     fp8 = cfg.dtype != WL.BF16
-    ch = cfg.dtype == WL.FP8_CHANNEL
-    assert cfg.dtype != WL.FP8_TENSOR, "per-tensor scales: use moe_forward"
+    tensor = cfg.dtype == WL.FP8_TENSOR
+    ch = cfg.dtype == WL.FP8_CHANNEL or tensor   # one scale per row of A and of H
+    amax = torch.empty(2, dtype=i32, device=dev)
     ld = (P + 3) // 4 * 4  # group-major FP8 row scales
     if fp8:
         sk = 1 if ch else K // 128
         xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
         xs = torch.empty((M, sk), dtype=f32, device=dev)
-        g.moe_quant_fp8_group(d["x"], xq, xs, group=K if ch else 128)
+        if tensor and a1_scale is not None:
+            g.moe_quant_fp8_tensor_static(d["x"], a1_scale, xq, xs.view(-1))
+        elif tensor:
+            g.moe_quant_fp8_tensor(d["x"], xq, xs.view(-1), amax[0:1])
+        else:
+            g.moe_quant_fp8_group(d["x"], xq, xs, group=K if ch else 128)
         A = torch.empty((P, K), dtype=torch.uint8, device=dev)
         As = torch.empty((sk, ld), dtype=f32, device=dev)
         g.moe_permute_rows(xq, xs, srt, offsets, k, E, cfg.dtype, A, As)
@@ -212,7 +219,12 @@ def run_stages(cfg, d, gw, ids, wts):
                                         cfg.dtype, Hb, None, err)
         H = torch.empty((P, N), dtype=torch.uint8, device=dev)
         Hs = torch.empty((P, 1), dtype=f32, device=dev)
-        g.moe_quant_fp8_group(Hb, H, Hs, group=N)
+        if tensor and a2_scale is not None:  # rows of pairs computed here: offsets[E]
+            g.moe_quant_fp8_tensor_static(Hb, a2_scale, H, Hs.view(-1), n_rows=offsets[E:])
+        elif tensor:
+            g.moe_quant_fp8_tensor(Hb, H, Hs.view(-1), amax[1:2], n_rows=offsets[E:])
+        else:
+            g.moe_quant_fp8_group(Hb, H, Hs, group=N)
         del Hb
     elif fp8:
         H = torch.empty((P, N), dtype=torch.uint8, device=dev)

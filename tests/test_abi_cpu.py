@@ -202,6 +202,12 @@ def test_gemm_calls_reject_bad_arguments(lib):
     assert rp(P16, None, 16, 256, P16, 33, P16, P16, None) == INVALID  # topk > 32
     assert rp(P16, None, 16, 256, None, 4, P16, P16, None) == INVALID  # no inverse map
     assert rp(P_ODD, None, 16, 256, P16, 4, P16, P16, None) == INVALID
+    tp = lib.moe_quant_fp8_tensor_permute
+    #         x    rw    M   K    inv  k  scale q    As   amax  s
+    assert tp(P16, None, 16, 256, P16, 4, None, P16, P16, None, None) == INVALID      # no scale, no amax
+    assert tp(P16, None, 16, 256, P16, 4, P16 + 2, P16, P16, None, None) == INVALID   # misaligned scale
+    assert tp(P16, P16, 16, 256, P16, 2, P16, P16, P16, None, None) == INVALID        # row weights need top-1
+    assert tp(P16, None, 16, 200, P16, 4, P16, P16, P16, None, None) == INVALID       # K % 128
     b = lib.moe_batched_masked_experts
     #        xb  xbs   cnt E  T   N    K    w1   w1s  w2   w2s  dt ac yb   ws   wsb  err  s
     assert b(P16, None, P16, 4, 16, 128, 256, P16, None, P16, None, 2, 0, P16, P16, 1 << 30, None, None) == UNSUPPORTED

@@ -151,10 +151,12 @@ def test_quant_fp8_group_bit_exact():
 
 
 @pytest.mark.parametrize("case", ["all_local", "expert_map", "weight_on_input"])
-@pytest.mark.parametrize("per_row", [False, True], ids=["groups_of_128", "one_scale_per_row"])
-def test_quant_fp8_group_permute_bit_exact(case, per_row):
-    """Quantisation and permutation in one pass (1 x 128 groups, or one scale
-    per row): codes and group-major scales
+@pytest.mark.parametrize("mode", ["groups_of_128", "one_scale_per_row", "tensor_dynamic",
+                                  "tensor_static"])
+def test_quant_fp8_group_permute_bit_exact(case, mode):
+    """Quantisation and permutation in one pass (1 x 128 groups, one scale per
+    row, or one scale for the tensor, from its maximum or given): codes and
+    group-major scales
     of every permuted row bit-exact against the oracle's group quantiser and
     stable sort (A[i] = codes of token sorted[i] / topk), pairs not routed to
     a local expert skipped, rows at and beyond the local total untouched;
@@ -183,14 +185,24 @@ def test_quant_fp8_group_permute_bit_exact(case, per_row):
                         E_global=E if emap is not None else None)
     ld = (P + 3) // 4 * 4
     A = torch.full((P, K), 0xA5, dtype=torch.uint8, device=DEV)
-    As = torch.full((1 if per_row else K // 128, ld), -7.0, dtype=torch.float32, device=DEV)
-    if per_row:  # moe_quant_fp8_row_permute: one scale per token (A_scales[row])
-        g.moe_quant_fp8_row_permute(x, inv, topk, A, As.view(-1), row_weights=rw)
-    else:
+    grouped = mode == "groups_of_128"
+    As = torch.full((K // 128 if grouped else 1, ld), -7.0, dtype=torch.float32, device=DEV)
+    rwn = None if rw is None else rw.cpu().numpy()
+    if grouped:
         g.moe_quant_fp8_group_permute(x, inv, topk, A, As, row_weights=rw)
+        rq, rs = orc.quant_fp8_group(WL.bf16_bits(x), group=128, row_weights=rwn)
+    elif mode == "one_scale_per_row":  # moe_quant_fp8_row_permute: A_scales[row]
+        g.moe_quant_fp8_row_permute(x, inv, topk, A, As.view(-1), row_weights=rw)
+        rq, rs = orc.quant_fp8_group(WL.bf16_bits(x), group=K, row_weights=rwn)
+    else:  # moe_quant_fp8_tensor_permute: one scale, repeated on every row
+        s_static = np.float32(0.02) if mode == "tensor_static" else None
+        amax = torch.empty(1, dtype=torch.int32, device=DEV)
+        g.moe_quant_fp8_tensor_permute(
+            x, inv, topk, A, As.view(-1), amax_ws=amax, row_weights=rw,
+            scale=None if s_static is None else torch.tensor([s_static], device=DEV))
+        rq, s1 = orc.quant_fp8_tensor(WL.bf16_bits(x), row_weights=rwn, scale=s_static)
+        rs = np.full((M, 1), s1, np.float32)
     torch.cuda.synchronize()
-    rq, rs = orc.quant_fp8_group(WL.bf16_bits(x), group=K if per_row else 128,
-                                 row_weights=None if rw is None else rw.cpu().numpy())
     ro, rsrt, rinv = orc.align(ids.cpu().numpy(), E,
                                expert_map=None if emap is None else emap.cpu().numpy(),
                                E_local=E_loc)
@@ -451,6 +463,30 @@ def test_forward_parity_small(cfg):
     assert np.array_equal(ids.cpu().numpy(), rid)
     np.testing.assert_allclose(wts.cpu().numpy(), rw, atol=2e-6, rtol=0)
     assert_close_rel(out.float().cpu().numpy(), ref, TOL[cfg.dtype], cfg.name)
+
+
+@pytest.mark.parametrize("cfg", [WL.SMALL_FP8T, WL.SMALL_FP8CH, WL.SMALL_FP8],
+                         ids=lambda c: c.name)
+@pytest.mark.parametrize("static", [False, True], ids=["dynamic", "static_scales"])
+def test_forward_equals_its_separate_calls(cfg, static):
+    """The one-call layer (which quantises and permutes x in one pass) equals
+    the same layer run as its separate calls (quantise, then gather) bit for
+    bit, on every token; per-tensor e4m3 with dynamic and with static
+    activation scales."""
+    if static and cfg.dtype != WL.FP8_TENSOR:
+        pytest.skip("static activation scales are a per-tensor e4m3 option")
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    kw = {}
+    if static:
+        a1 = np.float32(d["x"].float().abs().max().item()) / np.float32(448) * np.float32(0.5)
+        kw = dict(a1_scale=torch.tensor([a1], dtype=torch.float32, device=DEV),
+                  a2_scale=torch.tensor([0.01], dtype=torch.float32, device=DEV))
+    out, ids, wts, err = run_forward(cfg, d, gw, **kw)
+    st = run_stages(cfg, d, gw, ids, wts, **kw)
+    torch.cuda.synchronize()
+    assert err.item() == 0 and st["err"].item() == 0
+    assert torch.equal(out.view(torch.int16), st["out"].view(torch.int16))
 
 
 def test_forward_is_deterministic():
