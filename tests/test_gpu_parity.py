@@ -465,16 +465,15 @@ def test_forward_parity_small(cfg):
     assert_close_rel(out.float().cpu().numpy(), ref, TOL[cfg.dtype], cfg.name)
 
 
-@pytest.mark.parametrize("cfg", [WL.SMALL_FP8T, WL.SMALL_FP8CH, WL.SMALL_FP8],
-                         ids=lambda c: c.name)
-@pytest.mark.parametrize("static", [False, True], ids=["dynamic", "static_scales"])
+@pytest.mark.parametrize("cfg,static", [(WL.SMALL_FP8T, False), (WL.SMALL_FP8T, True),
+                                        (WL.SMALL_FP8CH, False), (WL.SMALL_FP8, False)],
+                         ids=["fp8_tensor_dynamic", "fp8_tensor_static", "fp8_channel",
+                              "fp8_block"])
 def test_forward_equals_its_separate_calls(cfg, static):
     """The one-call layer (which quantises and permutes x in one pass) equals
     the same layer run as its separate calls (quantise, then gather) bit for
     bit, on every token; per-tensor e4m3 with dynamic and with static
     activation scales."""
-    if static and cfg.dtype != WL.FP8_TENSOR:
-        pytest.skip("static activation scales are a per-tensor e4m3 option")
     d = WL.make_inputs(cfg, DEV)
     gw = GpuWeights(cfg, d["w1"], d["w2"])
     kw = {}
