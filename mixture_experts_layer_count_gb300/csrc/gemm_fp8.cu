@@ -11,9 +11,9 @@
 // while the tensor core fills the other buffer.  Each epilogue thread owns one
 // row and 128 columns (4 lane quarters x 2 column halves cover the 128 x 256
 // tile: for gate/up the gate and up columns of 64 outputs), so the promotion
-// is 64 packed FFMA2 per thread per K block, in 16-column TMEM loads; at 320
-// threads (352 in down mode, with the store warp below) a thread has 168
-// registers, enough for its 128 accumulators.  The
+// is 64 packed FFMA2 per thread per K block, in 16-column TMEM loads; at 352
+// threads (with the output warp below) a thread has 168 registers, enough
+// for its 128 accumulators.  The
 // per-row scales of a K block travel with the operand tiles: the producer
 // loads them by TMA from the group-major scale array (one contiguous run of
 // rows per K block) into the stage's shared memory; the weight-block scales
