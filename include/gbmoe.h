@@ -54,6 +54,7 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st *gbmoe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+typedef struct CUevent_st *gbmoe_event_t;   /* a cudaEvent_t */
 
 typedef enum {
     GBMOE_OK = 0,
@@ -544,8 +545,8 @@ gbmoe_status_t moe_forward_shared(const uint16_t *x, const float *logits,
                                   size_t ws_shared_bytes, int32_t *err_word,
                                   gbmoe_stream_t stream,
                                   gbmoe_stream_t aux_stream,
-                                  struct CUevent_st *ev_input_ready,
-                                  struct CUevent_st *ev_output_ready);
+                                  gbmoe_event_t ev_input_ready,
+                                  gbmoe_event_t ev_output_ready);
 
 /* Expert-parallel dispatch in the worst-tokens mode of "EP: CUDA-graph-safe
  * HT internode dispatch+combine (worst-tokens mode)" (uccl pull request 7 and
