@@ -18,6 +18,19 @@ def _declared():
     return {n for n in names if n.startswith(("moe_", "gbmoe_"))}
 
 
+def test_header_is_plain_c():
+    """include/gbmoe.h is a C header: it compiles warning-free as C (and C++)."""
+    import shutil
+    import subprocess
+    hdr = os.path.join(ROOT, "include", "gbmoe.h")
+    for cc, lang in (("gcc", "c"), ("g++", "c++")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not found")
+        r = subprocess.run([cc, "-fsyntax-only", "-Wall", "-Wextra", "-Werror", "-x", lang, hdr],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol():
     import mixture_experts_layer_count_gb300 as g
     lib = g.load()
