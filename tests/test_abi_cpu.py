@@ -31,6 +31,17 @@ def test_header_is_plain_c():
         assert r.returncode == 0, r.stderr
 
 
+def test_c_caller_builds(tmp_path):
+    """A C program that uses the library through include/gbmoe.h alone
+    compiles warning-free and links against libgbmoe.so and the CUDA runtime."""
+    import c_example
+    try:
+        exe = c_example.build(str(tmp_path))
+    except FileNotFoundError as e:
+        pytest.skip(str(e))
+    assert os.access(exe, os.X_OK)
+
+
 def test_library_exports_every_declared_symbol():
     import mixture_experts_layer_count_gb300 as g
     lib = g.load()
