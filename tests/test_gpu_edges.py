@@ -2,7 +2,8 @@
 largest expert count (512) with grouped sigmoid routing, the largest top-k
 (32), every expert picked by every token (topk = E), a single expert, the
 largest K and N of the block-scaled e4m3 GEMMs (16384: 128 scale blocks,
-the whole per-tile scale table), and a single token in every dtype."""
+the whole per-tile scale table), a single token in every dtype, and empty
+inputs (no token, or no valid row) in every dtype."""
 import numpy as np
 import pytest
 import torch
@@ -91,3 +92,63 @@ def test_fp8_block_k_and_n_above_the_limit_are_rejected():
     assert ei.value.status == 1  # GBMOE_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(out == 3.0)
+
+
+@pytest.mark.parametrize("chunked", [False, True], ids=["one_call", "chunked"])
+@pytest.mark.parametrize("dtype,static", [(WL.FP8, False), (WL.FP8_CHANNEL, False),
+                                          (WL.FP8_TENSOR, False), (WL.FP8_TENSOR, True)],
+                         ids=["fp8_block", "fp8_channel", "fp8_tensor", "fp8_tensor_static"])
+def test_empty_input_is_a_no_op_in_every_dtype(dtype, static, chunked):
+    """M = 0 in every e4m3 mode (the bf16 case is in the parity tests):
+    GBMOE_OK, no error bit, and nothing written."""
+    cfg = WL.MoEConfig("edge_M0", M=0, K=256, N=256, E=8, topk=2, dtype=dtype, seed=62)
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    g = gbmoe()
+    out = torch.full((1, cfg.K), 3.0, dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = g.workspace(g.WS_FORWARD, 0, cfg.E, cfg.N, cfg.K, cfg.topk, dtype, device=DEV)
+    kw = {}
+    if static:
+        kw = dict(a1_scale=torch.full((1,), 0.01, device=DEV),
+                  a2_scale=torch.full((1,), 0.01, device=DEV))
+    args = (d["x"], d["logits"], None, cfg.N, cfg.E, cfg.topk, cfg.score_fn, 1, 1, True,
+            dtype, gw.w1, gw.w1s, gw.w2, gw.w2s, out, ws)
+    if chunked:
+        g.moe_forward_chunked(*args, 64, err_word=err, **kw)
+    else:
+        g.moe_forward(*args, err_word=err, **kw)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.all(out == 3.0)
+
+
+@pytest.mark.parametrize("dtype", [WL.BF16, WL.FP8], ids=["bf16", "fp8_block"])
+def test_batched_with_every_count_zero_writes_nothing(dtype):
+    """Every expert's device count is 0: no row is computed, no row of the
+    output is written, no error bit is set."""
+    E, T, K, N = 4, 96, 256, 256
+    g = gbmoe()
+    gen = torch.Generator(device=DEV).manual_seed(63)
+    xb = torch.randn((E, T, K), generator=gen, device=DEV).to(torch.bfloat16)
+    w1 = (torch.randn((E, 2 * N, K), generator=gen, device=DEV) / 16).to(torch.bfloat16)
+    w2 = (torch.randn((E, K, N), generator=gen, device=DEV) / 16).to(torch.bfloat16)
+    counts = torch.zeros(E, dtype=torch.int32, device=DEV)
+    yb = torch.empty((E, T, K), dtype=torch.bfloat16, device=DEV)
+    yb.view(torch.int16).fill_(0x7E7E)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = g.workspace(g.WS_BATCHED, T, E, N, K, 1, dtype, device=DEV)
+    if dtype == WL.BF16:
+        g.moe_batched_masked_experts(xb, counts, N, w1, w2, yb, ws, err_word=err)
+    else:
+        cfg = WL.MoEConfig("edge_batched_zero", M=T, K=K, N=N, E=E, topk=1, dtype=WL.FP8)
+        gw = GpuWeights(cfg, w1, w2)
+        q = torch.empty((E, T, K), dtype=torch.uint8, device=DEV)
+        sc = torch.empty((E * T, K // 128), dtype=torch.float32, device=DEV)
+        g.moe_quant_fp8_group(xb.reshape(E * T, K), q.view(E * T, K), sc)
+        g.moe_batched_masked_experts(q, counts, N, gw.w1, gw.w2, yb, ws, dtype=WL.FP8,
+                                     x_b_scales=sc, w1_scales=gw.w1s, w2_scales=gw.w2s,
+                                     err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.all(yb.view(torch.int16) == 0x7E7E)
