@@ -26,7 +26,11 @@ def _lib():
 # ------------------------------------------------------------------ router --
 
 ROUTE_CFGS = [WL.TINY, WL.SMALL_BF16, WL.SMALL_SIGMOID, WL.MIXTRAL_PREFILL,
-              WL.DSV3_PREFILL_FP8, WL.DSV3_DECODE]
+              WL.DSV3_PREFILL_FP8, WL.DSV3_DECODE,
+              # 262144 tokens: 32768 blocks of the route kernel, 2 M (token, slot) pairs
+              WL.MoEConfig("route_M262144_E256_top8_grouped", M=1 << 18, K=128, N=128, E=256,
+                           topk=8, score_fn=WL.SIGMOID, n_groups=8, topk_groups=4,
+                           zipf_bias=True, seed=64)]
 
 
 @pytest.mark.parametrize("cfg", ROUTE_CFGS, ids=lambda c: c.name)
@@ -85,8 +89,12 @@ def test_route_grouped_exact_key_ties():
 # -------------------------------------------------------- count / permute --
 
 @pytest.mark.parametrize("E,M,k,skew", [(8, 64, 2, 0.0), (256, 8192, 8, 1.1),
-                                        (32, 1, 1, 0.0), (512, 3001, 5, 2.0)])
+                                        (32, 1, 1, 0.0), (512, 3001, 5, 2.0),
+                                        (256, 1 << 20, 8, 1.1), (512, 99999, 32, 0.5)])
 def test_count_and_align_bit_exact(E, M, k, skew):
+    """Counts, offsets, sorted pair ids and inv bit-exact against the oracle's
+    stable counting sort, up to 8.4 M pairs (4096 sort chunks) and top-32 of
+    512 experts."""
     g = gbmoe()
     rng = np.random.default_rng(E * 7 + M)
     p = np.arange(1, E + 1, dtype=np.float64) ** -skew
