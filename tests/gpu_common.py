@@ -172,13 +172,17 @@ def check_ids(gpu_ids, ref_ids, margin, what="", cfg=None, logits=None, bias=Non
     return diff
 
 
-def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None):
+def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None, keep_hidden=False):
     """The Standard layer as its separate calls, on the given routing (ids
     (M, topk) int32 and weights (M, topk) fp32 on the device): align, [FP8
     quantise], gather, gate/up GEMM, [quantise H], down GEMM into the
     (M, topk, K) slots, and the ordered reduce (per-tensor e4m3: static
     scales a1_scale / a2_scale when given).  Returns the device tensors
-    counts, offsets, sorted, inv, y_slot, out and err."""
+    counts, offsets, sorted, inv, y_slot, out, err and amax (the per-tensor
+    maxima of x and H as float bits, dynamic per-tensor e4m3 only); with
+    keep_hidden (per-token and per-tensor e4m3) also xq / xs (x's codes and
+    row scales), Hb (the bf16 hidden rows) and H / Hs (their codes and row
+    scales)."""
     g = gbmoe()
     dev = d["x"].device
     M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
@@ -225,7 +229,8 @@ def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None):
             g.moe_quant_fp8_tensor(Hb, H, Hs.view(-1), amax[1:2], n_rows=offsets[E:])
         else:
             g.moe_quant_fp8_group(Hb, H, Hs, group=N)
-        del Hb
+        if not keep_hidden:
+            del Hb
     elif fp8:
         H = torch.empty((P, N), dtype=torch.uint8, device=dev)
         Hs = torch.empty((N // 128, ld), dtype=f32, device=dev)
@@ -242,8 +247,11 @@ def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None):
                             cfg.dtype, y, err)
     out = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
     g.moe_unpermute_weighted_reduce(y, inv, M, k, K, out)
-    return {"counts": counts, "offsets": offsets, "sorted": srt, "inv": inv,
-            "y_slot": y, "out": out, "err": err}
+    res = {"counts": counts, "offsets": offsets, "sorted": srt, "inv": inv,
+           "y_slot": y, "out": out, "err": err, "amax": amax}
+    if keep_hidden and ch:
+        res.update(xq=xq, xs=xs, Hb=Hb, H=H, Hs=Hs)
+    return res
 
 
 def oracle_pair_rows(cfg, d, w1, w2, rid, pairs):

@@ -661,3 +661,52 @@ def test_forward_parity_fp8_tensor_static_full_size_sampled():
     assert np.array_equal(rid_s, rid[tokens])
     assert_close_rel(out[torch.from_numpy(tokens).to(DEV)].float().cpu().numpy(), ref,
                      TOL[cfg.dtype], cfg.name + " static scales")
+
+
+def test_forward_parity_fp8_tensor_dynamic_full_size():
+    """The DeepSeek-V3-shaped prefill with per-tensor e4m3 activations and
+    dynamic scales, at full size.  The scale of H spans all 65536 hidden rows,
+    more than the oracle computes here, so the check is a chain:
+    - x's scale and codes equal the oracle's quantiser, bit for bit;
+    - H's scale is the maximum magnitude of the hidden rows the gate/up GEMM
+      wrote (over the computed rows only) / 448, and H's codes are torch's
+      saturating e4m3 cast of those rows divided by it;
+    - the one-call layer equals its separate calls, and equals the layer run
+      with those two scales given as static scales, bit for bit (the static
+      path at full size is checked against the oracle in the test above)."""
+    cfg = WL.DSV3_PREFILL_FP8T
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    out, ids, wts, err = run_forward(cfg, d, gw)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    st = run_stages(cfg, d, gw, ids, wts, keep_hidden=True)
+    torch.cuda.synchronize()
+    assert st["err"].item() == 0
+    assert torch.equal(st["out"].view(torch.int16), out.view(torch.int16))
+    # x: the oracle's per-tensor quantiser
+    q_ref, s_ref = orc.quant_fp8_tensor(WL.bf16_bits(d["x"]))
+    xs = st["xs"].view(-1)
+    assert torch.all(xs == xs[0])
+    assert np.float32(xs[0].item()) == s_ref
+    assert np.array_equal(st["xq"].cpu().numpy(), q_ref)
+    # H: the maximum of the computed rows, then the saturating cast
+    P = int(st["offsets"][cfg.E].item())
+    assert P == cfg.M * cfg.topk
+    hb = st["Hb"][:P].float().cpu().numpy()  # bf16 values, exact in fp32
+    hmax = np.float32(np.abs(hb).max())
+    assert np.float32(st["amax"][1:2].view(torch.float32).item()) == hmax
+    hs = st["Hs"].view(-1)[:P]
+    assert torch.all(hs == hs[0])
+    s_h = np.float32(hs[0].item())
+    assert s_h == hmax / np.float32(448)  # IEEE fp32 division
+    q = np.clip(hb / s_h, np.float32(-448), np.float32(448))
+    codes = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(st["H"][:P].cpu().numpy(), codes)
+    del hb, q, codes
+    # the dynamic layer is the static layer with its own scales
+    out_s, _, _, err_s = run_forward(cfg, d, gw, a1_scale=xs[:1].clone(),
+                                     a2_scale=hs[:1].clone())
+    torch.cuda.synchronize()
+    assert err_s.item() == 0
+    assert torch.equal(out_s.view(torch.int16), out.view(torch.int16))
