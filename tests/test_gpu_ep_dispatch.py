@@ -13,7 +13,7 @@ import torch
 
 import oracle as orc
 import workloads as WL
-from gpu_common import TOL, assert_close_rel, gbmoe, oracle_weights
+from gpu_common import TOL, assert_close_rel, check_ids, gbmoe, oracle_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -253,3 +253,84 @@ def test_ep_dispatch_flags_overflow_of_the_static_shape():
         assert torch.equal(recv_x[e].view(torch.int16), xv[:worst].view(torch.int16))
     assert torch.all(recv_x[4:].view(torch.int16) == SENTINEL)      # experts with no rows
     assert torch.all(flat[E * worst * K:].view(torch.int16) == SENTINEL)  # past the shape
+
+
+def test_ep_worst_tokens_fp8_full_size():
+    """The sharded e4m3 layer at the size the bench times: 8 shards of up to
+    256 tokens, K = 7168, N = 2048, 256 experts, grouped sigmoid top-8.
+    Captured and replayed once, the replay equals the eager run bit for bit.
+    Against the oracle: the router ids of every valid token (near-ties
+    validated); the per-expert counts and every valid pair's receive position,
+    bit-exact against the oracle's stable counting sort of those ids; the
+    tokens' 1 x 128 codes and scales, bit-exact, which every receive row
+    holds byte for byte; the outputs of 16 sampled valid tokens against the
+    oracle's e4m3 layer (h requantised).  Padded tokens' pairs are not
+    dispatched and their output rows are not written."""
+    cfg = WL.EP8_DSV3
+    G, M, K, N, E, k = cfg.G, cfg.M, cfg.K, cfg.N, cfg.E, cfg.topk
+    Wt = cfg.worst_tokens
+    d = WL.make_ep_inputs(cfg, DEV)
+    layer = EpLayer(cfg, d["w1"], d["w2"], WL.FP8)
+    layer.load(d)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.step()
+    layer.load(d)
+    graph.replay()
+    eager = EpLayer(cfg, d["w1"], d["w2"], WL.FP8)
+    eager.load(d)
+    eager.step()
+    torch.cuda.synchronize()
+    assert layer.err.item() == 0 and eager.err.item() == 0
+    for name in ("out", "recv_counts", "recv_pos", "ids"):
+        a, b = getattr(layer, name), getattr(eager, name)
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), f"{name} differs from the eager run"
+    del eager
+    n = d["num_tokens"].cpu().numpy()
+    xv = torch.cat([d["x"][r, :n[r]] for r in range(G)])
+    lv = torch.cat([d["logits"][r, :n[r]] for r in range(G)]).cpu().numpy()
+    rid, _, margin = orc.route(lv, None, k, cfg.score_fn, cfg.n_groups, cfg.topk_groups, True)
+    gids = layer.ids.cpu().numpy()
+    got_ids = np.concatenate([gids[r, :n[r]] for r in range(G)])
+    diff = check_ids(got_ids, rid, margin, cfg.name, cfg, lv, None)
+    # the dispatch of the GPU's (validated) routing
+    rc, bad = orc.count(got_ids, E)
+    ro, _, ri = orc.align(got_ids, E)
+    assert bad == 0
+    assert np.array_equal(layer.recv_counts.cpu().numpy(), rc)
+    gpos = layer.recv_pos.cpu().numpy()
+    got_pos = np.concatenate([gpos[r, :n[r]].ravel() for r in range(G)])
+    assert np.array_equal(got_pos, ri - ro[got_ids.ravel()])
+    for r in range(G):
+        assert np.all(gpos[r, n[r]:] == -1)
+    q_ref, s_ref = orc.quant_fp8_group(WL.bf16_bits(xv))
+    xq = torch.cat([layer.xq[r, :n[r]] for r in range(G)]).cpu().numpy()
+    xs = torch.cat([layer.xs[r * M:r * M + n[r]] for r in range(G)]).cpu().numpy()
+    assert np.array_equal(xq, q_ref)
+    assert np.array_equal(xs.view(np.uint32), s_ref.view(np.uint32))
+    pos, ids = layer.recv_pos, layer.ids
+    sh, tk, _ = torch.nonzero(pos >= 0, as_tuple=True)
+    pe, pp = ids[pos >= 0].long(), pos[pos >= 0].long()
+    assert torch.equal(layer.recv_x[pe, pp], layer.xq[sh, tk])
+    assert torch.equal(layer.recv_s[pe * Wt + pp], layer.xs[sh * M + tk])
+    # values of sampled valid tokens
+    rng = np.random.default_rng(6)
+    tokens = np.setdiff1d(np.sort(rng.choice(len(xv), 16, replace=False)), diff)
+    W = oracle_weights(WL.MoEConfig("ep8_fp8", M=1, K=K, N=N, E=E, topk=k, dtype=WL.FP8),
+                       d["w1"], d["w2"], np.unique(rid[tokens]))
+    ref, rid_s, _ = orc.moe_forward(WL.bf16_bits(xv), lv, None, k, cfg.score_fn, W,
+                                    cfg.n_groups, cfg.topk_groups, True, requant_h=True,
+                                    tokens=tokens)
+    assert np.array_equal(rid_s, rid[tokens])
+    got = torch.cat([layer.out[r, :n[r]] for r in range(G)])[torch.from_numpy(tokens).to(DEV)]
+    assert_close_rel(got.float().cpu().numpy(), ref, TOL[WL.FP8], cfg.name)
+    bits = layer.out.view(torch.int16).cpu().numpy()
+    for r in range(G):
+        assert np.all(bits[r, n[r]:] == np.int16(SENTINEL)), f"shard {r}: padded rows written"
