@@ -22,7 +22,9 @@ def _lib():
 
 @pytest.mark.parametrize("cfg,chunk", [(WL.SMALL_SIGMOID, 64), (WL.SMALL_FP8, 100),
                                        (WL.SMALL_BF16, 300), (WL.SMALL_FP8CH, 96),
-                                       (WL.SMALL_PAIR_TOP2, 200)],
+                                       (WL.SMALL_PAIR_TOP2, 200),
+                                       # the e4m3 prefill in the 2048-token chunks the bench times
+                                       (WL.DSV3_PREFILL_FP8, 2048)],
                          ids=lambda v: str(getattr(v, "name", v)))
 def test_chunked_equals_unchunked(cfg, chunk):
     g = gbmoe()
