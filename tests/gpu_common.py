@@ -85,18 +85,61 @@ def oracle_blocks(cfg, w1, w2, experts=None):
     return blocks
 
 
-def run_forward(cfg, d, gw, stream=None, a1_scale=None, a2_scale=None):
+GUARD = 4096  # bytes on each side; a multiple of 256 keeps the inner buffer's alignment
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """An allocator (shape, dtype) -> tensor whose buffers each sit between two
+    bands of GUARD sentinel bytes; check() asserts that no band changed."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.bufs = []
+
+    def __call__(self, shape, dtype):
+        shape = tuple(int(v) for v in shape)
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        raw = torch.full((GUARD + n + GUARD,), GUARD_BYTE, dtype=torch.uint8,
+                         device=self.device)
+        self.bufs.append((raw, n, f"{dtype} {shape}"))
+        return raw[GUARD:GUARD + n].view(dtype).view(shape)
+
+    def ws(self, which, *args):
+        n = gbmoe().moe_workspace_size(which, *args)
+        assert n > 0
+        return self((n,), torch.uint8)
+
+    def check(self, what):
+        if torch.device(self.device).type == "cuda":
+            torch.cuda.synchronize()
+        assert self.bufs
+        for raw, n, name in self.bufs:
+            head, tail = raw[:GUARD], raw[GUARD + n:]
+            bad_h = int((head != GUARD_BYTE).sum())
+            bad_t = int((tail != GUARD_BYTE).sum())
+            assert bad_h == 0 and bad_t == 0, \
+                f"{what}: {name}: {bad_h} bytes before and {bad_t} after the buffer overwritten"
+
+
+def _torch_alloc(dev):
+    return lambda shape, dtype: torch.empty(shape, dtype=dtype, device=dev)
+
+
+def run_forward(cfg, d, gw, stream=None, a1_scale=None, a2_scale=None, alloc=None):
     """The whole Standard layer on the GPU (per-tensor e4m3: static activation
     scales a1_scale / a2_scale, device fp32 scalars, when given); returns
-    out, ids, weights, err."""
+    out, ids, weights, err.  alloc(shape, dtype) makes the output buffers and
+    the workspace (default: torch.empty on x's device)."""
     g = gbmoe()
     dev = d["x"].device
+    alloc = alloc or _torch_alloc(dev)
     M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
-    out = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-    ids = torch.empty((M, k), dtype=torch.int32, device=dev)
-    wts = torch.empty((M, k), dtype=torch.float32, device=dev)
+    out = alloc((M, K), torch.bfloat16)
+    ids = alloc((M, k), torch.int32)
+    wts = alloc((M, k), torch.float32)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = g.workspace(g.WS_FORWARD, M, E, N, K, k, cfg.dtype, device=dev)
+    ws = alloc((g.moe_workspace_size(g.WS_FORWARD, M, E, N, K, k, cfg.dtype),), torch.uint8)
     g.moe_forward(d["x"], d["logits"], d["bias"], N, E, k, cfg.score_fn,
                   cfg.n_groups, cfg.topk_groups, cfg.renorm, cfg.dtype, gw.w1,
                   gw.w1s, gw.w2, gw.w2s, out, ws, topk_ids=ids, topk_weights=wts,
@@ -172,7 +215,8 @@ def check_ids(gpu_ids, ref_ids, margin, what="", cfg=None, logits=None, bias=Non
     return diff
 
 
-def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None, keep_hidden=False):
+def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None, keep_hidden=False,
+               alloc=None):
     """The Standard layer as its separate calls, on the given routing (ids
     (M, topk) int32 and weights (M, topk) fp32 on the device): align, [FP8
     quantise], gather, gate/up GEMM, [quantise H], down GEMM into the
@@ -182,47 +226,50 @@ def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None, keep_hidden=F
     maxima of x and H as float bits, dynamic per-tensor e4m3 only); with
     keep_hidden (per-token and per-tensor e4m3) also xq / xs (x's codes and
     row scales), Hb (the bf16 hidden rows) and H / Hs (their codes and row
-    scales)."""
+    scales).  alloc(shape, dtype) makes every buffer the calls write
+    (default: torch.empty on x's device)."""
     g = gbmoe()
     dev = d["x"].device
+    alloc = alloc or _torch_alloc(dev)
     M, E, N, K, k = cfg.M, cfg.E, cfg.N, cfg.K, cfg.topk
     P = M * k
     i32, f32 = torch.int32, torch.float32
-    counts = torch.full((E,), -7, dtype=i32, device=dev)
-    offsets = torch.empty(E + 1, dtype=i32, device=dev)
-    srt = torch.full((P,), -5, dtype=i32, device=dev)
-    inv = torch.empty(P, dtype=i32, device=dev)
+    counts = alloc((E,), i32).fill_(-7)
+    offsets = alloc((E + 1,), i32)
+    srt = alloc((P,), i32).fill_(-5)
+    inv = alloc((P,), i32)
     err = torch.zeros(1, dtype=i32, device=dev)
     g.moe_align_permute(ids, E, counts, offsets, srt, inv,
-                        g.workspace(g.WS_ALIGN, M, E, 0, 0, k, 0, device=dev), err)
+                        alloc((g.moe_workspace_size(g.WS_ALIGN, M, E, 0, 0, k, 0),), torch.uint8),
+                        err)
     fp8 = cfg.dtype != WL.BF16
     tensor = cfg.dtype == WL.FP8_TENSOR
     ch = cfg.dtype == WL.FP8_CHANNEL or tensor   # one scale per row of A and of H
-    amax = torch.empty(2, dtype=i32, device=dev)
+    amax = alloc((2,), i32)
     ld = (P + 3) // 4 * 4  # group-major FP8 row scales
     if fp8:
         sk = 1 if ch else K // 128
-        xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
-        xs = torch.empty((M, sk), dtype=f32, device=dev)
+        xq = alloc((M, K), torch.uint8)
+        xs = alloc((M, sk), f32)
         if tensor and a1_scale is not None:
             g.moe_quant_fp8_tensor_static(d["x"], a1_scale, xq, xs.view(-1))
         elif tensor:
             g.moe_quant_fp8_tensor(d["x"], xq, xs.view(-1), amax[0:1])
         else:
             g.moe_quant_fp8_group(d["x"], xq, xs, group=K if ch else 128)
-        A = torch.empty((P, K), dtype=torch.uint8, device=dev)
-        As = torch.empty((sk, ld), dtype=f32, device=dev)
+        A = alloc((P, K), torch.uint8)
+        As = alloc((sk, ld), f32)
         g.moe_permute_rows(xq, xs, srt, offsets, k, E, cfg.dtype, A, As)
     else:
-        A = torch.empty((P, K), dtype=torch.bfloat16, device=dev)
+        A = alloc((P, K), torch.bfloat16)
         As = None
         g.moe_permute_rows(d["x"], None, srt, offsets, k, E, cfg.dtype, A, None)
     if ch:
-        Hb = torch.empty((P, N), dtype=torch.bfloat16, device=dev)
+        Hb = alloc((P, N), torch.bfloat16)
         g.moe_grouped_gemm_gate_up_silu(A, As, offsets, M, k, E, N, K, gw.w1, gw.w1s,
                                         cfg.dtype, Hb, None, err)
-        H = torch.empty((P, N), dtype=torch.uint8, device=dev)
-        Hs = torch.empty((P, 1), dtype=f32, device=dev)
+        H = alloc((P, N), torch.uint8)
+        Hs = alloc((P, 1), f32)
         if tensor and a2_scale is not None:  # rows of pairs computed here: offsets[E]
             g.moe_quant_fp8_tensor_static(Hb, a2_scale, H, Hs.view(-1), n_rows=offsets[E:])
         elif tensor:
@@ -232,20 +279,20 @@ def run_stages(cfg, d, gw, ids, wts, a1_scale=None, a2_scale=None, keep_hidden=F
         if not keep_hidden:
             del Hb
     elif fp8:
-        H = torch.empty((P, N), dtype=torch.uint8, device=dev)
-        Hs = torch.empty((N // 128, ld), dtype=f32, device=dev)
+        H = alloc((P, N), torch.uint8)
+        Hs = alloc((N // 128, ld), f32)
         g.moe_grouped_gemm_gate_up_silu(A, As, offsets, M, k, E, N, K, gw.w1, gw.w1s,
                                         cfg.dtype, H, Hs, err)
     else:
-        H = torch.empty((P, N), dtype=torch.bfloat16, device=dev)
+        H = alloc((P, N), torch.bfloat16)
         Hs = None
         g.moe_grouped_gemm_gate_up_silu(A, None, offsets, M, k, E, N, K, gw.w1, None,
                                         cfg.dtype, H, None, err)
     del A, As
-    y = torch.empty((M, k, K), dtype=torch.bfloat16, device=dev)
+    y = alloc((M, k, K), torch.bfloat16)
     g.moe_grouped_gemm_down(H, Hs, srt, offsets, wts, M, k, E, N, K, gw.w2, gw.w2s,
                             cfg.dtype, y, err)
-    out = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    out = alloc((M, K), torch.bfloat16)
     g.moe_unpermute_weighted_reduce(y, inv, M, k, K, out)
     res = {"counts": counts, "offsets": offsets, "sorted": srt, "inv": inv,
            "y_slot": y, "out": out, "err": err, "amax": amax}

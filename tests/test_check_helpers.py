@@ -1,11 +1,14 @@
-"""The near-tie validity check the GPU routing tests rely on, pinned on the
-CPU: the oracle's own choice passes, a wrong expert or a wrong group fails,
-and when two group keys tie within the tolerance both group choices pass
-(and only those)."""
+"""Checks the GPU tests rely on, pinned on the CPU.  The near-tie validity
+check: the oracle's own choice passes, a wrong expert or a wrong group fails,
+and when two group keys tie within the tolerance both group choices pass (and
+only those).  The guard-band allocator: writes inside its buffers pass, one
+byte written just before or just past a buffer fails."""
 import numpy as np
+import pytest
+import torch
 
 import oracle as orc
-from gpu_common import _grouped_choice_is_valid
+from gpu_common import GUARD, Guarded, _grouped_choice_is_valid
 
 
 def _route_one(v, topk, n_groups, topk_groups):
@@ -52,3 +55,20 @@ def test_tied_group_keys_accept_either_group(orc):
     v2 = v.copy()
     v2[13] = 0.9
     assert not _grouped_choice_is_valid(v2, np.array([14, 13]), 2, 4, 1, 1e-6)
+
+
+def test_guard_bands_catch_a_write_just_outside_a_buffer():
+    guard = Guarded(device="cpu")
+    a = guard((3, 5), torch.float32)
+    b = guard((7,), torch.bfloat16)
+    a.fill_(1.0)
+    b.fill_(2.0)
+    guard.check("in bounds")
+    for buf, off in ((0, -1), (0, 60), (1, 14)):  # before a, just past a, just past b
+        raw = guard.bufs[buf][0]
+        old = int(raw[GUARD + off])
+        raw[GUARD + off] = 0
+        with pytest.raises(AssertionError):
+            guard.check("planted")
+        raw[GUARD + off] = old
+    guard.check("restored")
