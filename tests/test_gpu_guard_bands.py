@@ -103,6 +103,10 @@ def test_one_call_layers_write_only_their_buffers(cfg):
 @pytest.mark.parametrize("cfg", [WL.SMALL_BATCHED, WL.SMALL_BATCHED_SHORT, WL.SMALL_BATCHED_FP8,
                                  WL.SMALL_BATCHED_FP8_K640], ids=lambda c: c.name)
 def test_batched_writes_only_its_buffers(cfg):
+    _batched_guarded(cfg)
+
+
+def _batched_guarded(cfg):
     d = WL.make_inputs(cfg, DEV)
     g = gbmoe()
     E, T, K = cfg.E, cfg.M, cfg.K
@@ -183,3 +187,25 @@ def test_quantisers_write_only_their_buffers():
                                    guard((M * k,), torch.float32),
                                    amax_ws=guard((1,), torch.int32))
     guard.check("quantisers")
+
+
+@pytest.mark.parametrize("cfg", [WL.MIXTRAL_PREFILL, WL.DSV3_DECODE, WL.DSV3_PREFILL_FP8,
+                                 WL.DSV3_PREFILL_FP8CH, WL.DSV3_PREFILL_FP8T],
+                         ids=lambda c: c.name)
+def test_full_size_layers_write_only_their_buffers(cfg):
+    """The one-call layer at the bench's sizes (many tile waves, the CTA-pair
+    and block-scaled kernels' full schedules): outputs and the workspace
+    guarded."""
+    d = WL.make_inputs(cfg, DEV)
+    gw = GpuWeights(cfg, d["w1"], d["w2"])
+    guard = Guarded()
+    _, _, _, err = run_forward(cfg, d, gw, alloc=guard)
+    guard.check(cfg.name)
+    assert err.item() == 0
+
+
+@pytest.mark.parametrize("cfg", [WL.BATCHED_MASKED, WL.BATCHED_MASKED_FP8], ids=lambda c: c.name)
+def test_full_size_batched_writes_only_its_buffers(cfg):
+    """The batched masked layer at the bench's sizes (32 experts x 1024
+    rows, K = 7168), bf16 and e4m3."""
+    _batched_guarded(cfg)
