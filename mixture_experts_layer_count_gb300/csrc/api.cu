@@ -716,8 +716,10 @@ gbmoe_status_t moe_batched_masked_experts(
   a.err = err_word;
   cudaError_t ce;
   if (fp8) {
-    // the caller's (E*T, K/128) row-major scales -> (K/128, ld) group-major
-    ce = launch_scales_group_major(x_b_scales, R, K / 128, w.xs, scale_ld((size_t)R), sms, s);
+    // the caller's (E*T, K/128) row-major scales -> (K/128, ld) group-major,
+    // for the runs of rows that hold valid tokens (the GEMM stores no other)
+    ce = launch_scales_group_major(x_b_scales, R, K / 128, w.xs, scale_ld((size_t)R), sms, s,
+                                   expert_num_tokens, T);
     if (ce != cudaSuccess) return from_cuda(ce);
     a.A_scales = w.xs;
     a.scale_ld = scale_ld((size_t)R);

@@ -35,8 +35,12 @@ cudaError_t launch_gather_rows(const void *x, const float *xs, const float *row_
                                void *out, float *out_s, int64_t out_s_ld,
                                int num_sms, cudaStream_t s);
 // row-major (rows, G) fp32 -> group-major (G, ld), ld >= rows; G <= 128
+// counts (E) and T, when counts is given: the rows are (E, T) and a run of
+// 32 rows that holds no row r with r % T < clamp(counts[r / T], 0, T) is
+// not moved (its scales stay as the output held them)
 cudaError_t launch_scales_group_major(const float *in, int64_t rows, int G, float *out,
-                                      int64_t ld, int num_sms, cudaStream_t s);
+                                      int64_t ld, int num_sms, cudaStream_t s,
+                                      const int32_t *counts = nullptr, int T = 0);
 cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
                           int topk, int K, uint16_t *out, int num_sms,
                           cudaStream_t s);

@@ -292,11 +292,23 @@ __global__ void __launch_bounds__(256)
 // writes (32 consecutive floats of each of the G groups) are coalesced.
 __global__ void __launch_bounds__(256)
     scales_group_major_kernel(const float *__restrict__ in, int64_t rows, int G,
-                              float *__restrict__ out, int64_t ld) {
+                              float *__restrict__ out, int64_t ld,
+                              const int32_t *__restrict__ counts, int T) {
   extern __shared__ float tile[];  // [32][G + 1]
   const int gp = G + 1;
   for (int64_t r0 = (int64_t)blockIdx.x * 32; r0 < rows; r0 += (int64_t)gridDim.x * 32) {
     const int nr = (int)(rows - r0 < 32 ? rows - r0 : 32);
+    if (counts) {  // uniform over the block: r0 and counts are
+      // rows (E, T): row r holds a token of expert r / T when r % T is below
+      // that expert's count; a run of 32 rows with no such row is skipped
+      bool live = false;
+      if ((int)threadIdx.x < nr) {
+        const int64_t r = r0 + threadIdx.x;
+        const int c = __ldg(counts + r / T);
+        live = r % T < (int64_t)(c < 0 ? 0 : (c > T ? T : c));
+      }
+      if (!__syncthreads_or(live)) continue;
+    }
     for (int i = threadIdx.x; i < nr * G; i += blockDim.x)
       tile[(i / G) * gp + i % G] = in[r0 * G + i];
     __syncthreads();
@@ -377,11 +389,13 @@ cudaError_t launch_reduce(const uint16_t *y_slot, const int32_t *inv, int M,
 }
 
 cudaError_t launch_scales_group_major(const float *in, int64_t rows, int G, float *out,
-                                      int64_t ld, int num_sms, cudaStream_t s) {
+                                      int64_t ld, int num_sms, cudaStream_t s,
+                                      const int32_t *counts, int T) {
   int64_t blocks = (rows + 31) / 32;
   if (blocks > 4 * num_sms) blocks = 4 * num_sms;
   if (blocks < 1) blocks = 1;
-  scales_group_major_kernel<<<(int)blocks, 256, (size_t)32 * (G + 1) * 4, s>>>(in, rows, G, out, ld);
+  scales_group_major_kernel<<<(int)blocks, 256, (size_t)32 * (G + 1) * 4, s>>>(
+      in, rows, G, out, ld, counts, counts ? T : 1);
   return cudaGetLastError();
 }
 
